@@ -1,0 +1,309 @@
+/*
+ * gdn_oracle.c -- plain fp64 CPU oracle for the gated delta rule (GDN), its
+ * DeltaProduct generalisation and the camera-branch prep.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; only the test-suite, the smoke check and the bench's CPU
+ * baseline leg do.  It shares no code, header or constant with the CUDA path.
+ *
+ * Everything here is the plain definition written out, token by token, in
+ * double precision, with no blocking, chunking or reordering:
+ *
+ *  - GDN (gated_deltaproduct test.py, the state-scan kernel
+ *    `gated_chunk_delta_rule_fwd_kernel_h` and output kernel
+ *    `gated_chunk_linear_attn_fwd_kernel_o`; fused_cam_gdn.py,
+ *    `_cam_scan_kernel`, "decay, then predict, then correct"):
+ *        S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *        o_t = scale * S_t^T q_t              (inclusive of token t)
+ *    with S of shape Dk x Dv (rows = key dim, columns = value dim).
+ *
+ *  - DeltaProduct: per token the decay is applied once, then r Householder
+ *    sub-steps j = 0..r-1, each with its own k_{t,j}, v_{t,j}, beta_{t,j};
+ *    the output reads the state after the last sub-step.
+ *
+ *  - Camera prep (fused_cam_gdn.py, `_torch_cam_prep_reference` and
+ *    `_cam_prep_kernel`): full-C RMSNorm (C = H*D) with per-channel weight on
+ *    q and k, ReLU on q and k, K-scale on k, a 4x4 projection out = P*in on
+ *    each group of 4 in the first D/2 dims (proj_q for q, proj_kv for k and
+ *    v), interleaved-pair RoPE on the last D/2 dims, and ||k||^2 before and
+ *    after the projection/RoPE.
+ *
+ * exp/sqrt/sin/cos/pow are the host libm double routines.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* x <- x / max(||x||_2, 1e-12); the zero vector stays zero. */
+static void l2_normalise(double *x, int n) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += x[i] * x[i];
+    double nrm = sqrt(s);
+    if (nrm < 1e-12) nrm = 1e-12;
+    for (int i = 0; i < n; ++i) x[i] /= nrm;
+}
+
+/* One delta-rule correction on S (Dk x Dv, row-major):
+ *   p = S^T k ;  S += beta * k (v - p)^T
+ * which equals S <- (I - beta k k^T) S + beta k v^T. */
+static void delta_step(double *S, const double *k, const double *v, double beta,
+                       int Dk, int Dv, double *p) {
+    for (int j = 0; j < Dv; ++j) p[j] = 0.0;
+    for (int i = 0; i < Dk; ++i) {
+        const double ki = k[i];
+        const double *row = S + (size_t)i * Dv;
+        for (int j = 0; j < Dv; ++j) p[j] += row[j] * ki;
+    }
+    for (int i = 0; i < Dk; ++i) {
+        const double c = beta * k[i];
+        double *row = S + (size_t)i * Dv;
+        for (int j = 0; j < Dv; ++j) row[j] += c * (v[j] - p[j]);
+    }
+}
+
+/* o = scale * S^T q */
+static void read_out(const double *S, const double *q, double scale, int Dk, int Dv,
+                     double *o) {
+    for (int j = 0; j < Dv; ++j) o[j] = 0.0;
+    for (int i = 0; i < Dk; ++i) {
+        const double qi = q[i];
+        const double *row = S + (size_t)i * Dv;
+        for (int j = 0; j < Dv; ++j) o[j] += row[j] * qi;
+    }
+    for (int j = 0; j < Dv; ++j) o[j] *= scale;
+}
+
+/*
+ * GDN forward, token by token.
+ *   q, k : [B,H,T,Dk]      v, o : [B,H,T,Dv]      beta, g : [B,H,T]
+ *   s0 / s_final : [B,H,Dk,Dv] or NULL (NULL s0 = zero state).
+ *   l2norm != 0 normalises q_t and k_t to unit length before use.
+ * Returns 0, or -1 if scratch memory could not be allocated.
+ */
+int oracle_gdn_fwd(const double *q, const double *k, const double *v, const double *beta,
+                   const double *g, const double *s0, double *o, double *s_final, int B,
+                   int H, int T, int Dk, int Dv, double scale, int l2norm) {
+    const int BH = B * H;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = (double *)malloc(sizeof(double) * (size_t)Dk * Dv);
+        double *p = (double *)malloc(sizeof(double) * (size_t)Dv);
+        double *kt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        if (!S || !p || !kt || !qt) {
+            failed |= 1;
+        } else {
+            if (s0)
+                memcpy(S, s0 + (size_t)bh * Dk * Dv, sizeof(double) * (size_t)Dk * Dv);
+            else
+                memset(S, 0, sizeof(double) * (size_t)Dk * Dv);
+            for (int t = 0; t < T; ++t) {
+                const size_t tok = (size_t)bh * T + t;
+                memcpy(kt, k + tok * Dk, sizeof(double) * Dk);
+                memcpy(qt, q + tok * Dk, sizeof(double) * Dk);
+                if (l2norm) {
+                    l2_normalise(kt, Dk);
+                    l2_normalise(qt, Dk);
+                }
+                /* decay hits the old state only, before the correction */
+                const double a = exp(g[tok]);
+                for (size_t e = 0; e < (size_t)Dk * Dv; ++e) S[e] *= a;
+                delta_step(S, kt, v + tok * Dv, beta[tok], Dk, Dv, p);
+                read_out(S, qt, scale, Dk, Dv, o + tok * Dv);
+            }
+            if (s_final)
+                memcpy(s_final + (size_t)bh * Dk * Dv, S, sizeof(double) * (size_t)Dk * Dv);
+        }
+        free(S);
+        free(p);
+        free(kt);
+        free(qt);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * DeltaProduct forward: decay once per token, then r sub-steps in index order.
+ *   q : [B,H,T,Dk]   k : [B,H,T,r,Dk]   v : [B,H,T,r,Dv]   beta : [B,H,T,r]
+ *   g : [B,H,T]      o : [B,H,T,Dv]     s0 / s_final : [B,H,Dk,Dv] or NULL.
+ */
+int oracle_deltaproduct_fwd(const double *q, const double *k, const double *v,
+                            const double *beta, const double *g, const double *s0,
+                            double *o, double *s_final, int B, int H, int T, int r, int Dk,
+                            int Dv, double scale, int l2norm) {
+    const int BH = B * H;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = (double *)malloc(sizeof(double) * (size_t)Dk * Dv);
+        double *p = (double *)malloc(sizeof(double) * (size_t)Dv);
+        double *kt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        if (!S || !p || !kt || !qt) {
+            failed |= 1;
+        } else {
+            if (s0)
+                memcpy(S, s0 + (size_t)bh * Dk * Dv, sizeof(double) * (size_t)Dk * Dv);
+            else
+                memset(S, 0, sizeof(double) * (size_t)Dk * Dv);
+            for (int t = 0; t < T; ++t) {
+                const size_t tok = (size_t)bh * T + t;
+                const double a = exp(g[tok]);
+                for (size_t e = 0; e < (size_t)Dk * Dv; ++e) S[e] *= a;
+                for (int j = 0; j < r; ++j) {
+                    const size_t sub = tok * r + j;
+                    memcpy(kt, k + sub * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(kt, Dk);
+                    delta_step(S, kt, v + sub * Dv, beta[sub], Dk, Dv, p);
+                }
+                memcpy(qt, q + tok * Dk, sizeof(double) * Dk);
+                if (l2norm) l2_normalise(qt, Dk);
+                read_out(S, qt, scale, Dk, Dv, o + tok * Dv);
+            }
+            if (s_final)
+                memcpy(s_final + (size_t)bh * Dk * Dv, S, sizeof(double) * (size_t)Dk * Dv);
+        }
+        free(S);
+        free(p);
+        free(kt);
+        free(qt);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Camera-branch prep (fused_cam_gdn.py, `_torch_cam_prep_reference`).
+ *   q_raw, k_raw, v_raw : [B,N,H,D]
+ *   q_norm_w, k_norm_w  : [H*D] or NULL (NULL = all ones)
+ *   proj_q, proj_kv     : [B,N,4,4] row-major, applied as out_i = sum_j P[i][j] in_j
+ *   rope_cos, rope_sin  : [N, D/2] in the page's interleaved encoding
+ *                         y[d] = x[d] cos[d] + x[d^1] sin[d], or both NULL, in
+ *                         which case cos[2i]=cos[2i+1]=cos(th), sin[2i]=-sin(th),
+ *                         sin[2i+1]=+sin(th), th = n * rope_base^(-2i/(D/2)).
+ *   q_out, k_out, v_out : [B,H,N,D]
+ *   k_pre_sq, k_post_sq : [B,H,N] or NULL
+ */
+int oracle_cam_prep_fwd(const double *q_raw, const double *k_raw, const double *v_raw,
+                        const double *q_norm_w, const double *k_norm_w, const double *proj_q,
+                        const double *proj_kv, const double *rope_cos, const double *rope_sin,
+                        double rope_base, double *q_out, double *k_out, double *v_out,
+                        double *k_pre_sq, double *k_post_sq, int B, int N, int H, int D,
+                        double k_scale, double eps) {
+    if (D % 2 != 0 || (D / 2) % 4 != 0) return -2;
+    const int C = H * D;
+    const int Dh = D / 2;
+    const long BN = (long)B * N;
+    int failed = 0;
+#pragma omp parallel for schedule(static) reduction(| : failed)
+    for (long bn = 0; bn < BN; ++bn) {
+        const int b = (int)(bn / N);
+        const int n = (int)(bn % N);
+        double *xq = (double *)malloc(sizeof(double) * D);
+        double *xk = (double *)malloc(sizeof(double) * D);
+        double *xv = (double *)malloc(sizeof(double) * D);
+        double *cs = (double *)malloc(sizeof(double) * Dh);
+        double *sn = (double *)malloc(sizeof(double) * Dh);
+        if (!xq || !xk || !xv || !cs || !sn) {
+            failed |= 1;
+        } else {
+            const double *qr = q_raw + (size_t)bn * C;
+            const double *kr = k_raw + (size_t)bn * C;
+            const double *vr = v_raw + (size_t)bn * C;
+            /* full-C RMSNorm statistics, shared by all heads of the token */
+            double ssq = 0.0, ssk = 0.0;
+            for (int c = 0; c < C; ++c) {
+                ssq += qr[c] * qr[c];
+                ssk += kr[c] * kr[c];
+            }
+            const double iq = 1.0 / sqrt(ssq / C + eps);
+            const double ik = 1.0 / sqrt(ssk / C + eps);
+            /* rotary tables for this position */
+            for (int d = 0; d < Dh; ++d) {
+                if (rope_cos && rope_sin) {
+                    cs[d] = rope_cos[(size_t)n * Dh + d];
+                    sn[d] = rope_sin[(size_t)n * Dh + d];
+                } else {
+                    const int i = d / 2;
+                    const double th = (double)n * pow(rope_base, -2.0 * i / (double)Dh);
+                    cs[d] = cos(th);
+                    sn[d] = (d % 2 == 0) ? -sin(th) : sin(th);
+                }
+            }
+            const double *Pq = proj_q + (size_t)bn * 16;
+            const double *Pk = proj_kv + (size_t)bn * 16;
+            for (int h = 0; h < H; ++h) {
+                double pre = 0.0, post = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    const int c = h * D + d;
+                    const double wq = q_norm_w ? q_norm_w[c] : 1.0;
+                    const double wk = k_norm_w ? k_norm_w[c] : 1.0;
+                    double a = qr[c] * iq * wq;
+                    double bk = kr[c] * ik * wk;
+                    a = a > 0.0 ? a : 0.0;
+                    bk = (bk > 0.0 ? bk : 0.0) * k_scale;
+                    xq[d] = a;
+                    xk[d] = bk;
+                    xv[d] = vr[c];
+                    pre += bk * bk;
+                }
+                const size_t ob = (((size_t)b * H + h) * N + n) * D;
+                /* first half: out = P * in on each group of four */
+                for (int g0 = 0; g0 < Dh; g0 += 4) {
+                    for (int i = 0; i < 4; ++i) {
+                        double sq = 0.0, sk = 0.0, sv = 0.0;
+                        for (int j = 0; j < 4; ++j) {
+                            sq += Pq[i * 4 + j] * xq[g0 + j];
+                            sk += Pk[i * 4 + j] * xk[g0 + j];
+                            sv += Pk[i * 4 + j] * xv[g0 + j];
+                        }
+                        q_out[ob + g0 + i] = sq;
+                        k_out[ob + g0 + i] = sk;
+                        v_out[ob + g0 + i] = sv;
+                        post += sk * sk;
+                    }
+                }
+                /* second half: interleaved-pair rotation */
+                for (int d = 0; d < Dh; ++d) {
+                    const int e = Dh + d;
+                    const int pe = Dh + (d ^ 1);
+                    const double yq = xq[e] * cs[d] + xq[pe] * sn[d];
+                    const double yk = xk[e] * cs[d] + xk[pe] * sn[d];
+                    const double yv = xv[e] * cs[d] + xv[pe] * sn[d];
+                    q_out[ob + e] = yq;
+                    k_out[ob + e] = yk;
+                    v_out[ob + e] = yv;
+                    post += yk * yk;
+                }
+                const size_t si = ((size_t)b * H + h) * N + n;
+                if (k_pre_sq) k_pre_sq[si] = pre;
+                if (k_post_sq) k_post_sq[si] = post;
+            }
+        }
+        free(xq);
+        free(xk);
+        free(xv);
+        free(cs);
+        free(sn);
+    }
+    return failed ? -1 : 0;
+}
