@@ -1,0 +1,403 @@
+"""Throughput of the chunkwise GDN forward on one GB300 (or N, one process each).
+
+A step is one gdn_chunk_fwd call over the B=4, H=16, T=4096, Dk=Dv=128 bf16
+workload (chunk 64, fp32 state): decay cumsum, decay-masked KK^T, triangular
+inverse, w/u, the state scan and the output, all inside the library's kernels.
+Inputs stay resident in HBM; each step reads 192 MiB and writes 64 MiB, more
+than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on
+a bounded sample of the same workload (the method has no runnable reference
+implementation) and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gdn_b4h16t4096d128_bf16"
+METRIC = "GDN fwd tokens/s (B4,H16,T4096,D128 bf16) + % of binding roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+SCAN_SOURCES = ("scan_simt.cu", "scan_tc.cu")
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0}, "fallback"
+
+
+def gdn_bytes_per_token_head(D, s_in=2, s_out=2):
+    """Algorithmic HBM bytes per (token, head): q, k, v in, beta (dtype) and g
+    (fp32) in, o out; the fp32 state never leaves the chip."""
+    return 3 * D * s_in + s_in + 4 + D * s_out
+
+
+def gdn_flops_per_token_head(D, C):
+    """w.S, k^T v_new and q.S (2 D^2 each) + triangular-half KK^T, T.(beta k),
+    T.(beta v), q k^T and P.v_new (C.D each) + the C^3/3 inverse amortised."""
+    return 6 * D * D + 5 * C * D + C * C // 3
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for name in SCAN_SOURCES:
+        p = os.path.join(ROOT, "gated_delta_rule_47_gb300", "csrc", name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the scan kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "scan_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha") != source_sha():
+        return None, d.get("kernel")
+    return d.get("dram_bytes_per_launch"), d.get("kernel")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not found"}
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"unavailable": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(inp, n_heads, B, H, T):
+    """Time the fp64 oracle, as it stands, on n_heads whole heads of the
+    workload; returns (tokens/s scaled to the full workload, seconds, threads)."""
+    import oracle
+    from gated_delta_rule_47_gb300.inputs import to_f64
+    idx = list(range(n_heads))
+
+    def sub(x):
+        return to_f64(x).reshape(B * H, *x.shape[2:])[idx][None]
+
+    args = [sub(inp[k]) for k in ("q", "k", "v", "beta", "g")]
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.gdn_fwd(*args, return_final_state=False)
+    dt = time.perf_counter() - t0
+    tokens = B * T * n_heads / (B * H)
+    return tokens / dt, dt, threads
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 CPU oracle on a bounded sample of the workload."""
+    if rank != 0:
+        return 0
+    from gated_delta_rule_47_gb300.inputs import WORKLOADS
+    w = WORKLOADS[WORKLOAD]
+    inp = w.make()
+    n_heads = args.ref_heads
+    vals, secs = [], []
+    threads = None
+    for i in range(args.warmup + args.steps):
+        v, dt, threads = cpu_oracle_sample(inp, n_heads, w.B, w.H, w.T)
+        if i >= args.warmup:
+            vals.append(v)
+            secs.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; q,k unit-norm, v~N(0,1), beta=sigmoid(N), g=logsigmoid(N)/16)",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "chunk": w.chunk,
+                   "sample_heads": n_heads},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n_heads} of {w.B * w.H} heads, full T={w.T}, per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from gated_delta_rule_47_gb300 import binding, build
+    from gated_delta_rule_47_gb300.inputs import WORKLOADS
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    lib = binding.load()
+    w = WORKLOADS[WORKLOAD]
+    inp_cpu = w.make()
+    d = {k: v.to(dev) for k, v in inp_cpu.items()}
+    o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    n0 = binding.launch_count()
+    ev_s = torch.cuda.Event(enable_timing=True)
+    ev_e = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        ev_s.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev_e.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = binding.launch_count() - n0
+    ms = ev_s.elapsed_time(ev_e) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = w.B * w.T * world
+    value = tokens_per_step / (ms * 1e-3)
+
+    # end to end through the same C-ABI call: pinned host inputs copied in and
+    # the output copied back inside the timed region
+    host = {k: v.pin_memory() for k, v in inp_cpu.items()}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def e2e_step():
+        for k in host:
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    e_s.record(stream)
+    e2e_steps = max(1, min(args.steps, 20))
+    for _ in range(e2e_steps):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens_per_step / (e2e_ms * 1e-3)
+
+    if rank != 0:
+        return 0
+    peaks, peak_kind = measured_peaks()
+    th = w.B * w.H * w.T
+    alg_bytes = th * gdn_bytes_per_token_head(w.D)
+    alg_flops = th * gdn_flops_per_token_head(w.D, w.chunk)
+    launches_per_step = launches / args.steps
+    kernel_ms = ms / max(launches_per_step, 1.0)
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+    traffic, traffic_kernel = ncu_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k unit-norm, v~N(0,1), beta=sigmoid(N), g=logsigmoid(N)/16)",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "T": w.T, "Dk": w.D, "Dv": w.D,
+                   "chunk": w.chunk, "state": "fp32", "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "no flush: each step touches 270 MB > 129 MB L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": alg_flops,
+                     "kernel": traffic_kernel or "scan", "kernel_ms": kernel_ms},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if args.secondary:
+        line["secondary"] = secondary(args, dev)
+    if not args.no_cpu_baseline and world == 1:
+        v, dt, threads = cpu_oracle_sample(inp_cpu, args.ref_heads, w.B, w.H, w.T)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{args.ref_heads} of {w.B * w.H} heads, full T={w.T} "
+                                          f"({dt:.1f} s), scaled to the whole workload"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def secondary(args, dev):
+    """Device time of the other workloads (not the headline): long-sequence
+    GDN, DeltaProduct r=2, and the camera prep + scan."""
+    import torch
+    from gated_delta_rule_47_gb300 import binding
+    from gated_delta_rule_47_gb300.inputs import WORKLOADS
+    peaks, _ = measured_peaks()
+    out = {}
+    steps = max(3, min(args.steps, 10))
+
+    def timeit(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    for name in ("gdn_long_b1h32t32768d128_bf16", "deltaproduct_r2_b4h16t4096d128_bf16"):
+        w = WORKLOADS[name]
+        d = {k: v.to(dev) for k, v in w.make().items()}
+        o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+        if w.kind == "gdn":
+            fn = lambda: binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o)
+            nbytes = w.B * w.H * w.T * gdn_bytes_per_token_head(w.D)
+        else:
+            fn = lambda: binding.deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"],
+                                                        chunk=w.chunk, o=o)
+            nbytes = w.B * w.H * w.T * (w.D * (1 + 2 * w.r) * 2 + 2 * w.r + 4 + 2 * w.D)
+        ms = timeit(fn)
+        out[name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                     "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        del d, o
+        torch.cuda.empty_cache()
+    w = WORKLOADS["cam_b2n32760h16d128_bf16"]
+    d = {k: (v.to(dev) if v is not None else None) for k, v in w.make().items()}
+    outs = tuple(torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+
+    def prep():
+        return binding.cam_prep_fwd(d["q_raw"], d["k_raw"], d["v_raw"], d["proj_q"], d["proj_kv"],
+                                    d["q_norm_w"], d["k_norm_w"], d["rope_cos"], d["rope_sin"], outs=outs)
+
+    pre_ms = timeit(prep)
+    C = w.H * w.D
+    prep_bytes = w.B * w.T * (6 * C * 2 + 2 * 16 * 4 + 2 * w.H * 4)
+    scan_ms = timeit(lambda: binding.gdn_chunk_fwd(outs[0], outs[1], outs[2], d["beta"], d["g"],
+                                                   chunk=w.chunk, l2norm=True, o=o))
+    out[w.name] = {"prep_ms": pre_ms, "prep_gbs": prep_bytes / (pre_ms * 1e-3) / 1e9,
+                   "prep_hbm_frac": prep_bytes / (pre_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                   "scan_ms": scan_ms, "tokens_per_s": w.B * w.T / ((pre_ms + scan_ms) * 1e-3)}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--ref-heads", type=int, default=64,
+                    help="heads of the workload the CPU oracle runs per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True)
+    args = ap.parse_args()
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local_rank = env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

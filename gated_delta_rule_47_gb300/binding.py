@@ -1,0 +1,212 @@
+"""Thin ctypes binding of libgdn.so (argument marshalling only).
+
+Every function here checks that its tensors are CUDA, contiguous and of the
+expected dtype and shape, allocates the outputs with torch, and calls the C
+entry point of the same name with raw device pointers and the current CUDA
+stream.  All computation happens in the library's kernels; there is no
+fallback: if ``libgdn.so`` is missing or fails to load, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
+
+GDN_F32, GDN_BF16 = 0, 1
+GDN_QK_L2NORM = 1
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
+          4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
+
+EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
+           "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libgdn.so (built by ``gated_delta_rule_47_gb300.build``) and declare
+    the signatures of its entry points."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libgdn.so not found at {p}; build it with "
+                               "`python -m gated_delta_rule_47_gb300.build`")
+        lib = ctypes.CDLL(p)
+        vp, i, u, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float, ctypes.c_size_t
+        lib.gdn_status_string.argtypes = [i]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_version.restype = i
+        lib.gdn_chunk_fwd_workspace_bytes.argtypes = [i] * 8
+        lib.gdn_chunk_fwd_workspace_bytes.restype = sz
+        lib.gdn_chunk_fwd.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp, sz, vp]
+        lib.gdn_chunk_fwd.restype = i
+        lib.deltaproduct_chunk_fwd.argtypes = [vp] * 8 + [i] * 7 + [f, u, i, vp, sz, vp]
+        lib.deltaproduct_chunk_fwd.restype = i
+        lib.cam_prep_fwd.argtypes = [vp] * 9 + [f] + [vp] * 5 + [i] * 4 + [f, f, i, vp]
+        lib.cam_prep_fwd.restype = i
+        lib.gdn_get_device_error.argtypes = [vp]
+        lib.gdn_get_device_error.restype = i
+        lib.gdn_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+        lib.gdn_set_wait_limit.restype = i
+        lib.gdn_launch_count.restype = ctypes.c_ulonglong
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _check(t, name, shape, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _raise(fn, st):
+    if st != 0:
+        raise GdnError(fn, st)
+
+
+def workspace_bytes(B, H, T, Dk, Dv, chunk=64, r=1, dtype=torch.bfloat16):
+    code = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    n = load().gdn_chunk_fwd_workspace_bytes(B, H, T, r, Dk, Dv, chunk, code)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by gdn_chunk_fwd_workspace_bytes")
+    return int(n)
+
+
+def _scan(fn_name, q, k, v, beta, g, r, initial_state, output_final_state, chunk, scale, l2norm,
+          o, workspace, stream):
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    code = _dtype_code(q)
+    sub = () if r is None else (r,)
+    _check(q, "q", (B, H, T, Dk), dt)
+    _check(k, "k", (B, H, T, *sub, Dk), dt)
+    _check(v, "v", (B, H, T, *sub, Dv), dt)
+    _check(beta, "beta", (B, H, T, *sub), dt)
+    _check(g, "g", (B, H, T), torch.float32)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (B, H, Dk, Dv), torch.float32)
+    if o is None:
+        o = torch.empty(B, H, T, Dv, dtype=dt, device=q.device)
+    _check(o, "o", (B, H, T, Dv), dt)
+    sf = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=q.device) if output_final_state else None
+    need = workspace_bytes(B, H, T, Dk, Dv, chunk, 1 if r is None else r, dt)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = load()
+    flags = GDN_QK_L2NORM if l2norm else 0
+    common = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state), _ptr(o), _ptr(sf)]
+    if r is None:
+        st = lib.gdn_chunk_fwd(*common, B, H, T, Dk, Dv, chunk, float(scale), flags, code,
+                               _ptr(workspace), ws_bytes, _stream(stream))
+    else:
+        st = lib.deltaproduct_chunk_fwd(*common, B, H, T, r, Dk, Dv, chunk, float(scale), flags, code,
+                                        _ptr(workspace), ws_bytes, _stream(stream))
+    _raise(fn_name, st)
+    return o, sf
+
+
+def gdn_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_state=False, chunk=64,
+                  scale=1.0, l2norm=False, o=None, workspace=None, stream=None):
+    """Chunkwise GDN forward.  q,k [B,H,T,Dk]; v [B,H,T,Dv]; beta [B,H,T] (all
+    bf16 or all fp32); g [B,H,T] fp32.  Returns (o, final_state or None)."""
+    return _scan("gdn_chunk_fwd", q, k, v, beta, g, None, initial_state, output_final_state, chunk,
+                 scale, l2norm, o, workspace, stream)
+
+
+def deltaproduct_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_state=False, chunk=64,
+                           scale=1.0, l2norm=False, o=None, workspace=None, stream=None):
+    """DeltaProduct forward.  q [B,H,T,Dk]; k [B,H,T,r,Dk]; v [B,H,T,r,Dv];
+    beta [B,H,T,r]; g [B,H,T] fp32.  chunk counts expanded rows."""
+    r = k.shape[3]
+    return _scan("deltaproduct_chunk_fwd", q, k, v, beta, g, r, initial_state, output_final_state,
+                 chunk, scale, l2norm, o, workspace, stream)
+
+
+def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=None, rope_cos=None,
+                 rope_sin=None, rope_base=10000.0, k_scale=0.5, eps=1e-6, with_norms=True, outs=None,
+                 stream=None):
+    """Fused camera prep.  Raw q,k,v [B,N,H,D] -> q,k,v [B,H,N,D] plus
+    ||k||^2 before / after the projection and rotation, [B,H,N] fp32."""
+    B, N, H, D = q_raw.shape
+    dt = q_raw.dtype
+    code = _dtype_code(q_raw)
+    for name, t in (("q_raw", q_raw), ("k_raw", k_raw), ("v_raw", v_raw)):
+        _check(t, name, (B, N, H, D), dt)
+    _check(proj_q, "proj_q", (B, N, 4, 4), torch.float32)
+    _check(proj_kv, "proj_kv", (B, N, 4, 4), torch.float32)
+    for name, t in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if t is not None:
+            _check(t, name, (H * D,), torch.float32)
+    for name, t in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
+        if t is not None:
+            _check(t, name, (N, D // 2), torch.float32)
+    dev = q_raw.device
+    if outs is None:
+        outs = tuple(torch.empty(B, H, N, D, dtype=dt, device=dev) for _ in range(3))
+    pre = torch.empty(B, H, N, dtype=torch.float32, device=dev) if with_norms else None
+    post = torch.empty(B, H, N, dtype=torch.float32, device=dev) if with_norms else None
+    st = load().cam_prep_fwd(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(q_norm_w), _ptr(k_norm_w),
+                             _ptr(proj_q), _ptr(proj_kv), _ptr(rope_cos), _ptr(rope_sin),
+                             float(rope_base), _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(pre),
+                             _ptr(post), B, N, H, D, float(k_scale), float(eps), code, _stream(stream))
+    _raise("cam_prep_fwd", st)
+    return outs[0], outs[1], outs[2], pre, post
+
+
+def device_error(stream=None) -> int:
+    """Synchronise ``stream`` and read/clear the library's device error word."""
+    return int(load().gdn_get_device_error(_stream(stream)))
+
+
+def set_wait_limit(polls: int) -> None:
+    _raise("gdn_set_wait_limit", load().gdn_set_wait_limit(int(polls)))
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().gdn_launch_count())
+
+
+def status_string(code: int) -> str:
+    return load().gdn_status_string(int(code)).decode()

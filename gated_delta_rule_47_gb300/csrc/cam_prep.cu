@@ -1,0 +1,271 @@
+// cam_prep.cu -- fused camera-branch prep (fused_cam_gdn.py, `_cam_prep_kernel`
+// and `_torch_cam_prep_reference`), one pass over q, k and v.
+//
+// The pages run a separate full-C RMS reduction first and then one 1-warp
+// program per (b, n, h).  Here one warp owns one token: it loads the token's
+// whole q, k, v rows (C = H*D elements each) into registers with 16-byte
+// loads, reduces the two sums of squares with shuffles, and writes the three
+// outputs in the head-major [B,H,N,D] layout the scan reads.  A CTA holds 8
+// consecutive tokens so that the per-(b,h,n) norm statistics leave as 32-byte
+// runs and the rotary tables of the 8 positions are staged once in shared
+// memory.  The path is HBM-bound: 3 reads + 3 writes of C elements per token.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kTokPerCta = 8;  // one warp per token
+constexpr int kMaxDh = 128;    // D/2 <= 128
+
+struct CamParams {
+    const void *q_raw, *k_raw, *v_raw;
+    const float *q_norm_w, *k_norm_w, *proj_q, *proj_kv, *rope_cos, *rope_sin;
+    float log2_base;
+    void *q_out, *k_out, *v_out;
+    float *k_pre_sq, *k_post_sq;
+    int B, N, H, D;
+    float k_scale, eps;
+};
+
+// Eight consecutive elements as fp32.
+struct F8 {
+    float x[8];
+};
+
+__device__ __forceinline__ F8 load8(const __nv_bfloat16 *p) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    F8 r;
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.x[2 * i] = __uint_as_float(w[i] << 16);
+        r.x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    return r;
+}
+
+__device__ __forceinline__ F8 load8(const float *p) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    F8 r = {{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}};
+    return r;
+}
+
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const F8 &v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v.x[2 * i], v.x[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void store8(float *p, const F8 &v) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v.x[0], v.x[1], v.x[2], v.x[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v.x[4], v.x[5], v.x[6], v.x[7]);
+}
+
+// NPL = 8-element groups per lane (C = H*D <= 256*NPL).
+template <typename T, int NPL>
+__global__ void __launch_bounds__(32 * kTokPerCta) cam_prep_kernel(CamParams p) {
+    __shared__ float s_cos[kTokPerCta][kMaxDh];
+    __shared__ float s_sin[kTokPerCta][kMaxDh];
+    __shared__ float s_pre[kTokPerCta][64];
+    __shared__ float s_post[kTokPerCta][64];
+
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int H = p.H, D = p.D, N = p.N;
+    const int C = H * D, Dh = D / 2, G8 = C / 8;
+    const long tok_base = (long)blockIdx.x * kTokPerCta;
+    const long BN = (long)p.B * N;
+
+    // Rotary tables of the CTA's positions.
+    for (int i = threadIdx.x; i < kTokPerCta * Dh; i += blockDim.x) {
+        const int tt = i / Dh, d = i % Dh;
+        const long tok = tok_base + tt;
+        if (tok >= BN) continue;
+        const int n = (int)(tok % N);
+        float c, s;
+        if (p.rope_cos) {
+            c = p.rope_cos[(size_t)n * Dh + d];
+            s = p.rope_sin[(size_t)n * Dh + d];
+        } else {
+            // th = n * base^(-2i/Dh), i = d/2; the product and its reduction
+            // modulo 2*pi are done in double so large positions keep precision.
+            const int i2 = d >> 1;
+            const double inv_freq = exp2((double)p.log2_base * (-2.0 * i2 / (double)Dh));
+            double th = (double)n * inv_freq;
+            const double two_pi = 6.283185307179586476925286766559;
+            th -= two_pi * rint(th / two_pi);
+            float sv, cv;
+            sincosf((float)th, &sv, &cv);
+            c = cv;
+            s = (d & 1) ? sv : -sv;
+        }
+        s_cos[tt][d] = c;
+        s_sin[tt][d] = s;
+    }
+    __syncthreads();
+
+    const long tok = tok_base + w;
+    const bool active = tok < BN;
+    if (active) {
+        const int b = (int)(tok / N), n = (int)(tok % N);
+        const T *qr = static_cast<const T *>(p.q_raw) + (size_t)tok * C;
+        const T *kr = static_cast<const T *>(p.k_raw) + (size_t)tok * C;
+        const T *vr = static_cast<const T *>(p.v_raw) + (size_t)tok * C;
+        F8 xq[NPL], xk[NPL], xv[NPL];
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            const int gi = lane + 32 * i;
+            if (gi < G8) {
+                xq[i] = load8(qr + gi * 8);
+                xk[i] = load8(kr + gi * 8);
+                xv[i] = load8(vr + gi * 8);
+            }
+        }
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            if (lane + 32 * i < G8) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sq += xq[i].x[e] * xq[i].x[e];
+                    sk += xk[i].x[e] * xk[i].x[e];
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        }
+        const float iq = rsqrtf(sq / (float)C + p.eps);
+        const float ik = rsqrtf(sk / (float)C + p.eps);
+
+        float Pq[16], Pk[16];
+        const float4 *pq4 = reinterpret_cast<const float4 *>(p.proj_q + (size_t)tok * 16);
+        const float4 *pk4 = reinterpret_cast<const float4 *>(p.proj_kv + (size_t)tok * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 a = __ldg(pq4 + i), c = __ldg(pk4 + i);
+            Pq[4 * i] = a.x; Pq[4 * i + 1] = a.y; Pq[4 * i + 2] = a.z; Pq[4 * i + 3] = a.w;
+            Pk[4 * i] = c.x; Pk[4 * i + 1] = c.y; Pk[4 * i + 2] = c.z; Pk[4 * i + 3] = c.w;
+        }
+
+        const int lanes_per_head = D / 8;  // divides 32
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            const int gi = lane + 32 * i;
+            const bool ok = gi < G8;
+            const int e0 = gi * 8;
+            const int h = e0 / D, d0 = e0 % D;
+            F8 q = xq[i], k = xk[i], v = xv[i];
+            float pre = 0.f, post = 0.f;
+            if (ok) {
+                F8 wq, wk;
+                if (p.q_norm_w) wq = load8(p.q_norm_w + e0);
+                else for (int e = 0; e < 8; ++e) wq.x[e] = 1.f;
+                if (p.k_norm_w) wk = load8(p.k_norm_w + e0);
+                else for (int e = 0; e < 8; ++e) wk.x[e] = 1.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    q.x[e] = fmaxf(q.x[e] * iq * wq.x[e], 0.f);
+                    k.x[e] = fmaxf(k.x[e] * ik * wk.x[e], 0.f) * p.k_scale;
+                    pre += k.x[e] * k.x[e];
+                }
+                F8 oq, ok8, ov;
+                if (d0 < Dh) {
+#pragma unroll
+                    for (int gsub = 0; gsub < 2; ++gsub) {
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) {
+                            float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                s0 += Pq[a * 4 + c] * q.x[4 * gsub + c];
+                                s1 += Pk[a * 4 + c] * k.x[4 * gsub + c];
+                                s2 += Pk[a * 4 + c] * v.x[4 * gsub + c];
+                            }
+                            oq.x[4 * gsub + a] = s0;
+                            ok8.x[4 * gsub + a] = s1;
+                            ov.x[4 * gsub + a] = s2;
+                        }
+                    }
+                } else {
+                    const int dr = d0 - Dh;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float c = s_cos[w][dr + e], s = s_sin[w][dr + e];
+                        oq.x[e] = q.x[e] * c + q.x[e ^ 1] * s;
+                        ok8.x[e] = k.x[e] * c + k.x[e ^ 1] * s;
+                        ov.x[e] = v.x[e] * c + v.x[e ^ 1] * s;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) post += ok8.x[e] * ok8.x[e];
+                const size_t ob = (((size_t)b * H + h) * N + n) * D + d0;
+                store8(static_cast<T *>(p.q_out) + ob, oq);
+                store8(static_cast<T *>(p.k_out) + ob, ok8);
+                store8(static_cast<T *>(p.v_out) + ob, ov);
+            }
+            // per-head sums over the lanes_per_head lanes that hold head h
+            for (int off = lanes_per_head >> 1; off; off >>= 1) {
+                pre += __shfl_xor_sync(0xffffffffu, pre, off);
+                post += __shfl_xor_sync(0xffffffffu, post, off);
+            }
+            if (ok && (lane % lanes_per_head) == 0 && h < 64) {
+                s_pre[w][h] = pre;
+                s_post[w][h] = post;
+            }
+        }
+    }
+    __syncthreads();
+    // Norm statistics: for each head, the CTA's consecutive tokens are
+    // consecutive in [B,H,N]; write them run by run.
+    if (p.k_pre_sq || p.k_post_sq) {
+        for (int i = threadIdx.x; i < H * kTokPerCta; i += blockDim.x) {
+            const int h = i / kTokPerCta, tt = i % kTokPerCta;
+            const long t2 = tok_base + tt;
+            if (t2 >= BN || h >= 64) continue;
+            const int b = (int)(t2 / N), n = (int)(t2 % N);
+            const size_t si = ((size_t)b * H + h) * N + n;
+            if (p.k_pre_sq) p.k_pre_sq[si] = s_pre[tt][h];
+            if (p.k_post_sq) p.k_post_sq[si] = s_post[tt][h];
+        }
+    }
+}
+
+template <typename T>
+int launch_t(const CamArgs &a, cudaStream_t stream) {
+    CamParams p{a.q_raw, a.k_raw, a.v_raw, a.q_norm_w, a.k_norm_w, a.proj_q, a.proj_kv,
+                a.rope_cos, a.rope_sin, log2f(a.rope_base), a.q_out, a.k_out, a.v_out,
+                a.k_pre_sq, a.k_post_sq, a.B, a.N, a.H, a.D, a.k_scale, a.eps};
+    const long BN = (long)a.B * a.N;
+    const unsigned grid = (unsigned)((BN + kTokPerCta - 1) / kTokPerCta);
+    const int C = a.H * a.D;
+    const int npl = (C / 8 + 31) / 32;
+    if (npl <= 1) cam_prep_kernel<T, 1><<<grid, 32 * kTokPerCta, 0, stream>>>(p);
+    else if (npl <= 2) cam_prep_kernel<T, 2><<<grid, 32 * kTokPerCta, 0, stream>>>(p);
+    else if (npl <= 4) cam_prep_kernel<T, 4><<<grid, 32 * kTokPerCta, 0, stream>>>(p);
+    else if (npl <= 8) cam_prep_kernel<T, 8><<<grid, 32 * kTokPerCta, 0, stream>>>(p);
+    else if (npl <= 16) cam_prep_kernel<T, 16><<<grid, 32 * kTokPerCta, 0, stream>>>(p);
+    else return GDN_ERR_UNSUPPORTED;
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_cam_prep(const CamArgs &a, cudaStream_t stream) {
+    if (a.dtype == GDN_BF16) return launch_t<__nv_bfloat16>(a, stream);
+    if (a.dtype == GDN_F32) return launch_t<float>(a, stream);
+    return GDN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gdn

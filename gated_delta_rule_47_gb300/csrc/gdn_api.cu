@@ -1,0 +1,153 @@
+// gdn_api.cu -- the extern "C" boundary of libgdn.so: host-side argument
+// checks, dispatch between the tcgen05 and SIMT scan paths, status strings.
+// No allocation, no synchronisation, no exception crosses this file.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace gdn
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_scan(const gdn::ScanArgs &a) {
+    if (a.B < 0 || a.H < 0 || a.T < 0 || a.r < 1) return GDN_ERR_INVALID_ARG;
+    if (a.dtype != GDN_F32 && a.dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (a.flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (a.chunk <= 0) return GDN_ERR_INVALID_ARG;
+    if (a.chunk != 16 && a.chunk != 32 && a.chunk != 64) return GDN_ERR_UNSUPPORTED;
+    if (a.r > 8) return GDN_ERR_UNSUPPORTED;
+    if ((a.Dk != 64 && a.Dk != 128) || (a.Dv != 64 && a.Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)a.B * a.H > 65535) return GDN_ERR_UNSUPPORTED;  // grid.y limit
+    if ((long long)a.T * a.r > (1LL << 30)) return GDN_ERR_UNSUPPORTED;
+    const bool empty = (long long)a.B * a.H * a.T == 0;
+    if (!empty) {
+        if (!a.q || !a.k || !a.v || !a.beta || !a.g || !a.o) return GDN_ERR_INVALID_ARG;
+        const void *ps[] = {a.q, a.k, a.v, a.beta, a.g, a.o};
+        for (const void *p : ps)
+            if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    }
+    if ((a.s0 && !aligned16(a.s0)) || (a.sf && !aligned16(a.sf))) return GDN_ERR_MISALIGNED;
+    return GDN_OK;
+}
+
+size_t scan_workspace(const gdn::ScanArgs &a) {
+    return gdn::scan_tc_supported(a) ? gdn::scan_tc_workspace_bytes(a) : 0;
+}
+
+int run_scan(gdn::ScanArgs &a, void *stream_v) {
+    int st = check_scan(a);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const size_t need = scan_workspace(a);
+    if (need > 0 && (a.ws == nullptr || a.ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    if ((long long)a.B * a.H == 0) return GDN_OK;
+    if (a.T == 0) {
+        if (a.sf) {
+            const size_t bytes = sizeof(float) * (size_t)a.B * a.H * a.Dk * a.Dv;
+            cudaError_t e = a.s0 ? cudaMemcpyAsync(a.sf, a.s0, bytes, cudaMemcpyDeviceToDevice, stream)
+                                 : cudaMemsetAsync(a.sf, 0, bytes, stream);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    if (gdn::scan_tc_supported(a)) return gdn::launch_scan_tc(a, stream);
+    return gdn::launch_scan_simt(a, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+        default: return "GDN_ERR_UNKNOWN";
+    }
+}
+
+int gdn_version(void) { return 100; }
+
+size_t gdn_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int chunk,
+                                     int dtype) {
+    gdn::ScanArgs a{};
+    a.B = B; a.H = H; a.T = T; a.r = r; a.Dk = Dk; a.Dv = Dv; a.chunk = chunk;
+    a.dtype = dtype; a.scale = 1.f;
+    // pointer checks do not apply to a size query
+    if (B < 0 || H < 0 || T < 0 || r < 1 || chunk <= 0) return (size_t)-1;
+    if ((chunk != 16 && chunk != 32 && chunk != 64) || r > 8) return (size_t)-1;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return (size_t)-1;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
+    return scan_workspace(a);
+}
+
+int gdn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                  const float *g, const float *initial_state, void *o, float *final_state,
+                  int B, int H, int T, int Dk, int Dv, int chunk, float scale,
+                  unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
+                  void *stream) {
+    gdn::ScanArgs a{q, k, v, beta, g, initial_state, o, final_state, B, H, T, 1, Dk, Dv,
+                    chunk, scale, flags, dtype, workspace, workspace_bytes};
+    return run_scan(a, stream);
+}
+
+int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                           const float *g, const float *initial_state, void *o,
+                           float *final_state, int B, int H, int T, int r, int Dk, int Dv,
+                           int chunk, float scale, unsigned flags, int dtype, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    gdn::ScanArgs a{q, k, v, beta, g, initial_state, o, final_state, B, H, T, r, Dk, Dv,
+                    chunk, scale, flags, dtype, workspace, workspace_bytes};
+    return run_scan(a, stream);
+}
+
+int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *q_norm_w,
+                 const float *k_norm_w, const float *proj_q, const float *proj_kv,
+                 const float *rope_cos, const float *rope_sin, float rope_base, void *q_out,
+                 void *k_out, void *v_out, float *k_pre_sq, float *k_post_sq, int B, int N,
+                 int H, int D, float k_scale, float eps, int dtype, void *stream) {
+    if (B < 0 || N < 0 || H < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (D % 2 != 0 || (D / 2) % 4 != 0) return GDN_ERR_INVALID_ARG;  // page's own rule
+    if (D % 16 != 0 || 32 % (D / 8) != 0 || D > 256) return GDN_ERR_UNSUPPORTED;
+    if ((long long)H * D > 4096 || H > 64) return GDN_ERR_UNSUPPORTED;
+    if (!(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if ((long long)B * N == 0 || H == 0) return GDN_OK;
+    if (!q_raw || !k_raw || !v_raw || !proj_q || !proj_kv || !q_out || !k_out || !v_out)
+        return GDN_ERR_INVALID_ARG;
+    const void *ps[] = {q_raw, k_raw, v_raw, proj_q, proj_kv, q_out, k_out, v_out,
+                        q_norm_w, k_norm_w, rope_cos, rope_sin, k_pre_sq, k_post_sq};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    if (rope_cos == nullptr && !(rope_base > 0.f)) return GDN_ERR_INVALID_ARG;
+    gdn::CamArgs a{q_raw, k_raw, v_raw, q_norm_w, k_norm_w, proj_q, proj_kv, rope_cos, rope_sin,
+                   rope_base, q_out, k_out, v_out, k_pre_sq, k_post_sq, B, N, H, D, k_scale, eps,
+                   dtype};
+    return gdn::launch_cam_prep(a, static_cast<cudaStream_t>(stream));
+}
+
+int gdn_get_device_error(void *stream) {
+    return gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
+}
+
+unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }
+
+int gdn_set_wait_limit(unsigned long long polls) { return gdn::scan_tc_set_wait_limit(polls); }
+
+}  // extern "C"

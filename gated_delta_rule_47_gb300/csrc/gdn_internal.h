@@ -1,0 +1,54 @@
+// Internal host-side declarations shared by the translation units of libgdn.so.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Arguments of one scan call.  r = 1 for GDN; for DeltaProduct the r
+// sub-steps of token t are rows t*r .. t*r+r-1 of one sequence of T*r rows.
+struct ScanArgs {
+    const void *q, *k, *v, *beta;
+    const float *g;
+    const float *s0;
+    void *o;
+    float *sf;
+    int B, H, T, r, Dk, Dv, chunk;
+    float scale;
+    unsigned flags;
+    int dtype;
+    void *ws;
+    size_t ws_bytes;
+};
+
+struct CamArgs {
+    const void *q_raw, *k_raw, *v_raw;
+    const float *q_norm_w, *k_norm_w, *proj_q, *proj_kv, *rope_cos, *rope_sin;
+    float rope_base;
+    void *q_out, *k_out, *v_out;
+    float *k_pre_sq, *k_post_sq;
+    int B, N, H, D;
+    float k_scale, eps;
+    int dtype;
+};
+
+// SIMT chunkwise path (any supported dtype, Dk/Dv in {64,128}, chunk in {16,32,64}).
+int launch_scan_simt(const ScanArgs &a, cudaStream_t stream);
+
+// tcgen05 path (bf16, Dk = Dv = 128, chunk 64).  Returns GDN_ERR_UNSUPPORTED
+// for anything else so that the caller can pick the SIMT path.
+bool scan_tc_supported(const ScanArgs &a);
+size_t scan_tc_workspace_bytes(const ScanArgs &a);
+int launch_scan_tc(const ScanArgs &a, cudaStream_t stream);
+int scan_tc_read_clear_error(cudaStream_t stream);
+int scan_tc_set_wait_limit(unsigned long long polls);
+
+int launch_cam_prep(const CamArgs &a, cudaStream_t stream);
+
+// Counts one kernel launch (thread-safe); read by gdn_launch_count().
+void note_launch();
+
+}  // namespace gdn

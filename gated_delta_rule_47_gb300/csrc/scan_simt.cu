@@ -1,0 +1,272 @@
+// scan_simt.cu -- chunkwise GDN / DeltaProduct forward on the CUDA cores, in
+// fp32 arithmetic.  This is the path for fp32 tensors (tensor-core kinds with
+// fp32 operands would round to tf32) and for shapes the tcgen05 path does not
+// take.  One CTA per (batch*head, 64-wide value tile); the chunks of a head are
+// processed in order with the fp32 state tile resident in shared memory.
+//
+// Per chunk of C rows starting from state S (gated_deltaproduct test.py, the
+// KK^T, triangular solve, w/u recompute, state-scan and output kernels):
+//   gam_t = sum_{i<=t} g_i within the chunk
+//   A[t][s] = beta_t exp(gam_t - gam_s) (k_t . k_s)           for s < t
+//   R[t]    = beta_t (v_t - exp(gam_t) S^T k_t)
+//   Delta   = (I + A)^-1 R          (= u - w S in the WY form)
+//   o_t     = scale (exp(gam_t) S^T q_t + sum_{s<=t} exp(gam_t-gam_s)(q_t.k_s) Delta_s)
+//   S      <- exp(gam_last) S + sum_s exp(gam_last - gam_s) k_s Delta_s^T
+// Rows past the end of the sequence are zero (k, v, beta) with g = 0, so they
+// change nothing.  For DeltaProduct the decay g_t sits on row (t, 0) and the
+// query q_t is read at row (t, r-1); a chunk holds floor(C/r) whole tokens.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBV = 64;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f32(float *p, float x) { *p = x; }
+__device__ __forceinline__ void from_f32(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+struct SimtParams {
+    const void *q, *k, *v, *beta;
+    const float *g, *s0;
+    void *o;
+    float *sf;
+    int T, r, Dv;
+    float scale;
+    unsigned flags;
+};
+
+template <int DK, int C>
+struct SimtSmem {
+    static constexpr int KP = DK + 1, VP = kBV + 1, CP = C + 1;
+    static constexpr int floats = 2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C;
+    static constexpr size_t bytes = sizeof(float) * floats;
+};
+
+// Inclusive prefix sum of x[0..n) (n <= 64) by one warp.
+__device__ __forceinline__ void warp_cumsum64(float *x, int n, int lane) {
+    float a = lane < n ? x[lane] : 0.f;
+    float b = lane + 32 < n ? x[lane + 32] : 0.f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float ya = __shfl_up_sync(0xffffffffu, a, off);
+        float yb = __shfl_up_sync(0xffffffffu, b, off);
+        if (lane >= off) {
+            a += ya;
+            b += yb;
+        }
+    }
+    b += __shfl_sync(0xffffffffu, a, 31);
+    __syncwarp();
+    if (lane < n) x[lane] = a;
+    if (lane + 32 < n) x[lane + 32] = b;
+}
+
+// Scale rows [0, nrows) of a [.][stride] fp32 tile to unit L2 norm over DK.
+template <int DK>
+__device__ void unit_rows(float *X, int stride, int nrows, int warp, int lane, int nwarps) {
+    for (int t = warp; t < nrows; t += nwarps) {
+        float s = 0.f;
+        for (int d = lane; d < DK; d += 32) s += X[t * stride + d] * X[t * stride + d];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        const float inv = 1.f / fmaxf(sqrtf(s), 1e-12f);
+        for (int d = lane; d < DK; d += 32) X[t * stride + d] *= inv;
+    }
+}
+
+template <typename Tin, int DK, int C>
+__global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
+    using L = SimtSmem<DK, C>;
+    constexpr int KP = L::KP, VP = L::VP, CP = L::CP;
+    extern __shared__ float smem[];
+    float *Ks = smem;            // [C][KP]   keys of the chunk
+    float *Qs = Ks + C * KP;     // [C][KP]   queries (C/r rows used)
+    float *Vs = Qs + C * KP;     // [C][VP]   value tile
+    float *Ss = Vs + C * VP;     // [DK][VP]  fp32 state tile
+    float *As = Ss + DK * VP;    // [C][CP]   A (strictly lower)
+    float *Ts = As + C * CP;     // [C][CP]   (I + A)^-1
+    float *Ps = Ts + C * CP;     // [C][CP]   decay-masked q.k, s <= t
+    float *Rs = Ps + C * CP;     // [C][VP]   R
+    float *Ds = Rs + C * VP;     // [C][VP]   Delta
+    float *gam = Ds + C * VP;    // [C]
+    float *bet = gam + C;        // [C]
+    float *eS = bet + C;         // [C] exp(gam_last - gam_s)
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int vt = blockIdx.x;
+    const size_t head = blockIdx.y;
+    const int r = p.r, Dv = p.Dv, T = p.T;
+    const int CQ = C / r;    // whole tokens per chunk
+    const int Ce = CQ * r;   // rows per chunk (<= C; the rest of the tile is padding)
+    const long rows = (long)T * r;
+
+    const Tin *kp = static_cast<const Tin *>(p.k) + head * rows * DK;
+    const Tin *vp = static_cast<const Tin *>(p.v) + head * rows * Dv + vt * kBV;
+    const Tin *qp = static_cast<const Tin *>(p.q) + head * (size_t)T * DK;
+    const Tin *bp = static_cast<const Tin *>(p.beta) + head * rows;
+    const float *gp = p.g + head * (size_t)T;
+    Tin *op = static_cast<Tin *>(p.o) + head * (size_t)T * Dv + vt * kBV;
+
+    for (int i = tid; i < DK * kBV; i += kThreads) {
+        const int d = i / kBV, j = i % kBV;
+        Ss[d * VP + j] = p.s0 ? p.s0[(head * DK + d) * Dv + vt * kBV + j] : 0.f;
+    }
+
+    for (long c0 = 0; c0 < rows; c0 += Ce) {
+        const int Lr = (int)min((long)Ce, rows - c0);  // valid rows (a multiple of r)
+        const int LQ = Lr / r;                         // valid query rows
+        const long tok0 = c0 / r;
+        __syncthreads();
+        for (int i = tid; i < C * DK; i += kThreads) {
+            const int t = i / DK, d = i % DK;
+            Ks[t * KP + d] = t < Lr ? to_f32(kp[(c0 + t) * DK + d]) : 0.f;
+            Qs[t * KP + d] = t < LQ ? to_f32(qp[(tok0 + t) * DK + d]) : 0.f;
+        }
+        for (int i = tid; i < C * kBV; i += kThreads) {
+            const int t = i / kBV, j = i % kBV;
+            Vs[t * VP + j] = t < Lr ? to_f32(vp[(c0 + t) * Dv + j]) : 0.f;
+        }
+        if (tid < C) {
+            const bool ok = tid < Lr;
+            bet[tid] = ok ? to_f32(bp[c0 + tid]) : 0.f;
+            gam[tid] = (ok && (c0 + tid) % r == 0) ? gp[(c0 + tid) / r] : 0.f;
+        }
+        __syncthreads();
+        if (p.flags & GDN_QK_L2NORM) {
+            unit_rows<DK>(Ks, KP, Lr, warp, lane, kThreads / 32);
+            unit_rows<DK>(Qs, KP, LQ, warp, lane, kThreads / 32);
+        }
+        if (warp == 0) warp_cumsum64(gam, C, lane);
+        __syncthreads();
+        const float glast = gam[C - 1];
+        if (tid < C) eS[tid] = expf(glast - gam[tid]);
+
+        // A (strictly lower) and the decay-masked query-key scores.
+        for (int i = tid; i < C * C; i += kThreads) {
+            const int t = i / C, s = i % C;
+            float a = 0.f;
+            if (s < t) {
+                float acc = 0.f;
+#pragma unroll 8
+                for (int d = 0; d < DK; ++d) acc += Ks[t * KP + d] * Ks[s * KP + d];
+                a = bet[t] * expf(gam[t] - gam[s]) * acc;
+            }
+            As[t * CP + s] = a;
+            float pv = 0.f;
+            if (t < CQ) {
+                const int row = t * r + r - 1;
+                if (s <= row) {
+                    float acc = 0.f;
+#pragma unroll 8
+                    for (int d = 0; d < DK; ++d) acc += Qs[t * KP + d] * Ks[s * KP + d];
+                    pv = expf(gam[row] - gam[s]) * acc;
+                }
+            }
+            Ps[t * CP + s] = pv;
+        }
+        // R = diag(beta) (V - diag(exp(gam)) K S)
+        for (int i = tid; i < C * kBV; i += kThreads) {
+            const int t = i / kBV, j = i % kBV;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int d = 0; d < DK; ++d) acc += Ks[t * KP + d] * Ss[d * VP + j];
+            Rs[t * VP + j] = bet[t] * (Vs[t * VP + j] - expf(gam[t]) * acc);
+        }
+        __syncthreads();
+        // (I + A)^-1 by forward substitution, one column per thread.
+        if (tid < C) {
+            const int j = tid;
+            for (int i = 0; i < C; ++i) {
+                float x = (i == j) ? 1.f : 0.f;
+                for (int kk = 0; kk < i; ++kk) x -= As[i * CP + kk] * Ts[kk * CP + j];
+                Ts[i * CP + j] = x;
+            }
+        }
+        __syncthreads();
+        // Delta = (I + A)^-1 R
+        for (int i = tid; i < C * kBV; i += kThreads) {
+            const int t = i / kBV, j = i % kBV;
+            float acc = 0.f;
+            for (int s = 0; s <= t; ++s) acc += Ts[t * CP + s] * Rs[s * VP + j];
+            Ds[t * VP + j] = acc;
+        }
+        __syncthreads();
+        // Outputs of the chunk's tokens (read the state before this chunk's update).
+        for (int i = tid; i < LQ * kBV; i += kThreads) {
+            const int t = i / kBV, j = i % kBV;
+            const int row = t * r + r - 1;
+            float inter = 0.f;
+#pragma unroll 8
+            for (int d = 0; d < DK; ++d) inter += Qs[t * KP + d] * Ss[d * VP + j];
+            float intra = 0.f;
+            for (int s = 0; s <= row; ++s) intra += Ps[t * CP + s] * Ds[s * VP + j];
+            from_f32(op + (tok0 + t) * Dv + j, p.scale * (expf(gam[row]) * inter + intra));
+        }
+        __syncthreads();
+        // State update.
+        const float dl = expf(glast);
+        for (int i = tid; i < DK * kBV; i += kThreads) {
+            const int d = i / kBV, j = i % kBV;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int s = 0; s < C; ++s) acc += Ks[s * KP + d] * eS[s] * Ds[s * VP + j];
+            Ss[d * VP + j] = dl * Ss[d * VP + j] + acc;
+        }
+    }
+    __syncthreads();
+    if (p.sf) {
+        for (int i = tid; i < DK * kBV; i += kThreads) {
+            const int d = i / kBV, j = i % kBV;
+            p.sf[(head * DK + d) * Dv + vt * kBV + j] = Ss[d * VP + j];
+        }
+    }
+}
+
+template <typename Tin, int DK, int C>
+int launch_one(const ScanArgs &a, cudaStream_t stream) {
+    auto kern = scan_simt_kernel<Tin, DK, C>;
+    constexpr size_t smem = SimtSmem<DK, C>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    SimtParams p{a.q, a.k, a.v, a.beta, a.g, a.s0, a.o, a.sf, a.T, a.r, a.Dv, a.scale, a.flags};
+    dim3 grid(a.Dv / kBV, a.B * a.H);
+    kern<<<grid, kThreads, smem, stream>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename Tin, int DK>
+int launch_chunk(const ScanArgs &a, cudaStream_t stream) {
+    switch (a.chunk) {
+        case 16: return launch_one<Tin, DK, 16>(a, stream);
+        case 32: return launch_one<Tin, DK, 32>(a, stream);
+        case 64: return launch_one<Tin, DK, 64>(a, stream);
+        default: return GDN_ERR_UNSUPPORTED;
+    }
+}
+
+template <typename Tin>
+int launch_dk(const ScanArgs &a, cudaStream_t stream) {
+    switch (a.Dk) {
+        case 64: return launch_chunk<Tin, 64>(a, stream);
+        case 128: return launch_chunk<Tin, 128>(a, stream);
+        default: return GDN_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int launch_scan_simt(const ScanArgs &a, cudaStream_t stream) {
+    if (a.Dv % kBV != 0) return GDN_ERR_UNSUPPORTED;
+    if (a.dtype == GDN_F32) return launch_dk<float>(a, stream);
+    if (a.dtype == GDN_BF16) return launch_dk<__nv_bfloat16>(a, stream);
+    return GDN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gdn

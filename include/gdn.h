@@ -1,0 +1,185 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: chunkwise forward of the gated delta rule (GDN),
+ * its DeltaProduct generalisation, and the camera-branch prep, for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * General rules for every entry point below:
+ *  - All tensor arguments are DEVICE pointers to contiguous, row-major
+ *    buffers owned by the caller.  The library never allocates, frees or
+ *    keeps a pointer after the call returns, and never synchronises.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream).
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns an error status and enqueues nothing.
+ *  - Tensor base pointers must be 16-byte aligned (GDN_ERR_MISALIGNED).
+ *  - A launch failure returns GDN_ERR_CUDA.  A device-side bounded wait that
+ *    gives up (it never spins forever) records GDN_ERR_TIMEOUT in a device
+ *    word that gdn_get_device_error() reads back.
+ *  - No C++ exception crosses this interface.
+ *
+ * State convention (fixed by this library): the per-(batch, head) state S is
+ * Dk x Dv, rows indexed by the key dimension, columns by the value dimension,
+ * stored row-major as fp32 [B,H,Dk,Dv], and
+ *
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * (gated_deltaproduct test.py: `gated_chunk_delta_rule_fwd_kernel_h`, the
+ * state is [K, V] and `b_v -= dot(w, h)` predicts with the decayed state;
+ * `gated_chunk_linear_attn_fwd_kernel_o` includes token t's own update via
+ * the `>=` causal mask.  fused_cam_gdn.py, `_cam_scan_kernel`: decay the
+ * state, then predict, then correct.)
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_F32 = 0,  /* fp32 tensors; all arithmetic in fp32                  */
+    GDN_BF16 = 1  /* bf16 tensors; fp32 state and accumulation             */
+} gdn_dtype_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* null required pointer, bad size or shape   */
+    GDN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. Dk=96)     */
+    GDN_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned    */
+    GDN_ERR_WORKSPACE = 4,    /* workspace missing or smaller than queried  */
+    GDN_ERR_CUDA = 5,         /* a CUDA launch or runtime call failed       */
+    GDN_ERR_TIMEOUT = 6       /* a bounded device wait gave up             */
+} gdn_status_t;
+
+/* flags */
+#define GDN_QK_L2NORM 1u /* normalise q_t and k_t to unit L2 norm at load,
+                            q <- q / max(||q||, 1e-12) per (token, head)   */
+
+/* Human-readable name of a status code; never NULL. */
+const char *gdn_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int gdn_version(void);
+
+/*
+ * Bytes of device workspace gdn_chunk_fwd / deltaproduct_chunk_fwd need for
+ * these sizes (r = 1 for GDN).  May be 0.  Returns (size_t)-1 for sizes the
+ * library rejects.
+ */
+size_t gdn_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int chunk,
+                                     int dtype);
+
+/*
+ * gdn_chunk_fwd -- chunkwise GDN forward (gated_deltaproduct test.py: the
+ * decay-masked KK^T kernel `gated_chunk_scaled_dot_kkt_fwd_kernel`, the
+ * 16x16 triangular solve and merge kernels, `gated_fwd_recompute_w_u_kernel`,
+ * the state scan `gated_chunk_delta_rule_fwd_kernel_h` and the output kernel
+ * `gated_chunk_linear_attn_fwd_kernel_o`, run as one pass).
+ *
+ *   q, k    [B,H,T,Dk]  dtype
+ *   v, o    [B,H,T,Dv]  dtype (o is written; it may not alias an input)
+ *   beta    [B,H,T]     dtype
+ *   g       [B,H,T]     fp32, natural-log decay: the state is multiplied by
+ *                       exp(g_t) before token t's correction
+ *   initial_state [B,H,Dk,Dv] fp32 or NULL (NULL = zero state)
+ *   final_state   [B,H,Dk,Dv] fp32 or NULL (written when given)
+ *   chunk   rows per chunk: 16, 32 or 64.  Results do not depend on it beyond
+ *           rounding.  T need not be a multiple of it.
+ *   scale   multiplies every output (1.0 for the plain definition)
+ *   flags   0 or GDN_QK_L2NORM
+ *   dtype   GDN_F32 or GDN_BF16
+ *   Dk, Dv  64 or 128 each
+ *   workspace / workspace_bytes: device scratch of at least
+ *           gdn_chunk_fwd_workspace_bytes(...) bytes (NULL if that is 0)
+ * T = 0 or B*H = 0 is valid and enqueues nothing (final_state, if given,
+ * receives initial_state or zeros).
+ */
+int gdn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                  const float *g, const float *initial_state, void *o, float *final_state,
+                  int B, int H, int T, int Dk, int Dv, int chunk, float scale,
+                  unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
+                  void *stream);
+
+/*
+ * deltaproduct_chunk_fwd -- DeltaProduct forward: per token the decay exp(g_t)
+ * is applied once, then r corrections in order j = 0..r-1,
+ *     S <- (I - beta_{t,j} k_{t,j} k_{t,j}^T) S + beta_{t,j} k_{t,j} v_{t,j}^T,
+ * and o_t = scale * S^T q_t reads the state after the last one.  Each
+ * sub-step has its own key, value and beta (the rows (t,j) form one sequence
+ * of r*T rows; gated_deltaproduct test.py interleaves them the same way, as
+ * BT*r rows per chunk).
+ *
+ *   q, o    [B,H,T,Dk] / [B,H,T,Dv]   dtype
+ *   k       [B,H,T,r,Dk]              dtype
+ *   v       [B,H,T,r,Dv]              dtype
+ *   beta    [B,H,T,r]                 dtype
+ *   g       [B,H,T]                   fp32
+ *   chunk   row capacity of a chunk (16, 32 or 64); each chunk holds
+ *           floor(chunk / r) whole tokens, i.e. r*floor(chunk/r) rows
+ *   r       1..8
+ * Everything else as gdn_chunk_fwd.  r = 1 computes exactly gdn_chunk_fwd.
+ */
+int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                           const float *g, const float *initial_state, void *o,
+                           float *final_state, int B, int H, int T, int r, int Dk, int Dv,
+                           int chunk, float scale, unsigned flags, int dtype, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * cam_prep_fwd -- fused camera-branch prep (fused_cam_gdn.py, `_cam_prep_kernel`
+ * and `_torch_cam_prep_reference`), one pass over q, k, v:
+ *   1. full-C RMSNorm of q and k per token, C = H*D:
+ *        x <- x * rsqrt(sum_{h,d} x^2 / C + eps) * w[h*D+d]
+ *   2. ReLU on q and k; k additionally times k_scale.  v gets neither.
+ *   3. first D/2 dims, each group of 4: out_i = sum_j P[i][j] in_j with
+ *      P = proj_q[b,n] for q and P = proj_kv[b,n] for k and v;
+ *   4. last D/2 dims, interleaved pairs: y[d] = x[d] cos[d] + x[d^1] sin[d]
+ *      with the tables' encoding cos[2i] = cos[2i+1] = cos(th_i),
+ *      sin[2i] = -sin(th_i), sin[2i+1] = +sin(th_i);
+ *   5. optional ||k||^2 per (b,h,n) after step 2 (k_pre_sq) and after 4
+ *      (k_post_sq).
+ *
+ *   q_raw, k_raw, v_raw  [B,N,H,D]  dtype
+ *   q_norm_w, k_norm_w   [H*D] fp32 or NULL (= all ones)
+ *   proj_q, proj_kv      [B,N,4,4] fp32 row-major
+ *   rope_cos, rope_sin   [N,D/2] fp32 in the encoding above, or both NULL:
+ *                        then th_i = n * rope_base^(-2i/(D/2)), n = token index
+ *   q_out, k_out, v_out  [B,H,N,D]  dtype (head-major, ready for the scan)
+ *   k_pre_sq, k_post_sq  [B,H,N] fp32 or NULL
+ *   D a multiple of 16 with D/8 dividing 32 (16, 32, 64, 128 or 256);
+ *   H*D <= 4096.
+ */
+int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *q_norm_w,
+                 const float *k_norm_w, const float *proj_q, const float *proj_kv,
+                 const float *rope_cos, const float *rope_sin, float rope_base, void *q_out,
+                 void *k_out, void *v_out, float *k_pre_sq, float *k_post_sq, int B, int N,
+                 int H, int D, float k_scale, float eps, int dtype, void *stream);
+
+/*
+ * Reads and clears the device error word of the current device after
+ * synchronising `stream`.  Returns GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+int gdn_get_device_error(void *stream);
+
+/*
+ * Number of kernels this library has launched in this process (all devices,
+ * all entry points) since it was loaded.  Host-side counter; never blocks.
+ */
+unsigned long long gdn_launch_count(void);
+
+/*
+ * Test hook for the bounded-wait path: sets the number of polls a device
+ * wait makes before it gives up (0 restores the default).  Affects later
+ * launches on the current device only.
+ */
+int gdn_set_wait_limit(unsigned long long polls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every entry point gdn.h declares, and
+its host-side argument checks reject bad calls before anything is launched.
+No call here reaches a kernel, so these run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_47_gb300 import binding, build
+
+HEADER = os.path.join(build.INCLUDE, "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:unsigned\s+long\s+long|\w+)\s*\*?\s*(\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for n in ("gdn_chunk_fwd", "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_status_string",
+              "gdn_chunk_fwd_workspace_bytes", "gdn_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(binding.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert binding.status_string(code) == name
+    assert binding.status_string(99) == "GDN_ERR_UNKNOWN"
+    assert lib.gdn_version() >= 100
+
+
+def test_workspace_query(lib):
+    f = lib.gdn_chunk_fwd_workspace_bytes
+    bad = ctypes.c_size_t(-1).value
+    assert f(1, 2, 256, 1, 64, 64, 64, binding.GDN_F32) != bad
+    assert f(1, 2, 256, 1, 96, 64, 64, binding.GDN_F32) == bad   # Dk unsupported
+    assert f(1, 2, 256, 1, 64, 64, 48, binding.GDN_F32) == bad   # chunk unsupported
+    assert f(1, 2, 256, 3, 64, 64, 64, binding.GDN_F32) != bad   # 21 tokens per chunk
+    assert f(1, 2, 256, 9, 64, 64, 64, binding.GDN_F32) == bad   # r > 8
+    assert f(-1, 2, 256, 1, 64, 64, 64, binding.GDN_F32) == bad
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails its host checks first
+
+
+def scan_call(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, g=FAKE, s0=None, o=FAKE, sf=None, B=1, H=1, T=8,
+             Dk=64, Dv=64, chunk=64, scale=1.0, flags=0, dtype=binding.GDN_F32, ws=None, wsb=0)
+    a.update(kw)
+    return lib.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["beta"], a["g"], a["s0"], a["o"], a["sf"],
+                             a["B"], a["H"], a["T"], a["Dk"], a["Dv"], a["chunk"], a["scale"],
+                             a["flags"], a["dtype"], a["ws"], a["wsb"], None)
+
+
+def test_scan_argument_checks(lib):
+    assert scan_call(lib, q=None) == 1
+    assert scan_call(lib, dtype=7) == 1
+    assert scan_call(lib, flags=4) == 1
+    assert scan_call(lib, B=-1) == 1
+    assert scan_call(lib, Dk=96) == 2
+    assert scan_call(lib, chunk=128) == 2
+    assert scan_call(lib, v=FAKE + 8) == 3
+    assert scan_call(lib, s0=FAKE + 4) == 3
+
+
+def test_deltaproduct_argument_checks(lib):
+    f = lib.deltaproduct_chunk_fwd
+    args = lambda r, chunk: [FAKE] * 5 + [None, FAKE, None, 1, 1, 8, r, 64, 64, chunk, 1.0, 0,
+                                          binding.GDN_BF16, None, 0, None]
+    assert f(*args(0, 64)) == 1      # r < 1
+    assert f(*args(16, 64)) == 2     # r > 8
+
+
+def test_cam_prep_argument_checks(lib):
+    f = lib.cam_prep_fwd
+
+    def call(D=128, H=16, cos=None, sin=None, base=10000.0, q=FAKE, dtype=binding.GDN_BF16):
+        return f(q, FAKE, FAKE, None, None, FAKE, FAKE, cos, sin, base, FAKE, FAKE, FAKE, None, None,
+                 1, 4, H, D, 0.5, 1e-6, dtype, None)
+
+    assert call(D=12) == 1               # D/2 not divisible by 4
+    assert call(D=24) == 2               # not a multiple of 16
+    assert call(H=64, D=128) == 2        # H*D > 4096
+    assert call(cos=FAKE) == 1           # one table without the other
+    assert call(base=0.0) == 1
+    assert call(q=None) == 1
+    assert call(q=FAKE + 2) == 3
+    assert call(dtype=5) == 1
