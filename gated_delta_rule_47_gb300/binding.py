@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
 
 GDN_F32, GDN_BF16 = 0, 1
 GDN_QK_L2NORM = 1
+GDN_PATH_SIMT = 2
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
           4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
 
@@ -112,7 +113,7 @@ def workspace_bytes(B, H, T, Dk, Dv, chunk=64, r=1, dtype=torch.bfloat16):
 
 
 def _scan(fn_name, q, k, v, beta, g, r, initial_state, output_final_state, chunk, scale, l2norm,
-          o, workspace, stream):
+          o, workspace, stream, simt=False):
     B, H, T, Dk = q.shape
     Dv = v.shape[-1]
     dt = q.dtype
@@ -134,7 +135,7 @@ def _scan(fn_name, q, k, v, beta, g, r, initial_state, output_final_state, chunk
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     lib = load()
-    flags = GDN_QK_L2NORM if l2norm else 0
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0)
     common = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state), _ptr(o), _ptr(sf)]
     if r is None:
         st = lib.gdn_chunk_fwd(*common, B, H, T, Dk, Dv, chunk, float(scale), flags, code,
@@ -147,20 +148,21 @@ def _scan(fn_name, q, k, v, beta, g, r, initial_state, output_final_state, chunk
 
 
 def gdn_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_state=False, chunk=64,
-                  scale=1.0, l2norm=False, o=None, workspace=None, stream=None):
+                  scale=1.0, l2norm=False, o=None, workspace=None, stream=None, simt=False):
     """Chunkwise GDN forward.  q,k [B,H,T,Dk]; v [B,H,T,Dv]; beta [B,H,T] (all
-    bf16 or all fp32); g [B,H,T] fp32.  Returns (o, final_state or None)."""
+    bf16 or all fp32); g [B,H,T] fp32.  Returns (o, final_state or None).
+    simt=True takes the CUDA-core path even where the tensor-core one applies."""
     return _scan("gdn_chunk_fwd", q, k, v, beta, g, None, initial_state, output_final_state, chunk,
-                 scale, l2norm, o, workspace, stream)
+                 scale, l2norm, o, workspace, stream, simt)
 
 
 def deltaproduct_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_state=False, chunk=64,
-                           scale=1.0, l2norm=False, o=None, workspace=None, stream=None):
+                           scale=1.0, l2norm=False, o=None, workspace=None, stream=None, simt=False):
     """DeltaProduct forward.  q [B,H,T,Dk]; k [B,H,T,r,Dk]; v [B,H,T,r,Dv];
     beta [B,H,T,r]; g [B,H,T] fp32.  chunk counts expanded rows."""
     r = k.shape[3]
     return _scan("deltaproduct_chunk_fwd", q, k, v, beta, g, r, initial_state, output_final_state,
-                 chunk, scale, l2norm, o, workspace, stream)
+                 chunk, scale, l2norm, o, workspace, stream, simt)
 
 
 def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=None, rope_cos=None,
@@ -199,8 +201,9 @@ def device_error(stream=None) -> int:
     return int(load().gdn_get_device_error(_stream(stream)))
 
 
-def set_wait_limit(polls: int) -> None:
-    _raise("gdn_set_wait_limit", load().gdn_set_wait_limit(int(polls)))
+def set_wait_limit(us: int) -> None:
+    """Wall-clock limit in microseconds of each bounded device wait (0 = default)."""
+    _raise("gdn_set_wait_limit", load().gdn_set_wait_limit(int(us)))
 
 
 def launch_count() -> int:

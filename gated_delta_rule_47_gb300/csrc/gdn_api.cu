@@ -22,7 +22,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_scan(const gdn::ScanArgs &a) {
     if (a.B < 0 || a.H < 0 || a.T < 0 || a.r < 1) return GDN_ERR_INVALID_ARG;
     if (a.dtype != GDN_F32 && a.dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-    if (a.flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (a.flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
     if (a.chunk <= 0) return GDN_ERR_INVALID_ARG;
     if (a.chunk != 16 && a.chunk != 32 && a.chunk != 64) return GDN_ERR_UNSUPPORTED;
     if (a.r > 8) return GDN_ERR_UNSUPPORTED;
@@ -148,6 +148,6 @@ int gdn_get_device_error(void *stream) {
 
 unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }
 
-int gdn_set_wait_limit(unsigned long long polls) { return gdn::scan_tc_set_wait_limit(polls); }
+int gdn_set_wait_limit(unsigned long long us) { return gdn::scan_tc_set_wait_limit(us); }
 
 }  // extern "C"

@@ -57,6 +57,9 @@ typedef enum {
 /* flags */
 #define GDN_QK_L2NORM 1u /* normalise q_t and k_t to unit L2 norm at load,
                             q <- q / max(||q||, 1e-12) per (token, head)   */
+#define GDN_PATH_SIMT 2u /* use the CUDA-core path even where the tensor-core
+                            path applies (bf16, Dk = Dv = 128, chunk 64,
+                            r in {1, 2, 4})                                */
 
 /* Human-readable name of a status code; never NULL. */
 const char *gdn_status_string(int status);
@@ -89,7 +92,7 @@ size_t gdn_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv,
  *   chunk   rows per chunk: 16, 32 or 64.  Results do not depend on it beyond
  *           rounding.  T need not be a multiple of it.
  *   scale   multiplies every output (1.0 for the plain definition)
- *   flags   0 or GDN_QK_L2NORM
+ *   flags   0 or a combination of GDN_QK_L2NORM and GDN_PATH_SIMT
  *   dtype   GDN_F32 or GDN_BF16
  *   Dk, Dv  64 or 128 each
  *   workspace / workspace_bytes: device scratch of at least
@@ -172,9 +175,11 @@ int gdn_get_device_error(void *stream);
 unsigned long long gdn_launch_count(void);
 
 /*
- * Test hook for the bounded-wait path: sets the number of polls a device
- * wait makes before it gives up (0 restores the default).  Affects later
- * launches on the current device only.
+ * Test hook for the bounded-wait path: sets the wall-clock limit, in
+ * microseconds, of every bounded device wait in later launches (0 restores
+ * the default of one second).  A wait that runs out sets GDN_ERR_TIMEOUT in
+ * the device error word and its kernel stops early; the outputs of that
+ * call are then undefined, but the context stays usable.
  */
 int gdn_set_wait_limit(unsigned long long polls);
 

@@ -139,3 +139,60 @@ def test_full_size_deltaproduct_sampled_heads():
     ro, _ = oracle.deltaproduct_fwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"])
     assert rel_err(heads(o, idx).cpu(), ro) <= TOL_BF16
     assert torch.isfinite(o).all()
+
+
+# --- the tensor-core path (bf16, Dk = Dv = 128, chunk 64, r in {1,2,4}) against
+# --- the oracle and against the CUDA-core path on the same inputs.
+
+@pytest.mark.parametrize("T", [64, 300, 1000])
+def test_tensor_core_and_cuda_core_paths_agree(T):
+    inp = gdn_inputs(2, 3, T, 128, 128, seed=T + 5, dtype="bf16", initial_state=True)
+    d = to_dev(inp)
+    args = (d["q"], d["k"], d["v"], d["beta"], d["g"], d["initial_state"])
+    o_tc, s_tc = binding.gdn_chunk_fwd(*args, output_final_state=True)
+    o_sm, s_sm = binding.gdn_chunk_fwd(*args, output_final_state=True, simt=True)
+    torch.cuda.synchronize()
+    ro, rs = ref_gdn(inp)
+    assert rel_err(o_tc, ro) <= TOL_BF16 and rel_err(s_tc, rs) <= TOL_BF16
+    assert rel_err(o_sm, ro) <= TOL_BF16 and rel_err(s_sm, rs) <= TOL_BF16
+    assert binding.device_error() == 0
+
+
+@pytest.mark.parametrize("r", [2, 4])
+def test_tensor_core_deltaproduct(r):
+    inp = gdn_inputs(1, 2, 150, 128, 128, seed=40 + r, dtype="bf16", r=r, initial_state=True)
+    d = to_dev(inp)
+    o, sf = binding.deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["initial_state"],
+                                           output_final_state=True, chunk=64)
+    ro, rs = oracle.deltaproduct_fwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"],
+                                     inp["initial_state"])
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
+def test_tensor_core_l2norm_and_scale():
+    inp = gdn_inputs(1, 2, 200, 128, 128, seed=77, dtype="bf16", normalise_qk=False, initial_state=True)
+    o, sf = run_gdn(inp, l2norm=True, scale=0.5)
+    ro, rs = ref_gdn(inp, l2norm=True, scale=0.5)
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """A 1-microsecond wait limit makes the kernel's first mbarrier wait run
+    out: the call reports GDN_ERR_TIMEOUT through the device error word, and
+    with the default limit restored the next call is correct."""
+    inp = gdn_inputs(1, 2, 1024, 128, 128, seed=3, dtype="bf16")
+    d = to_dev(inp)
+    assert binding.device_error() == 0
+    try:
+        binding.set_wait_limit(1)
+        binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"])
+        assert binding.device_error() == 6
+    finally:
+        binding.set_wait_limit(0)
+    assert binding.device_error() == 0
+    o, _ = binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"])
+    torch.cuda.synchronize()
+    ro, _ = ref_gdn(inp)
+    assert rel_err(o, ro) <= TOL_BF16
