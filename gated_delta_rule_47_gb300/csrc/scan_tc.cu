@@ -21,13 +21,13 @@
 // state S^T stays in tensor memory in fp32 for the whole sequence and only
 // q, k, v, beta, g are read and o written.
 //
-// Warp roles (384 threads):
+// Warp roles (512 threads):
 //   warp 0        TMA producer: K, Q (two stages) and V tiles.
 //   warp 1        MMA issuer; owns the 512-column TMEM allocation.
 //   warps 4..7    scan epilogue (SE): S^T -> bf16 operand, state decay,
 //                 Vn^T -> bf16 operands, output tile -> TMA store.
-//   warps 8..11   WY producer: cumulative decay, A, blocked (I+A)^-1, the
-//                 scaled T tiles, P, Qg, and W^T -> bf16 operand.
+//   warps 8..15   WY producer: cumulative decay, A, blocked (I+A)^-1 in
+//                 place, the scaled T tiles, P, Qg, and W^T -> bf16 operand.
 // Every wait on an mbarrier is bounded in wall time; on expiry the CTA sets
 // an error word, stops issuing work, drains what is in flight, frees TMEM
 // and exits.
@@ -48,18 +48,33 @@ __device__ unsigned int g_tc_error = 0;
 unsigned long long g_timeout_ns = 1000000000ull;  // host copy of the wait limit
 }  // namespace
 
+// Optional timeline instrumentation (compiled in only with -DGDN_TRACE): the
+// first CTA records clock64() at fixed points of each role, per chunk.
+#ifdef GDN_TRACE
+__device__ unsigned long long *g_trace = nullptr;
+#define GDN_TR(c, ev)                                                          \
+    do {                                                                       \
+        if (blockIdx.x == 0 && g_trace != nullptr && (c) < 1024)               \
+            g_trace[(size_t)(c) * 32 + (ev)] = clock64();                      \
+    } while (0)
+#else
+#define GDN_TR(c, ev) \
+    do {              \
+    } while (0)
+#endif
+
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kAS = 68;  // fp32 row stride of the A / T tiles
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KQ0 = 0;        // [K rows 0..63 | Q rows 64..] x 2 K-blocks, 32 KB
 constexpr uint32_t OFF_KQ1 = 32768;
 constexpr uint32_t OFF_V = 65536;      // V tile [64 s][128 dv], 2 MN-atoms, 16 KB
-constexpr uint32_t OFF_AF = 81920;     // A fp32 [64][68]; later Tw (+0) and Tu (+8192), bf16
-constexpr uint32_t OFF_TF = 99328;     // T fp32 [64][68]
+constexpr uint32_t OFF_AF = 81920;     // A fp32 [64][68], inverted in place into T
+constexpr uint32_t OFF_TWU = 99328;    // Tw (+0) and Tu (+8192), bf16 [64 t][64 s] K-major
 constexpr uint32_t OFF_P0 = 116736;    // P bf16 [NQ t][64 s] K-major, 8 KB each
 constexpr uint32_t OFF_P1 = 124928;
 constexpr uint32_t OFF_WT = 133120;    // W^T bf16 [128 d][64 t] MN-major, 16 KB
@@ -67,10 +82,9 @@ constexpr uint32_t OFF_ST = 149504;    // S^T bf16 [128 dv][128 dk] K-major, 32 
 constexpr uint32_t OFF_VN = 182272;    // Vn^T bf16 [128 dv][64 s] K-major, 16 KB
 constexpr uint32_t OFF_VS = 198656;    // decayed Vn^T, 16 KB; also the output staging tile
 constexpr uint32_t OFF_MISC = 215040;  // 2 x Misc
-constexpr uint32_t OFF_SEF = 219136;   // SE: exp(g_last - g_s) n_s, 64 floats
-constexpr uint32_t OFF_X = 219392;     // inverse scratch, 32x32 fp32
-constexpr uint32_t OFF_BAR = 223488;   // mbarriers
-constexpr uint32_t OFF_FLAGS = 223744; // TMEM base, abort flag
+constexpr uint32_t OFF_X = 221184;     // inverse scratch, 32x32 fp32
+constexpr uint32_t OFF_BAR = 225280;   // mbarriers
+constexpr uint32_t OFF_FLAGS = 225536; // TMEM base, abort flag
 constexpr uint32_t kSmemBytes = OFF_FLAGS + 64 + 1024;
 
 // TMEM columns
@@ -81,15 +95,22 @@ enum Bar {
     B_VN_DONE, B_VN_READY, B_UPD_DONE, B_STG_FREE0, B_STG_FREE1, B_MISC0, B_MISC1, B_DRAIN, B_NUM
 };
 
+// Per-chunk vectors written by the WY warps (two copies, by chunk parity).
 struct Misc {
-    float beta[64];  // beta of each row (0 past the end)
-    float gam[64];   // within-chunk cumulative log-decay
-    float n[64];     // 1/||k_s|| with GDN_QK_L2NORM, else 1
-    float m[64];     // 1/||q_t|| with GDN_QK_L2NORM, else 1
-    float wsc[64];   // beta_s exp(gam_s) n_s
-    float pad[192];
+    float beta[64];   // beta of each row (0 past the end)
+    float gam[64];    // within-chunk cumulative log-decay
+    float n[64];      // 1/||k_s|| with GDN_QK_L2NORM, else 1
+    float m[64];      // 1/||q_t|| with GDN_QK_L2NORM, else 1
+    float wsc[64];    // beta_s exp(gam_s) n_s          (columns of Tw)
+    float bn[64];     // exp(gam_0 - gam_s) n_s         (column factor of A and P)
+    float ea[64];     // exp(gam_t - gam_0)             (row factor of A and P)
+    float sef[64];    // exp(gam_last - gam_s) n_s      (columns of the decayed Vn^T)
+    float qp[2][64];  // partial q_t^2 sums over the two key-dim halves
+    float el;         // exp(gam_last)
+    int safe;         // 1 if |gam_t - gam_0| <= 80 for all rows (factorised exponentials)
+    float pad[126];
 };
-static_assert(sizeof(Misc) == 2048, "Misc layout");
+static_assert(sizeof(Misc) == 3072, "Misc layout");
 
 struct TcParams {
     const __nv_bfloat16 *beta;
@@ -111,7 +132,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, unsigne
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > timeout_ns) {
             *abort_flag = 1;
@@ -142,17 +163,6 @@ __device__ __forceinline__ bool group_all(bool ok, int id, int n) {
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
 
-__device__ __forceinline__ void ld64(uint32_t taddr, float (&x)[64]) {
-    uint32_t r[16];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        tmem_ld16(taddr + 16 * j, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[16 * j + i] = __uint_as_float(r[i]);
-    }
-}
-
 // Writes 64 fp32 values as one bf16 row of a 128-byte-swizzled tile.
 __device__ __forceinline__ void store_row_sw128(uint8_t *tile, int row, const float (&x)[64]) {
 #pragma unroll
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TcParams p) {
     constexpr int NQ = 64 / R;  // query rows (tokens) per chunk
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_FLAGS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_FLAGS + 4);
@@ -212,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < NT; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !wait_bar(&bars[B_STG_FREE0 + s], ((c - 2) >> 1) & 1, tmo, abort_flag, 1u)) break;
+                GDN_TR(c, 0);
                 uint8_t *kq = sm + (s ? OFF_KQ1 : OFF_KQ0);
                 mbar_arrive_expect_tx(&bars[B_FULL0 + s], 2 * 8192 + 2 * NQ * 128);
                 tma_load_3d(kq, &mK, &bars[B_FULL0 + s], 0, c * 64, bh);
@@ -220,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(kq + 24576, &mQ, &bars[B_FULL0 + s], 64, c * NQ, bh);
                 armed_full[s]++;
                 if (c >= 1 && !wait_bar(&bars[B_WU_DONE], (c - 1) & 1, tmo, abort_flag, 1u)) break;
+                GDN_TR(c, 1);
                 mbar_arrive_expect_tx(&bars[B_VFULL], 16384);
                 tma_load_3d(sm + OFF_V, &mV, &bars[B_VFULL], 0, c * 64, bh);
                 tma_load_3d(sm + OFF_V + 8192, &mV, &bars[B_VFULL], 64, c * 64, bh);
@@ -261,26 +273,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tO = tmem + ((c & 1) ? TM_O1 : TM_O0);
                 // W^T and U^T of chunk c
                 if (!wait_bar(&bars[B_WY_READY], c & 1, tmo, abort_flag, 2u)) break;
+                GDN_TR(c, 2);
                 if (!wait_bar(&bars[B_VFULL], c & 1, tmo, abort_flag, 2u)) break;
+                GDN_TR(c, 3);
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t a = smem_desc(kq + ks * 2048, 16384, 1024);
-                    const uint64_t b = smem_desc(sbase + OFF_AF + ks * 32, 16, 1024);
+                    const uint64_t b = smem_desc(sbase + OFF_TWU + ks * 32, 16, 1024);
                     mma_bf16_ss(tmem + TM_W, a, b, idWU, ks > 0);
                 }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t a = smem_desc(sbase + OFF_V + ks * 2048, 8192, 1024);
-                    const uint64_t b = smem_desc(sbase + OFF_AF + 8192 + ks * 32, 16, 1024);
+                    const uint64_t b = smem_desc(sbase + OFF_TWU + 8192 + ks * 32, 16, 1024);
                     mma_bf16_ss(tvn, a, b, idWU, ks > 0);
                 }
                 mma_commit(&bars[B_WU_DONE]);
                 // K K^T / Q K^T of the next chunk, so the WY warps can start on it
                 if (c + 1 < NT && !issue_kq(c + 1)) break;
+                GDN_TR(c, 4);
                 // Vn^T = U^T - S^T W^T ;  O^T = S^T Qg^T
                 if (!wait_bar(&bars[B_WT_READY], c & 1, tmo, abort_flag, 2u)) break;
+                GDN_TR(c, 5);
                 if (!wait_bar(&bars[B_S_READY], c & 1, tmo, abort_flag, 2u)) break;
+                GDN_TR(c, 6);
                 tc_fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -288,31 +305,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t b = smem_desc(sbase + OFF_WT + ks * 2048, 8192, 1024);
                     mma_bf16_ss(tvn, a, b, idVN, 1u);
                 }
+                mma_commit(&bars[B_VN_DONE]);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t a = smem_desc(sbase + OFF_ST + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
                     const uint64_t b = smem_desc(kq + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
                     mma_bf16_ss(tO, a, b, idO, ks > 0);
                 }
-                mma_commit(&bars[B_VN_DONE]);
                 // O^T += Vn^T P^T ;  S^T += (decayed Vn^T) K
                 if (!wait_bar(&bars[B_VN_READY], c & 1, tmo, abort_flag, 2u)) break;
+                GDN_TR(c, 7);
                 tc_fence_after_sync();
                 const uint32_t pt = sbase + ((c & 1) ? OFF_P1 : OFF_P0);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t a = smem_desc(sbase + OFF_VN + ks * 32, 16, 1024);
-                    const uint64_t b = smem_desc(pt + ks * 32, 16, 1024);
-                    mma_bf16_ss(tO, a, b, idO, 1u);
-                }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t a = smem_desc(sbase + OFF_VS + ks * 32, 16, 1024);
                     const uint64_t b = smem_desc(kq + ks * 2048, 16384, 1024);
                     mma_bf16_ss(tmem + TM_S, a, b, idUP, 1u);
                 }
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t a = smem_desc(sbase + OFF_VN + ks * 32, 16, 1024);
+                    const uint64_t b = smem_desc(pt + ks * 32, 16, 1024);
+                    mma_bf16_ss(tO, a, b, idO, 1u);
+                }
                 mma_commit(&bars[B_UPD_DONE]);
                 mma_commit(&bars[B_STG_FREE0 + s]);
+                GDN_TR(c, 8);
             }
             // every issued MMA completes before TMEM is released
             mma_commit(&bars[B_DRAIN]);
@@ -322,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ scan epilogue
         const int st = threadIdx.x - 128;  // value index dv = TMEM lane
         const uint32_t lb = tmem_lane_base(warp);
-        float *sef = reinterpret_cast<float *>(sm + OFF_SEF);
         uint8_t *ostage = sm + OFF_VS;
         // initial state into TMEM: S^T[dv][dk] = S0[dk][dv]
         {
@@ -339,14 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto out_epilogue = [&](int cc) {
             const uint32_t tO = tmem + lb + ((cc & 1) ? TM_O1 : TM_O0);
 #pragma unroll 1
-            for (int j = 0; j < NQ / 16; ++j) {
-                uint32_t r[16];
-                tmem_ld16(tO + 16 * j, r);
+            for (int j = 0; j < NQ / 32 + (NQ == 16); ++j) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tO + 32 * j, r0);
+                if (NQ >= 32) tmem_ld16(tO + 32 * j + 16, r1);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const __nv_bfloat16 h = __float2bfloat16_rn(p.scale * __uint_as_float(r[i]));
-                    *reinterpret_cast<__nv_bfloat16 *>(ostage + (16 * j + i) * 256 + st * 2) = h;
+                    *reinterpret_cast<__nv_bfloat16 *>(ostage + (32 * j + i) * 256 + st * 2) =
+                        __float2bfloat16_rn(p.scale * __uint_as_float(r0[i]));
+                    if (NQ >= 32)
+                        *reinterpret_cast<__nv_bfloat16 *>(ostage + (32 * j + 16 + i) * 256 + st * 2) =
+                            __float2bfloat16_rn(p.scale * __uint_as_float(r1[i]));
                 }
             }
             tc_fence_before_sync();
@@ -364,53 +386,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool w = wait_bar(&bars[B_MISC0 + s], (c >> 1) & 1, tmo, abort_flag, 4u);
             if (w && c >= 1) w = wait_bar(&bars[B_UPD_DONE], (c - 1) & 1, tmo, abort_flag, 4u);
             if (!group_all(w, 2, 128)) { ok = false; break; }
+            if (st == 0) GDN_TR(c, 9);
             tc_fence_after_sync();
-            const float glast = ms->gam[63];
-            if (st < 64) sef[st] = __expf(glast - ms->gam[st]) * ms->n[st];
             // state: S^T -> bf16 operand, then S^T <- exp(g_last) S^T in TMEM
-            const float el = __expf(glast);
+            const float el = ms->el;
 #pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
-                uint32_t r[16];
-                tmem_ld16(tmem + lb + TM_S + 16 * j, r);
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tmem + lb + TM_S + 32 * j, r0);
+                tmem_ld16(tmem + lb + TM_S + 32 * j + 16, r1);
                 tmem_wait_ld();
-                uint8_t *blk = sm + OFF_ST + (j >> 2) * 16384;
-                const int col = (16 * j) & 63;
-                uint4 v0, v1;
-                v0.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
-                v0.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
-                v0.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
-                v0.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
-                v1.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
-                v1.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
-                v1.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
-                v1.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
-                *reinterpret_cast<uint4 *>(blk + sw128_offset(st, col)) = v0;
-                *reinterpret_cast<uint4 *>(blk + sw128_offset(st, col + 8)) = v1;
+                uint8_t *blk = sm + OFF_ST + (j >> 1) * 16384;
+                const int col = (32 * j) & 63;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(el * __uint_as_float(r[i]));
-                tmem_st16(tmem + lb + TM_S + 16 * j, r);
+                for (int k = 0; k < 2; ++k) {
+                    const uint32_t *r = k ? r1 : r0;
+                    uint4 v0, v1;
+                    v0.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
+                    v0.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
+                    v0.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
+                    v0.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
+                    v1.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
+                    v1.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
+                    v1.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
+                    v1.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
+                    *reinterpret_cast<uint4 *>(blk + sw128_offset(st, col + 16 * k)) = v0;
+                    *reinterpret_cast<uint4 *>(blk + sw128_offset(st, col + 16 * k + 8)) = v1;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    r0[i] = __float_as_uint(el * __uint_as_float(r0[i]));
+                    r1[i] = __float_as_uint(el * __uint_as_float(r1[i]));
+                }
+                tmem_st16(tmem + lb + TM_S + 32 * j, r0);
+                tmem_st16(tmem + lb + TM_S + 32 * j + 16, r1);
             }
             tmem_wait_st();
             tc_fence_before_sync();
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_S_READY]);
+            if (st == 0) GDN_TR(c, 10);
             // output of the previous chunk (its MMAs completed with UPD_DONE)
             if (c >= 1) out_epilogue(c - 1);
+            if (st == 0) GDN_TR(c, 11);
             // Vn^T of this chunk -> two bf16 operands
             const bool wv = wait_bar(&bars[B_VN_DONE], c & 1, tmo, abort_flag, 4u);
             if (st == 0) tma_store_wait_read<0>();
-            if (!group_all(wv, 2, 128)) { ok = false; break; }  // staging tile free, sef visible
+            if (!group_all(wv, 2, 128)) { ok = false; break; }  // staging tile free
+            if (st == 0) GDN_TR(c, 12);
             tc_fence_after_sync();
             float x[64];
-            ld64(tmem + lb + ((c & 1) ? TM_VN1 : TM_VN0), x);
+            {
+                const uint32_t tv = tmem + lb + ((c & 1) ? TM_VN1 : TM_VN0);
+                uint32_t r[4][16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld16(tv + 16 * j, r[j]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) x[16 * j + i] = __uint_as_float(r[j][i]);
+            }
             store_row_sw128(sm + OFF_VN, st, x);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] *= sef[i];
+            for (int i = 0; i < 64; i += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(&ms->sef[i]);
+                x[i] *= f.x;
+                x[i + 1] *= f.y;
+                x[i + 2] *= f.z;
+                x[i + 3] *= f.w;
+            }
             store_row_sw128(sm + OFF_VS, st, x);
             tc_fence_before_sync();
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_VN_READY]);
+            if (st == 0) GDN_TR(c, 13);
         }
         bool fin = ok && NT > 0 && wait_bar(&bars[B_UPD_DONE], (NT - 1) & 1, tmo, abort_flag, 4u);
         if (st == 0) tma_store_wait_read<0>();
@@ -432,30 +482,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (st == 0) tma_store_wait_all<0>();
     } else if (warp >= 8) {
         // ------------------------------------------------------------ WY producer
-        const int wt = threadIdx.x - 256;  // 0..127
-        const int wq = wt >> 5;
+        // 8 warps.  Warp w reads TMEM lane quarter (w & 3) and works on column
+        // half h = (w - 8) / 4 of the 64-wide chunk tiles.
+        const int wt = threadIdx.x - 256;  // 0..255
+        const int q = warp & 3;
+        const int h = (warp - 8) >> 2;
         const uint32_t lb = tmem_lane_base(warp);
         float *AF = reinterpret_cast<float *>(sm + OFF_AF);
-        float *TF = reinterpret_cast<float *>(sm + OFF_TF);
         float *XS = reinterpret_cast<float *>(sm + OFF_X);
+        uint8_t *twu = sm + OFF_TWU;
         const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
         const __nv_bfloat16 *betap = p.beta + (size_t)bh * p.rows;
         const float *gp = p.g + (size_t)bh * p.T;
+        // beta / g of a chunk, fetched one chunk ahead into a register
+        auto prefetch = [&](int cc) -> float {
+            if (wt < 64) {
+                const int row = cc * 64 + wt;
+                return row < p.rows ? __bfloat162float(betap[row]) : 0.f;
+            }
+            if (wt < 128) {
+                const int row = cc * 64 + wt - 64;
+                return (row < p.rows && row % R == 0) ? gp[row / R] : 0.f;
+            }
+            return 0.f;
+        };
+        float pf = NT > 0 ? prefetch(0) : 0.f;
         for (int c = 0; c < NT; ++c) {
             const int s = c & 1;
             Misc *ms = misc + s;
             uint8_t *kq = sm + (s ? OFF_KQ1 : OFF_KQ0);
             uint8_t *ptile = sm + ((c & 1) ? OFF_P1 : OFF_P0);
-            // 1. beta and g of the chunk's rows
-            if (wt < 64) {
-                const int row = c * 64 + wt;
-                ms->beta[wt] = row < p.rows ? __bfloat162float(betap[row]) : 0.f;
-            } else {
-                const int t = wt - 64, row = c * 64 + t;
-                ms->gam[t] = (row < p.rows && row % R == 0) ? gp[row / R] : 0.f;
-            }
-            named_bar(1, 128);
-            if (wq == 0) {
+            if (wt == 0) GDN_TR(c, 14);
+            // 1. beta and g of the chunk's rows; cumulative decay
+            if (wt < 64) ms->beta[wt] = pf;
+            else if (wt < 128) ms->gam[wt - 64] = pf;
+            if (c + 1 < NT) pf = prefetch(c + 1);
+            named_bar(1, 256);
+            if (wt < 32) {
                 float a = ms->gam[lane], b = ms->gam[lane + 32];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -466,198 +529,291 @@ __global__ void __launch_bounds__(kThreads, 1)
                 b += __shfl_sync(0xffffffffu, a, 31);
                 ms->gam[lane] = a;
                 ms->gam[lane + 32] = b;
+                const float g0 = __shfl_sync(0xffffffffu, a, 0);
+                float dev = fmaxf(fabsf(a - g0), fabsf(b - g0));
+#pragma unroll
+                for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
+                if (lane == 31) {
+                    ms->safe = dev <= 80.f ? 1 : 0;
+                    ms->el = __expf(b);
+                }
             }
             const bool wk = wait_bar(&bars[B_KQ_DONE], c & 1, tmo, abort_flag, 8u);
-            if (!group_all(wk, 1, 128)) break;  // also makes gam visible
+            if (!group_all(wk, 1, 256)) break;  // also publishes gam
+            if (wt == 0) GDN_TR(c, 15);
             tc_fence_after_sync();
-            // 2. rows of K K^T (warps 0,1) and Q K^T (warps 2,3)
-            float x[64];
-            ld64(tmem + lb + TM_KQ, x);
-            if (wq < 2) {
-                float diag = 0.f;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) diag = (i == wt) ? x[i] : diag;
-                ms->n[wt] = l2n ? rsqrtf(fmaxf(diag, 1e-24f)) : 1.f;
-            } else {
-                const int t = wt - 64;
-                float mq = 1.f;
-                if (l2n && t < NQ) {
-                    float ss = 0.f;
-#pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const uint4 *row = reinterpret_cast<const uint4 *>(kq + 8192 + blk * 16384 + t * 128);
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            const uint4 u = row[ch];
-                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
-                                ss += lo * lo + hi * hi;
-                            }
-                        }
-                    }
-                    mq = rsqrtf(fmaxf(ss, 1e-24f));
-                }
-                ms->m[t] = mq;
-            }
-            tc_fence_before_sync();
-            named_bar(1, 128);  // n, m visible; TMEM rows read
-            if (wt == 0) mbar_arrive(&bars[B_KQ_FREE]);
-            if (wt < 64) {
-                const float bn = ms->beta[wt] * ms->n[wt];
-                const float gt = ms->gam[wt];
-                ms->wsc[wt] = ms->beta[wt] * __expf(gt) * ms->n[wt];
-#pragma unroll
-                for (int sidx = 0; sidx < 64; ++sidx) {
-                    float a = 0.f;
-                    if (sidx < wt) a = bn * __expf(gt - ms->gam[sidx]) * ms->n[sidx] * x[sidx];
-                    AF[wt * kAS + sidx] = a;
-                }
-            } else {
-                const int t = wt - 64;
-                if (t < NQ) {
-                    const int row = t * R + R - 1;
-                    const float gr = ms->gam[row];
-                    const float mq = ms->m[t];
-#pragma unroll
-                    for (int sidx = 0; sidx < 64; ++sidx)
-                        x[sidx] = (sidx <= row) ? __expf(gr - ms->gam[sidx]) * mq * ms->n[sidx] * x[sidx] : 0.f;
-                    store_row_sw128(ptile, t, x);
-                    // Qg row: q_t exp(g_row) / ||q_t||
-                    const float qs = __expf(gr) * mq;
-#pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        uint4 *rowp = reinterpret_cast<uint4 *>(kq + 8192 + blk * 16384 + t * 128);
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            uint4 u = rowp[ch];
-                            uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float lo = __uint_as_float(w4[e] << 16) * qs;
-                                const float hi = __uint_as_float(w4[e] & 0xffff0000u) * qs;
-                                w4[e] = pack_bf16(lo, hi);
-                            }
-                            rowp[ch] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
-                    }
-                }
-            }
-            named_bar(1, 128);  // A complete
-            if (wt == 0) mbar_arrive(&bars[B_MISC0 + s]);
-            // 3. T = (I + A)^-1, blocked: 16x16 diagonal blocks by substitution,
-            //    then the 16- and 32-level off-diagonal merges T21 = -T22 A21 T11.
-            if (wt < 64) {
-                const int b = wt >> 4, cc = wt & 15;
-                float xs[16];
+            // 2. this thread's 32 columns of its K K^T (q < 2) or Q K^T (q >= 2) row
+            float x[32];
+            {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tmem + lb + TM_KQ + 32 * h, r0);
+                tmem_ld16(tmem + lb + TM_KQ + 32 * h + 16, r1);
+                tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float acc = (i == cc) ? 1.f : 0.f;
-#pragma unroll
-                    for (int j = 0; j < i; ++j) acc -= AF[(16 * b + i) * kAS + 16 * b + j] * xs[j];
-                    xs[i] = acc;
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) TF[(16 * b + i) * kAS + 16 * b + cc] = xs[i];
-            } else {
-                // zero the blocks above the diagonal
-                for (int e = wt - 64; e < 6 * 256; e += 64) {
-                    const int blk = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
-                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    TF[(16 * bi + rr) * kAS + 16 * bj + cl] = 0.f;
+                    x[i] = __uint_as_float(r0[i]);
+                    x[16 + i] = __uint_as_float(r1[i]);
                 }
             }
-            named_bar(1, 128);
-            // 16-level merges inside each 32 half: blocks (1,0) and (3,2)
-            {
+            const int t = 32 * (q & 1) + lane;  // row of K K^T, or query row of Q K^T
+            if (q < 2) {
+                if (h == (q & 1)) {
+                    float diag = 0.f;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = wt + 128 * k;           // 0..511
-                    const int h = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
-                    const int i0 = 32 * h + 16, j0 = 32 * h;  // block (i0, j0)
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) acc += AF[(i0 + rr) * kAS + j0 + m] * TF[(j0 + m) * kAS + j0 + cl];
-                    XS[e] = acc;
+                    for (int i = 0; i < 32; ++i) diag = (i == lane) ? x[i] : diag;
+                    ms->n[t] = l2n ? rsqrtf(fmaxf(diag, 1e-24f)) : 1.f;
                 }
-                named_bar(1, 128);
+            } else if (l2n) {
+                float ss = 0.f;
+                const uint4 *rowp = reinterpret_cast<const uint4 *>(kq + 8192 + h * 16384 + t * 128);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = wt + 128 * k;
-                    const int h = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
-                    const int i0 = 32 * h + 16, j0 = 32 * h;
-                    float acc = 0.f;
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 u = rowp[ch];
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) acc += TF[(i0 + rr) * kAS + i0 + m] * XS[(h << 8) + m * 16 + cl];
-                    TF[(i0 + rr) * kAS + j0 + cl] = -acc;
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+                        ss += lo * lo + hi * hi;
+                    }
                 }
-                named_bar(1, 128);
+                ms->qp[h][t] = ss;
             }
-            // 32-level merge: rows 32..63, cols 0..31
-            {
-                const int cl = wt & 31, r0 = wt >> 5;  // rows r0 + 4k
-                float acc[8];
+            tc_fence_before_sync();
+            named_bar(1, 256);  // n and partial q norms visible; TMEM rows read
+            if (wt == 0) mbar_arrive(&bars[B_KQ_FREE]);
+            if (wt == 0) GDN_TR(c, 16);
+            // per-row / per-column factors of the chunk
+            if (wt < 64) {
+                const float g0 = ms->gam[0], gi = ms->gam[wt], gl = ms->gam[63];
+                const float ni = ms->n[wt];
+                ms->m[wt] = l2n ? rsqrtf(fmaxf(ms->qp[0][wt] + ms->qp[1][wt], 1e-24f)) : 1.f;
+                ms->wsc[wt] = ms->beta[wt] * __expf(gi) * ni;
+                ms->bn[wt] = __expf(g0 - gi) * ni;
+                ms->ea[wt] = __expf(gi - g0);
+                ms->sef[wt] = __expf(gl - gi) * ni;
+            }
+            named_bar(1, 256);
+            if (wt == 0) mbar_arrive(&bars[B_MISC0 + s]);
+            // 3. A rows (q < 2), P rows and scaled query rows (q >= 2)
+            const bool safe = ms->safe != 0;
+            if (q < 2) {
+                const float gt = ms->gam[t];
+                const float rowb = ms->beta[t] * ms->n[t];
+                float av[32];
+                if (safe) {
+                    const float rowf = rowb * ms->ea[t];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll 4
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 bn4 = *reinterpret_cast<const float4 *>(&ms->bn[32 * h + 4 * j]);
+                        av[4 * j] = rowf * bn4.x * x[4 * j];
+                        av[4 * j + 1] = rowf * bn4.y * x[4 * j + 1];
+                        av[4 * j + 2] = rowf * bn4.z * x[4 * j + 2];
+                        av[4 * j + 3] = rowf * bn4.w * x[4 * j + 3];
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        av[i] = rowb * __expf(gt - ms->gam[32 * h + i]) * ms->n[32 * h + i] * x[i];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int s0 = 32 * h + 4 * j;
+                    *reinterpret_cast<float4 *>(&AF[t * kAS + s0]) =
+                        make_float4(s0 < t ? av[4 * j] : 0.f, s0 + 1 < t ? av[4 * j + 1] : 0.f,
+                                    s0 + 2 < t ? av[4 * j + 2] : 0.f, s0 + 3 < t ? av[4 * j + 3] : 0.f);
+                }
+            } else if (t < NQ) {
+                const int row = t * R + R - 1;
+                const float gr = ms->gam[row];
+                const float mt = ms->m[t];
+                float pv[32];
+                if (safe) {
+                    const float rowf = mt * ms->ea[row];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 bn4 = *reinterpret_cast<const float4 *>(&ms->bn[32 * h + 4 * j]);
+                        pv[4 * j] = rowf * bn4.x * x[4 * j];
+                        pv[4 * j + 1] = rowf * bn4.y * x[4 * j + 1];
+                        pv[4 * j + 2] = rowf * bn4.z * x[4 * j + 2];
+                        pv[4 * j + 3] = rowf * bn4.w * x[4 * j + 3];
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        pv[i] = mt * __expf(gr - ms->gam[32 * h + i]) * ms->n[32 * h + i] * x[i];
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s0 = 32 * h + 2 * j;
+                    pk[j] = pack_bf16(s0 <= row ? pv[2 * j] : 0.f, s0 + 1 <= row ? pv[2 * j + 1] : 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(ptile + sw128_offset(t, 32 * h + 8 * j)) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                // Qg row t, key-dim half h: q_t exp(g_row) / ||q_t||
+                const float qs = __expf(gr) * mt;
+                uint4 *rowp = reinterpret_cast<uint4 *>(kq + 8192 + h * 16384 + t * 128);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 u = rowp[ch];
+                    uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16(__uint_as_float(w4[e] << 16) * qs, __uint_as_float(w4[e] & 0xffff0000u) * qs);
+                    rowp[ch] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+            named_bar(1, 256);  // A complete
+            if (wt == 0) GDN_TR(c, 17);
+            // 4. T = (I + A)^-1 in place over A: 16x16 diagonal blocks by
+            //    substitution, then the merges T_ij = -T_ii A_ij T_jj (16 level)
+            //    and T_bl = -T_bot A_bl T_top (32 level).
+            float xs[16];
+            const int db = wt >> 4, dc = wt & 15;
+            if (wt < 64) {
+                float pp[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pp[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    xs[j] = ((j == dc) ? 1.f : 0.f) - pp[j];
+#pragma unroll
+                    for (int i = j + 1; i < 16; ++i) pp[i] += AF[(16 * db + i) * kAS + 16 * db + j] * xs[j];
+                }
+            }
+            if (wt == 0) GDN_TR(c, 22);
+            named_bar(1, 256);
+            if (wt < 64) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) AF[(16 * db + i) * kAS + 16 * db + dc] = xs[i];
+            }
+            named_bar(1, 256);
+            {
+                float acc[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int e = wt + 256 * k;
+                    const int hh = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
+                    const int i0 = 32 * hh + 16, j0 = 32 * hh;
+                    float a = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) a += AF[(i0 + rr) * kAS + j0 + m] * AF[(j0 + m) * kAS + j0 + cl];
+                    acc[k] = a;
+                }
+                XS[wt] = acc[0];
+                XS[wt + 256] = acc[1];
+                if (wt == 0) GDN_TR(c, 23);
+                named_bar(1, 256);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int e = wt + 256 * k;
+                    const int hh = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
+                    const int i0 = 32 * hh + 16;
+                    float a = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) a += AF[(i0 + rr) * kAS + i0 + m] * XS[(hh << 8) + m * 16 + cl];
+                    acc[k] = a;
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int e = wt + 256 * k;
+                    const int hh = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
+                    AF[(32 * hh + 16 + rr) * kAS + 32 * hh + cl] = -acc[k];
+                }
+                named_bar(1, 256);
+            }
+            {
+                const int cl = wt & 31, r0 = wt >> 5;  // rows r0 + 8k, k < 4
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
                 for (int m = 0; m < 32; m += 4) {
-                    const float t0 = TF[(m + 0) * kAS + cl], t1 = TF[(m + 1) * kAS + cl];
-                    const float t2 = TF[(m + 2) * kAS + cl], t3 = TF[(m + 3) * kAS + cl];
+                    const float t0 = AF[(m + 0) * kAS + cl], t1 = AF[(m + 1) * kAS + cl];
+                    const float t2 = AF[(m + 2) * kAS + cl], t3 = AF[(m + 3) * kAS + cl];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(&AF[(32 + r0 + 4 * k) * kAS + m]);
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&AF[(32 + r0 + 8 * k) * kAS + m]);
                         acc[k] += a4.x * t0 + a4.y * t1 + a4.z * t2 + a4.w * t3;
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) XS[(r0 + 4 * k) * 32 + cl] = acc[k];
-                named_bar(1, 128);
+                for (int k = 0; k < 4; ++k) XS[(r0 + 8 * k) * 32 + cl] = acc[k];
+                if (wt == 0) GDN_TR(c, 24);
+                named_bar(1, 256);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll 4
+                for (int k = 0; k < 4; ++k) acc[k] = 0.f;
+#pragma unroll
                 for (int m = 0; m < 32; m += 4) {
                     const float x0 = XS[(m + 0) * 32 + cl], x1 = XS[(m + 1) * 32 + cl];
                     const float x2 = XS[(m + 2) * 32 + cl], x3 = XS[(m + 3) * 32 + cl];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float4 t4 = *reinterpret_cast<const float4 *>(&TF[(32 + r0 + 4 * k) * kAS + 32 + m]);
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(&AF[(32 + r0 + 8 * k) * kAS + 32 + m]);
                         acc[k] += t4.x * x0 + t4.y * x1 + t4.z * x2 + t4.w * x3;
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) TF[(32 + r0 + 4 * k) * kAS + cl] = -acc[k];
-                named_bar(1, 128);
+                for (int k = 0; k < 4; ++k) AF[(32 + r0 + 8 * k) * kAS + cl] = -acc[k];
+                named_bar(1, 256);
             }
-            // 4. Tw = T diag(beta e^g n), Tu = T diag(beta) as bf16 K-major tiles
+            if (wt == 0) GDN_TR(c, 18);
+            // 5. Tw = T diag(beta e^g n), Tu = T diag(beta) as bf16 K-major tiles
             {
-                const int t = wt & 63;
-                const bool isw = wt < 64;
-                float row[64];
+                const int tr = wt & 63, which = (wt >> 6) & 1, hf = wt >> 7;
+                const float *sc = which ? ms->beta : ms->wsc;
+                uint32_t pk[16];
 #pragma unroll
-                for (int sidx = 0; sidx < 64; sidx += 4) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(&TF[t * kAS + sidx]);
-                    row[sidx] = t4.x; row[sidx + 1] = t4.y; row[sidx + 2] = t4.z; row[sidx + 3] = t4.w;
+                for (int j = 0; j < 8; ++j) {
+                    const int s0 = 32 * hf + 4 * j;
+                    const float4 t4 = *reinterpret_cast<const float4 *>(&AF[tr * kAS + s0]);
+                    const float4 f4 = *reinterpret_cast<const float4 *>(&sc[s0]);
+                    pk[2 * j] = pack_bf16(t4.x * f4.x, t4.y * f4.y);
+                    pk[2 * j + 1] = pack_bf16(t4.z * f4.z, t4.w * f4.w);
                 }
+                uint8_t *tile = twu + which * 8192;
 #pragma unroll
-                for (int sidx = 0; sidx < 64; ++sidx) row[sidx] *= isw ? ms->wsc[sidx] : ms->beta[sidx];
-                store_row_sw128(sm + OFF_AF + (isw ? 0 : 8192), t, row);
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(tile + sw128_offset(tr, 32 * hf + 8 * j)) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
             }
             fence_proxy_async_smem();
-            named_bar(1, 128);
+            named_bar(1, 256);
             if (wt == 0) mbar_arrive(&bars[B_WY_READY]);
-            // 5. W^T -> bf16 MN-major operand (thread = key dim d)
+            if (wt == 0) GDN_TR(c, 19);
+            // 6. W^T -> bf16 MN-major operand (row = key index d)
             bool ww = wait_bar(&bars[B_WU_DONE], c & 1, tmo, abort_flag, 8u);
             if (ww && c >= 1) ww = wait_bar(&bars[B_VN_DONE], (c - 1) & 1, tmo, abort_flag, 8u);
-            if (!group_all(ww, 1, 128)) break;
+            if (!group_all(ww, 1, 256)) break;
+            if (wt == 0) GDN_TR(c, 20);
             tc_fence_after_sync();
-            ld64(tmem + lb + TM_W, x);
-            store_row_sw128(sm + OFF_WT, wt, x);
+            {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tmem + lb + TM_W + 32 * h, r0);
+                tmem_ld16(tmem + lb + TM_W + 32 * h + 16, r1);
+                tmem_wait_ld();
+                const int d = 32 * q + lane;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t *r = j ? r1 : r0;
+                    uint4 v0, v1;
+                    v0.x = pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1]));
+                    v0.y = pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3]));
+                    v0.z = pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5]));
+                    v0.w = pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7]));
+                    v1.x = pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9]));
+                    v1.y = pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11]));
+                    v1.z = pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13]));
+                    v1.w = pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15]));
+                    *reinterpret_cast<uint4 *>(sm + OFF_WT + sw128_offset(d, 32 * h + 16 * j)) = v0;
+                    *reinterpret_cast<uint4 *>(sm + OFF_WT + sw128_offset(d, 32 * h + 16 * j + 8)) = v1;
+                }
+            }
             tc_fence_before_sync();
             fence_proxy_async_smem();
-            named_bar(1, 128);
+            named_bar(1, 256);
             if (wt == 0) mbar_arrive(&bars[B_WT_READY]);
+            if (wt == 0) GDN_TR(c, 21);
         }
     }
 
@@ -762,6 +918,12 @@ int scan_tc_read_clear_error(cudaStream_t stream) {
     if (v && cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
     return v ? GDN_ERR_TIMEOUT : GDN_OK;
 }
+
+#ifdef GDN_TRACE
+extern "C" int gdn_trace_set(void *buf) {
+    return cudaMemcpyToSymbol(g_trace, &buf, sizeof(buf)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 int scan_tc_set_wait_limit(unsigned long long us) {
     g_timeout_ns = us == 0 ? 1000000000ull : us * 1000ull;
