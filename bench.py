@@ -100,7 +100,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -219,19 +219,31 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
-    n0 = binding.launch_count()
     ev_s = torch.cuda.Event(enable_timing=True)
     ev_e = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    # The sampler runs over a busy window of at least `clock_window` seconds:
+    # untimed steps before and after the timed ones keep the GPU on this
+    # workload so that nvidia-smi sees the clocks it runs at.
     with ClockSampler(local_rank) as clk:
+        t_win = time.perf_counter()
+        while time.perf_counter() - t_win < args.clock_window / 2:
+            step()
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        n0 = binding.launch_count()
         ev_s.record(stream)
         for _ in range(args.steps):
             step()
         ev_e.record(stream)
+        launches = binding.launch_count() - n0  # kernels the library launched in the timed steps
         torch.cuda.synchronize()
+        while time.perf_counter() - t_win < args.clock_window:
+            step()
+            torch.cuda.synchronize()
     barrier()
-    launches = binding.launch_count() - n0
     ms = ev_s.elapsed_time(ev_e) / args.steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -298,7 +310,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window_s=args.clock_window),
     }
     if args.secondary:
         line["secondary"] = secondary(args, dev)
@@ -379,6 +391,8 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=64,
                     help="heads of the workload the CPU oracle runs per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-window", type=float, default=0.6,
+                    help="seconds of GPU activity around the timed steps during which clocks are sampled")
     ap.add_argument("--secondary", action=argparse.BooleanOptionalAction, default=True)
     args = ap.parse_args()
     world = env_int("WORLD_SIZE", 1)

@@ -55,6 +55,38 @@ __device__ __forceinline__ F8 load8(const float *p) {
     return r;
 }
 
+// Eight consecutive raw elements as loaded (bf16: one 16-byte word; fp32: two),
+// kept packed in registers until they are used.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = __ldg(reinterpret_cast<const uint4 *>(p)); }
+    __device__ __forceinline__ F8 unpack() const {
+        F8 r;
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            r.x[2 * i] = __uint_as_float(w[i] << 16);
+            r.x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+        return r;
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float *p) {
+        a = __ldg(reinterpret_cast<const float4 *>(p));
+        b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    __device__ __forceinline__ F8 unpack() const {
+        F8 r = {{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}};
+        return r;
+    }
+};
+
 __device__ __forceinline__ void store8(__nv_bfloat16 *p, const F8 &v) {
     uint32_t w[4];
 #pragma unroll
@@ -72,7 +104,7 @@ __device__ __forceinline__ void store8(float *p, const F8 &v) {
 
 // NPL = 8-element groups per lane (C = H*D <= 256*NPL).
 template <typename T, int NPL>
-__global__ void __launch_bounds__(32 * kTokPerCta) cam_prep_kernel(CamParams p) {
+__global__ void __launch_bounds__(32 * kTokPerCta, 2) cam_prep_kernel(CamParams p) {
     __shared__ float s_cos[kTokPerCta][kMaxDh];
     __shared__ float s_sin[kTokPerCta][kMaxDh];
     __shared__ float s_pre[kTokPerCta][64];
@@ -119,24 +151,25 @@ __global__ void __launch_bounds__(32 * kTokPerCta) cam_prep_kernel(CamParams p) 
         const T *qr = static_cast<const T *>(p.q_raw) + (size_t)tok * C;
         const T *kr = static_cast<const T *>(p.k_raw) + (size_t)tok * C;
         const T *vr = static_cast<const T *>(p.v_raw) + (size_t)tok * C;
-        F8 xq[NPL], xk[NPL], xv[NPL];
+        Raw8<T> xq[NPL], xk[NPL], xv[NPL];
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             const int gi = lane + 32 * i;
             if (gi < G8) {
-                xq[i] = load8(qr + gi * 8);
-                xk[i] = load8(kr + gi * 8);
-                xv[i] = load8(vr + gi * 8);
+                xq[i].load(qr + gi * 8);
+                xk[i].load(kr + gi * 8);
+                xv[i].load(vr + gi * 8);
             }
         }
         float sq = 0.f, sk = 0.f;
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             if (lane + 32 * i < G8) {
+                const F8 a = xq[i].unpack(), b = xk[i].unpack();
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    sq += xq[i].x[e] * xq[i].x[e];
-                    sk += xk[i].x[e] * xk[i].x[e];
+                    sq += a.x[e] * a.x[e];
+                    sk += b.x[e] * b.x[e];
                 }
             }
         }
@@ -165,7 +198,7 @@ __global__ void __launch_bounds__(32 * kTokPerCta) cam_prep_kernel(CamParams p) 
             const bool ok = gi < G8;
             const int e0 = gi * 8;
             const int h = e0 / D, d0 = e0 % D;
-            F8 q = xq[i], k = xk[i], v = xv[i];
+            F8 q = xq[i].unpack(), k = xk[i].unpack(), v = xv[i].unpack();
             float pre = 0.f, post = 0.f;
             if (ok) {
                 F8 wq, wk;
