@@ -77,9 +77,10 @@ constexpr uint32_t S_K0 = 0, S_K1 = 16384;      // K tile [64][128] as 2 MN-atom
 constexpr uint32_t S_Q0 = 32768, S_Q1 = 49152;  // Q tile [NQ][128] as 2 K-blocks
 constexpr uint32_t S_V = 65536;                 // V tile [64][128] as 2 MN-atoms
 constexpr uint32_t S_RECV0 = 81920;             // receive slots (one per chunk parity)
-constexpr uint32_t RS = 33792;                  // slot: W^T | Tu | P | vectors
-constexpr uint32_t R_WT = 0, R_TU = 16384, R_P = 24576, R_VEC = 32768;
-constexpr uint32_t S_ST = S_RECV0 + 2 * RS;     // S^T bf16 [128 dv][128 dk] K-major
+constexpr uint32_t RS = 25600;                  // slot: Tw | Tu | P | vectors
+constexpr uint32_t R_TW = 0, R_TU = 8192, R_P = 16384, R_VEC = 24576;
+constexpr uint32_t S_WT = S_RECV0 + 2 * RS;     // W^T bf16 [128 d][64 t] MN-major
+constexpr uint32_t S_ST = S_WT + 16384;         // S^T bf16 [128 dv][128 dk] K-major
 constexpr uint32_t S_VN = S_ST + 32768;         // Vn^T bf16 [128 dv][64 s]
 constexpr uint32_t S_VS = S_VN + 16384;         // decayed Vn^T; also the output staging tile
 constexpr uint32_t S_QS = S_VS + 16384;         // per-query output scales, 2 x 64 floats
@@ -92,7 +93,6 @@ constexpr uint32_t GS = 99328;  // bytes per WY pipeline
 constexpr uint32_t G_KQ = 0;        // [K rows 0..63 | Q rows 64..] x 2 K-blocks
 constexpr uint32_t G_TWU = 32768;   // Tw (+0), Tu (+8192): bf16 [64 t][64 s] K-major
 constexpr uint32_t G_P = 49152;     // P bf16 [NQ][64] K-major
-constexpr uint32_t G_WT = 57344;    // W^T bf16 [128 d][64 t] MN-major
 constexpr uint32_t G_AF = 73728;    // A fp32 [64][68], inverted in place
 constexpr uint32_t G_X = 91136;     // inverse scratch 32x32 fp32
 constexpr uint32_t G_VEC = 95232;   // shipped vectors
@@ -108,14 +108,14 @@ constexpr uint32_t kSmemBytes = (S_END > W_END ? S_END : W_END) + 1024;
 constexpr uint32_t V_SEF = 0, V_QS = 64, V_EL = 128;
 
 // scan TMEM columns
-constexpr uint32_t TM_S = 0, TM_VN0 = 128, TM_VN1 = 192, TM_O10 = 256, TM_O11 = 320, TM_O20 = 384,
-                   TM_O21 = 448;
+constexpr uint32_t TM_S = 0, TM_VN = 128, TM_W = 192, TM_O10 = 256, TM_O11 = 320, TM_O20 = 384, TM_O21 = 448;
 
 enum ScanBar {
     SB_FULLKQ0, SB_FULLKQ1, SB_VFULL, SB_VFREE, SB_S_READY, SB_VN_DONE, SB_VN_READY, SB_UPD_DONE,
-    SB_STG_FREE0, SB_STG_FREE1, SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_DRAIN, SB_NUM
+    SB_STG_FREE0, SB_STG_FREE1, SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_W_DONE, SB_WT_READY,
+    SB_DRAIN, SB_WDRAIN, SB_NUM
 };
-enum WyBar { WB_FULL, WB_KQ_DONE, WB_WY_READY, WB_W_DONE, WB_RECV_FREE, WB_DRAIN, WB_PER_GROUP };
+enum WyBar { WB_FULL, WB_KQ_DONE, WB_KQ_FREE, WB_RECV_FREE, WB_DRAIN, WB_PER_GROUP };
 
 // Per-chunk vectors of one WY pipeline.
 struct Misc {
@@ -223,7 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         if (is_scan) {
             for (int i = 0; i < SB_NUM; ++i)
-                mbar_init(&bars[i], (i == SB_S_READY || i == SB_VN_READY) ? 256u : 1u);
+                mbar_init(&bars[i], (i == SB_S_READY || i == SB_VN_READY) ? 256u : (i == SB_WT_READY ? 128u : 1u));
         } else {
             for (int i = 0; i < 2 * WB_PER_GROUP; ++i) mbar_init(&bars[i], 1u);
         }
@@ -285,7 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t recv = sbase + S_RECV0 + b * RS;
                     const uint32_t kt = sbase + (b ? S_K1 : S_K0);
                     const uint32_t qt = sbase + (b ? S_Q1 : S_Q0);
-                    const uint32_t tvn = tmem + (b ? TM_VN1 : TM_VN0);
+                    const uint32_t tvn = tmem + TM_VN;
                     // U^T = V^T Tu^T
                     if (!wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 2u, true)) break;
                     if (!wait_bar(&bars[SB_VFULL], c & 1, tmo, abort_flag, 2u)) break;
@@ -297,13 +297,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     smem_desc(recv + R_TU + ks * 32, 16, 1024), idU, ks > 0);
                     mma_commit(&bars[SB_VFREE]);
                     // Vn^T = U^T - S^T W^T
+                    if (!wait_bar(&bars[SB_WT_READY], c & 1, tmo, abort_flag, 2u)) break;
                     if (!wait_bar(&bars[SB_S_READY], c & 1, tmo, abort_flag, 2u)) break;
                     GDN_TR(c, 1);
                     tc_fence_after_sync();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16_ss(tvn, smem_desc(sbase + S_ST + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    smem_desc(recv + R_WT + ks * 2048, 8192, 1024), idVN, 1u);
+                                    smem_desc(sbase + S_WT + ks * 2048, 8192, 1024), idVN, 1u);
                     mma_commit(&bars[SB_VN_DONE]);
                     // O1^T = S^T Q^T
                     if (!wait_bar(&bars[SB_FULLKQ0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
@@ -341,6 +342,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!wait_bar(&bars[SB_SLOT_DONE0 + b], (c >> 1) & 1, tmo, abort_flag, 16u)) break;
                     mbar_arrive_remote(map_to_rank(sbase + W_BAR + 8 * (WB_PER_GROUP * b + WB_RECV_FREE), 1));
                 }
+            }
+        } else if (warp == 3) {
+            // ------------------------------------------------------ W^T issuer
+            // W^T = K^T Tw^T for each chunk as soon as its K and Tw are here, off
+            // the state chain
+            if (lane == 0) {
+                const uint32_t idW = idesc_bf16(128, 64, true, false);
+                for (int c = 0; c < NT; ++c) {
+                    const int b = c & 1;
+                    if (!wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 2u, true)) break;
+                    if (!wait_bar(&bars[SB_FULLKQ0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
+                    if (c >= 1 && !wait_bar(&bars[SB_WT_READY], (c - 1) & 1, tmo, abort_flag, 2u)) break;
+                    tc_fence_after_sync();
+                    const uint32_t kt = sbase + (b ? S_K1 : S_K0);
+                    const uint32_t recv = sbase + S_RECV0 + b * RS;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ss(tmem + TM_W, smem_desc(kt + ks * 2048, 8192, 1024),
+                                    smem_desc(recv + R_TW + ks * 32, 16, 1024), idW, ks > 0);
+                    mma_commit(&bars[SB_W_DONE]);
+                }
+                mma_commit(&bars[SB_WDRAIN]);
+                mbar_wait(&bars[SB_WDRAIN], 0, kCleanupNs);
+            }
+        } else if (warp >= 12 && warp < 16) {
+            // ------------------------------------------------------ W^T -> bf16 operand
+            const int d = 32 * (warp & 3) + lane;  // key index = TMEM lane
+            const uint32_t lb = tmem_lane_base(warp);
+            for (int c = 0; c < NT; ++c) {
+                bool w = wait_bar(&bars[SB_W_DONE], c & 1, tmo, abort_flag, 128u);
+                if (w && c >= 1) w = wait_bar(&bars[SB_VN_DONE], (c - 1) & 1, tmo, abort_flag, 128u);
+                if (!group_all(w, 4, 128)) break;
+                tc_fence_after_sync();
+                uint32_t r[4][16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld16(tmem + lb + TM_W + 16 * j, r[j]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) store16_sw128(sm + S_WT, d, 16 * j, r[j]);
+                tc_fence_before_sync();
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[SB_WT_READY]);
             }
         } else if (warp >= 4 && warp < 12) {
             // ------------------------------------------------------ scan epilogue
@@ -445,7 +488,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (si == 0) GDN_TR(c, 5);
                 tc_fence_after_sync();
                 {
-                    const uint32_t tv = tmem + lb + (b ? TM_VN1 : TM_VN0) + 32 * hh;
+                    const uint32_t tv = tmem + lb + TM_VN + 32 * hh;
                     uint32_t r0[16], r1[16];
                     tmem_ld16(tv, r0);
                     tmem_ld16(tv + 16, r1);
@@ -489,18 +532,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ================================================================== WY CTA
         if (warp < 2) {
             // ---------------------------------- control thread of pipeline g:
-            // TMA of K/Q, the K K^T / Q K^T MMA and the W^T MMA for its chunks
+            // TMA of K/Q and the K K^T / Q K^T MMA for its chunks; the next
+            // chunk's load starts as soon as the pipeline has read this one
             const int g = warp;
             if (lane == 0) {
                 uint64_t *gb = bars + WB_PER_GROUP * g;
                 uint8_t *kq = sm + g * GS + G_KQ;
                 const uint32_t kqa = sbase + g * GS + G_KQ;
-                const uint32_t tkq = tmem + 128 * g, tw = tmem + 128 * g + 64;
+                const uint32_t tkq = tmem + 128 * g;
                 const uint32_t idKQ = idesc_bf16(128, 64, false, false);
-                const uint32_t idW = idesc_bf16(128, 64, true, false);
                 int armed = 0;
                 for (int k = 0, c = g; c < NT; ++k, c += 2) {
-                    if (k >= 1 && !wait_bar(&gb[WB_W_DONE], (k - 1) & 1, tmo, abort_flag, 32u)) break;
+                    if (k >= 1 && !wait_bar(&gb[WB_KQ_FREE], (k - 1) & 1, tmo, abort_flag, 32u)) break;
                     mbar_arrive_expect_tx(&gb[WB_FULL], 16384 + 2 * NQ * 128);
                     tma_load_3d(kq, &mK, &gb[WB_FULL], 0, c * 64, bh);
                     tma_load_3d(kq + 16384, &mK, &gb[WB_FULL], 64, c * 64, bh);
@@ -515,13 +558,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mma_bf16_ss(tkq, smem_desc(a, 16, 1024), smem_desc(a, 16, 1024), idKQ, ks > 0);
                     }
                     mma_commit(&gb[WB_KQ_DONE]);
-                    if (!wait_bar(&gb[WB_WY_READY], k & 1, tmo, abort_flag, 32u)) break;
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ss(tw, smem_desc(kqa + ks * 2048, 16384, 1024),
-                                    smem_desc(sbase + g * GS + G_TWU + ks * 32, 16, 1024), idW, ks > 0);
-                    mma_commit(&gb[WB_W_DONE]);
                 }
                 mma_commit(&gb[WB_DRAIN]);
                 mbar_wait(&gb[WB_DRAIN], 0, kCleanupNs);
@@ -545,7 +581,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float *vec = reinterpret_cast<float *>(gbase + G_VEC);
             Misc *ms = reinterpret_cast<Misc *>(gbase + G_MISC);
             const uint32_t lb = tmem_lane_base(warp);
-            const uint32_t tkq = tmem + 128 * g, tw = tmem + 128 * g + 64;
+            const uint32_t tkq = tmem + 128 * g;
             const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
             const __nv_bfloat16 *betap = p.beta + (size_t)bh * p.rows;
             const float *gp = p.g + (size_t)bh * p.T;
@@ -633,7 +669,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     ms->qp[h][t] = ss;
                 }
-                named_bar(bar_id, 256);  // n and partial q norms visible
+                tc_fence_before_sync();
+                named_bar(bar_id, 256);  // n and partial q norms visible; K/Q tile and TMEM rows read
+                if (wt == 0) mbar_arrive(&gb[WB_KQ_FREE]);
                 // per-row / per-column factors of the chunk
                 if (wt < 64) {
                     const float g0 = ms->gam[0], gi = ms->gam[wt], gl = ms->gam[63];
@@ -764,35 +802,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     named_bar(bar_id, 256);
                 }
                 {
-                    const int cl = wt & 31, r0 = wt >> 5;  // rows r0 + 8k, k < 4
+                    // X = A_bl T_top (rows 32..63, cols 0..31 of A; T_top lower triangular):
+                    // warp wi owns columns 4wi..4wi+3, so its sum starts at m = 4wi
+                    const int cl = 4 * wi + (lane >> 3), rr = lane & 7;  // rows rr + 8k, k < 4
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int m = 0; m < 32; m += 4) {
+#pragma unroll 1
+                    for (int m = 4 * wi; m < 32; m += 4) {
                         const float t0 = AF[(m + 0) * kAS + cl], t1 = AF[(m + 1) * kAS + cl];
                         const float t2 = AF[(m + 2) * kAS + cl], t3 = AF[(m + 3) * kAS + cl];
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const float4 a4 = *reinterpret_cast<const float4 *>(&AF[(32 + r0 + 8 * kk) * kAS + m]);
+                            const float4 a4 = *reinterpret_cast<const float4 *>(&AF[(32 + rr + 8 * kk) * kAS + m]);
                             acc[kk] += a4.x * t0 + a4.y * t1 + a4.z * t2 + a4.w * t3;
                         }
                     }
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) XS[(r0 + 8 * kk) * 32 + cl] = acc[kk];
+                    for (int kk = 0; kk < 4; ++kk) XS[(rr + 8 * kk) * 32 + cl] = acc[kk];
                     named_bar(bar_id, 256);
+                    // T_bl = -T_bot X (T_bot lower triangular): row r needs m <= r only
+                    const int cl2 = wt & 31, r0 = wi;  // rows r0 + 8k, k < 4 (warp-uniform)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) acc[kk] = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 32; m += 4) {
-                        const float x0 = XS[(m + 0) * 32 + cl], x1 = XS[(m + 1) * 32 + cl];
-                        const float x2 = XS[(m + 2) * 32 + cl], x3 = XS[(m + 3) * 32 + cl];
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const float4 t4 = *reinterpret_cast<const float4 *>(&AF[(32 + r0 + 8 * kk) * kAS + 32 + m]);
-                            acc[kk] += t4.x * x0 + t4.y * x1 + t4.z * x2 + t4.w * x3;
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int r = r0 + 8 * kk;
+                        float a = 0.f;
+#pragma unroll 1
+                        for (int m = 0; m <= r; m += 4) {
+                            const float4 t4 = *reinterpret_cast<const float4 *>(&AF[(32 + r) * kAS + 32 + m]);
+                            a += t4.x * XS[(m + 0) * 32 + cl2] + t4.y * XS[(m + 1) * 32 + cl2] +
+                                 t4.z * XS[(m + 2) * 32 + cl2] + t4.w * XS[(m + 3) * 32 + cl2];
                         }
+                        acc[kk] = a;
                     }
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) AF[(32 + r0 + 8 * kk) * kAS + cl] = -acc[kk];
+                    for (int kk = 0; kk < 4; ++kk) AF[(32 + r0 + 8 * kk) * kAS + cl2] = -acc[kk];
                     named_bar(bar_id, 256);
                 }
                 if (wt == 0) GDN_TR(c, 11 + 8 * g);
@@ -817,32 +859,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 named_bar(bar_id, 256);
-                if (wt == 0) mbar_arrive(&gb[WB_WY_READY]);
                 if (wt == 0) GDN_TR(c, 12 + 8 * g);
-                // 6. W^T -> bf16 MN-major operand (row = key index d)
-                const bool ww = wait_bar(&gb[WB_W_DONE], k & 1, tmo, abort_flag, 8u);
-                if (!group_all(ww, bar_id, 256)) break;
-                tc_fence_after_sync();
-                {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(tw + lb + 32 * h, r0);
-                    tmem_ld16(tw + lb + 32 * h + 16, r1);
-                    tmem_wait_ld();
-                    const int d = 32 * q + lane;
-                    store16_sw128(gbase + G_WT, d, 32 * h, r0);
-                    store16_sw128(gbase + G_WT, d, 32 * h + 16, r1);
-                }
-                tc_fence_before_sync();
-                fence_proxy_async_smem();
-                named_bar(bar_id, 256);
-                if (wt == 0) GDN_TR(c, 13 + 8 * g);
-                // 7. ship W^T, Tu, P and the vectors into the scan CTA's slot
+                // 6. ship Tw, Tu, P and the vectors into the scan CTA's slot
                 if (wt == 0) {
                     if (k >= 1) ship_ok = wait_bar(&gb[WB_RECV_FREE], (k - 1) & 1, tmo, abort_flag, 64u, true);
                     if (ship_ok) {
-                        mbar_arrive_expect_tx_remote(map_to_rank(recv_bar, 0), 16384 + 8192 + NQ * 128 + 1024);
+                        mbar_arrive_expect_tx_remote(map_to_rank(recv_bar, 0), 16384 + NQ * 128 + 1024);
                         const uint32_t rb = map_to_rank(recv_bar, 0);
-                        bulk_copy_to_peer(map_to_rank(recv + R_WT, 0), gbase + G_WT, 16384, rb);
+                        bulk_copy_to_peer(map_to_rank(recv + R_TW, 0), twu, 8192, rb);
                         bulk_copy_to_peer(map_to_rank(recv + R_TU, 0), twu + 8192, 8192, rb);
                         bulk_copy_to_peer(map_to_rank(recv + R_P, 0), ptile, NQ * 128, rb);
                         bulk_copy_to_peer(map_to_rank(recv + R_VEC, 0), vec, 1024, rb);
