@@ -22,14 +22,15 @@
 //   CTA rank 1 ("WY")   computes the chunk-local products, which need no state:
 //                       two independent 8-warp pipelines take alternate
 //                       chunks (K K^T / Q K^T by MMA, A, the blocked inverse,
-//                       Tw/Tu, P, W^T by MMA) and ship W^T, Tu, P and the
-//                       per-row factors into CTA 0's shared memory with
-//                       cp.async.bulk over the cluster (DSMEM).
-//   CTA rank 0 ("scan") runs only the sequential part: the fp32 state S^T
-//                       lives in tensor memory for the whole sequence; a TMA
-//                       warp streams K, Q, V; one thread issues the MMAs; 8
-//                       epilogue warps turn S^T and Vn^T into bf16 operands and
-//                       store the output tile with TMA.
+//                       Tw/Tu, P) and ship Tw, Tu, P and the per-row factors
+//                       into CTA 0's shared memory with cp.async.bulk over
+//                       the cluster (DSMEM).
+//   CTA rank 0 ("scan") runs the sequential part: the fp32 state S^T lives in
+//                       tensor memory for the whole sequence; a TMA warp
+//                       streams K, Q, V; one thread issues the chain's MMAs
+//                       and another W^T = K^T Tw^T; 8 epilogue warps turn S^T
+//                       and Vn^T into bf16 operands; 4 aux warps convert W^T
+//                       and write the output rows of the previous chunk.
 //
 // Only q, k, v, beta, g are read from HBM and o written.  Every mbarrier wait
 // is bounded in wall time; on expiry the CTA sets an error word, stops
@@ -58,7 +59,7 @@ __device__ unsigned long long *g_trace = nullptr;
 #define GDN_TR(c, ev)                                                          \
     do {                                                                       \
         if (blockIdx.x < 2 && g_trace != nullptr && (c) < 1024)                \
-            g_trace[(size_t)(c) * 32 + (ev)] = clock64();                      \
+            g_trace[(size_t)(c) * 64 + (ev)] = clock64();                      \
     } while (0)
 #else
 #define GDN_TR(c, ev) \
@@ -69,7 +70,7 @@ __device__ unsigned long long *g_trace = nullptr;
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 576;  // 18 warps
+constexpr int kThreads = 512;  // 16 warps: 4 per SM sub-partition, up to 128 registers a thread
 constexpr int kAS = 68;        // fp32 row stride of the A / T tiles
 
 // ---------------------------------------------------------------- scan CTA map
@@ -82,8 +83,8 @@ constexpr uint32_t R_TW = 0, R_TU = 8192, R_P = 16384, R_VEC = 24576;
 constexpr uint32_t S_WT = S_RECV0 + 2 * RS;     // W^T bf16 [128 d][64 t] MN-major
 constexpr uint32_t S_ST = S_WT + 16384;         // S^T bf16 [128 dv][128 dk] K-major
 constexpr uint32_t S_VN = S_ST + 32768;         // Vn^T bf16 [128 dv][64 s]
-constexpr uint32_t S_VS = S_VN + 16384;         // decayed Vn^T; also the output staging tile
-constexpr uint32_t S_QS = S_VS + 16384;         // per-query output scales, 2 x 64 floats
+constexpr uint32_t S_VS = S_VN + 16384;         // decayed Vn^T
+constexpr uint32_t S_QS = S_VS + 16384;         // per-query output scales, 2 x 64 floats (aux warps)
 constexpr uint32_t S_BAR = S_QS + 512;
 constexpr uint32_t S_FLAGS = S_BAR + 256;
 constexpr uint32_t S_END = S_FLAGS + 64;
@@ -92,10 +93,11 @@ constexpr uint32_t S_END = S_FLAGS + 64;
 constexpr uint32_t GS = 99328;  // bytes per WY pipeline
 constexpr uint32_t G_KQ = 0;        // [K rows 0..63 | Q rows 64..] x 2 K-blocks
 constexpr uint32_t G_TWU = 32768;   // Tw (+0), Tu (+8192): bf16 [64 t][64 s] K-major
-constexpr uint32_t G_P = 49152;     // P bf16 [NQ][64] K-major
+constexpr uint32_t G_P = 49152;     // P bf16 [NQ][64] K-major, two buffers (+8192)
+constexpr uint32_t G_VEC1 = 65536;  // second buffer of the shipped vectors
 constexpr uint32_t G_AF = 73728;    // A fp32 [64][68], inverted in place
 constexpr uint32_t G_X = 91136;     // inverse scratch 32x32 fp32
-constexpr uint32_t G_VEC = 95232;   // shipped vectors
+constexpr uint32_t G_VEC = 95232;   // shipped vectors (first buffer)
 constexpr uint32_t G_MISC = 96256;  // Misc
 constexpr uint32_t W_BAR = 2 * GS;
 constexpr uint32_t W_FLAGS = W_BAR + 256;
@@ -113,9 +115,9 @@ constexpr uint32_t TM_S = 0, TM_VN = 128, TM_W = 192, TM_O10 = 256, TM_O11 = 320
 enum ScanBar {
     SB_FULLKQ0, SB_FULLKQ1, SB_VFULL, SB_VFREE, SB_S_READY, SB_VN_DONE, SB_VN_READY, SB_UPD_DONE,
     SB_STG_FREE0, SB_STG_FREE1, SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_W_DONE, SB_WT_READY,
-    SB_DRAIN, SB_WDRAIN, SB_NUM
+    SB_DRAIN, SB_WDRAIN, SB_OFREE0, SB_OFREE1, SB_NUM
 };
-enum WyBar { WB_FULL, WB_KQ_DONE, WB_KQ_FREE, WB_RECV_FREE, WB_DRAIN, WB_PER_GROUP };
+enum WyBar { WB_FULL, WB_KQ_DONE, WB_RECV_FREE, WB_DRAIN, WB_PER_GROUP };
 
 // Per-chunk vectors of one WY pipeline.
 struct Misc {
@@ -137,6 +139,7 @@ struct TcParams {
     const float *g;
     const float *s0;
     float *sf;
+    __nv_bfloat16 *o;
     int T, rows, NT;
     float scale;
     unsigned flags;
@@ -205,7 +208,7 @@ __device__ __forceinline__ void store16_sw128(uint8_t *tile, int row, int col, c
 template <int R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gdn_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
-                  const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO, TcParams p) {
+                  const __grid_constant__ CUtensorMap mV, TcParams p) {
     constexpr int NQ = 64 / R;  // query rows (tokens) per chunk
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
@@ -223,7 +226,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         if (is_scan) {
             for (int i = 0; i < SB_NUM; ++i)
-                mbar_init(&bars[i], (i == SB_S_READY || i == SB_VN_READY) ? 256u : (i == SB_WT_READY ? 128u : 1u));
+                mbar_init(&bars[i], (i == SB_S_READY || i == SB_VN_READY)
+                                        ? 256u
+                                        : ((i == SB_WT_READY || i == SB_OFREE0 || i == SB_OFREE1) ? 128u : 1u));
         } else {
             for (int i = 0; i < 2 * WB_PER_GROUP; ++i) mbar_init(&bars[i], 1u);
         }
@@ -238,7 +243,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&mK);
         prefetch_tensormap(&mQ);
         prefetch_tensormap(&mV);
-        prefetch_tensormap(&mO);
     }
     tc_fence_before_sync();
     cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
@@ -306,8 +310,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mma_bf16_ss(tvn, smem_desc(sbase + S_ST + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                     smem_desc(sbase + S_WT + ks * 2048, 8192, 1024), idVN, 1u);
                     mma_commit(&bars[SB_VN_DONE]);
-                    // O1^T = S^T Q^T
+                    // O1^T = S^T Q^T (its TMEM columns free once chunk c-2's output is read)
                     if (!wait_bar(&bars[SB_FULLKQ0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
+                    if (c >= 2 && !wait_bar(&bars[SB_OFREE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 2u)) break;
                     tc_fence_after_sync();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
@@ -322,11 +327,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ss(tmem + TM_S, smem_desc(sbase + S_VS + ks * 32, 16, 1024),
                                     smem_desc(kt + ks * 2048, 8192, 1024), idUP, 1u);
+                    // the state is ready before O2 runs (S_VN, which O2 reads, is only
+                    // rewritten after the next VN_DONE, which completes after O2)
+                    mma_commit(&bars[SB_UPD_DONE]);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ss(tmem + (b ? TM_O21 : TM_O20), smem_desc(sbase + S_VN + ks * 32, 16, 1024),
                                     smem_desc(recv + R_P + ks * 32, 16, 1024), idO, ks > 0);
-                    mma_commit(&bars[SB_UPD_DONE]);
                     mma_commit(&bars[SB_STG_FREE0 + b]);
                     mma_commit(&bars[SB_SLOT_DONE0 + b]);
                 }
@@ -355,6 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!wait_bar(&bars[SB_FULLKQ0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
                     if (c >= 1 && !wait_bar(&bars[SB_WT_READY], (c - 1) & 1, tmo, abort_flag, 2u)) break;
                     tc_fence_after_sync();
+                    GDN_TR(c, 10);
                     const uint32_t kt = sbase + (b ? S_K1 : S_K0);
                     const uint32_t recv = sbase + S_RECV0 + b * RS;
 #pragma unroll
@@ -367,14 +375,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars[SB_WDRAIN], 0, kCleanupNs);
             }
         } else if (warp >= 12 && warp < 16) {
-            // ------------------------------------------------------ W^T -> bf16 operand
-            const int d = 32 * (warp & 3) + lane;  // key index = TMEM lane
+            // ------------------------------------------------------ aux warps
+            // W^T -> bf16 operand for each chunk, and the output rows of the
+            // previous chunk, o_t = scale (qs_t O1_t + O2_t): each thread holds one
+            // value index for all NQ queries, so a warp writes 64 contiguous bytes
+            // of a row per store
+            const int d = 32 * (warp & 3) + lane;  // TMEM lane: key index of W^T, value index of O^T
+            const int ai = (warp - 12) * 32 + lane;
             const uint32_t lb = tmem_lane_base(warp);
+            float *qsl = reinterpret_cast<float *>(sm + S_QS);
+            auto out_tile = [&](int cc) {
+                const int b = cc & 1;
+                const uint32_t t1 = tmem + lb + (b ? TM_O11 : TM_O10);
+                const uint32_t t2 = tmem + lb + (b ? TM_O21 : TM_O20);
+                const float *qs = qsl + 64 * b;
+                __nv_bfloat16 *orow = p.o + ((size_t)bh * p.T + (size_t)cc * NQ) * 128 + d;
+                const int nrow = min(NQ, p.T - cc * NQ);
+                static_assert(NQ >= 16, "at least one 16-column TMEM block per chunk");
+                constexpr int NB = NQ >= 32 ? 2 : 1;  // 16-column blocks per TMEM wait
+#pragma unroll
+                for (int j0 = 0; j0 < NQ / 16; j0 += NB) {
+                    uint32_t a[NB][16], e[NB][16];
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        tmem_ld16(t1 + 16 * (j0 + j), a[j]);
+                        tmem_ld16(t2 + 16 * (j0 + j), e[j]);
+                    }
+                    tmem_wait_ld();
+                    if (j0 + NB == NQ / 16) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&bars[SB_OFREE0 + b]);  // O1/O2 columns of parity b may be overwritten
+                    }
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int t = 16 * (j0 + j) + i;
+                            const float o = p.scale * (qs[t] * __uint_as_float(a[j][i]) + __uint_as_float(e[j][i]));
+                            if (t < nrow) orow[(size_t)t * 128] = __float2bfloat16_rn(o);
+                        }
+                    }
+                }
+            };
+            bool ok = true;
             for (int c = 0; c < NT; ++c) {
-                bool w = wait_bar(&bars[SB_W_DONE], c & 1, tmo, abort_flag, 128u);
+                const int b = c & 1;
+                bool w = wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 128u, true);
+                if (w) w = wait_bar(&bars[SB_W_DONE], c & 1, tmo, abort_flag, 128u);
                 if (w && c >= 1) w = wait_bar(&bars[SB_VN_DONE], (c - 1) & 1, tmo, abort_flag, 128u);
-                if (!group_all(w, 4, 128)) break;
+                if (!group_all(w, 4, 128)) { ok = false; break; }
                 tc_fence_after_sync();
+                // this chunk's per-query output scales, kept past the slot's release
+                if (ai < NQ) qsl[64 * b + ai] = reinterpret_cast<const float *>(sm + S_RECV0 + b * RS + R_VEC)[V_QS + ai];
                 uint32_t r[4][16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) tmem_ld16(tmem + lb + TM_W + 16 * j, r[j]);
@@ -384,6 +436,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[SB_WT_READY]);
+                if (ai == 0) GDN_TR(c, 7);
+                if (c >= 1) {
+                    // chunk c-1's MMAs (O1, O2) are complete with its slot's release
+                    const bool wo = wait_bar(&bars[SB_SLOT_DONE0 + (b ^ 1)], ((c - 1) >> 1) & 1, tmo, abort_flag, 128u);
+                    if (!group_all(wo, 4, 128)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    if (ai == 0) GDN_TR(c, 8);
+                    out_tile(c - 1);
+                    if (ai == 0) GDN_TR(c, 9);
+                }
+            }
+            if (ok && NT > 0) {
+                const bool wo = wait_bar(&bars[SB_SLOT_DONE0 + ((NT - 1) & 1)], ((NT - 1) >> 1) & 1, tmo, abort_flag, 128u);
+                if (group_all(wo, 4, 128)) {
+                    tc_fence_after_sync();
+                    out_tile(NT - 1);
+                }
             }
         } else if (warp >= 4 && warp < 12) {
             // ------------------------------------------------------ scan epilogue
@@ -391,8 +460,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int dv = 32 * sq + lane;          // TMEM lane = value index
             const int si = (warp - 4) * 32 + lane;  // 0..255
             const uint32_t lb = tmem_lane_base(warp);
-            uint8_t *ostage = sm + S_VS;
-            float *qsl = reinterpret_cast<float *>(sm + S_QS);
             {  // initial state: S^T[dv][dk] = S0[dk][dv], this thread's 64 columns
                 const float *s0 = p.s0 ? p.s0 + (size_t)bh * 128 * 128 : nullptr;
 #pragma unroll 1
@@ -405,46 +472,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            auto out_epilogue = [&](int cc) {
-                const int b = cc & 1;
-                const uint32_t t1 = tmem + lb + (b ? TM_O11 : TM_O10);
-                const uint32_t t2 = tmem + lb + (b ? TM_O21 : TM_O20);
-                const float *qs = qsl + 64 * b;
-                constexpr int HALF = NQ / 2;
-                if constexpr (HALF >= 16) {
-#pragma unroll
-                    for (int j = 0; j < HALF / 16; ++j) {
-                        const int t0 = hh * HALF + 16 * j;
-                        uint32_t a[16], c2[16];
-                        tmem_ld16(t1 + t0, a);
-                        tmem_ld16(t2 + t0, c2);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float o = p.scale * (qs[t0 + i] * __uint_as_float(a[i]) + __uint_as_float(c2[i]));
-                            *reinterpret_cast<__nv_bfloat16 *>(ostage + (t0 + i) * 256 + dv * 2) = __float2bfloat16_rn(o);
-                        }
-                    }
-                } else {
-                    const int t0 = hh * HALF;
-                    uint32_t a[8], c2[8];
-                    tmem_ld8(t1 + t0, a);
-                    tmem_ld8(t2 + t0, c2);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float o = p.scale * (qs[t0 + i] * __uint_as_float(a[i]) + __uint_as_float(c2[i]));
-                        *reinterpret_cast<__nv_bfloat16 *>(ostage + (t0 + i) * 256 + dv * 2) = __float2bfloat16_rn(o);
-                    }
-                }
-                tc_fence_before_sync();
-                fence_proxy_async_smem();
-                named_bar(3, 256);
-                if (si == 0) {
-                    tma_store_3d(&mO, ostage, 0, cc * NQ, bh);
-                    tma_store_commit();
-                }
-            };
             bool ok = true;
             for (int c = 0; c < NT; ++c) {
                 const int b = c & 1;
@@ -454,7 +481,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!group_all(w, 3, 256)) { ok = false; break; }
                 if (si == 0) GDN_TR(c, 3);
                 tc_fence_after_sync();
-                if (si < 64) qsl[64 * b + si] = vec[V_QS + si];
                 // state: S^T -> bf16 operand (K-block hh), then S^T <- exp(g_last) S^T
                 const float el = vec[V_EL];
 #pragma unroll
@@ -480,11 +506,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[SB_S_READY]);
                 if (si == 0) GDN_TR(c, 4);
-                if (c >= 1) out_epilogue(c - 1);
                 // Vn^T -> bf16 operand and its decayed copy (columns 32hh..32hh+31)
                 const bool wv = wait_bar(&bars[SB_VN_DONE], c & 1, tmo, abort_flag, 4u);
-                if (si == 0) tma_store_wait_read<0>();
-                if (!group_all(wv, 3, 256)) { ok = false; break; }  // staging tile free
+                if (!group_all(wv, 3, 256)) { ok = false; break; }
                 if (si == 0) GDN_TR(c, 5);
                 tc_fence_after_sync();
                 {
@@ -509,10 +533,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (si == 0) GDN_TR(c, 6);
             }
             bool fin = ok && NT > 0 && wait_bar(&bars[SB_UPD_DONE], (NT - 1) & 1, tmo, abort_flag, 4u);
-            if (si == 0) tma_store_wait_read<0>();
             if (group_all(fin, 3, 256)) {
                 tc_fence_after_sync();
-                out_epilogue(NT - 1);
                 if (p.sf) {
                     float *sf = p.sf + (size_t)bh * 128 * 128;
 #pragma unroll 1
@@ -526,47 +548,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (si == 0) tma_store_wait_all<0>();
         }
     } else {
         // ================================================================== WY CTA
-        if (warp < 2) {
-            // ---------------------------------- control thread of pipeline g:
-            // TMA of K/Q and the K K^T / Q K^T MMA for its chunks; the next
-            // chunk's load starts as soon as the pipeline has read this one
-            const int g = warp;
-            if (lane == 0) {
-                uint64_t *gb = bars + WB_PER_GROUP * g;
-                uint8_t *kq = sm + g * GS + G_KQ;
-                const uint32_t kqa = sbase + g * GS + G_KQ;
-                const uint32_t tkq = tmem + 128 * g;
-                const uint32_t idKQ = idesc_bf16(128, 64, false, false);
-                int armed = 0;
-                for (int k = 0, c = g; c < NT; ++k, c += 2) {
-                    if (k >= 1 && !wait_bar(&gb[WB_KQ_FREE], (k - 1) & 1, tmo, abort_flag, 32u)) break;
-                    mbar_arrive_expect_tx(&gb[WB_FULL], 16384 + 2 * NQ * 128);
-                    tma_load_3d(kq, &mK, &gb[WB_FULL], 0, c * 64, bh);
-                    tma_load_3d(kq + 16384, &mK, &gb[WB_FULL], 64, c * 64, bh);
-                    tma_load_3d(kq + 8192, &mQ, &gb[WB_FULL], 0, c * NQ, bh);
-                    tma_load_3d(kq + 16384 + 8192, &mQ, &gb[WB_FULL], 64, c * NQ, bh);
-                    armed++;
-                    if (!wait_bar(&gb[WB_FULL], k & 1, tmo, abort_flag, 32u)) break;
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t a = kqa + (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16_ss(tkq, smem_desc(a, 16, 1024), smem_desc(a, 16, 1024), idKQ, ks > 0);
-                    }
-                    mma_commit(&gb[WB_KQ_DONE]);
-                }
-                mma_commit(&gb[WB_DRAIN]);
-                mbar_wait(&gb[WB_DRAIN], 0, kCleanupNs);
-                if (armed) mbar_wait(&gb[WB_FULL], (armed - 1) & 1, kCleanupNs);
-            }
-        } else {
-            // ---------------------------------- WY pipeline g: warps 2..9 / 10..17
-            const int g = (warp - 2) >> 3;
-            const int wi = (warp - 2) & 7;
+        {
+            // ---------------------------------- WY pipeline g: warps 0..7 / 8..15.
+            // One thread of warp 6 also loads K/Q with TMA and issues the
+            // K K^T / Q K^T MMA: the next chunk's load starts as soon as this
+            // chunk's tile and TMEM rows have been read, its MMA once this
+            // chunk's Tw / Tu are built.
+            const int g = warp >> 3;
+            const int wi = warp & 7;
             const int wt = wi * 32 + lane;  // 0..255
             const int q = warp & 3;         // TMEM lane quarter
             const int h = wi >> 2;          // column half of the 64-wide tiles
@@ -575,11 +567,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint8_t *gbase = sm + g * GS;
             uint8_t *kq = gbase + G_KQ;
             uint8_t *twu = gbase + G_TWU;
-            uint8_t *ptile = gbase + G_P;
             float *AF = reinterpret_cast<float *>(gbase + G_AF);
             float *XS = reinterpret_cast<float *>(gbase + G_X);
-            float *vec = reinterpret_cast<float *>(gbase + G_VEC);
             Misc *ms = reinterpret_cast<Misc *>(gbase + G_MISC);
+            const uint32_t kqa = sbase + g * GS + G_KQ;
+            const uint32_t idKQ = idesc_bf16(128, 64, false, false);
+            const bool ctl = wt == 192;  // warp 6: not one of the diagonal-block warps
+            int armed = 0, kq_issued = 0;  // thread 0: TMA loads and KQ MMAs issued
+            auto load_kq = [&](int cc) {
+                mbar_arrive_expect_tx(&gb[WB_FULL], 16384 + 2 * NQ * 128);
+                tma_load_3d(kq, &mK, &gb[WB_FULL], 0, cc * 64, bh);
+                tma_load_3d(kq + 16384, &mK, &gb[WB_FULL], 64, cc * 64, bh);
+                tma_load_3d(kq + 8192, &mQ, &gb[WB_FULL], 0, cc * NQ, bh);
+                tma_load_3d(kq + 16384 + 8192, &mQ, &gb[WB_FULL], 64, cc * NQ, bh);
+                armed++;
+            };
+            auto mma_kq = [&]() -> bool {
+                if (!wait_bar(&gb[WB_FULL], kq_issued & 1, tmo, abort_flag, 32u)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t a = kqa + (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_bf16_ss(tmem + 128 * g, smem_desc(a, 16, 1024), smem_desc(a, 16, 1024), idKQ, ks > 0);
+                }
+                mma_commit(&gb[WB_KQ_DONE]);
+                kq_issued++;
+                return true;
+            };
+            bool kq_ok = true;  // thread 0 only
+            if (ctl && g < NT) {
+                load_kq(g);
+                kq_ok = mma_kq();
+            }
             const uint32_t lb = tmem_lane_base(warp);
             const uint32_t tkq = tmem + 128 * g;
             const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
@@ -601,14 +620,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float pf = g < NT ? prefetch(g) : 0.f;
             bool ship_ok = true;
             for (int k = 0, c = g; c < NT; ++k, c += 2) {
-                if (wt == 0) GDN_TR(c, 8 + 8 * g);
-                // the previous shipment has been read out of P, Tu, W^T and the vectors
-                if (wt == 0) tma_store_wait_read<0>();
+                if (wt == 0) GDN_TR(c, 32 + 16 * g);
+                // P and the vectors alternate between two buffers; the shipment of
+                // chunk c-2 that last read this pair was waited for in chunk c-1
+                uint8_t *ptile = gbase + G_P + (k & 1) * 8192;
+                float *vec = reinterpret_cast<float *>(gbase + ((k & 1) ? G_VEC1 : G_VEC));
                 // 1. beta and g of the chunk's rows; cumulative decay
                 if (wt < 64) ms->beta[wt] = pf;
                 else if (wt < 128) ms->gam[wt - 64] = pf;
                 if (c + 2 < NT) pf = prefetch(c + 2);
-                if (!group_all(ship_ok, bar_id, 256)) break;
+                if (!group_all(ship_ok && kq_ok, bar_id, 256)) break;
                 if (wt < 32) {
                     float a = ms->gam[lane], b2 = ms->gam[lane + 32];
 #pragma unroll
@@ -631,7 +652,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const bool wk = wait_bar(&gb[WB_KQ_DONE], k & 1, tmo, abort_flag, 8u);
                 if (!group_all(wk, bar_id, 256)) break;  // also publishes gam
-                if (wt == 0) GDN_TR(c, 9 + 8 * g);
+                if (wt == 0) GDN_TR(c, 33 + 16 * g);
                 tc_fence_after_sync();
                 // 2. this thread's 32 columns of its K K^T (q < 2) or Q K^T (q >= 2) row
                 float x[32];
@@ -671,7 +692,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before_sync();
                 named_bar(bar_id, 256);  // n and partial q norms visible; K/Q tile and TMEM rows read
-                if (wt == 0) mbar_arrive(&gb[WB_KQ_FREE]);
+                if (ctl && kq_ok && c + 2 < NT) load_kq(c + 2);
+                if (wt == 0) GDN_TR(c, 34 + 16 * g);
                 // per-row / per-column factors of the chunk
                 if (wt < 64) {
                     const float g0 = ms->gam[0], gi = ms->gam[wt], gl = ms->gam[63];
@@ -685,6 +707,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     vec[V_QS + wt] = wt < NQ ? __expf(ms->gam[wt * R + R - 1]) * mi : 0.f;
                 }
                 named_bar(bar_id, 256);
+                if (wt == 0) GDN_TR(c, 35 + 16 * g);
                 // 3. A rows (q < 2) and P rows (q >= 2)
                 const bool safe = ms->safe != 0;
                 if (q < 2) {
@@ -744,8 +767,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(ptile + sw128_offset(t, 32 * h + 8 * j)) =
                             make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
+                if (wt == 0) GDN_TR(c, 47 + 16 * g);
                 named_bar(bar_id, 256);  // A complete
-                if (wt == 0) GDN_TR(c, 10 + 8 * g);
+                if (wt == 0) GDN_TR(c, 36 + 16 * g);
                 // 4. T = (I + A)^-1 in place over A: 16x16 diagonal blocks by
                 //    substitution, then the merges T_ij = -T_ii A_ij T_jj (16 level)
                 //    and T_bl = -T_bot A_bl T_top (32 level).
@@ -763,6 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 named_bar(bar_id, 256);
+                if (wt == 0) GDN_TR(c, 37 + 16 * g);
                 if (wt < 64) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) AF[(16 * db + i) * kAS + 16 * db + dc] = xs[i];
@@ -780,6 +805,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int m = 0; m < 16; ++m) a += AF[(i0 + rr) * kAS + j0 + m] * AF[(j0 + m) * kAS + j0 + cl];
                         acc[kk] = a;
                     }
+                    if (lane == 0 && (wi == 0 || wi == 7)) GDN_TR(c, 43 + 16 * g + (wi == 7 ? 1 : 0));
                     XS[wt] = acc[0];
                     XS[wt + 256] = acc[1];
                     named_bar(bar_id, 256);
@@ -801,6 +827,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     named_bar(bar_id, 256);
                 }
+                if (wt == 0) GDN_TR(c, 38 + 16 * g);
                 {
                     // X = A_bl T_top (rows 32..63, cols 0..31 of A; T_top lower triangular):
                     // warp wi owns columns 4wi..4wi+3, so its sum starts at m = 4wi
@@ -816,9 +843,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             acc[kk] += a4.x * t0 + a4.y * t1 + a4.z * t2 + a4.w * t3;
                         }
                     }
+                    if (lane == 0 && (wi == 0 || wi == 7)) GDN_TR(c, 45 + 16 * g + (wi == 7 ? 1 : 0));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) XS[(rr + 8 * kk) * 32 + cl] = acc[kk];
                     named_bar(bar_id, 256);
+                    if (wt == 0) GDN_TR(c, 39 + 16 * g);
                     // T_bl = -T_bot X (T_bot lower triangular): row r needs m <= r only
                     const int cl2 = wt & 31, r0 = wi;  // rows r0 + 8k, k < 4 (warp-uniform)
 #pragma unroll
@@ -835,9 +864,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) AF[(32 + r0 + 8 * kk) * kAS + cl2] = -acc[kk];
+                    // the previous shipment has been read out of Tw / Tu
+                    if (wt == 0) tma_store_wait_read<0>();
                     named_bar(bar_id, 256);
                 }
-                if (wt == 0) GDN_TR(c, 11 + 8 * g);
+                if (wt == 0) GDN_TR(c, 40 + 16 * g);
                 // 5. Tw = T diag(beta e^g n), Tu = T diag(beta) as bf16 K-major tiles
                 {
                     const int tr = wt & 63, which = (wt >> 6) & 1, hf = wt >> 7;
@@ -859,7 +890,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 named_bar(bar_id, 256);
-                if (wt == 0) GDN_TR(c, 12 + 8 * g);
+                if (wt == 0) GDN_TR(c, 41 + 16 * g);
+                // K K^T / Q K^T of the next chunk (its load has had the whole chunk)
+                if (ctl && kq_ok && c + 2 < NT) kq_ok = mma_kq();
                 // 6. ship Tw, Tu, P and the vectors into the scan CTA's slot
                 if (wt == 0) {
                     if (k >= 1) ship_ok = wait_bar(&gb[WB_RECV_FREE], (k - 1) & 1, tmo, abort_flag, 64u, true);
@@ -872,10 +905,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_copy_to_peer(map_to_rank(recv + R_VEC, 0), vec, 1024, rb);
                         tma_store_commit();
                     }
-                    GDN_TR(c, 14 + 8 * g);
+                    GDN_TR(c, 42 + 16 * g);
                 }
             }
             if (wt == 0) tma_store_wait_all<0>();
+            if (ctl) {
+                mma_commit(&gb[WB_DRAIN]);
+                mbar_wait(&gb[WB_DRAIN], 0, kCleanupNs);
+                if (armed) mbar_wait(&gb[WB_FULL], (armed - 1) & 1, kCleanupNs);
+            }
         }
     }
 
@@ -928,15 +966,16 @@ int launch_r(const ScanArgs &a, cudaStream_t stream) {
     constexpr int NQ = 64 / R;
     const long rows = (long)a.T * R;
     const int BH = a.B * a.H;
-    CUtensorMap mK, mQ, mV, mO;
+    CUtensorMap mK, mQ, mV;
     if (!make_map(&mK, a.k, BH, rows, 64, 64, true) || !make_map(&mQ, a.q, BH, a.T, 64, NQ, true) ||
-        !make_map(&mV, a.v, BH, rows, 64, 64, true) || !make_map(&mO, a.o, BH, a.T, 128, NQ, false))
+        !make_map(&mV, a.v, BH, rows, 64, 64, true))
         return GDN_ERR_CUDA;
     TcParams p;
     p.beta = static_cast<const __nv_bfloat16 *>(a.beta);
     p.g = a.g;
     p.s0 = a.s0;
     p.sf = a.sf;
+    p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.T = a.T;
     p.rows = (int)rows;
     p.NT = (int)((rows + 63) / 64);
@@ -946,7 +985,7 @@ int launch_r(const ScanArgs &a, cudaStream_t stream) {
     auto kern = gdn_tc_kernel<R>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
         return GDN_ERR_CUDA;
-    kern<<<2 * BH, kThreads, kSmemBytes, stream>>>(mK, mQ, mV, mO, p);  // one 2-CTA cluster per head
+    kern<<<2 * BH, kThreads, kSmemBytes, stream>>>(mK, mQ, mV, p);  // one 2-CTA cluster per head
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
