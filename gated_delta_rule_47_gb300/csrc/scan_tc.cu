@@ -93,11 +93,9 @@ constexpr uint32_t S_END = S_FLAGS + 64;
 constexpr uint32_t GS = 99328;  // bytes per WY pipeline
 constexpr uint32_t G_KQ = 0;        // [K rows 0..63 | Q rows 64..] x 2 K-blocks
 constexpr uint32_t G_TWU = 32768;   // Tw (+0), Tu (+8192): bf16 [64 t][64 s] K-major
-constexpr uint32_t G_P = 49152;     // P bf16 [NQ][64] K-major, two buffers (+8192)
-constexpr uint32_t G_VEC1 = 65536;  // second buffer of the shipped vectors
+constexpr uint32_t G_PV = 49152;    // two buffers (+9216) of P bf16 [NQ][64] K-major (8 KB) + vectors (1 KB)
 constexpr uint32_t G_AF = 73728;    // A fp32 [64][68], inverted in place
 constexpr uint32_t G_X = 91136;     // inverse scratch 32x32 fp32
-constexpr uint32_t G_VEC = 95232;   // shipped vectors (first buffer)
 constexpr uint32_t G_MISC = 96256;  // Misc
 constexpr uint32_t W_BAR = 2 * GS;
 constexpr uint32_t W_FLAGS = W_BAR + 256;
@@ -108,6 +106,9 @@ constexpr uint32_t kSmemBytes = (S_END > W_END ? S_END : W_END) + 1024;
 // vectors shipped per chunk (floats): exp(g_last - g_s) n_s, output scale of
 // each query row, exp(g_last)
 constexpr uint32_t V_SEF = 0, V_QS = 64, V_EL = 128;
+// bytes shipped per chunk: Tw | Tu (16 KB), then P (8 KB region) | vectors (1 KB)
+constexpr uint32_t kShipBytes = 16384 + 8192 + 1024;
+static_assert(R_TU == R_TW + 8192 && R_VEC == R_P + 8192, "receive slot layout matches the two shipped blocks");
 
 // scan TMEM columns
 constexpr uint32_t TM_S = 0, TM_VN = 128, TM_W = 192, TM_O10 = 256, TM_O11 = 320, TM_O20 = 384, TM_O21 = 448;
@@ -232,6 +233,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
             for (int i = 0; i < 2 * WB_PER_GROUP; ++i) mbar_init(&bars[i], 1u);
         }
+        if (is_scan) {
+            // the receive barriers expect their first shipments; later phases are
+            // armed by the slot-release warp when it hands a slot back
+            for (int b = 0; b < 2 && b < p.NT; ++b) mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -347,6 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;
                     if (!wait_bar(&bars[SB_SLOT_DONE0 + b], (c >> 1) & 1, tmo, abort_flag, 16u)) break;
+                    if (c + 2 < NT) mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);  // chunk c+2's shipment
                     mbar_arrive_remote(map_to_rank(sbase + W_BAR + 8 * (WB_PER_GROUP * b + WB_RECV_FREE), 1));
                 }
             }
@@ -591,6 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_bf16_ss(tmem + 128 * g, smem_desc(a, 16, 1024), smem_desc(a, 16, 1024), idKQ, ks > 0);
                 }
                 mma_commit(&gb[WB_KQ_DONE]);
+                GDN_TR(g + 2 * kq_issued, 46 + 16 * g);  // KQ MMA of that chunk issued
                 kq_issued++;
                 return true;
             };
@@ -606,52 +614,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float *gp = p.g + (size_t)bh * p.T;
             const uint32_t recv = sbase + S_RECV0 + g * RS;  // this pipeline's slot in the scan CTA
             const uint32_t recv_bar = sbase + S_BAR + 8 * (SB_RECV0 + g);
-            auto prefetch = [&](int cc) -> float {
-                if (wt < 64) {
-                    const int row = cc * 64 + wt;
-                    return row < p.rows ? __bfloat162float(betap[row]) : 0.f;
+            // beta (warp 0) and g (warp 1) of rows lane and lane + 32 of a chunk are
+            // loaded one chunk ahead; warp 1 turns g into the within-chunk
+            // cumulative decay in registers at the end of the previous chunk, so
+            // that the start of a chunk only stores them
+            // The loads read clamped in-range addresses and nothing touches their
+            // results until the values are used, so no thread waits on them here.
+            float pf0 = 0.f, pf1 = 0.f;             // values of the current chunk
+            uint32_t ld0 = 0, ld1 = 0;              // raw loads for the next chunk
+            bool lv0 = false, lv1 = false;          // whether those rows exist
+            const unsigned short *betab = reinterpret_cast<const unsigned short *>(betap);
+            const uint32_t *gpb = reinterpret_cast<const uint32_t *>(gp);
+            auto prefetch = [&](int cc) {
+                const int r0 = cc * 64 + lane, r1 = r0 + 32;
+                if (wi == 0) {
+                    lv0 = r0 < p.rows;
+                    lv1 = r1 < p.rows;
+                    ld0 = betab[lv0 ? r0 : 0];
+                    ld1 = betab[lv1 ? r1 : 0];
+                } else if (wi == 1) {
+                    lv0 = r0 < p.rows && r0 % R == 0;
+                    lv1 = r1 < p.rows && r1 % R == 0;
+                    ld0 = gpb[lv0 ? r0 / R : 0];
+                    ld1 = gpb[lv1 ? r1 / R : 0];
                 }
-                if (wt < 128) {
-                    const int row = cc * 64 + wt - 64;
-                    return (row < p.rows && row % R == 0) ? gp[row / R] : 0.f;
-                }
-                return 0.f;
             };
-            float pf = g < NT ? prefetch(g) : 0.f;
+            auto take = [&]() {  // the prefetched values, as floats
+                if (wi == 0) {
+                    pf0 = lv0 ? __uint_as_float(ld0 << 16) : 0.f;
+                    pf1 = lv1 ? __uint_as_float(ld1 << 16) : 0.f;
+                } else {
+                    pf0 = lv0 ? __uint_as_float(ld0) : 0.f;
+                    pf1 = lv1 ? __uint_as_float(ld1) : 0.f;
+                }
+            };
+            int cs_safe = 1;
+            float cs_el = 1.f;
+            auto cumsum = [&]() {  // warp 1: g of rows lane / lane + 32 -> cumulative decay
+                take();
+                float a = pf0, b2 = pf1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float ya = __shfl_up_sync(0xffffffffu, a, off);
+                    const float yb = __shfl_up_sync(0xffffffffu, b2, off);
+                    if (lane >= off) { a += ya; b2 += yb; }
+                }
+                b2 += __shfl_sync(0xffffffffu, a, 31);
+                const float g0 = __shfl_sync(0xffffffffu, a, 0);
+                float dev = fmaxf(fabsf(a - g0), fabsf(b2 - g0));
+#pragma unroll
+                for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
+                pf0 = a;
+                pf1 = b2;
+                cs_safe = dev <= 80.f ? 1 : 0;
+                cs_el = __expf(b2);
+            };
+            if (g < NT) {
+                prefetch(g);
+                if (wi == 0) take();
+                if (wi == 1) cumsum();
+            }
             bool ship_ok = true;
             for (int k = 0, c = g; c < NT; ++k, c += 2) {
                 if (wt == 0) GDN_TR(c, 32 + 16 * g);
                 // P and the vectors alternate between two buffers; the shipment of
                 // chunk c-2 that last read this pair was waited for in chunk c-1
-                uint8_t *ptile = gbase + G_P + (k & 1) * 8192;
-                float *vec = reinterpret_cast<float *>(gbase + ((k & 1) ? G_VEC1 : G_VEC));
-                // 1. beta and g of the chunk's rows; cumulative decay
-                if (wt < 64) ms->beta[wt] = pf;
-                else if (wt < 128) ms->gam[wt - 64] = pf;
-                if (c + 2 < NT) pf = prefetch(c + 2);
-                if (!group_all(ship_ok && kq_ok, bar_id, 256)) break;
-                if (wt < 32) {
-                    float a = ms->gam[lane], b2 = ms->gam[lane + 32];
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float ya = __shfl_up_sync(0xffffffffu, a, off);
-                        const float yb = __shfl_up_sync(0xffffffffu, b2, off);
-                        if (lane >= off) { a += ya; b2 += yb; }
-                    }
-                    b2 += __shfl_sync(0xffffffffu, a, 31);
-                    ms->gam[lane] = a;
-                    ms->gam[lane + 32] = b2;
-                    const float g0 = __shfl_sync(0xffffffffu, a, 0);
-                    float dev = fmaxf(fabsf(a - g0), fabsf(b2 - g0));
-#pragma unroll
-                    for (int off = 16; off; off >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, off));
+                uint8_t *ptile = gbase + G_PV + (k & 1) * 9216;
+                float *vec = reinterpret_cast<float *>(ptile + 8192);
+                // 1. beta, cumulative decay (published by the barrier below)
+                if (wi == 0) {
+                    if (k > 0) take();
+                    ms->beta[lane] = pf0;
+                    ms->beta[lane + 32] = pf1;
+                } else if (wi == 1) {
+                    ms->gam[lane] = pf0;
+                    ms->gam[lane + 32] = pf1;
                     if (lane == 31) {
-                        ms->safe = dev <= 80.f ? 1 : 0;
-                        vec[V_EL] = __expf(b2);
+                        ms->safe = cs_safe;
+                        vec[V_EL] = cs_el;
                     }
                 }
+                if (c + 2 < NT) prefetch(c + 2);
+                if (wt == 0) GDN_TR(c, 44 + 16 * g);
                 const bool wk = wait_bar(&gb[WB_KQ_DONE], k & 1, tmo, abort_flag, 8u);
-                if (!group_all(wk, bar_id, 256)) break;  // also publishes gam
+                if (wt == 0) GDN_TR(c, 45 + 16 * g);
+                if (!group_all(wk && ship_ok && kq_ok, bar_id, 256)) break;  // also publishes beta, gam
                 if (wt == 0) GDN_TR(c, 33 + 16 * g);
                 tc_fence_after_sync();
                 // 2. this thread's 32 columns of its K K^T (q < 2) or Q K^T (q >= 2) row
@@ -767,7 +814,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(ptile + sw128_offset(t, 32 * h + 8 * j)) =
                             make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
-                if (wt == 0) GDN_TR(c, 47 + 16 * g);
                 named_bar(bar_id, 256);  // A complete
                 if (wt == 0) GDN_TR(c, 36 + 16 * g);
                 // 4. T = (I + A)^-1 in place over A: 16x16 diagonal blocks by
@@ -805,7 +851,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int m = 0; m < 16; ++m) a += AF[(i0 + rr) * kAS + j0 + m] * AF[(j0 + m) * kAS + j0 + cl];
                         acc[kk] = a;
                     }
-                    if (lane == 0 && (wi == 0 || wi == 7)) GDN_TR(c, 43 + 16 * g + (wi == 7 ? 1 : 0));
                     XS[wt] = acc[0];
                     XS[wt + 256] = acc[1];
                     named_bar(bar_id, 256);
@@ -843,7 +888,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             acc[kk] += a4.x * t0 + a4.y * t1 + a4.z * t2 + a4.w * t3;
                         }
                     }
-                    if (lane == 0 && (wi == 0 || wi == 7)) GDN_TR(c, 45 + 16 * g + (wi == 7 ? 1 : 0));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) XS[(rr + 8 * kk) * 32 + cl] = acc[kk];
                     named_bar(bar_id, 256);
@@ -893,16 +937,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (wt == 0) GDN_TR(c, 41 + 16 * g);
                 // K K^T / Q K^T of the next chunk (its load has had the whole chunk)
                 if (ctl && kq_ok && c + 2 < NT) kq_ok = mma_kq();
+                if (wi == 1 && c + 2 < NT) cumsum();
                 // 6. ship Tw, Tu, P and the vectors into the scan CTA's slot
                 if (wt == 0) {
                     if (k >= 1) ship_ok = wait_bar(&gb[WB_RECV_FREE], (k - 1) & 1, tmo, abort_flag, 64u, true);
+                    GDN_TR(c, 47 + 16 * g);
                     if (ship_ok) {
-                        mbar_arrive_expect_tx_remote(map_to_rank(recv_bar, 0), 16384 + NQ * 128 + 1024);
+                        // the scan CTA armed its receive barrier for these bytes
                         const uint32_t rb = map_to_rank(recv_bar, 0);
-                        bulk_copy_to_peer(map_to_rank(recv + R_TW, 0), twu, 8192, rb);
-                        bulk_copy_to_peer(map_to_rank(recv + R_TU, 0), twu + 8192, 8192, rb);
-                        bulk_copy_to_peer(map_to_rank(recv + R_P, 0), ptile, NQ * 128, rb);
-                        bulk_copy_to_peer(map_to_rank(recv + R_VEC, 0), vec, 1024, rb);
+                        bulk_copy_to_peer(map_to_rank(recv + R_TW, 0), twu, 16384, rb);
+                        bulk_copy_to_peer(map_to_rank(recv + R_P, 0), ptile, 8192 + 1024, rb);
                         tma_store_commit();
                     }
                     GDN_TR(c, 42 + 16 * g);
