@@ -95,8 +95,10 @@ constexpr uint32_t G_KQ = 0;        // [K rows 0..63 | Q rows 64..] x 2 K-blocks
 constexpr uint32_t G_TWU = 32768;   // Tw (+0), Tu (+8192): bf16 [64 t][64 s] K-major
 constexpr uint32_t G_PV = 49152;    // two buffers (+9216) of P bf16 [NQ][64] K-major (8 KB) + vectors (1 KB)
 constexpr uint32_t G_AF = 73728;    // A fp32 [64][68], inverted in place
-constexpr uint32_t G_X = 91136;     // inverse scratch 32x32 fp32
+constexpr uint32_t G_X = 91136;     // inverse scratch: 32x32 fp32, row stride kXS (36) words
+constexpr int kXS = 36;             // makes the column-strided stores of X conflict-free
 constexpr uint32_t G_MISC = 96256;  // Misc
+static_assert(G_X + 32 * kXS * 4 <= G_MISC, "inverse scratch fits");
 constexpr uint32_t W_BAR = 2 * GS;
 constexpr uint32_t W_FLAGS = W_BAR + 256;
 constexpr uint32_t W_END = W_FLAGS + 64;
@@ -889,22 +891,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) XS[(rr + 8 * kk) * 32 + cl] = acc[kk];
+                    for (int kk = 0; kk < 4; ++kk) XS[(rr + 8 * kk) * kXS + cl] = acc[kk];
                     named_bar(bar_id, 256);
                     if (wt == 0) GDN_TR(c, 39 + 16 * g);
                     // T_bl = -T_bot X (T_bot lower triangular): row r needs m <= r only
-                    const int cl2 = wt & 31, r0 = wi;  // rows r0 + 8k, k < 4 (warp-uniform)
+                    // (rows r0 + 8k, k < 4, warp-uniform; one column per lane): each X
+                    // element is loaded once for the four rows, T_bot elements are
+                    // warp-wide broadcasts
+                    const int cl2 = wt & 31, r0 = wi;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const int r = r0 + 8 * kk;
-                        float a = 0.f;
-#pragma unroll 1
-                        for (int m = 0; m <= r; m += 4) {
-                            const float4 t4 = *reinterpret_cast<const float4 *>(&AF[(32 + r) * kAS + 32 + m]);
-                            a += t4.x * XS[(m + 0) * 32 + cl2] + t4.y * XS[(m + 1) * 32 + cl2] +
-                                 t4.z * XS[(m + 2) * 32 + cl2] + t4.w * XS[(m + 3) * 32 + cl2];
-                        }
-                        acc[kk] = a;
+                    for (int kk = 0; kk < 4; ++kk) acc[kk] = 0.f;
+                    const float *tcol = &AF[(32 + r0) * kAS + 32];
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) {
+                        if (m > r0 + 24) break;
+                        const float xv = XS[m * kXS + cl2];
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            if (m <= r0 + 8 * kk) acc[kk] += tcol[8 * kk * kAS + m] * xv;
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) AF[(32 + r0 + 8 * kk) * kAS + cl2] = -acc[kk];
