@@ -842,36 +842,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 named_bar(bar_id, 256);
                 {
-                    float acc[2];
+                    // 16-level merges T_10 = -T_11 (A_10 T_00) (warps 0..3) and
+                    // T_32 = -T_33 (A_32 T_22) (warps 4..7): rows rr and rr + 8 of the
+                    // 16x16 block and column cl per thread, sharing each T / X load
+                    const int hb = wi >> 2, rr = (wt >> 4) & 7, cl = wt & 15;
+                    const int i0 = 32 * hb + 16, j0 = 32 * hb;
+                    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int e = wt + 256 * kk;
-                        const int hb = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
-                        const int i0 = 32 * hb + 16, j0 = 32 * hb;
-                        float a = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) a += AF[(i0 + rr) * kAS + j0 + m] * AF[(j0 + m) * kAS + j0 + cl];
-                        acc[kk] = a;
+                    for (int m = 0; m < 16; ++m) {
+                        const float tv = AF[(j0 + m) * kAS + j0 + cl];
+                        a0 += AF[(i0 + rr) * kAS + j0 + m] * tv;
+                        a1 += AF[(i0 + rr + 8) * kAS + j0 + m] * tv;
                     }
-                    XS[wt] = acc[0];
-                    XS[wt + 256] = acc[1];
+                    XS[(hb << 8) + rr * 16 + cl] = a0;
+                    XS[(hb << 8) + (rr + 8) * 16 + cl] = a1;
                     named_bar(bar_id, 256);
+                    float b0 = 0.f, b1 = 0.f;
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int e = wt + 256 * kk;
-                        const int hb = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
-                        const int i0 = 32 * hb + 16;
-                        float a = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) a += AF[(i0 + rr) * kAS + i0 + m] * XS[(hb << 8) + m * 16 + cl];
-                        acc[kk] = a;
+                    for (int m = 0; m < 16; ++m) {
+                        const float xv = XS[(hb << 8) + m * 16 + cl];
+                        b0 += AF[(i0 + rr) * kAS + i0 + m] * xv;
+                        b1 += AF[(i0 + rr + 8) * kAS + i0 + m] * xv;
                     }
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int e = wt + 256 * kk;
-                        const int hb = e >> 8, rr = (e >> 4) & 15, cl = e & 15;
-                        AF[(32 * hb + 16 + rr) * kAS + 32 * hb + cl] = -acc[kk];
-                    }
+                    AF[(i0 + rr) * kAS + j0 + cl] = -b0;
+                    AF[(i0 + rr + 8) * kAS + j0 + cl] = -b1;
                     named_bar(bar_id, 256);
                 }
                 if (wt == 0) GDN_TR(c, 38 + 16 * g);
