@@ -24,7 +24,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
           4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
-           "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count")
+           "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
+           "gdn_set_cluster_shape")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +65,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdn_get_device_error.restype = i
         lib.gdn_set_wait_limit.argtypes = [ctypes.c_ulonglong]
         lib.gdn_set_wait_limit.restype = i
+        lib.gdn_set_cluster_shape.argtypes = [i, i]
+        lib.gdn_set_cluster_shape.restype = i
         lib.gdn_launch_count.restype = ctypes.c_ulonglong
         if path is None:
             _lib = lib
@@ -204,6 +207,11 @@ def device_error(stream=None) -> int:
 def set_wait_limit(us: int) -> None:
     """Wall-clock limit in microseconds of each bounded device wait (0 = default)."""
     _raise("gdn_set_wait_limit", load().gdn_set_wait_limit(int(us)))
+
+
+def set_cluster_shape(heads_per_cluster: int = 0, wy_ctas_per_cluster: int = 0) -> None:
+    """Cluster shape of the tcgen05 path (0, 0: automatic)."""
+    _raise("gdn_set_cluster_shape", load().gdn_set_cluster_shape(int(heads_per_cluster), int(wy_ctas_per_cluster)))
 
 
 def launch_count() -> int:

@@ -150,4 +150,8 @@ unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }
 
 int gdn_set_wait_limit(unsigned long long us) { return gdn::scan_tc_set_wait_limit(us); }
 
+int gdn_set_cluster_shape(int heads_per_cluster, int wy_ctas_per_cluster) {
+    return gdn::scan_tc_set_cluster_shape(heads_per_cluster, wy_ctas_per_cluster);
+}
+
 }  // extern "C"

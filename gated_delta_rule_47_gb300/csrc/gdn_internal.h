@@ -45,6 +45,8 @@ size_t scan_tc_workspace_bytes(const ScanArgs &a);
 int launch_scan_tc(const ScanArgs &a, cudaStream_t stream);
 int scan_tc_read_clear_error(cudaStream_t stream);
 int scan_tc_set_wait_limit(unsigned long long polls);
+// Cluster shape of the tcgen05 path (heads and WY CTAs per cluster); 0, 0 = automatic.
+int scan_tc_set_cluster_shape(int hc, int nwy);
 
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream);
 

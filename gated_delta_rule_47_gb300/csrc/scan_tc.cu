@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -50,15 +51,17 @@ namespace gdn {
 namespace {
 __device__ unsigned int g_tc_error = 0;
 unsigned long long g_timeout_ns = 1000000000ull;  // host copy of the wait limit
+int g_force_hc = 0, g_force_nwy = 0;               // cluster shape override (0: automatic)
 }  // namespace
 
 // Optional timeline instrumentation (compiled in only with -DGDN_TRACE): the
-// first cluster records clock64() at fixed points of each role, per chunk.
+// first cluster records clock64() at fixed points of each role, per chunk of
+// its first head (tr_on is true in the roles and items that belong to it).
 #ifdef GDN_TRACE
 __device__ unsigned long long *g_trace = nullptr;
 #define GDN_TR(c, ev)                                                          \
     do {                                                                       \
-        if (blockIdx.x < 2 && g_trace != nullptr && (c) < 1024)                \
+        if (tr_on && g_trace != nullptr && (c) < 1024)                         \
             g_trace[(size_t)(c) * 64 + (ev)] = clock64();                      \
     } while (0)
 #else
@@ -120,7 +123,11 @@ enum ScanBar {
     SB_STG_FREE0, SB_STG_FREE1, SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_W_DONE, SB_WT_READY,
     SB_DRAIN, SB_WDRAIN, SB_OFREE0, SB_OFREE1, SB_NUM
 };
-enum WyBar { WB_FULL, WB_KQ_DONE, WB_RECV_FREE, WB_DRAIN, WB_PER_GROUP };
+// Per WY pipeline: FULL, KQ_DONE, DRAIN, then RECV_FREE for each (scan CTA of
+// the cluster, receive slot) the pipeline may ship to.
+constexpr int kMaxHc = 4;  // heads per cluster at most
+enum WyBar { WB_FULL, WB_KQ_DONE, WB_DRAIN, WB_RECV_FREE0, WB_PER_GROUP = WB_RECV_FREE0 + 2 * kMaxHc };
+static_assert(2 * WB_PER_GROUP <= 32, "WY barriers fit their 256 bytes");
 
 // Per-chunk vectors of one WY pipeline.
 struct Misc {
@@ -144,6 +151,9 @@ struct TcParams {
     float *sf;
     __nv_bfloat16 *o;
     int T, rows, NT;
+    int BH;   // heads (batch x head)
+    int hc;   // scan CTAs (heads) per cluster, ranks 0 .. hc-1
+    int nwy;  // WY CTAs per cluster, ranks hc .. hc+nwy-1
     float scale;
     unsigned flags;
     unsigned long long timeout_ns;
@@ -209,19 +219,26 @@ __device__ __forceinline__ void store16_sw128(uint8_t *tile, int row, int col, c
 
 // =========================================================================== kernel
 template <int R>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gdn_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
                   const __grid_constant__ CUtensorMap mV, TcParams p) {
     constexpr int NQ = 64 / R;  // query rows (tokens) per chunk
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
+    // A cluster holds hc scan CTAs (one head each, ranks 0..hc-1) and nwy WY CTAs
+    // whose 2*nwy pipelines take the cluster's (head, chunk) items round-robin.
     const uint32_t rank = cluster_ctarank();
-    const bool is_scan = rank == 0;
+    const int hc = p.hc, nwy = p.nwy;
+    const int h0 = (int)(blockIdx.x / (unsigned)(hc + nwy)) * hc;  // first head of the cluster
+    const int hce = min(hc, p.BH - h0);                             // heads it holds
+    const bool is_scan = (int)rank < hc;
+    bool tr_on = blockIdx.x < (unsigned)(hc + nwy) && rank == 0;
+    (void)tr_on;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + (is_scan ? S_BAR : W_BAR));
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + (is_scan ? S_FLAGS : W_FLAGS));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + (is_scan ? S_FLAGS : W_FLAGS) + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x >> 1;
+    const int bh = h0 + (int)rank;  // the scan CTA's head
     const int NT = p.NT;
     const unsigned long long tmo = p.timeout_ns;
     const uint32_t ncols = is_scan ? 512u : 256u;
@@ -233,9 +250,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                         ? 256u
                                         : ((i == SB_WT_READY || i == SB_OFREE0 || i == SB_OFREE1) ? 128u : 1u));
         } else {
-            for (int i = 0; i < 2 * WB_PER_GROUP; ++i) mbar_init(&bars[i], 1u);
+            for (int i = 0; i < 2 * WB_PER_GROUP; ++i) mbar_init(&bars[i], 1u);  // pipelines 2*(rank-hc) + 0, 1
         }
-        if (is_scan) {
+        if (is_scan && (int)rank < hce) {
             // the receive barriers expect their first shipments; later phases are
             // armed by the slot-release warp when it hands a slot back
             for (int b = 0; b < 2 && b < p.NT; ++b) mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);
@@ -253,14 +270,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&mV);
     }
     tc_fence_before_sync();
-    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+    cluster_sync_all();  // every CTA's barriers exist before any remote arrive
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t sbase = smem_u32(sm);
 
     if (is_scan) {
         // ================================================================= scan CTA
-        if (warp == 0) {
+        // (a scan CTA past the last head only takes part in the cluster barriers)
+        if ((int)rank >= hce) {
+        } else if (warp == 0) {
             // ------------------------------------------------------ TMA producer
             if (lane == 0) {
                 int armed[2] = {0, 0}, armed_v = 0;
@@ -355,8 +374,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;
                     if (!wait_bar(&bars[SB_SLOT_DONE0 + b], (c >> 1) & 1, tmo, abort_flag, 16u)) break;
-                    if (c + 2 < NT) mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);  // chunk c+2's shipment
-                    mbar_arrive_remote(map_to_rank(sbase + W_BAR + 8 * (WB_PER_GROUP * b + WB_RECV_FREE), 1));
+                    if (c + 2 < NT) {
+                        mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);  // chunk c+2's shipment
+                        // the pipeline that ships chunk c+2 of this head: item (c+2)*hce + rank
+                        const int pp = ((c + 2) * hce + (int)rank) % (2 * nwy);
+                        const uint32_t fb = sbase + W_BAR + 8 * (WB_PER_GROUP * (pp & 1) + WB_RECV_FREE0 + 2 * (int)rank + b);
+                        mbar_arrive_remote(map_to_rank(fb, (uint32_t)(hc + (pp >> 1))));
+                    }
                 }
             }
         } else if (warp == 3) {
@@ -562,10 +586,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ================================================================== WY CTA
         {
             // ---------------------------------- WY pipeline g: warps 0..7 / 8..15.
-            // One thread of warp 6 also loads K/Q with TMA and issues the
-            // K K^T / Q K^T MMA: the next chunk's load starts as soon as this
-            // chunk's tile and TMEM rows have been read, its MMA once this
-            // chunk's Tw / Tu are built.
+            // Pipeline pidx = 2 (rank - hc) + g of the cluster takes items
+            // pidx, pidx + 2 nwy, ...; item i is chunk i / hce of the cluster's
+            // head i % hce, shipped to that head's scan CTA.  One thread of warp 6
+            // also loads K/Q with TMA and issues the K K^T / Q K^T MMA: the next
+            // item's load starts as soon as this item's tile and TMEM rows have
+            // been read, its MMA once this item's Tw / Tu are built.
             const int g = warp >> 3;
             const int wi = warp & 7;
             const int wt = wi * 32 + lane;  // 0..255
@@ -582,13 +608,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t kqa = sbase + g * GS + G_KQ;
             const uint32_t idKQ = idesc_bf16(128, 64, false, false);
             const bool ctl = wt == 192;  // warp 6: not one of the diagonal-block warps
-            int armed = 0, kq_issued = 0;  // thread 0: TMA loads and KQ MMAs issued
-            auto load_kq = [&](int cc) {
+            const int nP = 2 * nwy, pidx = 2 * ((int)rank - hc) + g;  // pipelines of the cluster, this one
+            const int nitems = NT * hce;
+            int armed = 0, kq_issued = 0;  // control thread: TMA loads and KQ MMAs issued
+            auto load_kq = [&](int item) {
+                const int cc = item / hce, ibh = h0 + item % hce;
                 mbar_arrive_expect_tx(&gb[WB_FULL], 16384 + 2 * NQ * 128);
-                tma_load_3d(kq, &mK, &gb[WB_FULL], 0, cc * 64, bh);
-                tma_load_3d(kq + 16384, &mK, &gb[WB_FULL], 64, cc * 64, bh);
-                tma_load_3d(kq + 8192, &mQ, &gb[WB_FULL], 0, cc * NQ, bh);
-                tma_load_3d(kq + 16384 + 8192, &mQ, &gb[WB_FULL], 64, cc * NQ, bh);
+                tma_load_3d(kq, &mK, &gb[WB_FULL], 0, cc * 64, ibh);
+                tma_load_3d(kq + 16384, &mK, &gb[WB_FULL], 64, cc * 64, ibh);
+                tma_load_3d(kq + 8192, &mQ, &gb[WB_FULL], 0, cc * NQ, ibh);
+                tma_load_3d(kq + 16384 + 8192, &mQ, &gb[WB_FULL], 64, cc * NQ, ibh);
                 armed++;
             };
             auto mma_kq = [&]() -> bool {
@@ -600,22 +629,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mma_bf16_ss(tmem + 128 * g, smem_desc(a, 16, 1024), smem_desc(a, 16, 1024), idKQ, ks > 0);
                 }
                 mma_commit(&gb[WB_KQ_DONE]);
-                GDN_TR(g + 2 * kq_issued, 46 + 16 * g);  // KQ MMA of that chunk issued
                 kq_issued++;
                 return true;
             };
-            bool kq_ok = true;  // thread 0 only
-            if (ctl && g < NT) {
-                load_kq(g);
+            bool kq_ok = true;  // control thread only
+            if (ctl && pidx < nitems) {
+                load_kq(pidx);
                 kq_ok = mma_kq();
             }
             const uint32_t lb = tmem_lane_base(warp);
             const uint32_t tkq = tmem + 128 * g;
             const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
-            const __nv_bfloat16 *betap = p.beta + (size_t)bh * p.rows;
-            const float *gp = p.g + (size_t)bh * p.T;
-            const uint32_t recv = sbase + S_RECV0 + g * RS;  // this pipeline's slot in the scan CTA
-            const uint32_t recv_bar = sbase + S_BAR + 8 * (SB_RECV0 + g);
             // beta (warp 0) and g (warp 1) of rows lane and lane + 32 of a chunk are
             // loaded one chunk ahead; warp 1 turns g into the within-chunk
             // cumulative decay in registers at the end of the previous chunk, so
@@ -625,9 +649,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float pf0 = 0.f, pf1 = 0.f;             // values of the current chunk
             uint32_t ld0 = 0, ld1 = 0;              // raw loads for the next chunk
             bool lv0 = false, lv1 = false;          // whether those rows exist
-            const unsigned short *betab = reinterpret_cast<const unsigned short *>(betap);
-            const uint32_t *gpb = reinterpret_cast<const uint32_t *>(gp);
-            auto prefetch = [&](int cc) {
+            auto prefetch = [&](int item) {
+                const int cc = item / hce, ibh = h0 + item % hce;
+                const unsigned short *betab = reinterpret_cast<const unsigned short *>(p.beta) + (size_t)ibh * p.rows;
+                const uint32_t *gpb = reinterpret_cast<const uint32_t *>(p.g) + (size_t)ibh * p.T;
                 const int r0 = cc * 64 + lane, r1 = r0 + 32;
                 if (wi == 0) {
                     lv0 = r0 < p.rows;
@@ -671,13 +696,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 cs_safe = dev <= 80.f ? 1 : 0;
                 cs_el = __expf(b2);
             };
-            if (g < NT) {
-                prefetch(g);
+            if (pidx < nitems) {
+                prefetch(pidx);
                 if (wi == 0) take();
                 if (wi == 1) cumsum();
             }
+            uint32_t rf_par = 0;  // thread 0: parity of the next RECV_FREE phase, bit 2 * head + slot
             bool ship_ok = true;
-            for (int k = 0, c = g; c < NT; ++k, c += 2) {
+            for (int k = 0, it = pidx; it < nitems; ++k, it += nP) {
+                const int c = it / hce, hh = it % hce;  // chunk c of the cluster's head hh
+                const bool more = it + nP < nitems;     // this pipeline has a next item
+                tr_on = blockIdx.x < (unsigned)(hc + nwy) && hh == 0;
                 if (wt == 0) GDN_TR(c, 32 + 16 * g);
                 // P and the vectors alternate between two buffers; the shipment of
                 // chunk c-2 that last read this pair was waited for in chunk c-1
@@ -696,7 +725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         vec[V_EL] = cs_el;
                     }
                 }
-                if (c + 2 < NT) prefetch(c + 2);
+                if (more) prefetch(it + nP);
                 if (wt == 0) GDN_TR(c, 44 + 16 * g);
                 const bool wk = wait_bar(&gb[WB_KQ_DONE], k & 1, tmo, abort_flag, 8u);
                 if (wt == 0) GDN_TR(c, 45 + 16 * g);
@@ -741,7 +770,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before_sync();
                 named_bar(bar_id, 256);  // n and partial q norms visible; K/Q tile and TMEM rows read
-                if (ctl && kq_ok && c + 2 < NT) load_kq(c + 2);
+                if (ctl && kq_ok && more) load_kq(it + nP);
                 if (wt == 0) GDN_TR(c, 34 + 16 * g);
                 // per-row / per-column factors of the chunk
                 if (wt < 64) {
@@ -934,17 +963,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 named_bar(bar_id, 256);
                 if (wt == 0) GDN_TR(c, 41 + 16 * g);
                 // K K^T / Q K^T of the next chunk (its load has had the whole chunk)
-                if (ctl && kq_ok && c + 2 < NT) kq_ok = mma_kq();
-                if (wi == 1 && c + 2 < NT) cumsum();
-                // 6. ship Tw, Tu, P and the vectors into the scan CTA's slot
+                if (ctl && kq_ok && more) kq_ok = mma_kq();
+                if (wi == 1 && more) cumsum();
+                // 6. ship Tw, Tu, P and the vectors into slot c & 1 of head hh's scan
+                //    CTA (cluster rank hh), once that head's chunk c-2 has left it
                 if (wt == 0) {
-                    if (k >= 1) ship_ok = wait_bar(&gb[WB_RECV_FREE], (k - 1) & 1, tmo, abort_flag, 64u, true);
+                    const int sl = c & 1, fbit = 2 * hh + sl;
+                    if (c >= 2) {
+                        ship_ok = wait_bar(&gb[WB_RECV_FREE0 + fbit], (rf_par >> fbit) & 1u, tmo, abort_flag, 64u, true);
+                        rf_par ^= 1u << fbit;
+                    }
                     GDN_TR(c, 47 + 16 * g);
                     if (ship_ok) {
                         // the scan CTA armed its receive barrier for these bytes
-                        const uint32_t rb = map_to_rank(recv_bar, 0);
-                        bulk_copy_to_peer(map_to_rank(recv + R_TW, 0), twu, 16384, rb);
-                        bulk_copy_to_peer(map_to_rank(recv + R_P, 0), ptile, 8192 + 1024, rb);
+                        const uint32_t recv = sbase + S_RECV0 + sl * RS;
+                        const uint32_t rb = map_to_rank(sbase + S_BAR + 8 * (SB_RECV0 + sl), (uint32_t)hh);
+                        bulk_copy_to_peer(map_to_rank(recv + R_TW, (uint32_t)hh), twu, 16384, rb);
+                        bulk_copy_to_peer(map_to_rank(recv + R_P, (uint32_t)hh), ptile, 8192 + 1024, rb);
                         tma_store_commit();
                     }
                     GDN_TR(c, 42 + 16 * g);
@@ -1003,6 +1038,74 @@ bool device_is_sm100_family() {
     return major == 10;
 }
 
+// Cluster shape for BH heads: hc heads (scan CTAs) and nwy WY CTAs per cluster,
+// one CTA per SM.  Among the shapes whose clusters are all resident at once, the
+// most WY pipelines per head (2 nwy / hc, counted up to 4, past which the state
+// chain is the limit) wins; then two heads per cluster, then three, one, four
+// (with two, a head's chunks alternate between two WY CTAs that also serve
+// another head, which measured fastest: B4 H16 T4096 0.201 ms against 0.233 ms
+// for one head per cluster on the same 128 SMs); then the fewest SMs.  With too
+// many heads for one wave, one WY CTA per head.  Cached per head count and device.
+template <int R>
+bool pick_shape(int BH, int *hc_out, int *nwy_out) {
+    static std::mutex mu;
+    static int cache_dev[16], cache_bh[16], cache_hc[16], cache_nwy[16], cache_n = 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < cache_n; ++i)
+        if (cache_dev[i] == dev && cache_bh[i] == BH) {
+            *hc_out = cache_hc[i];
+            *nwy_out = cache_nwy[i];
+            return true;
+        }
+    static const int kPref[kMaxHc + 1] = {0, 2, 4, 3, 1};  // preference among equal pipeline counts
+    int best_hc = 1, best_nwy = 1, best_q = -1, best_pref = -1, best_sms = 1 << 30;
+    for (int hc = 1; hc <= kMaxHc; ++hc) {
+        for (int nwy = 1; hc + nwy <= 16; ++nwy) {
+            const int clusters = (BH + hc - 1) / hc, need = clusters * (hc + nwy);
+            if (need > sms) continue;
+            const int q = std::min(8 * nwy / hc, 16);  // 4x WY pipelines per head, capped at 4
+            if (q < best_q) continue;
+            if (q == best_q && (kPref[hc] < best_pref || (kPref[hc] == best_pref && need >= best_sms))) continue;
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            cfg.gridDim = dim3((unsigned)need);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = kSmemBytes;
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)(hc + nwy);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int resident = 0;
+            if (cudaOccupancyMaxActiveClusters(&resident, gdn_tc_kernel<R>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                continue;
+            }
+            if (resident < clusters) continue;
+            best_hc = hc;
+            best_nwy = nwy;
+            best_q = q;
+            best_pref = kPref[hc];
+            best_sms = need;
+        }
+    }
+    if (cache_n < 16) {
+        cache_dev[cache_n] = dev;
+        cache_bh[cache_n] = BH;
+        cache_hc[cache_n] = best_hc;
+        cache_nwy[cache_n] = best_nwy;
+        ++cache_n;
+    }
+    *hc_out = best_hc;
+    *nwy_out = best_nwy;
+    return true;
+}
+
 template <int R>
 int launch_r(const ScanArgs &a, cudaStream_t stream) {
     constexpr int NQ = 64 / R;
@@ -1025,9 +1128,33 @@ int launch_r(const ScanArgs &a, cudaStream_t stream) {
     p.flags = a.flags;
     p.timeout_ns = g_timeout_ns;
     auto kern = gdn_tc_kernel<R>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return GDN_ERR_CUDA;
-    kern<<<2 * BH, kThreads, kSmemBytes, stream>>>(mK, mQ, mV, p);  // one 2-CTA cluster per head
+    int hc = 1, nwy = 1;
+    if (g_force_hc > 0) {
+        hc = g_force_hc;
+        nwy = g_force_nwy;
+    } else if (!pick_shape<R>(BH, &hc, &nwy)) {
+        return GDN_ERR_CUDA;
+    }
+    p.BH = BH;
+    p.hc = hc;
+    p.nwy = nwy;
+    const int clusters = (BH + hc - 1) / hc;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(clusters * (hc + nwy)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)(hc + nwy);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mK, mQ, mV, p) != cudaSuccess) return GDN_ERR_CUDA;
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -1061,6 +1188,17 @@ int scan_tc_read_clear_error(cudaStream_t stream) {
     if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
     if (v && cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
     return v ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
+int scan_tc_set_cluster_shape(int hc, int nwy) {
+    if (hc == 0 && nwy == 0) {
+        g_force_hc = g_force_nwy = 0;
+        return GDN_OK;
+    }
+    if (hc < 1 || hc > kMaxHc || nwy < 1 || hc + nwy > 16) return GDN_ERR_INVALID_ARG;
+    g_force_hc = hc;
+    g_force_nwy = nwy;
+    return GDN_OK;
 }
 
 #ifdef GDN_TRACE

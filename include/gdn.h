@@ -183,6 +183,19 @@ unsigned long long gdn_launch_count(void);
  */
 int gdn_set_wait_limit(unsigned long long polls);
 
+/*
+ * Cluster shape of the tcgen05 path for later calls on this process: each
+ * thread-block cluster holds heads_per_cluster scan CTAs (one (batch, head)
+ * each) and wy_ctas_per_cluster CTAs that compute the chunk-local WY products
+ * for them (two pipelines each, taking the cluster's (head, chunk) items in
+ * turn).  0, 0 restores the automatic choice: the shape with the most WY
+ * pipelines per head whose clusters are all resident on the device at once.
+ * Returns GDN_ERR_INVALID_ARG unless 1 <= heads_per_cluster <= 4,
+ * wy_ctas_per_cluster >= 1 and their sum <= 16.  A shape whose clusters cannot
+ * be scheduled makes the next launch fail with GDN_ERR_CUDA.
+ */
+int gdn_set_cluster_shape(int heads_per_cluster, int wy_ctas_per_cluster);
+
 #ifdef __cplusplus
 }
 #endif

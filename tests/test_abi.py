@@ -102,3 +102,13 @@ def test_cam_prep_argument_checks(lib):
     assert call(q=None) == 1
     assert call(q=FAKE + 2) == 3
     assert call(dtype=5) == 1
+
+
+def test_cluster_shape_checks(lib):
+    """The cluster-shape override accepts 1..4 heads and at least one WY CTA
+    per cluster (at most 16 CTAs), and 0, 0 restores the automatic choice."""
+    for hc, nwy in ((0, 1), (5, 1), (1, 0), (4, 13), (-1, 2)):
+        assert lib.gdn_set_cluster_shape(hc, nwy) == 1, (hc, nwy)
+    for hc, nwy in ((1, 1), (4, 5), (2, 14)):
+        assert lib.gdn_set_cluster_shape(hc, nwy) == 0
+    assert lib.gdn_set_cluster_shape(0, 0) == 0

@@ -170,6 +170,44 @@ def test_tensor_core_deltaproduct(r):
     assert rel_err(sf, rs) <= TOL_BF16
 
 
+@pytest.mark.parametrize("hc,nwy", [(1, 1), (1, 2), (1, 3), (2, 1), (2, 3), (3, 2), (4, 1), (4, 5)])
+def test_tensor_core_cluster_shapes(hc, nwy):
+    """Every cluster shape gives the oracle's results: hc scan CTAs share the
+    WY pipelines of nwy CTAs, which take the cluster's (head, chunk) items in
+    turn. Six heads leave the last cluster of hc = 4 half empty, and T = 300
+    gives five chunks per head with a ragged last one."""
+    inp = gdn_inputs(2, 3, 300, 128, 128, seed=90 + 10 * hc + nwy, dtype="bf16", initial_state=True)
+    d = to_dev(inp)
+    try:
+        binding.set_cluster_shape(hc, nwy)
+        o, sf = binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["initial_state"],
+                                      output_final_state=True)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_cluster_shape(0, 0)
+    assert binding.device_error() == 0
+    ro, rs = ref_gdn(inp)
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("hc,nwy", [(1, 2), (4, 5)])
+def test_tensor_core_deltaproduct_cluster_shapes(hc, nwy):
+    inp = gdn_inputs(1, 5, 150, 128, 128, seed=60 + hc, dtype="bf16", r=2, initial_state=True)
+    d = to_dev(inp)
+    try:
+        binding.set_cluster_shape(hc, nwy)
+        o, sf = binding.deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["initial_state"],
+                                               output_final_state=True, chunk=64)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_cluster_shape(0, 0)
+    assert binding.device_error() == 0
+    ro, rs = oracle.deltaproduct_fwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["initial_state"])
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
 def test_tensor_core_l2norm_and_scale():
     inp = gdn_inputs(1, 2, 200, 128, 128, seed=77, dtype="bf16", normalise_qk=False, initial_state=True)
     o, sf = run_gdn(inp, l2norm=True, scale=0.5)
