@@ -62,6 +62,24 @@ def gdn_flops_per_token_head(D, C):
     return 6 * D * D + 5 * C * D + C * C // 3
 
 
+def max_over_ranks(x, world, device):
+    """The largest of each rank's value (a step time): the job is as slow as
+    its slowest replica.  Needs an initialised process group when world > 1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens(tokens_per_replica, world):
+    """Tokens one step processes over all ranks: each rank runs its own replica
+    of the workload (independent heads, no collective on the data path)."""
+    return tokens_per_replica * world
+
+
 def source_sha():
     h = hashlib.sha256()
     for name in SCAN_SOURCES:
@@ -244,12 +262,8 @@ def run_ours(args, rank, world, local_rank):
             step()
             torch.cuda.synchronize()
     barrier()
-    ms = ev_s.elapsed_time(ev_e) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_per_step = w.B * w.T * world
+    ms = max_over_ranks(ev_s.elapsed_time(ev_e) / args.steps, world, dev)
+    tokens_per_step = whole_job_tokens(w.B * w.T, world)
     value = tokens_per_step / (ms * 1e-3)
 
     # End to end through the same C-ABI call: every step copies its inputs in
@@ -306,11 +320,7 @@ def run_ours(args, rank, world, local_rank):
     stream.wait_stream(s_out)
     e_e.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, world, dev)
     e2e_value = tokens_per_step / (e2e_ms * 1e-3)
 
     if rank != 0:
