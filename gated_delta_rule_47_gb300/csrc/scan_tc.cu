@@ -121,7 +121,7 @@ constexpr uint32_t TM_S = 0, TM_VN = 128, TM_W = 192, TM_O10 = 256, TM_O11 = 320
 enum ScanBar {
     SB_FULLKQ0, SB_FULLKQ1, SB_VFULL, SB_VFREE, SB_S_READY, SB_VN_DONE, SB_VN_READY, SB_UPD_DONE,
     SB_STG_FREE0, SB_STG_FREE1, SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_W_DONE, SB_WT_READY,
-    SB_DRAIN, SB_WDRAIN, SB_OFREE0, SB_OFREE1, SB_NUM
+    SB_DRAIN, SB_WDRAIN, SB_OFREE0, SB_OFREE1, SB_VN2_READY, SB_NUM
 };
 // Per WY pipeline: FULL, KQ_DONE, DRAIN, then RECV_FREE for each (scan CTA of
 // the cluster, receive slot) the pipeline may ship to.
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         if (is_scan) {
             for (int i = 0; i < SB_NUM; ++i)
-                mbar_init(&bars[i], (i == SB_S_READY || i == SB_VN_READY)
+                mbar_init(&bars[i], (i == SB_S_READY || i == SB_VN_READY || i == SB_VN2_READY)
                                         ? 256u
                                         : ((i == SB_WT_READY || i == SB_OFREE0 || i == SB_OFREE1) ? 128u : 1u));
         } else {
@@ -357,6 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the state is ready before O2 runs (S_VN, which O2 reads, is only
                     // rewritten after the next VN_DONE, which completes after O2)
                     mma_commit(&bars[SB_UPD_DONE]);
+                    if (!wait_bar(&bars[SB_VN2_READY], c & 1, tmo, abort_flag, 2u)) break;
+                    tc_fence_after_sync();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ss(tmem + (b ? TM_O21 : TM_O20), smem_desc(sbase + S_VN + ks * 32, 16, 1024),
@@ -514,30 +516,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!group_all(w, 3, 256)) { ok = false; break; }
                 if (si == 0) GDN_TR(c, 3);
                 tc_fence_after_sync();
-                // state: S^T -> bf16 operand (K-block hh), then S^T <- exp(g_last) S^T
+                // state: S^T -> bf16 operand (K-block hh), signalled at once (Vn and
+                // O1 read only the operand); then S^T <- exp(g_last) S^T in TMEM,
+                // which only the state update (after VN_READY) needs
                 const float el = vec[V_EL];
+                {
+                    uint32_t r[4][16];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t col = TM_S + 64 * hh + 32 * j;
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(tmem + lb + col, r0);
-                    tmem_ld16(tmem + lb + col + 16, r1);
+                    for (int j = 0; j < 4; ++j) tmem_ld16(tmem + lb + TM_S + 64 * hh + 16 * j, r[j]);
                     tmem_wait_ld();
                     uint8_t *blk = sm + S_ST + hh * 16384;
-                    store16_sw128(blk, dv, 32 * j, r0);
-                    store16_sw128(blk, dv, 32 * j + 16, r1);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        r0[i] = __float_as_uint(el * __uint_as_float(r0[i]));
-                        r1[i] = __float_as_uint(el * __uint_as_float(r1[i]));
+                    for (int j = 0; j < 4; ++j) store16_sw128(blk, dv, 16 * j, r[j]);
+                    tc_fence_before_sync();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[SB_S_READY]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) r[j][i] = __float_as_uint(el * __uint_as_float(r[j][i]));
+                        tmem_st16(tmem + lb + TM_S + 64 * hh + 16 * j, r[j]);
                     }
-                    tmem_st16(tmem + lb + col, r0);
-                    tmem_st16(tmem + lb + col + 16, r1);
                 }
-                tmem_wait_st();
-                tc_fence_before_sync();
-                fence_proxy_async_smem();
-                mbar_arrive(&bars[SB_S_READY]);
                 if (si == 0) GDN_TR(c, 4);
                 // Vn^T -> bf16 operand and its decayed copy (columns 32hh..32hh+31)
                 const bool wv = wait_bar(&bars[SB_VN_DONE], c & 1, tmo, abort_flag, 4u);
@@ -550,19 +550,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld16(tv, r0);
                     tmem_ld16(tv + 16, r1);
                     tmem_wait_ld();
-                    store16_sw128(sm + S_VN, dv, 32 * hh, r0);
-                    store16_sw128(sm + S_VN, dv, 32 * hh + 16, r1);
+                    // the decayed copy first: the state update needs it (and the
+                    // decayed state stored above); the plain copy is for O2 only
+                    uint32_t e0[16], e1[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        r0[i] = __float_as_uint(vec[V_SEF + 32 * hh + i] * __uint_as_float(r0[i]));
-                        r1[i] = __float_as_uint(vec[V_SEF + 32 * hh + 16 + i] * __uint_as_float(r1[i]));
+                        e0[i] = __float_as_uint(vec[V_SEF + 32 * hh + i] * __uint_as_float(r0[i]));
+                        e1[i] = __float_as_uint(vec[V_SEF + 32 * hh + 16 + i] * __uint_as_float(r1[i]));
                     }
-                    store16_sw128(sm + S_VS, dv, 32 * hh, r0);
-                    store16_sw128(sm + S_VS, dv, 32 * hh + 16, r1);
+                    store16_sw128(sm + S_VS, dv, 32 * hh, e0);
+                    store16_sw128(sm + S_VS, dv, 32 * hh + 16, e1);
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[SB_VN_READY]);
+                    store16_sw128(sm + S_VN, dv, 32 * hh, r0);
+                    store16_sw128(sm + S_VN, dv, 32 * hh + 16, r1);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[SB_VN2_READY]);
                 }
-                tc_fence_before_sync();
-                fence_proxy_async_smem();
-                mbar_arrive(&bars[SB_VN_READY]);
                 if (si == 0) GDN_TR(c, 6);
             }
             bool fin = ok && NT > 0 && wait_bar(&bars[SB_UPD_DONE], (NT - 1) & 1, tmo, abort_flag, 4u);
