@@ -191,6 +191,18 @@ def test_tensor_core_cluster_shapes(hc, nwy):
     assert rel_err(sf, rs) <= TOL_BF16
 
 
+@pytest.mark.parametrize("B,H,T", [(1, 1, 200), (1, 1, 64), (3, 1, 130)])
+def test_tensor_core_few_heads_automatic_shape(B, H, T):
+    """With fewer heads than a cluster holds, the scan CTAs past the last head
+    only take part in the cluster barriers; results are unaffected."""
+    inp = gdn_inputs(B, H, T, 128, 128, seed=B * 7 + T, dtype="bf16", initial_state=True)
+    o, sf = run_gdn(inp)
+    assert binding.device_error() == 0
+    ro, rs = ref_gdn(inp)
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
 @pytest.mark.parametrize("hc,nwy", [(1, 2), (4, 5)])
 def test_tensor_core_deltaproduct_cluster_shapes(hc, nwy):
     inp = gdn_inputs(1, 5, 150, 128, 128, seed=60 + hc, dtype="bf16", r=2, initial_state=True)
