@@ -93,7 +93,7 @@ constexpr uint32_t S_FLAGS = S_BAR + 256;
 constexpr uint32_t S_END = S_FLAGS + 64;
 
 // ------------------------------------------------------------------ WY CTA map
-constexpr uint32_t GS = 99328;  // bytes per WY pipeline
+constexpr uint32_t GS = 107520;  // bytes per WY pipeline
 constexpr uint32_t G_KQ = 0;        // [K rows 0..63 | Q rows 64..] x 2 K-blocks
 constexpr uint32_t G_TWU = 32768;   // Tw (+0), Tu (+8192): bf16 [64 t][64 s] K-major
 constexpr uint32_t G_PV = 49152;    // two buffers (+9216) of P bf16 [NQ][64] K-major (8 KB) + vectors (1 KB)
@@ -102,6 +102,16 @@ constexpr uint32_t G_X = 91136;     // inverse scratch: 32x32 fp32, row stride k
 constexpr int kXS = 36;             // makes the column-strided stores of X conflict-free
 constexpr uint32_t G_MISC = 96256;  // Misc
 static_assert(G_X + 32 * kXS * 4 <= G_MISC, "inverse scratch fits");
+// Operands of the tensor-core 32-level merge of the inverse, bf16 hi / lo halves
+// (4 KB each, 128-byte rows).  The K-major M = 64 operands hold rows 32..63
+// only: their descriptors start 4 KB lower, inside this pipeline's region, and
+// rows 0..31 of the products are not used.  A2 and B1 borrow the Tw / Tu tile,
+// B2 the A1 tile.
+constexpr uint32_t G_A1 = 99328;   // A[32..63][0..31]            K-major, rows 32..63 (hi | lo)
+constexpr uint32_t G_A2 = 32768;   // T_bot = T[32..63][32..63]   K-major, rows 32..63 (hi | lo)
+constexpr uint32_t G_B1 = 40960;   // T_top = T[0..31][0..31]     MN-major, 32 k-rows (hi | lo)
+constexpr uint32_t G_B2 = G_A1;    // Y = A_bl T_top              MN-major, 32 k-rows (hi | lo)
+static_assert(G_MISC + sizeof(float) * 768 <= G_A1 && G_A1 + 8192 <= GS, "WY map");
 constexpr uint32_t W_BAR = 2 * GS;
 constexpr uint32_t W_FLAGS = W_BAR + 256;
 constexpr uint32_t W_END = W_FLAGS + 64;
@@ -126,7 +136,7 @@ enum ScanBar {
 // Per WY pipeline: FULL, KQ_DONE, DRAIN, then RECV_FREE for each (scan CTA of
 // the cluster, receive slot) the pipeline may ship to.
 constexpr int kMaxHc = 4;  // heads per cluster at most
-enum WyBar { WB_FULL, WB_KQ_DONE, WB_DRAIN, WB_RECV_FREE0, WB_PER_GROUP = WB_RECV_FREE0 + 2 * kMaxHc };
+enum WyBar { WB_FULL, WB_KQ_DONE, WB_DRAIN, WB_INV, WB_RECV_FREE0, WB_PER_GROUP = WB_RECV_FREE0 + 2 * kMaxHc };
 static_assert(2 * WB_PER_GROUP <= 32, "WY barriers fit their 256 bytes");
 
 // Per-chunk vectors of one WY pipeline.
@@ -820,6 +830,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_float4(s0 < t ? av[4 * j] : 0.f, s0 + 1 < t ? av[4 * j + 1] : 0.f,
                                         s0 + 2 < t ? av[4 * j + 2] : 0.f, s0 + 3 < t ? av[4 * j + 3] : 0.f);
                     }
+                    if (t >= 32 && h == 0) {
+                        // A[t][0..31] (all below the diagonal) as the merge's A1 operand
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const __nv_bfloat162 hv = __floats2bfloat162_rn(av[2 * i], av[2 * i + 1]);
+                            const float2 hf2 = __bfloat1622float2(hv);
+                            hi[i] = *reinterpret_cast<const uint32_t *>(&hv);
+                            lo[i] = pack_bf16(av[2 * i] - hf2.x, av[2 * i + 1] - hf2.y);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            *reinterpret_cast<uint4 *>(gbase + G_A1 + sw128_offset(t - 32, 8 * j)) =
+                                make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                            *reinterpret_cast<uint4 *>(gbase + G_A1 + 4096 + sw128_offset(t - 32, 8 * j)) =
+                                make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+                        }
+                    }
                 } else if (t < NQ) {
                     const int row = t * R + R - 1;
                     const float gr = ms->gam[row];
@@ -904,47 +932,120 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_bar(bar_id, 256);
                 }
                 if (wt == 0) GDN_TR(c, 38 + 16 * g);
+                // 32-level merge T_bl = -T_bot (A_bl T_top) on the tensor cores, each
+                // product as hi*hi + hi*lo + lo*hi of bf16 halves (about 2^-16
+                // relative), M = 64 with rows 32..63 used, into TMEM columns 64..127
+                // of this pipeline.  First T_top and T_bot become operands (in the
+                // Tw / Tu tile, which the previous shipment has left by then).
                 {
-                    // X = A_bl T_top (rows 32..63, cols 0..31 of A; T_top lower triangular):
-                    // warp wi owns columns 4wi..4wi+3, so its sum starts at m = 4wi
-                    const int cl = 4 * wi + (lane >> 3), rr = lane & 7;  // rows rr + 8k, k < 4
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int m = 4 * wi; m < 32; m += 4) {
-                        const float t0 = AF[(m + 0) * kAS + cl], t1 = AF[(m + 1) * kAS + cl];
-                        const float t2 = AF[(m + 2) * kAS + cl], t3 = AF[(m + 3) * kAS + cl];
+                    const int which = wt >> 7, row = (wt >> 2) & 31, c8 = (wt & 3) * 8;
+                    const float *src = &AF[(32 * which + row) * kAS + 32 * which + c8];
+                    const float4 x0 = *reinterpret_cast<const float4 *>(src);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(src + 4);
+                    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const float4 a4 = *reinterpret_cast<const float4 *>(&AF[(32 + rr + 8 * kk) * kAS + m]);
-                            acc[kk] += a4.x * t0 + a4.y * t1 + a4.z * t2 + a4.w * t3;
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        const __nv_bfloat162 hv = __floats2bfloat162_rn(xv[2 * i], xv[2 * i + 1]);
+                        const float2 hf2 = __bfloat1622float2(hv);
+                        hi[i] = *reinterpret_cast<const uint32_t *>(&hv);
+                        lo[i] = pack_bf16(xv[2 * i] - hf2.x, xv[2 * i + 1] - hf2.y);
                     }
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) XS[(rr + 8 * kk) * kXS + cl] = acc[kk];
-                    named_bar(bar_id, 256);
-                    if (wt == 0) GDN_TR(c, 39 + 16 * g);
-                    // T_bl = -T_bot X (T_bot lower triangular): row r needs m <= r only
-                    // (rows r0 + 8k, k < 4, warp-uniform; one column per lane): each X
-                    // element is loaded once for the four rows, T_bot elements are
-                    // warp-wide broadcasts
-                    const int cl2 = wt & 31, r0 = wi;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) acc[kk] = 0.f;
-                    const float *tcol = &AF[(32 + r0) * kAS + 32];
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) {
-                        if (m > r0 + 24) break;
-                        const float xv = XS[m * kXS + cl2];
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            if (m <= r0 + 8 * kk) acc[kk] += tcol[8 * kk * kAS + m] * xv;
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) AF[(32 + r0 + 8 * kk) * kAS + cl2] = -acc[kk];
-                    // the previous shipment has been read out of Tw / Tu
+                    // T_top[row][c8..] is (k = row, n = c8..) of the MN-major B1; T_bot[row][c8..]
+                    // is (m = 32 + row, k = c8..) of the K-major A2: the same offsets
+                    uint8_t *opnd = gbase + (which ? G_A2 : G_B1);
                     if (wt == 0) tma_store_wait_read<0>();
+                    named_bar(bar_id, 256);  // the previous shipment has left the Tw / Tu tile
+                    *reinterpret_cast<uint4 *>(opnd + sw128_offset(row, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(opnd + 4096 + sw128_offset(row, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    fence_proxy_async_smem();
                     named_bar(bar_id, 256);
                 }
+                const uint32_t tinv = tmem + 128 * g + 64;
+                const uint32_t gsb = sbase + g * GS;
+                auto merge_mma = [&](uint32_t abase, uint32_t bbase) {
+                    const uint32_t idM = idesc_bf16(64, 64, false, true);
+                    int n = 0;
+#pragma unroll
+                    for (int hl = 0; hl < 3; ++hl) {
+                        const uint32_t a = abase - 4096 + (hl == 2 ? 4096 : 0);  // hi, hi, lo (rows 32..63)
+                        const uint32_t b = bbase + (hl == 1 ? 4096 : 0);         // hi, lo, hi
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+                            mma_bf16_ss(tinv, smem_desc(a + ks * 32, 16, 1024), smem_desc(b + ks * 2048, 8192, 1024),
+                                        idM, (n++) > 0);
+                    }
+                    mma_commit(&gb[WB_INV]);
+                };
+                if (ctl) {
+                    tc_fence_after_sync();
+                    merge_mma(gsb + G_A1, gsb + G_B1);  // Y = A_bl T_top
+                }
+                // rows 32..63 of a product sit in TMEM lanes 64..79 and 96..111
+                const bool rd = (wi == 2 || wi == 3) && lane < 16;
+                const int mrow = 16 * (wi - 2) + lane;  // row of Y / T_bl within the bottom half
+                bool ok_inv = true;
+                if (wi == 2 || wi == 3) {
+                    ok_inv = wait_bar(&gb[WB_INV], 0, tmo, abort_flag, 8u);
+                    if (ok_inv) {
+                        tc_fence_after_sync();
+                        uint32_t r0[16], r1[16];
+                        tmem_ld16(tinv + lb, r0);
+                        tmem_ld16(tinv + lb + 16, r1);
+                        tmem_wait_ld();
+                        if (rd) {
+                            // Y row mrow as row k = mrow of the MN-major B2 (hi, lo)
+                            uint32_t hi[16], lo[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float y0 = __uint_as_float(i < 8 ? r0[2 * i] : r1[2 * i - 16]);
+                                const float y1 = __uint_as_float(i < 8 ? r0[2 * i + 1] : r1[2 * i - 15]);
+                                const __nv_bfloat162 hv = __floats2bfloat162_rn(y0, y1);
+                                const float2 hf2 = __bfloat1622float2(hv);
+                                hi[i] = *reinterpret_cast<const uint32_t *>(&hv);
+                                lo[i] = pack_bf16(y0 - hf2.x, y1 - hf2.y);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                *reinterpret_cast<uint4 *>(gbase + G_B2 + sw128_offset(mrow, 8 * j)) =
+                                    make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                                *reinterpret_cast<uint4 *>(gbase + G_B2 + 4096 + sw128_offset(mrow, 8 * j)) =
+                                    make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    tc_fence_before_sync();
+                }
+                if (!group_all(ok_inv, bar_id, 256)) break;
+                if (ctl) {
+                    tc_fence_after_sync();
+                    merge_mma(gsb + G_A2, gsb + G_B2);  // T_bot Y
+                }
+                if (wi == 2 || wi == 3) {
+                    ok_inv = wait_bar(&gb[WB_INV], 1, tmo, abort_flag, 8u);
+                    if (ok_inv) {
+                        tc_fence_after_sync();
+                        uint32_t r0[16], r1[16];
+                        tmem_ld16(tinv + lb, r0);
+                        tmem_ld16(tinv + lb + 16, r1);
+                        tmem_wait_ld();
+                        if (rd) {
+                            float *trow = &AF[(32 + mrow) * kAS];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                *reinterpret_cast<float4 *>(trow + 4 * j) =
+                                    make_float4(-__uint_as_float(r0[4 * j]), -__uint_as_float(r0[4 * j + 1]),
+                                                -__uint_as_float(r0[4 * j + 2]), -__uint_as_float(r0[4 * j + 3]));
+                                *reinterpret_cast<float4 *>(trow + 16 + 4 * j) =
+                                    make_float4(-__uint_as_float(r1[4 * j]), -__uint_as_float(r1[4 * j + 1]),
+                                                -__uint_as_float(r1[4 * j + 2]), -__uint_as_float(r1[4 * j + 3]));
+                            }
+                        }
+                    }
+                    tc_fence_before_sync();
+                }
+                if (!group_all(ok_inv, bar_id, 256)) break;
                 if (wt == 0) GDN_TR(c, 40 + 16 * g);
                 // 5. Tw = T diag(beta e^g n), Tu = T diag(beta) as bf16 K-major tiles
                 {
