@@ -41,6 +41,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -123,6 +124,7 @@ constexpr uint32_t kSmemBytes = (S_END > W_END ? S_END : W_END) + 1024;
 constexpr uint32_t V_SEF = 0, V_QS = 64, V_EL = 128;
 // bytes shipped per chunk: Tw | Tu (16 KB), then P (8 KB region) | vectors (1 KB)
 constexpr uint32_t kShipBytes = 16384 + 8192 + 1024;
+constexpr int kRing = 8;  // ring slots per head in ring mode
 static_assert(R_TU == R_TW + 8192 && R_VEC == R_P + 8192, "receive slot layout matches the two shipped blocks");
 
 // scan TMEM columns
@@ -167,6 +169,14 @@ struct TcParams {
     float scale;
     unsigned flags;
     unsigned long long timeout_ns;
+    // Ring mode (flat != 0): one grid of BH scan CTAs and nwy WY CTAs, all
+    // resident (a cooperative launch); chunk c of head h travels through slot
+    // c % kRing of the head's ring in global memory instead of a cluster copy.
+    int flat;
+    uint8_t *ring;                // [BH][kRing] slots of kShipBytes
+    unsigned long long *ready;    // [BH][kRing]: epoch << 32 | (chunk + 1) of the slot's contents
+    unsigned long long *cons;     // [BH]: epoch << 32 | chunks the scan CTA has taken out of its ring
+    unsigned epoch;               // tag of this launch, never 0
 };
 
 constexpr unsigned long long kCleanupNs = 200000000ull;  // 0.2 s for draining on the way out
@@ -182,6 +192,30 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, unsigne
         if (cluster ? mbar_try_wait_cluster(bar, parity, 20000u) : mbar_try_wait_sleep(bar, parity, 20000u))
             return true;
         if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(&g_tc_error, code);
+            return false;
+        }
+    }
+}
+
+// Bounded wait, like wait_bar, until *flag (written by another CTA with a
+// release store) holds this launch's epoch in its high word and at least
+// `need` in its low word.  Gives up early once any CTA has reported an error.
+__device__ __forceinline__ bool wait_tag(const unsigned long long *flag, unsigned epoch, unsigned need,
+                                         unsigned long long timeout_ns, volatile int *abort_flag, unsigned code) {
+    unsigned long long v = ld_acquire_gpu(flag);
+    if ((unsigned)(v >> 32) == epoch && (unsigned)v >= need) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(100);
+        v = ld_acquire_gpu(flag);
+        if ((unsigned)(v >> 32) == epoch && (unsigned)v >= need) return true;
+        if (*abort_flag || *reinterpret_cast<volatile unsigned *>(&g_tc_error) != 0u) {
+            *abort_flag = 1;
+            return false;
+        }
         if (global_timer_ns() - t0 > timeout_ns) {
             *abort_flag = 1;
             atomicOr(&g_tc_error, code);
@@ -237,7 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
     // A cluster holds hc scan CTAs (one head each, ranks 0..hc-1) and nwy WY CTAs
     // whose 2*nwy pipelines take the cluster's (head, chunk) items round-robin.
-    const uint32_t rank = cluster_ctarank();
+    // In ring mode the whole grid plays the part of one cluster: hc = BH scan
+    // CTAs, then nwy WY CTAs, ranked by block index.
+    const bool flat = p.flat != 0;
+    const uint32_t rank = flat ? blockIdx.x : cluster_ctarank();
     const int hc = p.hc, nwy = p.nwy;
     const int h0 = (int)(blockIdx.x / (unsigned)(hc + nwy)) * hc;  // first head of the cluster
     const int hce = min(hc, p.BH - h0);                             // heads it holds
@@ -262,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             for (int i = 0; i < 2 * WB_PER_GROUP; ++i) mbar_init(&bars[i], 1u);  // pipelines 2*(rank-hc) + 0, 1
         }
-        if (is_scan && (int)rank < hce) {
+        if (!flat && is_scan && (int)rank < hce) {
             // the receive barriers expect their first shipments; later phases are
             // armed by the slot-release warp when it hands a slot back
             for (int b = 0; b < 2 && b < p.NT; ++b) mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);
@@ -280,7 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&mV);
     }
     tc_fence_before_sync();
-    cluster_sync_all();  // every CTA's barriers exist before any remote arrive
+    if (flat)
+        __syncthreads();
+    else
+        cluster_sync_all();  // every CTA's barriers exist before any remote arrive
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t sbase = smem_u32(sm);
@@ -382,7 +422,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 2) {
             // ------------------------------------------------------ slot release
             // hands each receive slot back to the WY pipeline that fills it
-            if (lane == 0) {
+            if (lane == 0 && flat) {
+                // ring mode: fetch each chunk's Tw | Tu | P | vectors from the ring
+                // once its WY pipeline has published it, and report the chunks
+                // taken out so that the ring slots can be refilled
+                const unsigned long long tagc = (unsigned long long)p.epoch << 32;
+                int armed[2] = {0, 0};
+                for (int c = 0; c < NT; ++c) {
+                    const int b = c & 1;
+                    if (c >= 2) {
+                        if (!wait_bar(&bars[SB_SLOT_DONE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 16u)) break;
+                        st_release_gpu(p.cons + bh, tagc | (unsigned)(c - 1));  // chunks 0 .. c-2 are out
+                    }
+                    const size_t slot = (size_t)bh * kRing + c % kRing;
+                    if (!wait_tag(p.ready + slot, p.epoch, (unsigned)(c + 1), tmo, abort_flag, 256u)) break;
+                    fence_proxy_async_global();
+                    mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);
+                    bulk_load_global(sm + S_RECV0 + b * RS, p.ring + slot * kShipBytes, kShipBytes, &bars[SB_RECV0 + b]);
+                    armed[b]++;
+                }
+                for (int b = 0; b < 2; ++b)
+                    if (armed[b]) mbar_wait(&bars[SB_RECV0 + b], (armed[b] - 1) & 1, kCleanupNs);
+            } else if (lane == 0) {
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;
                     if (!wait_bar(&bars[SB_SLOT_DONE0 + b], (c >> 1) & 1, tmo, abort_flag, 16u)) break;
@@ -719,6 +780,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint32_t rf_par = 0;  // thread 0: parity of the next RECV_FREE phase, bit 2 * head + slot
             bool ship_ok = true;
+            int pend = -1, pend_tag = 0;  // thread 0, ring mode: slot and tag still to publish
+            auto publish = [&]() {        // once the slot's copies are complete
+                if (pend >= 0) {
+                    tma_store_wait_all<0>();
+                    fence_proxy_async_global();
+                    st_release_gpu(p.ready + pend, ((unsigned long long)p.epoch << 32) | (unsigned)pend_tag);
+                    pend = -1;
+                }
+            };
             for (int k = 0, it = pidx; it < nitems; ++k, it += nP) {
                 const int c = it / hce, hh = it % hce;  // chunk c of the cluster's head hh
                 const bool more = it + nP < nitems;     // this pipeline has a next item
@@ -743,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (more) prefetch(it + nP);
                 if (wt == 0) GDN_TR(c, 44 + 16 * g);
+                if (flat && wt == 0) publish();  // the previous chunk's ring slot
                 const bool wk = wait_bar(&gb[WB_KQ_DONE], k & 1, tmo, abort_flag, 8u);
                 if (wt == 0) GDN_TR(c, 45 + 16 * g);
                 if (!group_all(wk && ship_ok && kq_ok, bar_id, 256)) break;  // also publishes beta, gam
@@ -1070,11 +1141,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar(bar_id, 256);
                 if (wt == 0) GDN_TR(c, 41 + 16 * g);
                 // K K^T / Q K^T of the next chunk (its load has had the whole chunk)
-                if (ctl && kq_ok && more) kq_ok = mma_kq();
+                if (ctl && kq_ok && more) {
+                    GDN_TR(c, 46 + 16 * g);
+                    kq_ok = mma_kq();
+                }
                 if (wi == 1 && more) cumsum();
                 // 6. ship Tw, Tu, P and the vectors into slot c & 1 of head hh's scan
                 //    CTA (cluster rank hh), once that head's chunk c-2 has left it
-                if (wt == 0) {
+                if (wt == 0 && flat) {
+                    // ring mode: into slot c % kRing of the head's ring, once its
+                    // scan CTA has taken chunk c - kRing out of it; the ready tag
+                    // follows at the next chunk's start, when the copies are complete
+                    const int ibh = h0 + hh;
+                    if (c >= kRing)
+                        ship_ok = wait_tag(p.cons + ibh, p.epoch, (unsigned)(c - kRing + 1), tmo, abort_flag, 512u);
+                    GDN_TR(c, 47 + 16 * g);
+                    if (ship_ok) {
+                        fence_proxy_async_global();
+                        const int slot = ibh * kRing + c % kRing;
+                        uint8_t *dst = p.ring + (size_t)slot * kShipBytes;
+                        bulk_store_global(dst, twu, 16384);
+                        bulk_store_global(dst + 16384, ptile, 8192 + 1024);
+                        tma_store_commit();
+                        pend = slot;
+                        pend_tag = c + 1;
+                    }
+                    GDN_TR(c, 42 + 16 * g);
+                } else if (wt == 0) {
                     const int sl = c & 1, fbit = 2 * hh + sl;
                     if (c >= 2) {
                         ship_ok = wait_bar(&gb[WB_RECV_FREE0 + fbit], (rf_par >> fbit) & 1u, tmo, abort_flag, 64u, true);
@@ -1092,7 +1185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     GDN_TR(c, 42 + 16 * g);
                 }
             }
-            if (wt == 0) tma_store_wait_all<0>();
+            if (wt == 0) {
+                tma_store_wait_all<0>();
+                if (flat) publish();
+            }
             if (ctl) {
                 mma_commit(&gb[WB_DRAIN]);
                 mbar_wait(&gb[WB_DRAIN], 0, kCleanupNs);
@@ -1103,7 +1199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __syncwarp();
     tc_fence_before_sync();
-    cluster_sync_all();  // no CTA leaves while its peer may still touch its shared memory
+    if (flat)
+        __syncthreads();
+    else
+        cluster_sync_all();  // no CTA leaves while its peer may still touch its shared memory
     tc_fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, ncols);
 }
@@ -1213,6 +1312,68 @@ bool pick_shape(int BH, int *hc_out, int *nwy_out) {
     return true;
 }
 
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+// Ring mode serves up to half as many heads as there are SMs: each head gets a
+// scan CTA, and the other SMs, at least as many, run WY CTAs for all heads.
+bool ring_fits(int BH, int sms) { return BH >= 1 && 2 * BH <= sms; }
+
+size_t ring_bytes(int BH) {
+    return (size_t)BH * kRing * kShipBytes + (size_t)BH * kRing * sizeof(unsigned long long) +
+           (size_t)BH * sizeof(unsigned long long);
+}
+
+std::atomic<unsigned> g_epoch{0};
+
+// Launches the ring mode if it applies (no forced cluster shape, few enough
+// heads, a 16-byte aligned workspace of ring_bytes); returns -1 if it does not.
+template <int R>
+int launch_ring(const ScanArgs &a, TcParams p, const CUtensorMap &mK, const CUtensorMap &mQ, const CUtensorMap &mV,
+                cudaStream_t stream) {
+    const int BH = p.BH, sms = sm_count();
+    if (g_force_hc > 0 || !ring_fits(BH, sms) || a.ws == nullptr || a.ws_bytes < ring_bytes(BH) ||
+        (reinterpret_cast<uintptr_t>(a.ws) & 15u) != 0)
+        return -1;
+    auto kern = gdn_tc_kernel<R>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    // WY CTAs: three pipelines per head (past which the state chain is the
+    // limit), on the SMs the scan CTAs leave
+    const int nwy = std::max(1, std::min(per_sm * sms - BH, (3 * BH + 1) / 2));
+    if (per_sm < 1 || BH + nwy > per_sm * sms) return -1;
+    uint8_t *ws = static_cast<uint8_t *>(a.ws);
+    p.flat = 1;
+    p.hc = BH;
+    p.nwy = nwy;
+    p.ring = ws;
+    p.ready = reinterpret_cast<unsigned long long *>(ws + (size_t)BH * kRing * kShipBytes);
+    p.cons = p.ready + (size_t)BH * kRing;
+    unsigned e = ++g_epoch;
+    if (e == 0) e = ++g_epoch;
+    p.epoch = e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(BH + nwy));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeCooperative;  // scan and WY CTAs wait on one another
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mK, mQ, mV, p) != cudaSuccess) return GDN_ERR_CUDA;
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 template <int R>
 int launch_r(const ScanArgs &a, cudaStream_t stream) {
     constexpr int NQ = 64 / R;
@@ -1234,10 +1395,17 @@ int launch_r(const ScanArgs &a, cudaStream_t stream) {
     p.scale = a.scale;
     p.flags = a.flags;
     p.timeout_ns = g_timeout_ns;
+    p.BH = BH;
+    p.flat = 0;
+    p.ring = nullptr;
+    p.ready = p.cons = nullptr;
+    p.epoch = 0;
     auto kern = gdn_tc_kernel<R>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return GDN_ERR_CUDA;
+    const int rs = launch_ring<R>(a, p, mK, mQ, mV, stream);
+    if (rs >= 0) return rs;
     int hc = 1, nwy = 1;
     if (g_force_hc > 0) {
         hc = g_force_hc;
@@ -1278,7 +1446,10 @@ bool scan_tc_supported(const ScanArgs &a) {
     return sm100 == 1;
 }
 
-size_t scan_tc_workspace_bytes(const ScanArgs &) { return 0; }
+size_t scan_tc_workspace_bytes(const ScanArgs &a) {
+    const int BH = a.B * a.H;
+    return ring_fits(BH, sm_count()) ? ring_bytes(BH) : 0;
+}
 
 int launch_scan_tc(const ScanArgs &a, cudaStream_t stream) {
     switch (a.r) {
