@@ -124,7 +124,8 @@ constexpr uint32_t kSmemBytes = (S_END > W_END ? S_END : W_END) + 1024;
 constexpr uint32_t V_SEF = 0, V_QS = 64, V_EL = 128;
 // bytes shipped per chunk: Tw | Tu (16 KB), then P (8 KB region) | vectors (1 KB)
 constexpr uint32_t kShipBytes = 16384 + 8192 + 1024;
-constexpr int kRing = 8;  // ring slots per head in ring mode
+constexpr int kRing = 8;           // ring slots per head in ring mode
+constexpr int kMaxRingHeads = 80;  // heads a ring-mode launch serves at most
 static_assert(R_TU == R_TW + 8192 && R_VEC == R_P + 8192, "receive slot layout matches the two shipped blocks");
 
 // scan TMEM columns
@@ -152,7 +153,8 @@ struct Misc {
     float ea[64];     // exp(gam_t - gam_0)             (row factor of A and P)
     float qp[2][64];  // partial q_t^2 sums over the two key-dim halves
     int safe;         // 1 if |gam_t - gam_0| <= 80 for all rows (factorised exponentials)
-    float pad[191];
+    unsigned ccache[80];  // ring mode: chunks each head's scan CTA was last seen to have taken out
+    float pad[111];
 };
 static_assert(sizeof(Misc) == 3072, "Misc layout");
 
@@ -204,14 +206,21 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, unsigne
 // release store) holds this launch's epoch in its high word and at least
 // `need` in its low word.  Gives up early once any CTA has reported an error.
 __device__ __forceinline__ bool wait_tag(const unsigned long long *flag, unsigned epoch, unsigned need,
-                                         unsigned long long timeout_ns, volatile int *abort_flag, unsigned code) {
+                                         unsigned long long timeout_ns, volatile int *abort_flag, unsigned code,
+                                         unsigned *seen = nullptr) {
     unsigned long long v = ld_acquire_gpu(flag);
-    if ((unsigned)(v >> 32) == epoch && (unsigned)v >= need) return true;
+    if ((unsigned)(v >> 32) == epoch && (unsigned)v >= need) {
+        if (seen) *seen = (unsigned)v;
+        return true;
+    }
     const uint64_t t0 = global_timer_ns();
     while (true) {
         __nanosleep(100);
         v = ld_acquire_gpu(flag);
-        if ((unsigned)(v >> 32) == epoch && (unsigned)v >= need) return true;
+        if ((unsigned)(v >> 32) == epoch && (unsigned)v >= need) {
+            if (seen) *seen = (unsigned)v;
+            return true;
+        }
         if (*abort_flag || *reinterpret_cast<volatile unsigned *>(&g_tc_error) != 0u) {
             *abort_flag = 1;
             return false;
@@ -424,22 +433,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // hands each receive slot back to the WY pipeline that fills it
             if (lane == 0 && flat) {
                 // ring mode: fetch each chunk's Tw | Tu | P | vectors from the ring
-                // once its WY pipeline has published it, and report the chunks
-                // taken out so that the ring slots can be refilled
+                // once its WY pipeline has published it (checked ahead, while the
+                // slot is still in use) and the receive slot is free, then report
+                // the chunks taken out so that their ring slots can be refilled
                 const unsigned long long tagc = (unsigned long long)p.epoch << 32;
                 int armed[2] = {0, 0};
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;
-                    if (c >= 2) {
-                        if (!wait_bar(&bars[SB_SLOT_DONE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 16u)) break;
-                        st_release_gpu(p.cons + bh, tagc | (unsigned)(c - 1));  // chunks 0 .. c-2 are out
-                    }
                     const size_t slot = (size_t)bh * kRing + c % kRing;
+                    GDN_TR(c, 11);
                     if (!wait_tag(p.ready + slot, p.epoch, (unsigned)(c + 1), tmo, abort_flag, 256u)) break;
+                    GDN_TR(c, 12);
                     fence_proxy_async_global();
+                    if (c >= 2 && !wait_bar(&bars[SB_SLOT_DONE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 16u)) break;
+                    GDN_TR(c, 13);
                     mbar_arrive_expect_tx(&bars[SB_RECV0 + b], kShipBytes);
                     bulk_load_global(sm + S_RECV0 + b * RS, p.ring + slot * kShipBytes, kShipBytes, &bars[SB_RECV0 + b]);
                     armed[b]++;
+                    if (c >= 2) st_release_gpu(p.cons + bh, tagc | (unsigned)(c - 1));  // chunks 0 .. c-2 are out
                 }
                 for (int b = 0; b < 2; ++b)
                     if (armed[b]) mbar_wait(&bars[SB_RECV0 + b], (armed[b] - 1) & 1, kCleanupNs);
@@ -780,7 +791,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint32_t rf_par = 0;  // thread 0: parity of the next RECV_FREE phase, bit 2 * head + slot
             bool ship_ok = true;
-            int pend = -1, pend_tag = 0;  // thread 0, ring mode: slot and tag still to publish
+            // The thread that ships: thread 0 into the cluster; in ring mode one of
+            // warp 5, which is idle while warps 0 and 1 invert the diagonal blocks
+            // and publishes the previous shipment then.
+            const bool shipper = flat ? wt == 160 : wt == 0;
+            if (flat && shipper)
+                for (int i = 0; i < kMaxRingHeads; ++i) ms->ccache[i] = 0u;
+            int pend = -1, pend_tag = 0;  // ring mode, shipper: slot and tag still to publish
             auto publish = [&]() {        // once the slot's copies are complete
                 if (pend >= 0) {
                     tma_store_wait_all<0>();
@@ -813,7 +830,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (more) prefetch(it + nP);
                 if (wt == 0) GDN_TR(c, 44 + 16 * g);
-                if (flat && wt == 0) publish();  // the previous chunk's ring slot
                 const bool wk = wait_bar(&gb[WB_KQ_DONE], k & 1, tmo, abort_flag, 8u);
                 if (wt == 0) GDN_TR(c, 45 + 16 * g);
                 if (!group_all(wk && ship_ok && kq_ok, bar_id, 256)) break;  // also publishes beta, gam
@@ -967,6 +983,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = j + 1; i < 16; ++i) pp[i] += AF[(16 * db + i) * kAS + 16 * db + j] * xs[j];
                     }
+                } else if (flat && shipper) {
+                    publish();  // the previous chunk's ring slot
                 }
                 named_bar(bar_id, 256);
                 if (wt == 0) GDN_TR(c, 37 + 16 * g);
@@ -1025,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // T_top[row][c8..] is (k = row, n = c8..) of the MN-major B1; T_bot[row][c8..]
                     // is (m = 32 + row, k = c8..) of the K-major A2: the same offsets
                     uint8_t *opnd = gbase + (which ? G_A2 : G_B1);
-                    if (wt == 0) tma_store_wait_read<0>();
+                    if (shipper) tma_store_wait_read<0>();
                     named_bar(bar_id, 256);  // the previous shipment has left the Tw / Tu tile
                     *reinterpret_cast<uint4 *>(opnd + sw128_offset(row, c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     *reinterpret_cast<uint4 *>(opnd + 4096 + sw128_offset(row, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -1148,13 +1166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (wi == 1 && more) cumsum();
                 // 6. ship Tw, Tu, P and the vectors into slot c & 1 of head hh's scan
                 //    CTA (cluster rank hh), once that head's chunk c-2 has left it
-                if (wt == 0 && flat) {
+                if (shipper && flat) {
                     // ring mode: into slot c % kRing of the head's ring, once its
-                    // scan CTA has taken chunk c - kRing out of it; the ready tag
-                    // follows at the next chunk's start, when the copies are complete
+                    // scan CTA has taken chunk c - kRing out of it (known without a
+                    // global load while the last count seen suffices); the ready tag
+                    // follows in the next chunk, when the copies are complete
                     const int ibh = h0 + hh;
-                    if (c >= kRing)
-                        ship_ok = wait_tag(p.cons + ibh, p.epoch, (unsigned)(c - kRing + 1), tmo, abort_flag, 512u);
+                    const unsigned need = (unsigned)(c - kRing + 1);
+                    if (c >= kRing && ms->ccache[ibh] < need) {
+                        unsigned seen = 0;
+                        ship_ok = wait_tag(p.cons + ibh, p.epoch, need, tmo, abort_flag, 512u, &seen);
+                        if (ship_ok) ms->ccache[ibh] = seen;
+                    }
                     GDN_TR(c, 47 + 16 * g);
                     if (ship_ok) {
                         fence_proxy_async_global();
@@ -1167,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pend_tag = c + 1;
                     }
                     GDN_TR(c, 42 + 16 * g);
-                } else if (wt == 0) {
+                } else if (shipper) {  // cluster mode: thread 0
                     const int sl = c & 1, fbit = 2 * hh + sl;
                     if (c >= 2) {
                         ship_ok = wait_bar(&gb[WB_RECV_FREE0 + fbit], (rf_par >> fbit) & 1u, tmo, abort_flag, 64u, true);
@@ -1185,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     GDN_TR(c, 42 + 16 * g);
                 }
             }
-            if (wt == 0) {
+            if (shipper) {
                 tma_store_wait_all<0>();
                 if (flat) publish();
             }
@@ -1321,7 +1344,7 @@ int sm_count() {
 
 // Ring mode serves up to half as many heads as there are SMs: each head gets a
 // scan CTA, and the other SMs, at least as many, run WY CTAs for all heads.
-bool ring_fits(int BH, int sms) { return BH >= 1 && 2 * BH <= sms; }
+bool ring_fits(int BH, int sms) { return BH >= 1 && BH <= kMaxRingHeads && 2 * BH <= sms; }
 
 size_t ring_bytes(int BH) {
     return (size_t)BH * kRing * kShipBytes + (size_t)BH * kRing * sizeof(unsigned long long) +
