@@ -62,6 +62,15 @@ def gdn_flops_per_token_head(D, C):
     return 6 * D * D + 5 * C * D + C * C // 3
 
 
+def make_workspace(binding, w, dev):
+    """The library's device scratch for workload w (None when it needs none),
+    allocated once so that no step allocates."""
+    import torch
+    r = w.r if w.kind == "deltaproduct" else 1
+    n = binding.workspace_bytes(w.B, w.H, w.T, w.D, w.D, w.chunk, r)
+    return torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+
+
 def max_over_ranks(x, world, device):
     """The largest of each rank's value (a step time): the job is as slow as
     its slowest replica.  Needs an initialised process group when world > 1."""
@@ -225,10 +234,11 @@ def run_ours(args, rank, world, local_rank):
     inp_cpu = w.make()
     d = {k: v.to(dev) for k, v in inp_cpu.items()}
     o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+    ws = make_workspace(binding, w, dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o)
+        binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o, workspace=ws)
 
     def barrier():
         if world > 1:
@@ -294,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
         stream.wait_event(ev_in)
         if done_out[j] is not None:
             stream.wait_event(done_out[j])
-        binding.gdn_chunk_fwd(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], chunk=w.chunk, o=oo)
+        binding.gdn_chunk_fwd(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], chunk=w.chunk, o=oo, workspace=ws)
         ek = torch.cuda.Event()
         ek.record(stream)
         done_k[j] = ek
@@ -390,17 +400,19 @@ def secondary(args, dev):
         w = WORKLOADS[name]
         d = {k: v.to(dev) for k, v in w.make().items()}
         o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+        wsw = make_workspace(binding, w, dev)
         if w.kind == "gdn":
-            fn = lambda: binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o)
+            fn = lambda: binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o,
+                                               workspace=wsw)
             nbytes = w.B * w.H * w.T * gdn_bytes_per_token_head(w.D)
         else:
             fn = lambda: binding.deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"],
-                                                        chunk=w.chunk, o=o)
+                                                        chunk=w.chunk, o=o, workspace=wsw)
             nbytes = w.B * w.H * w.T * (w.D * (1 + 2 * w.r) * 2 + 2 * w.r + 4 + 2 * w.D)
         ms = timeit(fn)
         out[name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
                      "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
-        del d, o
+        del d, o, wsw
         torch.cuda.empty_cache()
     w = WORKLOADS["cam_b2n32760h16d128_bf16"]
     d = {k: (v.to(dev) if v is not None else None) for k, v in w.make().items()}
@@ -414,8 +426,9 @@ def secondary(args, dev):
     pre_ms = timeit(prep)
     C = w.H * w.D
     prep_bytes = w.B * w.T * (6 * C * 2 + 2 * 16 * 4 + 2 * w.H * 4)
+    wsc = make_workspace(binding, w, dev)
     scan_ms = timeit(lambda: binding.gdn_chunk_fwd(outs[0], outs[1], outs[2], d["beta"], d["g"],
-                                                   chunk=w.chunk, l2norm=True, o=o))
+                                                   chunk=w.chunk, l2norm=True, o=o, workspace=wsc))
     out[w.name] = {"prep_ms": pre_ms, "prep_gbs": prep_bytes / (pre_ms * 1e-3) / 1e9,
                    "prep_hbm_frac": prep_bytes / (pre_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                    "scan_ms": scan_ms, "tokens_per_s": w.B * w.T / ((pre_ms + scan_ms) * 1e-3)}
