@@ -25,7 +25,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
-           "gdn_set_cluster_shape")
+           "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -57,6 +57,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdn_chunk_fwd_workspace_bytes.restype = sz
         lib.gdn_chunk_fwd.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp, sz, vp]
         lib.gdn_chunk_fwd.restype = i
+        lib.gdn_chunk_fwd_noalloc.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp]
+        lib.gdn_chunk_fwd_noalloc.restype = i
         lib.deltaproduct_chunk_fwd.argtypes = [vp] * 8 + [i] * 7 + [f, u, i, vp, sz, vp]
         lib.deltaproduct_chunk_fwd.restype = i
         lib.cam_prep_fwd.argtypes = [vp] * 9 + [f] + [vp] * 5 + [i] * 4 + [f, f, i, vp]
@@ -157,6 +159,34 @@ def gdn_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_state=False
     simt=True takes the CUDA-core path even where the tensor-core one applies."""
     return _scan("gdn_chunk_fwd", q, k, v, beta, g, None, initial_state, output_final_state, chunk,
                  scale, l2norm, o, workspace, stream, simt)
+
+
+def gdn_chunk_fwd_noalloc(q, k, v, beta, g, initial_state=None, output_final_state=False, chunk=64,
+                          scale=1.0, l2norm=False, o=None, stream=None):
+    """gdn_chunk_fwd through the allocation-free entry point: the library uses
+    its own fixed scratch array instead of a workspace (B*H <= 64 heads where
+    the tensor-core path needs one).  Calls must not overlap on the GPU."""
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, T, Dk), dt)
+    _check(k, "k", (B, H, T, Dk), dt)
+    _check(v, "v", (B, H, T, Dv), dt)
+    _check(beta, "beta", (B, H, T), dt)
+    _check(g, "g", (B, H, T), torch.float32)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (B, H, Dk, Dv), torch.float32)
+    if o is None:
+        o = torch.empty(B, H, T, Dv, dtype=dt, device=q.device)
+    _check(o, "o", (B, H, T, Dv), dt)
+    sf = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=q.device) if output_final_state else None
+    flags = GDN_QK_L2NORM if l2norm else 0
+    st = load().gdn_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state),
+                                      _ptr(o), _ptr(sf), B, H, T, Dk, Dv, chunk, float(scale), flags, code,
+                                      _stream(stream))
+    _raise("gdn_chunk_fwd_noalloc", st)
+    return o, sf
 
 
 def deltaproduct_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_state=False, chunk=64,

@@ -106,6 +106,28 @@ int gdn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
     return run_scan(a, stream);
 }
 
+int gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *beta,
+                          const float *g, const float *initial_state, void *o, float *final_state,
+                          int B, int H, int T, int Dk, int Dv, int chunk, float scale,
+                          unsigned flags, int dtype, void *stream) {
+    // gdn_chunk_fwd with the library's own fixed scratch in place of a
+    // caller-provided workspace; nothing is allocated
+    gdn::ScanArgs a{q, k, v, beta, g, initial_state, o, final_state, B, H, T, 1, Dk, Dv,
+                    chunk, scale, flags, dtype, nullptr, 0};
+    const int st = check_scan(a);
+    if (st != GDN_OK) return st;
+    if (scan_workspace(a) > 0) {
+        void *ws = nullptr;
+        size_t bytes = 0;
+        const int ss = gdn::scan_tc_noalloc_scratch(&ws, &bytes);
+        if (ss != GDN_OK) return ss;
+        if (scan_workspace(a) > bytes) return GDN_ERR_WORKSPACE;  // more heads than the array serves
+        a.ws = ws;
+        a.ws_bytes = bytes;
+    }
+    return run_scan(a, stream);
+}
+
 int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
                            const float *g, const float *initial_state, void *o,
                            float *final_state, int B, int H, int T, int r, int Dk, int Dv,

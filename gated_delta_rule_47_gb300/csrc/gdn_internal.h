@@ -47,6 +47,9 @@ int scan_tc_read_clear_error(cudaStream_t stream);
 int scan_tc_set_wait_limit(unsigned long long polls);
 // Cluster shape of the tcgen05 path (heads and WY CTAs per cluster); 0, 0 = automatic.
 int scan_tc_set_cluster_shape(int hc, int nwy);
+// Device address and size of the fixed scratch array behind
+// gdn_chunk_fwd_noalloc (set up on the current device at the first call).
+int scan_tc_noalloc_scratch(void **ptr, size_t *bytes);
 
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the streamed camera prep (GDN_OK or GDN_ERR_TIMEOUT).

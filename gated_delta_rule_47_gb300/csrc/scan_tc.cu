@@ -1346,10 +1346,19 @@ int sm_count() {
 // scan CTA, and the other SMs, at least as many, run WY CTAs for all heads.
 bool ring_fits(int BH, int sms) { return BH >= 1 && BH <= kMaxRingHeads && 2 * BH <= sms; }
 
-size_t ring_bytes(int BH) {
+constexpr size_t ring_bytes(int BH) {
     return (size_t)BH * kRing * kShipBytes + (size_t)BH * kRing * sizeof(unsigned long long) +
            (size_t)BH * sizeof(unsigned long long);
 }
+
+// Scratch of the allocation-free entry point: the ring of up to kNoAllocHeads
+// heads (13.1 MB on every GPU that loads the library, until the process
+// exits).  It is zero when the module loads and is never cleared: each tag in
+// it carries the launch that wrote it, so one call's leftovers are never read
+// as another's.
+constexpr int kNoAllocHeads = 64;
+constexpr size_t kNoAllocBytes = ring_bytes(kNoAllocHeads);
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
 std::atomic<unsigned> g_epoch{0};
 
@@ -1489,6 +1498,28 @@ int scan_tc_read_clear_error(cudaStream_t stream) {
     if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
     if (v && cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
     return v ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
+int scan_tc_noalloc_scratch(void **ptr, size_t *bytes) {
+    // the device address of g_noalloc_scratch, looked up once per device with
+    // that device current (its host-side name is not a device address)
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return GDN_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    *bytes = kNoAllocBytes;
+    return GDN_OK;
 }
 
 int scan_tc_set_cluster_shape(int hc, int nwy) {

@@ -107,6 +107,33 @@ int gdn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
                   void *stream);
 
 /*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate
+ * device memory: code running where cudaMalloc is off limits (inside a host
+ * callback, from a plug-in whose host owns every allocation, or under a memory
+ * budget fixed in advance) cannot provide the workspace that gdn_chunk_fwd may
+ * ask for.  This entry point takes no workspace and allocates nothing; when
+ * the tensor-core path needs scratch it uses an array inside the library, of
+ * fixed size (13.1 MB, enough for B*H <= 64 heads), which every GPU that loads
+ * the library holds until the process exits.  The paper has no counterpart:
+ * this is a deployment convenience only.
+ *
+ * Arguments, layouts and results are those of gdn_chunk_fwd.
+ *   Returns GDN_ERR_WORKSPACE for sizes whose scratch would not fit the array
+ *   (more than 64 heads on the tensor-core path at a head count that uses the
+ *   scratch).
+ * The first call on a device looks up the array's device address with that
+ * device current (no allocation); make that first call before any stream
+ * capture.  All calls share the one array and nothing clears it between calls
+ * (nothing in it has to start at zero: every tag it holds names the launch
+ * that wrote it).  Two calls that overlap on the GPU, on different streams,
+ * race on it: serialise them.
+ */
+int gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *beta,
+                          const float *g, const float *initial_state, void *o, float *final_state,
+                          int B, int H, int T, int Dk, int Dv, int chunk, float scale,
+                          unsigned flags, int dtype, void *stream);
+
+/*
  * deltaproduct_chunk_fwd -- DeltaProduct forward: per token the decay exp(g_t)
  * is applied once, then r corrections in order j = 0..r-1,
  *     S <- (I - beta_{t,j} k_{t,j} k_{t,j}^T) S + beta_{t,j} k_{t,j} v_{t,j}^T,
