@@ -69,8 +69,8 @@ int gdn_version(void);
 
 /*
  * Bytes of device workspace gdn_chunk_fwd / deltaproduct_chunk_fwd need for
- * these sizes (r = 1 for GDN).  May be 0.  Returns (size_t)-1 for sizes the
- * library rejects.
+ * these sizes (r = 1 for GDN) on the current device.  May be 0.  Returns
+ * (size_t)-1 for sizes the library rejects.
  */
 size_t gdn_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int chunk,
                                      int dtype);
@@ -96,7 +96,14 @@ size_t gdn_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv,
  *   dtype   GDN_F32 or GDN_BF16
  *   Dk, Dv  64 or 128 each
  *   workspace / workspace_bytes: device scratch of at least
- *           gdn_chunk_fwd_workspace_bytes(...) bytes (NULL if that is 0)
+ *           gdn_chunk_fwd_workspace_bytes(...) bytes (NULL if that is 0),
+ *           16-byte aligned.  The tensor-core path uses it, for B*H up to
+ *           min(80, SMs/2) heads, as a ring through which the chunk-local
+ *           results travel to the state scan (about 205 KB per head).  Its
+ *           contents need no initialisation and are not meaningful after
+ *           the call; calls that may overlap on the GPU need separate
+ *           workspaces.  A smaller one is GDN_ERR_WORKSPACE; one that is
+ *           not 16-byte aligned makes the call run without the ring.
  * T = 0 or B*H = 0 is valid and enqueues nothing (final_state, if given,
  * receives initial_state or zeros).
  */
