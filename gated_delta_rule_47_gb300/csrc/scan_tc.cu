@@ -144,6 +144,7 @@ static_assert(2 * WB_PER_GROUP <= 32, "WY barriers fit their 256 bytes");
 
 // Per-chunk vectors of one WY pipeline.
 struct Misc {
+    alignas(16) unsigned long long tag[2];  // ring mode: the ready tag being published
     float beta[64];   // beta of each row (0 past the end)
     float gam[64];    // within-chunk cumulative log-decay
     float n[64];      // 1/||k_s|| with GDN_QK_L2NORM, else 1
@@ -154,7 +155,7 @@ struct Misc {
     float qp[2][64];  // partial q_t^2 sums over the two key-dim halves
     int safe;         // 1 if |gam_t - gam_0| <= 80 for all rows (factorised exponentials)
     unsigned ccache[80];  // ring mode: chunks each head's scan CTA was last seen to have taken out
-    float pad[111];
+    float pad[107];
 };
 static_assert(sizeof(Misc) == 3072, "Misc layout");
 
@@ -176,7 +177,7 @@ struct TcParams {
     // c % kRing of the head's ring in global memory instead of a cluster copy.
     int flat;
     uint8_t *ring;                // [BH][kRing] slots of kShipBytes
-    unsigned long long *ready;    // [BH][kRing]: epoch << 32 | (chunk + 1) of the slot's contents
+    unsigned long long *ready;    // [BH][kRing] x 16 B: epoch << 32 | (chunk + 1) of the slot's contents
     unsigned long long *cons;     // [BH]: epoch << 32 | chunks the scan CTA has taken out of its ring
     unsigned epoch;               // tag of this launch, never 0
 };
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int b = c & 1;
                     const size_t slot = (size_t)bh * kRing + c % kRing;
                     GDN_TR(c, 11);
-                    if (!wait_tag(p.ready + slot, p.epoch, (unsigned)(c + 1), tmo, abort_flag, 256u)) break;
+                    if (!wait_tag(p.ready + 2 * slot, p.epoch, (unsigned)(c + 1), tmo, abort_flag, 256u)) break;
                     GDN_TR(c, 12);
                     fence_proxy_async_global();
                     if (c >= 2 && !wait_bar(&bars[SB_SLOT_DONE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 16u)) break;
@@ -791,18 +792,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint32_t rf_par = 0;  // thread 0: parity of the next RECV_FREE phase, bit 2 * head + slot
             bool ship_ok = true;
-            // The thread that ships: thread 0 into the cluster; in ring mode one of
-            // warp 5, which is idle while warps 0 and 1 invert the diagonal blocks
+            // The thread that ships: thread 0 into the cluster; in ring mode lane 0
+            // of warp 5, which is idle while warps 0 and 1 form the chunk's factors
             // and publishes the previous shipment then.
             const bool shipper = flat ? wt == 160 : wt == 0;
             if (flat && shipper)
                 for (int i = 0; i < kMaxRingHeads; ++i) ms->ccache[i] = 0u;
             int pend = -1, pend_tag = 0;  // ring mode, shipper: slot and tag still to publish
-            auto publish = [&]() {        // once the slot's copies are complete
+            // Publishing a slot: once its copies are complete, the ready tag goes
+            // out as one more bulk copy (16 B from shared memory), which costs the
+            // thread far less than a release store.
+            auto publish = [&]() {
                 if (pend >= 0) {
-                    tma_store_wait_all<0>();
-                    fence_proxy_async_global();
-                    st_release_gpu(p.ready + pend, ((unsigned long long)p.epoch << 32) | (unsigned)pend_tag);
+                    tma_store_wait_all<0>();  // the slot's bytes, and the previous tag, are written
+                    ms->tag[0] = ((unsigned long long)p.epoch << 32) | (unsigned)pend_tag;
+                    ms->tag[1] = 0ull;
+                    fence_proxy_async_smem();
+                    bulk_store_global(p.ready + 2 * pend, ms->tag, 16);
+                    tma_store_commit();
                     pend = -1;
                 }
             };
@@ -886,6 +893,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ms->ea[wt] = __expf(gi - g0);
                     vec[V_SEF + wt] = __expf(gl - gi) * ni;
                     vec[V_QS + wt] = wt < NQ ? __expf(ms->gam[wt * R + R - 1]) * mi : 0.f;
+                } else if (flat && shipper) {
+                    publish();  // the previous chunk's ring slot, while warps 0-1 form the factors
                 }
                 named_bar(bar_id, 256);
                 if (wt == 0) GDN_TR(c, 35 + 16 * g);
@@ -983,8 +992,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = j + 1; i < 16; ++i) pp[i] += AF[(16 * db + i) * kAS + 16 * db + j] * xs[j];
                     }
-                } else if (flat && shipper) {
-                    publish();  // the previous chunk's ring slot
                 }
                 named_bar(bar_id, 256);
                 if (wt == 0) GDN_TR(c, 37 + 16 * g);
@@ -1347,8 +1354,7 @@ int sm_count() {
 bool ring_fits(int BH, int sms) { return BH >= 1 && BH <= kMaxRingHeads && 2 * BH <= sms; }
 
 constexpr size_t ring_bytes(int BH) {
-    return (size_t)BH * kRing * kShipBytes + (size_t)BH * kRing * sizeof(unsigned long long) +
-           (size_t)BH * sizeof(unsigned long long);
+    return (size_t)BH * kRing * kShipBytes + (size_t)BH * kRing * 16 + (size_t)BH * sizeof(unsigned long long);
 }
 
 // Scratch of the allocation-free entry point: the ring of up to kNoAllocHeads
@@ -1387,7 +1393,7 @@ int launch_ring(const ScanArgs &a, TcParams p, const CUtensorMap &mK, const CUte
     p.nwy = nwy;
     p.ring = ws;
     p.ready = reinterpret_cast<unsigned long long *>(ws + (size_t)BH * kRing * kShipBytes);
-    p.cons = p.ready + (size_t)BH * kRing;
+    p.cons = p.ready + (size_t)BH * kRing * 2;
     unsigned e = ++g_epoch;
     if (e == 0) e = ++g_epoch;
     p.epoch = e;
