@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t qt = sbase + (b ? S_Q1 : S_Q0);
                     const uint32_t tvn = tmem + TM_VN;
                     // U^T = V^T Tu^T
-                    if (!wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 2u, true)) break;
+                    if (!wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
                     if (!wait_bar(&bars[SB_VFULL], c & 1, tmo, abort_flag, 2u)) break;
                     GDN_TR(c, 0);
                     tc_fence_after_sync();
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idW = idesc_bf16(128, 64, true, false);
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;
-                    if (!wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 2u, true)) break;
+                    if (!wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
                     if (!wait_bar(&bars[SB_FULLKQ0 + b], (c >> 1) & 1, tmo, abort_flag, 2u)) break;
                     if (c >= 1 && !wait_bar(&bars[SB_WT_READY], (c - 1) & 1, tmo, abort_flag, 2u)) break;
                     tc_fence_after_sync();
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int c = 0; c < NT; ++c) {
                 const int b = c & 1;
-                bool w = wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 128u, true);
+                bool w = wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 128u);
                 if (w) w = wait_bar(&bars[SB_W_DONE], c & 1, tmo, abort_flag, 128u);
                 if (w && c >= 1) w = wait_bar(&bars[SB_VN_DONE], (c - 1) & 1, tmo, abort_flag, 128u);
                 if (!group_all(w, 4, 128)) { ok = false; break; }
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < NT; ++c) {
                 const int b = c & 1;
                 const float *vec = reinterpret_cast<const float *>(sm + S_RECV0 + b * RS + R_VEC);
-                bool w = wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 4u, true);
+                bool w = wait_bar(&bars[SB_RECV0 + b], (c >> 1) & 1, tmo, abort_flag, 4u);
                 if (w && c >= 1) w = wait_bar(&bars[SB_UPD_DONE], (c - 1) & 1, tmo, abort_flag, 4u);
                 if (!group_all(w, 3, 256)) { ok = false; break; }
                 if (si == 0) GDN_TR(c, 3);
