@@ -193,8 +193,8 @@ def test_tensor_core_cluster_shapes(hc, nwy):
 
 @pytest.mark.parametrize("B,H,T", [(1, 1, 200), (1, 1, 64), (3, 1, 130)])
 def test_tensor_core_few_heads_automatic_shape(B, H, T):
-    """With fewer heads than a cluster holds, the scan CTAs past the last head
-    only take part in the cluster barriers; results are unaffected."""
+    """One to three heads (ring mode, with many more WY pipelines than heads,
+    most of them without items); results are unaffected."""
     inp = gdn_inputs(B, H, T, 128, 128, seed=B * 7 + T, dtype="bf16", initial_state=True)
     o, sf = run_gdn(inp)
     assert binding.device_error() == 0
@@ -228,21 +228,93 @@ def test_tensor_core_l2norm_and_scale():
     assert rel_err(sf, rs) <= TOL_BF16
 
 
-def test_bounded_wait_gives_up_and_context_survives():
-    """A 1-microsecond wait limit makes the kernel's first mbarrier wait run
-    out: the call reports GDN_ERR_TIMEOUT through the device error word, and
-    with the default limit restored the next call is correct."""
+@pytest.mark.parametrize("shape", [(0, 0), (1, 1)])
+def test_bounded_wait_gives_up_and_context_survives(shape):
+    """A 1-microsecond wait limit makes the kernel's first wait run out (ring
+    mode, and a forced cluster shape): the call reports GDN_ERR_TIMEOUT through
+    the device error word, and with the default limit restored the next call
+    is correct."""
     inp = gdn_inputs(1, 2, 1024, 128, 128, seed=3, dtype="bf16")
     d = to_dev(inp)
     assert binding.device_error() == 0
     try:
+        binding.set_cluster_shape(*shape)
         binding.set_wait_limit(1)
         binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"])
         assert binding.device_error() == 6
     finally:
         binding.set_wait_limit(0)
+        binding.set_cluster_shape(0, 0)
     assert binding.device_error() == 0
     o, _ = binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"])
     torch.cuda.synchronize()
     ro, _ = ref_gdn(inp)
     assert rel_err(o, ro) <= TOL_BF16
+
+
+# --- ring mode: one cooperative grid, WY results through per-head rings of 8
+# --- slots in the workspace (the default for up to min(80, SMs / 2) heads).
+
+def test_ring_and_cluster_modes_agree():
+    """T = 700 gives 11 chunks per head, so every ring wraps and its slots are
+    refilled only after the scan has taken them out."""
+    inp = gdn_inputs(2, 5, 700, 128, 128, seed=123, dtype="bf16", initial_state=True)
+    d = to_dev(inp)
+    args = (d["q"], d["k"], d["v"], d["beta"], d["g"], d["initial_state"])
+    assert binding.workspace_bytes(2, 5, 700, 128, 128) > 0
+    o_ring, s_ring = binding.gdn_chunk_fwd(*args, output_final_state=True)
+    try:
+        binding.set_cluster_shape(2, 2)
+        o_cl, s_cl = binding.gdn_chunk_fwd(*args, output_final_state=True)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_cluster_shape(0, 0)
+    assert binding.device_error() == 0
+    ro, rs = ref_gdn(inp)
+    for o, sf in ((o_ring, s_ring), (o_cl, s_cl)):
+        assert rel_err(o, ro) <= TOL_BF16
+        assert rel_err(sf, rs) <= TOL_BF16
+
+
+def test_ring_workspace_with_stale_contents():
+    """The ring's tags carry the launch that wrote them: a workspace full of
+    random bytes, then one already used by a call on other inputs, both give
+    the right results."""
+    B, H, T = 1, 4, 600
+    ws = torch.randint(0, 256, (binding.workspace_bytes(B, H, T, 128, 128),), dtype=torch.uint8, device="cuda")
+    for seed in (7, 8):
+        inp = gdn_inputs(B, H, T, 128, 128, seed=seed, dtype="bf16")
+        d = to_dev(inp)
+        o, _ = binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        ro, _ = ref_gdn(inp)
+        assert rel_err(o, ro) <= TOL_BF16
+
+
+def test_misaligned_workspace_runs_without_the_ring():
+    B, H, T = 1, 2, 300
+    n = binding.workspace_bytes(B, H, T, 128, 128)
+    buf = torch.empty(n + 16, dtype=torch.uint8, device="cuda")
+    inp = gdn_inputs(B, H, T, 128, 128, seed=9, dtype="bf16")
+    d = to_dev(inp)
+    o, _ = binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], workspace=buf[8:8 + n])
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ro, _ = ref_gdn(inp)
+    assert rel_err(o, ro) <= TOL_BF16
+
+
+def test_ring_mode_head_limit():
+    """The most heads ring mode takes on this device, and one more (which goes
+    to the cluster mode and needs no workspace)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    most = min(80, sms // 2)
+    for BH in (most, most + 1):
+        inp = gdn_inputs(1, BH, 100, 128, 128, seed=BH, dtype="bf16", initial_state=True)
+        assert (binding.workspace_bytes(1, BH, 100, 128, 128) > 0) == (BH == most)
+        o, sf = run_gdn(inp)
+        assert binding.device_error() == 0
+        ro, rs = ref_gdn(inp)
+        assert rel_err(o, ro) <= TOL_BF16
+        assert rel_err(sf, rs) <= TOL_BF16
