@@ -62,8 +62,8 @@ int g_force_hc = 0, g_force_nwy = 0;               // cluster shape override (0:
 __device__ unsigned long long *g_trace = nullptr;
 #define GDN_TR(c, ev)                                                          \
     do {                                                                       \
-        if (tr_on && g_trace != nullptr && (c) < 1024)                         \
-            g_trace[(size_t)(c) * 64 + (ev)] = clock64();                      \
+        if (tr_on && tr_buf != nullptr && (c) < 1024)                          \
+            tr_buf[(size_t)(c) * 64 + (ev)] = clock64();                       \
     } while (0)
 #else
 #define GDN_TR(c, ev) \
@@ -291,6 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_scan = (int)rank < hc;
     bool tr_on = blockIdx.x < (unsigned)(hc + nwy) && rank == 0;
     (void)tr_on;
+#ifdef GDN_TRACE
+    unsigned long long *const tr_buf = g_trace;  // read once: a global load per event would skew the timeline
+#endif
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + (is_scan ? S_BAR : W_BAR));
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + (is_scan ? S_FLAGS : W_FLAGS));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + (is_scan ? S_FLAGS : W_FLAGS) + 4);
