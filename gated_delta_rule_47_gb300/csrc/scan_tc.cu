@@ -10,31 +10,39 @@
 //
 //   KQ   = [K; Q] K^T                   rows 0..63 K K^T, rows 64.. Q K^T
 //   A[t][s] = beta_t exp(g_t - g_s) (k_t . k_s), s < t      (CUDA cores)
-//   T    = (I + A)^-1                                       (CUDA cores, blocked)
+//   T    = (I + A)^-1     16x16 diagonal blocks and 16-level merges on the CUDA
+//                         cores, the 32-level merge on the tensor cores (bf16
+//                         hi/lo products)
 //   W^T  = K^T (T diag(beta e^g))^T,  U^T = V^T (T diag(beta))^T
 //   Vn^T = U^T - S^T W^T                (v_new of the WY form, negated-A MMA)
 //   O^T  = diag-scaled S^T Q^T + Vn^T P^T,  P[t][s] = e^{g_t-g_s} q_t.k_s (s <= t)
 //   S^T <- e^{g_last} S^T + (Vn^T diag(e^{g_last - g_s})) K
 //
 // The pages run these as separate launches with HBM round trips.  Here one
-// 2-CTA cluster owns one (batch, head):
+// launch holds two kinds of CTA, one per SM:
 //
-//   CTA rank 1 ("WY")   computes the chunk-local products, which need no state:
-//                       two independent 8-warp pipelines take alternate
-//                       chunks (K K^T / Q K^T by MMA, A, the blocked inverse,
-//                       Tw/Tu, P) and ship Tw, Tu, P and the per-row factors
-//                       into CTA 0's shared memory with cp.async.bulk over
-//                       the cluster (DSMEM).
-//   CTA rank 0 ("scan") runs the sequential part: the fp32 state S^T lives in
-//                       tensor memory for the whole sequence; a TMA warp
-//                       streams K, Q, V; one thread issues the chain's MMAs
-//                       and another W^T = K^T Tw^T; 8 epilogue warps turn S^T
-//                       and Vn^T into bf16 operands; 4 aux warps convert W^T
-//                       and write the output rows of the previous chunk.
+//   "WY" CTAs   compute the chunk-local products, which need no state: two
+//               independent 8-warp pipelines per CTA take (chunk, head) items
+//               (K K^T / Q K^T by MMA, A, the blocked inverse, Tw/Tu, P) and
+//               ship Tw, Tu, P and the per-row factors to the head's scan CTA.
+//   scan CTAs   (one per head) run the sequential part: the fp32 state S^T lives
+//               in tensor memory for the whole sequence; a TMA warp streams K,
+//               Q, V; one thread issues the chain's MMAs and another W^T =
+//               K^T Tw^T; 8 epilogue warps turn S^T and Vn^T into bf16
+//               operands; 4 aux warps convert W^T and write the output rows of
+//               the previous chunk.
 //
-// Only q, k, v, beta, g are read from HBM and o written.  Every mbarrier wait
-// is bounded in wall time; on expiry the CTA sets an error word, stops
-// issuing work, drains what is in flight, frees TMEM and exits.
+// Two ways to ship.  Ring mode (the default for up to min(80, SMs/2) heads):
+// one cooperative grid of all the scan CTAs and as many WY CTAs as SMs remain
+// (up to 1.5 per head); an item goes through slot c % 8 of its head's ring in
+// the workspace, with a tag published after it and a count of the chunks taken
+// out published back.  Cluster mode (more heads, or a forced shape): clusters
+// of hc scan CTAs and nwy WY CTAs, an item going straight into the scan CTA's
+// shared memory with cp.async.bulk over the cluster (DSMEM).
+//
+// Only q, k, v, beta, g are read from HBM and o written (the ring stays in L2).
+// Every wait is bounded in wall time; on expiry the CTA sets an error word,
+// stops issuing work, drains what is in flight, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -678,9 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================== WY CTA
         {
             // ---------------------------------- WY pipeline g: warps 0..7 / 8..15.
-            // Pipeline pidx = 2 (rank - hc) + g of the cluster takes items
-            // pidx, pidx + 2 nwy, ...; item i is chunk i / hce of the cluster's
-            // head i % hce, shipped to that head's scan CTA.  One thread of warp 6
+            // Pipeline pidx = 2 (rank - hc) + g of the cluster (in ring mode, of
+            // the grid) takes items pidx, pidx + 2 nwy, ...; item i is chunk
+            // i / hce of head h0 + i % hce, shipped to that head's scan CTA.  One thread of warp 6
             // also loads K/Q with TMA and issues the K K^T / Q K^T MMA: the next
             // item's load starts as soon as this item's tile and TMEM rows have
             // been read, its MMA once this item's Tw / Tu are built.
