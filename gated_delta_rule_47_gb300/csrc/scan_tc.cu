@@ -140,8 +140,8 @@ static_assert(R_TU == R_TW + 8192 && R_VEC == R_P + 8192, "receive slot layout m
 constexpr uint32_t TM_S = 0, TM_VN = 128, TM_W = 192, TM_O10 = 256, TM_O11 = 320, TM_O20 = 384, TM_O21 = 448;
 
 enum ScanBar {
-    SB_FULLKQ0, SB_FULLKQ1, SB_VFULL, SB_VFREE, SB_S_READY, SB_VN_DONE, SB_VN_READY, SB_UPD_DONE,
-    SB_STG_FREE0, SB_STG_FREE1, SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_W_DONE, SB_WT_READY,
+    SB_FULLKQ0, SB_FULLKQ1, SB_VFULL, SB_S_READY, SB_VN_DONE, SB_VN_READY, SB_UPD_DONE,
+    SB_SLOT_DONE0, SB_SLOT_DONE1, SB_RECV0, SB_RECV1, SB_W_DONE, SB_WT_READY,
     SB_DRAIN, SB_WDRAIN, SB_OFREE0, SB_OFREE1, SB_VN2_READY, SB_NUM
 };
 // Per WY pipeline: FULL, KQ_DONE, DRAIN, then RECV_FREE for each (scan CTA of
@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int armed[2] = {0, 0}, armed_v = 0;
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;
-                    if (c >= 2 && !wait_bar(&bars[SB_STG_FREE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 1u)) break;
+                    // stage b held chunk c-2, whose MMAs all completed before its slot's release
+                    if (c >= 2 && !wait_bar(&bars[SB_SLOT_DONE0 + b], ((c - 2) >> 1) & 1, tmo, abort_flag, 1u)) break;
                     uint8_t *kt = sm + (b ? S_K1 : S_K0);
                     uint8_t *qt = sm + (b ? S_Q1 : S_Q0);
                     mbar_arrive_expect_tx(&bars[SB_FULLKQ0 + b], 16384 + 2 * NQ * 128);
@@ -365,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(qt, &mQ, &bars[SB_FULLKQ0 + b], 0, c * NQ, bh);
                     tma_load_3d(qt + NQ * 128, &mQ, &bars[SB_FULLKQ0 + b], 64, c * NQ, bh);
                     armed[b]++;
-                    if (c >= 1 && !wait_bar(&bars[SB_VFREE], (c - 1) & 1, tmo, abort_flag, 1u)) break;
+                    // V(c-1) has been read once Vn(c-1), issued after U(c-1), is complete
+                    if (c >= 1 && !wait_bar(&bars[SB_VN_DONE], (c - 1) & 1, tmo, abort_flag, 1u)) break;
                     mbar_arrive_expect_tx(&bars[SB_VFULL], 16384);
                     tma_load_3d(sm + S_V, &mV, &bars[SB_VFULL], 0, c * 64, bh);
                     tma_load_3d(sm + S_V + 8192, &mV, &bars[SB_VFULL], 64, c * 64, bh);
@@ -397,7 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ss(tvn, smem_desc(sbase + S_V + ks * 2048, 8192, 1024),
                                     smem_desc(recv + R_TU + ks * 32, 16, 1024), idU, ks > 0);
-                    mma_commit(&bars[SB_VFREE]);
                     // Vn^T = U^T - S^T W^T
                     if (!wait_bar(&bars[SB_WT_READY], c & 1, tmo, abort_flag, 2u)) break;
                     if (!wait_bar(&bars[SB_S_READY], c & 1, tmo, abort_flag, 2u)) break;
@@ -434,7 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ss(tmem + (b ? TM_O21 : TM_O20), smem_desc(sbase + S_VN + ks * 32, 16, 1024),
                                     smem_desc(recv + R_P + ks * 32, 16, 1024), idO, ks > 0);
-                    mma_commit(&bars[SB_STG_FREE0 + b]);
                     mma_commit(&bars[SB_SLOT_DONE0 + b]);
                 }
                 mma_commit(&bars[SB_DRAIN]);
