@@ -39,18 +39,6 @@ struct F8 {
     float x[8];
 };
 
-__device__ __forceinline__ F8 load8(const __nv_bfloat16 *p) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
-    F8 r;
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        r.x[2 * i] = __uint_as_float(w[i] << 16);
-        r.x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-    return r;
-}
-
 __device__ __forceinline__ F8 load8(const float *p) {
     const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
     const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
@@ -377,13 +365,16 @@ __global__ void __launch_bounds__(32 * (2 * kStageTok + 1), 1) cam_prep_stream_k
     // squares through shared memory
     const int tw = w >> 1, hf = w & 1;
     int j = 0;
-    const int lanes_per_head = D / 8;  // divides 32
+    const int lanes_per_head = D / 8;              // a power of two that divides 32
+    const int lph_shift = __ffs(lanes_per_head) - 1;
+    const size_t ND = (size_t)N * D;
     for (long st = blockIdx.x; st < nstages; st += gridDim.x, ++j) {
         const int buf = j & 1;
         if (!cam_wait(&full[buf], (j >> 1) & 1)) break;
         const long tok = st * kStageTok + tw;
         if (tok < BN) {
             const int b = (int)(tok / N), n = (int)(tok % N);
+            const size_t obase = (size_t)b * H * ND + (size_t)n * D;  // head 0, dim 0 of this token's outputs
             const uint8_t *tb = tok_base(buf, tw);
             const __nv_bfloat16 *sq_ = reinterpret_cast<const __nv_bfloat16 *>(tb);
             const __nv_bfloat16 *sk_ = reinterpret_cast<const __nv_bfloat16 *>(tb + kRowBytes);
@@ -429,7 +420,7 @@ __global__ void __launch_bounds__(32 * (2 * kStageTok + 1), 1) cam_prep_stream_k
                 const int gi = lane + 32 * (2 * i + hf);
                 const bool ok = gi < G8;
                 const int e0 = gi * 8;
-                const int h = e0 / D, d0 = e0 % D;
+                const int h = gi >> lph_shift, d0 = (gi & (lanes_per_head - 1)) << 3;
                 float pre = 0.f, post = 0.f;
                 if (ok) {
                     Raw8<__nv_bfloat16> a, c, e;
@@ -467,10 +458,17 @@ __global__ void __launch_bounds__(32 * (2 * kStageTok + 1), 1) cam_prep_stream_k
                             }
                         }
                     } else {
+                        // dr is a multiple of 8 and Dh of 4: 16-byte aligned rows
                         const int dr = d0 - Dh;
+                        const float4 c0 = *reinterpret_cast<const float4 *>(cs + dr);
+                        const float4 c1 = *reinterpret_cast<const float4 *>(cs + dr + 4);
+                        const float4 s0 = *reinterpret_cast<const float4 *>(sn + dr);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(sn + dr + 4);
+                        const float cva[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        const float sva[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
                         for (int t = 0; t < 8; ++t) {
-                            const float cv = cs[dr + t], sv = sn[dr + t];
+                            const float cv = cva[t], sv = sva[t];
                             oq.x[t] = q.x[t] * cv + q.x[t ^ 1] * sv;
                             ok8.x[t] = k.x[t] * cv + k.x[t ^ 1] * sv;
                             ov.x[t] = v.x[t] * cv + v.x[t ^ 1] * sv;
@@ -478,7 +476,7 @@ __global__ void __launch_bounds__(32 * (2 * kStageTok + 1), 1) cam_prep_stream_k
                     }
 #pragma unroll
                     for (int t = 0; t < 8; ++t) post += ok8.x[t] * ok8.x[t];
-                    const size_t ob = (((size_t)b * H + h) * N + n) * D + d0;
+                    const size_t ob = obase + (size_t)h * ND + d0;
                     store8(static_cast<__nv_bfloat16 *>(p.q_out) + ob, oq);
                     store8(static_cast<__nv_bfloat16 *>(p.k_out) + ob, ok8);
                     store8(static_cast<__nv_bfloat16 *>(p.v_out) + ob, ov);
@@ -487,7 +485,7 @@ __global__ void __launch_bounds__(32 * (2 * kStageTok + 1), 1) cam_prep_stream_k
                     pre += __shfl_xor_sync(0xffffffffu, pre, off);
                     post += __shfl_xor_sync(0xffffffffu, post, off);
                 }
-                if (ok && (lane % lanes_per_head) == 0) {
+                if (ok && (lane & (lanes_per_head - 1)) == 0) {
                     const size_t si = ((size_t)b * H + h) * N + n;
                     if (p.k_pre_sq) p.k_pre_sq[si] = pre;
                     if (p.k_post_sq) p.k_post_sq[si] = post;
