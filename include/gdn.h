@@ -222,7 +222,10 @@ int gdn_set_wait_limit(unsigned long long polls);
  * thread-block cluster holds heads_per_cluster scan CTAs (one (batch, head)
  * each) and wy_ctas_per_cluster CTAs that compute the chunk-local WY products
  * for them (two pipelines each, taking the cluster's (head, chunk) items in
- * turn).  0, 0 restores the automatic choice: the shape with the most WY
+ * turn).  A forced shape also turns off the ring mode (one cooperative grid
+ * whose WY results travel through the workspace), which is otherwise the
+ * default up to min(80, SMs/2) heads.  0, 0 restores the automatic choice:
+ * the ring mode where it applies, else the cluster shape with the most WY
  * pipelines per head whose clusters are all resident on the device at once.
  * Returns GDN_ERR_INVALID_ARG unless 1 <= heads_per_cluster <= 4,
  * wy_ctas_per_cluster >= 1 and their sum <= 16.  A shape whose clusters cannot
