@@ -6,7 +6,7 @@ only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 
 Two independent restatements of the same definitions live here:
 
-* ``gdn_fwd`` / ``deltaproduct_fwd`` / ``cam_prep_fwd`` call the plain C
+* ``gdn_fwd`` / ``deltaproduct_fwd`` / ``cam_scan_fwd`` / ``cam_prep_fwd`` call the plain C
   implementation in ``gdn_oracle.c`` (compiled on first use with gcc and
   OpenMP, parallel over heads or tokens).
 * ``mirror`` holds a pure numpy restatement, token by token, used on small
@@ -62,6 +62,8 @@ def _load():
             lib.oracle_gdn_fwd.restype = i
             lib.oracle_deltaproduct_fwd.argtypes = [_dp] * 8 + [i] * 6 + [d, i]
             lib.oracle_deltaproduct_fwd.restype = i
+            lib.oracle_cam_scan_fwd.argtypes = [_dp] * 8 + [i] * 6 + [d, i, i]
+            lib.oracle_cam_scan_fwd.restype = i
             lib.oracle_cam_prep_fwd.argtypes = [_dp] * 9 + [d] + [_dp] * 5 + [i] * 4 + [d, d]
             lib.oracle_cam_prep_fwd.restype = i
             lib.oracle_max_threads.restype = i
@@ -133,6 +135,38 @@ def deltaproduct_fwd(q, k, v, beta, g, initial_state=None, scale=1.0, l2norm=Fal
                                          float(scale), int(bool(l2norm)))
     if rc != 0:
         raise MemoryError("oracle_deltaproduct_fwd failed")
+    return o, sf
+
+
+def cam_scan_fwd(q, k, v, beta, decay, initial_state=None, scale=1.0, reverse=False, l2norm=False,
+                 return_final_state=True):
+    """fp64 frame-level camera scan (fused_cam_gdn.py, ``_cam_scan_kernel``).
+
+    q, k: [B,H,N,Dk]; v: [B,H,N,Dv]; beta: [B,H,N]; decay: [B,H,F] factors,
+    N = F * S.  Per frame: S <- d_f S, then S += K^T diag(beta)(V - K S) with
+    every token predicting from the same decayed state, and o = scale S^T q
+    after the frame's update.  reverse=True is the anti-causal mode (frames
+    last to first, each reading only the frames after it); it takes no state.
+    Returns (o [B,H,N,Dv], final_state [B,H,Dk,Dv] or None).
+    """
+    q, k, v, beta, decay = map(_f64, (q, k, v, beta, decay))
+    s0 = _f64(initial_state)
+    B, H, N, Dk = q.shape
+    Dv = v.shape[-1]
+    F = decay.shape[-1]
+    assert decay.shape == (B, H, F) and F > 0 and N % F == 0
+    assert k.shape == (B, H, N, Dk) and v.shape == (B, H, N, Dv) and beta.shape == (B, H, N)
+    if reverse and (s0 is not None or return_final_state):
+        if s0 is not None:
+            raise ValueError("the reverse mode takes no initial state")
+        return_final_state = False
+    o = np.empty((B, H, N, Dv), np.float64)
+    sf = np.empty((B, H, Dk, Dv), np.float64) if return_final_state else None
+    rc = _load().oracle_cam_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(s0),
+                                     _ptr(o), _ptr(sf), B, H, F, N // F, Dk, Dv, float(scale),
+                                     int(bool(reverse)), int(bool(l2norm)))
+    if rc != 0:
+        raise MemoryError("oracle_cam_scan_fwd failed")
     return o, sf
 
 

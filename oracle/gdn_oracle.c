@@ -21,6 +21,18 @@
  *    sub-steps j = 0..r-1, each with its own k_{t,j}, v_{t,j}, beta_{t,j};
  *    the output reads the state after the last sub-step.
  *
+ *  - Frame-level camera scan (fused_cam_gdn.py, `_cam_scan_kernel`,
+ *    `_torch_cam_scan_single_chunk` and `_torch_cam_scan_reference`): the
+ *    tokens form F frames of S tokens; per frame the state is decayed once by
+ *    the frame's factor, then every token of the frame predicts from that
+ *    same decayed state and all S corrections are added at once,
+ *        S <- d_f S ;  S <- S + K_f^T diag(beta_f) (V_f - K_f S)
+ *    and every token of the frame reads the state after the frame's update,
+ *        o_s = scale * S^T q_s.
+ *    The reverse mode (the page's REVERSE=1, `flip_and_shift`) runs the frames
+ *    from last to first, each frame's output reading the state built from
+ *    the frames after it only (the last frame reads zero).
+ *
  *  - Camera prep (fused_cam_gdn.py, `_torch_cam_prep_reference` and
  *    `_cam_prep_kernel`): full-C RMSNorm (C = H*D) with per-channel weight on
  *    q and k, ReLU on q and k, K-scale on k, a 4x4 projection out = P*in on
@@ -186,6 +198,94 @@ int oracle_deltaproduct_fwd(const double *q, const double *k, const double *v,
         free(S);
         free(p);
         free(kt);
+        free(qt);
+    }
+    return failed ? -1 : 0;
+}
+
+/* One frame's joint update: P = K S with the state as it is on entry (every
+ * row predicts from the same S), then S += sum_s beta_s k_s (v_s - p_s)^T. */
+static void frame_update(double *S, const double *K, const double *V, const double *beta,
+                         int S_len, int Dk, int Dv, double *P) {
+    for (int s = 0; s < S_len; ++s) {
+        double *p = P + (size_t)s * Dv;
+        for (int j = 0; j < Dv; ++j) p[j] = 0.0;
+        for (int i = 0; i < Dk; ++i) {
+            const double ki = K[(size_t)s * Dk + i];
+            const double *row = S + (size_t)i * Dv;
+            for (int j = 0; j < Dv; ++j) p[j] += row[j] * ki;
+        }
+    }
+    for (int s = 0; s < S_len; ++s) {
+        const double *p = P + (size_t)s * Dv;
+        const double *vs = V + (size_t)s * Dv;
+        for (int i = 0; i < Dk; ++i) {
+            const double c = beta[s] * K[(size_t)s * Dk + i];
+            double *row = S + (size_t)i * Dv;
+            for (int j = 0; j < Dv; ++j) row[j] += c * (vs[j] - p[j]);
+        }
+    }
+}
+
+/*
+ * Frame-level camera scan, frame by frame.
+ *   q, k : [B,H,F*S_len,Dk]     v, o : [B,H,F*S_len,Dv]     beta : [B,H,F*S_len]
+ *   decay: [B,H,F] multiplicative factor of each frame (not its log)
+ *   s0 / s_final : [B,H,Dk,Dv] or NULL (forward only; NULL s0 = zero state)
+ *   reverse != 0: frames from last to first; the output of frame f reads the
+ *   state built from frames f+1 .. F-1, and frame f's factor decays the state
+ *   when frame f is taken in (the page's REVERSE=1).
+ *   l2norm != 0 normalises q and k per token before use.
+ * Returns 0, -1 if scratch memory could not be allocated, -2 if a state is
+ * passed in reverse mode.
+ */
+int oracle_cam_scan_fwd(const double *q, const double *k, const double *v, const double *beta,
+                        const double *decay, const double *s0, double *o, double *s_final,
+                        int B, int H, int F, int S_len, int Dk, int Dv, double scale,
+                        int reverse, int l2norm) {
+    if (reverse && (s0 || s_final)) return -2;
+    const int BH = B * H;
+    const long N = (long)F * S_len;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = (double *)malloc(sizeof(double) * (size_t)Dk * Dv);
+        double *P = (double *)malloc(sizeof(double) * (size_t)(S_len > 0 ? S_len : 1) * Dv);
+        double *Kf = (double *)malloc(sizeof(double) * (size_t)(S_len > 0 ? S_len : 1) * Dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        if (!S || !P || !Kf || !qt) {
+            failed |= 1;
+        } else {
+            if (s0)
+                memcpy(S, s0 + (size_t)bh * Dk * Dv, sizeof(double) * (size_t)Dk * Dv);
+            else
+                memset(S, 0, sizeof(double) * (size_t)Dk * Dv);
+            for (int it = 0; it < F; ++it) {
+                /* frame whose keys / values enter now, and frame whose queries read */
+                const int qf = reverse ? F - 1 - it : it;
+                const int kf = reverse ? F - it : it; /* reverse: none at it = 0 */
+                if (!reverse || it > 0) {
+                    const double d = decay[(size_t)bh * F + kf];
+                    for (size_t e = 0; e < (size_t)Dk * Dv; ++e) S[e] *= d;
+                    const size_t t0 = (size_t)bh * N + (size_t)kf * S_len;
+                    memcpy(Kf, k + t0 * Dk, sizeof(double) * (size_t)S_len * Dk);
+                    if (l2norm)
+                        for (int s = 0; s < S_len; ++s) l2_normalise(Kf + (size_t)s * Dk, Dk);
+                    frame_update(S, Kf, v + t0 * Dv, beta + t0, S_len, Dk, Dv, P);
+                }
+                const size_t q0 = (size_t)bh * N + (size_t)qf * S_len;
+                for (int s = 0; s < S_len; ++s) {
+                    memcpy(qt, q + (q0 + s) * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(qt, Dk);
+                    read_out(S, qt, scale, Dk, Dv, o + (q0 + s) * Dv);
+                }
+            }
+            if (s_final)
+                memcpy(s_final + (size_t)bh * Dk * Dv, S, sizeof(double) * (size_t)Dk * Dv);
+        }
+        free(S);
+        free(P);
+        free(Kf);
         free(qt);
     }
     return failed ? -1 : 0;

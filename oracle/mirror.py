@@ -57,6 +57,36 @@ def deltaproduct_fwd(q, k, v, beta, g, initial_state=None, scale=1.0, l2norm=Fal
     return o, S_all
 
 
+def cam_scan_fwd(q, k, v, beta, decay, initial_state=None, scale=1.0, reverse=False, l2norm=False):
+    """Frame-level scan: per frame S <- d_f S, then the joint update
+    S <- S + K_f^T diag(beta_f) (V_f - K_f S), and o = scale S^T q after it.
+    reverse: frames last to first, frame f reading frames f+1.. only."""
+    q, k, v, beta, decay = (np.asarray(a, np.float64) for a in (q, k, v, beta, decay))
+    B, H, N, Dk = q.shape
+    Dv = v.shape[-1]
+    F = decay.shape[-1]
+    S_len = N // F
+    if l2norm:
+        q, k = _unit(q), _unit(k)
+    o = np.zeros((B, H, N, Dv))
+    S_all = np.zeros((B, H, Dk, Dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((Dk, Dv)) if initial_state is None else np.array(initial_state[b, h], np.float64)
+            order = range(F - 1, -1, -1) if reverse else range(F)
+            for f in order:
+                take = f + 1 if reverse else f  # frame whose keys enter before frame f reads
+                if take < F:
+                    sl = slice(take * S_len, (take + 1) * S_len)
+                    Kf, Vf, bf = k[b, h, sl], v[b, h, sl], beta[b, h, sl]
+                    S = decay[b, h, take] * S
+                    S = S + Kf.T @ (bf[:, None] * (Vf - Kf @ S))
+                ql = slice(f * S_len, (f + 1) * S_len)
+                o[b, h, ql] = scale * (q[b, h, ql] @ S)
+            S_all[b, h] = S
+    return o, S_all
+
+
 def rope_tables(N, D_half, base=10000.0):
     """Interleaved cos/sin tables: cos[n,2i]=cos[n,2i+1]=cos th, sin[n,2i]=-sin th,
     sin[n,2i+1]=sin th, th = n * base^(-2i/D_half)."""
