@@ -89,6 +89,21 @@ def whole_job_tokens(tokens_per_replica, world):
     return tokens_per_replica * world
 
 
+def workload_config(w, world):
+    """The `config` object of both arms' JSON lines: the workload by name and
+    sizes (the same keys whichever arm runs it)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "Dk": w.D, "Dv": w.D, "chunk": w.chunk,
+            "state": "fp32", "parallelism": f"replicas x{world} (no collective)",
+            "l2": "no flush: each step touches 270 MB > 129 MB L2"}
+
+
+def median_step_ms(events):
+    """Per-step times from consecutive CUDA events recorded between steps on
+    the launching stream: (median, mean) in ms."""
+    per = [a.elapsed_time(b) for a, b in zip(events[:-1], events[1:])]
+    return statistics.median(per), sum(per) / len(per)
+
+
 def source_sha():
     h = hashlib.sha256()
     for name in SCAN_SOURCES:
@@ -210,9 +225,9 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; q,k unit-norm, v~N(0,1), beta=sigmoid(N), g=logsigmoid(N)/16)",
-        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "chunk": w.chunk,
-                   "sample_heads": n_heads},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+        "config": workload_config(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "cpu_count": os.cpu_count(),
+                         "kind": "oracle",
                          "sample": f"{n_heads} of {w.B * w.H} heads, full T={w.T}, per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -247,8 +262,6 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
-    ev_s = torch.cuda.Event(enable_timing=True)
-    ev_e = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     # The sampler runs over a busy window of at least `clock_window` seconds:
@@ -262,17 +275,19 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         torch.cuda.synchronize()
         n0 = binding.launch_count()
-        ev_s.record(stream)
-        for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evs[0].record(stream)
+        for i in range(args.steps):
             step()
-        ev_e.record(stream)
+            evs[i + 1].record(stream)
         launches = binding.launch_count() - n0  # kernels the library launched in the timed steps
         torch.cuda.synchronize()
         while time.perf_counter() - t_win < args.clock_window:
             step()
             torch.cuda.synchronize()
     barrier()
-    ms = max_over_ranks(ev_s.elapsed_time(ev_e) / args.steps, world, dev)
+    med_ms, mean_ms = median_step_ms(evs)
+    ms = max_over_ranks(med_ms, world, dev)
     tokens_per_step = whole_job_tokens(w.B * w.T, world)
     value = tokens_per_step / (ms * 1e-3)
 
@@ -345,12 +360,12 @@ def run_ours(args, rank, world, local_rank):
     traffic, traffic_kernel = ncu_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "ms_mean": mean_ms,
+        "timing": "median of per-step CUDA-event times on the launching stream",
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,k unit-norm, v~N(0,1), beta=sigmoid(N), g=logsigmoid(N)/16)",
-        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "T": w.T, "Dk": w.D, "Dv": w.D,
-                   "chunk": w.chunk, "state": "fp32", "parallelism": f"replicas x{world} (no collective)",
-                   "l2": "no flush: each step touches 270 MB > 129 MB L2"},
+        "config": workload_config(w, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs",
@@ -366,7 +381,8 @@ def run_ours(args, rank, world, local_rank):
         line["secondary"] = secondary(args, dev)
     if not args.no_cpu_baseline and world == 1:
         v, dt, threads = cpu_oracle_sample(inp_cpu, args.ref_heads, w.B, w.H, w.T)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "cpu_count": os.cpu_count(),
+                                "kind": "oracle",
                                 "sample": f"{args.ref_heads} of {w.B * w.H} heads, full T={w.T} "
                                           f"({dt:.1f} s), scaled to the whole workload"}
     print(json.dumps(line), flush=True)
@@ -381,20 +397,28 @@ def secondary(args, dev):
     from gated_delta_rule_47_gb300.inputs import WORKLOADS
     peaks, _ = measured_peaks()
     out = {}
-    steps = max(3, min(args.steps, 10))
+    steps = max(10, min(args.steps, 50))
 
     def timeit(fn):
-        for _ in range(2):
+        for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record()
+        for i in range(steps):
             fn()
-        b.record()
+            evs[i + 1].record()
         torch.cuda.synchronize()
-        return a.elapsed_time(b) / steps
+        return median_step_ms(evs)[0]
+
+    # the small fp32 workload (CUDA-core path; launch-latency bound, reported only)
+    w = WORKLOADS["gdn_tiny_f32"]
+    d = {k: v.to(dev) for k, v in w.make().items()}
+    o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.float32, device=dev)
+    ms = timeit(lambda: binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], chunk=w.chunk, o=o))
+    out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                   "hbm_frac": w.B * w.H * w.T * gdn_bytes_per_token_head(w.D, 4, 4) / (ms * 1e-3) / 1e9
+                   / peaks["hbm_gbs"], "dtype": "f32"}
 
     for name in ("gdn_long_b1h32t32768d128_bf16", "deltaproduct_r2_b4h16t4096d128_bf16"):
         w = WORKLOADS[name]
@@ -438,7 +462,7 @@ def secondary(args, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--ref-heads", type=int, default=64,

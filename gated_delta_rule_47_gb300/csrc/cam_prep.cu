@@ -2,13 +2,21 @@
 // and `_torch_cam_prep_reference`), one pass over q, k and v.
 //
 // The pages run a separate full-C RMS reduction first and then one 1-warp
-// program per (b, n, h).  Here one warp owns one token: it loads the token's
-// whole q, k, v rows (C = H*D elements each) into registers with 16-byte
-// loads, reduces the two sums of squares with shuffles, and writes the three
-// outputs in the head-major [B,H,N,D] layout the scan reads.  A CTA holds 8
-// consecutive tokens so that the per-(b,h,n) norm statistics leave as 32-byte
-// runs and the rotary tables of the 8 positions are staged once in shared
-// memory.  The path is HBM-bound: 3 reads + 3 writes of C elements per token.
+// program per (b, n, h).  Here a token is handled whole, so the two full-C
+// sums of squares never leave the chip, and the three outputs are written in
+// the head-major [B,H,N,D] layout the scan reads.  Two kernels:
+//
+//  - cam_prep_stream_kernel (bf16, C <= 2048, rotary tables given): one
+//    persistent CTA per SM walks stages of 8 consecutive tokens; a producer
+//    warp bulk-copies each stage's q, k, v rows, projections and rotary rows
+//    into one of two shared-memory buffers while 16 compute warps, two per
+//    token (each with half of the token's heads), work on the other buffer.
+//  - cam_prep_kernel (everything else: fp32 tensors, or angles formed in the
+//    kernel): one warp per token holds the token's rows in registers from
+//    16-byte loads, 8 tokens per CTA, the rotary rows of the 8 positions
+//    staged once in shared memory.
+//
+// The path is HBM-bound: 3 reads + 3 writes of C elements per token.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -27,7 +35,7 @@ constexpr int kMaxDh = 128;    // D/2 <= 128
 struct CamParams {
     const void *q_raw, *k_raw, *v_raw;
     const float *q_norm_w, *k_norm_w, *proj_q, *proj_kv, *rope_cos, *rope_sin;
-    float log2_base;
+    double log2_base;  // log2(rope_base) in double: a float one would shift angles at large positions
     void *q_out, *k_out, *v_out;
     float *k_pre_sq, *k_post_sq;
     int B, N, H, D;
@@ -121,7 +129,7 @@ __global__ void __launch_bounds__(32 * kTokPerCta, 2) cam_prep_kernel(CamParams 
             // th = n * base^(-2i/Dh), i = d/2; the product and its reduction
             // modulo 2*pi are done in double so large positions keep precision.
             const int i2 = d >> 1;
-            const double inv_freq = exp2((double)p.log2_base * (-2.0 * i2 / (double)Dh));
+            const double inv_freq = exp2(p.log2_base * (-2.0 * i2 / (double)Dh));
             double th = (double)n * inv_freq;
             const double two_pi = 6.283185307179586476925286766559;
             th -= two_pi * rint(th / two_pi);
@@ -515,7 +523,7 @@ int launch_stream(const CamParams &p, long BN, cudaStream_t stream) {
 template <typename T>
 int launch_t(const CamArgs &a, cudaStream_t stream) {
     CamParams p{a.q_raw, a.k_raw, a.v_raw, a.q_norm_w, a.k_norm_w, a.proj_q, a.proj_kv,
-                a.rope_cos, a.rope_sin, log2f(a.rope_base), a.q_out, a.k_out, a.v_out,
+                a.rope_cos, a.rope_sin, log2((double)a.rope_base), a.q_out, a.k_out, a.v_out,
                 a.k_pre_sq, a.k_post_sq, a.B, a.N, a.H, a.D, a.k_scale, a.eps};
     const long BN = (long)a.B * a.N;
     if (sizeof(T) == 2 && a.rope_cos != nullptr && a.H * a.D <= kMaxC && (a.D / 2) % 4 == 0) {

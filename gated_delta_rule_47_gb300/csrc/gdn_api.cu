@@ -44,12 +44,14 @@ size_t scan_workspace(const gdn::ScanArgs &a) {
     return gdn::scan_tc_supported(a) ? gdn::scan_tc_workspace_bytes(a) : 0;
 }
 
-int run_scan(gdn::ScanArgs &a, void *stream_v) {
+// need_ws = false lets a call without enough workspace run anyway: the
+// tensor-core path then takes its cluster mode, which needs no scratch.
+int run_scan(gdn::ScanArgs &a, void *stream_v, bool need_ws = true) {
     int st = check_scan(a);
     if (st != GDN_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     const size_t need = scan_workspace(a);
-    if (need > 0 && (a.ws == nullptr || a.ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    if (need_ws && need > 0 && (a.ws == nullptr || a.ws_bytes < need)) return GDN_ERR_WORKSPACE;
     if ((long long)a.B * a.H == 0) return GDN_OK;
     if (a.T == 0) {
         if (a.sf) {
@@ -121,11 +123,14 @@ int gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const voi
         size_t bytes = 0;
         const int ss = gdn::scan_tc_noalloc_scratch(&ws, &bytes);
         if (ss != GDN_OK) return ss;
-        if (scan_workspace(a) > bytes) return GDN_ERR_WORKSPACE;  // more heads than the array serves
-        a.ws = ws;
-        a.ws_bytes = bytes;
+        // more heads than the array's ring serves: no scratch, so the
+        // tensor-core path runs in its cluster mode
+        if (scan_workspace(a) <= bytes) {
+            a.ws = ws;
+            a.ws_bytes = bytes;
+        }
     }
-    return run_scan(a, stream);
+    return run_scan(a, stream, false);
 }
 
 int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,

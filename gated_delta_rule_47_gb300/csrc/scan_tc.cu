@@ -450,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the chunks taken out so that their ring slots can be refilled
                 const unsigned long long tagc = (unsigned long long)p.epoch << 32;
                 int armed[2] = {0, 0};
-                for (int c = 0; c < NT; ++c) {
+                int c = 0;
+                for (; c < NT; ++c) {
                     const int b = c & 1;
                     const size_t slot = (size_t)bh * kRing + c % kRing;
                     GDN_TR(c, 11);
@@ -466,6 +467,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int b = 0; b < 2; ++b)
                     if (armed[b]) mbar_wait(&bars[SB_RECV0 + b], (armed[b] - 1) & 1, kCleanupNs);
+                if (c == NT) {
+                    // Every chunk of this head has been published and taken out, so
+                    // nothing reads or writes its tags again in this launch: zero
+                    // them, so that the next launch on this workspace starts from
+                    // clean tags even when it carries the same epoch (a replayed
+                    // CUDA graph freezes the epoch it was captured with).
+                    for (int s = 0; s < kRing; ++s) p.ready[2 * ((size_t)bh * kRing + s)] = 0ull;
+                    p.cons[bh] = 0ull;
+                }
             } else if (lane == 0) {
                 for (int c = 0; c < NT; ++c) {
                     const int b = c & 1;

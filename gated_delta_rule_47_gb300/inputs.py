@@ -61,6 +61,34 @@ def gdn_inputs(B, H, T, Dk, Dv, seed, dtype="bf16", g_mu=0.0, g_div=16.0, r=None
     return out
 
 
+def mixed_decay(B, H, T, seed, r=1, chunk_rows=64, strong=2.0):
+    """Per-token log-decay g [B,H,T] fp32 whose 64-row chunks cycle through
+    three regimes, so that one head holds all of them: strong forgetting
+    (about -strong*r per token: a chunk's cumulative decay spans well over
+    80 nats), the workloads' weak decay logsigmoid(N(0,1))/16, and a chunk
+    whose cumulative decay spans about 70 nats.  r is the number of rows per
+    token (DeltaProduct sub-steps), so that chunks are counted in rows."""
+    gen = torch.Generator().manual_seed(int(seed))
+    z = torch.randn(B, H, T, generator=gen)
+    regime = ((torch.arange(T) * r) // chunk_rows) % 3
+    tok_per_chunk = chunk_rows / r
+    strong_g = -strong * r * (1.0 + 0.25 * z.abs())
+    weak_g = torch.nn.functional.logsigmoid(z) / 16.0
+    border_g = torch.full_like(z, -70.0 / tok_per_chunk)
+    g = torch.where(regime == 0, strong_g, torch.where(regime == 1, weak_g, border_g))
+    return g.float().contiguous()
+
+
+def orthonormal_keys(B, H, T, D, seed):
+    """[B,H,T,D] fp32 keys whose T <= D rows per head are orthonormal (rows of
+    a random orthogonal matrix from the QR factorisation of a Gaussian)."""
+    assert T <= D
+    gen = torch.Generator().manual_seed(int(seed))
+    a = torch.randn(B * H, D, D, generator=gen, dtype=torch.float64)
+    qm, _ = torch.linalg.qr(a)
+    return qm[:, :T, :].reshape(B, H, T, D).float().contiguous()
+
+
 def quaternion_rotations(n: int, gen: torch.Generator) -> torch.Tensor:
     """n rotation matrices from uniformly random unit quaternions (normalised
     4-D Gaussians), fp64, shape [n,3,3]."""
@@ -198,6 +226,6 @@ def split_heads_np(x, idx):
     return flat[list(idx)][None]
 
 
-__all__ = ["gdn_inputs", "cam_inputs", "rope_tables", "se3_poses", "se3_inverse",
+__all__ = ["gdn_inputs", "cam_inputs", "mixed_decay", "orthonormal_keys", "rope_tables", "se3_poses", "se3_inverse",
            "quaternion_rotations", "WORKLOADS", "Workload", "to_f64", "split_heads_np",
            "torch_dtype"]

@@ -102,8 +102,12 @@ size_t gdn_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv,
  *           results travel to the state scan (about 205 KB per head).  Its
  *           contents need no initialisation and are not meaningful after
  *           the call; calls that may overlap on the GPU need separate
- *           workspaces.  A smaller one is GDN_ERR_WORKSPACE; one that is
- *           not 16-byte aligned makes the call run without the ring.
+ *           workspaces.  A call that completes leaves the ring's tags zeroed,
+ *           so a workspace may be reused by launches that carry the same tag
+ *           epoch (replays of one captured CUDA graph); after a call that
+ *           ended in GDN_ERR_TIMEOUT, zero the workspace before such reuse.
+ *           A smaller workspace is GDN_ERR_WORKSPACE; one that is not
+ *           16-byte aligned makes the call run without the ring.
  * T = 0 or B*H = 0 is valid and enqueues nothing (final_state, if given,
  * receives initial_state or zeros).
  */
@@ -124,16 +128,17 @@ int gdn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
  * the library holds until the process exits.  The paper has no counterpart:
  * this is a deployment convenience only.
  *
- * Arguments, layouts and results are those of gdn_chunk_fwd.
- *   Returns GDN_ERR_WORKSPACE for sizes whose scratch would not fit the array
- *   (more than 64 heads on the tensor-core path at a head count that uses the
- *   scratch).
+ * Arguments, layouts and results are those of gdn_chunk_fwd.  For head
+ * counts whose ring would not fit the array (more than 64 heads), the
+ * tensor-core path runs in its cluster mode, which needs no scratch; no size
+ * that gdn_chunk_fwd accepts is refused for want of scratch.
  * The first call on a device looks up the array's device address with that
  * device current (no allocation); make that first call before any stream
- * capture.  All calls share the one array and nothing clears it between calls
- * (nothing in it has to start at zero: every tag it holds names the launch
- * that wrote it).  Two calls that overlap on the GPU, on different streams,
- * race on it: serialise them.
+ * capture.  All calls share the one array, which keeps the last call's
+ * contents; nothing in it has to start at zero (every tag it holds names the
+ * launch that wrote it, and a call that completes zeroes the tags it used).
+ * Two calls that overlap on the GPU, on different streams, race on it:
+ * serialise them.
  */
 int gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *beta,
                           const float *g, const float *initial_state, void *o, float *final_state,

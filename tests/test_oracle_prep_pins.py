@@ -176,3 +176,62 @@ def test_k_norm_outputs_are_sums_of_squares():
     assert np.allclose(pre, (kn ** 2).sum(-1).transpose(0, 2, 1), rtol=1e-13)
     infl = oracle.inflation_sq(pre, post)
     assert np.all(infl > 0)
+
+
+def _rope_probe(D=16, N=8):
+    """v_raw with a known pair (a, b) = (0.6, -0.8) in every rotary pair and
+    ones elsewhere; P = I so the projection half passes through.  v skips the
+    norm, ReLU and K-scale, so v_out's rotary half is the rotation alone."""
+    B, H = 1, 1
+    v = np.ones((B, N, H, D))
+    v[..., D // 2::2] = 0.6
+    v[..., D // 2 + 1::2] = -0.8
+    q = np.ones((B, N, H, D))
+    k = np.ones((B, N, H, D))
+    return q, k, v, eye_proj(B, N)
+
+
+def _hand_rotated_pair(n, i):
+    """fused_cam_gdn.py, ``_prepare_ucpe_rope_tables``: pair i of position n
+    turns by th = n * 10000^(-2i/(D/2)); with D = 16, D/2 = 8, that is
+    n * 10^-i (10000^(-2i/8) = 10^(-i)), so th(1, 0) = 1 rad and th(7, 3) =
+    0.007 rad.  y[2i] = x[2i] cos th - x[2i+1] sin th,
+    y[2i+1] = x[2i] sin th + x[2i+1] cos th."""
+    th = n * [1.0, 0.1, 0.01, 0.001][i]
+    a, b = 0.6, -0.8
+    return a * np.cos(th) - b * np.sin(th), a * np.sin(th) + b * np.cos(th)
+
+
+def test_rope_direction_and_frequencies_against_hand_computed_angles():
+    """Pins the rotation's sign and its frequency schedule at positions 1 and
+    7, pairs 0 and 3, with the angles the oracle forms itself and with the
+    interleaved tables the workloads pass.  A flipped sine, or i in place of
+    2i in the exponent (th(7,3) = 7 * 10000^(-3/8) = 0.22 rad), fails."""
+    from gated_delta_rule_47_gb300.inputs import rope_tables
+    D, N = 16, 8
+    q, k, v, P = _rope_probe(D, N)
+    tabs = [(None, None), tuple(t.double().numpy() for t in rope_tables(N, D // 2))]
+    for c, s in tabs:
+        for fn in (oracle.cam_prep_fwd, mirror.cam_prep_fwd):
+            _, _, vo, _, _ = fn(q, k, v, P, P, rope_cos=c, rope_sin=s, rope_base=10000.0)
+            for n in (1, 7):
+                for i in (0, 3):
+                    y0, y1 = _hand_rotated_pair(n, i)
+                    got = vo[0, 0, n, D // 2 + 2 * i: D // 2 + 2 * i + 2]
+                    tol = 1e-12 if c is None else 1e-6  # the tables are fp32
+                    assert abs(got[0] - y0) < tol and abs(got[1] - y1) < tol, (n, i, got, (y0, y1))
+            # position 0 turns nothing
+            assert np.allclose(vo[0, 0, 0, D // 2:], v[0, 0, 0, D // 2:], atol=1e-12)
+
+
+def test_rope_pin_catches_planted_mistakes():
+    """The pin above is sensitive: a sine of the wrong sign, or a frequency
+    schedule in i instead of 2i, moves the hand-checked pairs far outside its
+    tolerance."""
+    n, i = 7, 3
+    a, b = 0.6, -0.8
+    y0, _ = _hand_rotated_pair(n, i)
+    th_bad = n * 10000.0 ** (-i / 8.0)
+    assert abs((a * np.cos(th_bad) - b * np.sin(th_bad)) - y0) > 1e-2
+    th = n * 1e-3
+    assert abs((a * np.cos(th) + b * np.sin(th)) - y0) > 1e-2
