@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(_PKG, "_build", "libgdn.so")
 GDN_F32, GDN_BF16 = 0, 1
 GDN_QK_L2NORM = 1
 GDN_PATH_SIMT = 2
+GDN_CAM_REVERSE = 4
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
           4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
-           "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc")
+           "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +62,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdn_chunk_fwd_noalloc.restype = i
         lib.deltaproduct_chunk_fwd.argtypes = [vp] * 8 + [i] * 7 + [f, u, i, vp, sz, vp]
         lib.deltaproduct_chunk_fwd.restype = i
+        lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
+        lib.cam_scan_fwd_workspace_bytes.restype = sz
+        lib.cam_scan_fwd.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp, sz, vp]
+        lib.cam_scan_fwd.restype = i
         lib.cam_prep_fwd.argtypes = [vp] * 9 + [f] + [vp] * 5 + [i] * 4 + [f, f, i, vp]
         lib.cam_prep_fwd.restype = i
         lib.gdn_get_device_error.argtypes = [vp]
@@ -196,6 +201,50 @@ def deltaproduct_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_st
     r = k.shape[3]
     return _scan("deltaproduct_chunk_fwd", q, k, v, beta, g, r, initial_state, output_final_state,
                  chunk, scale, l2norm, o, workspace, stream, simt)
+
+
+def cam_scan_workspace_bytes(B, H, F, S, Dk, Dv, dtype=torch.bfloat16):
+    code = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    n = load().cam_scan_fwd_workspace_bytes(B, H, F, S, Dk, Dv, code)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by cam_scan_fwd_workspace_bytes")
+    return int(n)
+
+
+def cam_scan_fwd(q, k, v, beta, decay, initial_state=None, output_final_state=False, scale=1.0,
+                 reverse=False, l2norm=False, o=None, workspace=None, stream=None, simt=False):
+    """Frame-level camera scan.  q, k [B,H,N,Dk]; v [B,H,N,Dv]; beta [B,H,N]
+    (all bf16 or all fp32); decay [B,H,F] fp32 factors, N = F * S.  Returns
+    (o, final_state or None); reverse=True is the anti-causal mode."""
+    B, H, N, Dk = q.shape
+    Dv = v.shape[-1]
+    F = decay.shape[-1]
+    if F <= 0 or N % F != 0:
+        raise ValueError(f"{N} tokens do not split into {F} frames")
+    S = N // F
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, N, Dk), dt)
+    _check(k, "k", (B, H, N, Dk), dt)
+    _check(v, "v", (B, H, N, Dv), dt)
+    _check(beta, "beta", (B, H, N), dt)
+    _check(decay, "decay", (B, H, F), torch.float32)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (B, H, Dk, Dv), torch.float32)
+    if o is None:
+        o = torch.empty(B, H, N, Dv, dtype=dt, device=q.device)
+    _check(o, "o", (B, H, N, Dv), dt)
+    sf = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=q.device) if output_final_state else None
+    need = cam_scan_workspace_bytes(B, H, F, S, Dk, Dv, dt)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0) | (GDN_CAM_REVERSE if reverse else 0)
+    st = load().cam_scan_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(o),
+                             _ptr(sf), B, H, F, S, Dk, Dv, float(scale), flags, code, _ptr(workspace), ws_bytes,
+                             _stream(stream))
+    _raise("cam_scan_fwd", st)
+    return o, sf
 
 
 def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=None, rope_cos=None,

@@ -1,0 +1,863 @@
+// cam_scan.cu -- frame-level camera scan (fused_cam_gdn.py, `_cam_scan_kernel`,
+// `_torch_cam_scan_single_chunk`, `_torch_cam_scan_reference`), forward and
+// reverse.  The tokens of each (batch, head) form F frames of S tokens; per
+// frame the state is decayed once by the frame's factor d_f, every token of the
+// frame predicts from that same state, all S corrections enter at once, and
+// the frame's tokens read the state after the update:
+//
+//     S_f = d_f S_{f-1} + K_f^T diag(beta_f) (V_f - K_f d_f S_{f-1})
+//         = d_f (S_{f-1} - G_f S_{f-1}) + H_f,      o_s = scale S_f^T q_s,
+//     G_f = K_f^T diag(beta_f) K_f,   H_f = K_f^T diag(beta_f) V_f.
+//
+// G_f and H_f do not depend on the state, so the tensor-core path (bf16,
+// Dk = Dv = 128) runs three launches:
+//
+//   cam_gram_kernel   one (head, frame) item at a time per CTA: streams the
+//                     frame's K and V through TMA in 64-token tiles, scales a
+//                     copy of K by beta (and the unit-norm factors) on the CUDA
+//                     cores, and accumulates [G | H] = (beta K)^T [K | V] in TMEM
+//                     with tcgen05 (M = 128, N = 256); writes G as a bf16 MMA
+//                     operand image and H^T in fp32 to the workspace.
+//   cam_chain_kernel  one CTA per head: the 128 x 128 fp32 state lives in TMEM;
+//                     per frame one MMA S += (-G_f) bf16(S), then S <- d_f S + H_f
+//                     in fp32, and bf16(S_f) goes out as the output's operand.
+//   cam_out_kernel    (head, frame, 128-token tile) items: O = scale Q S_f by
+//                     tcgen05, rows scaled by 1/||q|| when asked.
+//
+// Keeping S in fp32 and rounding only G S's operands to bf16 keeps the chain's
+// error at the bf16 level of the correction term, not of the state.  The
+// reverse mode runs the same chain from the last frame to the first, frame f
+// reading the state built from frames f+1 .. F-1 (the last frame reads zero).
+// Every other shape and dtype takes cam_scan_simt_kernel, which runs the frame
+// loop as written on the CUDA cores in fp32.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "gdn_internal.h"
+#include "tc_util.cuh"
+
+namespace gdn {
+namespace {
+using namespace tc;
+
+__device__ unsigned int g_cs_error = 0;  // set when a bounded wait of these kernels gives up
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, unsigned code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*reinterpret_cast<volatile unsigned *>(&g_cs_error) != 0u) return false;
+        if (global_timer_ns() - t0 > kWaitNs) {
+            atomicOr(&g_cs_error, code);
+            return false;
+        }
+    }
+}
+
+// A wait's outcome made uniform across the warp, so that the warp's
+// .sync.aligned tcgen05 loads that follow are reached by all of its lanes.
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok) != 0; }
+
+__device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)(32 * (warp & 3)) << 16; }
+
+__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) { return __uint_as_float((uint32_t)b << 16); }
+
+// ============================================================== gram kernel
+constexpr int kGramThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 workers
+constexpr int kGramStages = 3;
+constexpr uint32_t GR_STAGE = 65536;    // K (16 KB) | V (16 KB) | A1 (16 KB) | A2 (16 KB)
+constexpr uint32_t GR_K = 0, GR_V = 16384, GR_A1 = 32768, GR_A2 = 49152;
+constexpr uint32_t GR_BAR = kGramStages * GR_STAGE;
+enum { GB_FULL = 0, GB_AREADY = 3, GB_EMPTY = 6, GB_ACCF = 9, GB_ACCE = 11, GB_DRAIN = 13, GB_NUM = 14 };
+constexpr uint32_t GR_SMEM = GR_BAR + 8 * 16 + 16 + 1024;
+constexpr uint32_t kImgBytes = 32768;                 // a 128 x 128 bf16 operand image
+constexpr uint32_t kHtFloats = 128 * 128;
+constexpr size_t kPerFrame = 2 * (size_t)kImgBytes + sizeof(float) * kHtFloats;  // G image | S image | H^T
+
+struct GramParams {
+    const unsigned short *beta;  // bf16 bits [BH][N]
+    uint8_t *gimg;               // [BH*F][32 KB]
+    float *ht;                   // [BH*F][128][128]: H^T
+    int BH, F, S, N;
+    unsigned flags;
+};
+
+__global__ void __launch_bounds__(kGramThreads, 1)
+    cam_gram_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, GramParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + GR_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + GR_BAR + 8 * 16);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
+    const int nt = (p.S + 63) / 64;
+    const int items = p.BH * p.F;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGramStages; ++s) {
+            mbar_init(&bars[GB_FULL + s], 1);
+            mbar_init(&bars[GB_AREADY + s], 256);
+            mbar_init(&bars[GB_EMPTY + s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars[GB_ACCF + a], 1);
+            mbar_init(&bars[GB_ACCE + a], 256);
+        }
+        mbar_init(&bars[GB_DRAIN], 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32 * 2) {
+        prefetch_tensormap(&mK);
+        prefetch_tensormap(&mV);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int j = 0, armed[kGramStages] = {0, 0, 0};
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                const int bh = it / p.F, f = it % p.F;
+                for (int i = 0; i < nt; ++i, ++j) {
+                    const int s = j % kGramStages;
+                    if (j >= kGramStages && !wait_phase(&bars[GB_EMPTY + s], ((j / kGramStages) - 1) & 1, 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = sm + s * GR_STAGE;
+                    const int row0 = f * p.S + 64 * i;
+                    mbar_arrive_expect_tx(&bars[GB_FULL + s], 32768);
+                    tma_load_3d(st + GR_K, &mK, &bars[GB_FULL + s], 0, row0, bh);
+                    tma_load_3d(st + GR_K + 8192, &mK, &bars[GB_FULL + s], 64, row0, bh);
+                    tma_load_3d(st + GR_V, &mV, &bars[GB_FULL + s], 0, row0, bh);
+                    tma_load_3d(st + GR_V + 8192, &mV, &bars[GB_FULL + s], 64, row0, bh);
+                    armed[s]++;
+                }
+            }
+            for (int s = 0; s < kGramStages; ++s)
+                if (armed[s]) mbar_wait(&bars[GB_FULL + s], (armed[s] - 1) & 1, 200000000ull);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id256 = idesc_bf16(128, 256, true, true);
+            const uint32_t id128 = idesc_bf16(128, 128, true, true);
+            int j = 0, acc = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++acc) {
+                const int a = acc & 1;
+                if (acc >= 2 && !wait_phase(&bars[GB_ACCE + a], ((acc >> 1) - 1) & 1, 2u)) break;
+                const uint32_t d = tmem + 256u * a;
+                for (int i = 0; i < nt; ++i, ++j) {
+                    const int s = j % kGramStages;
+                    if (!wait_phase(&bars[GB_AREADY + s], (j / kGramStages) & 1, 2u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t st = sbase + s * GR_STAGE;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t acc_on = (i > 0 || ks > 0) ? 1u : 0u;
+                        if (!l2n) {
+                            // [G | H] += (beta K)^T [K | V]: the K and V atoms sit at a
+                            // uniform 8 KB stride, so one N = 256 operand covers both
+                            mma_bf16_ss(d, smem_desc(st + GR_A1 + ks * 2048, 8192, 1024),
+                                        smem_desc(st + GR_K + ks * 2048, 8192, 1024), id256, acc_on);
+                        } else {
+                            mma_bf16_ss(d, smem_desc(st + GR_A1 + ks * 2048, 8192, 1024),
+                                        smem_desc(st + GR_K + ks * 2048, 8192, 1024), id128, acc_on);
+                            mma_bf16_ss(d + 128, smem_desc(st + GR_A2 + ks * 2048, 8192, 1024),
+                                        smem_desc(st + GR_V + ks * 2048, 8192, 1024), id128, acc_on);
+                        }
+                    }
+                    mma_commit(&bars[GB_EMPTY + s]);
+                }
+                if (!ok) break;
+                mma_commit(&bars[GB_ACCF + a]);
+            }
+            // every MMA issued here is complete before TMEM is released
+            mma_commit(&bars[GB_DRAIN]);
+            mbar_wait(&bars[GB_DRAIN], 0, 200000000ull);
+        }
+    } else {
+        // ------------------------------------------------------ workers
+        // A copies: each thread scales 32 columns of one token row; then, after
+        // an item's last tile, the epilogue writes G (warps 2..5) and H^T
+        // (warps 6..9) from TMEM.
+        const int wt = threadIdx.x - 64;  // 0..255
+        const int r = wt >> 2, cq = wt & 3;
+        const int atom = cq >> 1, c0 = 32 * (cq & 1);
+        const int half = (warp - 2) >> 2;  // 0: G columns, 1: H columns
+        const int dk = 32 * (warp & 3) + lane;
+        int j = 0, acc = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++acc) {
+            const int bh = it / p.F, f = it % p.F;
+            const unsigned short *brow = p.beta + (size_t)bh * p.N + (size_t)f * p.S;
+            for (int i = 0; i < nt; ++i, ++j) {
+                const int s = j % kGramStages;
+                const int t = 64 * i + r;  // token within the frame
+                const bool valid = t < p.S;
+                const float beta = valid ? bf16_bits_to_float(brow[t]) : 0.f;
+                if (!warp_all(wait_phase(&bars[GB_FULL + s], (j / kGramStages) & 1, 4u))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = sm + s * GR_STAGE;
+                uint4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    x[u] = *reinterpret_cast<const uint4 *>(st + GR_K + atom * 8192 + sw128_offset(r, c0 + 8 * u));
+                float nrm = 1.f;
+                if (l2n) {
+                    float ss = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                            ss += lo * lo + hi * hi;
+                        }
+                    }
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                    nrm = rsqrtf(fmaxf(ss, 1e-24f));  // 1 / max(||k||, 1e-12)
+                }
+                const float c1 = beta * nrm * nrm, c2 = beta * nrm;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                    uint32_t y1[4], y2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                        y1[e] = pack_bf16(c1 * lo, c1 * hi);
+                        y2[e] = pack_bf16(c2 * lo, c2 * hi);
+                    }
+                    const uint32_t off = atom * 8192 + sw128_offset(r, c0 + 8 * u);
+                    *reinterpret_cast<uint4 *>(st + GR_A1 + off) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+                    if (l2n) *reinterpret_cast<uint4 *>(st + GR_A2 + off) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[GB_AREADY + s]);
+            }
+            if (!ok) break;
+            // epilogue of this item
+            const int a = acc & 1;
+            if (!warp_all(wait_phase(&bars[GB_ACCF + a], (acc >> 1) & 1, 4u))) break;
+            tc_fence_after_sync();
+            const uint32_t tcol = tmem + lane_base(warp) + 256u * a + 128u * half;
+            const size_t fi = (size_t)bh * p.F + f;
+            if (half == 0) {
+                uint8_t *gimg = p.gimg + fi * kImgBytes;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tcol + c, v);
+                    tmem_wait_ld();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                    uint8_t *blk = gimg + (c >> 6) * 16384;
+                    *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, c & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, (c & 63) + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            } else {
+                float *ht = p.ht + fi * kHtFloats;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tcol + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ht[(size_t)(c + e) * 128 + dk] = __uint_as_float(v[e]);
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars[GB_ACCE + a]);
+        }
+    }
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================= chain kernel
+constexpr int kChainThreads = 128;  // thread dk owns row dk of the state (TMEM lane dk)
+constexpr uint32_t CH_G = 0;        // two G images (32 KB each)
+constexpr uint32_t CH_H = 65536;    // two H^T blocks (64 KB each)
+constexpr uint32_t CH_S = 196608;   // bf16(S) as the MMA's B operand (32 KB)
+constexpr uint32_t CH_BAR = CH_S + kImgBytes;
+constexpr uint32_t CH_SMEM = CH_BAR + 64 + 1024;
+static_assert(CH_SMEM <= 232448, "chain kernel fits the shared memory of one CTA");
+
+struct ChainParams {
+    const uint8_t *gimg;
+    const float *ht;
+    uint8_t *simg;       // [BH*F][32 KB]: bf16(S_f) read by the output kernel
+    const float *decay;  // [BH][F]
+    const float *s0;
+    float *sf;
+    int BH, F;
+    int reverse;
+};
+
+// One row of bf16(S) into a 128 x 128 MN-major operand image (two 64-column
+// atoms of 128 rows x 128 bytes, 128-byte swizzle): row dk, columns c .. c+15.
+__device__ __forceinline__ void put_img_row16(uint8_t *img, int dk, int c, const uint32_t (&pk)[8]) {
+    uint8_t *blk = img + (c >> 6) * 16384;
+    *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, c & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, (c & 63) + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+}
+
+__global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + CH_BAR);  // LOAD0, LOAD1, MMA
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CH_BAR + 32);
+    const int warp = threadIdx.x >> 5;
+    const int dk = threadIdx.x;
+    const int bh = blockIdx.x;
+    const int F = p.F;
+    const int nsteps = p.reverse ? F - 1 : F;
+    const size_t fbase = (size_t)bh * F;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);  // LOAD0, LOAD1, MMA, DRAIN
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tl = tmem + lane_base(warp);
+    const uint32_t sbase = smem_u32(sm);
+    int armed[2] = {0, 0};  // thread 0: loads issued into each buffer
+    auto kv_frame = [&](int st) { return p.reverse ? F - 1 - st : st; };
+    auto load = [&](int st) {  // G and H^T of step st into buffer st & 1
+        const int b = st & 1;
+        armed[b]++;
+        const size_t fi = fbase + kv_frame(st);
+        mbar_arrive_expect_tx(&bars[b], kImgBytes + 4 * kHtFloats);
+        bulk_load_global(sm + CH_G + b * kImgBytes, p.gimg + fi * kImgBytes, kImgBytes, &bars[b]);
+        bulk_load_global(sm + CH_H + b * 65536, p.ht + fi * kHtFloats, 32768, &bars[b]);
+        bulk_load_global(sm + CH_H + b * 65536 + 32768, p.ht + fi * kHtFloats + 8192, 32768, &bars[b]);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < 2 && st < nsteps; ++st) load(st);
+    }
+    // initial state (forward) or zero; bf16(S) for the first product, and in
+    // reverse mode the last frame's output operand, which is zero
+    {
+        const float *s0 = (p.s0 && !p.reverse) ? p.s0 + (size_t)bh * 16384 : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+            uint32_t v[16], pk[8];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(s0 ? s0[dk * 128 + c + e] : 0.f);
+            tmem_st16(tl + c, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            put_img_row16(sm + CH_S, dk, c, pk);
+            if (p.reverse) put_img_row16(p.simg + (fbase + F - 1) * kImgBytes, dk, c, pk);
+        }
+        tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    bool ok = true;
+    for (int st = 0; st < nsteps; ++st) {
+        const int b = st & 1;
+        const int kf = kv_frame(st);
+        const int of = p.reverse ? kf - 1 : kf;  // frame whose queries read the new state
+        if (threadIdx.x == 0) {
+            bool w = wait_phase(&bars[b], (st >> 1) & 1, 8u);
+            if (w) {
+                tc_fence_after_sync();
+                const uint32_t idm = idesc_bf16(128, 128, false, true, true);
+                const uint32_t g = sbase + CH_G + b * kImgBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ss(tmem, smem_desc(g + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                smem_desc(sbase + CH_S + ks * 2048, 16384, 1024), idm, 1u);
+                mma_commit(&bars[2]);
+            }
+        }
+        // every thread waits for the product S - G bf16(S) (the bounded wait
+        // also ends once thread 0 has reported an expired load)
+        if (!__syncthreads_and(wait_phase(&bars[2], st & 1, 8u) ? 1 : 0)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after_sync();
+        const float d = p.decay[fbase + kf];
+        const float *ht = reinterpret_cast<const float *>(sm + CH_H + b * 65536);
+        uint8_t *out_img = p.simg + (fbase + of) * kImgBytes;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+            uint32_t v[16], pk[8];
+            tmem_ld16(tl + c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(fmaf(d, __uint_as_float(v[e]), ht[(c + e) * 128 + dk]));
+            tmem_st16(tl + c, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            put_img_row16(sm + CH_S, dk, c, pk);
+            put_img_row16(out_img, dk, c, pk);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();  // buffer b and bf16(S) consumed; the new bf16(S) is complete
+        if (threadIdx.x == 0 && st + 2 < nsteps) load(st + 2);
+    }
+    if (ok && p.sf && !p.reverse) {
+        tc_fence_after_sync();
+        float *sf = p.sf + (size_t)bh * 16384;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tl + c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sf[dk * 128 + c + e] = __uint_as_float(v[e]);
+        }
+    }
+    if (threadIdx.x == 0) {
+        // drain: every MMA issued and every load armed completes before the
+        // CTA releases TMEM and its shared memory
+        mma_commit(&bars[3]);
+        mbar_wait(&bars[3], 0, 200000000ull);
+        for (int b = 0; b < 2; ++b)
+            if (armed[b]) mbar_wait(&bars[b], (armed[b] - 1) & 1, 200000000ull);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// =============================================================== out kernel
+constexpr int kOutThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kOutStages = 4;
+constexpr uint32_t OU_Q = 0;                        // Q tiles: [128 rows][128] as 2 K-blocks (32 KB)
+constexpr uint32_t OU_S = kOutStages * 32768;       // two bf16(S_f) images
+constexpr uint32_t OU_BAR = OU_S + 2 * kImgBytes;
+enum { OB_QFULL = 0, OB_QEMPTY = 4, OB_SFULL = 8, OB_SEMPTY = 10, OB_OFULL = 12, OB_OEMPTY = 14, OB_DRAIN = 16,
+       OB_NUM = 17 };
+constexpr uint32_t OU_SMEM = OU_BAR + 8 * OB_NUM + 16 + 1024;
+
+struct OutParams {
+    const uint8_t *simg;
+    __nv_bfloat16 *o;
+    int BH, F, S, N, nt;  // nt: 128-token tiles per frame
+    long long items;
+    float scale;
+    unsigned flags;
+};
+
+__global__ void __launch_bounds__(kOutThreads, 1)
+    cam_out_kernel(const __grid_constant__ CUtensorMap mQ, OutParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OU_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OU_BAR + 8 * OB_NUM);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
+    const long long i0 = p.items * blockIdx.x / gridDim.x, i1 = p.items * (blockIdx.x + 1) / gridDim.x;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kOutStages; ++s) {
+            mbar_init(&bars[OB_QFULL + s], 1);
+            mbar_init(&bars[OB_QEMPTY + s], l2n ? 129u : 1u);  // the MMA, and the row norms when asked
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[OB_SFULL + b], 1);
+            mbar_init(&bars[OB_SEMPTY + b], 1);
+            mbar_init(&bars[OB_OFULL + b], 1);
+            mbar_init(&bars[OB_OEMPTY + b], 128);
+        }
+        mbar_init(&bars[OB_DRAIN], 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) prefetch_tensormap(&mQ);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t sbase = smem_u32(sm);
+    // item -> (frame index bh*F + f, tile i)
+    auto frame_of = [&](long long it) { return it / p.nt; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int armed[kOutStages] = {0, 0, 0, 0}, sarmed[2] = {0, 0};
+            long long prev = -1;
+            int sidx = -1;
+            for (long long it = i0; it < i1; ++it) {
+                const int j = (int)(it - i0), s = j % kOutStages;
+                const long long fi = frame_of(it);
+                const int i = (int)(it % p.nt);
+                const int bh = (int)(fi / p.F), f = (int)(fi % p.F);
+                if (fi != prev) {
+                    ++sidx;
+                    const int sb = sidx & 1;
+                    if (sidx >= 2 && !wait_phase(&bars[OB_SEMPTY + sb], ((sidx >> 1) - 1) & 1, 16u)) break;
+                    mbar_arrive_expect_tx(&bars[OB_SFULL + sb], kImgBytes);
+                    bulk_load_global(sm + OU_S + sb * kImgBytes, p.simg + (size_t)fi * kImgBytes, kImgBytes,
+                                     &bars[OB_SFULL + sb]);
+                    sarmed[sb]++;
+                    prev = fi;
+                }
+                if (j >= kOutStages && !wait_phase(&bars[OB_QEMPTY + s], ((j / kOutStages) - 1) & 1, 16u)) break;
+                const int row0 = f * p.S + 128 * i;
+                mbar_arrive_expect_tx(&bars[OB_QFULL + s], 32768);
+                tma_load_3d(sm + OU_Q + s * 32768, &mQ, &bars[OB_QFULL + s], 0, row0, bh);
+                tma_load_3d(sm + OU_Q + s * 32768 + 16384, &mQ, &bars[OB_QFULL + s], 64, row0, bh);
+                armed[s]++;
+            }
+            for (int s = 0; s < kOutStages; ++s)
+                if (armed[s]) mbar_wait(&bars[OB_QFULL + s], (armed[s] - 1) & 1, 200000000ull);
+            for (int b = 0; b < 2; ++b)
+                if (sarmed[b]) mbar_wait(&bars[OB_SFULL + b], (sarmed[b] - 1) & 1, 200000000ull);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t ido = idesc_bf16(128, 128, false, true);
+            long long prev = -1;
+            int sidx = -1;
+            for (long long it = i0; it < i1; ++it) {
+                const int j = (int)(it - i0), s = j % kOutStages, a = j & 1;
+                const long long fi = frame_of(it);
+                if (fi != prev) {
+                    ++sidx;
+                    prev = fi;
+                    if (!wait_phase(&bars[OB_SFULL + (sidx & 1)], (sidx >> 1) & 1, 32u)) break;
+                }
+                if (j >= 2 && !wait_phase(&bars[OB_OEMPTY + a], ((j >> 1) - 1) & 1, 32u)) break;
+                if (!wait_phase(&bars[OB_QFULL + s], (j / kOutStages) & 1, 32u)) break;
+                tc_fence_after_sync();
+                const uint32_t q = sbase + OU_Q + s * 32768, sb = sbase + OU_S + (sidx & 1) * kImgBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ss(tmem + 128u * a, smem_desc(q + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                smem_desc(sb + ks * 2048, 16384, 1024), ido, ks > 0 ? 1u : 0u);
+                mma_commit(&bars[OB_QEMPTY + s]);
+                mma_commit(&bars[OB_OFULL + a]);
+                if (it + 1 >= i1 || frame_of(it + 1) != fi) mma_commit(&bars[OB_SEMPTY + (sidx & 1)]);
+            }
+            mma_commit(&bars[OB_DRAIN]);
+            mbar_wait(&bars[OB_DRAIN], 0, 200000000ull);
+        }
+    } else {
+        // epilogue: thread = token row of the tile (TMEM lane)
+        const int row = 32 * (warp & 3) + lane;
+        for (long long it = i0; it < i1; ++it) {
+            const int j = (int)(it - i0), s = j % kOutStages, a = j & 1;
+            const long long fi = frame_of(it);
+            const int i = (int)(it % p.nt);
+            const int bh = (int)(fi / p.F), f = (int)(fi % p.F);
+            float m = p.scale;
+            if (l2n) {
+                if (!warp_all(wait_phase(&bars[OB_QFULL + s], (j / kOutStages) & 1, 64u))) break;
+                const uint8_t *qt = sm + OU_Q + s * 32768;
+                float ss = 0.f;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(qt + kb * 16384 + sw128_offset(row, 8 * u));
+                        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                            ss += lo * lo + hi * hi;
+                        }
+                    }
+                m *= rsqrtf(fmaxf(ss, 1e-24f));
+                mbar_arrive(&bars[OB_QEMPTY + s]);
+            }
+            if (!warp_all(wait_phase(&bars[OB_OFULL + a], (j >> 1) & 1, 64u))) break;
+            tc_fence_after_sync();
+            const int t = 128 * i + row;
+            const bool valid = t < p.S;
+            __nv_bfloat16 *orow = p.o + ((size_t)bh * p.N + (size_t)f * p.S + t) * 128;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + lane_base(warp) + 128u * a + c, v);
+                tmem_wait_ld();
+                uint32_t pk[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(m * __uint_as_float(v[2 * e]), m * __uint_as_float(v[2 * e + 1]));
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars[OB_OEMPTY + a]);
+        }
+    }
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================== SIMT kernel
+// One CTA per (head, 32-column slice of the value dim); the slice of the fp32
+// state sits in shared memory.  Per frame: P = K S for 32-token tiles, the
+// corrections beta (v - d P) summed into registers as K^T (.), then
+// S <- d S + sum, then the frame's outputs from the new state.  All fp32.
+constexpr int kSimtThreads = 256;
+constexpr int kTile = 32;
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T *p, size_t i);
+template <>
+__device__ __forceinline__ float ldf<float>(const float *p, size_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+template <typename T>
+__device__ __forceinline__ void stf(T *p, size_t i, float v);
+template <>
+__device__ __forceinline__ void stf<float>(float *p, size_t i, float v) { p[i] = v; }
+template <>
+__device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+struct SimtParams {
+    const void *q, *k, *v, *beta;
+    const float *decay, *s0;
+    void *o;
+    float *sf;
+    int F, S, N, Dk, Dv;
+    float scale;
+    unsigned flags;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kSimtThreads) cam_scan_simt_kernel(SimtParams p) {
+    __shared__ float sS[128][33];     // state slice [dk][j]
+    __shared__ float sX[kTile][129];  // K (or Q) tile [token][dk]
+    __shared__ float sV[kTile][33];   // V slice tile, then the corrections
+    __shared__ float sB[kTile];       // beta (0 past the frame), then the query scales
+    const int bh = blockIdx.x, j0 = blockIdx.y * 32;
+    const int tid = threadIdx.x, Dk = p.Dk, Dv = p.Dv;
+    const bool l2n = (p.flags & GDN_QK_L2NORM) != 0, rev = (p.flags & GDN_CAM_REVERSE) != 0;
+    const T *q = static_cast<const T *>(p.q) + (size_t)bh * p.N * Dk;
+    const T *k = static_cast<const T *>(p.k) + (size_t)bh * p.N * Dk;
+    const T *v = static_cast<const T *>(p.v) + (size_t)bh * p.N * Dv;
+    const T *beta = static_cast<const T *>(p.beta) + (size_t)bh * p.N;
+    T *o = static_cast<T *>(p.o) + (size_t)bh * p.N * Dv;
+    for (int e = tid; e < Dk * 32; e += kSimtThreads) {
+        const int i = e >> 5, jj = e & 31;
+        sS[i][jj] = (p.s0 && !rev) ? p.s0[((size_t)bh * Dk + i) * Dv + j0 + jj] : 0.f;
+    }
+    __syncthreads();
+    // thread -> (row group, column) for the tile products: column jj = tid & 31,
+    // rows r8 = tid >> 5 .. step 8
+    const int jj = tid & 31, r8 = tid >> 5;
+    // load a [kTile][Dk] tile of x (K or Q) rows t0.. into sX, optionally unit rows
+    auto load_rows = [&](const T *x, long t0, int nrow) {
+        for (int e = tid; e < kTile * Dk; e += kSimtThreads) {
+            const int t = e / Dk, i = e % Dk;
+            sX[t][i] = t < nrow ? ldf(x, (size_t)(t0 + t) * Dk + i) : 0.f;
+        }
+        __syncthreads();
+        if (l2n) {
+            // one warp per 4 rows: sum of squares, then scale
+            const int w = tid >> 5, ln = tid & 31;
+            for (int t = w; t < kTile; t += kSimtThreads / 32) {
+                float ss = 0.f;
+                for (int i = ln; i < Dk; i += 32) ss += sX[t][i] * sX[t][i];
+#pragma unroll
+                for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float n = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+                for (int i = ln; i < Dk; i += 32) sX[t][i] *= n;
+            }
+            __syncthreads();
+        }
+    };
+    for (int itf = 0; itf < p.F; ++itf) {
+        const int qf = rev ? p.F - 1 - itf : itf;
+        const int kf = rev ? p.F - itf : itf;
+        if (!rev || itf > 0) {
+            const float d = p.decay[(size_t)bh * p.F + kf];
+            // dS[i][jj] for rows i = r8 + 8 m, accumulated over the frame
+            float acc[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+            for (int t0 = 0; t0 < p.S; t0 += kTile) {
+                const int nrow = min(kTile, p.S - t0);
+                const long g0 = (long)kf * p.S + t0;
+                load_rows(k, g0, nrow);
+                for (int e = tid; e < kTile * 32; e += kSimtThreads) {
+                    const int t = e >> 5, c = e & 31;
+                    sV[t][c] = t < nrow ? ldf(v, (size_t)(g0 + t) * Dv + j0 + c) : 0.f;
+                }
+                if (tid < kTile) sB[tid] = tid < nrow ? ldf(beta, (size_t)(g0 + tid)) : 0.f;
+                __syncthreads();
+                // corrections c[t][jj] = beta_t (v - d (K S))[t][jj], rows t = r8 + 8 m
+                float cr[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int t = r8 + 8 * m;
+                    float pr = 0.f;
+                    for (int i = 0; i < Dk; ++i) pr = fmaf(sX[t][i], sS[i][jj], pr);
+                    cr[m] = sB[t] * (sV[t][jj] - d * pr);
+                }
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < 4; ++m) sV[r8 + 8 * m][jj] = cr[m];
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int i = r8 + 8 * m;
+                    if (i < Dk) {
+                        float s = acc[m];
+                        for (int t = 0; t < kTile; ++t) s = fmaf(sX[t][i], sV[t][jj], s);
+                        acc[m] = s;
+                    }
+                }
+                __syncthreads();
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int i = r8 + 8 * m;
+                if (i < Dk) sS[i][jj] = fmaf(d, sS[i][jj], acc[m]);
+            }
+            __syncthreads();
+        }
+        // outputs of frame qf from the state as it now stands
+        for (int t0 = 0; t0 < p.S; t0 += kTile) {
+            const int nrow = min(kTile, p.S - t0);
+            const long g0 = (long)qf * p.S + t0;
+            load_rows(q, g0, nrow);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int t = r8 + 8 * m;
+                float pr = 0.f;
+                for (int i = 0; i < Dk; ++i) pr = fmaf(sX[t][i], sS[i][jj], pr);
+                if (t < nrow) stf(o, (size_t)(g0 + t) * Dv + j0 + jj, p.scale * pr);
+            }
+            __syncthreads();
+        }
+    }
+    if (p.sf && !rev)
+        for (int e = tid; e < Dk * 32; e += kSimtThreads) {
+            const int i = e >> 5, c = e & 31;
+            p.sf[((size_t)bh * Dk + i) * Dv + j0 + c] = sS[i][c];
+        }
+}
+
+// ================================================================ host side
+int launch_tc(const CamScanArgs &a, cudaStream_t stream) {
+    const int BH = a.B * a.H, N = a.F * a.S;
+    CUtensorMap mK, mV, mQ;
+    if (!make_bf16_map(&mK, a.k, BH, N, 64, 64) || !make_bf16_map(&mV, a.v, BH, N, 64, 64) ||
+        !make_bf16_map(&mQ, a.q, BH, N, 64, 128))
+        return GDN_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(a.ws);
+    const size_t frames = (size_t)BH * a.F;
+    uint8_t *gimg = ws;
+    uint8_t *simg = ws + frames * kImgBytes;
+    float *ht = reinterpret_cast<float *>(ws + 2 * frames * kImgBytes);
+    const int sms = device_sm_count();
+    if (sms <= 0) return GDN_ERR_CUDA;
+    const bool rev = (a.flags & GDN_CAM_REVERSE) != 0;
+
+    // 1. G and H^T of every (head, frame); in reverse mode frame 0 is never
+    //    taken in, but computing it keeps the item map simple
+    if (cudaFuncSetAttribute(cam_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GR_SMEM) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    GramParams gp{static_cast<const unsigned short *>(a.beta), gimg, ht, BH, a.F, a.S, N, a.flags};
+    const int g_grid = (int)std::min<size_t>(frames, (size_t)sms);
+    cam_gram_kernel<<<g_grid, kGramThreads, GR_SMEM, stream>>>(mK, mV, gp);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+
+    // 2. the state chain, one CTA per head
+    if (cudaFuncSetAttribute(cam_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CH_SMEM) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    ChainParams cp{gimg, ht, simg, a.decay, a.s0, a.sf, BH, a.F, rev ? 1 : 0};
+    cam_chain_kernel<<<BH, kChainThreads, CH_SMEM, stream>>>(cp);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+
+    // 3. outputs
+    if (cudaFuncSetAttribute(cam_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)OU_SMEM) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const int nt = (a.S + 127) / 128;
+    OutParams op{simg, static_cast<__nv_bfloat16 *>(a.o), BH, a.F, a.S, N, nt, (long long)frames * nt, a.scale,
+                 a.flags};
+    const int o_grid = (int)std::min<long long>(op.items, (long long)sms);
+    cam_out_kernel<<<o_grid, kOutThreads, OU_SMEM, stream>>>(mQ, op);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename T>
+int launch_simt(const CamScanArgs &a, cudaStream_t stream) {
+    SimtParams sp{a.q, a.k, a.v, a.beta, a.decay, a.s0, a.o, a.sf, a.F, a.S, a.F * a.S, a.Dk, a.Dv, a.scale, a.flags};
+    dim3 grid((unsigned)(a.B * a.H), (unsigned)(a.Dv / 32));
+    cam_scan_simt_kernel<T><<<grid, kSimtThreads, 0, stream>>>(sp);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+bool cam_scan_tc_supported(const CamScanArgs &a) {
+    if (a.flags & GDN_PATH_SIMT) return false;
+    if (a.dtype != GDN_BF16 || a.Dk != 128 || a.Dv != 128) return false;
+    if ((long long)a.F * a.S >= (1LL << 31)) return false;
+    return sm100_family();
+}
+
+size_t cam_scan_workspace_bytes(const CamScanArgs &a) {
+    return cam_scan_tc_supported(a) ? (size_t)a.B * a.H * a.F * kPerFrame : 0;
+}
+
+int launch_cam_scan(const CamScanArgs &a, cudaStream_t stream) {
+    if (cam_scan_tc_supported(a)) return launch_tc(a, stream);
+    if (a.dtype == GDN_BF16) return launch_simt<__nv_bfloat16>(a, stream);
+    return launch_simt<float>(a, stream);
+}
+
+int cam_scan_read_clear_error() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_cs_error, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_cs_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
+    return v ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
+}  // namespace gdn

@@ -66,6 +66,24 @@ int run_scan(gdn::ScanArgs &a, void *stream_v, bool need_ws = true) {
     return gdn::launch_scan_simt(a, stream);
 }
 
+int check_cam_scan(const gdn::CamScanArgs &a) {
+    if (a.B < 0 || a.H < 0 || a.F < 0 || a.S < 0) return GDN_ERR_INVALID_ARG;
+    if (a.F > 0 && a.S == 0) return GDN_ERR_INVALID_ARG;  // a frame holds at least one token
+    if (a.dtype != GDN_F32 && a.dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (a.flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT | GDN_CAM_REVERSE)) return GDN_ERR_INVALID_ARG;
+    if ((a.Dk != 64 && a.Dk != 128) || (a.Dv != 64 && a.Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if ((a.flags & GDN_CAM_REVERSE) && (a.s0 || a.sf)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)a.B * a.H > 65535 || (long long)a.F * a.S >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)a.B * a.H * a.F != 0) {
+        if (!a.q || !a.k || !a.v || !a.beta || !a.decay || !a.o) return GDN_ERR_INVALID_ARG;
+        const void *ps[] = {a.q, a.k, a.v, a.beta, a.decay, a.o};
+        for (const void *p : ps)
+            if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    }
+    if ((a.s0 && !aligned16(a.s0)) || (a.sf && !aligned16(a.sf))) return GDN_ERR_MISALIGNED;
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -143,6 +161,40 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
     return run_scan(a, stream);
 }
 
+size_t cam_scan_fwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, int dtype) {
+    gdn::CamScanArgs a{};
+    a.B = B; a.H = H; a.F = F; a.S = S; a.Dk = Dk; a.Dv = Dv; a.dtype = dtype; a.scale = 1.f;
+    if (B < 0 || H < 0 || F < 0 || S < 0 || (F > 0 && S == 0)) return (size_t)-1;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return (size_t)-1;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
+    return gdn::cam_scan_workspace_bytes(a);
+}
+
+int cam_scan_fwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
+                 const float *initial_state, void *o, float *final_state, int B, int H, int F, int S,
+                 int Dk, int Dv, float scale, unsigned flags, int dtype, void *workspace,
+                 size_t workspace_bytes, void *stream_v) {
+    gdn::CamScanArgs a{q, k, v, beta, decay, initial_state, o, final_state, B, H, F, S, Dk, Dv,
+                       scale, flags, dtype, workspace, workspace_bytes};
+    const int st = check_cam_scan(a);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const size_t need = gdn::cam_scan_workspace_bytes(a);
+    if (need > 0 && (a.ws == nullptr || a.ws_bytes < need || !aligned16(a.ws))) return GDN_ERR_WORKSPACE;
+    if ((long long)B * H == 0) return GDN_OK;
+    if (F == 0) {
+        if (final_state) {
+            const size_t bytes = sizeof(float) * (size_t)B * H * Dk * Dv;
+            cudaError_t e = initial_state
+                                ? cudaMemcpyAsync(final_state, initial_state, bytes, cudaMemcpyDeviceToDevice, stream)
+                                : cudaMemsetAsync(final_state, 0, bytes, stream);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    return gdn::launch_cam_scan(a, stream);
+}
+
 int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *q_norm_w,
                  const float *k_norm_w, const float *proj_q, const float *proj_kv,
                  const float *rope_cos, const float *rope_sin, float rope_base, void *q_out,
@@ -172,7 +224,8 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
 int gdn_get_device_error(void *stream) {
     const int a = gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
     const int b = gdn::cam_prep_read_clear_error();
-    return a != GDN_OK ? a : b;
+    const int c = gdn::cam_scan_read_clear_error();
+    return a != GDN_OK ? a : (b != GDN_OK ? b : c);
 }
 
 unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }

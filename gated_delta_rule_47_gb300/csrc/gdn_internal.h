@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "gdn.h"
@@ -50,6 +51,36 @@ int scan_tc_set_cluster_shape(int hc, int nwy);
 // Device address and size of the fixed scratch array behind
 // gdn_chunk_fwd_noalloc (set up on the current device at the first call).
 int scan_tc_noalloc_scratch(void **ptr, size_t *bytes);
+
+// Arguments of one frame-level camera scan call: q,k [B,H,F*S,Dk], v,o
+// [B,H,F*S,Dv], beta [B,H,F*S], decay [B,H,F] factors.
+struct CamScanArgs {
+    const void *q, *k, *v, *beta;
+    const float *decay;
+    const float *s0;
+    void *o;
+    float *sf;
+    int B, H, F, S, Dk, Dv;
+    float scale;
+    unsigned flags;
+    int dtype;
+    void *ws;
+    size_t ws_bytes;
+};
+
+// Frame scan: the tensor-core path (bf16, Dk = Dv = 128) needs a workspace of
+// cam_scan_workspace_bytes; everything else runs on the CUDA cores.
+bool cam_scan_tc_supported(const CamScanArgs &a);
+size_t cam_scan_workspace_bytes(const CamScanArgs &a);
+int launch_cam_scan(const CamScanArgs &a, cudaStream_t stream);
+int cam_scan_read_clear_error();
+
+// 3-D TMA map (128-byte swizzle) over a [heads][rows][128] bf16 tensor with a
+// {box0, box1, 1} box; false if the driver entry point is missing or rejects it.
+bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int box0, int box1);
+// True on an sm_10x device (tcgen05 available); cached.
+bool sm100_family();
+int device_sm_count();
 
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the streamed camera prep (GDN_OK or GDN_ERR_TIMEOUT).

@@ -1495,14 +1495,24 @@ int launch_r(const ScanArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
+bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int box0, int box1) {
+    return make_map(m, base, heads, rows, box0, box1, true);
+}
+
+bool sm100_family() {
+    static int sm100 = -1;
+    if (sm100 < 0) sm100 = device_is_sm100_family() ? 1 : 0;
+    return sm100 == 1;
+}
+
+int device_sm_count() { return sm_count(); }
+
 bool scan_tc_supported(const ScanArgs &a) {
     if (a.flags & GDN_PATH_SIMT) return false;
     if (a.dtype != GDN_BF16 || a.Dk != 128 || a.Dv != 128 || a.chunk != 64) return false;
     if (a.r != 1 && a.r != 2 && a.r != 4) return false;
     if ((long long)a.T * a.r > (1LL << 30)) return false;
-    static int sm100 = -1;
-    if (sm100 < 0) sm100 = device_is_sm100_family() ? 1 : 0;
-    return sm100 == 1;
+    return sm100_family();
 }
 
 size_t scan_tc_workspace_bytes(const ScanArgs &a) {

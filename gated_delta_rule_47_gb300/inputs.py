@@ -89,6 +89,41 @@ def orthonormal_keys(B, H, T, D, seed):
     return qm[:, :T, :].reshape(B, H, T, D).float().contiguous()
 
 
+def frame_gates(B, H, F, S, seed, dtype="bf16"):
+    """Gates of the frame-level camera scan: beta [B,H,F*S] = sigmoid(N(0,1)) / S
+    in ``dtype`` (each frame's S corrections enter at once, so their sum is
+    scaled by the frame size, which keeps I - K^T diag(beta) K contractive for
+    unit keys), and one decay factor per frame, decay [B,H,F] =
+    exp(logsigmoid(N(0,1)) / 16) in fp32."""
+    gen = torch.Generator().manual_seed(int(seed))
+    beta_logit = torch.randn(B, H, F * S, generator=gen)
+    g_logit = torch.randn(B, H, F, generator=gen)
+    return (torch.sigmoid(beta_logit) / S).to(_DTYPES[dtype]).contiguous(), \
+        torch.exp(torch.nn.functional.logsigmoid(g_logit) / 16.0).float().contiguous()
+
+
+def cam_scan_inputs(B, H, F, S, Dk, Dv, seed, dtype="bf16", initial_state=False, normalise_qk=True):
+    """Inputs of one frame-scan workload as CPU tensors: q, k [B,H,F*S,Dk]
+    (N(0,1), unit rows unless normalise_qk is False), v [B,H,F*S,Dv] ~ N(0,1),
+    the frame gates of ``frame_gates`` and, if asked, an initial state ~ N(0,1)
+    [B,H,Dk,Dv] fp32.  Draw order: q, k, v, initial state, then the gates."""
+    gen = torch.Generator().manual_seed(int(seed))
+    N = F * S
+    q = torch.randn(B, H, N, Dk, generator=gen)
+    k = torch.randn(B, H, N, Dk, generator=gen)
+    v = torch.randn(B, H, N, Dv, generator=gen)
+    s0 = torch.randn(B, H, Dk, Dv, generator=gen) if initial_state else None
+    if normalise_qk:
+        q, k = _unit_rows(q), _unit_rows(k)
+    td = _DTYPES[dtype]
+    beta, decay = frame_gates(B, H, F, S, seed + 7919, dtype)
+    out = {"q": q.to(td).contiguous(), "k": k.to(td).contiguous(), "v": v.to(td).contiguous(),
+           "beta": beta, "decay": decay}
+    if s0 is not None:
+        out["initial_state"] = s0.float().contiguous()
+    return out
+
+
 def quaternion_rotations(n: int, gen: torch.Generator) -> torch.Tensor:
     """n rotation matrices from uniformly random unit quaternions (normalised
     4-D Gaussians), fp64, shape [n,3,3]."""
@@ -226,6 +261,6 @@ def split_heads_np(x, idx):
     return flat[list(idx)][None]
 
 
-__all__ = ["gdn_inputs", "cam_inputs", "mixed_decay", "orthonormal_keys", "rope_tables", "se3_poses", "se3_inverse",
+__all__ = ["gdn_inputs", "cam_inputs", "mixed_decay", "orthonormal_keys", "frame_gates", "cam_scan_inputs", "rope_tables", "se3_poses", "se3_inverse",
            "quaternion_rotations", "WORKLOADS", "Workload", "to_f64", "split_heads_np",
            "torch_dtype"]

@@ -60,6 +60,7 @@ typedef enum {
 #define GDN_PATH_SIMT 2u /* use the CUDA-core path even where the tensor-core
                             path applies (bf16, Dk = Dv = 128, chunk 64,
                             r in {1, 2, 4})                                */
+#define GDN_CAM_REVERSE 4u /* cam_scan_fwd only: the anti-causal mode        */
 
 /* Human-readable name of a status code; never NULL. */
 const char *gdn_status_string(int status);
@@ -169,6 +170,46 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
                            float *final_state, int B, int H, int T, int r, int Dk, int Dv,
                            int chunk, float scale, unsigned flags, int dtype, void *workspace,
                            size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of device workspace cam_scan_fwd needs for these sizes on the current
+ * device (0 on the CUDA-core path).  (size_t)-1 for sizes it rejects.
+ */
+size_t cam_scan_fwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, int dtype);
+
+/*
+ * cam_scan_fwd -- frame-level, numerator-only camera scan (fused_cam_gdn.py:
+ * `_cam_scan_kernel`, `_torch_cam_scan_single_chunk`; the reverse mode is
+ * `_torch_cam_scan_reference` with `_flip_and_shift`).  The N = F*S tokens of
+ * each (batch, head) form F frames of S tokens.  Forward, for f = 0 .. F-1:
+ *     S <- decay_f S                                   (once per frame)
+ *     S <- S + K_f^T diag(beta_f) (V_f - K_f S)        (every token of the frame
+ *                                                       predicts from the same S)
+ *     o_s = scale * S^T q_s   for the frame's tokens    (after the update, so a
+ *                                                       frame sees all of itself)
+ * Reverse (flags & GDN_CAM_REVERSE): frames from last to first with a zero
+ * start; frame f's tokens read the state built from frames f+1 .. F-1 only
+ * (the last frame reads zero), frame j's factor decay_j decaying the state as
+ * frame j is taken in.
+ *
+ *   q, k    [B,H,N,Dk]  dtype (the layout cam_prep_fwd writes)
+ *   v, o    [B,H,N,Dv]  dtype
+ *   beta    [B,H,N]     dtype
+ *   decay   [B,H,F]     fp32 factors (not logs) of each frame
+ *   initial_state / final_state [B,H,Dk,Dv] fp32 or NULL: forward only
+ *           (GDN_ERR_UNSUPPORTED with GDN_CAM_REVERSE)
+ *   F >= 0 frames of S >= 1 tokens; Dk, Dv 64 or 128; flags: GDN_QK_L2NORM
+ *   (unit q and k per token and head), GDN_PATH_SIMT, GDN_CAM_REVERSE.
+ *   workspace: at least cam_scan_fwd_workspace_bytes(...) bytes, 16-byte
+ *           aligned (128 KB per head and frame on the tensor-core path: the
+ *           frame products K^T diag(beta) [K | V] and each frame's state).
+ * The page's scan takes [B,H,D,N] fp32 tensors; this library keeps the
+ * token-major layout of its other entry points.
+ */
+int cam_scan_fwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
+                 const float *initial_state, void *o, float *final_state, int B, int H, int F, int S,
+                 int Dk, int Dv, float scale, unsigned flags, int dtype, void *workspace,
+                 size_t workspace_bytes, void *stream);
 
 /*
  * cam_prep_fwd -- fused camera-branch prep (fused_cam_gdn.py, `_cam_prep_kernel`

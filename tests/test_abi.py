@@ -112,3 +112,26 @@ def test_cluster_shape_checks(lib):
     for hc, nwy in ((1, 1), (4, 5), (2, 14)):
         assert lib.gdn_set_cluster_shape(hc, nwy) == 0
     assert lib.gdn_set_cluster_shape(0, 0) == 0
+
+
+def test_cam_scan_argument_checks(lib):
+    f = lib.cam_scan_fwd
+    u = 0x10000
+
+    def call(q=u, s0=None, sf=None, B=1, H=2, F=3, S=5, Dk=64, Dv=64, flags=0, dtype=binding.GDN_F32):
+        return f(q, u, u, u, u, s0, u, sf, B, H, F, S, Dk, Dv, 1.0, flags, dtype, None, 0, None)
+
+    assert call(s0=u, flags=binding.GDN_CAM_REVERSE) == 2      # no state in the reverse mode
+    assert call(sf=u, flags=binding.GDN_CAM_REVERSE) == 2
+    assert call(S=0) == 1                                      # a frame holds at least one token
+    assert call(F=-1) == 1
+    assert call(flags=8) == 1
+    assert call(Dk=96) == 2
+    assert call(dtype=7) == 1
+    assert call(q=None) == 1
+    assert call(q=u + 8) == 3
+    q = lib.cam_scan_fwd_workspace_bytes
+    bad = ctypes.c_size_t(-1).value
+    assert q(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 0         # the CUDA-core path needs none
+    assert q(1, 2, 3, 0, 64, 64, binding.GDN_F32) == bad
+    assert q(1, 2, 3, 5, 96, 64, binding.GDN_F32) == bad
