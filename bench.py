@@ -56,6 +56,12 @@ def gdn_bytes_per_token_head(D, s_in=2, s_out=2):
     return 3 * D * s_in + s_in + 4 + D * s_out
 
 
+def cam_scan_bytes_per_token_head(D, s=2):
+    """Algorithmic HBM bytes per (token, head) of the frame-level scan: q, k, v
+    and beta in, o out (the per-frame decay and the state are negligible)."""
+    return 3 * D * s + s + D * s
+
+
 def gdn_flops_per_token_head(D, C):
     """w.S, k^T v_new and q.S (2 D^2 each) + triangular-half KK^T, T.(beta k),
     T.(beta v), q k^T and P.v_new (C.D each) + the C^3/3 inverse amortised."""
@@ -456,6 +462,22 @@ def secondary(args, dev):
     out[w.name] = {"prep_ms": pre_ms, "prep_gbs": prep_bytes / (pre_ms * 1e-3) / 1e9,
                    "prep_hbm_frac": prep_bytes / (pre_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                    "scan_ms": scan_ms, "tokens_per_s": w.B * w.T / ((pre_ms + scan_ms) * 1e-3)}
+    # the camera branch's own frame-level scan on the prep output: 21 frames of
+    # 30 x 52 tokens, unit-norm q and k, beta / S per token, one decay per frame
+    from gated_delta_rule_47_gb300.inputs import frame_gates
+    F, S = 21, 30 * 52
+    beta_f, decay_f = (x.to(dev) for x in frame_gates(w.B, w.H, F, S, seed=w.seed))
+    wsf = torch.empty(binding.cam_scan_workspace_bytes(w.B, w.H, F, S, w.D, w.D), dtype=torch.uint8, device=dev)
+    frame_bytes = w.B * w.H * w.T * cam_scan_bytes_per_token_head(w.D)
+    res = {}
+    for rev in (False, True):
+        ms = timeit(lambda: binding.cam_scan_fwd(outs[0], outs[1], outs[2], beta_f, decay_f, l2norm=True, o=o,
+                                                 workspace=wsf, reverse=rev))
+        res["reverse" if rev else "forward"] = {
+            "ms": ms, "gbs": frame_bytes / (ms * 1e-3) / 1e9,
+            "hbm_frac": frame_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "tokens_per_s_with_prep": w.B * w.T / ((pre_ms + ms) * 1e-3)}
+    out["cam_frames_b2f21s1560h16d128_bf16"] = dict(res, alg_bytes=frame_bytes, launches_per_call=3)
     return out
 
 

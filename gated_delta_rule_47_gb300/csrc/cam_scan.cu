@@ -68,16 +68,18 @@ __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)(32 *
 __device__ __forceinline__ float bf16_bits_to_float(unsigned short b) { return __uint_as_float((uint32_t)b << 16); }
 
 // ============================================================== gram kernel
-constexpr int kGramThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 workers
-constexpr int kGramStages = 3;
-constexpr uint32_t GR_STAGE = 65536;    // K (16 KB) | V (16 KB) | A1 (16 KB) | A2 (16 KB)
-constexpr uint32_t GR_K = 0, GR_V = 16384, GR_A1 = 32768, GR_A2 = 49152;
-constexpr uint32_t GR_BAR = kGramStages * GR_STAGE;
-enum { GB_FULL = 0, GB_AREADY = 3, GB_EMPTY = 6, GB_ACCF = 9, GB_ACCE = 11, GB_DRAIN = 13, GB_NUM = 14 };
-constexpr uint32_t GR_SMEM = GR_BAR + 8 * 16 + 16 + 1024;
+constexpr int kGramThreads = 448;       // warp 0 TMA, warp 1 MMA, warps 2..9 A copies, warps 10..13 epilogue
+constexpr int kGramStages = 4;          // K | V tiles in flight
+constexpr uint32_t GR_STAGE = 32768;    // K (16 KB) | V (16 KB)
+constexpr uint32_t GR_K = 0, GR_V = 16384;
+constexpr uint32_t GR_A = kGramStages * GR_STAGE;  // two buffers of A1 (16 KB) | A2 (16 KB)
+constexpr uint32_t GR_BAR = GR_A + 2 * 32768;
+enum { GB_FULL = 0, GB_EMPTY = 4, GB_AREADY = 8, GB_AEMPTY = 10, GB_ACCF = 12, GB_ACCE = 14, GB_DRAIN = 16, GB_NUM = 17 };
+constexpr uint32_t GR_SMEM = GR_BAR + 8 * GB_NUM + 16 + 1024;
 constexpr uint32_t kImgBytes = 32768;                 // a 128 x 128 bf16 operand image
 constexpr uint32_t kHtFloats = 128 * 128;
 constexpr size_t kPerFrame = 2 * (size_t)kImgBytes + sizeof(float) * kHtFloats;  // G image | S image | H^T
+static_assert(GR_SMEM <= 232448, "gram kernel fits the shared memory of one CTA");
 
 struct GramParams {
     const unsigned short *beta;  // bf16 bits [BH][N]
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + GR_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + GR_BAR + 8 * 16);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + GR_BAR + 8 * GB_NUM);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
     const int nt = (p.S + 63) / 64;
@@ -101,12 +103,13 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGramStages; ++s) {
             mbar_init(&bars[GB_FULL + s], 1);
-            mbar_init(&bars[GB_AREADY + s], 256);
             mbar_init(&bars[GB_EMPTY + s], 1);
         }
         for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars[GB_AREADY + a], 256);
+            mbar_init(&bars[GB_AEMPTY + a], 1);
             mbar_init(&bars[GB_ACCF + a], 1);
-            mbar_init(&bars[GB_ACCE + a], 256);
+            mbar_init(&bars[GB_ACCE + a], 128);
         }
         mbar_init(&bars[GB_DRAIN], 1);
         fence_mbar_init();
@@ -127,8 +130,10 @@ __global__ void __launch_bounds__(kGramThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
+        // Tiles of 64 tokens; a tile that runs past its frame's last token is
+        // clipped there by the frame-shaped map (zeros, no memory traffic).
         if (lane == 0) {
-            int j = 0, armed[kGramStages] = {0, 0, 0};
+            int j = 0, armed[kGramStages] = {0, 0, 0, 0};
             bool ok = true;
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
                 const int bh = it / p.F, f = it % p.F;
@@ -139,12 +144,11 @@ __global__ void __launch_bounds__(kGramThreads, 1)
                         break;
                     }
                     uint8_t *st = sm + s * GR_STAGE;
-                    const int row0 = f * p.S + 64 * i;
                     mbar_arrive_expect_tx(&bars[GB_FULL + s], 32768);
-                    tma_load_3d(st + GR_K, &mK, &bars[GB_FULL + s], 0, row0, bh);
-                    tma_load_3d(st + GR_K + 8192, &mK, &bars[GB_FULL + s], 64, row0, bh);
-                    tma_load_3d(st + GR_V, &mV, &bars[GB_FULL + s], 0, row0, bh);
-                    tma_load_3d(st + GR_V + 8192, &mV, &bars[GB_FULL + s], 64, row0, bh);
+                    tma_load_4d(st + GR_K, &mK, &bars[GB_FULL + s], 0, 64 * i, f, bh);
+                    tma_load_4d(st + GR_K + 8192, &mK, &bars[GB_FULL + s], 64, 64 * i, f, bh);
+                    tma_load_4d(st + GR_V, &mV, &bars[GB_FULL + s], 0, 64 * i, f, bh);
+                    tma_load_4d(st + GR_V + 8192, &mV, &bars[GB_FULL + s], 64, 64 * i, f, bh);
                     armed[s]++;
                 }
             }
@@ -163,29 +167,31 @@ __global__ void __launch_bounds__(kGramThreads, 1)
                 if (acc >= 2 && !wait_phase(&bars[GB_ACCE + a], ((acc >> 1) - 1) & 1, 2u)) break;
                 const uint32_t d = tmem + 256u * a;
                 for (int i = 0; i < nt; ++i, ++j) {
-                    const int s = j % kGramStages;
-                    if (!wait_phase(&bars[GB_AREADY + s], (j / kGramStages) & 1, 2u)) {
+                    const int s = j % kGramStages, x = j & 1;
+                    if (!wait_phase(&bars[GB_FULL + s], (j / kGramStages) & 1, 2u) ||
+                        !wait_phase(&bars[GB_AREADY + x], (j >> 1) & 1, 2u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t st = sbase + s * GR_STAGE;
+                    const uint32_t st = sbase + s * GR_STAGE, ab = sbase + GR_A + x * 32768;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc_on = (i > 0 || ks > 0) ? 1u : 0u;
                         if (!l2n) {
                             // [G | H] += (beta K)^T [K | V]: the K and V atoms sit at a
                             // uniform 8 KB stride, so one N = 256 operand covers both
-                            mma_bf16_ss(d, smem_desc(st + GR_A1 + ks * 2048, 8192, 1024),
+                            mma_bf16_ss(d, smem_desc(ab + ks * 2048, 8192, 1024),
                                         smem_desc(st + GR_K + ks * 2048, 8192, 1024), id256, acc_on);
                         } else {
-                            mma_bf16_ss(d, smem_desc(st + GR_A1 + ks * 2048, 8192, 1024),
+                            mma_bf16_ss(d, smem_desc(ab + ks * 2048, 8192, 1024),
                                         smem_desc(st + GR_K + ks * 2048, 8192, 1024), id128, acc_on);
-                            mma_bf16_ss(d + 128, smem_desc(st + GR_A2 + ks * 2048, 8192, 1024),
+                            mma_bf16_ss(d + 128, smem_desc(ab + 16384 + ks * 2048, 8192, 1024),
                                         smem_desc(st + GR_V + ks * 2048, 8192, 1024), id128, acc_on);
                         }
                     }
                     mma_commit(&bars[GB_EMPTY + s]);
+                    mma_commit(&bars[GB_AEMPTY + x]);
                 }
                 if (!ok) break;
                 mma_commit(&bars[GB_ACCF + a]);
@@ -194,44 +200,44 @@ __global__ void __launch_bounds__(kGramThreads, 1)
             mma_commit(&bars[GB_DRAIN]);
             mbar_wait(&bars[GB_DRAIN], 0, 200000000ull);
         }
-    } else {
-        // ------------------------------------------------------ workers
-        // A copies: each thread scales 32 columns of one token row; then, after
-        // an item's last tile, the epilogue writes G (warps 2..5) and H^T
-        // (warps 6..9) from TMEM.
+    } else if (warp < 10) {
+        // ------------------------------------------------------ A copies
+        // Each thread scales 32 columns of one token row of the K tile: A1 =
+        // beta n^2 k (for G), and with unit-norm keys A2 = beta n k (for H).
         const int wt = threadIdx.x - 64;  // 0..255
         const int r = wt >> 2, cq = wt & 3;
         const int atom = cq >> 1, c0 = 32 * (cq & 1);
-        const int half = (warp - 2) >> 2;  // 0: G columns, 1: H columns
-        const int dk = 32 * (warp & 3) + lane;
-        int j = 0, acc = 0;
+        int j = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++acc) {
+        for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             const int bh = it / p.F, f = it % p.F;
             const unsigned short *brow = p.beta + (size_t)bh * p.N + (size_t)f * p.S;
             for (int i = 0; i < nt; ++i, ++j) {
-                const int s = j % kGramStages;
+                const int s = j % kGramStages, x = j & 1;
                 const int t = 64 * i + r;  // token within the frame
                 const bool valid = t < p.S;
                 const float beta = valid ? bf16_bits_to_float(brow[t]) : 0.f;
-                if (!warp_all(wait_phase(&bars[GB_FULL + s], (j / kGramStages) & 1, 4u))) {
+                bool w = wait_phase(&bars[GB_FULL + s], (j / kGramStages) & 1, 4u);
+                if (w && j >= 2) w = wait_phase(&bars[GB_AEMPTY + x], ((j >> 1) - 1) & 1, 4u);
+                if (!warp_all(w)) {
                     ok = false;
                     break;
                 }
-                uint8_t *st = sm + s * GR_STAGE;
-                uint4 x[4];
+                const uint8_t *st = sm + s * GR_STAGE;
+                uint8_t *ab = sm + GR_A + x * 32768;
+                uint4 xv[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    x[u] = *reinterpret_cast<const uint4 *>(st + GR_K + atom * 8192 + sw128_offset(r, c0 + 8 * u));
+                    xv[u] = *reinterpret_cast<const uint4 *>(st + GR_K + atom * 8192 + sw128_offset(r, c0 + 8 * u));
                 float nrm = 1.f;
                 if (l2n) {
                     float ss = 0.f;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                        const uint32_t w4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                            const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
                             ss += lo * lo + hi * hi;
                         }
                     }
@@ -242,52 +248,50 @@ __global__ void __launch_bounds__(kGramThreads, 1)
                 const float c1 = beta * nrm * nrm, c2 = beta * nrm;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                    const uint32_t w4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
                     uint32_t y1[4], y2[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
                         y1[e] = pack_bf16(c1 * lo, c1 * hi);
                         y2[e] = pack_bf16(c2 * lo, c2 * hi);
                     }
                     const uint32_t off = atom * 8192 + sw128_offset(r, c0 + 8 * u);
-                    *reinterpret_cast<uint4 *>(st + GR_A1 + off) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-                    if (l2n) *reinterpret_cast<uint4 *>(st + GR_A2 + off) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+                    *reinterpret_cast<uint4 *>(ab + off) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+                    if (l2n) *reinterpret_cast<uint4 *>(ab + 16384 + off) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars[GB_AREADY + s]);
+                mbar_arrive(&bars[GB_AREADY + x]);
             }
-            if (!ok) break;
-            // epilogue of this item
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        // thread dk: row dk of G (bf16 operand image) and of H (as H^T, fp32)
+        const int dk = 32 * (warp & 3) + lane;
+        const uint32_t lb = lane_base(warp);
+        int acc = 0;
+        for (int it = blockIdx.x; it < items; it += gridDim.x, ++acc) {
+            const int bh = it / p.F, f = it % p.F;
             const int a = acc & 1;
             if (!warp_all(wait_phase(&bars[GB_ACCF + a], (acc >> 1) & 1, 4u))) break;
             tc_fence_after_sync();
-            const uint32_t tcol = tmem + lane_base(warp) + 256u * a + 128u * half;
             const size_t fi = (size_t)bh * p.F + f;
-            if (half == 0) {
-                uint8_t *gimg = p.gimg + fi * kImgBytes;
+            uint8_t *gimg = p.gimg + fi * kImgBytes;
+            float *ht = p.ht + fi * kHtFloats;
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tcol + c, v);
-                    tmem_wait_ld();
-                    uint32_t pk[8];
+            for (int c = 0; c < 128; c += 16) {
+                uint32_t g[16], h[16];
+                tmem_ld16(tmem + lb + 256u * a + c, g);
+                tmem_ld16(tmem + lb + 256u * a + 128u + c, h);
+                tmem_wait_ld();
+                uint32_t pk[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                    uint8_t *blk = gimg + (c >> 6) * 16384;
-                    *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, c & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, (c & 63) + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                }
-            } else {
-                float *ht = p.ht + fi * kHtFloats;
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tcol + c, v);
-                    tmem_wait_ld();
+                for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1]));
+                uint8_t *blk = gimg + (c >> 6) * 16384;
+                *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, c & 63)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(blk + sw128_offset(dk, (c & 63) + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) ht[(size_t)(c + e) * 128 + dk] = __uint_as_float(v[e]);
-                }
+                for (int e = 0; e < 16; ++e) ht[(size_t)(c + e) * 128 + dk] = __uint_as_float(h[e]);
             }
             tc_fence_before_sync();
             mbar_arrive(&bars[GB_ACCE + a]);
@@ -301,10 +305,10 @@ __global__ void __launch_bounds__(kGramThreads, 1)
 }
 
 // ============================================================= chain kernel
-constexpr int kChainThreads = 128;  // thread dk owns row dk of the state (TMEM lane dk)
+constexpr int kChainThreads = 256;  // thread (dk, half): TMEM lane dk, state columns 64 half .. 64 half + 63
 constexpr uint32_t CH_G = 0;        // two G images (32 KB each)
 constexpr uint32_t CH_H = 65536;    // two H^T blocks (64 KB each)
-constexpr uint32_t CH_S = 196608;   // bf16(S) as the MMA's B operand (32 KB)
+constexpr uint32_t CH_S = 196608;   // bf16(S) as the MMA's B operand (32 KB), also the image sent out
 constexpr uint32_t CH_BAR = CH_S + kImgBytes;
 constexpr uint32_t CH_SMEM = CH_BAR + 64 + 1024;
 static_assert(CH_SMEM <= 232448, "chain kernel fits the shared memory of one CTA");
@@ -331,16 +335,17 @@ __device__ __forceinline__ void put_img_row16(uint8_t *img, int dk, int c, const
 __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + CH_BAR);  // LOAD0, LOAD1, MMA
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + CH_BAR);  // LOAD0, LOAD1, MMA, DRAIN
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CH_BAR + 32);
     const int warp = threadIdx.x >> 5;
-    const int dk = threadIdx.x;
+    const int dk = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int c0 = 64 * (warp >> 2);  // this thread's 64 state columns
     const int bh = blockIdx.x;
     const int F = p.F;
     const int nsteps = p.reverse ? F - 1 : F;
     const size_t fbase = (size_t)bh * F;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);  // LOAD0, LOAD1, MMA, DRAIN
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -367,12 +372,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams
     if (threadIdx.x == 0) {
         for (int st = 0; st < 2 && st < nsteps; ++st) load(st);
     }
-    // initial state (forward) or zero; bf16(S) for the first product, and in
-    // reverse mode the last frame's output operand, which is zero
+    // initial state (forward) or zero, and bf16(S) for the first product
     {
         const float *s0 = (p.s0 && !p.reverse) ? p.s0 + (size_t)bh * 16384 : nullptr;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = c0; c < c0 + 64; c += 16) {
             uint32_t v[16], pk[8];
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(s0 ? s0[dk * 128 + c + e] : 0.f);
@@ -380,21 +384,27 @@ __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
             put_img_row16(sm + CH_S, dk, c, pk);
-            if (p.reverse) put_img_row16(p.simg + (fbase + F - 1) * kImgBytes, dk, c, pk);
         }
         tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
+    if (threadIdx.x == 0 && p.reverse) {
+        // the last frame reads the zero state
+        bulk_store_global(p.simg + (fbase + F - 1) * kImgBytes, sm + CH_S, kImgBytes);
+        tma_store_commit();
+    }
     bool ok = true;
+    float d_next = nsteps > 0 ? p.decay[fbase + kv_frame(0)] : 0.f;
     for (int st = 0; st < nsteps; ++st) {
         const int b = st & 1;
         const int kf = kv_frame(st);
         const int of = p.reverse ? kf - 1 : kf;  // frame whose queries read the new state
+        const float d = d_next;  // read one step ahead, off the chain's path
+        if (st + 1 < nsteps) d_next = p.decay[fbase + kv_frame(st + 1)];
         if (threadIdx.x == 0) {
-            bool w = wait_phase(&bars[b], (st >> 1) & 1, 8u);
-            if (w) {
+            if (wait_phase(&bars[b], (st >> 1) & 1, 8u)) {
                 tc_fence_after_sync();
                 const uint32_t idm = idesc_bf16(128, 128, false, true, true);
                 const uint32_t g = sbase + CH_G + b * kImgBytes;
@@ -404,6 +414,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams
                                 smem_desc(sbase + CH_S + ks * 2048, 16384, 1024), idm, 1u);
                 mma_commit(&bars[2]);
             }
+            tma_store_wait_read<0>();  // the previous state image has left CH_S
         }
         // every thread waits for the product S - G bf16(S) (the bounded wait
         // also ends once thread 0 has reported an expired load)
@@ -412,33 +423,41 @@ __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams
             break;
         }
         tc_fence_after_sync();
-        const float d = p.decay[fbase + kf];
         const float *ht = reinterpret_cast<const float *>(sm + CH_H + b * 65536);
-        uint8_t *out_img = p.simg + (fbase + of) * kImgBytes;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
-            uint32_t v[16], pk[8];
-            tmem_ld16(tl + c, v);
+        for (int c = c0; c < c0 + 64; c += 32) {
+            uint32_t v[2][16];
+            tmem_ld16(tl + c, v[0]);
+            tmem_ld16(tl + c + 16, v[1]);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(fmaf(d, __uint_as_float(v[e]), ht[(c + e) * 128 + dk]));
-            tmem_st16(tl + c, v);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-            put_img_row16(sm + CH_S, dk, c, pk);
-            put_img_row16(out_img, dk, c, pk);
+                for (int e = 0; e < 16; ++e)
+                    v[hh][e] = __float_as_uint(fmaf(d, __uint_as_float(v[hh][e]), ht[(c + 16 * hh + e) * 128 + dk]));
+                tmem_st16(tl + c + 16 * hh, v[hh]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    pk[e] = pack_bf16(__uint_as_float(v[hh][2 * e]), __uint_as_float(v[hh][2 * e + 1]));
+                put_img_row16(sm + CH_S, dk, c + 16 * hh, pk);
+            }
         }
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        __syncthreads();  // buffer b and bf16(S) consumed; the new bf16(S) is complete
-        if (threadIdx.x == 0 && st + 2 < nsteps) load(st + 2);
+        __syncthreads();  // buffer b and the old bf16(S) consumed; the new bf16(S) is complete
+        if (threadIdx.x == 0) {
+            bulk_store_global(p.simg + (fbase + of) * kImgBytes, sm + CH_S, kImgBytes);
+            tma_store_commit();
+            if (st + 2 < nsteps) load(st + 2);
+        }
     }
     if (ok && p.sf && !p.reverse) {
         tc_fence_after_sync();
         float *sf = p.sf + (size_t)bh * 16384;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = c0; c < c0 + 64; c += 16) {
             uint32_t v[16];
             tmem_ld16(tl + c, v);
             tmem_wait_ld();
@@ -447,12 +466,13 @@ __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams
         }
     }
     if (threadIdx.x == 0) {
-        // drain: every MMA issued and every load armed completes before the
-        // CTA releases TMEM and its shared memory
+        // drain: every MMA issued, every load armed and every image sent out
+        // completes before the CTA releases TMEM and its shared memory
         mma_commit(&bars[3]);
         mbar_wait(&bars[3], 0, 200000000ull);
         for (int b = 0; b < 2; ++b)
             if (armed[b]) mbar_wait(&bars[b], (armed[b] - 1) & 1, 200000000ull);
+        tma_store_wait_all<0>();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -462,25 +482,43 @@ __global__ void __launch_bounds__(kChainThreads, 1) cam_chain_kernel(ChainParams
 
 // =============================================================== out kernel
 constexpr int kOutThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kOutStages = 4;
+constexpr int kOutStages = 3;
 constexpr uint32_t OU_Q = 0;                        // Q tiles: [128 rows][128] as 2 K-blocks (32 KB)
 constexpr uint32_t OU_S = kOutStages * 32768;       // two bf16(S_f) images
-constexpr uint32_t OU_BAR = OU_S + 2 * kImgBytes;
-enum { OB_QFULL = 0, OB_QEMPTY = 4, OB_SFULL = 8, OB_SEMPTY = 10, OB_OFULL = 12, OB_OEMPTY = 14, OB_DRAIN = 16,
-       OB_NUM = 17 };
+constexpr uint32_t OU_O = OU_S + 2 * kImgBytes;     // two output staging tiles (TMA store boxes)
+constexpr uint32_t OU_BAR = OU_O + 2 * 32768;
+enum { OB_QFULL = 0, OB_QEMPTY = 3, OB_SFULL = 6, OB_SEMPTY = 8, OB_OFULL = 10, OB_OEMPTY = 12, OB_DRAIN = 14,
+       OB_NUM = 15 };
 constexpr uint32_t OU_SMEM = OU_BAR + 8 * OB_NUM + 16 + 1024;
+static_assert(OU_SMEM <= 232448, "output kernel fits the shared memory of one CTA");
 
 struct OutParams {
     const uint8_t *simg;
-    __nv_bfloat16 *o;
-    int BH, F, S, N, nt;  // nt: 128-token tiles per frame
+    int BH, F, S, nt;  // nt: 128-token tiles per frame
     long long items;
     float scale;
     unsigned flags;
 };
 
+__device__ __forceinline__ void named_sync_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier over the 128 epilogue threads that also ANDs a flag across
+// them, so that they all take the same branch after a bounded wait.
+__device__ __forceinline__ bool epi_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
 __global__ void __launch_bounds__(kOutThreads, 1)
-    cam_out_kernel(const __grid_constant__ CUtensorMap mQ, OutParams p) {
+    cam_out_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mO, OutParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OU_BAR);
@@ -506,18 +544,20 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tmem_alloc(tslot, 256);
         tmem_relinquish();
     }
-    if (threadIdx.x == 0) prefetch_tensormap(&mQ);
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&mQ);
+        prefetch_tensormap(&mO);
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
     const uint32_t sbase = smem_u32(sm);
-    // item -> (frame index bh*F + f, tile i)
-    auto frame_of = [&](long long it) { return it / p.nt; };
+    auto frame_of = [&](long long it) { return it / p.nt; };  // item -> bh * F + f
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed[kOutStages] = {0, 0, 0, 0}, sarmed[2] = {0, 0};
+            int armed[kOutStages] = {0, 0, 0}, sarmed[2] = {0, 0};
             long long prev = -1;
             int sidx = -1;
             for (long long it = i0; it < i1; ++it) {
@@ -536,10 +576,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                     prev = fi;
                 }
                 if (j >= kOutStages && !wait_phase(&bars[OB_QEMPTY + s], ((j / kOutStages) - 1) & 1, 16u)) break;
-                const int row0 = f * p.S + 128 * i;
                 mbar_arrive_expect_tx(&bars[OB_QFULL + s], 32768);
-                tma_load_3d(sm + OU_Q + s * 32768, &mQ, &bars[OB_QFULL + s], 0, row0, bh);
-                tma_load_3d(sm + OU_Q + s * 32768 + 16384, &mQ, &bars[OB_QFULL + s], 64, row0, bh);
+                tma_load_4d(sm + OU_Q + s * 32768, &mQ, &bars[OB_QFULL + s], 0, 128 * i, f, bh);
+                tma_load_4d(sm + OU_Q + s * 32768 + 16384, &mQ, &bars[OB_QFULL + s], 64, 128 * i, f, bh);
                 armed[s]++;
             }
             for (int s = 0; s < kOutStages; ++s)
@@ -576,55 +615,73 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             mbar_wait(&bars[OB_DRAIN], 0, 200000000ull);
         }
     } else {
-        // epilogue: thread = token row of the tile (TMEM lane)
+        // epilogue: thread = token row of the tile (TMEM lane); the tile goes
+        // through a 128-byte-swizzled staging buffer and leaves as two TMA
+        // stores, clipped at the frame's last row by the frame-shaped map
         const int row = 32 * (warp & 3) + lane;
+        const bool storer = threadIdx.x == 64;
         for (long long it = i0; it < i1; ++it) {
-            const int j = (int)(it - i0), s = j % kOutStages, a = j & 1;
+            const int j = (int)(it - i0), s = j % kOutStages, a = j & 1, x = j & 1;
             const long long fi = frame_of(it);
             const int i = (int)(it % p.nt);
             const int bh = (int)(fi / p.F), f = (int)(fi % p.F);
             float m = p.scale;
+            bool w = true;
             if (l2n) {
-                if (!warp_all(wait_phase(&bars[OB_QFULL + s], (j / kOutStages) & 1, 64u))) break;
-                const uint8_t *qt = sm + OU_Q + s * 32768;
-                float ss = 0.f;
+                w = wait_phase(&bars[OB_QFULL + s], (j / kOutStages) & 1, 64u);
+                if (w) {
+                    const uint8_t *qt = sm + OU_Q + s * 32768;
+                    float ss = 0.f;
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
+                    for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(qt + kb * 16384 + sw128_offset(row, 8 * u));
-                        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 xq = *reinterpret_cast<const uint4 *>(qt + kb * 16384 + sw128_offset(row, 8 * u));
+                            const uint32_t w4[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-                            ss += lo * lo + hi * hi;
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+                                ss += lo * lo + hi * hi;
+                            }
                         }
-                    }
-                m *= rsqrtf(fmaxf(ss, 1e-24f));
-                mbar_arrive(&bars[OB_QEMPTY + s]);
-            }
-            if (!warp_all(wait_phase(&bars[OB_OFULL + a], (j >> 1) & 1, 64u))) break;
-            tc_fence_after_sync();
-            const int t = 128 * i + row;
-            const bool valid = t < p.S;
-            __nv_bfloat16 *orow = p.o + ((size_t)bh * p.N + (size_t)f * p.S + t) * 128;
-#pragma unroll 1
-            for (int c = 0; c < 128; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_base(warp) + 128u * a + c, v);
-                tmem_wait_ld();
-                uint32_t pk[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(m * __uint_as_float(v[2 * e]), m * __uint_as_float(v[2 * e + 1]));
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    m *= rsqrtf(fmaxf(ss, 1e-24f));
+                    mbar_arrive(&bars[OB_QEMPTY + s]);
                 }
+            }
+            if (w) w = wait_phase(&bars[OB_OFULL + a], (j >> 1) & 1, 64u);
+            if (storer) tma_store_wait_read<1>();  // staging buffer x (item j-2's) has been read out
+            if (!epi_all(w)) break;
+            tc_fence_after_sync();
+            uint8_t *stg = sm + OU_O + x * 32768;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t v0[16], v1[16];
+                tmem_ld16(tmem + lane_base(warp) + 128u * a + c, v0);
+                tmem_ld16(tmem + lane_base(warp) + 128u * a + c + 16, v1);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    pk[e] = pack_bf16(m * __uint_as_float(v0[2 * e]), m * __uint_as_float(v0[2 * e + 1]));
+                    pk[8 + e] = pack_bf16(m * __uint_as_float(v1[2 * e]), m * __uint_as_float(v1[2 * e + 1]));
+                }
+                uint8_t *half = stg + (c >> 6) * 16384;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4 *>(half + sw128_offset(row, (c & 63) + 8 * u)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
             }
             tc_fence_before_sync();
             mbar_arrive(&bars[OB_OEMPTY + a]);
+            fence_proxy_async_smem();
+            named_sync_epi();
+            if (storer) {
+                tma_store_4d(&mO, stg, 0, 128 * i, f, bh);
+                tma_store_4d(&mO, stg + 16384, 64, 128 * i, f, bh);
+                tma_store_commit();
+            }
         }
+        if (storer) tma_store_wait_all<0>();
     }
     __syncwarp();
     tc_fence_before_sync();
@@ -782,9 +839,9 @@ __global__ void __launch_bounds__(kSimtThreads) cam_scan_simt_kernel(SimtParams 
 // ================================================================ host side
 int launch_tc(const CamScanArgs &a, cudaStream_t stream) {
     const int BH = a.B * a.H, N = a.F * a.S;
-    CUtensorMap mK, mV, mQ;
-    if (!make_bf16_map(&mK, a.k, BH, N, 64, 64) || !make_bf16_map(&mV, a.v, BH, N, 64, 64) ||
-        !make_bf16_map(&mQ, a.q, BH, N, 64, 128))
+    CUtensorMap mK, mV, mQ, mO;
+    if (!make_bf16_frame_map(&mK, a.k, BH, a.F, a.S, 64, 64) || !make_bf16_frame_map(&mV, a.v, BH, a.F, a.S, 64, 64) ||
+        !make_bf16_frame_map(&mQ, a.q, BH, a.F, a.S, 64, 128) || !make_bf16_frame_map(&mO, a.o, BH, a.F, a.S, 64, 128))
         return GDN_ERR_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
     const size_t frames = (size_t)BH * a.F;
@@ -817,10 +874,9 @@ int launch_tc(const CamScanArgs &a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(cam_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)OU_SMEM) != cudaSuccess)
         return GDN_ERR_CUDA;
     const int nt = (a.S + 127) / 128;
-    OutParams op{simg, static_cast<__nv_bfloat16 *>(a.o), BH, a.F, a.S, N, nt, (long long)frames * nt, a.scale,
-                 a.flags};
+    OutParams op{simg, BH, a.F, a.S, nt, (long long)frames * nt, a.scale, a.flags};
     const int o_grid = (int)std::min<long long>(op.items, (long long)sms);
-    cam_out_kernel<<<o_grid, kOutThreads, OU_SMEM, stream>>>(mQ, op);
+    cam_out_kernel<<<o_grid, kOutThreads, OU_SMEM, stream>>>(mQ, mO, op);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -78,6 +78,11 @@ int cam_scan_read_clear_error();
 // 3-D TMA map (128-byte swizzle) over a [heads][rows][128] bf16 tensor with a
 // {box0, box1, 1} box; false if the driver entry point is missing or rejects it.
 bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int box0, int box1);
+// 4-D TMA map (128-byte swizzle) over a [heads][frames][frame_rows][128] bf16
+// tensor with a {box0, box1, 1, 1} box: a box that runs past a frame's last
+// row is clipped there (zero-filled on loads, not written on stores).
+bool make_bf16_frame_map(CUtensorMap *m, const void *base, int heads, int frames, int frame_rows, int box0,
+                         int box1);
 // True on an sm_10x device (tcgen05 available); cached.
 bool sm100_family();
 int device_sm_count();

@@ -1499,6 +1499,20 @@ bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int b
     return make_map(m, base, heads, rows, box0, box1, true);
 }
 
+bool make_bf16_frame_map(CUtensorMap *m, const void *base, int heads, int frames, int frame_rows, int box0,
+                         int box1) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {128, (cuuint64_t)frame_rows, (cuuint64_t)frames, (cuuint64_t)heads};
+    cuuint64_t strides[3] = {256, (cuuint64_t)frame_rows * 256, (cuuint64_t)frame_rows * frames * 256};
+    cuuint32_t box[4] = {(cuuint32_t)box0, (cuuint32_t)box1, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool sm100_family() {
     static int sm100 = -1;
     if (sm100 < 0) sm100 = device_is_sm100_family() ? 1 : 0;
