@@ -62,6 +62,8 @@ def _load():
             lib.oracle_gdn_fwd.restype = i
             lib.oracle_deltaproduct_fwd.argtypes = [_dp] * 8 + [i] * 6 + [d, i]
             lib.oracle_deltaproduct_fwd.restype = i
+            lib.oracle_masked_deltaproduct_fwd.argtypes = [_dp] * 9 + [i] * 6 + [d, i]
+            lib.oracle_masked_deltaproduct_fwd.restype = i
             lib.oracle_cam_scan_fwd.argtypes = [_dp] * 8 + [i] * 6 + [d, i, i]
             lib.oracle_cam_scan_fwd.restype = i
             lib.oracle_cam_prep_fwd.argtypes = [_dp] * 9 + [d] + [_dp] * 5 + [i] * 4 + [d, d]
@@ -135,6 +137,34 @@ def deltaproduct_fwd(q, k, v, beta, g, initial_state=None, scale=1.0, l2norm=Fal
                                          float(scale), int(bool(l2norm)))
     if rc != 0:
         raise MemoryError("oracle_deltaproduct_fwd failed")
+    return o, sf
+
+
+def masked_deltaproduct_fwd(q, k, v, beta, g, mask, initial_state=None, scale=1.0, l2norm=False,
+                            return_final_state=True):
+    """fp64 block-masked DeltaProduct (gated_deltaproduct test.py, the mask_ij
+    variant): the key dim is cut into r = mask.shape[0] slices; per token one
+    decay, then every sub-row i predicts with k_t masked slice-wise by
+    mask[i][:] and corrects the slice-i rows of the state; one value and beta
+    per token; o_t = scale S_t^T q_t.
+
+    q, k: [B,H,T,Dk]; v: [B,H,T,Dv]; beta, g: [B,H,T]; mask: [r,r].
+    """
+    q, k, v, beta, g, mask = map(_f64, (q, k, v, beta, g, mask))
+    s0 = _f64(initial_state)
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    r = mask.shape[0]
+    assert mask.shape == (r, r) and Dk % r == 0
+    assert k.shape == (B, H, T, Dk) and v.shape == (B, H, T, Dv)
+    assert beta.shape == (B, H, T) and g.shape == (B, H, T)
+    o = np.empty((B, H, T, Dv), np.float64)
+    sf = np.empty((B, H, Dk, Dv), np.float64) if return_final_state else None
+    rc = _load().oracle_masked_deltaproduct_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
+                                                _ptr(s0), _ptr(o), _ptr(sf), B, H, T, r, Dk, Dv, float(scale),
+                                                int(bool(l2norm)))
+    if rc != 0:
+        raise MemoryError("oracle_masked_deltaproduct_fwd failed")
     return o, sf
 
 

@@ -21,6 +21,21 @@
  *    sub-steps j = 0..r-1, each with its own k_{t,j}, v_{t,j}, beta_{t,j};
  *    the output reads the state after the last sub-step.
  *
+ *  - Block-masked DeltaProduct (gated_deltaproduct test.py: the mask_ij
+ *    coupling of `gated_chunk_scaled_dot_kkt_fwd_kernel` and
+ *    `gated_fwd_recompute_w_u_kernel`, the per-slice state update of
+ *    `gated_chunk_delta_rule_fwd_kernel_h`, and the sum over r in
+ *    `gated_chunk_fwd_o_fn`): the key dimension is cut into r slices of
+ *    Dk/r; per token the decay is applied once, then every sub-row i < r
+ *    predicts from that same state with the read key k_t (.) m_i (slice j of
+ *    k_t times mask[i][j]) and corrects the state's slice-i rows with its
+ *    write key, slice i of k_t; one value and one beta per token:
+ *        S <- e^{g_t} S
+ *        z_j = S_(j)^T k_t,(j)                 (slice j rows of S and k_t)
+ *        d_i = beta_t (v_t - sum_j mask[i][j] z_j)
+ *        S_(i) <- S_(i) + k_t,(i) d_i^T        (all i from the same z)
+ *        o_t = scale * S^T q_t
+ *
  *  - Frame-level camera scan (fused_cam_gdn.py, `_cam_scan_kernel`,
  *    `_torch_cam_scan_single_chunk` and `_torch_cam_scan_reference`): the
  *    tokens form F frames of S tokens; per frame the state is decayed once by
@@ -197,6 +212,81 @@ int oracle_deltaproduct_fwd(const double *q, const double *k, const double *v,
         }
         free(S);
         free(p);
+        free(kt);
+        free(qt);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Block-masked DeltaProduct forward, token by token.
+ *   q, k : [B,H,T,Dk]   v, o : [B,H,T,Dv]   beta, g : [B,H,T]
+ *   mask : [r][r] row-major, shared by every head; r divides Dk
+ *   s0 / s_final : [B,H,Dk,Dv] or NULL.
+ */
+int oracle_masked_deltaproduct_fwd(const double *q, const double *k, const double *v,
+                                   const double *beta, const double *g, const double *mask,
+                                   const double *s0, double *o, double *s_final, int B, int H,
+                                   int T, int r, int Dk, int Dv, double scale, int l2norm) {
+    if (r < 1 || Dk % r != 0) return -2;
+    const int BH = B * H;
+    const int dk = Dk / r;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *S = (double *)malloc(sizeof(double) * (size_t)Dk * Dv);
+        double *z = (double *)malloc(sizeof(double) * (size_t)r * Dv);
+        double *d = (double *)malloc(sizeof(double) * (size_t)r * Dv);
+        double *kt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        double *qt = (double *)malloc(sizeof(double) * (size_t)Dk);
+        if (!S || !z || !d || !kt || !qt) {
+            failed |= 1;
+        } else {
+            if (s0)
+                memcpy(S, s0 + (size_t)bh * Dk * Dv, sizeof(double) * (size_t)Dk * Dv);
+            else
+                memset(S, 0, sizeof(double) * (size_t)Dk * Dv);
+            for (int t = 0; t < T; ++t) {
+                const size_t tok = (size_t)bh * T + t;
+                memcpy(kt, k + tok * Dk, sizeof(double) * Dk);
+                memcpy(qt, q + tok * Dk, sizeof(double) * Dk);
+                if (l2norm) {
+                    l2_normalise(kt, Dk);
+                    l2_normalise(qt, Dk);
+                }
+                const double a = exp(g[tok]);
+                for (size_t e = 0; e < (size_t)Dk * Dv; ++e) S[e] *= a;
+                /* per-slice predictions from the decayed state */
+                for (int jj = 0; jj < r; ++jj) {
+                    double *zj = z + (size_t)jj * Dv;
+                    for (int c = 0; c < Dv; ++c) zj[c] = 0.0;
+                    for (int i = jj * dk; i < (jj + 1) * dk; ++i) {
+                        const double *row = S + (size_t)i * Dv;
+                        for (int c = 0; c < Dv; ++c) zj[c] += row[c] * kt[i];
+                    }
+                }
+                for (int ii = 0; ii < r; ++ii) {
+                    double *di = d + (size_t)ii * Dv;
+                    for (int c = 0; c < Dv; ++c) {
+                        double pr = 0.0;
+                        for (int jj = 0; jj < r; ++jj) pr += mask[ii * r + jj] * z[(size_t)jj * Dv + c];
+                        di[c] = beta[tok] * (v[tok * Dv + c] - pr);
+                    }
+                }
+                /* sub-row i writes the slice-i rows */
+                for (int ii = 0; ii < r; ++ii)
+                    for (int i = ii * dk; i < (ii + 1) * dk; ++i) {
+                        double *row = S + (size_t)i * Dv;
+                        for (int c = 0; c < Dv; ++c) row[c] += kt[i] * d[(size_t)ii * Dv + c];
+                    }
+                read_out(S, qt, scale, Dk, Dv, o + tok * Dv);
+            }
+            if (s_final)
+                memcpy(s_final + (size_t)bh * Dk * Dv, S, sizeof(double) * (size_t)Dk * Dv);
+        }
+        free(S);
+        free(z);
+        free(d);
         free(kt);
         free(qt);
     }

@@ -57,6 +57,34 @@ def deltaproduct_fwd(q, k, v, beta, g, initial_state=None, scale=1.0, l2norm=Fal
     return o, S_all
 
 
+def masked_deltaproduct_fwd(q, k, v, beta, g, mask, initial_state=None, scale=1.0, l2norm=False):
+    """Block-masked DeltaProduct: the state is r row blocks of Dk/r key rows;
+    per token the decay once, then sub-row i reads sum_j mask[i][j] of the
+    blocks' predictions and writes block i; all sub-rows from the same state."""
+    q, k, v, beta, g, mask = (np.asarray(a, np.float64) for a in (q, k, v, beta, g, mask))
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    r = mask.shape[0]
+    dk = Dk // r
+    if l2norm:
+        q, k = _unit(q), _unit(k)
+    o = np.zeros((B, H, T, Dv))
+    S_all = np.zeros((B, H, Dk, Dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((Dk, Dv)) if initial_state is None else np.array(initial_state[b, h], np.float64)
+            for t in range(T):
+                S = np.exp(g[b, h, t]) * S
+                kb = k[b, h, t].reshape(r, dk)
+                z = np.stack([kb[j] @ S[j * dk:(j + 1) * dk] for j in range(r)])  # [r, Dv]
+                d = beta[b, h, t] * (v[b, h, t][None, :] - mask @ z)
+                for i in range(r):
+                    S[i * dk:(i + 1) * dk] += np.outer(kb[i], d[i])
+                o[b, h, t] = scale * (S.T @ q[b, h, t])
+            S_all[b, h] = S
+    return o, S_all
+
+
 def cam_scan_fwd(q, k, v, beta, decay, initial_state=None, scale=1.0, reverse=False, l2norm=False):
     """Frame-level scan: per frame S <- d_f S, then the joint update
     S <- S + K_f^T diag(beta_f) (V_f - K_f S), and o = scale S^T q after it.
