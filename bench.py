@@ -444,6 +444,17 @@ def secondary(args, dev):
                      "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del d, o, wsw
         torch.cuda.empty_cache()
+    # the block-masked DeltaProduct variant (CUDA-core path)
+    w = WORKLOADS["masked_dp_r2_b4h16t4096d128_bf16"]
+    d = {k: v.to(dev) for k, v in w.make().items()}
+    o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+    ms = timeit(lambda: binding.masked_deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"],
+                                                              chunk=w.chunk, o=o))
+    nbytes = w.B * w.H * w.T * gdn_bytes_per_token_head(w.D)
+    out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                   "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "path": "CUDA cores, fp32"}
+    del d, o
+    torch.cuda.empty_cache()
     w = WORKLOADS["cam_b2n32760h16d128_bf16"]
     d = {k: (v.to(dev) if v is not None else None) for k, v in w.make().items()}
     outs = tuple(torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev) for _ in range(3))

@@ -26,7 +26,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
-           "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd")
+           "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd",
+           "masked_deltaproduct_chunk_fwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +63,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdn_chunk_fwd_noalloc.restype = i
         lib.deltaproduct_chunk_fwd.argtypes = [vp] * 8 + [i] * 7 + [f, u, i, vp, sz, vp]
         lib.deltaproduct_chunk_fwd.restype = i
+        lib.masked_deltaproduct_chunk_fwd.argtypes = [vp] * 9 + [i] * 7 + [f, u, i, vp]
+        lib.masked_deltaproduct_chunk_fwd.restype = i
         lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
         lib.cam_scan_fwd_workspace_bytes.restype = sz
         lib.cam_scan_fwd.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp, sz, vp]
@@ -201,6 +204,35 @@ def deltaproduct_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_st
     r = k.shape[3]
     return _scan("deltaproduct_chunk_fwd", q, k, v, beta, g, r, initial_state, output_final_state,
                  chunk, scale, l2norm, o, workspace, stream, simt)
+
+
+def masked_deltaproduct_chunk_fwd(q, k, v, beta, g, mask, initial_state=None, output_final_state=False,
+                                  chunk=64, scale=1.0, l2norm=False, o=None, stream=None):
+    """Block-masked DeltaProduct forward.  q, k [B,H,T,Dk]; v [B,H,T,Dv]; beta
+    [B,H,T] (all bf16 or all fp32); g [B,H,T] fp32; mask [r,r] fp32 (CUDA).
+    chunk counts sub-rows (tokens x r)."""
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    r = mask.shape[0]
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, T, Dk), dt)
+    _check(k, "k", (B, H, T, Dk), dt)
+    _check(v, "v", (B, H, T, Dv), dt)
+    _check(beta, "beta", (B, H, T), dt)
+    _check(g, "g", (B, H, T), torch.float32)
+    _check(mask, "mask", (r, r), torch.float32)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (B, H, Dk, Dv), torch.float32)
+    if o is None:
+        o = torch.empty(B, H, T, Dv, dtype=dt, device=q.device)
+    _check(o, "o", (B, H, T, Dv), dt)
+    sf = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=q.device) if output_final_state else None
+    st = load().masked_deltaproduct_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
+                                              _ptr(initial_state), _ptr(o), _ptr(sf), B, H, T, r, Dk, Dv, chunk,
+                                              float(scale), GDN_QK_L2NORM if l2norm else 0, code, _stream(stream))
+    _raise("masked_deltaproduct_chunk_fwd", st)
+    return o, sf
 
 
 def cam_scan_workspace_bytes(B, H, F, S, Dk, Dv, dtype=torch.bfloat16):

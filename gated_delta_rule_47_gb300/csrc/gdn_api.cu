@@ -161,6 +161,42 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
     return run_scan(a, stream);
 }
 
+int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                                  const float *g, const float *mask, const float *initial_state, void *o,
+                                  float *final_state, int B, int H, int T, int r, int Dk, int Dv, int chunk,
+                                  float scale, unsigned flags, int dtype, void *stream_v) {
+    if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return chunk <= 0 ? GDN_ERR_INVALID_ARG : GDN_ERR_UNSUPPORTED;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if (r > 8 || Dk % r != 0 || chunk % r != 0) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H * T != 0) {
+        if (!q || !k || !v || !beta || !g || !mask || !o) return GDN_ERR_INVALID_ARG;
+        const void *ps[] = {q, k, v, beta, g, mask, o};
+        for (const void *p : ps)
+            if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    }
+    if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
+        return GDN_ERR_MISALIGNED;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if ((long long)B * H == 0) return GDN_OK;
+    if (T == 0) {
+        if (final_state) {
+            const size_t bytes = sizeof(float) * (size_t)B * H * Dk * Dv;
+            cudaError_t e = initial_state
+                                ? cudaMemcpyAsync(final_state, initial_state, bytes, cudaMemcpyDeviceToDevice, stream)
+                                : cudaMemsetAsync(final_state, 0, bytes, stream);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    gdn::MaskedDpArgs a{q, k, v, beta, g, mask, initial_state, o, final_state, B, H, T, r, Dk, Dv, chunk,
+                        scale, flags, dtype};
+    return gdn::launch_masked_dp(a, stream);
+}
+
 size_t cam_scan_fwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, int dtype) {
     gdn::CamScanArgs a{};
     a.B = B; a.H = H; a.F = F; a.S = S; a.Dk = Dk; a.Dv = Dv; a.dtype = dtype; a.scale = 1.f;

@@ -68,6 +68,20 @@ struct CamScanArgs {
     size_t ws_bytes;
 };
 
+// Arguments of one block-masked DeltaProduct call: q,k [B,H,T,Dk], v,o
+// [B,H,T,Dv], beta,g [B,H,T], mask [r][r]; chunk counts sub-rows (tokens x r).
+struct MaskedDpArgs {
+    const void *q, *k, *v, *beta;
+    const float *g, *mask, *s0;
+    void *o;
+    float *sf;
+    int B, H, T, r, Dk, Dv, chunk;
+    float scale;
+    unsigned flags;
+    int dtype;
+};
+int launch_masked_dp(const MaskedDpArgs &a, cudaStream_t stream);
+
 // Frame scan: the tensor-core path (bf16, Dk = Dv = 128) needs a workspace of
 // cam_scan_workspace_bytes; everything else runs on the CUDA cores.
 bool cam_scan_tc_supported(const CamScanArgs &a);

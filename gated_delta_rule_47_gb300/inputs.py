@@ -89,6 +89,18 @@ def orthonormal_keys(B, H, T, D, seed):
     return qm[:, :T, :].reshape(B, H, T, D).float().contiguous()
 
 
+def slice_mask(r, seed):
+    """An r x r mask for the block-masked DeltaProduct: a random correlation
+    matrix (X X^T scaled to a unit diagonal, X ~ N(0,1)^{r x r}), fp32.  Being
+    positive semi-definite with a unit diagonal, it keeps the transition
+    I - beta (k k^T) o M contractive for unit keys and beta <= 1."""
+    gen = torch.Generator().manual_seed(int(seed))
+    x = torch.randn(r, r, generator=gen, dtype=torch.float64)
+    m = x @ x.T
+    d = torch.sqrt(torch.diagonal(m))
+    return (m / d[:, None] / d[None, :]).float().contiguous()
+
+
 def frame_gates(B, H, F, S, seed, dtype="bf16"):
     """Gates of the frame-level camera scan: beta [B,H,F*S] = sigmoid(N(0,1)) / S
     in ``dtype`` (each frame's S corrections enter at once, so their sum is
@@ -206,7 +218,7 @@ def cam_inputs(B, N, H, D, seed, dtype="bf16", tables=True, g_mu=0.0, g_div=16.0
 class Workload:
     """One named workload: sizes, dtype, distribution knobs and seed."""
     name: str
-    kind: str  # "gdn" | "deltaproduct" | "cam"
+    kind: str  # "gdn" | "deltaproduct" | "cam" | "masked_dp"
     B: int
     H: int
     T: int
@@ -229,6 +241,11 @@ class Workload:
             N = kw.pop("T")
             kw.pop("g_mu")
             return cam_inputs(kw["B"], N, kw["H"], self.D, kw["seed"], dtype=kw["dtype"])
+        if self.kind == "masked_dp":
+            out = gdn_inputs(kw["B"], kw["H"], kw["T"], self.D, self.D, kw["seed"], dtype=kw["dtype"],
+                             g_mu=kw["g_mu"])
+            out["mask"] = slice_mask(self.r, kw["seed"] + 1)
+            return out
         r = None if self.kind == "gdn" else self.r
         return gdn_inputs(kw["B"], kw["H"], kw["T"], self.D, self.D, kw["seed"], dtype=kw["dtype"],
                           g_mu=kw["g_mu"], r=r)
@@ -244,6 +261,11 @@ WORKLOADS = {
                                                     4, 16, 4096, 128, 64, "bf16", 3, r=2),
     "cam_b2n32760h16d128_bf16": Workload("cam_b2n32760h16d128_bf16", "cam", 2, 16, 21 * 30 * 52, 128, 64,
                                          "bf16", 4),
+    # the block-masked DeltaProduct variant at the DeltaProduct workload's sizes:
+    # one key, value and beta per token (GDN's distributions), r = 2 slices
+    # coupled by a random correlation mask; chunk counts sub-rows
+    "masked_dp_r2_b4h16t4096d128_bf16": Workload("masked_dp_r2_b4h16t4096d128_bf16", "masked_dp", 4, 16, 4096,
+                                                 128, 64, "bf16", 5, r=2),
 }
 
 
@@ -261,6 +283,7 @@ def split_heads_np(x, idx):
     return flat[list(idx)][None]
 
 
-__all__ = ["gdn_inputs", "cam_inputs", "mixed_decay", "orthonormal_keys", "frame_gates", "cam_scan_inputs", "rope_tables", "se3_poses", "se3_inverse",
+__all__ = ["gdn_inputs", "cam_inputs", "mixed_decay", "orthonormal_keys", "frame_gates", "cam_scan_inputs",
+           "slice_mask", "rope_tables", "se3_poses", "se3_inverse",
            "quaternion_rotations", "WORKLOADS", "Workload", "to_f64", "split_heads_np",
            "torch_dtype"]

@@ -172,6 +172,32 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
                            size_t workspace_bytes, void *stream);
 
 /*
+ * masked_deltaproduct_chunk_fwd -- block-masked DeltaProduct forward
+ * (gated_deltaproduct test.py: the mask_ij coupling of
+ * `gated_chunk_scaled_dot_kkt_fwd_kernel` and `gated_fwd_recompute_w_u_kernel`,
+ * the per-slice state update of `gated_chunk_delta_rule_fwd_kernel_h`, and the
+ * sum over r of `gated_chunk_fwd_o_fn`).  The key dimension is cut into r
+ * slices of Dk/r; per token the decay is applied once, then each sub-row
+ * i < r predicts from that same state with k_t masked slice-wise by
+ * mask[i][:] and corrects the state's slice-i rows with slice i of k_t; one
+ * value and one beta per token:
+ *     S <- exp(g_t) S;   z_j = S_(j)^T k_t,(j);   d_i = beta_t (v_t - sum_j mask[i][j] z_j)
+ *     S_(i) <- S_(i) + k_t,(i) d_i^T   (every i from the same z);   o_t = scale * S^T q_t
+ * i.e. S_t = exp(g_t) (I - beta_t (k_t k_t^T) o M) S_{t-1} + beta_t k_t v_t^T with M
+ * the mask expanded to Dk/r x Dk/r blocks.  An all-ones mask is gdn_chunk_fwd.
+ *
+ *   q, k [B,H,T,Dk]; v, o [B,H,T,Dv]; beta [B,H,T] (all dtype); g [B,H,T] fp32
+ *   mask [r][r] fp32 (device), shared by all heads; 1 <= r <= 8, r | Dk
+ *   chunk   sub-rows per chunk (16, 32 or 64, a multiple of r): chunk / r tokens
+ *   flags   0 or GDN_QK_L2NORM.  CUDA-core path, fp32 arithmetic.
+ * State, scale, dtype and the empty cases as gdn_chunk_fwd.
+ */
+int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
+                                  const float *g, const float *mask, const float *initial_state, void *o,
+                                  float *final_state, int B, int H, int T, int r, int Dk, int Dv, int chunk,
+                                  float scale, unsigned flags, int dtype, void *stream);
+
+/*
  * Bytes of device workspace cam_scan_fwd needs for these sizes on the current
  * device (0 on the CUDA-core path).  (size_t)-1 for sizes it rejects.
  */

@@ -135,3 +135,20 @@ def test_cam_scan_argument_checks(lib):
     assert q(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 0         # the CUDA-core path needs none
     assert q(1, 2, 3, 0, 64, 64, binding.GDN_F32) == bad
     assert q(1, 2, 3, 5, 96, 64, binding.GDN_F32) == bad
+
+
+def test_masked_deltaproduct_argument_checks(lib):
+    f = lib.masked_deltaproduct_chunk_fwd
+    u = 0x10000
+
+    def call(r=2, Dk=64, chunk=64, flags=0, mask=u, q=u, dtype=binding.GDN_F32):
+        return f(q, u, u, u, u, mask, None, u, None, 1, 2, 8, r, Dk, 64, chunk, 1.0, flags, dtype, None)
+
+    assert call(r=3) == 2          # r must divide Dk
+    assert call(r=16, Dk=128) == 2  # r <= 8
+    assert call(chunk=48) == 2
+    assert call(chunk=0) == 1
+    assert call(flags=2) == 1      # only GDN_QK_L2NORM
+    assert call(mask=None) == 1
+    assert call(q=u + 4) == 3
+    assert call(dtype=3) == 1
