@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "tri_inverse.cuh"
 
 namespace gdn {
 namespace {
@@ -50,7 +51,8 @@ struct MdpSmem {
     static constexpr int KP = DK + 1, VP = kBV + 1, CP = C + 1;
     // Ks, Qs [C][KP]; Vs [C][VP]; Ss [DK][VP]; As, Ts, Ps [C][CP]; Rs, Ds [C][VP];
     // gam, bet, eS [C]; mask [kMaxR * kMaxR]
-    static constexpr int floats = 2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C + kMaxR * kMaxR;
+    static constexpr int floats =
+        2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C + kMaxR * kMaxR + C * C / 4;
     static constexpr size_t bytes = sizeof(float) * floats;
 };
 
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) masked_dp_kernel(MdpParams p) {
     float *bet = gam + C;        // [CQ]
     float *eS = bet + C;         // [CQ] exp(gam_last - gam_s)
     float *msk = eS + C;         // [r][r]
+    float *Xs = msk + kMaxR * kMaxR;  // [C*C/4] scratch of the blocked inverse
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vt = blockIdx.x;
@@ -188,16 +191,8 @@ __global__ void __launch_bounds__(kThreads) masked_dp_kernel(MdpParams p) {
             for (int j = 0; j < r; ++j) pr += msk[i * r + j] * Ds[(t * r + j) * VP + c];
             Rs[rho * VP + c] = bet[t] * (Vs[t * VP + c] - expf(gam[t]) * pr);
         }
-        // (I + A)^-1 by forward substitution, one column per thread
-        if (tid < C) {
-            const int j = tid;
-            for (int i = 0; i < C; ++i) {
-                float x = (i == j) ? 1.f : 0.f;
-                for (int kk = 0; kk < i; ++kk) x -= As[i * CP + kk] * Ts[kk * CP + j];
-                Ts[i * CP + j] = x;
-            }
-        }
-        __syncthreads();
+        // (I + A)^-1: 16 x 16 diagonal blocks, then the 16- and 32-level merges
+        unit_lower_inverse<C, kThreads>(As, Ts, Xs, CP);
         // Delta = (I + A)^-1 R
         for (int e = tid; e < C * kBV; e += kThreads) {
             const int rho = e / kBV, c = e % kBV;

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "tri_inverse.cuh"
 
 namespace gdn {
 namespace {
@@ -44,7 +45,7 @@ struct SimtParams {
 template <int DK, int C>
 struct SimtSmem {
     static constexpr int KP = DK + 1, VP = kBV + 1, CP = C + 1;
-    static constexpr int floats = 2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C;
+    static constexpr int floats = 2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C + C * C / 4;
     static constexpr size_t bytes = sizeof(float) * floats;
 };
 
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
     float *gam = Ds + C * VP;    // [C]
     float *bet = gam + C;        // [C]
     float *eS = bet + C;         // [C] exp(gam_last - gam_s)
+    float *Xs = eS + C;          // [C*C/4] scratch of the blocked inverse
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vt = blockIdx.x;
@@ -179,16 +181,8 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
             Rs[t * VP + j] = bet[t] * (Vs[t * VP + j] - expf(gam[t]) * acc);
         }
         __syncthreads();
-        // (I + A)^-1 by forward substitution, one column per thread.
-        if (tid < C) {
-            const int j = tid;
-            for (int i = 0; i < C; ++i) {
-                float x = (i == j) ? 1.f : 0.f;
-                for (int kk = 0; kk < i; ++kk) x -= As[i * CP + kk] * Ts[kk * CP + j];
-                Ts[i * CP + j] = x;
-            }
-        }
-        __syncthreads();
+        // (I + A)^-1: 16 x 16 diagonal blocks, then the 16- and 32-level merges
+        unit_lower_inverse<C, kThreads>(As, Ts, Xs, CP);
         // Delta = (I + A)^-1 R
         for (int i = tid; i < C * kBV; i += kThreads) {
             const int t = i / kBV, j = i % kBV;
