@@ -489,6 +489,17 @@ def secondary(args, dev):
             "hbm_frac": frame_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "tokens_per_s_with_prep": w.B * w.T / ((pre_ms + ms) * 1e-3)}
     out["cam_frames_b2f21s1560h16d128_bf16"] = dict(res, alg_bytes=frame_bytes, launches_per_call=3)
+    # the prep fused into the frame scan: raw q, k, v in, o out, one call
+    wsx = torch.empty(binding.cam_prep_scan_workspace_bytes(w.B, w.T, w.H, w.D, F), dtype=torch.uint8, device=dev)
+    C = w.H * w.D
+    fused_bytes = w.B * w.T * (3 * C * 2 + 2 * 16 * 4 + C * 2 + w.H * 2)
+    ms = timeit(lambda: binding.cam_prep_scan_fwd(d["q_raw"], d["k_raw"], d["v_raw"], d["proj_q"], d["proj_kv"],
+                                                  beta_f, decay_f, d["q_norm_w"], d["k_norm_w"], rope_base=10000.0,
+                                                  o=o, workspace=wsx))
+    out["cam_prep_frames_fused_b2n32760h16d128_bf16"] = {
+        "ms": ms, "gbs": fused_bytes / (ms * 1e-3) / 1e9, "hbm_frac": fused_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "alg_bytes": fused_bytes, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+        "unfused_ms": pre_ms + res["forward"]["ms"], "launches_per_call": 4}
     return out
 
 

@@ -27,7 +27,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
            "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd",
-           "masked_deltaproduct_chunk_fwd")
+           "masked_deltaproduct_chunk_fwd", "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +65,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.deltaproduct_chunk_fwd.restype = i
         lib.masked_deltaproduct_chunk_fwd.argtypes = [vp] * 9 + [i] * 7 + [f, u, i, vp]
         lib.masked_deltaproduct_chunk_fwd.restype = i
+        lib.cam_prep_scan_fwd_workspace_bytes.argtypes = [i] * 6
+        lib.cam_prep_scan_fwd_workspace_bytes.restype = sz
+        lib.cam_prep_scan_fwd.argtypes = [vp] * 7 + [f] + [vp] * 5 + [i] * 5 + [f, f, f, u, i, vp, sz, vp]
+        lib.cam_prep_scan_fwd.restype = i
         lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
         lib.cam_scan_fwd_workspace_bytes.restype = sz
         lib.cam_scan_fwd.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp, sz, vp]
@@ -276,6 +280,54 @@ def cam_scan_fwd(q, k, v, beta, decay, initial_state=None, output_final_state=Fa
                              _ptr(sf), B, H, F, S, Dk, Dv, float(scale), flags, code, _ptr(workspace), ws_bytes,
                              _stream(stream))
     _raise("cam_scan_fwd", st)
+    return o, sf
+
+
+def cam_prep_scan_workspace_bytes(B, N, H, D, F, dtype=torch.bfloat16):
+    code = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    n = load().cam_prep_scan_fwd_workspace_bytes(B, N, H, D, F, code)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("sizes rejected by cam_prep_scan_fwd_workspace_bytes")
+    return int(n)
+
+
+def cam_prep_scan_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, beta, decay, q_norm_w=None, k_norm_w=None,
+                      rope_base=10000.0, initial_state=None, output_final_state=False, k_scale=0.5, eps=1e-6,
+                      scale=1.0, reverse=False, l2norm=True, o=None, workspace=None, stream=None):
+    """Camera prep fused into the frame scan: raw q, k, v [B,N,H,D] bf16 ->
+    o [B,H,N,D] = cam_scan_fwd(cam_prep_fwd(...)).  beta [B,H,N] bf16, decay
+    [B,H,F] fp32 factors; rotation angles n * rope_base^(-2i/(D/2))."""
+    B, N, H, D = q_raw.shape
+    F = decay.shape[-1]
+    if F <= 0 or N % F != 0:
+        raise ValueError(f"{N} tokens do not split into {F} frames")
+    dt = q_raw.dtype
+    code = _dtype_code(q_raw)
+    for name, t in (("q_raw", q_raw), ("k_raw", k_raw), ("v_raw", v_raw)):
+        _check(t, name, (B, N, H, D), dt)
+    _check(proj_q, "proj_q", (B, N, 4, 4), torch.float32)
+    _check(proj_kv, "proj_kv", (B, N, 4, 4), torch.float32)
+    _check(beta, "beta", (B, H, N), dt)
+    _check(decay, "decay", (B, H, F), torch.float32)
+    for name, t in (("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+        if t is not None:
+            _check(t, name, (H * D,), torch.float32)
+    if initial_state is not None:
+        _check(initial_state, "initial_state", (B, H, D, D), torch.float32)
+    if o is None:
+        o = torch.empty(B, H, N, D, dtype=dt, device=q_raw.device)
+    _check(o, "o", (B, H, N, D), dt)
+    sf = torch.empty(B, H, D, D, dtype=torch.float32, device=q_raw.device) if output_final_state else None
+    if workspace is None:
+        workspace = torch.empty(cam_prep_scan_workspace_bytes(B, N, H, D, F, dt), dtype=torch.uint8,
+                                device=q_raw.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_CAM_REVERSE if reverse else 0)
+    st = load().cam_prep_scan_fwd(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(q_norm_w), _ptr(k_norm_w),
+                                  _ptr(proj_q), _ptr(proj_kv), float(rope_base), _ptr(beta), _ptr(decay),
+                                  _ptr(initial_state), _ptr(o), _ptr(sf), B, N, H, D, F, float(k_scale), float(eps),
+                                  float(scale), flags, code, _ptr(workspace), ws_bytes, _stream(stream))
+    _raise("cam_prep_scan_fwd", st)
     return o, sf
 
 

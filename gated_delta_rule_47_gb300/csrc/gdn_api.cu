@@ -231,6 +231,44 @@ int cam_scan_fwd(const void *q, const void *k, const void *v, const void *beta, 
     return gdn::launch_cam_scan(a, stream);
 }
 
+size_t cam_prep_scan_fwd_workspace_bytes(int B, int N, int H, int D, int F, int dtype) {
+    if (B < 0 || N < 0 || H < 1 || F < 1 || N % F != 0) return (size_t)-1;
+    if (dtype != GDN_BF16 || D != 128 || (long long)H * D > 4096) return (size_t)-1;
+    gdn::CamFusedArgs a{};
+    a.B = B; a.H = H; a.F = F; a.S = N / F;
+    return gdn::cam_fused_workspace_bytes(a);
+}
+
+int cam_prep_scan_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *q_norm_w,
+                      const float *k_norm_w, const float *proj_q, const float *proj_kv, float rope_base,
+                      const void *beta, const float *decay, const float *initial_state, void *o,
+                      float *final_state, int B, int N, int H, int D, int F, float k_scale, float eps, float scale,
+                      unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream_v) {
+    if (B < 0 || N < 0 || H < 1 || F < 1) return GDN_ERR_INVALID_ARG;
+    if (N % F != 0 || (N > 0 && N / F == 0)) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_CAM_REVERSE)) return GDN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (!(rope_base > 0.f)) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_BF16 || D != 128 || (long long)H * D > 4096) return GDN_ERR_UNSUPPORTED;
+    if ((flags & GDN_CAM_REVERSE) && (initial_state || final_state)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535 || (long long)N * H * D >= (1LL << 40)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * N != 0) {
+        if (!q_raw || !k_raw || !v_raw || !proj_q || !proj_kv || !beta || !decay || !o) return GDN_ERR_INVALID_ARG;
+    }
+    const void *ps[] = {q_raw, k_raw, v_raw, q_norm_w, k_norm_w, proj_q, proj_kv, beta, decay, initial_state, o,
+                        final_state};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::CamFusedArgs a{q_raw, k_raw, v_raw, q_norm_w, k_norm_w, proj_q, proj_kv, rope_base, beta, decay,
+                        initial_state, o, final_state, B, H, F, N / F, k_scale, eps, scale, flags, workspace,
+                        workspace_bytes};
+    const size_t need = gdn::cam_fused_workspace_bytes(a);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
+    if ((long long)B * N == 0) return GDN_OK;
+    return gdn::launch_cam_fused(a, static_cast<cudaStream_t>(stream_v));
+}
+
 int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *q_norm_w,
                  const float *k_norm_w, const float *proj_q, const float *proj_kv,
                  const float *rope_cos, const float *rope_sin, float rope_base, void *q_out,

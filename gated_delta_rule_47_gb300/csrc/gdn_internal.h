@@ -89,6 +89,25 @@ size_t cam_scan_workspace_bytes(const CamScanArgs &a);
 int launch_cam_scan(const CamScanArgs &a, cudaStream_t stream);
 int cam_scan_read_clear_error();
 
+// The camera prep fused into the frame scan (bf16, D = 128, rotary angles
+// from the base): raw q, k, v [B,N,H,128]; the scan's beta [B,H,N], decay [B,H,F].
+struct CamFusedArgs {
+    const void *q_raw, *k_raw, *v_raw;
+    const float *q_norm_w, *k_norm_w, *proj_q, *proj_kv;
+    float rope_base;
+    const void *beta;
+    const float *decay, *s0;
+    void *o;
+    float *sf;
+    int B, H, F, S;
+    float k_scale, eps, scale;
+    unsigned flags;
+    void *ws;
+    size_t ws_bytes;
+};
+size_t cam_fused_workspace_bytes(const CamFusedArgs &a);
+int launch_cam_fused(const CamFusedArgs &a, cudaStream_t stream);
+
 // 3-D TMA map (128-byte swizzle) over a [heads][rows][128] bf16 tensor with a
 // {box0, box1, 1} box; false if the driver entry point is missing or rejects it.
 bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int box0, int box1);
@@ -97,6 +116,10 @@ bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int b
 // row is clipped there (zero-filled on loads, not written on stores).
 bool make_bf16_frame_map(CUtensorMap *m, const void *base, int heads, int frames, int frame_rows, int box0,
                          int box1);
+// As make_bf16_frame_map over a [outer][frames][frame_rows][cols] tensor with
+// rows of `cols` bf16 (cols a multiple of 64).
+bool make_bf16_frame_map_wide(CUtensorMap *m, const void *base, int outer, int frames, int frame_rows, int cols,
+                              int box0, int box1);
 // True on an sm_10x device (tcgen05 available); cached.
 bool sm100_family();
 int device_sm_count();

@@ -1501,10 +1501,16 @@ bool make_bf16_map(CUtensorMap *m, const void *base, int heads, long rows, int b
 
 bool make_bf16_frame_map(CUtensorMap *m, const void *base, int heads, int frames, int frame_rows, int box0,
                          int box1) {
+    return make_bf16_frame_map_wide(m, base, heads, frames, frame_rows, 128, box0, box1);
+}
+
+bool make_bf16_frame_map_wide(CUtensorMap *m, const void *base, int outer, int frames, int frame_rows, int cols,
+                              int box0, int box1) {
     auto enc = encoder();
     if (!enc) return false;
-    cuuint64_t dims[4] = {128, (cuuint64_t)frame_rows, (cuuint64_t)frames, (cuuint64_t)heads};
-    cuuint64_t strides[3] = {256, (cuuint64_t)frame_rows * 256, (cuuint64_t)frame_rows * frames * 256};
+    const cuuint64_t rb = (cuuint64_t)cols * 2;  // bytes per row
+    cuuint64_t dims[4] = {(cuuint64_t)cols, (cuuint64_t)frame_rows, (cuuint64_t)frames, (cuuint64_t)outer};
+    cuuint64_t strides[3] = {rb, (cuuint64_t)frame_rows * rb, (cuuint64_t)frame_rows * frames * rb};
     cuuint32_t box[4] = {(cuuint32_t)box0, (cuuint32_t)box1, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,

@@ -238,6 +238,39 @@ int cam_scan_fwd(const void *q, const void *k, const void *v, const void *beta, 
                  size_t workspace_bytes, void *stream);
 
 /*
+ * Bytes of device workspace cam_prep_scan_fwd needs; (size_t)-1 for sizes it
+ * rejects.
+ */
+size_t cam_prep_scan_fwd_workspace_bytes(int B, int N, int H, int D, int F, int dtype);
+
+/*
+ * cam_prep_scan_fwd -- the camera prep fused into the frame scan
+ * (fused_cam_gdn.py: `cam_prep_func`, whose `_precompute_cam_inv_rms` is the
+ * separate reduction pass, then `_cam_scan_kernel`): computes
+ * cam_scan_fwd(cam_prep_fwd(raw ...)) without writing the prepped q, k, v.
+ * A pre-pass forms each token's full-C inverse RMS of q and k; the frame
+ * scan then reads the raw rows and applies the norm (with the weights), ReLU
+ * and K-scale, the 4 x 4 projection and the rotation at load.
+ *
+ *   q_raw, k_raw, v_raw [B,N,H,D] bf16; q_norm_w, k_norm_w [H*D] fp32 or NULL;
+ *   proj_q, proj_kv [B,N,4,4] fp32;
+ *   rope_base > 0: the rotation angles th_i = n * rope_base^(-2i/(D/2)) of
+ *   cam_prep_fwd without tables (this path takes no tables);
+ *   beta [B,H,N] bf16, decay [B,H,F] fp32 factors, o [B,H,N,D] bf16,
+ *   initial_state / final_state as cam_scan_fwd (forward only);
+ *   N = F * S; D = 128, H*D <= 4096, bf16 only; flags: GDN_QK_L2NORM (unit
+ *   prepped q and k), GDN_CAM_REVERSE; workspace of
+ *   cam_prep_scan_fwd_workspace_bytes bytes, 16-byte aligned.
+ * The k norms before and after the projection (cam_prep_fwd's k_pre_sq and
+ * k_post_sq) are not produced.
+ */
+int cam_prep_scan_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *q_norm_w,
+                      const float *k_norm_w, const float *proj_q, const float *proj_kv, float rope_base,
+                      const void *beta, const float *decay, const float *initial_state, void *o,
+                      float *final_state, int B, int N, int H, int D, int F, float k_scale, float eps, float scale,
+                      unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * cam_prep_fwd -- fused camera-branch prep (fused_cam_gdn.py, `_cam_prep_kernel`
  * and `_torch_cam_prep_reference`), one pass over q, k, v:
  *   1. full-C RMSNorm of q and k per token, C = H*D:

@@ -152,3 +152,24 @@ def test_masked_deltaproduct_argument_checks(lib):
     assert call(mask=None) == 1
     assert call(q=u + 4) == 3
     assert call(dtype=3) == 1
+
+
+def test_cam_prep_scan_argument_checks(lib):
+    f = lib.cam_prep_scan_fwd
+    u = 0x10000
+
+    def call(D=128, F=3, N=30, H=2, dtype=binding.GDN_BF16, base=10000.0, flags=0, s0=None, ws=u, wsb=1 << 30):
+        return f(u, u, u, None, None, u, u, base, u, u, s0, u, None, 1, N, H, D, F, 0.5, 1e-6, 1.0, flags, dtype,
+                 ws, wsb, None)
+
+    assert call(D=64) == 2
+    assert call(H=33) == 2                              # H * D <= 4096
+    assert call(dtype=binding.GDN_F32) == 2
+    assert call(base=0.0) == 1
+    assert call(flags=binding.GDN_CAM_REVERSE, s0=u) == 2
+    assert call(N=31) == 1                              # N is not a whole number of frames
+    assert call(flags=2) == 1                           # no CUDA-core switch here
+    assert call(ws=None) == 4
+    q = lib.cam_prep_scan_fwd_workspace_bytes
+    assert q(1, 30, 2, 128, 3, binding.GDN_BF16) == 2 * 3 * 131072 + 30 * 8
+    assert q(1, 30, 2, 64, 3, binding.GDN_BF16) == ctypes.c_size_t(-1).value
