@@ -68,6 +68,8 @@ def _load():
             lib.oracle_cam_scan_fwd.restype = i
             lib.oracle_cam_prep_fwd.argtypes = [_dp] * 9 + [d] + [_dp] * 5 + [i] * 4 + [d, d]
             lib.oracle_cam_prep_fwd.restype = i
+            lib.oracle_cam_prep_bwd.argtypes = [_dp] * 8 + [d] + [_dp] * 8 + [i] * 4 + [d, d]
+            lib.oracle_cam_prep_bwd.restype = i
             lib.oracle_max_threads.restype = i
             lib.oracle_set_threads.argtypes = [i]
             _lib = lib
@@ -221,6 +223,28 @@ def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=N
     if rc != 0:
         raise MemoryError("oracle_cam_prep_fwd failed")
     return outs[0], outs[1], outs[2], pre, post
+
+
+def cam_prep_bwd(q_raw, k_raw, v_raw, proj_q, proj_kv, dq_out, dk_out, dv_out, dk_pre_sq=None,
+                 dk_post_sq=None, q_norm_w=None, k_norm_w=None, rope_cos=None, rope_sin=None, rope_base=10000.0,
+                 k_scale=0.5, eps=1e-6):
+    """fp64 backward of ``cam_prep_fwd``: the gradients of the raw q, k, v
+    [B,N,H,D] given those of q_out, k_out, v_out [B,H,N,D] and of k_pre_sq,
+    k_post_sq [B,H,N] (None = zero)."""
+    q_raw, k_raw, proj_q, proj_kv, dq_out, dk_out, dv_out = map(
+        _f64, (q_raw, k_raw, proj_q, proj_kv, dq_out, dk_out, dv_out))
+    dpre, dpost, q_norm_w, k_norm_w, rope_cos, rope_sin = map(
+        _f64, (dk_pre_sq, dk_post_sq, q_norm_w, k_norm_w, rope_cos, rope_sin))
+    B, N, H, D = q_raw.shape
+    assert D <= 512
+    outs = [np.empty((B, N, H, D), np.float64) for _ in range(3)]
+    rc = _load().oracle_cam_prep_bwd(_ptr(q_raw), _ptr(k_raw), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(proj_q),
+                                     _ptr(proj_kv), _ptr(rope_cos), _ptr(rope_sin), float(rope_base), _ptr(dq_out),
+                                     _ptr(dk_out), _ptr(dv_out), _ptr(dpre), _ptr(dpost), _ptr(outs[0]),
+                                     _ptr(outs[1]), _ptr(outs[2]), B, N, H, D, float(k_scale), float(eps))
+    if rc != 0:
+        raise MemoryError("oracle_cam_prep_bwd failed")
+    return tuple(outs)
 
 
 def inflation_sq(k_pre_sq, k_post_sq):

@@ -48,6 +48,11 @@
  *    from last to first, each frame's output reading the state built from
  *    the frames after it only (the last frame reads zero).
  *
+ *  - Backward of the camera prep (fused_cam_gdn.py, `_cam_prep_bwd_kernel`,
+ *    continued through the full-C RMSNorm): the adjoint of the prep map from
+ *    the raw rows to q_out, k_out, v_out, k_pre_sq and k_post_sq, written as
+ *    the chain rule of the forward steps in reverse order.
+ *
  *  - Camera prep (fused_cam_gdn.py, `_torch_cam_prep_reference` and
  *    `_cam_prep_kernel`): full-C RMSNorm (C = H*D) with per-channel weight on
  *    q and k, ReLU on q and k, K-scale on k, a 4x4 projection out = P*in on
@@ -494,6 +499,139 @@ int oracle_cam_prep_fwd(const double *q_raw, const double *k_raw, const double *
         free(xv);
         free(cs);
         free(sn);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Backward of the camera prep: given the gradients of q_out, k_out, v_out
+ * ([B,H,N,D]) and of k_pre_sq, k_post_sq ([B,H,N], each may be NULL = zero),
+ * the gradients of q_raw, k_raw, v_raw ([B,N,H,D]).  Same arguments and
+ * tables as oracle_cam_prep_fwd.  Per token, in reverse order of the forward:
+ *   rotation:   dx[d] = dy[d] cos[d] + dy[d^1] sin[d^1]        (last D/2 dims)
+ *   projection: dx_j = sum_i P[i][j] dy_i                       (first D/2 dims)
+ *   k_post_sq:  dk_out += 2 k_out dpost;  k_pre_sq: da_k += 2 a_k dpre
+ *   K-scale, ReLU: dxhat = k_scale [xhat > 0] da  (q: no K-scale)
+ *   RMSNorm:    xhat_c = x_c r w_c, r = (sum x^2 / C + eps)^(-1/2):
+ *               dx_j = r w_j dxhat_j - (r^3 / C) x_j sum_c w_c x_c dxhat_c
+ *   v: the projection and rotation only.
+ */
+int oracle_cam_prep_bwd(const double *q_raw, const double *k_raw, const double *q_norm_w,
+                        const double *k_norm_w, const double *proj_q, const double *proj_kv,
+                        const double *rope_cos, const double *rope_sin, double rope_base,
+                        const double *dq_out, const double *dk_out, const double *dv_out,
+                        const double *dpre, const double *dpost, double *dq_raw, double *dk_raw,
+                        double *dv_raw, int B, int N, int H, int D, double k_scale, double eps) {
+    if (D % 2 != 0 || (D / 2) % 4 != 0) return -2;
+    const int C = H * D, Dh = D / 2;
+    const long BN = (long)B * N;
+    int failed = 0;
+#pragma omp parallel for schedule(static) reduction(| : failed)
+    for (long bn = 0; bn < BN; ++bn) {
+        const int b = (int)(bn / N), n = (int)(bn % N);
+        double *cs = (double *)malloc(sizeof(double) * Dh);
+        double *sn = (double *)malloc(sizeof(double) * Dh);
+        double *dxq = (double *)malloc(sizeof(double) * C);  /* gradient of xhat_q (per channel) */
+        double *dxk = (double *)malloc(sizeof(double) * C);
+        double *ak = (double *)malloc(sizeof(double) * D);
+        double *ko = (double *)malloc(sizeof(double) * D);
+        double *gk = (double *)malloc(sizeof(double) * D);
+        if (!cs || !sn || !dxq || !dxk || !ak || !ko || !gk) {
+            failed |= 1;
+        } else {
+            const double *qr = q_raw + (size_t)bn * C, *kr = k_raw + (size_t)bn * C;
+            double ssq = 0.0, ssk = 0.0;
+            for (int c = 0; c < C; ++c) {
+                ssq += qr[c] * qr[c];
+                ssk += kr[c] * kr[c];
+            }
+            const double iq = 1.0 / sqrt(ssq / C + eps), ik = 1.0 / sqrt(ssk / C + eps);
+            for (int d = 0; d < Dh; ++d) {
+                if (rope_cos && rope_sin) {
+                    cs[d] = rope_cos[(size_t)n * Dh + d];
+                    sn[d] = rope_sin[(size_t)n * Dh + d];
+                } else {
+                    const int i = d / 2;
+                    const double th = (double)n * pow(rope_base, -2.0 * i / (double)Dh);
+                    cs[d] = cos(th);
+                    sn[d] = (d % 2 == 0) ? -sin(th) : sin(th);
+                }
+            }
+            const double *Pq = proj_q + (size_t)bn * 16, *Pk = proj_kv + (size_t)bn * 16;
+            for (int h = 0; h < H; ++h) {
+                const size_t ob = (((size_t)b * H + h) * N + n) * D;
+                const size_t si = ((size_t)b * H + h) * N + n;
+                const double gpre = dpre ? dpre[si] : 0.0, gpost = dpost ? dpost[si] : 0.0;
+                /* forward values of k needed by the norm-square terms */
+                for (int d = 0; d < D; ++d) {
+                    const int c = h * D + d;
+                    const double x = kr[c] * ik * (k_norm_w ? k_norm_w[c] : 1.0);
+                    ak[d] = (x > 0.0 ? x : 0.0) * k_scale;
+                }
+                for (int g0 = 0; g0 < Dh; g0 += 4)
+                    for (int i = 0; i < 4; ++i) {
+                        double acc = 0.0;
+                        for (int j = 0; j < 4; ++j) acc += Pk[i * 4 + j] * ak[g0 + j];
+                        ko[g0 + i] = acc;
+                    }
+                for (int d = 0; d < Dh; ++d) {
+                    const int e = Dh + d, pe = Dh + (d ^ 1);
+                    ko[e] = ak[e] * cs[d] + ak[pe] * sn[d];
+                }
+                /* gradient reaching k_out, including ||k_out||^2 */
+                for (int d = 0; d < D; ++d) gk[d] = dk_out[ob + d] + 2.0 * ko[d] * gpost;
+                for (int t = 0; t < 3; ++t) {
+                    const double *dy = t == 0 ? dq_out + ob : (t == 1 ? gk : dv_out + ob);
+                    const double *P = t == 0 ? Pq : Pk;
+                    double *out = t == 2 ? dv_raw + (size_t)bn * C + h * D : NULL;
+                    double da[512];
+                    for (int g0 = 0; g0 < Dh; g0 += 4)
+                        for (int j = 0; j < 4; ++j) {
+                            double acc = 0.0;
+                            for (int i = 0; i < 4; ++i) acc += P[i * 4 + j] * dy[g0 + i];
+                            da[g0 + j] = acc;
+                        }
+                    for (int d = 0; d < Dh; ++d) {
+                        const int e = Dh + d, pe = Dh + (d ^ 1);
+                        da[e] = dy[e] * cs[d] + dy[pe] * sn[d ^ 1];
+                    }
+                    if (t == 2) {
+                        for (int d = 0; d < D; ++d) out[d] = da[d];
+                    } else {
+                        for (int d = 0; d < D; ++d) {
+                            const int c = h * D + d;
+                            if (t == 0) {
+                                const double x = qr[c] * iq * (q_norm_w ? q_norm_w[c] : 1.0);
+                                dxq[c] = x > 0.0 ? da[d] : 0.0;
+                            } else {
+                                const double x = kr[c] * ik * (k_norm_w ? k_norm_w[c] : 1.0);
+                                const double dak = da[d] + 2.0 * ak[d] * gpre;
+                                dxk[c] = x > 0.0 ? k_scale * dak : 0.0;
+                            }
+                        }
+                    }
+                }
+            }
+            /* RMSNorm over all C channels of the token */
+            double sq = 0.0, sk = 0.0;
+            for (int c = 0; c < C; ++c) {
+                sq += (q_norm_w ? q_norm_w[c] : 1.0) * qr[c] * dxq[c];
+                sk += (k_norm_w ? k_norm_w[c] : 1.0) * kr[c] * dxk[c];
+            }
+            for (int c = 0; c < C; ++c) {
+                dq_raw[(size_t)bn * C + c] =
+                    iq * (q_norm_w ? q_norm_w[c] : 1.0) * dxq[c] - iq * iq * iq / C * qr[c] * sq;
+                dk_raw[(size_t)bn * C + c] =
+                    ik * (k_norm_w ? k_norm_w[c] : 1.0) * dxk[c] - ik * ik * ik / C * kr[c] * sk;
+            }
+        }
+        free(cs);
+        free(sn);
+        free(dxq);
+        free(dxk);
+        free(ak);
+        free(ko);
+        free(gk);
     }
     return failed ? -1 : 0;
 }
