@@ -473,6 +473,15 @@ def secondary(args, dev):
     out[w.name] = {"prep_ms": pre_ms, "prep_gbs": prep_bytes / (pre_ms * 1e-3) / 1e9,
                    "prep_hbm_frac": prep_bytes / (pre_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                    "scan_ms": scan_ms, "tokens_per_s": w.B * w.T / ((pre_ms + scan_ms) * 1e-3)}
+    # the prep's backward at the same size (gradients of q, k, v out -> raw)
+    gq, gk, gv = (torch.randn(w.B, w.H, w.T, w.D, device=dev, dtype=torch.bfloat16) for _ in range(3))
+    bwd_ms = timeit(lambda: binding.cam_prep_bwd(d["q_raw"], d["k_raw"], d["proj_q"], d["proj_kv"], gq, gk, gv,
+                                                 None, None, d["q_norm_w"], d["k_norm_w"], d["rope_cos"],
+                                                 d["rope_sin"]))
+    bwd_bytes = w.B * w.T * (2 * C * 2 + 3 * C * 2 + 3 * C * 2 + 2 * 16 * 4)  # raw q, k + 3 grads in, 3 out
+    out["cam_prep_bwd_b2n32760h16d128_bf16"] = {"ms": bwd_ms, "gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
+                                                "hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    del gq, gk, gv
     # the camera branch's own frame-level scan on the prep output: 21 frames of
     # 30 x 52 tokens, unit-norm q and k, beta / S per token, one decay per frame
     from gated_delta_rule_47_gb300.inputs import frame_gates

@@ -27,7 +27,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
            "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd",
-           "masked_deltaproduct_chunk_fwd", "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd")
+           "masked_deltaproduct_chunk_fwd", "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd",
+           "cam_prep_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.cam_prep_scan_fwd_workspace_bytes.restype = sz
         lib.cam_prep_scan_fwd.argtypes = [vp] * 7 + [f] + [vp] * 5 + [i] * 5 + [f, f, f, u, i, vp, sz, vp]
         lib.cam_prep_scan_fwd.restype = i
+        lib.cam_prep_bwd.argtypes = [vp] * 8 + [f] + [vp] * 8 + [i] * 4 + [f, f, i, vp]
+        lib.cam_prep_bwd.restype = i
         lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
         lib.cam_scan_fwd_workspace_bytes.restype = sz
         lib.cam_scan_fwd.argtypes = [vp] * 8 + [i] * 6 + [f, u, i, vp, sz, vp]
@@ -360,6 +363,31 @@ def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=N
                              _ptr(post), B, N, H, D, float(k_scale), float(eps), code, _stream(stream))
     _raise("cam_prep_fwd", st)
     return outs[0], outs[1], outs[2], pre, post
+
+
+def cam_prep_bwd(q_raw, k_raw, proj_q, proj_kv, dq_out, dk_out, dv_out, dk_pre_sq=None, dk_post_sq=None,
+                 q_norm_w=None, k_norm_w=None, rope_cos=None, rope_sin=None, rope_base=10000.0, k_scale=0.5,
+                 eps=1e-6, stream=None):
+    """Backward of cam_prep_fwd: gradients of the raw q, k, v [B,N,H,D] from
+    those of q_out, k_out, v_out [B,H,N,D] (and of k_pre_sq, k_post_sq)."""
+    B, N, H, D = q_raw.shape
+    dt = q_raw.dtype
+    code = _dtype_code(q_raw)
+    _check(k_raw, "k_raw", (B, N, H, D), dt)
+    _check(proj_q, "proj_q", (B, N, 4, 4), torch.float32)
+    _check(proj_kv, "proj_kv", (B, N, 4, 4), torch.float32)
+    for name, t in (("dq_out", dq_out), ("dk_out", dk_out), ("dv_out", dv_out)):
+        _check(t, name, (B, H, N, D), dt)
+    for name, t in (("dk_pre_sq", dk_pre_sq), ("dk_post_sq", dk_post_sq)):
+        if t is not None:
+            _check(t, name, (B, H, N), torch.float32)
+    outs = tuple(torch.empty(B, N, H, D, dtype=dt, device=q_raw.device) for _ in range(3))
+    st = load().cam_prep_bwd(_ptr(q_raw), _ptr(k_raw), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(proj_q), _ptr(proj_kv),
+                             _ptr(rope_cos), _ptr(rope_sin), float(rope_base), _ptr(dq_out), _ptr(dk_out),
+                             _ptr(dv_out), _ptr(dk_pre_sq), _ptr(dk_post_sq), _ptr(outs[0]), _ptr(outs[1]),
+                             _ptr(outs[2]), B, N, H, D, float(k_scale), float(eps), code, _stream(stream))
+    _raise("cam_prep_bwd", st)
+    return outs
 
 
 def device_error(stream=None) -> int:

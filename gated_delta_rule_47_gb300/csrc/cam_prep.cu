@@ -556,6 +556,223 @@ int cam_prep_read_clear_error() {
     return v ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
+namespace {
+
+// Backward of the camera prep (fused_cam_gdn.py, `_cam_prep_bwd_kernel`,
+// continued through the full-C RMSNorm, which the page leaves to torch).  One
+// CTA per token, thread i taking channels 8i .. 8i+7 (head c / D, dims c % D):
+// the forward values it needs are recomputed, the rotation and projection are
+// transposed, the ||k||^2 terms, K-scale and ReLU mask are applied, and the
+// RMSNorm backward dx_j = r w_j dxhat_j - (r^3 / C) x_j sum_c w_c x_c dxhat_c
+// takes one block reduction.  All arithmetic in fp32.
+struct CamBwdParams {
+    const void *q_raw, *k_raw;
+    const float *q_norm_w, *k_norm_w, *proj_q, *proj_kv, *rope_cos, *rope_sin;
+    double log2_base;
+    const void *dq_out, *dk_out, *dv_out;
+    const float *dpre, *dpost;
+    void *dq_raw, *dk_raw, *dv_raw;
+    int B, N, H, D;
+    float k_scale, eps;
+};
+
+template <typename T>
+__device__ __forceinline__ void ld8(const T *p, float (&x)[8]);
+template <>
+__device__ __forceinline__ void ld8<float>(const float *p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void ld8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void st8(float *p, const float (&x)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16 *p, const float (&x)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Sum of a and b over the CTA (at most 16 warps).
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2 *red) {
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, off);
+        b += __shfl_xor_sync(0xffffffffu, b, off);
+    }
+    const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();  // red may still be read from a previous call
+    if ((threadIdx.x & 31) == 0) red[w] = make_float2(a, b);
+    __syncthreads();
+    float2 t = make_float2(0.f, 0.f);
+    for (int i = 0; i < nw; ++i) {
+        t.x += red[i].x;
+        t.y += red[i].y;
+    }
+    return t;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) cam_prep_bwd_kernel(CamBwdParams p) {
+    __shared__ float2 red[16];
+    const long long bn = blockIdx.x;
+    const int b = (int)(bn / p.N), n = (int)(bn % p.N);
+    const int C = p.H * p.D, Dh = p.D / 2;
+    const int c0 = 8 * threadIdx.x;
+    const bool act = c0 < C;
+    const int h = act ? c0 / p.D : 0, d0 = act ? c0 % p.D : 0;
+    float q[8] = {0}, k[8] = {0};
+    if (act) {
+        ld8(static_cast<const T *>(p.q_raw) + bn * C + c0, q);
+        ld8(static_cast<const T *>(p.k_raw) + bn * C + c0, k);
+    }
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        sq += q[e] * q[e];
+        sk += k[e] * k[e];
+    }
+    const float2 ss = block_sum2(sq, sk, red);
+    const float iq = rsqrtf(ss.x / C + p.eps), ik = rsqrtf(ss.y / C + p.eps);
+    float wq[8], wk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        wq[e] = (act && p.q_norm_w) ? p.q_norm_w[c0 + e] : 1.f;
+        wk[e] = (act && p.k_norm_w) ? p.k_norm_w[c0 + e] : 1.f;
+    }
+    float dxq[8] = {0}, dxk[8] = {0}, dav[8] = {0};
+    if (act) {
+        const size_t ob = (((size_t)b * p.H + h) * p.N + n) * p.D + d0;
+        const size_t si = ((size_t)b * p.H + h) * p.N + n;
+        const float gpre = p.dpre ? p.dpre[si] : 0.f, gpost = p.dpost ? p.dpost[si] : 0.f;
+        float P[2][16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            P[0][e] = p.proj_q[bn * 16 + e];
+            P[1][e] = p.proj_kv[bn * 16 + e];
+        }
+        // rotation of the four pairs of these dims (when in the last D/2)
+        float cs[8], sn[8];
+        if (d0 >= Dh) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int d = d0 - Dh + e;
+                if (p.rope_cos) {
+                    cs[e] = p.rope_cos[(size_t)n * Dh + d];
+                    sn[e] = p.rope_sin[(size_t)n * Dh + d];
+                } else {
+                    const double inv_freq = exp2(p.log2_base * (-2.0 * (d >> 1) / (double)Dh));
+                    double th = (double)n * inv_freq;
+                    const double two_pi = 6.283185307179586476925286766559;
+                    th -= two_pi * rint(th / two_pi);
+                    float sv, cv;
+                    sincosf((float)th, &sv, &cv);
+                    cs[e] = cv;
+                    sn[e] = (d & 1) ? sv : -sv;
+                }
+            }
+        }
+        float xq[8], xk[8], ak[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            xq[e] = q[e] * iq * wq[e];
+            xk[e] = k[e] * ik * wk[e];
+            ak[e] = fmaxf(xk[e], 0.f) * p.k_scale;
+        }
+        // k_out of these dims (for the ||k_out||^2 term)
+        float ko[8];
+        if (d0 < Dh) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    ko[4 * g + i] = P[1][4 * i] * ak[4 * g] + P[1][4 * i + 1] * ak[4 * g + 1] +
+                                    P[1][4 * i + 2] * ak[4 * g + 2] + P[1][4 * i + 3] * ak[4 * g + 3];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ko[e] = ak[e] * cs[e] + ak[e ^ 1] * sn[e];
+        }
+        float dy[3][8];
+        ld8(static_cast<const T *>(p.dq_out) + ob, dy[0]);
+        ld8(static_cast<const T *>(p.dk_out) + ob, dy[1]);
+        ld8(static_cast<const T *>(p.dv_out) + ob, dy[2]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dy[1][e] += 2.f * ko[e] * gpost;
+        float da[3][8];
+#pragma unroll
+        for (int tt = 0; tt < 3; ++tt) {
+            const float *PP = P[tt == 0 ? 0 : 1];
+            if (d0 < Dh) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        da[tt][4 * g + j] = PP[j] * dy[tt][4 * g] + PP[4 + j] * dy[tt][4 * g + 1] +
+                                            PP[8 + j] * dy[tt][4 * g + 2] + PP[12 + j] * dy[tt][4 * g + 3];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) da[tt][e] = dy[tt][e] * cs[e] + dy[tt][e ^ 1] * sn[e ^ 1];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            dxq[e] = xq[e] > 0.f ? da[0][e] : 0.f;
+            dxk[e] = xk[e] > 0.f ? p.k_scale * (da[1][e] + 2.f * ak[e] * gpre) : 0.f;
+            dav[e] = da[2][e];
+        }
+    }
+    float tq = 0.f, tk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        tq += wq[e] * q[e] * dxq[e];
+        tk += wk[e] * k[e] * dxk[e];
+    }
+    const float2 ts = block_sum2(tq, tk, red);
+    if (act) {
+        float oq[8], okk[8];
+        const float cq3 = iq * iq * iq / C * ts.x, ck3 = ik * ik * ik / C * ts.y;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            oq[e] = iq * wq[e] * dxq[e] - cq3 * q[e];
+            okk[e] = ik * wk[e] * dxk[e] - ck3 * k[e];
+        }
+        st8(static_cast<T *>(p.dq_raw) + bn * C + c0, oq);
+        st8(static_cast<T *>(p.dk_raw) + bn * C + c0, okk);
+        st8(static_cast<T *>(p.dv_raw) + bn * C + c0, dav);
+    }
+}
+
+}  // namespace
+
+int launch_cam_prep_bwd(const CamBwdArgs &a, cudaStream_t stream) {
+    CamBwdParams p{a.q_raw, a.k_raw, a.q_norm_w, a.k_norm_w, a.proj_q, a.proj_kv, a.rope_cos, a.rope_sin,
+                   log2((double)a.rope_base), a.dq_out, a.dk_out, a.dv_out, a.dpre, a.dpost, a.dq_raw, a.dk_raw,
+                   a.dv_raw, a.B, a.N, a.H, a.D, a.k_scale, a.eps};
+    const int C = a.H * a.D;
+    const int threads = ((C / 8 + 31) / 32) * 32;
+    const long long tokens = (long long)a.B * a.N;
+    if (a.dtype == GDN_BF16)
+        cam_prep_bwd_kernel<__nv_bfloat16><<<(unsigned)tokens, threads, 0, stream>>>(p);
+    else
+        cam_prep_bwd_kernel<float><<<(unsigned)tokens, threads, 0, stream>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream) {
     if (a.dtype == GDN_BF16) return launch_t<__nv_bfloat16>(a, stream);
     if (a.dtype == GDN_F32) return launch_t<float>(a, stream);

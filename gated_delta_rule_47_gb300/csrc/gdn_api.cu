@@ -295,6 +295,31 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
     return gdn::launch_cam_prep(a, static_cast<cudaStream_t>(stream));
 }
 
+int cam_prep_bwd(const void *q_raw, const void *k_raw, const float *q_norm_w, const float *k_norm_w,
+                 const float *proj_q, const float *proj_kv, const float *rope_cos, const float *rope_sin,
+                 float rope_base, const void *dq_out, const void *dk_out, const void *dv_out,
+                 const float *dk_pre_sq, const float *dk_post_sq, void *dq_raw, void *dk_raw, void *dv_raw, int B,
+                 int N, int H, int D, float k_scale, float eps, int dtype, void *stream) {
+    if (B < 0 || N < 0 || H < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (D % 2 != 0 || (D / 2) % 4 != 0) return GDN_ERR_INVALID_ARG;
+    if (D % 16 != 0 || (long long)H * D > 4096) return GDN_ERR_UNSUPPORTED;
+    if (!(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (rope_cos == nullptr && !(rope_base > 0.f)) return GDN_ERR_INVALID_ARG;
+    if ((long long)B * N == 0 || H == 0) return GDN_OK;
+    if ((long long)B * N > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    if (!q_raw || !k_raw || !proj_q || !proj_kv || !dq_out || !dk_out || !dv_out || !dq_raw || !dk_raw || !dv_raw)
+        return GDN_ERR_INVALID_ARG;
+    const void *ps[] = {q_raw, k_raw, q_norm_w, k_norm_w, proj_q, proj_kv, rope_cos, rope_sin, dq_out, dk_out,
+                        dv_out, dk_pre_sq, dk_post_sq, dq_raw, dk_raw, dv_raw};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::CamBwdArgs a{q_raw, k_raw, q_norm_w, k_norm_w, proj_q, proj_kv, rope_cos, rope_sin, rope_base, dq_out,
+                      dk_out, dv_out, dk_pre_sq, dk_post_sq, dq_raw, dk_raw, dv_raw, B, N, H, D, k_scale, eps, dtype};
+    return gdn::launch_cam_prep_bwd(a, static_cast<cudaStream_t>(stream));
+}
+
 int gdn_get_device_error(void *stream) {
     const int a = gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
     const int b = gdn::cam_prep_read_clear_error();

@@ -125,6 +125,21 @@ bool sm100_family();
 int device_sm_count();
 
 int launch_cam_prep(const CamArgs &a, cudaStream_t stream);
+
+// Backward of the camera prep: the gradients of the raw q, k, v from those of
+// q_out, k_out, v_out and of k_pre_sq, k_post_sq.
+struct CamBwdArgs {
+    const void *q_raw, *k_raw;
+    const float *q_norm_w, *k_norm_w, *proj_q, *proj_kv, *rope_cos, *rope_sin;
+    float rope_base;
+    const void *dq_out, *dk_out, *dv_out;
+    const float *dpre, *dpost;
+    void *dq_raw, *dk_raw, *dv_raw;
+    int B, N, H, D;
+    float k_scale, eps;
+    int dtype;
+};
+int launch_cam_prep_bwd(const CamBwdArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the streamed camera prep (GDN_OK or GDN_ERR_TIMEOUT).
 int cam_prep_read_clear_error();
 

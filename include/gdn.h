@@ -301,6 +301,31 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
                  int H, int D, float k_scale, float eps, int dtype, void *stream);
 
 /*
+ * cam_prep_bwd -- backward of cam_prep_fwd (fused_cam_gdn.py,
+ * `_cam_prep_bwd_kernel`, continued through the full-C RMSNorm that the page
+ * leaves to torch): the gradients of the raw rows given those of the outputs.
+ * In reverse order of the forward, per token: the rotation and the 4 x 4
+ * projection transposed (dx[d] = dy[d] cos[d] + dy[d^1] sin[d^1];
+ * dx_j = sum_i P[i][j] dy_i), the ||k_out||^2 and ||k||^2 terms, K-scale, the
+ * ReLU mask, and the RMSNorm backward
+ *     dx_j = r w_j dxhat_j - (r^3 / C) x_j sum_c w_c x_c dxhat_c,
+ *     r = (sum_c x_c^2 / C + eps)^(-1/2).
+ *
+ *   q_raw, k_raw, norm weights, projections, rotary tables / rope_base,
+ *   k_scale, eps: as given to cam_prep_fwd (v_raw is not needed)
+ *   dq_out, dk_out, dv_out  [B,H,N,D] dtype
+ *   dk_pre_sq, dk_post_sq   [B,H,N] fp32 or NULL (= zero)
+ *   dq_raw, dk_raw, dv_raw  [B,N,H,D] dtype (written)
+ * Gradients of the norm weights and projections are not formed.  fp32
+ * arithmetic; H*D <= 4096.
+ */
+int cam_prep_bwd(const void *q_raw, const void *k_raw, const float *q_norm_w, const float *k_norm_w,
+                 const float *proj_q, const float *proj_kv, const float *rope_cos, const float *rope_sin,
+                 float rope_base, const void *dq_out, const void *dk_out, const void *dv_out,
+                 const float *dk_pre_sq, const float *dk_post_sq, void *dq_raw, void *dk_raw, void *dv_raw, int B,
+                 int N, int H, int D, float k_scale, float eps, int dtype, void *stream);
+
+/*
  * Reads and clears the device error word of the current device after
  * synchronising `stream`.  Returns GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if
  * the synchronisation itself failed.

@@ -173,3 +173,20 @@ def test_cam_prep_scan_argument_checks(lib):
     q = lib.cam_prep_scan_fwd_workspace_bytes
     assert q(1, 30, 2, 128, 3, binding.GDN_BF16) == 2 * 3 * 131072 + 30 * 8
     assert q(1, 30, 2, 64, 3, binding.GDN_BF16) == ctypes.c_size_t(-1).value
+
+
+def test_cam_prep_bwd_argument_checks(lib):
+    f = lib.cam_prep_bwd
+    u = 0x10000
+
+    def call(D=128, H=4, dtype=binding.GDN_BF16, cos=None, sin=None, base=10000.0, q=u):
+        return f(q, u, None, None, u, u, cos, sin, base, u, u, u, None, None, u, u, u, 1, 8, H, D, 0.5, 1e-6, dtype,
+                 None)
+
+    assert call(D=36) == 1                 # D/2 not a multiple of 4
+    assert call(H=64) == 2                 # H * D > 4096
+    assert call(cos=u) == 1                # one table without the other
+    assert call(base=0.0) == 1
+    assert call(dtype=4) == 1
+    assert call(q=None) == 1
+    assert call(q=u + 4) == 3
