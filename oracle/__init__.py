@@ -70,6 +70,8 @@ def _load():
             lib.oracle_cam_prep_fwd.restype = i
             lib.oracle_cam_prep_bwd.argtypes = [_dp] * 8 + [d] + [_dp] * 8 + [i] * 4 + [d, d]
             lib.oracle_cam_prep_bwd.restype = i
+            lib.oracle_cam_scan_bwd.argtypes = [_dp] * 14 + [i] * 6 + [d, i]
+            lib.oracle_cam_scan_bwd.restype = i
             lib.oracle_max_threads.restype = i
             lib.oracle_set_threads.argtypes = [i]
             _lib = lib
@@ -200,6 +202,25 @@ def cam_scan_fwd(q, k, v, beta, decay, initial_state=None, scale=1.0, reverse=Fa
     if rc != 0:
         raise MemoryError("oracle_cam_scan_fwd failed")
     return o, sf
+
+
+def cam_scan_bwd(q, k, v, beta, decay, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False):
+    """fp64 backward of ``cam_scan_fwd`` (forward direction): gradients
+    (dq, dk, dv, dbeta, ddecay, dinitial_state) given do [B,H,N,Dv] and the
+    gradient of the final state (None = zero)."""
+    q, k, v, beta, decay, do = map(_f64, (q, k, v, beta, decay, do))
+    s0, dsf = _f64(initial_state), _f64(dfinal_state)
+    B, H, N, Dk = q.shape
+    Dv = v.shape[-1]
+    F = decay.shape[-1]
+    outs = [np.empty((B, H, N, Dk)), np.empty((B, H, N, Dk)), np.empty((B, H, N, Dv)), np.empty((B, H, N)),
+            np.empty((B, H, F)), np.empty((B, H, Dk, Dv))]
+    rc = _load().oracle_cam_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(s0), _ptr(do),
+                                     _ptr(dsf), *[_ptr(x) for x in outs], B, H, F, N // F, Dk, Dv, float(scale),
+                                     int(bool(l2norm)))
+    if rc != 0:
+        raise MemoryError("oracle_cam_scan_bwd failed")
+    return tuple(outs)
 
 
 def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=None,

@@ -48,6 +48,10 @@
  *    from last to first, each frame's output reading the state built from
  *    the frames after it only (the last frame reads zero).
  *
+ *  - Backward of the frame-level camera scan (fused_cam_gdn.py,
+ *    `_cam_scan_bwd_kernel`, forward direction): the adjoint of the frame
+ *    loop, frames from last to first, with the states recomputed forward.
+ *
  *  - Backward of the camera prep (fused_cam_gdn.py, `_cam_prep_bwd_kernel`,
  *    continued through the full-C RMSNorm): the adjoint of the prep map from
  *    the raw rows to q_out, k_out, v_out, k_pre_sq and k_post_sq, written as
@@ -632,6 +636,152 @@ int oracle_cam_prep_bwd(const double *q_raw, const double *k_raw, const double *
         free(ak);
         free(ko);
         free(gk);
+    }
+    return failed ? -1 : 0;
+}
+
+/* y = x / max(||x||, 1e-12); given dy returns dx = (dy - y (y . dy)) / max(||x||, 1e-12)
+ * (for ||x|| below the floor the map is x / 1e-12 and dx = dy / 1e-12). */
+static void l2_normalise_bwd(const double *x, const double *dy, double *dx, int n) {
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += x[i] * x[i];
+    const double nrm = sqrt(s);
+    if (nrm < 1e-12) {
+        for (int i = 0; i < n; ++i) dx[i] = dy[i] / 1e-12;
+        return;
+    }
+    double yd = 0.0;
+    for (int i = 0; i < n; ++i) yd += x[i] / nrm * dy[i];
+    for (int i = 0; i < n; ++i) dx[i] = (dy[i] - x[i] / nrm * yd) / nrm;
+}
+
+/*
+ * Backward of oracle_cam_scan_fwd (forward direction).  Given do [B,H,N,Dv]
+ * and dsf [B,H,Dk,Dv] (or NULL), the gradients dq, dk [B,H,N,Dk], dv
+ * [B,H,N,Dv], dbeta [B,H,N], ddecay [B,H,F] and ds0 [B,H,Dk,Dv] (or NULL).
+ * With S' the state entering frame f and S_f the state after it,
+ *   R = diag(beta) (V - d K S'),  S_f = d S' + K^T R,  O = scale Q S_f,
+ * frames from last to first, dS the adjoint of S_f:
+ *   dS += scale Q^T dO;  dq_t = scale S_f do_t
+ *   dR = K dS;  dv_t = beta_t dR_t;  dbeta_t = dR_t . (v_t - d S'^T k_t)
+ *   dk_t = dS r_t - d beta_t S' dR_t           (r_t = beta_t (v_t - d S'^T k_t))
+ *   dd  = <dS, S'> - sum_t beta_t dR_t . (S'^T k_t)
+ *   dS' = d (dS - K^T diag(beta) dR)
+ * and with l2norm the unit-norm map's adjoint on each q_t and k_t.
+ */
+int oracle_cam_scan_bwd(const double *q, const double *k, const double *v, const double *beta,
+                        const double *decay, const double *s0, const double *dout, const double *dsf,
+                        double *dq, double *dk, double *dv, double *dbeta, double *ddecay, double *ds0,
+                        int B, int H, int F, int S_len, int Dk, int Dv, double scale, int l2norm) {
+    const int BH = B * H;
+    const long N = (long)F * S_len;
+    const size_t SD = (size_t)Dk * Dv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *St = (double *)malloc(sizeof(double) * SD * (F + 1)); /* St[f] = state entering frame f */
+        double *dS = (double *)malloc(sizeof(double) * SD);
+        double *X = (double *)malloc(sizeof(double) * SD);
+        double *P = (double *)malloc(sizeof(double) * (size_t)(S_len > 0 ? S_len : 1) * Dv);
+        double *Kf = (double *)malloc(sizeof(double) * (size_t)(S_len > 0 ? S_len : 1) * Dk);
+        double *vec = (double *)malloc(sizeof(double) * (size_t)(Dk + Dv) * 4);
+        if (!St || !dS || !X || !P || !Kf || !vec) {
+            failed |= 1;
+        } else {
+            double *dR = vec, *Pk = vec + Dv, *r = vec + 2 * Dv, *gk = vec + 3 * Dv, *tk = gk + Dk;
+            double *qt = tk + Dk, *tq = qt + Dk;
+            if (s0)
+                memcpy(St, s0 + (size_t)bh * SD, sizeof(double) * SD);
+            else
+                memset(St, 0, sizeof(double) * SD);
+            /* forward: the states entering each frame, and the last */
+            for (int f = 0; f < F; ++f) {
+                double *Sn = St + (size_t)(f + 1) * SD;
+                memcpy(Sn, St + (size_t)f * SD, sizeof(double) * SD);
+                const double d = decay[(size_t)bh * F + f];
+                for (size_t e = 0; e < SD; ++e) Sn[e] *= d;
+                const size_t t0 = (size_t)bh * N + (size_t)f * S_len;
+                memcpy(Kf, k + t0 * Dk, sizeof(double) * (size_t)S_len * Dk);
+                if (l2norm)
+                    for (int s = 0; s < S_len; ++s) l2_normalise(Kf + (size_t)s * Dk, Dk);
+                frame_update(Sn, Kf, v + t0 * Dv, beta + t0, S_len, Dk, Dv, P);
+            }
+            if (dsf)
+                memcpy(dS, dsf + (size_t)bh * SD, sizeof(double) * SD);
+            else
+                memset(dS, 0, sizeof(double) * SD);
+            for (int f = F - 1; f >= 0; --f) {
+                const double *Sp = St + (size_t)f * SD, *Sf = St + (size_t)(f + 1) * SD;
+                const double d = decay[(size_t)bh * F + f];
+                const size_t t0 = (size_t)bh * N + (size_t)f * S_len;
+                /* outputs of the frame */
+                for (int s = 0; s < S_len; ++s) {
+                    const size_t tok = t0 + s;
+                    memcpy(qt, q + tok * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(qt, Dk);
+                    const double *go = dout + tok * Dv;
+                    for (int i = 0; i < Dk; ++i) {
+                        double acc = 0.0;
+                        for (int c = 0; c < Dv; ++c) {
+                            acc += Sf[(size_t)i * Dv + c] * go[c];
+                            dS[(size_t)i * Dv + c] += scale * qt[i] * go[c];
+                        }
+                        tq[i] = scale * acc;
+                    }
+                    if (l2norm)
+                        l2_normalise_bwd(q + tok * Dk, tq, dq + tok * Dk, Dk);
+                    else
+                        memcpy(dq + tok * Dk, tq, sizeof(double) * Dk);
+                }
+                /* the frame's update */
+                double dd = 0.0;
+                for (size_t e = 0; e < SD; ++e) dd += dS[e] * Sp[e];
+                memset(X, 0, sizeof(double) * SD);
+                for (int s = 0; s < S_len; ++s) {
+                    const size_t tok = t0 + s;
+                    memcpy(tk, k + tok * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(tk, Dk);
+                    const double bt = beta[tok];
+                    for (int c = 0; c < Dv; ++c) {
+                        double a = 0.0, b2 = 0.0;
+                        for (int i = 0; i < Dk; ++i) {
+                            a += tk[i] * dS[(size_t)i * Dv + c];
+                            b2 += tk[i] * Sp[(size_t)i * Dv + c];
+                        }
+                        dR[c] = a;
+                        Pk[c] = b2;
+                        r[c] = bt * (v[tok * Dv + c] - d * b2);
+                    }
+                    double db = 0.0;
+                    for (int c = 0; c < Dv; ++c) {
+                        dv[tok * Dv + c] = bt * dR[c];
+                        db += dR[c] * (v[tok * Dv + c] - d * Pk[c]);
+                        dd -= bt * dR[c] * Pk[c];
+                    }
+                    dbeta[tok] = db;
+                    for (int i = 0; i < Dk; ++i) {
+                        double acc = 0.0;
+                        for (int c = 0; c < Dv; ++c)
+                            acc += dS[(size_t)i * Dv + c] * r[c] - d * bt * Sp[(size_t)i * Dv + c] * dR[c];
+                        gk[i] = acc;
+                        for (int c = 0; c < Dv; ++c) X[(size_t)i * Dv + c] += tk[i] * bt * dR[c];
+                    }
+                    if (l2norm)
+                        l2_normalise_bwd(k + tok * Dk, gk, dk + tok * Dk, Dk);
+                    else
+                        memcpy(dk + tok * Dk, gk, sizeof(double) * Dk);
+                }
+                ddecay[(size_t)bh * F + f] = dd;
+                for (size_t e = 0; e < SD; ++e) dS[e] = d * (dS[e] - X[e]);
+            }
+            if (ds0) memcpy(ds0 + (size_t)bh * SD, dS, sizeof(double) * SD);
+        }
+        free(St);
+        free(dS);
+        free(X);
+        free(P);
+        free(Kf);
+        free(vec);
     }
     return failed ? -1 : 0;
 }
