@@ -498,6 +498,15 @@ def secondary(args, dev):
             "hbm_frac": frame_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "tokens_per_s_with_prep": w.B * w.T / ((pre_ms + ms) * 1e-3)}
     out["cam_frames_b2f21s1560h16d128_bf16"] = dict(res, alg_bytes=frame_bytes, launches_per_call=3)
+    # the frame scan's backward (CUDA cores, fp32), on the same inputs
+    gob = torch.randn(w.B, w.H, w.T, w.D, device=dev, dtype=torch.bfloat16)
+    wsb = torch.empty(binding.load().cam_scan_bwd_workspace_bytes(w.B, w.H, F, S, w.D, w.D, 1), dtype=torch.uint8,
+                      device=dev)
+    bms = timeit(lambda: binding.cam_scan_bwd(outs[0], outs[1], outs[2], beta_f, decay_f, gob, l2norm=True,
+                                              workspace=wsb))
+    out["cam_frames_bwd_b2f21s1560h16d128_bf16"] = {"ms": bms, "tokens_per_s": w.B * w.T / (bms * 1e-3),
+                                                    "path": "CUDA cores, fp32, one CTA per head"}
+    del gob, wsb
     # the prep fused into the frame scan: raw q, k, v in, o out, one call
     wsx = torch.empty(binding.cam_prep_scan_workspace_bytes(w.B, w.T, w.H, w.D, F), dtype=torch.uint8, device=dev)
     C = w.H * w.D

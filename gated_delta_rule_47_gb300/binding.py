@@ -28,7 +28,7 @@ EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", 
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
            "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd",
            "masked_deltaproduct_chunk_fwd", "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd",
-           "cam_prep_bwd")
+           "cam_prep_bwd", "cam_scan_bwd_workspace_bytes", "cam_scan_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +70,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.cam_prep_scan_fwd_workspace_bytes.restype = sz
         lib.cam_prep_scan_fwd.argtypes = [vp] * 7 + [f] + [vp] * 5 + [i] * 5 + [f, f, f, u, i, vp, sz, vp]
         lib.cam_prep_scan_fwd.restype = i
+        lib.cam_scan_bwd_workspace_bytes.argtypes = [i] * 7
+        lib.cam_scan_bwd_workspace_bytes.restype = sz
+        lib.cam_scan_bwd.argtypes = [vp] * 14 + [i] * 6 + [f, u, i, vp, sz, vp]
+        lib.cam_scan_bwd.restype = i
         lib.cam_prep_bwd.argtypes = [vp] * 8 + [f] + [vp] * 8 + [i] * 4 + [f, f, i, vp]
         lib.cam_prep_bwd.restype = i
         lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
@@ -363,6 +367,47 @@ def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=N
                              _ptr(post), B, N, H, D, float(k_scale), float(eps), code, _stream(stream))
     _raise("cam_prep_fwd", st)
     return outs[0], outs[1], outs[2], pre, post
+
+
+def cam_scan_bwd(q, k, v, beta, decay, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False,
+                 need_dinitial=False, workspace=None, stream=None):
+    """Backward of cam_scan_fwd (forward direction).  Returns (dq, dk, dv,
+    dbeta, ddecay, dinitial_state or None); dq, dk, dv in the inputs' dtype,
+    the rest fp32."""
+    B, H, N, Dk = q.shape
+    Dv = v.shape[-1]
+    F = decay.shape[-1]
+    if F <= 0 or N % F != 0:
+        raise ValueError(f"{N} tokens do not split into {F} frames")
+    S = N // F
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, N, Dk), dt)
+    _check(k, "k", (B, H, N, Dk), dt)
+    _check(v, "v", (B, H, N, Dv), dt)
+    _check(beta, "beta", (B, H, N), dt)
+    _check(decay, "decay", (B, H, F), torch.float32)
+    _check(do, "do", (B, H, N, Dv), dt)
+    for name, t in (("initial_state", initial_state), ("dfinal_state", dfinal_state)):
+        if t is not None:
+            _check(t, name, (B, H, Dk, Dv), torch.float32)
+    dev = q.device
+    dq, dk = torch.empty_like(q), torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dbeta = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    ddecay = torch.empty(B, H, F, dtype=torch.float32, device=dev)
+    ds0 = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=dev) if need_dinitial else None
+    lib = load()
+    need = lib.cam_scan_bwd_workspace_bytes(B, H, F, S, Dk, Dv, code)
+    if workspace is None:
+        workspace = torch.empty(int(need), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.cam_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(do),
+                          _ptr(dfinal_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(ddecay), _ptr(ds0),
+                          B, H, F, S, Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace),
+                          ws_bytes, _stream(stream))
+    _raise("cam_scan_bwd", st)
+    return dq, dk, dv, dbeta, ddecay, ds0
 
 
 def cam_prep_bwd(q_raw, k_raw, proj_q, proj_kv, dq_out, dk_out, dv_out, dk_pre_sq=None, dk_post_sq=None,

@@ -295,6 +295,54 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
     return gdn::launch_cam_prep(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, int dtype) {
+    if (B < 0 || H < 0 || F < 0 || S < 0 || (F > 0 && S == 0)) return (size_t)-1;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return (size_t)-1;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
+    gdn::CamScanBwdArgs a{};
+    a.B = B; a.H = H; a.F = F; a.S = S; a.Dk = Dk; a.Dv = Dv;
+    return gdn::cam_scan_bwd_workspace_bytes(a);
+}
+
+int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
+                 const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
+                 void *dv, float *dbeta, float *ddecay, float *dinitial_state, int B, int H, int F, int S, int Dk,
+                 int Dv, float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+    if (B < 0 || H < 0 || F < 0 || S < 0 || (F > 0 && S == 0)) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_CAM_REVERSE)) return GDN_ERR_INVALID_ARG;
+    if (flags & GDN_CAM_REVERSE) return GDN_ERR_UNSUPPORTED;  // forward direction only
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535 || (long long)F * S >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H * F != 0) {
+        if (!q || !k || !v || !beta || !decay || !dout || !dq || !dk || !dv || !dbeta || !ddecay)
+            return GDN_ERR_INVALID_ARG;
+    }
+    const void *ps[] = {q, k, v, beta, decay, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, ddecay,
+                        dinitial_state};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::CamScanBwdArgs a{q, k, v, beta, decay, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, ddecay,
+                          dinitial_state, B, H, F, S, Dk, Dv, scale, flags, dtype, workspace, workspace_bytes};
+    const size_t need = gdn::cam_scan_bwd_workspace_bytes(a);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((long long)B * H == 0) return GDN_OK;
+    if (F == 0) {  // nothing depends on the inputs: the initial state's gradient is the final state's
+        if (dinitial_state) {
+            const size_t bytes = sizeof(float) * (size_t)B * H * Dk * Dv;
+            cudaError_t e = dfinal_state ? cudaMemcpyAsync(dinitial_state, dfinal_state, bytes,
+                                                           cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(dinitial_state, 0, bytes, st);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    return gdn::launch_cam_scan_bwd(a, st);
+}
+
 int cam_prep_bwd(const void *q_raw, const void *k_raw, const float *q_norm_w, const float *k_norm_w,
                  const float *proj_q, const float *proj_kv, const float *rope_cos, const float *rope_sin,
                  float rope_base, const void *dq_out, const void *dk_out, const void *dv_out,

@@ -106,6 +106,25 @@ struct CamFusedArgs {
     size_t ws_bytes;
 };
 size_t cam_fused_workspace_bytes(const CamFusedArgs &a);
+
+// Backward of the frame scan (forward direction): q,k [B,H,N,Dk], v [B,H,N,Dv],
+// beta [B,H,N], decay [B,H,F], dout [B,H,N,Dv], dsf [B,H,Dk,Dv] or null.
+struct CamScanBwdArgs {
+    const void *q, *k, *v, *beta;
+    const float *decay, *s0;
+    const void *dout;
+    const float *dsf;
+    void *dq, *dk, *dv;
+    float *dbeta, *ddecay, *ds0;
+    int B, H, F, S, Dk, Dv;
+    float scale;
+    unsigned flags;
+    int dtype;
+    void *ws;
+    size_t ws_bytes;
+};
+size_t cam_scan_bwd_workspace_bytes(const CamScanBwdArgs &a);
+int launch_cam_scan_bwd(const CamScanBwdArgs &a, cudaStream_t stream);
 int launch_cam_fused(const CamFusedArgs &a, cudaStream_t stream);
 
 // 3-D TMA map (128-byte swizzle) over a [heads][rows][128] bf16 tensor with a

@@ -301,6 +301,40 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
                  int H, int D, float k_scale, float eps, int dtype, void *stream);
 
 /*
+ * Bytes of device workspace cam_scan_bwd needs ((size_t)-1 for sizes it
+ * rejects): the fp32 state entering every frame, and the last.
+ */
+size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, int dtype);
+
+/*
+ * cam_scan_bwd -- backward of cam_scan_fwd, forward direction
+ * (fused_cam_gdn.py, `_cam_scan_bwd_kernel`): the gradients of q, k, v, beta,
+ * each frame's decay and the initial state, given the gradient of o (and of
+ * the final state).  With S' the state entering frame f and S_f the state
+ * after it, R = diag(beta)(V - d K S'), S_f = d S' + K^T R, O = scale Q S_f; the
+ * frames are taken from last to first with dS the gradient of S_f:
+ *     dS += scale Q^T dO;   dq_t = scale S_f do_t
+ *     dR = K dS;   dv_t = beta_t dR_t;   dbeta_t = dR_t . (v_t - d S'^T k_t)
+ *     dk_t = dS r_t - d beta_t S' dR_t;   ddecay_f = <dS, S'> - sum_t beta_t dR_t . S'^T k_t
+ *     dS <- d (dS - K^T diag(beta) dR)
+ * and, with GDN_QK_L2NORM, the unit-norm map's adjoint on q and k.
+ *
+ *   q, k, v, beta, decay, initial_state, scale, flags, dtype: as given to
+ *           cam_scan_fwd (GDN_CAM_REVERSE is GDN_ERR_UNSUPPORTED)
+ *   dout    [B,H,N,Dv] dtype;  dfinal_state [B,H,Dk,Dv] fp32 or NULL (= zero)
+ *   dq, dk [B,H,N,Dk], dv [B,H,N,Dv] dtype;  dbeta [B,H,N] fp32;
+ *   ddecay [B,H,F] fp32;  dinitial_state [B,H,Dk,Dv] fp32 or NULL
+ *   workspace: cam_scan_bwd_workspace_bytes bytes, 16-byte aligned.
+ * CUDA-core kernels, fp32 arithmetic: a forward pass that keeps the states,
+ * then one CTA per head walking the frames backwards.
+ */
+int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
+                 const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
+                 void *dv, float *dbeta, float *ddecay, float *dinitial_state, int B, int H, int F, int S, int Dk,
+                 int Dv, float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/*
  * cam_prep_bwd -- backward of cam_prep_fwd (fused_cam_gdn.py,
  * `_cam_prep_bwd_kernel`, continued through the full-C RMSNorm that the page
  * leaves to torch): the gradients of the raw rows given those of the outputs.

@@ -190,3 +190,22 @@ def test_cam_prep_bwd_argument_checks(lib):
     assert call(dtype=4) == 1
     assert call(q=None) == 1
     assert call(q=u + 4) == 3
+
+
+def test_cam_scan_bwd_argument_checks(lib):
+    f = lib.cam_scan_bwd
+    u = 0x10000
+
+    def call(flags=0, Dk=64, S=5, dtype=binding.GDN_F32, q=u, ws=u):
+        return f(q, u, u, u, u, None, u, None, u, u, u, u, u, None, 1, 2, 3, S, Dk, 64, 1.0, flags, dtype, ws,
+                 1 << 40, None)
+
+    assert call(flags=binding.GDN_CAM_REVERSE) == 2
+    assert call(flags=8) == 1
+    assert call(Dk=96) == 2
+    assert call(S=0) == 1
+    assert call(dtype=5) == 1
+    assert call(q=None) == 1
+    assert call(q=u + 4) == 3
+    assert call(ws=None) == 4
+    assert lib.cam_scan_bwd_workspace_bytes(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 4 * 2 * 4 * 64 * 64
