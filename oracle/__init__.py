@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the GDN / DeltaProduct forward and the camera prep.
+"""fp64 CPU oracle for the GDN / DeltaProduct forward and backward and the camera branch.
 
 TEST INFRASTRUCTURE ONLY.  The product package never imports this module;
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -19,6 +19,8 @@ fused_cam_gdn.py, ``_cam_scan_kernel`` and ``_torch_cam_prep_reference``):
     o_t = scale * S_t^T q_t
 
 DeltaProduct applies the decay once per token and then r such corrections.
+The ``*_bwd`` functions are the adjoints of those token loops, written out in
+reverse token order (pinned by finite differences of the forward functions).
 """
 from __future__ import annotations
 
@@ -72,6 +74,10 @@ def _load():
             lib.oracle_cam_prep_bwd.restype = i
             lib.oracle_cam_scan_bwd.argtypes = [_dp] * 14 + [i] * 6 + [d, i]
             lib.oracle_cam_scan_bwd.restype = i
+            lib.oracle_deltaproduct_bwd.argtypes = [_dp] * 14 + [i] * 6 + [d, i]
+            lib.oracle_deltaproduct_bwd.restype = i
+            lib.oracle_masked_deltaproduct_bwd.argtypes = [_dp] * 15 + [i] * 6 + [d, i]
+            lib.oracle_masked_deltaproduct_bwd.restype = i
             lib.oracle_max_threads.restype = i
             lib.oracle_set_threads.argtypes = [i]
             _lib = lib
@@ -220,6 +226,51 @@ def cam_scan_bwd(q, k, v, beta, decay, do, initial_state=None, dfinal_state=None
                                      int(bool(l2norm)))
     if rc != 0:
         raise MemoryError("oracle_cam_scan_bwd failed")
+    return tuple(outs)
+
+
+def deltaproduct_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False):
+    """fp64 backward of ``deltaproduct_fwd``: gradients (dq, dk, dv, dbeta, dg,
+    dinitial_state) given do [B,H,T,Dv] and the gradient of the final state
+    (None = zero).  k, v, beta carry the sub-step axis: [B,H,T,r,*]."""
+    q, k, v, beta, g, do = map(_f64, (q, k, v, beta, g, do))
+    s0, dsf = _f64(initial_state), _f64(dfinal_state)
+    B, H, T, Dk = q.shape
+    r, Dv = k.shape[3], v.shape[-1]
+    outs = [np.empty((B, H, T, Dk)), np.empty((B, H, T, r, Dk)), np.empty((B, H, T, r, Dv)),
+            np.empty((B, H, T, r)), np.empty((B, H, T)), np.empty((B, H, Dk, Dv))]
+    rc = _load().oracle_deltaproduct_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(s0), _ptr(do),
+                                         _ptr(dsf), *[_ptr(x) for x in outs], B, H, T, r, Dk, Dv, float(scale),
+                                         int(bool(l2norm)))
+    if rc != 0:
+        raise MemoryError("oracle_deltaproduct_bwd failed")
+    return tuple(outs)
+
+
+def gdn_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False):
+    """fp64 backward of ``gdn_fwd``: (dq, dk, dv, dbeta, dg, dinitial_state)."""
+    dq, dk, dv, db, dg, ds0 = deltaproduct_bwd(q, _f64(k)[:, :, :, None], _f64(v)[:, :, :, None],
+                                               _f64(beta)[:, :, :, None], g, do, initial_state,
+                                               dfinal_state, scale, l2norm)
+    return dq, dk[:, :, :, 0], dv[:, :, :, 0], db[:, :, :, 0], dg, ds0
+
+
+def masked_deltaproduct_bwd(q, k, v, beta, g, mask, do, initial_state=None, dfinal_state=None, scale=1.0,
+                            l2norm=False):
+    """fp64 backward of ``masked_deltaproduct_fwd``: (dq, dk, dv, dbeta, dg,
+    dinitial_state) given do and the gradient of the final state (None = 0)."""
+    q, k, v, beta, g, mask, do = map(_f64, (q, k, v, beta, g, mask, do))
+    s0, dsf = _f64(initial_state), _f64(dfinal_state)
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    r = mask.shape[0]
+    outs = [np.empty((B, H, T, Dk)), np.empty((B, H, T, Dk)), np.empty((B, H, T, Dv)), np.empty((B, H, T)),
+            np.empty((B, H, T)), np.empty((B, H, Dk, Dv))]
+    rc = _load().oracle_masked_deltaproduct_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
+                                                _ptr(s0), _ptr(do), _ptr(dsf), *[_ptr(x) for x in outs], B, H, T,
+                                                r, Dk, Dv, float(scale), int(bool(l2norm)))
+    if rc != 0:
+        raise MemoryError("oracle_masked_deltaproduct_bwd failed")
     return tuple(outs)
 
 

@@ -785,3 +785,357 @@ int oracle_cam_scan_bwd(const double *q, const double *k, const double *v, const
     }
     return failed ? -1 : 0;
 }
+
+/*
+ * Backward of oracle_deltaproduct_fwd (r = 1 is oracle_gdn_fwd): the adjoint
+ * of its token loop, tokens from last to first (gated_deltaproduct test.py
+ * computes the same gradients chunk-wise: `gated_chunk_delta_rule_bwd_kernel_dhu`,
+ * `gated_chunk_delta_rule_bwd_kernel_dqkw`, `gated_bwd_prepare_wy_repr_kernel`).
+ * Given dout = dL/do [B,H,T,Dv] and dsf = dL/dS_final [B,H,Dk,Dv] (NULL = 0),
+ * it writes dq [B,H,T,Dk], dk [B,H,T,r,Dk], dv [B,H,T,r,Dv], dbeta [B,H,T,r],
+ * dg [B,H,T] and ds0 [B,H,Dk,Dv] (NULL = not wanted).  With G the adjoint of
+ * the state after a step:
+ *   output o = scale S^T q:             G += scale q do^T;  dq = scale S do
+ *   sub-step X -> X + b k (v - X^T k)^T, e = v - X^T k, w = G^T k:
+ *       dv = b w;  db = k . (G e);  dk = b (G e - X w);  G <- G - b k w^T
+ *   decay D = e^{g} E (E the state entering the token, D = X before sub-step 0):
+ *       dg = <G, D>;  G <- e^{g} G
+ * and with l2norm the unit-norm map's adjoint on q and every k.  The states
+ * entering the tokens are rebuilt from checkpoints every 64 tokens with the
+ * forward's own arithmetic, so they are exactly the forward's.
+ */
+int oracle_deltaproduct_bwd(const double *q, const double *k, const double *v, const double *beta,
+                            const double *g, const double *s0, const double *dout, const double *dsf,
+                            double *dq, double *dk, double *dv, double *dbeta, double *dg, double *ds0,
+                            int B, int H, int T, int r, int Dk, int Dv, double scale, int l2norm) {
+    if (r < 1) return -2;
+    const int BH = B * H;
+    const int BLK = 64;
+    const int nblk = (T + BLK - 1) / BLK;
+    const size_t SD = (size_t)Dk * Dv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Cp = (double *)malloc(sizeof(double) * SD * (nblk > 0 ? nblk : 1)); /* entering token BLK*b */
+        double *E = (double *)malloc(sizeof(double) * SD * BLK);                    /* entering each token */
+        double *X = (double *)malloc(sizeof(double) * SD * (r + 1));                /* before each sub-step */
+        double *G = (double *)malloc(sizeof(double) * SD);
+        double *vec = (double *)malloc(sizeof(double) * (size_t)(4 * Dk + 3 * Dv));
+        if (!Cp || !E || !X || !G || !vec) {
+            failed |= 1;
+        } else {
+            double *kt = vec, *qt = vec + Dk, *gk = vec + 2 * Dk, *tq = vec + 3 * Dk;
+            double *p = vec + 4 * Dk, *e = p + Dv, *w = e + Dv;
+            double *S = X; /* scratch for the forward pass */
+            if (s0)
+                memcpy(S, s0 + (size_t)bh * SD, sizeof(double) * SD);
+            else
+                memset(S, 0, sizeof(double) * SD);
+            /* forward: checkpoints of the state entering every BLK-th token */
+            for (int t = 0; t < T; ++t) {
+                if (t % BLK == 0) memcpy(Cp + (size_t)(t / BLK) * SD, S, sizeof(double) * SD);
+                const size_t tok = (size_t)bh * T + t;
+                const double a = exp(g[tok]);
+                for (size_t x = 0; x < SD; ++x) S[x] *= a;
+                for (int j = 0; j < r; ++j) {
+                    const size_t sub = tok * r + j;
+                    memcpy(kt, k + sub * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(kt, Dk);
+                    delta_step(S, kt, v + sub * Dv, beta[sub], Dk, Dv, p);
+                }
+            }
+            if (dsf)
+                memcpy(G, dsf + (size_t)bh * SD, sizeof(double) * SD);
+            else
+                memset(G, 0, sizeof(double) * SD);
+            for (int b = nblk - 1; b >= 0; --b) {
+                const int t0 = b * BLK, t1 = (t0 + BLK < T) ? t0 + BLK : T;
+                /* rebuild the states entering the block's tokens */
+                memcpy(E, Cp + (size_t)b * SD, sizeof(double) * SD);
+                for (int t = t0; t + 1 < t1; ++t) {
+                    const size_t tok = (size_t)bh * T + t;
+                    double *Sn = E + (size_t)(t - t0 + 1) * SD;
+                    memcpy(Sn, E + (size_t)(t - t0) * SD, sizeof(double) * SD);
+                    const double a = exp(g[tok]);
+                    for (size_t x = 0; x < SD; ++x) Sn[x] *= a;
+                    for (int j = 0; j < r; ++j) {
+                        const size_t sub = tok * r + j;
+                        memcpy(kt, k + sub * Dk, sizeof(double) * Dk);
+                        if (l2norm) l2_normalise(kt, Dk);
+                        delta_step(Sn, kt, v + sub * Dv, beta[sub], Dk, Dv, p);
+                    }
+                }
+                for (int t = t1 - 1; t >= t0; --t) {
+                    const size_t tok = (size_t)bh * T + t;
+                    const double a = exp(g[tok]);
+                    /* the token's states: X[0] decayed, X[j+1] after sub-step j */
+                    const double *Et = E + (size_t)(t - t0) * SD;
+                    for (size_t x = 0; x < SD; ++x) X[x] = a * Et[x];
+                    for (int j = 0; j < r; ++j) {
+                        const size_t sub = tok * r + j;
+                        memcpy(X + (size_t)(j + 1) * SD, X + (size_t)j * SD, sizeof(double) * SD);
+                        memcpy(kt, k + sub * Dk, sizeof(double) * Dk);
+                        if (l2norm) l2_normalise(kt, Dk);
+                        delta_step(X + (size_t)(j + 1) * SD, kt, v + sub * Dv, beta[sub], Dk, Dv, p);
+                    }
+                    /* output */
+                    const double *Sr = X + (size_t)r * SD;
+                    const double *go = dout + tok * Dv;
+                    memcpy(qt, q + tok * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(qt, Dk);
+                    for (int i = 0; i < Dk; ++i) {
+                        double acc = 0.0;
+                        for (int c = 0; c < Dv; ++c) {
+                            acc += Sr[(size_t)i * Dv + c] * go[c];
+                            G[(size_t)i * Dv + c] += scale * qt[i] * go[c];
+                        }
+                        tq[i] = scale * acc;
+                    }
+                    if (l2norm)
+                        l2_normalise_bwd(q + tok * Dk, tq, dq + tok * Dk, Dk);
+                    else
+                        memcpy(dq + tok * Dk, tq, sizeof(double) * Dk);
+                    /* sub-steps, last first */
+                    for (int j = r - 1; j >= 0; --j) {
+                        const size_t sub = tok * r + j;
+                        const double *Xj = X + (size_t)j * SD;
+                        const double bt = beta[sub];
+                        const double *vt = v + sub * Dv;
+                        memcpy(kt, k + sub * Dk, sizeof(double) * Dk);
+                        if (l2norm) l2_normalise(kt, Dk);
+                        for (int c = 0; c < Dv; ++c) {
+                            double xk = 0.0, gk2 = 0.0;
+                            for (int i = 0; i < Dk; ++i) {
+                                xk += Xj[(size_t)i * Dv + c] * kt[i];
+                                gk2 += G[(size_t)i * Dv + c] * kt[i];
+                            }
+                            e[c] = vt[c] - xk;
+                            w[c] = gk2;
+                            dv[sub * Dv + c] = bt * gk2;
+                        }
+                        double db = 0.0;
+                        for (int i = 0; i < Dk; ++i) {
+                            double ge = 0.0, xw = 0.0;
+                            for (int c = 0; c < Dv; ++c) {
+                                ge += G[(size_t)i * Dv + c] * e[c];
+                                xw += Xj[(size_t)i * Dv + c] * w[c];
+                            }
+                            db += kt[i] * ge;
+                            gk[i] = bt * (ge - xw);
+                        }
+                        dbeta[sub] = db;
+                        if (l2norm)
+                            l2_normalise_bwd(k + sub * Dk, gk, dk + sub * Dk, Dk);
+                        else
+                            memcpy(dk + sub * Dk, gk, sizeof(double) * Dk);
+                        for (int i = 0; i < Dk; ++i)
+                            for (int c = 0; c < Dv; ++c) G[(size_t)i * Dv + c] -= bt * kt[i] * w[c];
+                    }
+                    /* decay */
+                    double dd = 0.0;
+                    for (size_t x = 0; x < SD; ++x) dd += G[x] * X[x];
+                    dg[tok] = dd;
+                    for (size_t x = 0; x < SD; ++x) G[x] *= a;
+                }
+            }
+            if (ds0) memcpy(ds0 + (size_t)bh * SD, G, sizeof(double) * SD);
+        }
+        free(Cp);
+        free(E);
+        free(X);
+        free(G);
+        free(vec);
+    }
+    return failed ? -1 : 0;
+}
+
+/* One token of oracle_masked_deltaproduct_fwd on S in place, in the same order
+ * of operations: decay, the slice predictions z_j, d_i, the slice writes.  kt
+ * receives the token's (unit, with l2norm) key; z, d are r x Dv scratch. */
+static void masked_token_step(double *S, const double *k, const double *v, double beta, double g,
+                              const double *mask, int r, int Dk, int Dv, int l2norm, double *kt,
+                              double *z, double *d) {
+    const int sl = Dk / r;
+    memcpy(kt, k, sizeof(double) * Dk);
+    if (l2norm) l2_normalise(kt, Dk);
+    const double a = exp(g);
+    for (size_t e = 0; e < (size_t)Dk * Dv; ++e) S[e] *= a;
+    for (int jj = 0; jj < r; ++jj) {
+        double *zj = z + (size_t)jj * Dv;
+        for (int c = 0; c < Dv; ++c) zj[c] = 0.0;
+        for (int i = jj * sl; i < (jj + 1) * sl; ++i) {
+            const double *row = S + (size_t)i * Dv;
+            for (int c = 0; c < Dv; ++c) zj[c] += row[c] * kt[i];
+        }
+    }
+    for (int ii = 0; ii < r; ++ii) {
+        double *di = d + (size_t)ii * Dv;
+        for (int c = 0; c < Dv; ++c) {
+            double pr = 0.0;
+            for (int jj = 0; jj < r; ++jj) pr += mask[ii * r + jj] * z[(size_t)jj * Dv + c];
+            di[c] = beta * (v[c] - pr);
+        }
+    }
+    for (int ii = 0; ii < r; ++ii)
+        for (int i = ii * sl; i < (ii + 1) * sl; ++i) {
+            double *row = S + (size_t)i * Dv;
+            for (int c = 0; c < Dv; ++c) row[c] += kt[i] * d[(size_t)ii * Dv + c];
+        }
+}
+
+/*
+ * Backward of oracle_masked_deltaproduct_fwd, tokens from last to first.  Per
+ * token, with D the decayed state, sub-row i's read key kr_i (slice j of k
+ * times mask[i][j]) and write key kw_i (slice i of k, zero elsewhere),
+ * e_i = v - D^T kr_i and S = D + sum_i b kw_i e_i^T, the adjoint G of S gives
+ *   w_i = G^T kw_i;  dv = b sum_i w_i;  db = sum_i kw_i . (G e_i)
+ *   dkw_i = b G e_i;  dkr_i = -b D w_i;  dD = G - b sum_i kr_i w_i^T
+ * then dk's slice j = slice j of (dkw_j + sum_i mask[i][j] dkr_i), dg = <dD, D>
+ * and the state entering the token gets e^{g} dD.  Output, norms, shapes and
+ * checkpoints (rebuilt with the forward's token step) as oracle_deltaproduct_bwd, with k, dk [B,H,T,Dk], v, dv
+ * [B,H,T,Dv] and beta, dbeta [B,H,T].
+ */
+int oracle_masked_deltaproduct_bwd(const double *q, const double *k, const double *v,
+                                   const double *beta, const double *g, const double *mask,
+                                   const double *s0, const double *dout, const double *dsf, double *dq,
+                                   double *dk, double *dv, double *dbeta, double *dg, double *ds0, int B,
+                                   int H, int T, int r, int Dk, int Dv, double scale, int l2norm) {
+    if (r < 1 || Dk % r != 0) return -2;
+    const int BH = B * H;
+    const int sl = Dk / r;
+    const int BLK = 64;
+    const int nblk = (T + BLK - 1) / BLK;
+    const size_t SD = (size_t)Dk * Dv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int bh = 0; bh < BH; ++bh) {
+        double *Cp = (double *)malloc(sizeof(double) * SD * (nblk > 0 ? nblk : 1));
+        double *E = (double *)malloc(sizeof(double) * SD * BLK);
+        double *D = (double *)malloc(sizeof(double) * SD);
+        double *S = (double *)malloc(sizeof(double) * SD);
+        double *G = (double *)malloc(sizeof(double) * SD);
+        double *kr = (double *)malloc(sizeof(double) * (size_t)r * Dk);
+        double *ev = (double *)malloc(sizeof(double) * (size_t)r * Dv);
+        double *wv = (double *)malloc(sizeof(double) * (size_t)r * Dv);
+        double *z = (double *)malloc(sizeof(double) * (size_t)r * Dv);
+        double *vec = (double *)malloc(sizeof(double) * (size_t)(4 * Dk));
+        if (!Cp || !E || !D || !S || !G || !kr || !ev || !wv || !z || !vec) {
+            failed |= 1;
+        } else {
+            double *kt = vec, *qt = vec + Dk, *gk = vec + 2 * Dk, *tq = vec + 3 * Dk;
+            if (s0)
+                memcpy(S, s0 + (size_t)bh * SD, sizeof(double) * SD);
+            else
+                memset(S, 0, sizeof(double) * SD);
+            for (int t = 0; t < T; ++t) {
+                if (t % BLK == 0) memcpy(Cp + (size_t)(t / BLK) * SD, S, sizeof(double) * SD);
+                const size_t tok = (size_t)bh * T + t;
+                masked_token_step(S, k + tok * Dk, v + tok * Dv, beta[tok], g[tok], mask, r, Dk, Dv, l2norm, kt, z, ev);
+            }
+            if (dsf)
+                memcpy(G, dsf + (size_t)bh * SD, sizeof(double) * SD);
+            else
+                memset(G, 0, sizeof(double) * SD);
+            for (int b = nblk - 1; b >= 0; --b) {
+                const int t0 = b * BLK, t1 = (t0 + BLK < T) ? t0 + BLK : T;
+                memcpy(E, Cp + (size_t)b * SD, sizeof(double) * SD);
+                for (int t = t0; t + 1 < t1; ++t) {
+                    const size_t tok = (size_t)bh * T + t;
+                    double *Sn = E + (size_t)(t - t0 + 1) * SD;
+                    memcpy(Sn, E + (size_t)(t - t0) * SD, sizeof(double) * SD);
+                    masked_token_step(Sn, k + tok * Dk, v + tok * Dv, beta[tok], g[tok], mask, r, Dk, Dv, l2norm, kt, z,
+                                      ev);
+                }
+                for (int t = t1 - 1; t >= t0; --t) {
+                    const size_t tok = (size_t)bh * T + t;
+                    const double a = exp(g[tok]);
+                    memcpy(S, E + (size_t)(t - t0) * SD, sizeof(double) * SD);
+                    masked_token_step(S, k + tok * Dk, v + tok * Dv, beta[tok], g[tok], mask, r, Dk, Dv, l2norm, kt, z,
+                                      ev); /* S: the state after the token; kt: its (unit) key */
+                    const double *Et = E + (size_t)(t - t0) * SD;
+                    for (size_t x = 0; x < SD; ++x) D[x] = a * Et[x];
+                    /* e_i = v - D^T kr_i, and the read keys */
+                    for (int i = 0; i < r; ++i)
+                        for (int m = 0; m < Dk; ++m) kr[(size_t)i * Dk + m] = mask[i * r + m / sl] * kt[m];
+                    for (int i = 0; i < r; ++i)
+                        for (int c = 0; c < Dv; ++c) {
+                            double pr = 0.0;
+                            for (int m = 0; m < Dk; ++m) pr += kr[(size_t)i * Dk + m] * D[(size_t)m * Dv + c];
+                            ev[(size_t)i * Dv + c] = v[tok * Dv + c] - pr;
+                        }
+                    /* output */
+                    const double *go = dout + tok * Dv;
+                    memcpy(qt, q + tok * Dk, sizeof(double) * Dk);
+                    if (l2norm) l2_normalise(qt, Dk);
+                    for (int m = 0; m < Dk; ++m) {
+                        double acc = 0.0;
+                        for (int c = 0; c < Dv; ++c) {
+                            acc += S[(size_t)m * Dv + c] * go[c];
+                            G[(size_t)m * Dv + c] += scale * qt[m] * go[c];
+                        }
+                        tq[m] = scale * acc;
+                    }
+                    if (l2norm)
+                        l2_normalise_bwd(q + tok * Dk, tq, dq + tok * Dk, Dk);
+                    else
+                        memcpy(dq + tok * Dk, tq, sizeof(double) * Dk);
+                    /* w_i = G^T kw_i (slice i rows only) */
+                    const double bt = beta[tok];
+                    for (int i = 0; i < r; ++i)
+                        for (int c = 0; c < Dv; ++c) {
+                            double acc = 0.0;
+                            for (int m = i * sl; m < (i + 1) * sl; ++m) acc += G[(size_t)m * Dv + c] * kt[m];
+                            wv[(size_t)i * Dv + c] = acc;
+                        }
+                    double db = 0.0;
+                    for (int c = 0; c < Dv; ++c) {
+                        double acc = 0.0;
+                        for (int i = 0; i < r; ++i) acc += wv[(size_t)i * Dv + c];
+                        dv[tok * Dv + c] = bt * acc;
+                    }
+                    for (int m = 0; m < Dk; ++m) {
+                        const int i = m / sl; /* the write key of sub-row i covers slice i */
+                        double ge = 0.0;
+                        for (int c = 0; c < Dv; ++c) ge += G[(size_t)m * Dv + c] * ev[(size_t)i * Dv + c];
+                        db += kt[m] * ge;
+                        double acc = bt * ge; /* dkw_i at row m */
+                        for (int ii = 0; ii < r; ++ii) {
+                            double dw = 0.0;
+                            for (int c = 0; c < Dv; ++c) dw += D[(size_t)m * Dv + c] * wv[(size_t)ii * Dv + c];
+                            acc += mask[ii * r + i] * (-bt * dw); /* mask[ii][j] dkr_ii, j = slice of m */
+                        }
+                        gk[m] = acc;
+                    }
+                    dbeta[tok] = db;
+                    if (l2norm)
+                        l2_normalise_bwd(k + tok * Dk, gk, dk + tok * Dk, Dk);
+                    else
+                        memcpy(dk + tok * Dk, gk, sizeof(double) * Dk);
+                    /* dD = G - b sum_i kr_i w_i^T;  dg = <dD, D>;  G <- e^{g} dD */
+                    for (int m = 0; m < Dk; ++m)
+                        for (int c = 0; c < Dv; ++c) {
+                            double acc = 0.0;
+                            for (int i = 0; i < r; ++i) acc += kr[(size_t)i * Dk + m] * wv[(size_t)i * Dv + c];
+                            G[(size_t)m * Dv + c] -= bt * acc;
+                        }
+                    double dd = 0.0;
+                    for (size_t x = 0; x < SD; ++x) dd += G[x] * D[x];
+                    dg[tok] = dd;
+                    for (size_t x = 0; x < SD; ++x) G[x] *= a;
+                }
+            }
+            if (ds0) memcpy(ds0 + (size_t)bh * SD, G, sizeof(double) * SD);
+        }
+        free(Cp);
+        free(E);
+        free(D);
+        free(S);
+        free(G);
+        free(kr);
+        free(ev);
+        free(wv);
+        free(z);
+        free(vec);
+    }
+    return failed ? -1 : 0;
+}
