@@ -397,7 +397,8 @@ def run_ours(args, rank, world, local_rank):
 
 def secondary(args, dev):
     """Device time of the other workloads (not the headline): long-sequence
-    GDN, DeltaProduct r=2, and the camera prep + scan."""
+    GDN, DeltaProduct r=2, the block-masked variant, the GDN backward, and the
+    camera branch (prep, scans, backward passes, fused path)."""
     import torch
     from gated_delta_rule_47_gb300 import binding
     from gated_delta_rule_47_gb300.inputs import WORKLOADS
@@ -454,6 +455,20 @@ def secondary(args, dev):
     out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
                    "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "path": "CUDA cores, fp32"}
     del d, o
+    torch.cuda.empty_cache()
+    # the chunkwise GDN backward on the headline's shape (CUDA cores, fp32 arithmetic)
+    w = WORKLOADS["gdn_b4h16t4096d128_bf16"]
+    d = {k: v.to(dev) for k, v in w.make().items()}
+    gen = torch.Generator(device=dev).manual_seed(3)
+    go = torch.randn(w.B, w.H, w.T, w.D, device=dev, generator=gen).to(torch.bfloat16)
+    wsg = torch.empty(binding.gdn_chunk_bwd_workspace_bytes(w.B, w.H, w.T, w.D, w.D), dtype=torch.uint8,
+                      device=dev)
+    ms = timeit(lambda: binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], go, workspace=wsg))
+    nbytes = w.B * w.H * w.T * (14 * w.D + 14)  # q, k, v, beta, g, do in; dq, dk, dv, dbeta, dg out
+    out["gdn_bwd_b4h16t4096d128_bf16"] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                                          "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                          "launches_per_call": 3, "path": "CUDA cores, fp32"}
+    del d, go, wsg
     torch.cuda.empty_cache()
     w = WORKLOADS["cam_b2n32760h16d128_bf16"]
     d = {k: (v.to(dev) if v is not None else None) for k, v in w.make().items()}

@@ -28,7 +28,8 @@ EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", 
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
            "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd",
            "masked_deltaproduct_chunk_fwd", "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd",
-           "cam_prep_bwd", "cam_scan_bwd_workspace_bytes", "cam_scan_bwd")
+           "cam_prep_bwd", "cam_scan_bwd_workspace_bytes", "cam_scan_bwd", "gdn_chunk_bwd_workspace_bytes",
+           "gdn_chunk_bwd", "deltaproduct_chunk_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +75,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.cam_scan_bwd_workspace_bytes.restype = sz
         lib.cam_scan_bwd.argtypes = [vp] * 14 + [i] * 6 + [f, u, i, vp, sz, vp]
         lib.cam_scan_bwd.restype = i
+        lib.gdn_chunk_bwd_workspace_bytes.argtypes = [i] * 7
+        lib.gdn_chunk_bwd_workspace_bytes.restype = sz
+        lib.gdn_chunk_bwd.argtypes = [vp] * 14 + [i] * 5 + [f, u, i, vp, sz, vp]
+        lib.gdn_chunk_bwd.restype = i
+        lib.deltaproduct_chunk_bwd.argtypes = [vp] * 14 + [i] * 6 + [f, u, i, vp, sz, vp]
+        lib.deltaproduct_chunk_bwd.restype = i
         lib.cam_prep_bwd.argtypes = [vp] * 8 + [f] + [vp] * 8 + [i] * 4 + [f, f, i, vp]
         lib.cam_prep_bwd.restype = i
         lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
@@ -408,6 +415,82 @@ def cam_scan_bwd(q, k, v, beta, decay, do, initial_state=None, dfinal_state=None
                           ws_bytes, _stream(stream))
     _raise("cam_scan_bwd", st)
     return dq, dk, dv, dbeta, ddecay, ds0
+
+
+def gdn_chunk_bwd_workspace_bytes(B, H, T, Dk, Dv, dtype=torch.bfloat16, r=1):
+    code = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    return int(load().gdn_chunk_bwd_workspace_bytes(B, H, T, r, Dk, Dv, code))
+
+
+def deltaproduct_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False,
+                           need_dinitial=False, workspace=None, stream=None):
+    """Backward of deltaproduct_chunk_fwd: k [B,H,T,r,Dk], v [B,H,T,r,Dv],
+    beta [B,H,T,r].  Returns (dq, dk, dv, dbeta, dg, dinitial_state or None);
+    dq, dk, dv in the inputs' dtype, the rest fp32."""
+    B, H, T, Dk = q.shape
+    r, Dv = k.shape[3], v.shape[-1]
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, T, Dk), dt)
+    _check(k, "k", (B, H, T, r, Dk), dt)
+    _check(v, "v", (B, H, T, r, Dv), dt)
+    _check(beta, "beta", (B, H, T, r), dt)
+    _check(g, "g", (B, H, T), torch.float32)
+    _check(do, "do", (B, H, T, Dv), dt)
+    for name, t in (("initial_state", initial_state), ("dfinal_state", dfinal_state)):
+        if t is not None:
+            _check(t, name, (B, H, Dk, Dv), torch.float32)
+    dev = q.device
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbeta = torch.empty(B, H, T, r, dtype=torch.float32, device=dev)
+    dg = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ds0 = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=dev) if need_dinitial else None
+    lib = load()
+    if workspace is None:
+        need = lib.gdn_chunk_bwd_workspace_bytes(B, H, T, r, Dk, Dv, code)
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.deltaproduct_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state), _ptr(do),
+                                    _ptr(dfinal_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
+                                    _ptr(ds0), B, H, T, r, Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code,
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+    _raise("deltaproduct_chunk_bwd", st)
+    return dq, dk, dv, dbeta, dg, ds0
+
+
+def gdn_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False,
+                  need_dinitial=False, workspace=None, stream=None):
+    """Backward of gdn_chunk_fwd.  Returns (dq, dk, dv, dbeta, dg,
+    dinitial_state or None); dq, dk, dv in the inputs' dtype, the rest fp32."""
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, T, Dk), dt)
+    _check(k, "k", (B, H, T, Dk), dt)
+    _check(v, "v", (B, H, T, Dv), dt)
+    _check(beta, "beta", (B, H, T), dt)
+    _check(g, "g", (B, H, T), torch.float32)
+    _check(do, "do", (B, H, T, Dv), dt)
+    for name, t in (("initial_state", initial_state), ("dfinal_state", dfinal_state)):
+        if t is not None:
+            _check(t, name, (B, H, Dk, Dv), torch.float32)
+    dev = q.device
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbeta = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    dg = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ds0 = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=dev) if need_dinitial else None
+    lib = load()
+    if workspace is None:
+        need = lib.gdn_chunk_bwd_workspace_bytes(B, H, T, 1, Dk, Dv, code)
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state), _ptr(do),
+                           _ptr(dfinal_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(ds0), B, H, T,
+                           Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace), ws_bytes,
+                           _stream(stream))
+    _raise("gdn_chunk_bwd", st)
+    return dq, dk, dv, dbeta, dg, ds0
 
 
 def cam_prep_bwd(q_raw, k_raw, proj_q, proj_kv, dq_out, dk_out, dv_out, dk_pre_sq=None, dk_post_sq=None,

@@ -368,6 +368,62 @@ int cam_prep_bwd(const void *q_raw, const void *k_raw, const float *q_norm_w, co
     return gdn::launch_cam_prep_bwd(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype) {
+    if (B < 0 || H < 0 || T < 0 || r < 1 || r > 8) return (size_t)-1;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return (size_t)-1;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
+    gdn::ChunkBwdArgs a{};
+    a.B = B; a.H = H; a.T = T; a.r = r; a.Dk = Dk; a.Dv = Dv;
+    return gdn::chunk_bwd_workspace_bytes(a);
+}
+
+int deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, const void *beta, const float *g,
+                           const float *initial_state, const void *dout, const float *dfinal_state, void *dq,
+                           void *dk, void *dv, float *dbeta, float *dg, float *dinitial_state, int B, int H, int T,
+                           int r, int Dk, int Dv, float scale, unsigned flags, int dtype, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (B < 0 || H < 0 || T < 0 || r < 1 || r > 8) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535 || (long long)T * r >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H * T != 0) {
+        if (!q || !k || !v || !beta || !g || !dout || !dq || !dk || !dv || !dbeta || !dg)
+            return GDN_ERR_INVALID_ARG;
+    }
+    const void *ps[] = {q, k, v, beta, g, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, dg,
+                        dinitial_state};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::ChunkBwdArgs a{q, k, v, beta, g, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, dg,
+                        dinitial_state, B, H, T, r, Dk, Dv, scale, flags, dtype, workspace, workspace_bytes};
+    const size_t need = gdn::chunk_bwd_workspace_bytes(a);
+    if ((long long)B * H * T != 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((long long)B * H == 0) return GDN_OK;
+    if (T == 0) {  // the initial state's gradient is the final state's
+        if (dinitial_state) {
+            const size_t bytes = sizeof(float) * (size_t)B * H * Dk * Dv;
+            cudaError_t e = dfinal_state ? cudaMemcpyAsync(dinitial_state, dfinal_state, bytes,
+                                                           cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(dinitial_state, 0, bytes, st);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    return gdn::launch_chunk_bwd(a, st);
+}
+
+int gdn_chunk_bwd(const void *q, const void *k, const void *v, const void *beta, const float *g,
+                  const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
+                  void *dv, float *dbeta, float *dg, float *dinitial_state, int B, int H, int T, int Dk, int Dv,
+                  float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    return deltaproduct_chunk_bwd(q, k, v, beta, g, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, dg,
+                                  dinitial_state, B, H, T, 1, Dk, Dv, scale, flags, dtype, workspace,
+                                  workspace_bytes, stream);
+}
+
 int gdn_get_device_error(void *stream) {
     const int a = gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
     const int b = gdn::cam_prep_read_clear_error();

@@ -162,6 +162,24 @@ int launch_cam_prep_bwd(const CamBwdArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the streamed camera prep (GDN_OK or GDN_ERR_TIMEOUT).
 int cam_prep_read_clear_error();
 
+// Backward of the chunkwise GDN / DeltaProduct forward (r = 1 for GDN).
+struct ChunkBwdArgs {
+    const void *q, *k, *v, *beta;
+    const float *g, *s0;
+    const void *dout;
+    const float *dsf;
+    void *dq, *dk, *dv;
+    float *dbeta, *dg, *ds0;
+    int B, H, T, r, Dk, Dv;
+    float scale;
+    unsigned flags;
+    int dtype;
+    void *ws;
+    size_t ws_bytes;
+};
+size_t chunk_bwd_workspace_bytes(const ChunkBwdArgs &a);
+int launch_chunk_bwd(const ChunkBwdArgs &a, cudaStream_t stream);
+
 // Counts one kernel launch (thread-safe); read by gdn_launch_count().
 void note_launch();
 

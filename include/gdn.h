@@ -301,6 +301,59 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
                  int H, int D, float k_scale, float eps, int dtype, void *stream);
 
 /*
+ * Bytes of device workspace gdn_chunk_bwd / deltaproduct_chunk_bwd need
+ * (r = 1 for GDN): per head and chunk of floor(64 / r) tokens, the chunk's
+ * WY factors, the states entering it and their gradients (about 340 KB at
+ * Dk = Dv = 128).  0 when T = 0; (size_t)-1 for sizes they reject.
+ */
+size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype);
+
+/*
+ * gdn_chunk_bwd -- backward of gdn_chunk_fwd (gated_deltaproduct test.py: the
+ * state-gradient kernel `gated_chunk_delta_rule_bwd_kernel_dhu`, the
+ * chunk-local `gated_chunk_delta_rule_bwd_kernel_dqkw` and the WY backward
+ * `gated_bwd_prepare_wy_repr_kernel`): the gradients of q, k, v, beta, g and
+ * the initial state, given the gradient of o and (optionally) of the final
+ * state.  Per token, with G the gradient of the state after the token and X
+ * the decayed state the correction starts from:
+ *     G += scale q do^T;  dq = scale S do;  e = v - X^T k,  w = G^T k
+ *     dv = beta w;  dbeta = k.(G e);  dk = beta (G e - X w);  G <- G - beta k w^T
+ *     dg = <G, X>;  G <- exp(g) G
+ * computed chunk-wise in the WY form (64-row chunks, fp32 arithmetic on the
+ * CUDA cores, three launches: the chunk factors, the forward state chain and
+ * the reverse gradient chain side by side, then the input gradients).
+ *
+ *   q, k, v, beta, g, initial_state, scale, dtype, Dk, Dv: as given to
+ *           gdn_chunk_fwd (flags: GDN_QK_L2NORM and GDN_PATH_SIMT, which
+ *           changes nothing: this is the only path)
+ *   dout    [B,H,T,Dv] dtype;  dfinal_state [B,H,Dk,Dv] fp32 or NULL (= zero)
+ *   dq, dk [B,H,T,Dk], dv [B,H,T,Dv] dtype (written);  dbeta [B,H,T] fp32;
+ *   dg [B,H,T] fp32;  dinitial_state [B,H,Dk,Dv] fp32 or NULL (not wanted)
+ *   workspace: gdn_chunk_bwd_workspace_bytes(...) bytes, 16-byte aligned
+ *           (GDN_ERR_WORKSPACE when missing or short); its contents need no
+ *           initialisation and are not meaningful afterwards.
+ * T = 0 or B*H = 0 enqueues at most the copy of dfinal_state (or zeros) into
+ * dinitial_state.
+ */
+int gdn_chunk_bwd(const void *q, const void *k, const void *v, const void *beta, const float *g,
+                  const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
+                  void *dv, float *dbeta, float *dg, float *dinitial_state, int B, int H, int T, int Dk, int Dv,
+                  float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * deltaproduct_chunk_bwd -- backward of deltaproduct_chunk_fwd: per token the
+ * r sub-steps are undone last first, then the decay (gdn_chunk_bwd's step per
+ * sub-step).  k, dk [B,H,T,r,Dk]; v, dv [B,H,T,r,Dv]; beta, dbeta [B,H,T,r];
+ * 1 <= r <= 8; each chunk holds floor(64 / r) tokens.  Everything else as
+ * gdn_chunk_bwd; r = 1 computes exactly gdn_chunk_bwd.
+ */
+int deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, const void *beta, const float *g,
+                           const float *initial_state, const void *dout, const float *dfinal_state, void *dq,
+                           void *dk, void *dv, float *dbeta, float *dg, float *dinitial_state, int B, int H, int T,
+                           int r, int Dk, int Dv, float scale, unsigned flags, int dtype, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace cam_scan_bwd needs ((size_t)-1 for sizes it
  * rejects): the fp32 state entering every frame, and the last.
  */

@@ -209,3 +209,33 @@ def test_cam_scan_bwd_argument_checks(lib):
     assert call(q=u + 4) == 3
     assert call(ws=None) == 4
     assert lib.cam_scan_bwd_workspace_bytes(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 4 * 2 * 4 * 64 * 64
+
+
+def test_chunk_bwd_argument_checks(lib):
+    f = lib.deltaproduct_chunk_bwd
+    u = 0x10000
+    bad = ctypes.c_size_t(-1).value
+
+    def call(r=1, flags=0, Dk=64, T=70, dtype=binding.GDN_F32, q=u, ws=u, ws_bytes=1 << 40):
+        return f(q, u, u, u, u, None, u, None, u, u, u, u, u, None, 1, 2, T, r, Dk, 64, 1.0, flags, dtype, ws,
+                 ws_bytes, None)
+
+    assert call(r=0) == 1
+    assert call(r=9) == 1
+    assert call(flags=binding.GDN_CAM_REVERSE) == 1
+    assert call(Dk=96) == 2
+    assert call(T=-1) == 1
+    assert call(dtype=5) == 1
+    assert call(q=None) == 1
+    assert call(q=u + 4) == 3
+    assert call(ws=None) == 4
+    assert call(ws_bytes=16) == 4
+    assert lib.gdn_chunk_bwd(u, u, u, u, u, None, u, None, None, u, u, u, u, None, 1, 2, 5, 64, 64, 1.0, 0,
+                             binding.GDN_F32, u, 1 << 40, None) == 1  # dq missing
+    wsb = lib.gdn_chunk_bwd_workspace_bytes
+    per = 64 * 64 + 2 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 64 + 64  # floats per head and chunk at D = 64
+    assert wsb(1, 2, 70, 1, 64, 64, binding.GDN_F32) == 4 * 2 * 2 * per  # 70 tokens: 2 chunks of 64
+    assert wsb(1, 2, 70, 3, 64, 64, binding.GDN_F32) == 4 * 2 * 4 * per  # 21 tokens per chunk
+    assert wsb(1, 2, 0, 1, 64, 64, binding.GDN_F32) == 0
+    assert wsb(1, 2, 70, 9, 64, 64, binding.GDN_F32) == bad
+    assert wsb(1, 2, 70, 1, 96, 64, binding.GDN_F32) == bad

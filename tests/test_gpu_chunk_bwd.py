@@ -1,0 +1,141 @@
+"""GPU parity of the chunkwise GDN / DeltaProduct backward (gated_deltaproduct
+test.py: `gated_chunk_delta_rule_bwd_kernel_dhu`,
+`gated_chunk_delta_rule_bwd_kernel_dqkw`, `gated_bwd_prepare_wy_repr_kernel`)
+against the fp64 oracle backward, itself pinned by finite differences of the
+forward oracle, through the C ABI.  Metric: max|g - g_ref| / max|g_ref| per
+gradient, at most 1e-4 with fp32 tensors and 1e-2 with bf16 tensors."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_47_gb300 import binding
+from gated_delta_rule_47_gb300.inputs import gdn_inputs
+from tests.gpu_util import TOL_BF16, TOL_F32, ensure_lib, heads, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("dq", "dk", "dv", "dbeta", "dg", "ds0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def grads_case(B, H, T, Dk, Dv, dtype, l2norm, r=None, seed=0, state=True):
+    inp = gdn_inputs(B, H, T, Dk, Dv, seed=seed, dtype=dtype, r=r, initial_state=state, normalise_qk=not l2norm)
+    gen = torch.Generator().manual_seed(seed + 1)
+    do = torch.randn(B, H, T, Dv, generator=gen).to(inp["q"].dtype)
+    dsf = torch.randn(B, H, Dk, Dv, generator=gen) if state else None
+    return inp, do, dsf
+
+
+@pytest.mark.parametrize("l2norm", [False, True])
+@pytest.mark.parametrize("dtype,tol", [("f32", TOL_F32), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("T,Dk,Dv", [(150, 128, 128), (64, 64, 64), (1, 128, 64), (97, 64, 128), (200, 128, 64)])
+def test_gdn_backward(T, Dk, Dv, dtype, tol, l2norm):
+    inp, do, dsf = grads_case(1, 2, T, Dk, Dv, dtype, l2norm, seed=T + Dk + Dv)
+    d = to_dev(inp)
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"], dsf.cuda(),
+                                scale=0.8, l2norm=l2norm, need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf,
+                         scale=0.8, l2norm=l2norm)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= tol, name
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", TOL_F32), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("r,T", [(2, 90), (3, 50), (4, 33), (8, 17)])
+def test_deltaproduct_backward(r, T, dtype, tol):
+    inp, do, dsf = grads_case(1, 2, T, 128, 128, dtype, False, r=r, seed=10 * r + T)
+    d = to_dev(inp)
+    got = binding.deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"],
+                                         dsf.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.deltaproduct_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= tol, name
+
+
+def test_deltaproduct_r1_is_gdn():
+    """r = 1 of the DeltaProduct entry point computes exactly the GDN backward."""
+    inp, do, dsf = grads_case(1, 2, 77, 128, 128, "bf16", True, seed=5)
+    d = to_dev(inp)
+    a = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"], dsf.cuda(),
+                              l2norm=True, need_dinitial=True)
+    b = binding.deltaproduct_chunk_bwd(d["q"], d["k"][:, :, :, None].contiguous(), d["v"][:, :, :, None].contiguous(),
+                                       d["beta"][:, :, :, None].contiguous(), d["g"], do.cuda(), d["initial_state"],
+                                       dsf.cuda(), l2norm=True, need_dinitial=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x.reshape(y.shape), y)
+
+
+def test_no_state_and_no_final_gradient():
+    """No initial state (zero) and no final-state gradient (zero)."""
+    inp, do, _ = grads_case(2, 1, 130, 128, 128, "bf16", False, seed=3, state=False)
+    d = to_dev(inp)
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name
+
+
+def test_empty_sequence_passes_the_final_gradient_through():
+    """T = 0: the initial state's gradient is the final state's (zeros without one)."""
+    B, H, Dk, Dv = 1, 3, 64, 128
+    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    q, k, v, beta = e(B, H, 0, Dk), e(B, H, 0, Dk), e(B, H, 0, Dv), e(B, H, 0)
+    g = torch.empty(B, H, 0, device="cuda")
+    do = e(B, H, 0, Dv)
+    dsf = torch.randn(B, H, Dk, Dv, device="cuda")
+    got = binding.gdn_chunk_bwd(q, k, v, beta, g, do, None, dsf, need_dinitial=True)
+    torch.cuda.synchronize()
+    assert torch.equal(got[5], dsf)
+    got = binding.gdn_chunk_bwd(q, k, v, beta, g, do, None, None, need_dinitial=True)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(got[5]) == 0
+
+
+def test_zero_keys_under_the_unit_norm():
+    """Zero key and query rows stay zero under the unit-norm map; their
+    gradients follow the map's floor (x / 1e-12) as in the oracle."""
+    inp, do, dsf = grads_case(1, 1, 70, 64, 64, "f32", True, seed=4)
+    inp["k"][0, 0, 5] = 0.0
+    inp["q"][0, 0, 9] = 0.0
+    d = to_dev(inp)
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"], dsf.cuda(),
+                                l2norm=True, need_dinitial=True)
+    torch.cuda.synchronize()
+    ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf,
+                         l2norm=True)
+    for name, x, y in zip(NAMES, got, ref):
+        if name in ("dq", "dk"):  # the floored rows are ~1e12 larger: compare them on their own
+            row = 9 if name == "dq" else 5
+            xr, yr = x[0, 0, row].double().cpu().numpy(), y[0, 0, row]
+            assert np.max(np.abs(xr - yr)) <= 1e-3 * max(np.max(np.abs(yr)), 1.0), name
+            x = x.clone()
+            x[0, 0, row] = 0
+            y = y.copy()
+            y[0, 0, row] = 0
+        assert rel_err(x, y) <= TOL_F32, name
+
+
+def test_full_size_sampled_heads():
+    """B4 H16 T4096 D128 bf16 (the headline forward's shape): every head's
+    gradients on the GPU, three heads against the oracle."""
+    B, H, T = 4, 16, 4096
+    inp, do, dsf = grads_case(B, H, T, 128, 128, "bf16", False, seed=21, state=False)
+    d = to_dev(inp)
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda())
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    idx = [0, 37, 63]
+    sub = {k: heads(v, idx) for k, v in inp.items()}
+    ref = oracle.gdn_bwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], heads(do, idx))
+    for name, x, y in zip(NAMES[:5], got[:5], ref[:5]):
+        assert rel_err(heads(x, idx).cpu(), y) <= TOL_BF16, name
