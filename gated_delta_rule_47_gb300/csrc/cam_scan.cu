@@ -1016,12 +1016,11 @@ __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, f
 struct SimtParams {
     const void *q, *k, *v, *beta;
     const float *decay, *s0;
-    void *o;       // may be null: no outputs (the backward's state pass)
+    void *o;
     float *sf;
     int F, S, N, Dk, Dv;
     float scale;
     unsigned flags;
-    float *snap;   // may be null: [BH][F+1][Dk][Dv] fp32, the state entering each frame, then the last
 };
 
 template <typename T>
@@ -1070,12 +1069,6 @@ __global__ void __launch_bounds__(kSimtThreads) cam_scan_simt_kernel(SimtParams 
     for (int itf = 0; itf < p.F; ++itf) {
         const int qf = rev ? p.F - 1 - itf : itf;
         const int kf = rev ? p.F - itf : itf;
-        if (p.snap && !rev) {
-            for (int e = tid; e < Dk * 32; e += kSimtThreads) {
-                const int i = e >> 5, c = e & 31;
-                p.snap[(((size_t)bh * (p.F + 1) + kf) * Dk + i) * Dv + j0 + c] = sS[i][c];
-            }
-        }
         if (!rev || itf > 0) {
             const float d = p.decay[(size_t)bh * p.F + kf];
             // dS[i][jj] for rows i = r8 + 8 m, accumulated over the frame
@@ -1143,221 +1136,8 @@ __global__ void __launch_bounds__(kSimtThreads) cam_scan_simt_kernel(SimtParams 
             const int i = e >> 5, c = e & 31;
             p.sf[((size_t)bh * Dk + i) * Dv + j0 + c] = sS[i][c];
         }
-    if (p.snap && !rev)
-        for (int e = tid; e < Dk * 32; e += kSimtThreads) {
-            const int i = e >> 5, c = e & 31;
-            p.snap[(((size_t)bh * (p.F + 1) + p.F) * Dk + i) * Dv + j0 + c] = sS[i][c];
-        }
 }
 
-// ======================================================= backward kernel
-// Backward of the frame scan (fused_cam_gdn.py, `_cam_scan_bwd_kernel`,
-// forward direction), one CTA per head, fp32.  With S' the state entering
-// frame f and S_f the state after it (both from the forward pass's
-// snapshots), R = diag(beta)(V - d K S'), S_f = d S' + K^T R, O = scale Q S_f,
-// and dS the adjoint of S_f, frames from last to first:
-//   dS += scale Q^T dO;   dq_t = scale S_f do_t
-//   dR = K dS;  dv_t = beta_t dR_t;  dbeta_t = dR_t . (v_t - d S'^T k_t)
-//   dk_t = dS r_t - d beta_t S' dR_t;   dd_f = <dS, S'> - sum_t beta_t dR_t . S'^T k_t
-//   dS <- d (dS - K^T diag(beta) dR)
-// and with unit-norm q, k the adjoint of x / ||x||.  Tiles of 16 tokens, one
-// warp per token; the state-sized sums are spread over the threads, thread
-// tid owning elements tid + 512 m of the row-major Dk x Dv matrices.
-constexpr int kBwdThreads = 512;
-constexpr int kBwdTok = 16;
-
-struct BwdParams {
-    const void *q, *k, *v, *beta, *dout;
-    const float *decay, *snap, *dsf;
-    void *dq, *dk, *dv;
-    float *dbeta, *ddecay, *ds0;
-    int F, S, N, Dk, Dv;
-    float scale;
-    unsigned flags;
-};
-
-template <typename T>
-__global__ void __launch_bounds__(kBwdThreads, 1) cam_scan_bwd_kernel(BwdParams p) {
-    extern __shared__ float bsm[];
-    const int Dk = p.Dk, Dv = p.Dv, VP = Dv + 1;
-    float *dS = bsm;                         // [Dk][VP]
-    float *Sb = dS + Dk * VP;                // [Dk][VP]  S_f, then S'
-    float *Xt = Sb + Dk * VP;                // [16][Dk]  q or k rows (unit when asked)
-    float *Yt = Xt + kBwdTok * Dk;           // [16][Dv]  do or v rows
-    float *dRt = Yt + kBwdTok * Dv;          // [16][Dv]
-    float *Rt = dRt + kBwdTok * Dv;          // [16][Dv]
-    float *red = Rt + kBwdTok * Dv;          // [16] block-reduction scratch
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const size_t bh = blockIdx.x;
-    const bool l2n = (p.flags & GDN_QK_L2NORM) != 0;
-    const T *q = static_cast<const T *>(p.q) + bh * p.N * Dk;
-    const T *k = static_cast<const T *>(p.k) + bh * p.N * Dk;
-    const T *v = static_cast<const T *>(p.v) + bh * p.N * Dv;
-    const T *bt = static_cast<const T *>(p.beta) + bh * p.N;
-    const T *go = static_cast<const T *>(p.dout) + bh * p.N * Dv;
-    T *dq = static_cast<T *>(p.dq) + bh * p.N * Dk;
-    T *dk = static_cast<T *>(p.dk) + bh * p.N * Dk;
-    T *dv = static_cast<T *>(p.dv) + bh * p.N * Dv;
-    const int nel = Dk * Dv;
-    for (int e = tid; e < nel; e += kBwdThreads) {
-        const int i = e / Dv, c = e % Dv;
-        dS[i * VP + c] = p.dsf ? p.dsf[bh * nel + e] : 0.f;
-    }
-    // rows of x (q or k) for the tile's tokens into Xt, unit when asked; returns
-    // this warp's row norm (warp w = token w of the tile)
-    auto load_x = [&](const T *x, int t0, int nrow) -> float {
-        float ss = 0.f;
-        for (int i = lane; i < Dk; i += 32) {
-            const float a = w < nrow ? ldf(x, (size_t)(t0 + w) * Dk + i) : 0.f;
-            Xt[w * Dk + i] = a;
-            ss += a * a;
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float nrm = fmaxf(sqrtf(ss), 1e-12f);
-        if (l2n)
-            for (int i = lane; i < Dk; i += 32) Xt[w * Dk + i] /= nrm;
-        return nrm;
-    };
-    // dx of row w from dxhat (per lane, dims lane + 32 m): the unit-norm adjoint
-    auto store_dx = [&](T *dst, int t, float (&g)[4], float nrm, bool valid) {
-        if (l2n) {
-            float yd = 0.f;
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                if (lane + 32 * m < Dk) yd += Xt[w * Dk + lane + 32 * m] * g[m];
-#pragma unroll
-            for (int off = 16; off; off >>= 1) yd += __shfl_xor_sync(0xffffffffu, yd, off);
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                if (lane + 32 * m < Dk) g[m] = (g[m] - Xt[w * Dk + lane + 32 * m] * yd) / nrm;
-        }
-        if (valid)
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                if (lane + 32 * m < Dk) stf(dst, (size_t)t * Dk + lane + 32 * m, g[m]);
-    };
-    for (int f = p.F - 1; f >= 0; --f) {
-        const float d = p.decay[bh * p.F + f];
-        const float *Sf = p.snap + (bh * (p.F + 1) + f + 1) * nel, *Sp = p.snap + (bh * (p.F + 1) + f) * nel;
-        __syncthreads();
-        for (int e = tid; e < nel; e += kBwdThreads) Sb[(e / Dv) * VP + e % Dv] = Sf[e];
-        // ---- outputs: dq and dS += scale Q^T dO
-        for (int t0 = 0; t0 < p.S; t0 += kBwdTok) {
-            const int nrow = min(kBwdTok, p.S - t0);
-            const int g0 = f * p.S + t0;
-            __syncthreads();
-            const float nq = load_x(q, g0, nrow);
-            for (int c = lane; c < Dv; c += 32) Yt[w * Dv + c] = w < nrow ? ldf(go, (size_t)(g0 + w) * Dv + c) : 0.f;
-            __syncthreads();
-            float gq[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int i = lane + 32 * m;
-                float acc = 0.f;
-                if (i < Dk)
-                    for (int c = 0; c < Dv; ++c) acc += Sb[i * VP + c] * Yt[w * Dv + c];
-                gq[m] = p.scale * acc;
-            }
-            store_dx(dq, g0 + w, gq, nq, w < nrow);
-            for (int e = tid; e < nel; e += kBwdThreads) {
-                const int i = e / Dv, c = e % Dv;
-                float acc = 0.f;
-#pragma unroll 4
-                for (int t = 0; t < kBwdTok; ++t) acc += Xt[t * Dk + i] * Yt[t * Dv + c];
-                dS[i * VP + c] += p.scale * acc;
-            }
-        }
-        __syncthreads();
-        for (int e = tid; e < nel; e += kBwdThreads) Sb[(e / Dv) * VP + e % Dv] = Sp[e];
-        __syncthreads();
-        // ---- the frame's update
-        float dd = 0.f;
-        for (int e = tid; e < nel; e += kBwdThreads) dd += dS[(e / Dv) * VP + e % Dv] * Sb[(e / Dv) * VP + e % Dv];
-        float X[32];
-#pragma unroll
-        for (int m = 0; m < 32; ++m) X[m] = 0.f;
-        for (int t0 = 0; t0 < p.S; t0 += kBwdTok) {
-            const int nrow = min(kBwdTok, p.S - t0);
-            const int g0 = f * p.S + t0;
-            __syncthreads();
-            const float nk = load_x(k, g0, nrow);
-            for (int c = lane; c < Dv; c += 32) Yt[w * Dv + c] = w < nrow ? ldf(v, (size_t)(g0 + w) * Dv + c) : 0.f;
-            const float b = w < nrow ? ldf(bt, (size_t)(g0 + w)) : 0.f;
-            __syncthreads();
-            // dR, S'^T k, r of token w, values c = lane + 32 m
-            float db = 0.f;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int c = lane + 32 * m;
-                if (c < Dv) {
-                    float a = 0.f, pk = 0.f;
-                    for (int i = 0; i < Dk; ++i) {
-                        const float x = Xt[w * Dk + i];
-                        a += x * dS[i * VP + c];
-                        pk += x * Sb[i * VP + c];
-                    }
-                    const float vv = Yt[w * Dv + c] - d * pk;
-                    dRt[w * Dv + c] = a;
-                    Rt[w * Dv + c] = b * vv;
-                    db += a * vv;
-                    dd -= b * a * pk;
-                    if (w < nrow) stf(dv, (size_t)(g0 + w) * Dv + c, b * a);
-                }
-            }
-#pragma unroll
-            for (int off = 16; off; off >>= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
-            if (lane == 0 && w < nrow) p.dbeta[bh * p.N + g0 + w] = db;
-            __syncthreads();
-            // dk of token w, dims i = lane + 32 m
-            float gk[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int i = lane + 32 * m;
-                float acc = 0.f;
-                if (i < Dk)
-                    for (int c = 0; c < Dv; ++c)
-                        acc += dS[i * VP + c] * Rt[w * Dv + c] - d * b * Sb[i * VP + c] * dRt[w * Dv + c];
-                gk[m] = acc;
-            }
-            // X += K^T diag(beta) dR over the tile (before Xt is overwritten)
-#pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const int e = tid + kBwdThreads * m;
-                if (e < nel) {
-                    const int i = e / Dv, c = e % Dv;
-                    float acc = 0.f;
-                    for (int t = 0; t < nrow; ++t)
-                        acc += Xt[t * Dk + i] * ldf(bt, (size_t)(g0 + t)) * dRt[t * Dv + c];
-                    X[m] += acc;
-                }
-            }
-            store_dx(dk, g0 + w, gk, nk, w < nrow);
-        }
-        // ddecay of frame f, then dS <- d (dS - X)
-#pragma unroll
-        for (int off = 16; off; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
-        __syncthreads();
-        if (lane == 0) red[w] = dd;
-        __syncthreads();
-        if (tid == 0) {
-            float t = 0.f;
-            for (int i = 0; i < kBwdThreads / 32; ++i) t += red[i];
-            p.ddecay[bh * p.F + f] = t;
-        }
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const int e = tid + kBwdThreads * m;
-            if (e < nel) {
-                const int i = e / Dv, c = e % Dv;
-                dS[i * VP + c] = d * (dS[i * VP + c] - X[m]);
-            }
-        }
-    }
-    __syncthreads();
-    if (p.ds0)
-        for (int e = tid; e < nel; e += kBwdThreads) p.ds0[bh * nel + e] = dS[(e / Dv) * VP + e % Dv];
-}
 
 // ================================================================ host side
 int launch_tc(const CamScanArgs &a, cudaStream_t stream) {
@@ -1461,44 +1241,16 @@ int launch_fused(const CamFusedArgs &a, cudaStream_t stream) {
 
 template <typename T>
 int launch_simt(const CamScanArgs &a, cudaStream_t stream) {
-    SimtParams sp{a.q, a.k, a.v, a.beta, a.decay, a.s0, a.o, a.sf, a.F, a.S, a.F * a.S, a.Dk, a.Dv, a.scale, a.flags,
-                  nullptr};
+    SimtParams sp{a.q, a.k, a.v, a.beta, a.decay, a.s0, a.o, a.sf, a.F, a.S, a.F * a.S, a.Dk, a.Dv, a.scale, a.flags};
     dim3 grid((unsigned)(a.B * a.H), (unsigned)(a.Dv / 32));
     cam_scan_simt_kernel<T><<<grid, kSimtThreads, 0, stream>>>(sp);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-template <typename T>
-int launch_bwd_t(const CamScanBwdArgs &a, cudaStream_t stream) {
-    float *snap = static_cast<float *>(a.ws);
-    // 1. the forward states entering each frame, and the last
-    SimtParams sp{a.q, a.k, a.v, a.beta, a.decay, a.s0, nullptr, nullptr, a.F, a.S, a.F * a.S, a.Dk, a.Dv, 1.f,
-                  a.flags, snap};
-    cam_scan_simt_kernel<T><<<dim3((unsigned)(a.B * a.H), (unsigned)(a.Dv / 32)), kSimtThreads, 0, stream>>>(sp);
-    note_launch();
-    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    // 2. the adjoint, frames from last to first
-    const size_t smem = sizeof(float) * (2 * (size_t)a.Dk * (a.Dv + 1) + kBwdTok * (size_t)a.Dk + 3 * kBwdTok * (size_t)a.Dv + 16);
-    if (cudaFuncSetAttribute(cam_scan_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return GDN_ERR_CUDA;
-    BwdParams bp{a.q, a.k, a.v, a.beta, a.dout, a.decay, snap, a.dsf, a.dq, a.dk, a.dv, a.dbeta, a.ddecay, a.ds0,
-                 a.F, a.S, a.F * a.S, a.Dk, a.Dv, a.scale, a.flags};
-    cam_scan_bwd_kernel<T><<<(unsigned)(a.B * a.H), kBwdThreads, smem, stream>>>(bp);
-    note_launch();
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-}
 
 }  // namespace
 
-size_t cam_scan_bwd_workspace_bytes(const CamScanBwdArgs &a) {
-    return sizeof(float) * (size_t)a.B * a.H * (a.F + 1) * a.Dk * a.Dv;
-}
-
-int launch_cam_scan_bwd(const CamScanBwdArgs &a, cudaStream_t stream) {
-    return a.dtype == GDN_BF16 ? launch_bwd_t<__nv_bfloat16>(a, stream) : launch_bwd_t<float>(a, stream);
-}
 
 bool cam_scan_tc_supported(const CamScanArgs &a) {
     if (a.flags & GDN_PATH_SIMT) return false;

@@ -37,96 +37,17 @@
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
+#include "simt_tile.cuh"
 #include "tri_inverse.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kC = 64;          // rows of a chunk (padded)
+using namespace tile;
 constexpr int LC = kC + 1;      // leading dimension of the 64 x 64 tiles
-constexpr int kThr = 512;       // threads of the per-chunk kernels
 constexpr int kChainThr = 256;  // threads of a chain CTA
 constexpr int kSlice = 32;      // value columns per chain CTA
 constexpr int LS = kSlice + 1;
-
-__device__ __forceinline__ float ld_f(const float *p) { return *p; }
-__device__ __forceinline__ float ld_f(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
-__device__ __forceinline__ void st_f(float *p, float x) { *p = x; }
-__device__ __forceinline__ void st_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
-
-// acc[i][j] += sum_{k < K} A(m_i, k) B(k, n_j) with m_i = ty + (NTHR/16) i and
-// n_j = tx + 16 j (tx = thread % 16, ty = thread / 16), A(m, k) = A[m am + k ak]
-// and B(k, n) = B[k bk + n bn] in shared memory.  Tiles with an odd leading
-// dimension keep both orientations free of bank conflicts.
-template <int NTHR, int TI, int TJ>
-__device__ __forceinline__ void mm(float (&acc)[TI][TJ], const float *A, int am, int ak, const float *B, int bk,
-                                   int bn, int K) {
-    constexpr int RS = NTHR / 16;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const float *a0 = A + ty * am;
-    const float *b0 = B + tx * bn;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[TI], b[TJ];
-#pragma unroll
-        for (int i = 0; i < TI; ++i) a[i] = a0[RS * i * am + k * ak];
-#pragma unroll
-        for (int j = 0; j < TJ; ++j) b[j] = b0[k * bk + 16 * j * bn];
-#pragma unroll
-        for (int i = 0; i < TI; ++i)
-#pragma unroll
-            for (int j = 0; j < TJ; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-}
-
-template <int TI, int TJ>
-__device__ __forceinline__ void zero(float (&a)[TI][TJ]) {
-#pragma unroll
-    for (int i = 0; i < TI; ++i)
-#pragma unroll
-        for (int j = 0; j < TJ; ++j) a[i][j] = 0.f;
-}
-
-// Sum over the 16 lanes that hold one row of a tile (lanes differing in bits 0..3).
-__device__ __forceinline__ float row_sum16(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    return x;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// dst[a][0..D) (leading dimension D + 1) = row a of src for a < nvalid, else 0,
-// for the 64 rows of a chunk.  With norm, each row is divided by max(|row|,
-// 1e-12) and its plain norm kept in nrm[a].
-template <typename T, int D>
-__device__ void load_rows(float *dst, const T *src, int nvalid, bool norm, float *nrm) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int a = warp; a < kC; a += kThr / 32) {
-        float x[D / 32];
-        float ss = 0.f;
-#pragma unroll
-        for (int u = 0; u < D / 32; ++u) {
-            x[u] = a < nvalid ? ld_f(src + (size_t)a * D + lane + 32 * u) : 0.f;
-            ss += x[u] * x[u];
-        }
-        if (norm) {
-            ss = warp_sum(ss);
-            const float n = sqrtf(ss);
-            const float inv = 1.f / fmaxf(n, 1e-12f);
-#pragma unroll
-            for (int u = 0; u < D / 32; ++u) x[u] *= inv;
-            if (lane == 0) nrm[a] = n;
-        }
-#pragma unroll
-        for (int u = 0; u < D / 32; ++u) dst[a * (D + 1) + lane + 32 * u] = x[u];
-    }
-}
 
 struct BwdParams {
     const void *q, *k, *v, *beta, *dout;

@@ -355,7 +355,9 @@ int deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, const vo
 
 /*
  * Bytes of device workspace cam_scan_bwd needs ((size_t)-1 for sizes it
- * rejects): the fp32 state entering every frame, and the last.
+ * rejects): per head and frame, the frame's products K^T diag(beta) K,
+ * K^T diag(beta) V and scale Q^T dO, the state entering it and the gradient
+ * of the state after it (fp32), and one float per 64-token tile.
  */
 size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, int dtype);
 
@@ -378,8 +380,10 @@ size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, 
  *   dq, dk [B,H,N,Dk], dv [B,H,N,Dv] dtype;  dbeta [B,H,N] fp32;
  *   ddecay [B,H,F] fp32;  dinitial_state [B,H,Dk,Dv] fp32 or NULL
  *   workspace: cam_scan_bwd_workspace_bytes bytes, 16-byte aligned.
- * CUDA-core kernels, fp32 arithmetic: a forward pass that keeps the states,
- * then one CTA per head walking the frames backwards.
+ * CUDA-core kernels, fp32 arithmetic, four launches: the frame products (one
+ * CTA per frame, head and product), the forward state chain and the reverse
+ * gradient chain side by side (32 value columns per CTA), the token
+ * gradients (one CTA per 64-token tile), then each frame's ddecay.
  */
 int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
                  const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,

@@ -208,7 +208,9 @@ def test_cam_scan_bwd_argument_checks(lib):
     assert call(q=None) == 1
     assert call(q=u + 4) == 3
     assert call(ws=None) == 4
-    assert lib.cam_scan_bwd_workspace_bytes(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 4 * 2 * 4 * 64 * 64
+    # G, H, P and dX per frame, the states entering each frame and the last, one share per tile
+    assert lib.cam_scan_bwd_workspace_bytes(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 4 * (
+        2 * 3 * 4 * 64 * 64 + 2 * 4 * 64 * 64 + 2 * 3 * 1)
 
 
 def test_chunk_bwd_argument_checks(lib):
