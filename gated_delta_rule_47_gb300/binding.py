@@ -377,10 +377,10 @@ def cam_prep_fwd(q_raw, k_raw, v_raw, proj_q, proj_kv, q_norm_w=None, k_norm_w=N
 
 
 def cam_scan_bwd(q, k, v, beta, decay, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False,
-                 need_dinitial=False, workspace=None, stream=None):
+                 need_dinitial=False, workspace=None, stream=None, simt=False):
     """Backward of cam_scan_fwd (forward direction).  Returns (dq, dk, dv,
     dbeta, ddecay, dinitial_state or None); dq, dk, dv in the inputs' dtype,
-    the rest fp32."""
+    the rest fp32.  simt=True keeps the token gradients on the CUDA cores."""
     B, H, N, Dk = q.shape
     Dv = v.shape[-1]
     F = decay.shape[-1]
@@ -411,8 +411,9 @@ def cam_scan_bwd(q, k, v, beta, decay, do, initial_state=None, dfinal_state=None
     ws_bytes = workspace.numel() * workspace.element_size()
     st = lib.cam_scan_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(decay), _ptr(initial_state), _ptr(do),
                           _ptr(dfinal_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(ddecay), _ptr(ds0),
-                          B, H, F, S, Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace),
-                          ws_bytes, _stream(stream))
+                          B, H, F, S, Dk, Dv, float(scale),
+                          (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0), code,
+                          _ptr(workspace), ws_bytes, _stream(stream))
     _raise("cam_scan_bwd", st)
     return dq, dk, dv, dbeta, ddecay, ds0
 

@@ -21,17 +21,28 @@
 //   2. fb_chain_kernel: the states E_f (forward) and the gradients dX_f
 //      (reverse, down to the initial state's) side by side, each CTA holding
 //      32 value columns of one head.
-//   3. fb_token_kernel (one CTA per 64-token tile of a frame): every token's
-//      gradients, and the tile's share of ddecay.
+//   3. the token gradients, and each tile's share of ddecay:
+//      fb_token_tc_kernel (bf16, Dk = Dv = 128, one CTA per 128-token tile):
+//      K and dO tiles by TMA, the frame's E_f, dX_f and X_f as bf16 hi / lo
+//      operand images (written by the chain kernel) by bulk copies; K E and
+//      K dX, then dk += R dX^T + (-d diag(beta) dR) E^T and dq = dO X^T, all on
+//      tcgen05 with fp32 accumulators in TMEM, each fp32 operand split into
+//      bf16 hi + lo (products hi.hi + hi.lo + lo.hi, about 2^-16 relative);
+//      fb_token_kernel (every other shape, CUDA cores, 64-token tiles).
 //   4. fb_decay_kernel: each frame's ddecay, its tiles' shares summed in order.
+#include <cuda.h>
+#include <stdint.h>
+
 #include "gdn_internal.h"
 #include "simt_tile.cuh"
+#include "tc_util.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace tile;
 constexpr int kFChainThr = 256;
+constexpr uint32_t kImg = 65536;  // a 128 x 128 matrix as bf16 hi | lo operand images (2 x 32 KB)
 constexpr int kSl = 32;  // value columns per chain CTA
 constexpr int LSl = kSl + 1;
 
@@ -43,6 +54,10 @@ struct FbParams {
     // workspace: G [BH][F][Dk][Dk], H and P [BH][F][Dk][Dv], E [BH][F+1][Dk][Dv],
     // dX [BH][F][Dk][Dv], ddecay shares [BH][F][tiles per frame]
     float *Gw, *Hw, *Pw, *Ew, *dXw, *part;
+    // tensor-core path only (else null): E_f (f <= F) and dX_f as bf16 hi | lo
+    // images, [BH][F+1][kImg] and [BH][F][kImg]; each image holds the 128 x 128
+    // matrix row-major as two 64-column blocks of 128-byte swizzled rows
+    uint8_t *Eimg, *dXimg;
     int F, S, N, tiles;
     float scale;
     int l2;
@@ -107,6 +122,25 @@ __global__ void __launch_bounds__(kThr, 1) fb_frame_kernel(FbParams p) {
     }
 }
 
+// This CTA's 32 columns (col0 ..) of a 128 x 128 fp32 matrix St [128][LSl]
+// into its bf16 hi | lo operand images: element (m, c) at block c / 64, row m,
+// 16-byte chunk (c % 64) / 8 of the row swizzled by m % 8; lo = x - hi.
+__device__ __forceinline__ void write_image(uint8_t *img, const float *St, int col0) {
+    for (int e = threadIdx.x; e < 128 * (kSl / 8); e += kFChainThr) {
+        const int m = e / (kSl / 8), c8 = (e % (kSl / 8)) * 8, col = col0 + c8;
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = St[m * LSl + c8 + 2 * i], x1 = St[m * LSl + c8 + 2 * i + 1];
+            hi[i] = tc::pack_bf16(x0, x1);
+            lo[i] = tc::pack_bf16(x0 - __uint_as_float(hi[i] << 16), x1 - __uint_as_float(hi[i] & 0xffff0000u));
+        }
+        const uint32_t off = (uint32_t)(col >> 6) * 16384u + tc::sw128_offset((uint32_t)m, (uint32_t)(col & 63));
+        *reinterpret_cast<uint4 *>(img + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(img + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
 // ================================================================ 2. chains
 // blockIdx.x: 32-column slice; blockIdx.y: head; blockIdx.z: 0 = states,
 // 1 = gradients.
@@ -134,6 +168,7 @@ __global__ void __launch_bounds__(kFChainThr) fb_chain_kernel(FbParams p) {
                 const int m = e / kSl, n = e % kSl;
                 Eg[(size_t)m * DV + col0 + n] = St[m * LSl + n];
             }
+            if (p.Eimg) write_image(p.Eimg + ((size_t)bh * (F + 1) + f) * kImg, St, col0);
         } else {  // dX_f = dE_{f+1} + P_f, out
             const float *Pg = p.Pw + fi * DK * DV;
             float *dXg = p.dXw + fi * DK * DV;
@@ -142,6 +177,10 @@ __global__ void __launch_bounds__(kFChainThr) fb_chain_kernel(FbParams p) {
                 const float x = St[m * LSl + n] + Pg[(size_t)m * DV + col0 + n];
                 St[m * LSl + n] = x;
                 dXg[(size_t)m * DV + col0 + n] = x;
+            }
+            if (p.dXimg) {
+                __syncthreads();
+                write_image(p.dXimg + fi * kImg, St, col0);
             }
         }
         const float *Gg = p.Gw + fi * DK * DK;
@@ -168,6 +207,7 @@ __global__ void __launch_bounds__(kFChainThr) fb_chain_kernel(FbParams p) {
             const int m = e / kSl, n = e % kSl;
             Eg[(size_t)m * DV + col0 + n] = St[m * LSl + n];
         }
+        if (p.Eimg) write_image(p.Eimg + ((size_t)bh * (F + 1) + F) * kImg, St, col0);
     } else if (p.ds0) {
         for (int e = tid; e < DK * kSl; e += kFChainThr) {
             const int m = e / kSl, n = e % kSl;
@@ -320,6 +360,376 @@ __global__ void __launch_bounds__(kThr, 1) fb_token_kernel(FbParams p) {
     }
 }
 
+// ====================================== 3a. token gradients on the tensor cores
+// One CTA per (frame, 128-token tile, head), bf16, Dk = Dv = 128.  Warp 0
+// loads (TMA for the K and dO tiles, bulk copies for the operand images),
+// warp 1 issues the MMAs, warps 2..5 (one TMEM lane quarter each, thread =
+// token row) form r, -d beta dR, dv, dbeta and the outputs.  The products, all
+// M = N = 128 with fp32 accumulators in TMEM:
+//   KE = K E_f,  dR' = K dX_f                          (E, dX images MN-major)
+//   DK = R dX_f^T + W E_f^T,  W = -d diag(beta) dR     (by 64-column halves of Dv)
+//   DQ = dO X_f^T                                      (X_f = E_{f+1})
+// With the unit-norm flag the raw K tile is the operand and its rows' scale
+// 1/|k| is applied to KE and dR' in the epilogue (k-hat = k / |k|).
+constexpr int kTcThr = 192;
+constexpr int kTcRows = 128;
+constexpr uint32_t TB_A = 0;        // K tile, then dO tile: two 64-column blocks of 128 swizzled rows
+constexpr uint32_t TB_E = 32768;    // E_f image (hi | lo), then the X_f image
+constexpr uint32_t TB_DX = 98304;   // dX_f image (hi | lo)
+constexpr uint32_t TB_R = 163840;   // R, one 64-column half: hi (16 KB) | lo
+constexpr uint32_t TB_W = 196608;   // W = -d beta dR, one half: hi | lo
+constexpr uint32_t TB_BAR = 229376;
+enum { TBB_K = 0, TBB_E, TBB_DX, TBB_DO, TBB_X, TBB_MMA1, TBB_OPND, TBB_MMA2, TBB_MMA3, TBB_DRAIN, TBB_NUM };
+constexpr uint32_t TB_MISC = TB_BAR + 8 * TBB_NUM;  // TMEM address, then 8 reduction floats
+constexpr uint32_t TB_SMEM = TB_MISC + 48 + 1024;    // + alignment of the base to 1024 bytes
+static_assert(TB_SMEM <= 232448, "token kernel fits the shared memory of one CTA");
+constexpr uint32_t TM_KE = 0, TM_DR = 128, TM_DK = 256, TM_DQ = 384;
+
+__device__ unsigned int g_fb_error = 0;  // set when a bounded wait of the token kernel gives up
+constexpr unsigned long long kFbWaitNs = 1000000000ull;
+
+__device__ __forceinline__ bool fb_wait(uint64_t *bar, uint32_t parity, unsigned code) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::global_timer_ns();
+    while (true) {
+        if (tc::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*reinterpret_cast<volatile unsigned *>(&g_fb_error) != 0u) return false;
+        if (tc::global_timer_ns() - t0 > kFbWaitNs) {
+            atomicOr(&g_fb_error, code);
+            return false;
+        }
+    }
+}
+
+// A wait's outcome made uniform across the warp, so that the warp's
+// .sync.aligned TMEM loads that follow are reached by all of its lanes.
+__device__ __forceinline__ bool warp_all_ok(bool ok) { return __all_sync(0xffffffffu, ok) != 0; }
+
+__device__ __forceinline__ void split8(const float (&x)[8], uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = tc::pack_bf16(x[2 * i], x[2 * i + 1]);
+        l[i] = tc::pack_bf16(x[2 * i] - __uint_as_float(h[i] << 16), x[2 * i + 1] - __uint_as_float(h[i] & 0xffff0000u));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    return make_uint4(tc::pack_bf16(x[0], x[1]), tc::pack_bf16(x[2], x[3]), tc::pack_bf16(x[4], x[5]),
+                      tc::pack_bf16(x[6], x[7]));
+}
+
+// |row| of a 128-wide bf16 row in global memory
+__device__ __forceinline__ float row_norm128(const __nv_bfloat16 *row) {
+    float s = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4 *>(row + 8 * j), x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s += x[i] * x[i];
+    }
+    return sqrtf(s);
+}
+
+__global__ void __launch_bounds__(kTcThr, 1)
+    fb_token_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mDO, FbParams p) {
+    using namespace tc;
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + TB_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TB_MISC);
+    float *red = reinterpret_cast<float *>(sm + TB_MISC + 16);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int f = blockIdx.x / p.tiles, tl = blockIdx.x % p.tiles, bh = blockIdx.y;
+    const int t0 = tl * kTcRows, n = min(kTcRows, p.S - t0);
+    const size_t fi = (size_t)bh * p.F + f;
+    const size_t tok0 = (size_t)bh * p.N + (size_t)f * p.S + t0;
+    const float d = p.decay[fi];
+    const uint8_t *Ei = p.Eimg + ((size_t)bh * (p.F + 1) + f) * kImg;  // E_f; E_{f+1} = X_f follows
+    const uint8_t *dXi = p.dXimg + fi * kImg;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < TBB_NUM; ++i) mbar_init(&bars[i], i == TBB_OPND ? 128u : 1u);
+        fence_mbar_init();
+        prefetch_tensormap(&mK);
+        prefetch_tensormap(&mDO);
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[TBB_K], 32768);
+            tma_load_4d(sm + TB_A, &mK, &bars[TBB_K], 0, t0, f, bh);
+            tma_load_4d(sm + TB_A + 16384, &mK, &bars[TBB_K], 64, t0, f, bh);
+            mbar_arrive_expect_tx(&bars[TBB_E], kImg);
+            bulk_load_global(sm + TB_E, Ei, 32768, &bars[TBB_E]);
+            bulk_load_global(sm + TB_E + 32768, Ei + 32768, 32768, &bars[TBB_E]);
+            mbar_arrive_expect_tx(&bars[TBB_DX], kImg);
+            bulk_load_global(sm + TB_DX, dXi, 32768, &bars[TBB_DX]);
+            bulk_load_global(sm + TB_DX + 32768, dXi + 32768, 32768, &bars[TBB_DX]);
+            bool armed_do = false, armed_x = false;
+            // dO over K once the first products have read it
+            if (fb_wait(&bars[TBB_MMA1], 0, 1u)) {
+                mbar_arrive_expect_tx(&bars[TBB_DO], 32768);
+                tma_load_4d(sm + TB_A, &mDO, &bars[TBB_DO], 0, t0, f, bh);
+                tma_load_4d(sm + TB_A + 16384, &mDO, &bars[TBB_DO], 64, t0, f, bh);
+                armed_do = true;
+                // X_f over E_f once both halves of the dk products have read it
+                if (fb_wait(&bars[TBB_MMA2], 0, 1u) && fb_wait(&bars[TBB_MMA2], 1, 1u)) {
+                    mbar_arrive_expect_tx(&bars[TBB_X], kImg);
+                    bulk_load_global(sm + TB_E, Ei + kImg, 32768, &bars[TBB_X]);
+                    bulk_load_global(sm + TB_E + 32768, Ei + kImg + 32768, 32768, &bars[TBB_X]);
+                    armed_x = true;
+                }
+            }
+            // every copy issued has landed before the CTA may exit
+            fb_wait(&bars[TBB_K], 0, 1u);
+            fb_wait(&bars[TBB_E], 0, 1u);
+            fb_wait(&bars[TBB_DX], 0, 1u);
+            if (armed_do) fb_wait(&bars[TBB_DO], 0, 1u);
+            if (armed_x) fb_wait(&bars[TBB_X], 0, 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idMN = idesc_bf16(128, 128, false, true);  // B MN-major
+            const uint32_t idK = idesc_bf16(128, 128, false, false);  // both K-major
+            bool ok = fb_wait(&bars[TBB_K], 0, 2u) && fb_wait(&bars[TBB_E], 0, 2u);
+            if (ok) {
+                tc_fence_after_sync();
+                int nmm = 0;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem + TM_KE, smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    smem_desc(sb + TB_E + part * 32768 + ks * 2048, 16384, 1024), idMN,
+                                    (nmm++) > 0);
+            }
+            ok = ok && fb_wait(&bars[TBB_DX], 0, 2u);
+            if (ok) {
+                tc_fence_after_sync();
+                int nmm = 0;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem + TM_DR, smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    smem_desc(sb + TB_DX + part * 32768 + ks * 2048, 16384, 1024), idMN,
+                                    (nmm++) > 0);
+                mma_commit(&bars[TBB_MMA1]);
+            }
+            for (int h = 0; h < 2 && ok; ++h) {
+                ok = fb_wait(&bars[TBB_OPND], (uint32_t)h, 3u);
+                if (!ok) break;
+                tc_fence_after_sync();
+                // DK += R_h dX_h^T + W_h E_h^T, each as hi.hi + hi.lo + lo.hi
+#pragma unroll
+                for (int term = 0; term < 2; ++term) {
+                    const uint32_t abase = sb + (term ? TB_W : TB_R);
+                    const uint32_t bbase = sb + (term ? TB_E : TB_DX) + h * 16384;
+#pragma unroll
+                    for (int c = 0; c < 3; ++c) {
+                        const uint32_t a = abase + (c == 2 ? 16384 : 0);
+                        const uint32_t b = bbase + (c == 1 ? 32768 : 0);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ss(tmem + TM_DK, smem_desc(a + ks * 32, 16, 1024),
+                                        smem_desc(b + ks * 32, 16, 1024), idK, (h | term | c | ks) != 0);
+                    }
+                }
+                mma_commit(&bars[TBB_MMA2]);
+            }
+            ok = ok && fb_wait(&bars[TBB_DO], 0, 2u) && fb_wait(&bars[TBB_X], 0, 2u);
+            if (ok) {
+                tc_fence_after_sync();
+                int nmm = 0;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem + TM_DQ, smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    smem_desc(sb + TB_E + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    idK, (nmm++) > 0);
+                mma_commit(&bars[TBB_MMA3]);
+            }
+            // every MMA issued has completed before TMEM is released
+            mma_commit(&bars[TBB_DRAIN]);
+            fb_wait(&bars[TBB_DRAIN], 0, 2u);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int t = 32 * (warp & 3) + lane;  // token row = TMEM lane
+        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+        const bool valid = t < n;
+        const size_t tok = tok0 + t;
+        const __nv_bfloat16 *vrow = static_cast<const __nv_bfloat16 *>(p.v) + tok * 128;
+        const __nv_bfloat16 *krow = static_cast<const __nv_bfloat16 *>(p.k) + tok * 128;
+        const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) + tok * 128;
+        const float bt = valid ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[tok]) : 0.f;
+        float nk = 1.f, nq = 1.f;
+        if (p.l2 && valid) {
+            nk = row_norm128(krow);
+            nq = row_norm128(qrow);
+        }
+        const float sk = p.l2 ? 1.f / fmaxf(nk, 1e-12f) : 1.f;
+        float dbeta = 0.f, dec = 0.f;
+        bool ok = warp_all_ok(fb_wait(&bars[TBB_MMA1], 0, 4u));
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1) ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA2], 0, 4u));
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t ke[16], dr[16];
+                    tmem_ld16(tmem + lb + TM_KE + 64 * h + 16 * cc, ke);
+                    tmem_ld16(tmem + lb + TM_DR + 64 * h + 16 * cc, dr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int c8 = 16 * cc + 8 * j;  // column within the half
+                        float vv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        if (valid) unpack8(*reinterpret_cast<const uint4 *>(vrow + 64 * h + c8), vv);
+                        float rr[8], ww[8], dv8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float kt = __uint_as_float(ke[8 * j + e]) * sk;
+                            const float drt = __uint_as_float(dr[8 * j + e]) * sk;
+                            const float u = vv[e] - d * kt;
+                            rr[e] = bt * u;
+                            ww[e] = -d * bt * drt;
+                            dv8[e] = bt * drt;
+                            dbeta += drt * u;
+                            dec += bt * drt * kt;
+                        }
+                        if (valid)
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + tok * 128 + 64 * h + c8) =
+                                pack8(dv8);
+                        uint4 hi, lo;
+                        const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)c8);
+                        split8(rr, hi, lo);
+                        *reinterpret_cast<uint4 *>(sm + TB_R + off) = hi;
+                        *reinterpret_cast<uint4 *>(sm + TB_R + 16384 + off) = lo;
+                        split8(ww, hi, lo);
+                        *reinterpret_cast<uint4 *>(sm + TB_W + off) = hi;
+                        *reinterpret_cast<uint4 *>(sm + TB_W + 16384 + off) = lo;
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars[TBB_OPND]);
+        }
+        if (ok && valid) p.dbeta[tok] = dbeta;
+        // the tile's share of ddecay (and <dX_f, E_f> on the frame's first tile)
+        float dot = 0.f;
+        if (tl == 0) {
+            const float *Eg = p.Ew + ((size_t)bh * (p.F + 1) + f) * 16384, *dXg = p.dXw + fi * 16384;
+            for (int e = threadIdx.x - 64; e < 16384; e += 128) dot += dXg[e] * Eg[e];
+        }
+        dec = warp_sum(dec);
+        dot = warp_sum(dot);
+        if (lane == 0) {
+            red[warp - 2] = dec;
+            red[4 + warp - 2] = dot;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) {
+            float s = 0.f;
+            for (int w = 0; w < 4; ++w) s += red[4 + w] - red[w];
+            p.part[fi * p.tiles + tl] = s;
+        }
+        // dk and dq, through the unit-norm map when asked
+        ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA3], 0, 4u));
+        if (ok) {
+            tc_fence_after_sync();
+            float kd = 0.f, qd = 0.f;
+            if (p.l2) {
+#pragma unroll 1
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t gk[16], gq[16];
+                    tmem_ld16(tmem + lb + TM_DK + 16 * cc, gk);
+                    tmem_ld16(tmem + lb + TM_DQ + 16 * cc, gq);
+                    tmem_wait_ld();
+                    if (valid) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            float kx[8], qx[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(krow + 16 * cc + 8 * j), kx);
+                            unpack8(*reinterpret_cast<const uint4 *>(qrow + 16 * cc + 8 * j), qx);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                kd += kx[e] * __uint_as_float(gk[8 * j + e]);
+                                qd += qx[e] * __uint_as_float(gq[8 * j + e]);
+                            }
+                        }
+                    }
+                }
+                kd *= sk;                              // k-hat . dk
+                qd *= p.scale / fmaxf(nq, 1e-12f);     // q-hat . dq
+            }
+            const float sq = 1.f / fmaxf(nq, 1e-12f);
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t gk[16], gq[16];
+                tmem_ld16(tmem + lb + TM_DK + 16 * cc, gk);
+                tmem_ld16(tmem + lb + TM_DQ + 16 * cc, gq);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float kx[8], qx[8], ok8[8], oq8[8];
+                        if (p.l2) {
+                            unpack8(*reinterpret_cast<const uint4 *>(krow + 16 * cc + 8 * j), kx);
+                            unpack8(*reinterpret_cast<const uint4 *>(qrow + 16 * cc + 8 * j), qx);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float xk = __uint_as_float(gk[8 * j + e]);
+                            float xq = p.scale * __uint_as_float(gq[8 * j + e]);
+                            if (p.l2) {
+                                xk = nk < 1e-12f ? xk * 1e12f : (xk - kx[e] * sk * kd) / nk;
+                                xq = nq < 1e-12f ? xq * 1e12f : (xq - qx[e] * sq * qd) / nq;
+                            }
+                            ok8[e] = xk;
+                            oq8[e] = xq;
+                        }
+                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dk) + tok * 128 + 16 * cc + 8 * j) =
+                            pack8(ok8);
+                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dq) + tok * 128 + 16 * cc + 8 * j) =
+                            pack8(oq8);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ======================================================= 4. ddecay per frame
 __global__ void fb_decay_kernel(FbParams p) {
     const int bh = blockIdx.x;
@@ -339,10 +749,16 @@ constexpr size_t token_smem(int DK, int DV) {
     return sizeof(float) * ((size_t)2 * kC * (DK + 1) + 4 * kC * (DV + 1) + 5 * kC + 16);
 }
 
+// The shapes the tensor-core token kernel serves (bf16, Dk = Dv = 128); the
+// workspace holds its operand images for these whatever the flags.
+bool tc_shape(const CamScanBwdArgs &a) { return a.dtype == GDN_BF16 && a.Dk == 128 && a.Dv == 128; }
+
 size_t ws_floats(const CamScanBwdArgs &a) {
     const size_t BH = (size_t)a.B * a.H, F = (size_t)a.F, DK = (size_t)a.Dk, DV = (size_t)a.Dv;
     const size_t tiles = (size_t)(a.S + kC - 1) / kC;
-    return BH * F * DK * DK + 3 * BH * F * DK * DV + BH * (F + 1) * DK * DV + BH * F * tiles;
+    const size_t imgs = tc_shape(a) ? BH * (2 * F + 1) * (kImg / sizeof(float)) : 0;
+    const size_t shares = (BH * F * tiles + 63) / 64 * 64;  // keeps the images 256-byte aligned
+    return BH * F * DK * DK + 3 * BH * F * DK * DV + BH * (F + 1) * DK * DV + shares + imgs;
 }
 
 template <typename T, int DK, int DV>
@@ -371,6 +787,16 @@ int run(const CamScanBwdArgs &a, cudaStream_t st) {
     p.dXw = p.Pw + nf * DK * DV;
     p.Ew = p.dXw + nf * DK * DV;
     p.part = p.Ew + (size_t)BH * (a.F + 1) * DK * DV;
+    // the tensor-core token kernel: its operand images after the shares
+    CUtensorMap mK, mDO;
+    const bool tc = tc_shape(a) && !(a.flags & GDN_PATH_SIMT) && sm100_family() &&
+                    make_bf16_frame_map(&mK, a.k, BH, a.F, a.S, 64, 128) &&
+                    make_bf16_frame_map(&mDO, a.dout, BH, a.F, a.S, 64, 128);
+    if (tc) {
+        uint8_t *img = reinterpret_cast<uint8_t *>(p.part + (nf * tiles + 63) / 64 * 64);
+        p.Eimg = img;
+        p.dXimg = img + (size_t)BH * (a.F + 1) * kImg;
+    }
     p.F = a.F;
     p.S = a.S;
     p.N = a.F * a.S;
@@ -389,7 +815,15 @@ int run(const CamScanBwdArgs &a, cudaStream_t st) {
     note_launch();
     fb_chain_kernel<DK, DV><<<dim3((unsigned)(DV / kSl), (unsigned)BH, 2), kFChainThr, s2, st>>>(p);
     note_launch();
-    fb_token_kernel<T, DK, DV><<<dim3((unsigned)(a.F * tiles), (unsigned)BH), kThr, s3, st>>>(p);
+    if (tc) {
+        p.tiles = (a.S + kTcRows - 1) / kTcRows;
+        if (cudaFuncSetAttribute(fb_token_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TB_SMEM) !=
+            cudaSuccess)
+            return GDN_ERR_CUDA;
+        fb_token_tc_kernel<<<dim3((unsigned)(a.F * p.tiles), (unsigned)BH), kTcThr, TB_SMEM, st>>>(mK, mDO, p);
+    } else {
+        fb_token_kernel<T, DK, DV><<<dim3((unsigned)(a.F * tiles), (unsigned)BH), kThr, s3, st>>>(p);
+    }
     note_launch();
     fb_decay_kernel<<<(unsigned)BH, 32, 0, st>>>(p);
     note_launch();
@@ -411,6 +845,13 @@ size_t cam_scan_bwd_workspace_bytes(const CamScanBwdArgs &a) { return sizeof(flo
 
 int launch_cam_scan_bwd(const CamScanBwdArgs &a, cudaStream_t stream) {
     return a.dtype == GDN_BF16 ? run_t<__nv_bfloat16>(a, stream) : run_t<float>(a, stream);
+}
+
+int cam_scan_bwd_read_clear_error() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fb_error, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_fb_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
+    return v ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 }  // namespace gdn

@@ -31,8 +31,9 @@
 //   1. bwd_wy_kernel (one CTA per chunk): T, W, U, Kd, gamma and B to the workspace.
 //   2. bwd_chain_kernel: the forward state chain (S entering each chunk, and
 //      Vn) and the reverse gradient chain (dS' of each chunk, and the initial
-//      state's gradient) run side by side; each CTA holds 32 value columns of
-//      one head's state, since the columns of both chains are independent.
+//      state's gradient) run side by side; each CTA holds 64 value columns of
+//      one head's state, since the columns of both chains are independent
+//      (64 heads of 128 columns make 256 CTAs, one wave at two per SM).
 //   3. bwd_grad_kernel (one CTA per chunk): every input gradient.
 #include <cuda_bf16.h>
 
@@ -46,7 +47,7 @@ namespace {
 using namespace tile;
 constexpr int LC = kC + 1;      // leading dimension of the 64 x 64 tiles
 constexpr int kChainThr = 256;  // threads of a chain CTA
-constexpr int kSlice = 32;      // value columns per chain CTA
+constexpr int kSlice = 64;      // value columns per chain CTA
 constexpr int LS = kSlice + 1;
 
 struct BwdParams {
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
 }
 
 // ============================================================== 2. the chains
-// blockIdx.x: 32-column slice of the value dimension; blockIdx.y: head;
+// blockIdx.x: 64-column slice of the value dimension; blockIdx.y: head;
 // blockIdx.z: 0 = forward state chain, 1 = reverse gradient chain.
 template <int DK, int DV>
 __global__ void __launch_bounds__(kChainThr) bwd_chain_kernel(BwdParams p) {
@@ -266,14 +267,14 @@ __global__ void __launch_bounds__(kChainThr) bwd_chain_kernel(BwdParams p) {
         __syncthreads();
         // role 0: Vn = U - W S;  role 1: Y = Kd dS'
         {
-            float acc[4][2];
+            float acc[4][kSlice / 16];
             zero(acc);
-            mm<kChainThr, 4, 2>(acc, Wt, LK, 1, St, LS, 1, DK);
+            mm<kChainThr, 4, kSlice / 16>(acc, Wt, LK, 1, St, LS, 1, DK);
             float *Vng = p.Vnw + ci * kC * DV;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < kSlice / 16; ++j) {
                     const int m = ty + 16 * i, n = tx + 16 * j;
                     if (role == 0) {
                         const float vn = Ut[m * LS + n] - acc[i][j];
@@ -289,14 +290,14 @@ __global__ void __launch_bounds__(kChainThr) bwd_chain_kernel(BwdParams p) {
         __syncthreads();
         // role 0: S = e^{gl} S + Kd^T Vn;  role 1: dS = e^{gl} dS' - W^T Y + B
         {
-            float acc[DK / 16][2];
+            float acc[DK / 16][kSlice / 16];
             zero(acc);
-            mm<kChainThr, DK / 16, 2>(acc, Wt, 1, LK, Ut, LS, 1, kC);
+            mm<kChainThr, DK / 16, kSlice / 16>(acc, Wt, 1, LK, Ut, LS, 1, kC);
             const float *Bg = p.Bw + ci * DK * DV;
 #pragma unroll
             for (int i = 0; i < DK / 16; ++i)
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < kSlice / 16; ++j) {
                     const int m = ty + 16 * i, n = tx + 16 * j;
                     const float old = St[m * LS + n];
                     St[m * LS + n] = role == 0 ? el * old + acc[i][j]

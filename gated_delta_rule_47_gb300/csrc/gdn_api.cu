@@ -300,7 +300,7 @@ size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, 
     if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return (size_t)-1;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
     gdn::CamScanBwdArgs a{};
-    a.B = B; a.H = H; a.F = F; a.S = S; a.Dk = Dk; a.Dv = Dv;
+    a.B = B; a.H = H; a.F = F; a.S = S; a.Dk = Dk; a.Dv = Dv; a.dtype = dtype;
     return gdn::cam_scan_bwd_workspace_bytes(a);
 }
 
@@ -311,7 +311,7 @@ int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, 
                  void *stream) {
     if (B < 0 || H < 0 || F < 0 || S < 0 || (F > 0 && S == 0)) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-    if (flags & ~(GDN_QK_L2NORM | GDN_CAM_REVERSE)) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_CAM_REVERSE | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
     if (flags & GDN_CAM_REVERSE) return GDN_ERR_UNSUPPORTED;  // forward direction only
     if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
     if ((long long)B * H > 65535 || (long long)F * S >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
@@ -428,7 +428,8 @@ int gdn_get_device_error(void *stream) {
     const int a = gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
     const int b = gdn::cam_prep_read_clear_error();
     const int c = gdn::cam_scan_read_clear_error();
-    return a != GDN_OK ? a : (b != GDN_OK ? b : c);
+    const int d = gdn::cam_scan_bwd_read_clear_error();
+    return a != GDN_OK ? a : (b != GDN_OK ? b : (c != GDN_OK ? c : d));
 }
 
 unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }

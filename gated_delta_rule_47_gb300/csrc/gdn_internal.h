@@ -125,6 +125,8 @@ struct CamScanBwdArgs {
 };
 size_t cam_scan_bwd_workspace_bytes(const CamScanBwdArgs &a);
 int launch_cam_scan_bwd(const CamScanBwdArgs &a, cudaStream_t stream);
+// Reads and clears the error word of the frame scan's backward (GDN_OK or GDN_ERR_TIMEOUT).
+int cam_scan_bwd_read_clear_error();
 int launch_cam_fused(const CamFusedArgs &a, cudaStream_t stream);
 
 // 3-D TMA map (128-byte swizzle) over a [heads][rows][128] bf16 tensor with a

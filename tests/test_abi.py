@@ -210,7 +210,10 @@ def test_cam_scan_bwd_argument_checks(lib):
     assert call(ws=None) == 4
     # G, H, P and dX per frame, the states entering each frame and the last, one share per tile
     assert lib.cam_scan_bwd_workspace_bytes(1, 2, 3, 5, 64, 64, binding.GDN_F32) == 4 * (
-        2 * 3 * 4 * 64 * 64 + 2 * 4 * 64 * 64 + 2 * 3 * 1)
+        2 * 3 * 4 * 64 * 64 + 2 * 4 * 64 * 64 + 64)
+    # bf16 at D = 128 adds the bf16 hi / lo images of the states (F + 1) and gradients (F), 64 KB each
+    assert lib.cam_scan_bwd_workspace_bytes(1, 2, 3, 5, 128, 128, binding.GDN_BF16) == 4 * (
+        2 * 3 * 4 * 128 * 128 + 2 * 4 * 128 * 128 + 64) + 2 * 7 * 65536
 
 
 def test_chunk_bwd_argument_checks(lib):

@@ -21,7 +21,8 @@ def _lib():
 
 @pytest.mark.parametrize("l2norm", [False, True])
 @pytest.mark.parametrize("dtype,tol", [("f32", TOL_F32), ("bf16", TOL_BF16)])
-@pytest.mark.parametrize("F,S,Dk,Dv", [(4, 37, 128, 128), (3, 16, 64, 64), (5, 7, 64, 128), (2, 70, 128, 64)])
+@pytest.mark.parametrize("F,S,Dk,Dv", [(4, 37, 128, 128), (3, 16, 64, 64), (5, 7, 64, 128), (2, 70, 128, 64),
+                                        (3, 300, 128, 128), (2, 129, 128, 128)])
 def test_frame_scan_backward(F, S, Dk, Dv, dtype, tol, l2norm):
     inp = cam_scan_inputs(1, 2, F, S, Dk, Dv, seed=F * S + Dk, dtype=dtype, initial_state=True,
                           normalise_qk=not l2norm)
@@ -38,6 +39,26 @@ def test_frame_scan_backward(F, S, Dk, Dv, dtype, tol, l2norm):
                               scale=0.9, l2norm=l2norm)
     for name, x, y in zip(("dq", "dk", "dv", "dbeta", "ddecay", "ds0"), got, ref):
         assert rel_err(x, y) <= tol, name
+
+
+@pytest.mark.parametrize("l2norm", [False, True])
+def test_tensor_core_and_cuda_core_token_gradients_agree(l2norm):
+    """The tensor-core token kernel (bf16, D 128, 128-token tiles, bf16 hi/lo
+    operands) and the CUDA-core one (fp32, 64-token tiles) on the same inputs,
+    across ragged tiles: both within the bf16 bound of each other."""
+    inp = cam_scan_inputs(1, 3, 3, 200, 128, 128, seed=12, dtype="bf16", initial_state=True,
+                          normalise_qk=not l2norm)
+    g = torch.Generator().manual_seed(9)
+    do = torch.randn(1, 3, 600, 128, generator=g).to(torch.bfloat16).cuda()
+    dsf = torch.randn(1, 3, 128, 128, generator=g).cuda()
+    d = to_dev(inp)
+    args = (d["q"], d["k"], d["v"], d["beta"], d["decay"], do, d["initial_state"], dsf)
+    a = binding.cam_scan_bwd(*args, l2norm=l2norm, need_dinitial=True)
+    b = binding.cam_scan_bwd(*args, l2norm=l2norm, need_dinitial=True, simt=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    for name, x, y in zip(("dq", "dk", "dv", "dbeta", "ddecay", "ds0"), a, b):
+        assert rel_err(x, y.double().cpu().numpy()) <= TOL_BF16, name
 
 
 def test_camera_workload_shape_sampled_heads():
