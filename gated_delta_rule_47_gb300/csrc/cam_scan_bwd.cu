@@ -730,6 +730,169 @@ __global__ void __launch_bounds__(kTcThr, 1)
     }
 }
 
+// ======================================== 1a. frame products on the tensor cores
+// One CTA per (frame, head, product), bf16, Dk = Dv = 128: the frame's tokens
+// stream through TMA in 128-token tiles (the last clipped at the frame's end
+// and zero-filled); four builder warps (thread = token row) scale the A-side
+// tile's rows and split them into bf16 hi + lo; the MMAs accumulate
+// D = sum_t a_t b_t^T in TMEM with M = N = 128 and K = the tile's tokens,
+// both operands MN-major (the tiles as loaded):
+//   G: a_t = beta_t n_t^2 k_t,  b_t = k_t      (n_t = 1 / |k_t| with the
+//   H: a_t = beta_t n_t k_t,    b_t = v_t       unit-norm flag, else 1)
+//   P: a_t = m_t q_t,           b_t = do_t     (m_t = 1 / |q_t| or 1; times scale)
+constexpr int kFrThr = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 builders then epilogue
+constexpr uint32_t FR_STAGE = 65536;   // A-side tile | B-side tile (32 KB each)
+constexpr uint32_t FR_A = 2 * FR_STAGE;  // A hi (32 KB) | lo
+constexpr uint32_t FR_BAR = FR_A + 65536;
+enum { FRB_FULL = 0, FRB_EMPTY = 2, FRB_AREADY = 4, FRB_AFREE = 5, FRB_DONE = 6, FRB_NUM = 7 };
+constexpr uint32_t FR_MISC = FR_BAR + 8 * FRB_NUM;
+constexpr uint32_t FR_SMEM = FR_MISC + 16 + 1024;
+static_assert(FR_SMEM <= 232448, "frame-product kernel fits the shared memory of one CTA");
+
+__global__ void __launch_bounds__(kFrThr, 1)
+    fb_frame_tc_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                       const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mDO, FbParams p) {
+    using namespace tc;
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + FR_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + FR_MISC);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int f = blockIdx.x, bh = blockIdx.y, part = blockIdx.z;  // 0 = G, 1 = H, 2 = P
+    const int nt = (p.S + 127) / 128;
+    const size_t fi = (size_t)bh * p.F + f;
+    const CUtensorMap *ma = part == 2 ? &mQ : &mK;
+    const CUtensorMap *mb = part == 0 ? &mK : (part == 1 ? &mV : &mDO);
+    const bool same = part == 0;  // G: the A side and the B side are the same tile
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < FRB_NUM; ++i) mbar_init(&bars[i], i == FRB_AREADY ? 128u : 1u);
+        fence_mbar_init();
+        prefetch_tensormap(ma);
+        prefetch_tensormap(mb);
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int armed[2] = {0, 0};
+            for (int i = 0; i < nt; ++i) {
+                const int s = i & 1;
+                if (i >= 2 && !fb_wait(&bars[FRB_EMPTY + s], ((i - 2) >> 1) & 1, 16u)) break;
+                uint8_t *st = sm + s * FR_STAGE;
+                mbar_arrive_expect_tx(&bars[FRB_FULL + s], same ? 32768 : 65536);
+                tma_load_4d(st, ma, &bars[FRB_FULL + s], 0, 128 * i, f, bh);
+                tma_load_4d(st + 16384, ma, &bars[FRB_FULL + s], 64, 128 * i, f, bh);
+                if (!same) {
+                    tma_load_4d(st + 32768, mb, &bars[FRB_FULL + s], 0, 128 * i, f, bh);
+                    tma_load_4d(st + 49152, mb, &bars[FRB_FULL + s], 64, 128 * i, f, bh);
+                }
+                armed[s]++;
+            }
+            for (int s = 0; s < 2; ++s)
+                if (armed[s]) fb_wait(&bars[FRB_FULL + s], (armed[s] - 1) & 1, 16u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id = idesc_bf16(128, 128, true, true);
+            bool ok = true;
+            for (int i = 0; i < nt && ok; ++i) {
+                const int s = i & 1;
+                ok = fb_wait(&bars[FRB_AREADY], i & 1, 17u);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t bt = sb + s * FR_STAGE + (same ? 0 : 32768);
+#pragma unroll
+                for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem, smem_desc(sb + FR_A + hl * 32768 + ks * 2048, 16384, 1024),
+                                    smem_desc(bt + ks * 2048, 16384, 1024), id, (i | hl | ks) != 0);
+                mma_commit(&bars[FRB_EMPTY + s]);
+                mma_commit(&bars[FRB_AFREE]);
+            }
+            mma_commit(&bars[FRB_DONE]);
+            fb_wait(&bars[FRB_DONE], 0, 17u);
+        }
+    } else {
+        // ------------------------------------- builders (thread = token row)
+        const int r = 32 * (warp & 3) + lane;
+        const size_t tok_f = (size_t)bh * p.N + (size_t)f * p.S;
+        bool ok = true;
+        for (int i = 0; i < nt; ++i) {
+            const int s = i & 1, t = 128 * i + r;
+            const bool valid = t < p.S;
+            float fac = 0.f;
+            if (valid) fac = part == 2 ? 1.f : __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[tok_f + t]);
+            ok = ok && warp_all_ok(fb_wait(&bars[FRB_FULL + s], (i >> 1) & 1, 18u));
+            if (i >= 1) ok = ok && warp_all_ok(fb_wait(&bars[FRB_AFREE], (i - 1) & 1, 18u));
+            if (ok) {
+                const uint8_t *src = sm + s * FR_STAGE;
+                if (p.l2) {
+                    float ss = 0.f;
+#pragma unroll 4
+                    for (int c = 0; c < 16; ++c) {
+                        float x[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(src + (c >> 3) * 16384 + sw128_offset(r, 8 * (c & 7))), x);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+                    }
+                    const float nrm = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+                    fac *= part == 0 ? nrm * nrm : nrm;
+                }
+#pragma unroll 4
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t off = (c >> 3) * 16384 + sw128_offset(r, 8 * (c & 7));
+                    float x[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(src + off), x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] *= fac;
+                    uint4 hi, lo;
+                    split8(x, hi, lo);
+                    *reinterpret_cast<uint4 *>(sm + FR_A + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + FR_A + 32768 + off) = lo;
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars[FRB_AREADY]);
+        }
+        // ---------------------------------------- epilogue (thread = row of D)
+        ok = ok && warp_all_ok(fb_wait(&bars[FRB_DONE], 0, 18u));
+        if (ok) {
+            tc_fence_after_sync();
+            const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+            const float sc = part == 2 ? p.scale : 1.f;
+            float *out = (part == 0 ? p.Gw : (part == 1 ? p.Hw : p.Pw)) + fi * 16384 + (size_t)r * 128;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t x[16];
+                tmem_ld16(tmem + lb + 16 * cc, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<float4 *>(out + 16 * cc + 4 * j) =
+                        make_float4(sc * __uint_as_float(x[4 * j]), sc * __uint_as_float(x[4 * j + 1]),
+                                    sc * __uint_as_float(x[4 * j + 2]), sc * __uint_as_float(x[4 * j + 3]));
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
 // ======================================================= 4. ddecay per frame
 __global__ void fb_decay_kernel(FbParams p) {
     const int bh = blockIdx.x;
@@ -811,7 +974,16 @@ int run(const CamScanBwdArgs &a, cudaStream_t st) {
         cudaFuncSetAttribute(fb_token_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3) !=
             cudaSuccess)
         return GDN_ERR_CUDA;
-    fb_frame_kernel<T, DK, DV><<<dim3((unsigned)a.F, (unsigned)BH, 3), kThr, s1, st>>>(p);
+    CUtensorMap mV, mQ;
+    if (tc && make_bf16_frame_map(&mV, a.v, BH, a.F, a.S, 64, 128) &&
+        make_bf16_frame_map(&mQ, a.q, BH, a.F, a.S, 64, 128)) {
+        if (cudaFuncSetAttribute(fb_frame_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FR_SMEM) !=
+            cudaSuccess)
+            return GDN_ERR_CUDA;
+        fb_frame_tc_kernel<<<dim3((unsigned)a.F, (unsigned)BH, 3), kFrThr, FR_SMEM, st>>>(mK, mV, mQ, mDO, p);
+    } else {
+        fb_frame_kernel<T, DK, DV><<<dim3((unsigned)a.F, (unsigned)BH, 3), kThr, s1, st>>>(p);
+    }
     note_launch();
     fb_chain_kernel<DK, DV><<<dim3((unsigned)(DV / kSl), (unsigned)BH, 2), kFChainThr, s2, st>>>(p);
     note_launch();
