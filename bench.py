@@ -449,12 +449,15 @@ def secondary(args, dev):
     w = WORKLOADS["masked_dp_r2_b4h16t4096d128_bf16"]
     d = {k: v.to(dev) for k, v in w.make().items()}
     o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
+    wsm = torch.empty(binding.masked_deltaproduct_workspace_bytes(w.B, w.H, w.T, w.r, w.D, w.D), dtype=torch.uint8,
+                      device=dev)
     ms = timeit(lambda: binding.masked_deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"],
-                                                              chunk=w.chunk, o=o))
+                                                              chunk=w.chunk, o=o, workspace=wsm))
     nbytes = w.B * w.H * w.T * gdn_bytes_per_token_head(w.D)
     out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
-                   "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "path": "CUDA cores, fp32"}
-    del d, o
+                   "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "path": "CUDA cores, fp32",
+                   "launches_per_call": 3}
+    del d, o, wsm
     torch.cuda.empty_cache()
     # the chunkwise GDN backward on the headline's shape (CUDA cores, fp32 arithmetic)
     w = WORKLOADS["gdn_b4h16t4096d128_bf16"]

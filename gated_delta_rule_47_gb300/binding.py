@@ -27,7 +27,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "G
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", "gdn_chunk_fwd",
            "deltaproduct_chunk_fwd", "cam_prep_fwd", "gdn_get_device_error", "gdn_set_wait_limit", "gdn_launch_count",
            "gdn_set_cluster_shape", "gdn_chunk_fwd_noalloc", "cam_scan_fwd_workspace_bytes", "cam_scan_fwd",
-           "masked_deltaproduct_chunk_fwd", "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd",
+           "masked_deltaproduct_chunk_fwd", "masked_deltaproduct_chunk_fwd_workspace_bytes",
+           "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd",
            "cam_prep_bwd", "cam_scan_bwd_workspace_bytes", "cam_scan_bwd", "gdn_chunk_bwd_workspace_bytes",
            "gdn_chunk_bwd", "deltaproduct_chunk_bwd")
 
@@ -65,7 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdn_chunk_fwd_noalloc.restype = i
         lib.deltaproduct_chunk_fwd.argtypes = [vp] * 8 + [i] * 7 + [f, u, i, vp, sz, vp]
         lib.deltaproduct_chunk_fwd.restype = i
-        lib.masked_deltaproduct_chunk_fwd.argtypes = [vp] * 9 + [i] * 7 + [f, u, i, vp]
+        lib.masked_deltaproduct_chunk_fwd.argtypes = [vp] * 9 + [i] * 7 + [f, u, i, vp, sz, vp]
+        lib.masked_deltaproduct_chunk_fwd_workspace_bytes.argtypes = [i] * 7
+        lib.masked_deltaproduct_chunk_fwd_workspace_bytes.restype = sz
         lib.masked_deltaproduct_chunk_fwd.restype = i
         lib.cam_prep_scan_fwd_workspace_bytes.argtypes = [i] * 6
         lib.cam_prep_scan_fwd_workspace_bytes.restype = sz
@@ -224,8 +227,13 @@ def deltaproduct_chunk_fwd(q, k, v, beta, g, initial_state=None, output_final_st
                  chunk, scale, l2norm, o, workspace, stream, simt)
 
 
+def masked_deltaproduct_workspace_bytes(B, H, T, r, Dk, Dv, dtype=torch.bfloat16):
+    code = GDN_BF16 if dtype == torch.bfloat16 else GDN_F32
+    return int(load().masked_deltaproduct_chunk_fwd_workspace_bytes(B, H, T, r, Dk, Dv, code))
+
+
 def masked_deltaproduct_chunk_fwd(q, k, v, beta, g, mask, initial_state=None, output_final_state=False,
-                                  chunk=64, scale=1.0, l2norm=False, o=None, stream=None):
+                                  chunk=64, scale=1.0, l2norm=False, o=None, workspace=None, stream=None):
     """Block-masked DeltaProduct forward.  q, k [B,H,T,Dk]; v [B,H,T,Dv]; beta
     [B,H,T] (all bf16 or all fp32); g [B,H,T] fp32; mask [r,r] fp32 (CUDA).
     chunk counts sub-rows (tokens x r)."""
@@ -246,9 +254,15 @@ def masked_deltaproduct_chunk_fwd(q, k, v, beta, g, mask, initial_state=None, ou
         o = torch.empty(B, H, T, Dv, dtype=dt, device=q.device)
     _check(o, "o", (B, H, T, Dv), dt)
     sf = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=q.device) if output_final_state else None
-    st = load().masked_deltaproduct_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
-                                              _ptr(initial_state), _ptr(o), _ptr(sf), B, H, T, r, Dk, Dv, chunk,
-                                              float(scale), GDN_QK_L2NORM if l2norm else 0, code, _stream(stream))
+    lib = load()
+    if workspace is None:
+        need = lib.masked_deltaproduct_chunk_fwd_workspace_bytes(B, H, T, r, Dk, Dv, code)
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.masked_deltaproduct_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
+                                           _ptr(initial_state), _ptr(o), _ptr(sf), B, H, T, r, Dk, Dv, chunk,
+                                           float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace),
+                                           ws_bytes, _stream(stream))
     _raise("masked_deltaproduct_chunk_fwd", st)
     return o, sf
 

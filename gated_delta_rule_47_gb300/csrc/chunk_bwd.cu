@@ -29,7 +29,7 @@
 //
 // Three launches:
 //   1. bwd_wy_kernel (one CTA per chunk): T, W, U, Kd, gamma and B to the workspace.
-//   2. bwd_chain_kernel: the forward state chain (S entering each chunk, and
+//   2. wy_chain_kernel: the forward state chain (S entering each chunk, and
 //      Vn) and the reverse gradient chain (dS' of each chunk, and the initial
 //      state's gradient) run side by side; each CTA holds 64 value columns of
 //      one head's state, since the columns of both chains are independent
@@ -40,15 +40,14 @@
 #include "gdn_internal.h"
 #include "simt_tile.cuh"
 #include "tri_inverse.cuh"
+#include "wy_chain.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace tile;
 constexpr int LC = kC + 1;      // leading dimension of the 64 x 64 tiles
-constexpr int kChainThr = 256;  // threads of a chain CTA
 constexpr int kSlice = 64;      // value columns per chain CTA
-constexpr int LS = kSlice + 1;
 
 struct BwdParams {
     const void *q, *k, *v, *beta, *dout;
@@ -222,95 +221,6 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
         for (int i = 0; i < DK / 32; ++i)
 #pragma unroll
             for (int j = 0; j < DV / 16; ++j) Bg[(ty + 32 * i) * DV + tx + 16 * j] = acc[i][j];
-    }
-}
-
-// ============================================================== 2. the chains
-// blockIdx.x: 64-column slice of the value dimension; blockIdx.y: head;
-// blockIdx.z: 0 = forward state chain, 1 = reverse gradient chain.
-template <int DK, int DV>
-__global__ void __launch_bounds__(kChainThr) bwd_chain_kernel(BwdParams p) {
-    extern __shared__ float sm[];
-    constexpr int LK = DK + 1;
-    float *St = sm;             // [DK][LS]  state (or gradient) slice
-    float *Wt = St + DK * LS;   // [kC][LK]  W or Kd of the chunk
-    float *Ut = Wt + kC * LK;   // [kC][LS]  U / Vn or Kd dS'
-    const int col0 = blockIdx.x * kSlice, bh = blockIdx.y, role = blockIdx.z;
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int NT = p.NT;
-
-    const float *init = role == 0 ? p.s0 : p.dsf;
-    for (int e = tid; e < DK * kSlice; e += kChainThr) {
-        const int m = e / kSlice, n = e % kSlice;
-        St[m * LS + n] = init ? init[((size_t)bh * DK + m) * DV + col0 + n] : 0.f;
-    }
-    __syncthreads();
-    for (int s = 0; s < NT; ++s) {
-        const int c = role == 0 ? s : NT - 1 - s;
-        const size_t ci = (size_t)bh * NT + c;
-        const float el = expf(p.Gw[ci * kC + kC - 1]);
-        float *snap = (role == 0 ? p.Sw : p.dSw) + ci * DK * DV;
-        for (int e = tid; e < DK * kSlice; e += kChainThr) {
-            const int m = e / kSlice, n = e % kSlice;
-            snap[(size_t)m * DV + col0 + n] = St[m * LS + n];
-        }
-        const float *Wg = p.Ww + ci * kC * DK, *Kdg = p.Kdw + ci * kC * DK;
-        const float *first = role == 0 ? Wg : Kdg, *second = role == 0 ? Kdg : Wg;
-        for (int e = tid; e < kC * DK; e += kChainThr) Wt[(e / DK) * LK + e % DK] = first[e];
-        if (role == 0) {
-            const float *Ug = p.Uw + ci * kC * DV;
-            for (int e = tid; e < kC * kSlice; e += kChainThr) {
-                const int m = e / kSlice, n = e % kSlice;
-                Ut[m * LS + n] = Ug[(size_t)m * DV + col0 + n];
-            }
-        }
-        __syncthreads();
-        // role 0: Vn = U - W S;  role 1: Y = Kd dS'
-        {
-            float acc[4][kSlice / 16];
-            zero(acc);
-            mm<kChainThr, 4, kSlice / 16>(acc, Wt, LK, 1, St, LS, 1, DK);
-            float *Vng = p.Vnw + ci * kC * DV;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < kSlice / 16; ++j) {
-                    const int m = ty + 16 * i, n = tx + 16 * j;
-                    if (role == 0) {
-                        const float vn = Ut[m * LS + n] - acc[i][j];
-                        Vng[(size_t)m * DV + col0 + n] = vn;
-                        Ut[m * LS + n] = vn;
-                    } else {
-                        Ut[m * LS + n] = acc[i][j];
-                    }
-                }
-        }
-        __syncthreads();
-        for (int e = tid; e < kC * DK; e += kChainThr) Wt[(e / DK) * LK + e % DK] = second[e];
-        __syncthreads();
-        // role 0: S = e^{gl} S + Kd^T Vn;  role 1: dS = e^{gl} dS' - W^T Y + B
-        {
-            float acc[DK / 16][kSlice / 16];
-            zero(acc);
-            mm<kChainThr, DK / 16, kSlice / 16>(acc, Wt, 1, LK, Ut, LS, 1, kC);
-            const float *Bg = p.Bw + ci * DK * DV;
-#pragma unroll
-            for (int i = 0; i < DK / 16; ++i)
-#pragma unroll
-                for (int j = 0; j < kSlice / 16; ++j) {
-                    const int m = ty + 16 * i, n = tx + 16 * j;
-                    const float old = St[m * LS + n];
-                    St[m * LS + n] = role == 0 ? el * old + acc[i][j]
-                                               : el * old - acc[i][j] + Bg[(size_t)m * DV + col0 + n];
-                }
-        }
-        __syncthreads();
-    }
-    if (role == 1 && p.ds0) {
-        for (int e = tid; e < DK * kSlice; e += kChainThr) {
-            const int m = e / kSlice, n = e % kSlice;
-            p.ds0[((size_t)bh * DK + m) * DV + col0 + n] = St[m * LS + n];
-        }
     }
 }
 
@@ -627,7 +537,6 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
 constexpr size_t wy_smem(int DK, int DV) {
     return sizeof(float) * ((size_t)3 * kC * (DK + 1) + 2 * kC * (DV + 1) + 2 * kC * LC + kC * kC / 4 + 4 * kC);
 }
-constexpr size_t chain_smem(int DK) { return sizeof(float) * ((size_t)DK * LS + kC * (DK + 1) + kC * LS); }
 constexpr size_t grad_smem(int DK, int DV) {
     return sizeof(float) * ((size_t)2 * kC * (DK + 1) + 3 * kC * (DV + 1) + 2 * kC * LC + 9 * kC + 32 * kC + 16);
 }
@@ -673,17 +582,18 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
     p.scale = a.scale;
     p.l2 = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
 
-    constexpr size_t s1 = wy_smem(DK, DV), s2 = chain_smem(DK), s3 = grad_smem(DK, DV);
+    constexpr size_t s1 = wy_smem(DK, DV), s2 = wy_chain_smem<DK, kSlice>(), s3 = grad_smem(DK, DV);
     if (cudaFuncSetAttribute(bwd_wy_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(bwd_chain_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2) !=
+        cudaFuncSetAttribute(wy_chain_kernel<DK, DV, kSlice>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2) !=
             cudaSuccess ||
         cudaFuncSetAttribute(bwd_grad_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3) !=
             cudaSuccess)
         return GDN_ERR_CUDA;
     bwd_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
     note_launch();
-    bwd_chain_kernel<DK, DV><<<dim3((unsigned)(DV / kSlice), (unsigned)BH, 2), kChainThr, s2, st>>>(p);
+    WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};
+    wy_chain_kernel<DK, DV, kSlice><<<dim3((unsigned)(DV / kSlice), (unsigned)BH, 2), kChainThr, s2, st>>>(cp);
     note_launch();
     bwd_grad_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s3, st>>>(p);
     note_launch();

@@ -161,10 +161,20 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
     return run_scan(a, stream);
 }
 
+size_t masked_deltaproduct_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype) {
+    if (B < 0 || H < 0 || T < 0 || r < 1 || r > 8 || 64 % r != 0) return (size_t)-1;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128) || Dk % r != 0) return (size_t)-1;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
+    gdn::MaskedDpArgs a{};
+    a.B = B; a.H = H; a.T = T; a.r = r; a.Dk = Dk; a.Dv = Dv; a.dtype = dtype;
+    return gdn::masked_dp_workspace_bytes(a);
+}
+
 int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
                                   const float *g, const float *mask, const float *initial_state, void *o,
                                   float *final_state, int B, int H, int T, int r, int Dk, int Dv, int chunk,
-                                  float scale, unsigned flags, int dtype, void *stream_v) {
+                                  float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream_v) {
     if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
@@ -193,7 +203,9 @@ int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, c
         return GDN_OK;
     }
     gdn::MaskedDpArgs a{q, k, v, beta, g, mask, initial_state, o, final_state, B, H, T, r, Dk, Dv, chunk,
-                        scale, flags, dtype};
+                        scale, flags, dtype, workspace, workspace_bytes};
+    const size_t need = gdn::masked_dp_workspace_bytes(a);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
     return gdn::launch_masked_dp(a, stream);
 }
 

@@ -79,7 +79,10 @@ struct MaskedDpArgs {
     float scale;
     unsigned flags;
     int dtype;
+    void *ws;
+    size_t ws_bytes;
 };
+size_t masked_dp_workspace_bytes(const MaskedDpArgs &a);
 int launch_masked_dp(const MaskedDpArgs &a, cudaStream_t stream);
 
 // Frame scan: the tensor-core path (bf16, Dk = Dv = 128) needs a workspace of

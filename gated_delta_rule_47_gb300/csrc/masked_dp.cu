@@ -4,270 +4,300 @@
 // the per-slice state update of `gated_chunk_delta_rule_fwd_kernel_h`, and the
 // sum over r of `gated_chunk_fwd_o_fn`).
 //
-// The key dimension is cut into r slices of dk = Dk/r.  Token t has r sub-rows
+// The key dimension is cut into r slices of Dk/r.  Token t has r sub-rows
 // (t, i): sub-row i predicts from the token's decayed state with the read key
-// k_t masked slice-wise by mask[i][:], and writes the state's slice-i rows with
-// the write key k_t,(i); all sub-rows of a token act on the same state.  Per
-// chunk of CQ tokens (rows rho = (t, i), C = CQ r), from state S:
-//   G_t       = within-chunk cumulative log-decay
-//   A[(t,i),(s,j)] = beta_t e^{G_t - G_s} mask[i][j] (k_t,(j) . k_s,(j)),  s < t
-//   R[(t,i)]  = beta_t (v_t - e^{G_t} sum_j mask[i][j] S_(j)^T k_t,(j))
-//   Delta     = (I + A)^-1 R
-//   o_t       = scale (e^{G_t} S^T q_t + sum_{s<=t, j} e^{G_t-G_s} (q_t,(j) . k_s,(j)) Delta_(s,j))
-//   S_(j)    <- e^{G_last} S_(j) + sum_s e^{G_last - G_s} k_s,(j) Delta_(s,j)^T
-// One CTA per (batch*head, 64-wide value tile), the fp32 state tile resident in
-// shared memory.  Tokens past the end of the sequence have k = v = beta = 0 and
-// g = 0, so they change nothing.
+// kr_(t,i) = k_t masked slice-wise by mask[i][:] (slice j scaled by
+// mask[i][j]), and writes the state's slice-i rows with the write key
+// kw_(t,i) = slice i of k_t (zero elsewhere); all sub-rows of a token act on
+// the same state and share v_t and beta_t.  In the WY form over the chunk's
+// sub-rows a = (t, i), with gamma the cumulative log-decay (one value per
+// token) and S the state entering the chunk:
+//   A[a][b] = beta_a e^{gamma_a - gamma_b} kr_a . kw_b   for token(b) < token(a)
+//   T = (I + A)^-1,  W = T diag(beta e^gamma) Kr,  U = T diag(beta) V
+//   Vn = U - W S,    S <- e^{gamma_last} S + Kw^T diag(e^{gamma_last - gamma}) Vn
+//   o_t = scale (e^{gamma_t} S^T q_t + sum_{token(b) <= t} e^{gamma_t - gamma_b} (q_t . kw_b) vn_b)
+// Three launches on 64-row chunks (64 / r tokens; r divides 64):
+//   1. mdp_wy_kernel (one CTA per chunk): the keys, A, T, W, U,
+//      Kd = diag(e^{gamma_last - gamma}) Kw, and the output factors
+//      P[t][b] = scale e^{gamma_t - gamma_b} q_t . kw_b (token(b) <= t).
+//   2. wy_chain_kernel, forward: the state entering each chunk and Vn (32
+//      value columns per CTA), and the final state.
+//   3. mdp_out_kernel (one CTA per chunk): o = diag(scale e^gamma) Q S + P Vn.
+// Tokens past the end of the sequence have k = v = beta = 0 and g = 0, so
+// they change nothing.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "simt_tile.cuh"
 #include "tri_inverse.cuh"
+#include "wy_chain.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kBV = 64;
+using namespace tile;
+constexpr int LC = kC + 1;
 constexpr int kMaxR = 8;
-
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void from_f32(float *p, float x) { *p = x; }
-__device__ __forceinline__ void from_f32(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+constexpr int kMSlice = 32;  // value columns per chain CTA
 
 struct MdpParams {
     const void *q, *k, *v, *beta;
-    const float *g, *mask, *s0;
+    const float *g, *mask;
     void *o;
-    float *sf;
-    int T, r, Dv;
+    // workspace, per (head, chunk): W, Kd [64][Dk]; U, Vn [64][Dv]; S [Dk][Dv];
+    // P [64][64]; gamma [64]
+    float *Ww, *Kdw, *Uw, *Vnw, *Sw, *Pw, *Gw;
+    int T, r, Ct, NT;
     float scale;
-    unsigned flags;
+    int l2;
 };
 
-template <int DK, int C>
-struct MdpSmem {
-    static constexpr int KP = DK + 1, VP = kBV + 1, CP = C + 1;
-    // Ks, Qs [C][KP]; Vs [C][VP]; Ss [DK][VP]; As, Ts, Ps [C][CP]; Rs, Ds [C][VP];
-    // gam, bet, eS [C]; mask [kMaxR * kMaxR]
-    static constexpr int floats =
-        2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C + kMaxR * kMaxR + C * C / 4;
-    static constexpr size_t bytes = sizeof(float) * floats;
+struct MChunk {
+    int ntok, nrows;
+    size_t htok, ci;
 };
 
-__device__ __forceinline__ void warp_cumsum64(float *x, int n, int lane) {
-    float a = lane < n ? x[lane] : 0.f;
-    float b = lane + 32 < n ? x[lane + 32] : 0.f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float ya = __shfl_up_sync(0xffffffffu, a, off);
-        const float yb = __shfl_up_sync(0xffffffffu, b, off);
-        if (lane >= off) {
-            a += ya;
-            b += yb;
-        }
-    }
-    b += __shfl_sync(0xffffffffu, a, 31);
-    __syncwarp();
-    if (lane < n) x[lane] = a;
-    if (lane + 32 < n) x[lane + 32] = b;
+__device__ __forceinline__ MChunk mchunk(const MdpParams &p) {
+    MChunk ch;
+    const int c = blockIdx.x, bh = blockIdx.y, t0 = c * p.Ct;
+    ch.ntok = min(p.Ct, p.T - t0);
+    ch.nrows = ch.ntok * p.r;
+    ch.htok = (size_t)bh * p.T + t0;
+    ch.ci = (size_t)bh * p.NT + c;
+    return ch;
 }
 
-template <int DK>
-__device__ void unit_rows(float *X, int stride, int nrows, int warp, int lane, int nwarps) {
-    for (int t = warp; t < nrows; t += nwarps) {
-        float s = 0.f;
-        for (int d = lane; d < DK; d += 32) s += X[t * stride + d] * X[t * stride + d];
-#pragma unroll
-        for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        const float inv = 1.f / fmaxf(sqrtf(s), 1e-12f);
-        for (int d = lane; d < DK; d += 32) X[t * stride + d] *= inv;
+// ============================================================ 1. WY factors
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
+    extern __shared__ float sm[];
+    constexpr int LK = DK + 1, LV = DV + 1;
+    float *Kt = sm;                // [64][LK] token keys (unit when asked)
+    float *Kr = Kt + kC * LK;      // [64][LK] read keys of the sub-rows
+    float *Kw = Kr + kC * LK;      // [64][LK] write keys of the sub-rows
+    float *Qs = Kw + kC * LK;      // [64][LK] queries
+    float *Vs = Qs + kC * LK;      // [64][LV] values of the sub-rows
+    float *Xa = Vs + kC * LV, *Xb = Xa + kC * LC, *X4 = Xb + kC * LC;
+    float *gam = X4 + kC * kC / 4, *eg = gam + kC, *bet = eg + kC, *nrm = bet + kC, *msk = nrm + kC;
+    const MChunk ch = mchunk(p);
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, r = p.r, sl = DK / r;
+
+    load_rows<T, DK>(Kt, (const T *)p.k + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    for (int e = tid; e < kC * DV; e += kThr) {
+        const int a = e / DV, c = e % DV;
+        Vs[a * LV + c] = a < ch.nrows ? ld_f((const T *)p.v + (ch.htok + a / r) * DV + c) : 0.f;
     }
-}
-
-template <typename Tin, int DK, int C>
-__global__ void __launch_bounds__(kThreads) masked_dp_kernel(MdpParams p) {
-    using L = MdpSmem<DK, C>;
-    constexpr int KP = L::KP, VP = L::VP, CP = L::CP;
-    extern __shared__ float smem[];
-    float *Ks = smem;            // [CQ][KP] token keys
-    float *Qs = Ks + C * KP;     // [CQ][KP] token queries
-    float *Vs = Qs + C * KP;     // [CQ][VP] token values (value tile)
-    float *Ss = Vs + C * VP;     // [DK][VP] state tile
-    float *As = Ss + DK * VP;    // [C][CP]  A over sub-rows
-    float *Ts = As + C * CP;     // [C][CP]  (I + A)^-1
-    float *Ps = Ts + C * CP;     // [CQ][CP] decay-masked slice-wise q.k scores, s <= t
-    float *Rs = Ps + C * CP;     // [C][VP]  R
-    float *Ds = Rs + C * VP;     // [C][VP]  per-slice predictions, then Delta
-    float *gam = Ds + C * VP;    // [CQ]
-    float *bet = gam + C;        // [CQ]
-    float *eS = bet + C;         // [CQ] exp(gam_last - gam_s)
-    float *msk = eS + C;         // [r][r]
-    float *Xs = msk + kMaxR * kMaxR;  // [C*C/4] scratch of the blocked inverse
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int vt = blockIdx.x;
-    const size_t head = blockIdx.y;
-    const int r = p.r, Dv = p.Dv, T = p.T;
-    const int CQ = C / r;  // tokens per chunk
-    const int dk = DK / r;
-
-    const Tin *kp = static_cast<const Tin *>(p.k) + head * (size_t)T * DK;
-    const Tin *qp = static_cast<const Tin *>(p.q) + head * (size_t)T * DK;
-    const Tin *vp = static_cast<const Tin *>(p.v) + head * (size_t)T * Dv + vt * kBV;
-    const Tin *bp = static_cast<const Tin *>(p.beta) + head * (size_t)T;
-    const float *gp = p.g + head * (size_t)T;
-    Tin *op = static_cast<Tin *>(p.o) + head * (size_t)T * Dv + vt * kBV;
-
-    for (int i = tid; i < DK * kBV; i += kThreads) {
-        const int d = i / kBV, j = i % kBV;
-        Ss[d * VP + j] = p.s0 ? p.s0[(head * DK + d) * Dv + vt * kBV + j] : 0.f;
-    }
+    if (tid < kC) bet[tid] = tid < ch.nrows ? ld_f((const T *)p.beta + ch.htok + tid / r) : 0.f;
     if (tid < r * r) msk[tid] = p.mask[tid];
-
-    for (long c0 = 0; c0 < T; c0 += CQ) {
-        const int LQ = (int)min((long)CQ, (long)T - c0);  // valid tokens
-        __syncthreads();
-        for (int i = tid; i < CQ * DK; i += kThreads) {
-            const int t = i / DK, d = i % DK;
-            Ks[t * KP + d] = t < LQ ? to_f32(kp[(c0 + t) * DK + d]) : 0.f;
-            Qs[t * KP + d] = t < LQ ? to_f32(qp[(c0 + t) * DK + d]) : 0.f;
-        }
-        for (int i = tid; i < CQ * kBV; i += kThreads) {
-            const int t = i / kBV, j = i % kBV;
-            Vs[t * VP + j] = t < LQ ? to_f32(vp[(c0 + t) * Dv + j]) : 0.f;
-        }
-        if (tid < C) {
-            const bool ok = tid < LQ;
-            bet[tid] = ok ? to_f32(bp[c0 + tid]) : 0.f;
-            gam[tid] = ok ? gp[c0 + tid] : 0.f;
-        }
-        __syncthreads();
-        if (p.flags & GDN_QK_L2NORM) {
-            unit_rows<DK>(Ks, KP, LQ, warp, lane, kThreads / 32);
-            unit_rows<DK>(Qs, KP, LQ, warp, lane, kThreads / 32);
-        }
-        if (warp == 0) warp_cumsum64(gam, CQ, lane);
-        __syncthreads();
-        const float glast = gam[CQ - 1];
-        if (tid < CQ) eS[tid] = expf(glast - gam[tid]);
-
-        // A over sub-rows, and the slice-wise query-key scores
-        for (int e = tid; e < C * C; e += kThreads) {
-            const int rho = e / C, rho2 = e % C;
-            const int t = rho / r, i = rho % r, s = rho2 / r, j = rho2 % r;
-            float a = 0.f;
-            if (s < t) {
-                float acc = 0.f;
-                for (int d = j * dk; d < (j + 1) * dk; ++d) acc += Ks[t * KP + d] * Ks[s * KP + d];
-                a = bet[t] * expf(gam[t] - gam[s]) * msk[i * r + j] * acc;
-            }
-            As[rho * CP + rho2] = a;
-            if (rho < CQ) {  // query row t = rho against sub-row (s, j)
-                float pv = 0.f;
-                if (s <= rho) {
-                    float acc = 0.f;
-                    for (int d = j * dk; d < (j + 1) * dk; ++d) acc += Qs[rho * KP + d] * Ks[s * KP + d];
-                    pv = expf(gam[rho] - gam[s]) * acc;
-                }
-                Ps[rho * CP + rho2] = pv;
+    if (tid < 32) {  // gamma per sub-row: the token's g enters on its first sub-row
+        const int a0 = tid, a1 = tid + 32;
+        float x0 = (a0 < ch.nrows && a0 % r == 0) ? p.g[ch.htok + a0 / r] : 0.f;
+        float x1 = (a1 < ch.nrows && a1 % r == 0) ? p.g[ch.htok + a1 / r] : 0.f;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (tid >= o) {
+                x0 += y0;
+                x1 += y1;
             }
         }
-        // per-slice predictions Z[(t,j)] = S_(j)^T k_t,(j) into Ds
-        for (int e = tid; e < C * kBV; e += kThreads) {
-            const int rho = e / kBV, c = e % kBV;
-            const int t = rho / r, j = rho % r;
-            float acc = 0.f;
-            for (int d = j * dk; d < (j + 1) * dk; ++d) acc += Ks[t * KP + d] * Ss[d * VP + c];
-            Ds[rho * VP + c] = acc;
-        }
-        __syncthreads();
-        // R[(t,i)] = beta_t (v_t - e^{G_t} sum_j mask[i][j] Z[(t,j)])
-        for (int e = tid; e < C * kBV; e += kThreads) {
-            const int rho = e / kBV, c = e % kBV;
-            const int t = rho / r, i = rho % r;
-            float pr = 0.f;
-            for (int j = 0; j < r; ++j) pr += msk[i * r + j] * Ds[(t * r + j) * VP + c];
-            Rs[rho * VP + c] = bet[t] * (Vs[t * VP + c] - expf(gam[t]) * pr);
-        }
-        // (I + A)^-1: 16 x 16 diagonal blocks, then the 16- and 32-level merges
-        unit_lower_inverse<C, kThreads>(As, Ts, Xs, CP);
-        // Delta = (I + A)^-1 R
-        for (int e = tid; e < C * kBV; e += kThreads) {
-            const int rho = e / kBV, c = e % kBV;
-            float acc = 0.f;
-            for (int s = 0; s <= rho; ++s) acc += Ts[rho * CP + s] * Rs[s * VP + c];
-            Ds[rho * VP + c] = acc;
-        }
-        __syncthreads();
-        // outputs of the chunk's tokens (the state before this chunk's update)
-        for (int e = tid; e < LQ * kBV; e += kThreads) {
-            const int t = e / kBV, c = e % kBV;
-            float inter = 0.f;
-            for (int d = 0; d < DK; ++d) inter += Qs[t * KP + d] * Ss[d * VP + c];
-            float intra = 0.f;
-            for (int rho2 = 0; rho2 < (t + 1) * r; ++rho2) intra += Ps[t * CP + rho2] * Ds[rho2 * VP + c];
-            from_f32(op + (c0 + t) * Dv + c, p.scale * (expf(gam[t]) * inter + intra));
-        }
-        __syncthreads();
-        // state update: slice j rows take the sub-rows (s, j)
-        const float dl = expf(glast);
-        for (int e = tid; e < DK * kBV; e += kThreads) {
-            const int d = e / kBV, c = e % kBV;
-            const int j = d / dk;
-            float acc = 0.f;
-            for (int s = 0; s < CQ; ++s) acc += Ks[s * KP + d] * eS[s] * Ds[(s * r + j) * VP + c];
-            Ss[d * VP + c] = dl * Ss[d * VP + c] + acc;
-        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        gam[a0] = x0;
+        gam[a1] = x1;
+        eg[a0] = expf(x0);
+        eg[a1] = expf(x1);
+    }
+    for (int e = tid; e < kC * LC; e += kThr) Xb[e] = 0.f;
+    __syncthreads();
+    // the sub-rows' read and write keys
+    for (int e = tid; e < kC * DK; e += kThr) {
+        const int a = e / DK, c = e % DK, i = a % r, j = c / sl;
+        const float x = Kt[(a / r) * LK + c];
+        Kr[a * LK + c] = x * msk[i * r + j];
+        Kw[a * LK + c] = j == i ? x : 0.f;
     }
     __syncthreads();
-    if (p.sf) {
-        for (int i = tid; i < DK * kBV; i += kThreads) {
-            const int d = i / kBV, j = i % kBV;
-            p.sf[(head * DK + d) * Dv + vt * kBV + j] = Ss[d * VP + j];
+    // A over the sub-rows of earlier tokens
+    {
+        float acc[2][4];
+        zero(acc);
+        mm<kThr, 2, 4>(acc, Kr, LK, 1, Kw, 1, LK, DK);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int a = ty + 32 * i, b = tx + 16 * j;
+                Xa[a * LC + b] = b / r < a / r ? bet[a] * expf(gam[a] - gam[b]) * acc[i][j] : 0.f;
+            }
+    }
+    __syncthreads();
+    unit_lower_inverse<kC, kThr>(Xa, Xb, X4, LC);  // Xb = T
+    for (int e = tid; e < kC * kC; e += kThr) {
+        const int m = e / kC, b = e % kC;
+        const float t = Xb[m * LC + b];
+        Xa[m * LC + b] = t * bet[b] * eg[b];
+        Xb[m * LC + b] = t * bet[b];
+    }
+    __syncthreads();
+    {
+        float acc[2][DK / 16];
+        zero(acc);
+        mm<kThr, 2, DK / 16>(acc, Xa, LC, 1, Kr, LK, 1, kC);
+        float *Wg = p.Ww + ch.ci * kC * DK;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < DK / 16; ++j) Wg[(ty + 32 * i) * DK + tx + 16 * j] = acc[i][j];
+    }
+    {
+        float acc[2][DV / 16];
+        zero(acc);
+        mm<kThr, 2, DV / 16>(acc, Xb, LC, 1, Vs, LV, 1, kC);
+        float *Ug = p.Uw + ch.ci * kC * DV;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < DV / 16; ++j) Ug[(ty + 32 * i) * DV + tx + 16 * j] = acc[i][j];
+    }
+    {
+        const float gl = gam[kC - 1];
+        float *Kdg = p.Kdw + ch.ci * kC * DK;
+        for (int e = tid; e < kC * DK; e += kThr) Kdg[e] = expf(gl - gam[e / DK]) * Kw[(e / DK) * LK + e % DK];
+        if (tid < kC) p.Gw[ch.ci * kC + tid] = gam[tid];
+    }
+    // the output factors P[t][b] over the sub-rows of tokens up to t
+    {
+        float acc[2][4];
+        zero(acc);
+        mm<kThr, 2, 4>(acc, Qs, LK, 1, Kw, 1, LK, DK);
+        float *Pg = p.Pw + ch.ci * kC * kC;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = ty + 32 * i, b = tx + 16 * j;
+                Pg[t * kC + b] = (t < ch.ntok && b / r <= t) ? p.scale * expf(gam[t * r] - gam[b]) * acc[i][j] : 0.f;
+            }
+    }
+}
+
+// ============================================================== 3. outputs
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThr, 1) mdp_out_kernel(MdpParams p) {
+    extern __shared__ float sm[];
+    constexpr int LK = DK + 1, LV = DV + 1, NH = DK / 64;
+    float *Qs = sm;              // [64][LK]
+    float *Vn = Qs + kC * LK;    // [64][LV]
+    float *Hs = Vn + kC * LV;    // [64][LV] a 64-row block of S
+    float *Ps = Hs + kC * LV;    // [64][LC]
+    float *gam = Ps + kC * LC, *nrm = gam + kC;
+    const MChunk ch = mchunk(p);
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, r = p.r;
+    const float *Sg = p.Sw + ch.ci * DK * DV;
+
+    load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    load_rows<float, DV>(Vn, p.Vnw + ch.ci * kC * DV, kC, false, nullptr);
+    for (int e = tid; e < kC * kC; e += kThr) Ps[(e / kC) * LC + e % kC] = p.Pw[ch.ci * kC * kC + e];
+    if (tid < kC) gam[tid] = p.Gw[ch.ci * kC + tid];
+    float accQS[2][DV / 16], accPV[2][DV / 16];
+    zero(accQS);
+    zero(accPV);
+    for (int h = 0; h < NH; ++h) {
+        __syncthreads();
+        for (int e = tid; e < 64 * DV; e += kThr) Hs[(e / DV) * LV + e % DV] = Sg[(size_t)64 * h * DV + e];
+        __syncthreads();
+        mm<kThr, 2, DV / 16>(accQS, Qs + 64 * h, LK, 1, Hs, LV, 1, 64);
+    }
+    mm<kThr, 2, DV / 16>(accPV, Ps, LC, 1, Vn, LV, 1, kC);
+    T *op = (T *)p.o + ch.htok * DV;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int t = ty + 32 * i;
+        if (t < ch.ntok) {
+            const float qs = p.scale * expf(gam[t * r]);
+#pragma unroll
+            for (int j = 0; j < DV / 16; ++j) st_f(op + (size_t)t * DV + tx + 16 * j, qs * accQS[i][j] + accPV[i][j]);
         }
     }
 }
 
-template <typename Tin, int DK, int C>
-int launch_one(const MaskedDpArgs &a, cudaStream_t stream) {
-    auto kern = masked_dp_kernel<Tin, DK, C>;
-    constexpr size_t smem = MdpSmem<DK, C>::bytes;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+constexpr size_t wy_smem(int DK, int DV) {
+    return sizeof(float) * ((size_t)4 * kC * (DK + 1) + kC * (DV + 1) + 2 * kC * LC + kC * kC / 4 + 4 * kC + 64);
+}
+constexpr size_t out_smem(int DK, int DV) {
+    return sizeof(float) * ((size_t)kC * (DK + 1) + 2 * kC * (DV + 1) + kC * LC + 2 * kC);
+}
+
+size_t per_chunk_floats(int Dk, int Dv) {
+    return 2 * (size_t)kC * Dk + 2 * (size_t)kC * Dv + (size_t)Dk * Dv + (size_t)kC * kC + kC;
+}
+
+template <typename T, int DK, int DV>
+int run(const MaskedDpArgs &a, cudaStream_t st) {
+    const int BH = a.B * a.H, Ct = kC / a.r, NT = (a.T + Ct - 1) / Ct;
+    const size_t nc = (size_t)BH * NT;
+    float *w = static_cast<float *>(a.ws);
+    MdpParams p{};
+    p.q = a.q;
+    p.k = a.k;
+    p.v = a.v;
+    p.beta = a.beta;
+    p.g = a.g;
+    p.mask = a.mask;
+    p.o = a.o;
+    p.Ww = w;
+    p.Kdw = p.Ww + nc * kC * DK;
+    p.Uw = p.Kdw + nc * kC * DK;
+    p.Vnw = p.Uw + nc * kC * DV;
+    p.Sw = p.Vnw + nc * kC * DV;
+    p.Pw = p.Sw + nc * DK * DV;
+    p.Gw = p.Pw + nc * kC * kC;
+    p.T = a.T;
+    p.r = a.r;
+    p.Ct = Ct;
+    p.NT = NT;
+    p.scale = a.scale;
+    p.l2 = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
+    constexpr size_t s1 = wy_smem(DK, DV), s2 = wy_chain_smem<DK, kMSlice>(), s3 = out_smem(DK, DV);
+    if (cudaFuncSetAttribute(mdp_wy_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(wy_chain_kernel<DK, DV, kMSlice>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)s2) != cudaSuccess ||
+        cudaFuncSetAttribute(mdp_out_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3) !=
+            cudaSuccess)
         return GDN_ERR_CUDA;
-    MdpParams p{a.q, a.k, a.v, a.beta, a.g, a.mask, a.s0, a.o, a.sf, a.T, a.r, a.Dv, a.scale, a.flags};
-    dim3 grid(a.Dv / kBV, a.B * a.H);
-    kern<<<grid, kThreads, smem, stream>>>(p);
+    mdp_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
+    note_launch();
+    WyChainParams cp{a.s0, nullptr, a.sf, nullptr, p.Sw, nullptr, p.Ww, p.Kdw, p.Uw, p.Vnw, nullptr, p.Gw, NT};
+    wy_chain_kernel<DK, DV, kMSlice><<<dim3((unsigned)(DV / kMSlice), (unsigned)BH, 1), kChainThr, s2, st>>>(cp);
+    note_launch();
+    mdp_out_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s3, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-template <typename Tin, int DK>
-int launch_chunk(const MaskedDpArgs &a, cudaStream_t stream) {
-    switch (a.chunk) {
-        case 16: return launch_one<Tin, DK, 16>(a, stream);
-        case 32: return launch_one<Tin, DK, 32>(a, stream);
-        case 64: return launch_one<Tin, DK, 64>(a, stream);
-        default: return GDN_ERR_UNSUPPORTED;
-    }
-}
-
-template <typename Tin>
-int launch_dk(const MaskedDpArgs &a, cudaStream_t stream) {
-    switch (a.Dk) {
-        case 64: return launch_chunk<Tin, 64>(a, stream);
-        case 128: return launch_chunk<Tin, 128>(a, stream);
-        default: return GDN_ERR_UNSUPPORTED;
-    }
+template <typename T>
+int run_t(const MaskedDpArgs &a, cudaStream_t st) {
+    if (a.Dk == 128 && a.Dv == 128) return run<T, 128, 128>(a, st);
+    if (a.Dk == 128 && a.Dv == 64) return run<T, 128, 64>(a, st);
+    if (a.Dk == 64 && a.Dv == 128) return run<T, 64, 128>(a, st);
+    if (a.Dk == 64 && a.Dv == 64) return run<T, 64, 64>(a, st);
+    return GDN_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
+size_t masked_dp_workspace_bytes(const MaskedDpArgs &a) {
+    if (a.r < 1 || a.r > kMaxR || kC % a.r != 0 || a.T <= 0) return 0;
+    const int Ct = kC / a.r, NT = (a.T + Ct - 1) / Ct;
+    return sizeof(float) * (size_t)a.B * a.H * NT * per_chunk_floats(a.Dk, a.Dv);
+}
+
 int launch_masked_dp(const MaskedDpArgs &a, cudaStream_t stream) {
-    if (a.Dv % kBV != 0 || a.r > kMaxR) return GDN_ERR_UNSUPPORTED;
-    if (a.dtype == GDN_F32) return launch_dk<float>(a, stream);
-    if (a.dtype == GDN_BF16) return launch_dk<__nv_bfloat16>(a, stream);
+    if (a.r > kMaxR || kC % a.r != 0) return GDN_ERR_UNSUPPORTED;
+    if (a.dtype == GDN_F32) return run_t<float>(a, stream);
+    if (a.dtype == GDN_BF16) return run_t<__nv_bfloat16>(a, stream);
     return GDN_ERR_UNSUPPORTED;
 }
 

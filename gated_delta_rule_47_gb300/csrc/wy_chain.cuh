@@ -1,0 +1,124 @@
+// wy_chain.cuh -- the sequential part of the chunkwise WY form on the CUDA
+// cores (fp32), for kernels that have formed each chunk's factors in a
+// parallel pass: per head, with W, U, Kd = diag(e^{gamma_last - gamma}) K_write
+// and gamma of every 64-row chunk in global memory,
+//   forward:  Vn = U - W S  (kept),  S <- e^{gamma_last} S + Kd^T Vn
+//   reverse:  dS <- e^{gamma_last} dS - W^T (Kd dS) + B_c
+// keeping the state entering each chunk (forward) and the gradient of the
+// state leaving it (reverse).  The value columns of both chains are
+// independent, so each CTA holds SLICE columns of one head's state.
+#pragma once
+
+#include "simt_tile.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kChainThr = 256;  // threads of a chain CTA
+
+struct WyChainParams {
+    const float *s0, *dsf;  // [BH][Dk][Dv] or null (zero)
+    float *sf, *ds0;        // [BH][Dk][Dv] or null (not wanted): final state, initial state's gradient
+    // per (head, chunk): S entering and dS' leaving [Dk][Dv], W and Kd [64][Dk], U and Vn
+    // [64][Dv], B [Dk][Dv], gamma [64]
+    float *Sw, *dSw, *Ww, *Kdw, *Uw, *Vnw, *Bw, *Gw;
+    int NT;  // chunks per head
+};
+
+template <int DK, int SLICE>
+constexpr size_t wy_chain_smem() {
+    return sizeof(float) * ((size_t)DK * (SLICE + 1) + tile::kC * (DK + 1) + tile::kC * (SLICE + 1));
+}
+
+// blockIdx.x: SLICE-column slice of the value dimension; blockIdx.y: head;
+// blockIdx.z: 0 = forward state chain, 1 = reverse gradient chain.
+template <int DK, int DV, int SLICE>
+__global__ void __launch_bounds__(kChainThr) wy_chain_kernel(WyChainParams p) {
+    using namespace tile;
+    extern __shared__ float sm[];
+    constexpr int LK = DK + 1, LS = SLICE + 1;
+    float *St = sm;             // [DK][LS]  state (or gradient) slice
+    float *Wt = St + DK * LS;   // [kC][LK]  W or Kd of the chunk
+    float *Ut = Wt + kC * LK;   // [kC][LS]  U / Vn or Kd dS'
+    const int col0 = blockIdx.x * SLICE, bh = blockIdx.y, role = blockIdx.z;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int NT = p.NT;
+
+    const float *init = role == 0 ? p.s0 : p.dsf;
+    for (int e = tid; e < DK * SLICE; e += kChainThr) {
+        const int m = e / SLICE, n = e % SLICE;
+        St[m * LS + n] = init ? init[((size_t)bh * DK + m) * DV + col0 + n] : 0.f;
+    }
+    __syncthreads();
+    for (int s = 0; s < NT; ++s) {
+        const int c = role == 0 ? s : NT - 1 - s;
+        const size_t ci = (size_t)bh * NT + c;
+        const float el = expf(p.Gw[ci * kC + kC - 1]);
+        float *snap = (role == 0 ? p.Sw : p.dSw) + ci * DK * DV;
+        for (int e = tid; e < DK * SLICE; e += kChainThr) {
+            const int m = e / SLICE, n = e % SLICE;
+            snap[(size_t)m * DV + col0 + n] = St[m * LS + n];
+        }
+        const float *Wg = p.Ww + ci * kC * DK, *Kdg = p.Kdw + ci * kC * DK;
+        const float *first = role == 0 ? Wg : Kdg, *second = role == 0 ? Kdg : Wg;
+        for (int e = tid; e < kC * DK; e += kChainThr) Wt[(e / DK) * LK + e % DK] = first[e];
+        if (role == 0) {
+            const float *Ug = p.Uw + ci * kC * DV;
+            for (int e = tid; e < kC * SLICE; e += kChainThr) {
+                const int m = e / SLICE, n = e % SLICE;
+                Ut[m * LS + n] = Ug[(size_t)m * DV + col0 + n];
+            }
+        }
+        __syncthreads();
+        // role 0: Vn = U - W S;  role 1: Y = Kd dS'
+        {
+            float acc[4][SLICE / 16];
+            zero(acc);
+            mm<kChainThr, 4, SLICE / 16>(acc, Wt, LK, 1, St, LS, 1, DK);
+            float *Vng = p.Vnw + ci * kC * DV;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < SLICE / 16; ++j) {
+                    const int m = ty + 16 * i, n = tx + 16 * j;
+                    if (role == 0) {
+                        const float vn = Ut[m * LS + n] - acc[i][j];
+                        Vng[(size_t)m * DV + col0 + n] = vn;
+                        Ut[m * LS + n] = vn;
+                    } else {
+                        Ut[m * LS + n] = acc[i][j];
+                    }
+                }
+        }
+        __syncthreads();
+        for (int e = tid; e < kC * DK; e += kChainThr) Wt[(e / DK) * LK + e % DK] = second[e];
+        __syncthreads();
+        // role 0: S = e^{gl} S + Kd^T Vn;  role 1: dS = e^{gl} dS' - W^T Y + B
+        {
+            float acc[DK / 16][SLICE / 16];
+            zero(acc);
+            mm<kChainThr, DK / 16, SLICE / 16>(acc, Wt, 1, LK, Ut, LS, 1, kC);
+            const float *Bg = p.Bw + ci * DK * DV;
+#pragma unroll
+            for (int i = 0; i < DK / 16; ++i)
+#pragma unroll
+                for (int j = 0; j < SLICE / 16; ++j) {
+                    const int m = ty + 16 * i, n = tx + 16 * j;
+                    const float old = St[m * LS + n];
+                    St[m * LS + n] = role == 0 ? el * old + acc[i][j]
+                                               : el * old - acc[i][j] + Bg[(size_t)m * DV + col0 + n];
+                }
+        }
+        __syncthreads();
+    }
+    float *out = role == 0 ? p.sf : p.ds0;
+    if (out) {
+        for (int e = tid; e < DK * SLICE; e += kChainThr) {
+            const int m = e / SLICE, n = e % SLICE;
+            out[((size_t)bh * DK + m) * DV + col0 + n] = St[m * LS + n];
+        }
+    }
+}
+
+}  // namespace
+}  // namespace gdn

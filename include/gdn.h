@@ -187,15 +187,24 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
  * the mask expanded to Dk/r x Dk/r blocks.  An all-ones mask is gdn_chunk_fwd.
  *
  *   q, k [B,H,T,Dk]; v, o [B,H,T,Dv]; beta [B,H,T] (all dtype); g [B,H,T] fp32
- *   mask [r][r] fp32 (device), shared by all heads; 1 <= r <= 8, r | Dk
- *   chunk   sub-rows per chunk (16, 32 or 64, a multiple of r): chunk / r tokens
- *   flags   0 or GDN_QK_L2NORM.  CUDA-core path, fp32 arithmetic.
+ *   mask [r][r] fp32 (device), shared by all heads; r in {1, 2, 4, 8}, r | Dk
+ *   chunk   16, 32 or 64, a multiple of r (accepted for symmetry with the other
+ *           entry points: the kernels work on 64 sub-rows, 64 / r tokens, per
+ *           chunk, and results do not depend on the chunk beyond rounding)
+ *   flags   0 or GDN_QK_L2NORM.  CUDA-core path, fp32 arithmetic: the chunks'
+ *           WY factors in parallel, the state chain by 32 value columns per
+ *           CTA, then the outputs in parallel (three launches).
+ *   workspace: masked_deltaproduct_chunk_fwd_workspace_bytes(...) bytes,
+ *           16-byte aligned (GDN_ERR_WORKSPACE when missing or short); no
+ *           initialisation needed, contents not meaningful afterwards.
  * State, scale, dtype and the empty cases as gdn_chunk_fwd.
  */
+size_t masked_deltaproduct_chunk_fwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype);
 int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
                                   const float *g, const float *mask, const float *initial_state, void *o,
                                   float *final_state, int B, int H, int T, int r, int Dk, int Dv, int chunk,
-                                  float scale, unsigned flags, int dtype, void *stream);
+                                  float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream);
 
 /*
  * Bytes of device workspace cam_scan_fwd needs for these sizes on the current

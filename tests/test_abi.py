@@ -141,9 +141,12 @@ def test_masked_deltaproduct_argument_checks(lib):
     f = lib.masked_deltaproduct_chunk_fwd
     u = 0x10000
 
-    def call(r=2, Dk=64, chunk=64, flags=0, mask=u, q=u, dtype=binding.GDN_F32):
-        return f(q, u, u, u, u, mask, None, u, None, 1, 2, 8, r, Dk, 64, chunk, 1.0, flags, dtype, None)
+    def call(r=2, Dk=64, chunk=64, flags=0, mask=u, q=u, dtype=binding.GDN_F32, ws=u, ws_bytes=1 << 40):
+        return f(q, u, u, u, u, mask, None, u, None, 1, 2, 8, r, Dk, 64, chunk, 1.0, flags, dtype, ws, ws_bytes,
+                 None)
 
+    assert call(ws=None) == 4      # workspace missing
+    assert call(ws_bytes=16) == 4  # or short
     assert call(r=3) == 2          # r must divide Dk
     assert call(r=16, Dk=128) == 2  # r <= 8
     assert call(chunk=48) == 2
@@ -152,6 +155,11 @@ def test_masked_deltaproduct_argument_checks(lib):
     assert call(mask=None) == 1
     assert call(q=u + 4) == 3
     assert call(dtype=3) == 1
+    q = lib.masked_deltaproduct_chunk_fwd_workspace_bytes
+    per = 2 * 64 * 64 + 2 * 64 * 64 + 64 * 64 + 64 * 64 + 64  # W, Kd, U, Vn, S, P, gamma at D = 64
+    assert q(1, 2, 40, 2, 64, 64, binding.GDN_F32) == 4 * 2 * 2 * per  # 40 tokens: two chunks of 32
+    assert q(1, 2, 0, 2, 64, 64, binding.GDN_F32) == 0
+    assert q(1, 2, 40, 3, 64, 64, binding.GDN_F32) == ctypes.c_size_t(-1).value
 
 
 def test_cam_prep_scan_argument_checks(lib):
