@@ -457,7 +457,15 @@ def secondary(args, dev):
     out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
                    "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "path": "CUDA cores, fp32",
                    "launches_per_call": 3}
-    del d, o, wsm
+    # its backward
+    gom = torch.randn(w.B, w.H, w.T, w.D, device=dev).to(torch.bfloat16)
+    wsmb = torch.empty(binding.load().masked_deltaproduct_chunk_bwd_workspace_bytes(w.B, w.H, w.T, w.r, w.D, w.D, 1),
+                       dtype=torch.uint8, device=dev)
+    ms = timeit(lambda: binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"],
+                                                              gom, workspace=wsmb))
+    out["masked_dp_bwd_r2_b4h16t4096d128_bf16"] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                                                   "path": "CUDA cores, fp32", "launches_per_call": 3}
+    del d, o, wsm, gom, wsmb
     torch.cuda.empty_cache()
     # the chunkwise GDN backward on the headline's shape (CUDA cores, fp32 arithmetic)
     w = WORKLOADS["gdn_b4h16t4096d128_bf16"]

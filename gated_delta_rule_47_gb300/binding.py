@@ -30,7 +30,8 @@ EXPORTS = ("gdn_status_string", "gdn_version", "gdn_chunk_fwd_workspace_bytes", 
            "masked_deltaproduct_chunk_fwd", "masked_deltaproduct_chunk_fwd_workspace_bytes",
            "cam_prep_scan_fwd_workspace_bytes", "cam_prep_scan_fwd",
            "cam_prep_bwd", "cam_scan_bwd_workspace_bytes", "cam_scan_bwd", "gdn_chunk_bwd_workspace_bytes",
-           "gdn_chunk_bwd", "deltaproduct_chunk_bwd")
+           "gdn_chunk_bwd", "deltaproduct_chunk_bwd", "masked_deltaproduct_chunk_bwd_workspace_bytes",
+           "masked_deltaproduct_chunk_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +85,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.gdn_chunk_bwd.restype = i
         lib.deltaproduct_chunk_bwd.argtypes = [vp] * 14 + [i] * 6 + [f, u, i, vp, sz, vp]
         lib.deltaproduct_chunk_bwd.restype = i
+        lib.masked_deltaproduct_chunk_bwd_workspace_bytes.argtypes = [i] * 7
+        lib.masked_deltaproduct_chunk_bwd_workspace_bytes.restype = sz
+        lib.masked_deltaproduct_chunk_bwd.argtypes = [vp] * 15 + [i] * 6 + [f, u, i, vp, sz, vp]
+        lib.masked_deltaproduct_chunk_bwd.restype = i
         lib.cam_prep_bwd.argtypes = [vp] * 8 + [f] + [vp] * 8 + [i] * 4 + [f, f, i, vp]
         lib.cam_prep_bwd.restype = i
         lib.cam_scan_fwd_workspace_bytes.argtypes = [i] * 7
@@ -470,6 +475,44 @@ def deltaproduct_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_stat
                                     _ptr(ds0), B, H, T, r, Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code,
                                     _ptr(workspace), ws_bytes, _stream(stream))
     _raise("deltaproduct_chunk_bwd", st)
+    return dq, dk, dv, dbeta, dg, ds0
+
+
+def masked_deltaproduct_chunk_bwd(q, k, v, beta, g, mask, do, initial_state=None, dfinal_state=None, scale=1.0,
+                                  l2norm=False, need_dinitial=False, workspace=None, stream=None):
+    """Backward of masked_deltaproduct_chunk_fwd.  Returns (dq, dk, dv, dbeta,
+    dg, dinitial_state or None); dq, dk, dv in the inputs' dtype, the rest fp32."""
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    r = mask.shape[0]
+    dt = q.dtype
+    code = _dtype_code(q)
+    _check(q, "q", (B, H, T, Dk), dt)
+    _check(k, "k", (B, H, T, Dk), dt)
+    _check(v, "v", (B, H, T, Dv), dt)
+    _check(beta, "beta", (B, H, T), dt)
+    _check(g, "g", (B, H, T), torch.float32)
+    _check(mask, "mask", (r, r), torch.float32)
+    _check(do, "do", (B, H, T, Dv), dt)
+    for name, t in (("initial_state", initial_state), ("dfinal_state", dfinal_state)):
+        if t is not None:
+            _check(t, name, (B, H, Dk, Dv), torch.float32)
+    dev = q.device
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbeta = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    dg = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ds0 = torch.empty(B, H, Dk, Dv, dtype=torch.float32, device=dev) if need_dinitial else None
+    lib = load()
+    if workspace is None:
+        need = lib.masked_deltaproduct_chunk_bwd_workspace_bytes(B, H, T, r, Dk, Dv, code)
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.masked_deltaproduct_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
+                                           _ptr(initial_state), _ptr(do), _ptr(dfinal_state), _ptr(dq), _ptr(dk),
+                                           _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(ds0), B, H, T, r, Dk, Dv,
+                                           float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace),
+                                           ws_bytes, _stream(stream))
+    _raise("masked_deltaproduct_chunk_bwd", st)
     return dq, dk, dv, dbeta, dg, ds0
 
 

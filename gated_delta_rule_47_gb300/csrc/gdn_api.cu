@@ -436,6 +436,54 @@ int gdn_chunk_bwd(const void *q, const void *k, const void *v, const void *beta,
                                   workspace_bytes, stream);
 }
 
+size_t masked_deltaproduct_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype) {
+    if (B < 0 || H < 0 || T < 0 || r < 1 || r > 8 || 64 % r != 0) return (size_t)-1;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128) || Dk % r != 0) return (size_t)-1;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return (size_t)-1;
+    gdn::MaskedBwdArgs a{};
+    a.B = B; a.H = H; a.T = T; a.r = r; a.Dk = Dk; a.Dv = Dv; a.dtype = dtype;
+    return gdn::masked_bwd_workspace_bytes(a);
+}
+
+int masked_deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, const void *beta, const float *g,
+                                  const float *mask, const float *initial_state, const void *dout,
+                                  const float *dfinal_state, void *dq, void *dk, void *dv, float *dbeta, float *dg,
+                                  float *dinitial_state, int B, int H, int T, int r, int Dk, int Dv, float scale,
+                                  unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if (r > 8 || 64 % r != 0 || Dk % r != 0) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535 || (long long)T * r >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)B * H * T != 0) {
+        if (!q || !k || !v || !beta || !g || !mask || !dout || !dq || !dk || !dv || !dbeta || !dg)
+            return GDN_ERR_INVALID_ARG;
+    }
+    const void *ps[] = {q, k, v, beta, g, mask, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, dg,
+                        dinitial_state};
+    for (const void *p : ps)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::MaskedBwdArgs a{q, k, v, beta, g, mask, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, dg,
+                         dinitial_state, B, H, T, r, Dk, Dv, scale, flags, dtype, workspace, workspace_bytes};
+    const size_t need = gdn::masked_bwd_workspace_bytes(a);
+    if ((long long)B * H * T != 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return GDN_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((long long)B * H == 0) return GDN_OK;
+    if (T == 0) {  // the initial state's gradient is the final state's
+        if (dinitial_state) {
+            const size_t bytes = sizeof(float) * (size_t)B * H * Dk * Dv;
+            cudaError_t e = dfinal_state ? cudaMemcpyAsync(dinitial_state, dfinal_state, bytes,
+                                                           cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(dinitial_state, 0, bytes, st);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
+    return gdn::launch_masked_bwd(a, st);
+}
+
 int gdn_get_device_error(void *stream) {
     const int a = gdn::scan_tc_read_clear_error(static_cast<cudaStream_t>(stream));
     const int b = gdn::cam_prep_read_clear_error();

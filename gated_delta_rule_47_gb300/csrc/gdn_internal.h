@@ -185,6 +185,24 @@ struct ChunkBwdArgs {
 size_t chunk_bwd_workspace_bytes(const ChunkBwdArgs &a);
 int launch_chunk_bwd(const ChunkBwdArgs &a, cudaStream_t stream);
 
+// Backward of the block-masked DeltaProduct forward.
+struct MaskedBwdArgs {
+    const void *q, *k, *v, *beta;
+    const float *g, *mask, *s0;
+    const void *dout;
+    const float *dsf;
+    void *dq, *dk, *dv;
+    float *dbeta, *dg, *ds0;
+    int B, H, T, r, Dk, Dv;
+    float scale;
+    unsigned flags;
+    int dtype;
+    void *ws;
+    size_t ws_bytes;
+};
+size_t masked_bwd_workspace_bytes(const MaskedBwdArgs &a);
+int launch_masked_bwd(const MaskedBwdArgs &a, cudaStream_t stream);
+
 // Counts one kernel launch (thread-safe); read by gdn_launch_count().
 void note_launch();
 

@@ -42,6 +42,26 @@ __device__ __forceinline__ void mm(float (&acc)[TI][TJ], const float *A, int am,
     }
 }
 
+// As mm, with the operands given by accessors fa(m, k) and fb(k, n) (for
+// operands formed on the fly from others).
+template <int NTHR, int TI, int TJ, class FA, class FB>
+__device__ __forceinline__ void mm_f(float (&acc)[TI][TJ], const FA &fa, const FB &fb, int K) {
+    constexpr int RS = NTHR / 16;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[TI], b[TJ];
+#pragma unroll
+        for (int i = 0; i < TI; ++i) a[i] = fa(ty + RS * i, k);
+#pragma unroll
+        for (int j = 0; j < TJ; ++j) b[j] = fb(k, tx + 16 * j);
+#pragma unroll
+        for (int i = 0; i < TI; ++i)
+#pragma unroll
+            for (int j = 0; j < TJ; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+}
+
 template <int TI, int TJ>
 __device__ __forceinline__ void zero(float (&a)[TI][TJ]) {
 #pragma unroll

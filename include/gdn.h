@@ -207,6 +207,41 @@ int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, c
                                   void *stream);
 
 /*
+ * Bytes of device workspace masked_deltaproduct_chunk_bwd needs: per head and
+ * chunk of 64 / r tokens the chunk's WY factors, the state entering it and the
+ * gradient of the state leaving it (about 340 KB at Dk = Dv = 128).  0 when
+ * T = 0; (size_t)-1 for sizes it rejects.
+ */
+size_t masked_deltaproduct_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype);
+
+/*
+ * masked_deltaproduct_chunk_bwd -- backward of masked_deltaproduct_chunk_fwd
+ * (gated_deltaproduct test.py: `gated_chunk_delta_rule_bwd_kernel_dhu`,
+ * `gated_chunk_delta_rule_bwd_kernel_dqkw`, `gated_bwd_prepare_wy_repr_kernel`).
+ * Per token, with D the decayed state, the sub-rows' read keys kr_i and write
+ * keys kw_i as in the forward, e_i = v - D^T kr_i and G the gradient of the
+ * state after the token:
+ *     w_i = G^T kw_i;  dv = beta sum_i w_i;  dbeta = sum_i kw_i . (G e_i)
+ *     dkw_i = beta G e_i;  dkr_i = -beta D w_i;  dD = G - beta sum_i kr_i w_i^T
+ * slice j of dk = slice j of (dkw_j + sum_i mask[i][j] dkr_i), dg = <dD, D>,
+ * and the state entering the token gets exp(g) dD; computed chunk-wise
+ * (CUDA cores, fp32, three launches as gdn_chunk_bwd).
+ *   q, k, v, beta, g, mask, initial_state, scale, flags, dtype, Dk, Dv, r: as
+ *           given to masked_deltaproduct_chunk_fwd (r in {1, 2, 4, 8})
+ *   dout [B,H,T,Dv] dtype;  dfinal_state [B,H,Dk,Dv] fp32 or NULL (= zero)
+ *   dq, dk [B,H,T,Dk], dv [B,H,T,Dv] dtype;  dbeta, dg [B,H,T] fp32;
+ *   dinitial_state [B,H,Dk,Dv] fp32 or NULL (not wanted)
+ *   workspace: masked_deltaproduct_chunk_bwd_workspace_bytes(...) bytes,
+ *           16-byte aligned.
+ * The empty cases as gdn_chunk_bwd.
+ */
+int masked_deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, const void *beta, const float *g,
+                                  const float *mask, const float *initial_state, const void *dout,
+                                  const float *dfinal_state, void *dq, void *dk, void *dv, float *dbeta, float *dg,
+                                  float *dinitial_state, int B, int H, int T, int r, int Dk, int Dv, float scale,
+                                  unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace cam_scan_fwd needs for these sizes on the current
  * device (0 on the CUDA-core path).  (size_t)-1 for sizes it rejects.
  */

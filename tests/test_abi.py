@@ -252,3 +252,25 @@ def test_chunk_bwd_argument_checks(lib):
     assert wsb(1, 2, 0, 1, 64, 64, binding.GDN_F32) == 0
     assert wsb(1, 2, 70, 9, 64, 64, binding.GDN_F32) == bad
     assert wsb(1, 2, 70, 1, 96, 64, binding.GDN_F32) == bad
+
+
+def test_masked_bwd_argument_checks(lib):
+    f = lib.masked_deltaproduct_chunk_bwd
+    u = 0x10000
+
+    def call(r=2, flags=0, Dk=64, dtype=binding.GDN_F32, mask=u, ws=u, ws_bytes=1 << 40):
+        return f(u, u, u, u, u, mask, None, u, None, u, u, u, u, u, None, 1, 2, 40, r, Dk, 64, 1.0, flags, dtype, ws,
+                 ws_bytes, None)
+
+    assert call(r=3) == 2          # r must divide 64 and Dk
+    assert call(r=16) == 2
+    assert call(flags=2) == 1      # only GDN_QK_L2NORM
+    assert call(Dk=96) == 2
+    assert call(dtype=4) == 1
+    assert call(mask=None) == 1
+    assert call(ws=None) == 4
+    assert call(ws_bytes=16) == 4
+    q = lib.masked_deltaproduct_chunk_bwd_workspace_bytes
+    per = 64 * 64 + 2 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 64 + 64
+    assert q(1, 2, 40, 2, 64, 64, binding.GDN_F32) == 4 * 2 * 2 * per  # 40 tokens: two chunks of 32
+    assert q(1, 2, 40, 3, 64, 64, binding.GDN_F32) == ctypes.c_size_t(-1).value
