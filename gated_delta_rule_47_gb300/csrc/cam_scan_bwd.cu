@@ -33,6 +33,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "gdn_internal.h"
 #include "simt_tile.cuh"
 #include "tc_util.cuh"
@@ -58,7 +60,7 @@ struct FbParams {
     // images, [BH][F+1][kImg] and [BH][F][kImg]; each image holds the 128 x 128
     // matrix row-major as two 64-column blocks of 128-byte swizzled rows
     uint8_t *Eimg, *dXimg;
-    int F, S, N, tiles;
+    int F, S, N, tiles, BH;
     float scale;
     int l2;
 };
@@ -361,27 +363,34 @@ __global__ void __launch_bounds__(kThr, 1) fb_token_kernel(FbParams p) {
 }
 
 // ====================================== 3a. token gradients on the tensor cores
-// One CTA per (frame, 128-token tile, head), bf16, Dk = Dv = 128.  Warp 0
-// loads (TMA for the K and dO tiles, bulk copies for the operand images),
-// warp 1 issues the MMAs, warps 2..5 (one TMEM lane quarter each, thread =
-// token row) form r, -d beta dR, dv, dbeta and the outputs.  The products, all
-// M = N = 128 with fp32 accumulators in TMEM:
+// Persistent CTAs over the (head, frame, 128-token tile) items, bf16,
+// Dk = Dv = 128.  Warp 0 loads (TMA for the K and dO tiles, bulk copies for
+// the operand images), warp 1 issues the MMAs, warps 2..9 form r, -d beta dR,
+// dv, dbeta and the outputs (two warps per TMEM lane quarter, thread = token
+// row, each warp half of the columns).  The products, all M = N = 128 with
+// fp32 accumulators in TMEM:
 //   KE = K E_f,  dR' = K dX_f                          (E, dX images MN-major)
 //   DK = R dX_f^T + W E_f^T,  W = -d diag(beta) dR     (by 64-column halves of Dv)
 //   DQ = dO X_f^T                                      (X_f = E_{f+1})
-// With the unit-norm flag the raw K tile is the operand and its rows' scale
-// 1/|k| is applied to KE and dR' in the epilogue (k-hat = k / |k|).
-constexpr int kTcThr = 192;
+// The next item's loads and first products (columns 0..255) start as soon as
+// the current item's last product has read its operands, while the epilogue
+// still reads DK and DQ (columns 256..511).  With the unit-norm flag the raw K
+// tile is the operand and its rows' scale 1/|k| is applied to KE and dR' in
+// the epilogue (k-hat = k / |k|).
+constexpr int kTcThr = 320;
+constexpr int kTcEpi = 256;  // epilogue threads
 constexpr int kTcRows = 128;
 constexpr uint32_t TB_A = 0;        // K tile, then dO tile: two 64-column blocks of 128 swizzled rows
 constexpr uint32_t TB_E = 32768;    // E_f image (hi | lo), then the X_f image
 constexpr uint32_t TB_DX = 98304;   // dX_f image (hi | lo)
-constexpr uint32_t TB_R = 163840;   // R, one 64-column half: hi (16 KB) | lo
+constexpr uint32_t TB_R = 163840;   // R, one 64-column half: hi (16 KB) | lo; row exchange at the end
 constexpr uint32_t TB_W = 196608;   // W = -d beta dR, one half: hi | lo
 constexpr uint32_t TB_BAR = 229376;
-enum { TBB_K = 0, TBB_E, TBB_DX, TBB_DO, TBB_X, TBB_MMA1, TBB_OPND, TBB_MMA2, TBB_MMA3, TBB_DRAIN, TBB_NUM };
-constexpr uint32_t TB_MISC = TB_BAR + 8 * TBB_NUM;  // TMEM address, then 8 reduction floats
-constexpr uint32_t TB_SMEM = TB_MISC + 48 + 1024;    // + alignment of the base to 1024 bytes
+// Every barrier but OPND completes once per item, so a wait for item j uses
+// parity j & 1; OPND completes twice per item (the two halves of Dv).
+enum { TBB_K = 0, TBB_E, TBB_DX, TBB_DO, TBB_X, TBB_MMA1, TBB_OPND, TBB_MMA2A, TBB_MMA2B, TBB_MMA3, TBB_DRAIN, TBB_NUM };
+constexpr uint32_t TB_MISC = TB_BAR + 8 * TBB_NUM;  // TMEM address, then 16 reduction floats
+constexpr uint32_t TB_SMEM = TB_MISC + 80 + 1024;    // + alignment of the base to 1024 bytes
 static_assert(TB_SMEM <= 232448, "token kernel fits the shared memory of one CTA");
 constexpr uint32_t TM_KE = 0, TM_DR = 128, TM_DK = 256, TM_DQ = 384;
 
@@ -453,16 +462,10 @@ __global__ void __launch_bounds__(kTcThr, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TB_MISC);
     float *red = reinterpret_cast<float *>(sm + TB_MISC + 16);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int f = blockIdx.x / p.tiles, tl = blockIdx.x % p.tiles, bh = blockIdx.y;
-    const int t0 = tl * kTcRows, n = min(kTcRows, p.S - t0);
-    const size_t fi = (size_t)bh * p.F + f;
-    const size_t tok0 = (size_t)bh * p.N + (size_t)f * p.S + t0;
-    const float d = p.decay[fi];
-    const uint8_t *Ei = p.Eimg + ((size_t)bh * (p.F + 1) + f) * kImg;  // E_f; E_{f+1} = X_f follows
-    const uint8_t *dXi = p.dXimg + fi * kImg;
+    const int items = p.F * p.tiles * p.BH;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < TBB_NUM; ++i) mbar_init(&bars[i], i == TBB_OPND ? 128u : 1u);
+        for (int i = 0; i < TBB_NUM; ++i) mbar_init(&bars[i], i == TBB_OPND ? (uint32_t)kTcEpi : 1u);
         fence_mbar_init();
         prefetch_tensormap(&mK);
         prefetch_tensormap(&mDO);
@@ -475,101 +478,119 @@ __global__ void __launch_bounds__(kTcThr, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tslot;
+    // item it -> (head, frame, tile), tiles fastest so that a frame's tiles run together
+    auto decode = [&](int it, int &bh, int &f, int &tl) {
+        tl = it % p.tiles;
+        f = (it / p.tiles) % p.F;
+        bh = it / (p.tiles * p.F);
+    };
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[TBB_K], 32768);
-            tma_load_4d(sm + TB_A, &mK, &bars[TBB_K], 0, t0, f, bh);
-            tma_load_4d(sm + TB_A + 16384, &mK, &bars[TBB_K], 64, t0, f, bh);
-            mbar_arrive_expect_tx(&bars[TBB_E], kImg);
-            bulk_load_global(sm + TB_E, Ei, 32768, &bars[TBB_E]);
-            bulk_load_global(sm + TB_E + 32768, Ei + 32768, 32768, &bars[TBB_E]);
-            mbar_arrive_expect_tx(&bars[TBB_DX], kImg);
-            bulk_load_global(sm + TB_DX, dXi, 32768, &bars[TBB_DX]);
-            bulk_load_global(sm + TB_DX + 32768, dXi + 32768, 32768, &bars[TBB_DX]);
-            bool armed_do = false, armed_x = false;
-            // dO over K once the first products have read it
-            if (fb_wait(&bars[TBB_MMA1], 0, 1u)) {
+            int j = 0;
+            for (int it = blockIdx.x; it < items; it += gridDim.x, ++j) {
+                int bh, f, tl;
+                decode(it, bh, f, tl);
+                const uint8_t *Ei = p.Eimg + ((size_t)bh * (p.F + 1) + f) * kImg;
+                const uint8_t *dXi = p.dXimg + ((size_t)bh * p.F + f) * kImg;
+                // the previous item's last product has read K / dO, E / X and dX
+                if (j > 0 && !fb_wait(&bars[TBB_MMA3], (j - 1) & 1, 1u)) break;
+                mbar_arrive_expect_tx(&bars[TBB_K], 32768);
+                tma_load_4d(sm + TB_A, &mK, &bars[TBB_K], 0, tl * kTcRows, f, bh);
+                tma_load_4d(sm + TB_A + 16384, &mK, &bars[TBB_K], 64, tl * kTcRows, f, bh);
+                mbar_arrive_expect_tx(&bars[TBB_E], kImg);
+                bulk_load_global(sm + TB_E, Ei, 32768, &bars[TBB_E]);
+                bulk_load_global(sm + TB_E + 32768, Ei + 32768, 32768, &bars[TBB_E]);
+                mbar_arrive_expect_tx(&bars[TBB_DX], kImg);
+                bulk_load_global(sm + TB_DX, dXi, 32768, &bars[TBB_DX]);
+                bulk_load_global(sm + TB_DX + 32768, dXi + 32768, 32768, &bars[TBB_DX]);
+                // dO over K once the first products have read it
+                if (!fb_wait(&bars[TBB_MMA1], j & 1, 1u)) break;
                 mbar_arrive_expect_tx(&bars[TBB_DO], 32768);
-                tma_load_4d(sm + TB_A, &mDO, &bars[TBB_DO], 0, t0, f, bh);
-                tma_load_4d(sm + TB_A + 16384, &mDO, &bars[TBB_DO], 64, t0, f, bh);
-                armed_do = true;
+                tma_load_4d(sm + TB_A, &mDO, &bars[TBB_DO], 0, tl * kTcRows, f, bh);
+                tma_load_4d(sm + TB_A + 16384, &mDO, &bars[TBB_DO], 64, tl * kTcRows, f, bh);
                 // X_f over E_f once both halves of the dk products have read it
-                if (fb_wait(&bars[TBB_MMA2], 0, 1u) && fb_wait(&bars[TBB_MMA2], 1, 1u)) {
-                    mbar_arrive_expect_tx(&bars[TBB_X], kImg);
-                    bulk_load_global(sm + TB_E, Ei + kImg, 32768, &bars[TBB_X]);
-                    bulk_load_global(sm + TB_E + 32768, Ei + kImg + 32768, 32768, &bars[TBB_X]);
-                    armed_x = true;
-                }
+                if (!fb_wait(&bars[TBB_MMA2B], j & 1, 1u)) break;
+                mbar_arrive_expect_tx(&bars[TBB_X], kImg);
+                bulk_load_global(sm + TB_E, Ei + kImg, 32768, &bars[TBB_X]);
+                bulk_load_global(sm + TB_E + 32768, Ei + kImg + 32768, 32768, &bars[TBB_X]);
             }
-            // every copy issued has landed before the CTA may exit
-            fb_wait(&bars[TBB_K], 0, 1u);
-            fb_wait(&bars[TBB_E], 0, 1u);
-            fb_wait(&bars[TBB_DX], 0, 1u);
-            if (armed_do) fb_wait(&bars[TBB_DO], 0, 1u);
-            if (armed_x) fb_wait(&bars[TBB_X], 0, 1u);
+            // every copy issued has landed before the CTA may exit (the last item's dq product has read them)
+            if (j > 0) fb_wait(&bars[TBB_MMA3], (j - 1) & 1, 1u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idMN = idesc_bf16(128, 128, false, true);  // B MN-major
             const uint32_t idK = idesc_bf16(128, 128, false, false);  // both K-major
-            bool ok = fb_wait(&bars[TBB_K], 0, 2u) && fb_wait(&bars[TBB_E], 0, 2u);
-            if (ok) {
-                tc_fence_after_sync();
-                int nmm = 0;
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ss(tmem + TM_KE, smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    smem_desc(sb + TB_E + part * 32768 + ks * 2048, 16384, 1024), idMN,
-                                    (nmm++) > 0);
-            }
-            ok = ok && fb_wait(&bars[TBB_DX], 0, 2u);
-            if (ok) {
-                tc_fence_after_sync();
-                int nmm = 0;
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ss(tmem + TM_DR, smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    smem_desc(sb + TB_DX + part * 32768 + ks * 2048, 16384, 1024), idMN,
-                                    (nmm++) > 0);
-                mma_commit(&bars[TBB_MMA1]);
-            }
-            for (int h = 0; h < 2 && ok; ++h) {
-                ok = fb_wait(&bars[TBB_OPND], (uint32_t)h, 3u);
+            int j = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++j) {
+                const uint32_t par = (uint32_t)(j & 1);
+                ok = fb_wait(&bars[TBB_K], par, 2u) && fb_wait(&bars[TBB_E], par, 2u);
                 if (!ok) break;
                 tc_fence_after_sync();
-                // DK += R_h dX_h^T + W_h E_h^T, each as hi.hi + hi.lo + lo.hi
+                {
+                    int nmm = 0;
 #pragma unroll
-                for (int term = 0; term < 2; ++term) {
-                    const uint32_t abase = sb + (term ? TB_W : TB_R);
-                    const uint32_t bbase = sb + (term ? TB_E : TB_DX) + h * 16384;
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int c = 0; c < 3; ++c) {
-                        const uint32_t a = abase + (c == 2 ? 16384 : 0);
-                        const uint32_t b = bbase + (c == 1 ? 32768 : 0);
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_bf16_ss(tmem + TM_DK, smem_desc(a + ks * 32, 16, 1024),
-                                        smem_desc(b + ks * 32, 16, 1024), idK, (h | term | c | ks) != 0);
-                    }
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_bf16_ss(tmem + TM_KE,
+                                        smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                        smem_desc(sb + TB_E + part * 32768 + ks * 2048, 16384, 1024), idMN,
+                                        (nmm++) > 0);
                 }
-                mma_commit(&bars[TBB_MMA2]);
-            }
-            ok = ok && fb_wait(&bars[TBB_DO], 0, 2u) && fb_wait(&bars[TBB_X], 0, 2u);
-            if (ok) {
+                ok = fb_wait(&bars[TBB_DX], par, 2u);
+                if (!ok) break;
                 tc_fence_after_sync();
-                int nmm = 0;
+                {
+                    int nmm = 0;
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ss(tmem + TM_DQ, smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    smem_desc(sb + TB_E + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    idK, (nmm++) > 0);
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_bf16_ss(tmem + TM_DR,
+                                        smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                        smem_desc(sb + TB_DX + part * 32768 + ks * 2048, 16384, 1024), idMN,
+                                        (nmm++) > 0);
+                }
+                mma_commit(&bars[TBB_MMA1]);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    ok = fb_wait(&bars[TBB_OPND], (uint32_t)h, 3u);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    // DK += R_h dX_h^T + W_h E_h^T, each as hi.hi + hi.lo + lo.hi
+#pragma unroll
+                    for (int term = 0; term < 2; ++term) {
+                        const uint32_t abase = sb + (term ? TB_W : TB_R);
+                        const uint32_t bbase = sb + (term ? TB_E : TB_DX) + h * 16384;
+#pragma unroll
+                        for (int c = 0; c < 3; ++c) {
+                            const uint32_t a = abase + (c == 2 ? 16384 : 0);
+                            const uint32_t b = bbase + (c == 1 ? 32768 : 0);
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                mma_bf16_ss(tmem + TM_DK, smem_desc(a + ks * 32, 16, 1024),
+                                            smem_desc(b + ks * 32, 16, 1024), idK, (h | term | c | ks) != 0);
+                        }
+                    }
+                    mma_commit(&bars[h ? TBB_MMA2B : TBB_MMA2A]);
+                }
+                ok = ok && fb_wait(&bars[TBB_DO], par, 2u) && fb_wait(&bars[TBB_X], par, 2u);
+                if (!ok) break;
+                tc_fence_after_sync();
+                {
+                    int nmm = 0;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_bf16_ss(tmem + TM_DQ,
+                                        smem_desc(sb + TB_A + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                        smem_desc(sb + TB_E + part * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16,
+                                                  1024),
+                                        idK, (nmm++) > 0);
+                }
                 mma_commit(&bars[TBB_MMA3]);
             }
             // every MMA issued has completed before TMEM is released
@@ -578,148 +599,171 @@ __global__ void __launch_bounds__(kTcThr, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int t = 32 * (warp & 3) + lane;  // token row = TMEM lane
-        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-        const bool valid = t < n;
-        const size_t tok = tok0 + t;
-        const __nv_bfloat16 *vrow = static_cast<const __nv_bfloat16 *>(p.v) + tok * 128;
-        const __nv_bfloat16 *krow = static_cast<const __nv_bfloat16 *>(p.k) + tok * 128;
-        const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) + tok * 128;
-        const float bt = valid ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[tok]) : 0.f;
-        float nk = 1.f, nq = 1.f;
-        if (p.l2 && valid) {
-            nk = row_norm128(krow);
-            nq = row_norm128(qrow);
-        }
-        const float sk = p.l2 ? 1.f / fmaxf(nk, 1e-12f) : 1.f;
-        float dbeta = 0.f, dec = 0.f;
-        bool ok = warp_all_ok(fb_wait(&bars[TBB_MMA1], 0, 4u));
-        for (int h = 0; h < 2; ++h) {
-            if (h == 1) ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA2], 0, 4u));
+        const int ew = warp - 2;                    // 0..7
+        const int q = warp & 3, half = ew >> 2;     // TMEM lane quarter; column half
+        const int t = 32 * q + lane;                // token row = TMEM lane
+        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        float *xch = reinterpret_cast<float *>(sm + TB_R);  // [2][128][4] row exchange at the end of an item
+        int j = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items; it += gridDim.x, ++j) {
+            int bh, f, tl;
+            decode(it, bh, f, tl);
+            const int n = min(kTcRows, p.S - tl * kTcRows);
+            const size_t fi = (size_t)bh * p.F + f;
+            const size_t tok = (size_t)bh * p.N + (size_t)f * p.S + tl * kTcRows + t;
+            const float d = p.decay[fi];
+            const bool valid = t < n;
+            const __nv_bfloat16 *vrow = static_cast<const __nv_bfloat16 *>(p.v) + tok * 128;
+            const __nv_bfloat16 *krow = static_cast<const __nv_bfloat16 *>(p.k) + tok * 128;
+            const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) + tok * 128;
+            const float bt = valid ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[tok]) : 0.f;
+            float nk = 1.f, nq = 1.f;
+            if (p.l2 && valid) {
+                nk = row_norm128(krow);
+                nq = row_norm128(qrow);
+            }
+            const float sk = p.l2 ? 1.f / fmaxf(nk, 1e-12f) : 1.f;
+            float dbeta = 0.f, dec = 0.f;
+            ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA1], j & 1, 4u));
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1) ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA2A], j & 1, 4u));
+                if (ok) {
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {  // 16 columns at a time
+                        uint32_t ke[16], dr[16];
+                        tmem_ld16(tmem + lb + TM_KE + 64 * h + 16 * cc, ke);
+                        tmem_ld16(tmem + lb + TM_DR + 64 * h + 16 * cc, dr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int c8 = 16 * cc + 8 * jj;  // column within the half
+                            float vv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (valid) unpack8(*reinterpret_cast<const uint4 *>(vrow + 64 * h + c8), vv);
+                            float rr[8], ww[8], dv8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float kt = __uint_as_float(ke[8 * jj + e]) * sk;
+                                const float drt = __uint_as_float(dr[8 * jj + e]) * sk;
+                                const float u = vv[e] - d * kt;
+                                rr[e] = bt * u;
+                                ww[e] = -d * bt * drt;
+                                dv8[e] = bt * drt;
+                                dbeta += drt * u;
+                                dec += bt * drt * kt;
+                            }
+                            if (valid)
+                                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + tok * 128 + 64 * h +
+                                                           c8) = pack8(dv8);
+                            uint4 hi, lo;
+                            const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)c8);
+                            split8(rr, hi, lo);
+                            *reinterpret_cast<uint4 *>(sm + TB_R + off) = hi;
+                            *reinterpret_cast<uint4 *>(sm + TB_R + 16384 + off) = lo;
+                            split8(ww, hi, lo);
+                            *reinterpret_cast<uint4 *>(sm + TB_W + off) = hi;
+                            *reinterpret_cast<uint4 *>(sm + TB_W + 16384 + off) = lo;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before_sync();
+                mbar_arrive(&bars[TBB_OPND]);
+            }
+            // the tile's share of ddecay (and <dX_f, E_f> on the frame's first tile)
+            float dot = 0.f;
+            if (tl == 0) {
+                const float *Eg = p.Ew + ((size_t)bh * (p.F + 1) + f) * 16384, *dXg = p.dXw + fi * 16384;
+                for (int e = threadIdx.x - 64; e < 16384; e += kTcEpi) dot += dXg[e] * Eg[e];
+            }
+            dec = warp_sum(dec);
+            dot = warp_sum(dot);
+            // the last product has completed: R and W are free for the row exchange
+            ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA3], j & 1, 4u));
+            if (lane == 0) {
+                red[ew] = dec;
+                red[8 + ew] = dot;
+            }
+            float kd = 0.f, qd = 0.f;
             if (ok) {
                 tc_fence_after_sync();
+                if (p.l2) {
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t ke[16], dr[16];
-                    tmem_ld16(tmem + lb + TM_KE + 64 * h + 16 * cc, ke);
-                    tmem_ld16(tmem + lb + TM_DR + 64 * h + 16 * cc, dr);
-                    tmem_wait_ld();
+                    for (int cc = 4 * half; cc < 4 * half + 4; ++cc) {
+                        uint32_t gk[16], gq[16];
+                        tmem_ld16(tmem + lb + TM_DK + 16 * cc, gk);
+                        tmem_ld16(tmem + lb + TM_DQ + 16 * cc, gq);
+                        tmem_wait_ld();
+                        if (valid) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int c8 = 16 * cc + 8 * j;  // column within the half
-                        float vv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        if (valid) unpack8(*reinterpret_cast<const uint4 *>(vrow + 64 * h + c8), vv);
-                        float rr[8], ww[8], dv8[8];
+                            for (int jj = 0; jj < 2; ++jj) {
+                                float kx[8], qx[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(krow + 16 * cc + 8 * jj), kx);
+                                unpack8(*reinterpret_cast<const uint4 *>(qrow + 16 * cc + 8 * jj), qx);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float kt = __uint_as_float(ke[8 * j + e]) * sk;
-                            const float drt = __uint_as_float(dr[8 * j + e]) * sk;
-                            const float u = vv[e] - d * kt;
-                            rr[e] = bt * u;
-                            ww[e] = -d * bt * drt;
-                            dv8[e] = bt * drt;
-                            dbeta += drt * u;
-                            dec += bt * drt * kt;
+                                for (int e = 0; e < 8; ++e) {
+                                    kd += kx[e] * __uint_as_float(gk[8 * jj + e]);
+                                    qd += qx[e] * __uint_as_float(gq[8 * jj + e]);
+                                }
+                            }
                         }
-                        if (valid)
-                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + tok * 128 + 64 * h + c8) =
-                                pack8(dv8);
-                        uint4 hi, lo;
-                        const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)c8);
-                        split8(rr, hi, lo);
-                        *reinterpret_cast<uint4 *>(sm + TB_R + off) = hi;
-                        *reinterpret_cast<uint4 *>(sm + TB_R + 16384 + off) = lo;
-                        split8(ww, hi, lo);
-                        *reinterpret_cast<uint4 *>(sm + TB_W + off) = hi;
-                        *reinterpret_cast<uint4 *>(sm + TB_W + 16384 + off) = lo;
                     }
                 }
-                fence_proxy_async_smem();
             }
-            tc_fence_before_sync();
-            mbar_arrive(&bars[TBB_OPND]);
-        }
-        if (ok && valid) p.dbeta[tok] = dbeta;
-        // the tile's share of ddecay (and <dX_f, E_f> on the frame's first tile)
-        float dot = 0.f;
-        if (tl == 0) {
-            const float *Eg = p.Ew + ((size_t)bh * (p.F + 1) + f) * 16384, *dXg = p.dXw + fi * 16384;
-            for (int e = threadIdx.x - 64; e < 16384; e += 128) dot += dXg[e] * Eg[e];
-        }
-        dec = warp_sum(dec);
-        dot = warp_sum(dot);
-        if (lane == 0) {
-            red[warp - 2] = dec;
-            red[4 + warp - 2] = dot;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (warp == 2 && lane == 0) {
-            float s = 0.f;
-            for (int w = 0; w < 4; ++w) s += red[4 + w] - red[w];
-            p.part[fi * p.tiles + tl] = s;
-        }
-        // dk and dq, through the unit-norm map when asked
-        ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA3], 0, 4u));
-        if (ok) {
-            tc_fence_after_sync();
-            float kd = 0.f, qd = 0.f;
-            if (p.l2) {
+            xch[(half * 128 + t) * 4 + 0] = dbeta;
+            xch[(half * 128 + t) * 4 + 1] = kd;
+            xch[(half * 128 + t) * 4 + 2] = qd;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            dbeta += xch[((half ^ 1) * 128 + t) * 4 + 0];
+            kd += xch[((half ^ 1) * 128 + t) * 4 + 1];
+            qd += xch[((half ^ 1) * 128 + t) * 4 + 2];
+            if (ew == 0 && lane == 0) {
+                float s = 0.f;
+                for (int w = 0; w < 8; ++w) s += red[8 + w] - red[w];
+                p.part[fi * p.tiles + tl] = s;
+            }
+            if (ok && valid && half == 0) p.dbeta[tok] = dbeta;
+            if (ok) {
+                kd *= sk;                           // k-hat . dk
+                qd *= p.scale / fmaxf(nq, 1e-12f);  // q-hat . dq
+                const float sq = 1.f / fmaxf(nq, 1e-12f);
 #pragma unroll 1
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 4 * half; cc < 4 * half + 4; ++cc) {
                     uint32_t gk[16], gq[16];
                     tmem_ld16(tmem + lb + TM_DK + 16 * cc, gk);
                     tmem_ld16(tmem + lb + TM_DQ + 16 * cc, gq);
                     tmem_wait_ld();
                     if (valid) {
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            float kx[8], qx[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(krow + 16 * cc + 8 * j), kx);
-                            unpack8(*reinterpret_cast<const uint4 *>(qrow + 16 * cc + 8 * j), qx);
+                        for (int jj = 0; jj < 2; ++jj) {
+                            float kx[8], qx[8], ok8[8], oq8[8];
+                            if (p.l2) {
+                                unpack8(*reinterpret_cast<const uint4 *>(krow + 16 * cc + 8 * jj), kx);
+                                unpack8(*reinterpret_cast<const uint4 *>(qrow + 16 * cc + 8 * jj), qx);
+                            }
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                kd += kx[e] * __uint_as_float(gk[8 * j + e]);
-                                qd += qx[e] * __uint_as_float(gq[8 * j + e]);
+                                float xk = __uint_as_float(gk[8 * jj + e]);
+                                float xq = p.scale * __uint_as_float(gq[8 * jj + e]);
+                                if (p.l2) {
+                                    xk = nk < 1e-12f ? xk * 1e12f : (xk - kx[e] * sk * kd) / nk;
+                                    xq = nq < 1e-12f ? xq * 1e12f : (xq - qx[e] * sq * qd) / nq;
+                                }
+                                ok8[e] = xk;
+                                oq8[e] = xq;
                             }
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dk) + tok * 128 + 16 * cc +
+                                                       8 * jj) = pack8(ok8);
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dq) + tok * 128 + 16 * cc +
+                                                       8 * jj) = pack8(oq8);
                         }
                     }
                 }
-                kd *= sk;                              // k-hat . dk
-                qd *= p.scale / fmaxf(nq, 1e-12f);     // q-hat . dq
             }
-            const float sq = 1.f / fmaxf(nq, 1e-12f);
-#pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                uint32_t gk[16], gq[16];
-                tmem_ld16(tmem + lb + TM_DK + 16 * cc, gk);
-                tmem_ld16(tmem + lb + TM_DQ + 16 * cc, gq);
-                tmem_wait_ld();
-                if (valid) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        float kx[8], qx[8], ok8[8], oq8[8];
-                        if (p.l2) {
-                            unpack8(*reinterpret_cast<const uint4 *>(krow + 16 * cc + 8 * j), kx);
-                            unpack8(*reinterpret_cast<const uint4 *>(qrow + 16 * cc + 8 * j), qx);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            float xk = __uint_as_float(gk[8 * j + e]);
-                            float xq = p.scale * __uint_as_float(gq[8 * j + e]);
-                            if (p.l2) {
-                                xk = nk < 1e-12f ? xk * 1e12f : (xk - kx[e] * sk * kd) / nk;
-                                xq = nq < 1e-12f ? xq * 1e12f : (xq - qx[e] * sq * qd) / nq;
-                            }
-                            ok8[e] = xk;
-                            oq8[e] = xq;
-                        }
-                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dk) + tok * 128 + 16 * cc + 8 * j) =
-                            pack8(ok8);
-                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dq) + tok * 128 + 16 * cc + 8 * j) =
-                            pack8(oq8);
-                    }
-                }
-            }
+            tc_fence_before_sync();
+            // the exchange area is R / W again for the next item, and red is reused
+            asm volatile("bar.sync 1, 256;" ::: "memory");
         }
     }
     tc_fence_before_sync();
@@ -964,6 +1008,7 @@ int run(const CamScanBwdArgs &a, cudaStream_t st) {
     p.S = a.S;
     p.N = a.F * a.S;
     p.tiles = tiles;
+    p.BH = BH;
     p.scale = a.scale;
     p.l2 = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
     constexpr size_t s1 = frame_smem(DK, DV), s2 = fchain_smem(DK), s3 = token_smem(DK, DV);
@@ -992,7 +1037,9 @@ int run(const CamScanBwdArgs &a, cudaStream_t st) {
         if (cudaFuncSetAttribute(fb_token_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TB_SMEM) !=
             cudaSuccess)
             return GDN_ERR_CUDA;
-        fb_token_tc_kernel<<<dim3((unsigned)(a.F * p.tiles), (unsigned)BH), kTcThr, TB_SMEM, st>>>(mK, mDO, p);
+        const long long items = (long long)a.F * p.tiles * BH;
+        const int grid = (int)std::min<long long>(items, (long long)device_sm_count());
+        fb_token_tc_kernel<<<(unsigned)grid, kTcThr, TB_SMEM, st>>>(mK, mDO, p);
     } else {
         fb_token_kernel<T, DK, DV><<<dim3((unsigned)(a.F * tiles), (unsigned)BH), kThr, s3, st>>>(p);
     }
