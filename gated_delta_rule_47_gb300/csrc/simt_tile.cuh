@@ -70,6 +70,17 @@ __device__ __forceinline__ void zero(float (&a)[TI][TJ]) {
         for (int j = 0; j < TJ; ++j) a[i][j] = 0.f;
 }
 
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte
+// aligned), completed by cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(sdst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // Sum over the 16 lanes that hold one row of a tile (lanes differing in bits 0..3).
 __device__ __forceinline__ float row_sum16(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 8);

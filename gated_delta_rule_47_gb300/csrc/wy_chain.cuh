@@ -27,7 +27,7 @@ struct WyChainParams {
 
 template <int DK, int SLICE>
 constexpr size_t wy_chain_smem() {
-    return sizeof(float) * ((size_t)DK * (SLICE + 1) + tile::kC * (DK + 1) + tile::kC * (SLICE + 1));
+    return sizeof(float) * ((size_t)DK * (SLICE + 1) + tile::kC * (DK + 4) + tile::kC * (SLICE + 4));
 }
 
 // blockIdx.x: SLICE-column slice of the value dimension; blockIdx.y: head;
@@ -35,11 +35,14 @@ constexpr size_t wy_chain_smem() {
 template <int DK, int DV, int SLICE>
 __global__ void __launch_bounds__(kChainThr) wy_chain_kernel(WyChainParams p) {
     using namespace tile;
-    extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LS = SLICE + 1;
+    extern __shared__ __align__(16) float sm[];
+    // St rows are odd-strided (conflict-free both ways); Wt and Ut rows are
+    // 16-byte aligned for the asynchronous copies that stage them
+    constexpr int LS = SLICE + 1, LW = DK + 4, LU = SLICE + 4;
+    constexpr int TI = DK / 16, TJ = SLICE / 16;
     float *St = sm;             // [DK][LS]  state (or gradient) slice
-    float *Wt = St + DK * LS;   // [kC][LK]  W or Kd of the chunk
-    float *Ut = Wt + kC * LK;   // [kC][LS]  U / Vn or Kd dS'
+    float *Wt = St + DK * LS;   // [kC][LW]  W or Kd of the chunk
+    float *Ut = Wt + kC * LW;   // [kC][LU]  U / Vn or Kd dS'
     const int col0 = blockIdx.x * SLICE, bh = blockIdx.y, role = blockIdx.z;
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int NT = p.NT;
@@ -54,59 +57,74 @@ __global__ void __launch_bounds__(kChainThr) wy_chain_kernel(WyChainParams p) {
         const int c = role == 0 ? s : NT - 1 - s;
         const size_t ci = (size_t)bh * NT + c;
         const float el = expf(p.Gw[ci * kC + kC - 1]);
+        const float *Wg = p.Ww + ci * kC * DK, *Kdg = p.Kdw + ci * kC * DK;
+        const float *first = role == 0 ? Wg : Kdg, *second = role == 0 ? Kdg : Wg;
+        for (int e = tid; e < kC * DK / 4; e += kChainThr) {
+            const int m = e / (DK / 4), c4 = 4 * (e % (DK / 4));
+            cp_async16(Wt + m * LW + c4, first + (size_t)m * DK + c4);
+        }
+        if (role == 0) {
+            const float *Ug = p.Uw + ci * kC * DV;
+            for (int e = tid; e < kC * SLICE / 4; e += kChainThr) {
+                const int m = e / (SLICE / 4), c4 = 4 * (e % (SLICE / 4));
+                cp_async16(Ut + m * LU + c4, Ug + (size_t)m * DV + col0 + c4);
+            }
+        }
+        // the reverse chain's B slice, loaded now and used at the end of the step
+        float bpre[TI][TJ];
+        if (role == 1) {
+            const float *Bg = p.Bw + ci * DK * DV;
+#pragma unroll
+            for (int i = 0; i < TI; ++i)
+#pragma unroll
+                for (int j = 0; j < TJ; ++j) bpre[i][j] = Bg[(size_t)(ty + 16 * i) * DV + col0 + tx + 16 * j];
+        }
         float *snap = (role == 0 ? p.Sw : p.dSw) + ci * DK * DV;
         for (int e = tid; e < DK * SLICE; e += kChainThr) {
             const int m = e / SLICE, n = e % SLICE;
             snap[(size_t)m * DV + col0 + n] = St[m * LS + n];
         }
-        const float *Wg = p.Ww + ci * kC * DK, *Kdg = p.Kdw + ci * kC * DK;
-        const float *first = role == 0 ? Wg : Kdg, *second = role == 0 ? Kdg : Wg;
-        for (int e = tid; e < kC * DK; e += kChainThr) Wt[(e / DK) * LK + e % DK] = first[e];
-        if (role == 0) {
-            const float *Ug = p.Uw + ci * kC * DV;
-            for (int e = tid; e < kC * SLICE; e += kChainThr) {
-                const int m = e / SLICE, n = e % SLICE;
-                Ut[m * LS + n] = Ug[(size_t)m * DV + col0 + n];
-            }
-        }
+        cp_async_wait_all();
         __syncthreads();
         // role 0: Vn = U - W S;  role 1: Y = Kd dS'
         {
-            float acc[4][SLICE / 16];
+            float acc[4][TJ];
             zero(acc);
-            mm<kChainThr, 4, SLICE / 16>(acc, Wt, LK, 1, St, LS, 1, DK);
+            mm<kChainThr, 4, TJ>(acc, Wt, LW, 1, St, LS, 1, DK);
             float *Vng = p.Vnw + ci * kC * DV;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < SLICE / 16; ++j) {
+                for (int j = 0; j < TJ; ++j) {
                     const int m = ty + 16 * i, n = tx + 16 * j;
                     if (role == 0) {
-                        const float vn = Ut[m * LS + n] - acc[i][j];
+                        const float vn = Ut[m * LU + n] - acc[i][j];
                         Vng[(size_t)m * DV + col0 + n] = vn;
-                        Ut[m * LS + n] = vn;
+                        Ut[m * LU + n] = vn;
                     } else {
-                        Ut[m * LS + n] = acc[i][j];
+                        Ut[m * LU + n] = acc[i][j];
                     }
                 }
         }
         __syncthreads();
-        for (int e = tid; e < kC * DK; e += kChainThr) Wt[(e / DK) * LK + e % DK] = second[e];
+        for (int e = tid; e < kC * DK / 4; e += kChainThr) {
+            const int m = e / (DK / 4), c4 = 4 * (e % (DK / 4));
+            cp_async16(Wt + m * LW + c4, second + (size_t)m * DK + c4);
+        }
+        cp_async_wait_all();
         __syncthreads();
         // role 0: S = e^{gl} S + Kd^T Vn;  role 1: dS = e^{gl} dS' - W^T Y + B
         {
-            float acc[DK / 16][SLICE / 16];
+            float acc[TI][TJ];
             zero(acc);
-            mm<kChainThr, DK / 16, SLICE / 16>(acc, Wt, 1, LK, Ut, LS, 1, kC);
-            const float *Bg = p.Bw + ci * DK * DV;
+            mm<kChainThr, TI, TJ>(acc, Wt, 1, LW, Ut, LU, 1, kC);
 #pragma unroll
-            for (int i = 0; i < DK / 16; ++i)
+            for (int i = 0; i < TI; ++i)
 #pragma unroll
-                for (int j = 0; j < SLICE / 16; ++j) {
+                for (int j = 0; j < TJ; ++j) {
                     const int m = ty + 16 * i, n = tx + 16 * j;
                     const float old = St[m * LS + n];
-                    St[m * LS + n] = role == 0 ? el * old + acc[i][j]
-                                               : el * old - acc[i][j] + Bg[(size_t)m * DV + col0 + n];
+                    St[m * LS + n] = role == 0 ? el * old + acc[i][j] : el * old - acc[i][j] + bpre[i][j];
                 }
         }
         __syncthreads();
