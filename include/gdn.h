@@ -423,11 +423,17 @@ size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, 
  *   dout    [B,H,N,Dv] dtype;  dfinal_state [B,H,Dk,Dv] fp32 or NULL (= zero)
  *   dq, dk [B,H,N,Dk], dv [B,H,N,Dv] dtype;  dbeta [B,H,N] fp32;
  *   ddecay [B,H,F] fp32;  dinitial_state [B,H,Dk,Dv] fp32 or NULL
+ *   flags   GDN_QK_L2NORM, and GDN_PATH_SIMT to keep every product on the
+ *           CUDA cores
  *   workspace: cam_scan_bwd_workspace_bytes bytes, 16-byte aligned.
- * CUDA-core kernels, fp32 arithmetic, four launches: the frame products (one
- * CTA per frame, head and product), the forward state chain and the reverse
- * gradient chain side by side (32 value columns per CTA), the token
- * gradients (one CTA per 64-token tile), then each frame's ddecay.
+ * Four launches: the frame products (one CTA per frame, head and product),
+ * the forward state chain and the reverse gradient chain side by side (32
+ * value columns per CTA, fp32 on the CUDA cores), the token gradients, then
+ * each frame's ddecay.  For bf16 with Dk = Dv = 128 on an sm_10x device the
+ * frame products and the token gradients run on tcgen05 (fp32 accumulators
+ * in TMEM; the fp32 operands split into bf16 hi + lo, products formed as
+ * hi.hi + hi.lo + lo.hi; the token kernel persistent over 128-token tiles);
+ * otherwise on the CUDA cores in fp32 (64-token tiles).
  */
 int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
                  const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
