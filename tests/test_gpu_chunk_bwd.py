@@ -139,3 +139,32 @@ def test_full_size_sampled_heads():
     ref = oracle.gdn_bwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], heads(do, idx))
     for name, x, y in zip(NAMES[:5], got[:5], ref[:5]):
         assert rel_err(heads(x, idx).cpu(), y) <= TOL_BF16, name
+
+
+@pytest.mark.parametrize("cut", [37, 64, 100])
+def test_split_and_resume(cut):
+    """The backward over T tokens equals two calls chained through the state
+    arguments: the tail's backward given the forward state at the cut (and the
+    final-state gradient), then the head's backward given the tail's
+    initial-state gradient as its final-state gradient; the cut need not fall
+    on a chunk boundary."""
+    T = 150
+    inp, do, dsf = grads_case(1, 2, T, 128, 128, "f32", True, seed=31)
+    d = to_dev(inp)
+    dsf = dsf.cuda()
+    full = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"], dsf,
+                                 l2norm=True, need_dinitial=True)
+    head = {k: (v[:, :, :cut].contiguous() if k != "initial_state" else v) for k, v in d.items()}
+    tail = {k: (v[:, :, cut:].contiguous() if k != "initial_state" else v) for k, v in d.items()}
+    _, s_cut = binding.gdn_chunk_fwd(head["q"], head["k"], head["v"], head["beta"], head["g"],
+                                     initial_state=d["initial_state"], output_final_state=True, l2norm=True)
+    gt = binding.gdn_chunk_bwd(tail["q"], tail["k"], tail["v"], tail["beta"], tail["g"],
+                               do[:, :, cut:].contiguous().cuda(), s_cut, dsf, l2norm=True, need_dinitial=True)
+    gh = binding.gdn_chunk_bwd(head["q"], head["k"], head["v"], head["beta"], head["g"],
+                               do[:, :, :cut].contiguous().cuda(), d["initial_state"], gt[5], l2norm=True,
+                               need_dinitial=True)
+    torch.cuda.synchronize()
+    for i, name in enumerate(NAMES[:5]):
+        joined = torch.cat([gh[i], gt[i]], dim=2)
+        assert rel_err(joined, full[i].double().cpu().numpy()) <= TOL_F32, name
+    assert rel_err(gh[5], full[5].double().cpu().numpy()) <= TOL_F32
