@@ -55,8 +55,9 @@ struct BwdParams {
     void *dq, *dk, *dv;
     float *dbeta, *dg, *ds0;
     // workspace, per (head, chunk): T [64][64], W [64][Dk], U [64][Dv], Kd [64][Dk],
-    // B [Dk][Dv], S [Dk][Dv], dS' [Dk][Dv], Vn [64][Dv], gamma [64]
-    float *Tw, *Ww, *Uw, *Kdw, *Bw, *Sw, *dSw, *Vnw, *Gw;
+    // B [Dk][Dv], S [Dk][Dv], dS' [Dk][Dv], Vn [64][Dv], gamma [64], and the
+    // products P^ [64][64] and K K^T [64][64] for the gradient kernel
+    float *Tw, *Ww, *Uw, *Kdw, *Bw, *Sw, *dSw, *Vnw, *Gw, *Pw, *KKw;
     int T, r, Ct, NT;
     float scale;
     int l2;
@@ -122,11 +123,13 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
         float acc[2][4];
         zero(acc);
         mm<kThr, 2, 4>(acc, Ks, LK, 1, Ks, 1, LK, DK);
+        float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int a = ty + 32 * i, b = tx + 16 * j;
+                KKg[a * kC + b] = acc[i][j];
                 Xa[a * LC + b] = b < a ? bet[a] * expf(gam[a] - gam[b]) * acc[i][j] : 0.f;
             }
     }
@@ -185,12 +188,16 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
         float acc[2][4];
         zero(acc);
         mm<kThr, 2, 4>(acc, Qs, LK, 1, Ks, 1, LK, DK);
+        float *Pg = p.Pw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int qi = ty + 32 * i, b = tx + 16 * j, rho = qi * r + r - 1;
-                Xa[qi * LC + b] = (qi < ch.ntok && b <= rho) ? p.scale * expf(gam[rho] - gam[b]) * acc[i][j] : 0.f;
+                const float x =
+                    (qi < ch.ntok && b <= rho) ? p.scale * expf(gam[rho] - gam[b]) * acc[i][j] : 0.f;
+                Xa[qi * LC + b] = x;
+                Pg[qi * kC + b] = x;
             }
     }
     __syncthreads();
@@ -299,20 +306,13 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         }
     }
 
-    // 2. P^ into Xa, T into Xb
+    // 2. P^ (formed by the WY kernel) into Xa, T into Xb
     {
-        float acc[2][4];
-        zero(acc);
-        mm<kThr, 2, 4>(acc, Qs, LK, 1, Ks, 1, LK, DK);
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int qi = ty + 32 * i, b = tx + 16 * j, rho = qi * r + r - 1;
-                Xa[qi * LC + b] = (qi < ntok && b <= rho) ? p.scale * expf(gam[rho] - gam[b]) * acc[i][j] : 0.f;
-            }
-        const float *Tg = p.Tw + ch.ci * kC * kC;
-        for (int e = tid; e < kC * kC; e += kThr) Xb[(e / kC) * LC + e % kC] = Tg[e];
+        const float *Pg = p.Pw + ch.ci * kC * kC, *Tg = p.Tw + ch.ci * kC * kC;
+        for (int e = tid; e < kC * kC; e += kThr) {
+            Xa[(e / kC) * LC + e % kC] = Pg[e];
+            Xb[(e / kC) * LC + e % kC] = Tg[e];
+        }
     }
     __syncthreads();
 
@@ -378,9 +378,14 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     {
         float ta[2][4], tk[2][4];
         zero(ta);
-        zero(tk);
         mm<kThr, 2, 4>(ta, Hs, LV, 1, Vns, 1, LV, DV);
-        mm<kThr, 2, 4>(tk, Ks, LK, 1, Ks, 1, LK, DK);
+        {  // K K^T, formed by the WY kernel
+            const float *KKg = p.KKw + ch.ci * kC * kC;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tk[i][j] = KKg[(ty + 32 * i) * kC + tx + 16 * j];
+        }
         float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -421,41 +426,11 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     mm<kThr, 2, TK>(accDQ, Xa, LC, 1, Ks, LK, 1, kC);
     __syncthreads();
 
-    // 8. through the state entering the chunk (staged in halves of Dk rows in Vns)
-    {
-        float accKS[2][TV], accQS[2][TV];
-        zero(accKS);
-        zero(accQS);
-        for (int h = 0; h < NH; ++h) {
-            for (int e = tid; e < 64 * DV; e += kThr) Vns[(e / DV) * LV + e % DV] = Sg[(size_t)64 * h * DV + e];
-            __syncthreads();
-            mm<kThr, 2, TV>(accKS, Ks + 64 * h, LK, 1, Vns, LV, 1, 64);
-            mm<kThr, 2, TV>(accQS, Qs + 64 * h, LK, 1, Vns, LV, 1, 64);
-            __syncthreads();
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int b = ty + 32 * i;
-            float rb = 0.f, rg = 0.f, rq = 0.f;
-#pragma unroll
-            for (int j = 0; j < TV; ++j) {
-                const int n = tx + 16 * j;
-                const float x = Hs[b * LV + n];
-                const float vv = b < nrows ? ld_f(vp + (size_t)b * DV + n) : 0.f;
-                rb += x * (vv - eg[b] * accKS[i][j]);
-                rg += x * accKS[i][j];
-                rq += dOs[b * LV + n] * accQS[i][j];
-            }
-            rb = row_sum16(rb);
-            rg = row_sum16(rg);
-            rq = row_sum16(rq);
-            if (tx == 0) {
-                dbet[b] += rb;
-                rowg[b] -= bet[b] * eg[b] * rg;
-                if (b < ntok) qg[b] += p.scale * eg[b * r + r - 1] * rq;
-            }
-        }
-    }
+    // 8. through the state entering the chunk (staged in 64-row blocks of Dk in Vns):
+    //    dq += diag(scale e^{gamma_rho}) dO S^T and dk -= diag(beta e^gamma) dR S^T.  The
+    //    same two products give the dots the decay and beta gradients need:
+    //    (S^T q_i).do_i = q_i.(S do_i) and (S^T k_b).dR_b = k_b.(S dR_b).
+    float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
     for (int h = 0; h < NH; ++h) {
         for (int e = tid; e < 64 * DV; e += kThr) Vns[(e / DV) * LV + e % DV] = Sg[(size_t)64 * h * DV + e];
         __syncthreads();
@@ -471,11 +446,31 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
             const float sk = bet[m] * eg[m];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                const int c = 64 * h + tx + 16 * j;
                 accDQ[i][4 * h + j] += sq * t1[i][j];
                 accDK[i][4 * h + j] -= sk * t2[i][j];
+                rq[i] += Qs[m * LK + c] * t1[i][j];
+                rk[i] += Ks[m * LK + c] * t2[i][j];
             }
         }
         __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int b = ty + 32 * i;
+        float rv = 0.f;  // dR_b . v_b
+#pragma unroll
+        for (int j = 0; j < TV; ++j) {
+            const int n = tx + 16 * j;
+            rv += Hs[b * LV + n] * (b < nrows ? ld_f(vp + (size_t)b * DV + n) : 0.f);
+        }
+        rv = row_sum16(rv);
+        const float sq = row_sum16(rq[i]), skd = row_sum16(rk[i]);
+        if (tx == 0) {
+            dbet[b] += rv - eg[b] * skd;
+            rowg[b] -= bet[b] * eg[b] * skd;
+            if (b < ntok) qg[b] += p.scale * eg[b * r + r - 1] * sq;
+        }
     }
     __syncthreads();
 
@@ -543,7 +538,7 @@ constexpr size_t grad_smem(int DK, int DV) {
 
 // Workspace floats per (head, chunk).
 size_t per_chunk_floats(int Dk, int Dv) {
-    return (size_t)kC * kC + 2 * (size_t)kC * Dk + 2 * (size_t)kC * Dv + 3 * (size_t)Dk * Dv + kC;
+    return 3 * (size_t)kC * kC + 2 * (size_t)kC * Dk + 2 * (size_t)kC * Dv + 3 * (size_t)Dk * Dv + kC;
 }
 
 template <typename T, int DK, int DV>
@@ -575,6 +570,8 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
     p.dSw = p.Sw + nc * DK * DV;
     p.Vnw = p.dSw + nc * DK * DV;
     p.Gw = p.Vnw + nc * kC * DV;
+    p.Pw = p.Gw + nc * kC;
+    p.KKw = p.Pw + nc * kC * kC;
     p.T = a.T;
     p.r = a.r;
     p.Ct = Ct;

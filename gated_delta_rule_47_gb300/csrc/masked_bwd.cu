@@ -39,7 +39,8 @@ struct MbParams {
     const float *g, *mask, *s0, *dsf;
     void *dq, *dk, *dv;
     float *dbeta, *dg, *ds0;
-    float *Tw, *Ww, *Uw, *Kdw, *Bw, *Sw, *dSw, *Vnw, *Gw;  // as the chunk backward's workspace
+    // as the chunk backward's workspace (P^ and Kr Kw^T in the last two)
+    float *Tw, *Ww, *Uw, *Kdw, *Bw, *Sw, *dSw, *Vnw, *Gw, *Pw, *KKw;
     int T, r, lr, lsl, Ct, NT;                              // lr = log2 r, lsl = log2 (Dk / r)
     float scale;
     int l2;
@@ -149,11 +150,13 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
         float acc[2][4];
         zero(acc);
         mm<kThr, 2, 4>(acc, Kr, LX, 1, Kw, 1, LK, DK);
+        float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int a = ty + 32 * i, b = tx + 16 * j;
+                KKg[a * kC + b] = acc[i][j];
                 Xa[a * LC + b] = (b >> p.lr) < (a >> p.lr) ? bet[a] * expf(gam[a] - gam[b]) * acc[i][j] : 0.f;
             }
     }
@@ -204,13 +207,16 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
         float acc[2][4];
         zero(acc);
         mm<kThr, 2, 4>(acc, Qs, LK, 1, Kw, 1, LK, DK);
+        float *Pg = p.Pw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int t = ty + 32 * i, b = tx + 16 * j;
-                Xa[t * LC + b] =
+                const float x =
                     (t < ch.ntok && (b >> p.lr) <= t) ? p.scale * expf(gam[t * r] - gam[b]) * acc[i][j] : 0.f;
+                Xa[t * LC + b] = x;
+                Pg[t * kC + b] = x;
             }
     }
     __syncthreads();
@@ -321,21 +327,13 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
             lastg[b] = w;
         }
     }
-    // 2. P^ into Xa, T into Xb
+    // 2. P^ (formed by the WY kernel) into Xa, T into Xb
     {
-        float acc[2][4];
-        zero(acc);
-        mm_f<kThr, 2, 4>(acc, Sm{Qs, LK, 1}, Tr<SubKey<true>>{KW, 0}, DK);
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int qi = ty + 32 * i, b = tx + 16 * j;
-                Xa[qi * LC + b] =
-                    (qi < ntok && (b >> lr) <= qi) ? p.scale * expf(gam[qi * r] - gam[b]) * acc[i][j] : 0.f;
-            }
-        const float *Tg = p.Tw + ch.ci * kC * kC;
-        for (int e = tid; e < kC * kC; e += kThr) Xb[(e / kC) * LC + e % kC] = Tg[e];
+        const float *Pg = p.Pw + ch.ci * kC * kC, *Tg = p.Tw + ch.ci * kC * kC;
+        for (int e = tid; e < kC * kC; e += kThr) {
+            Xa[(e / kC) * LC + e % kC] = Pg[e];
+            Xb[(e / kC) * LC + e % kC] = Tg[e];
+        }
     }
     __syncthreads();
     // 3. dVn = Kd dS' + P^^T dO into Hs
@@ -393,9 +391,14 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     {
         float ta[2][4], tk[2][4];
         zero(ta);
-        zero(tk);
         mm<kThr, 2, 4>(ta, Hs, LV, 1, Vns, 1, LX, DV);
-        mm_f<kThr, 2, 4>(tk, KR, Tr<SubKey<true>>{KW, 0}, DK);
+        {  // Kr Kw^T, formed by the WY kernel
+            const float *KKg = p.KKw + ch.ci * kC * kC;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tk[i][j] = KKg[(ty + 32 * i) * kC + tx + 16 * j];
+        }
         float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -447,41 +450,10 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     zero(accDQ);
     mm_f<kThr, 2, TK>(accDQ, Sm{Xa, LC, 1}, KW, kC);
     __syncthreads();
-    // 8. through the state entering the chunk (staged in 64-row blocks of Dk in Vns)
-    {
-        float accKS[2][TV], accQS[2][TV];
-        zero(accKS);
-        zero(accQS);
-        for (int h = 0; h < NH; ++h) {
-            for (int e = tid; e < 64 * DV; e += kThr) Vns[(e / DV) * LX + e % DV] = Sg[(size_t)64 * h * DV + e];
-            __syncthreads();
-            mm_f<kThr, 2, TV>(accKS, Off<SubKey<false>>{KR, 64 * h}, Sm{Vns, LX, 1}, 64);
-            mm<kThr, 2, TV>(accQS, Qs + 64 * h, LK, 1, Vns, LX, 1, 64);
-            __syncthreads();
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int b = ty + 32 * i;
-            float rb = 0.f, rg = 0.f, rq = 0.f;
-#pragma unroll
-            for (int j = 0; j < TV; ++j) {
-                const int n = tx + 16 * j;
-                const float x = Hs[b * LV + n];
-                const float vv = b < nrows ? ld_f(vp + (size_t)(b >> lr) * DV + n) : 0.f;
-                rb += x * (vv - eg[b] * accKS[i][j]);
-                rg += x * accKS[i][j];
-                rq += dOs[b * LV + n] * accQS[i][j];
-            }
-            rb = row_sum16(rb);
-            rg = row_sum16(rg);
-            rq = row_sum16(rq);
-            if (tx == 0) {
-                dbet[b] += rb;
-                rowg[b] -= bet[b] * eg[b] * rg;
-                if (b < ntok) qg[b] += p.scale * eg[b * r] * rq;
-            }
-        }
-    }
+    // 8. through the state entering the chunk (staged in 64-row blocks of Dk in Vns):
+    //    dq += diag(scale e^{gamma}) dO S^T and dKr -= diag(beta e^gamma) dR S^T; the same
+    //    products give (S^T q_t).do_t = q_t.(S do_t) and (S^T kr_b).dR_b = kr_b.(S dR_b).
+    float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
     for (int h = 0; h < NH; ++h) {
         for (int e = tid; e < 64 * DV; e += kThr) Vns[(e / DV) * LX + e % DV] = Sg[(size_t)64 * h * DV + e];
         __syncthreads();
@@ -497,12 +469,34 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
             const float sk = bet[m] * eg[m];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                const int c = 64 * h + tx + 16 * j;
                 accDQ[i][4 * h + j] += sq * t1[i][j];
-                accD[i][4 * h + j] -= wr(m, 64 * h + tx + 16 * j) * sk * t2[i][j];
+                accD[i][4 * h + j] -= wr(m, c) * sk * t2[i][j];
+                rq[i] += Qs[m * LK + c] * t1[i][j];
+                rk[i] += KR(m, c) * t2[i][j];
             }
         }
         __syncthreads();
     }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int b = ty + 32 * i;
+        float rv = 0.f;  // dR_b . v_(token of b)
+#pragma unroll
+        for (int j = 0; j < TV; ++j) {
+            const int n = tx + 16 * j;
+            rv += Hs[b * LV + n] * (b < nrows ? ld_f(vp + (size_t)(b >> lr) * DV + n) : 0.f);
+        }
+        rv = row_sum16(rv);
+        const float sq = row_sum16(rq[i]), skd = row_sum16(rk[i]);
+        if (tx == 0) {
+            dbet[b] += rv - eg[b] * skd;
+            rowg[b] -= bet[b] * eg[b] * skd;
+            if (b < ntok) qg[b] += p.scale * eg[b * r] * sq;
+        }
+    }
+    __syncthreads();
+
     // 9. dgamma in a fixed order, dg its reverse cumulative sum; dbeta and dv by token
     if (tid < kC) {
         const int a = tid;
@@ -597,7 +591,7 @@ constexpr size_t mgrad_smem(int DK, int DV) {
 }
 
 size_t per_chunk_floats(int Dk, int Dv) {
-    return (size_t)kC * kC + 2 * (size_t)kC * Dk + 2 * (size_t)kC * Dv + 3 * (size_t)Dk * Dv + kC;
+    return 3 * (size_t)kC * kC + 2 * (size_t)kC * Dk + 2 * (size_t)kC * Dv + 3 * (size_t)Dk * Dv + kC;
 }
 
 int ilog2(int x) {
@@ -636,6 +630,8 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
     p.dSw = p.Sw + nc * DK * DV;
     p.Vnw = p.dSw + nc * DK * DV;
     p.Gw = p.Vnw + nc * kC * DV;
+    p.Pw = p.Gw + nc * kC;
+    p.KKw = p.Pw + nc * kC * kC;
     p.T = a.T;
     p.r = a.r;
     p.lr = ilog2(a.r);

@@ -209,7 +209,7 @@ int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, c
 /*
  * Bytes of device workspace masked_deltaproduct_chunk_bwd needs: per head and
  * chunk of 64 / r tokens the chunk's WY factors, the state entering it and the
- * gradient of the state leaving it (about 340 KB at Dk = Dv = 128).  0 when
+ * gradient of the state leaving it (about 370 KB at Dk = Dv = 128).  0 when
  * T = 0; (size_t)-1 for sizes it rejects.
  */
 size_t masked_deltaproduct_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype);
@@ -347,7 +347,7 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
 /*
  * Bytes of device workspace gdn_chunk_bwd / deltaproduct_chunk_bwd need
  * (r = 1 for GDN): per head and chunk of floor(64 / r) tokens, the chunk's
- * WY factors, the states entering it and their gradients (about 340 KB at
+ * WY factors, the states entering it and their gradients (about 370 KB at
  * Dk = Dv = 128).  0 when T = 0; (size_t)-1 for sizes they reject.
  */
 size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv, int dtype);

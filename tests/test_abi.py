@@ -246,7 +246,7 @@ def test_chunk_bwd_argument_checks(lib):
     assert lib.gdn_chunk_bwd(u, u, u, u, u, None, u, None, None, u, u, u, u, None, 1, 2, 5, 64, 64, 1.0, 0,
                              binding.GDN_F32, u, 1 << 40, None) == 1  # dq missing
     wsb = lib.gdn_chunk_bwd_workspace_bytes
-    per = 64 * 64 + 2 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 64 + 64  # floats per head and chunk at D = 64
+    per = 3 * 64 * 64 + 2 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 64 + 64  # floats per head and chunk at D = 64
     assert wsb(1, 2, 70, 1, 64, 64, binding.GDN_F32) == 4 * 2 * 2 * per  # 70 tokens: 2 chunks of 64
     assert wsb(1, 2, 70, 3, 64, 64, binding.GDN_F32) == 4 * 2 * 4 * per  # 21 tokens per chunk
     assert wsb(1, 2, 0, 1, 64, 64, binding.GDN_F32) == 0
@@ -271,6 +271,6 @@ def test_masked_bwd_argument_checks(lib):
     assert call(ws=None) == 4
     assert call(ws_bytes=16) == 4
     q = lib.masked_deltaproduct_chunk_bwd_workspace_bytes
-    per = 64 * 64 + 2 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 64 + 64
+    per = 3 * 64 * 64 + 2 * 64 * 64 + 2 * 64 * 64 + 3 * 64 * 64 + 64
     assert q(1, 2, 40, 2, 64, 64, binding.GDN_F32) == 4 * 2 * 2 * per  # 40 tokens: two chunks of 32
     assert q(1, 2, 40, 3, 64, 64, binding.GDN_F32) == ctypes.c_size_t(-1).value
