@@ -238,10 +238,12 @@ def masked_deltaproduct_workspace_bytes(B, H, T, r, Dk, Dv, dtype=torch.bfloat16
 
 
 def masked_deltaproduct_chunk_fwd(q, k, v, beta, g, mask, initial_state=None, output_final_state=False,
-                                  chunk=64, scale=1.0, l2norm=False, o=None, workspace=None, stream=None):
+                                  chunk=64, scale=1.0, l2norm=False, o=None, workspace=None, stream=None,
+                                  simt=False):
     """Block-masked DeltaProduct forward.  q, k [B,H,T,Dk]; v [B,H,T,Dv]; beta
     [B,H,T] (all bf16 or all fp32); g [B,H,T] fp32; mask [r,r] fp32 (CUDA).
-    chunk counts sub-rows (tokens x r)."""
+    chunk counts sub-rows (tokens x r).  simt keeps the state chain on the
+    CUDA cores where the tensor-core chain would run."""
     B, H, T, Dk = q.shape
     Dv = v.shape[-1]
     r = mask.shape[0]
@@ -264,9 +266,11 @@ def masked_deltaproduct_chunk_fwd(q, k, v, beta, g, mask, initial_state=None, ou
         need = lib.masked_deltaproduct_chunk_fwd_workspace_bytes(B, H, T, r, Dk, Dv, code)
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0)
     st = lib.masked_deltaproduct_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
                                            _ptr(initial_state), _ptr(o), _ptr(sf), B, H, T, r, Dk, Dv, chunk,
-                                           float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace),
+                                           float(scale), flags,
+                                           code, _ptr(workspace),
                                            ws_bytes, _stream(stream))
     _raise("masked_deltaproduct_chunk_fwd", st)
     return o, sf
@@ -443,7 +447,7 @@ def gdn_chunk_bwd_workspace_bytes(B, H, T, Dk, Dv, dtype=torch.bfloat16, r=1):
 
 
 def deltaproduct_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False,
-                           need_dinitial=False, workspace=None, stream=None):
+                           need_dinitial=False, workspace=None, stream=None, simt=False):
     """Backward of deltaproduct_chunk_fwd: k [B,H,T,r,Dk], v [B,H,T,r,Dv],
     beta [B,H,T,r].  Returns (dq, dk, dv, dbeta, dg, dinitial_state or None);
     dq, dk, dv in the inputs' dtype, the rest fp32."""
@@ -470,16 +474,18 @@ def deltaproduct_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_stat
         need = lib.gdn_chunk_bwd_workspace_bytes(B, H, T, r, Dk, Dv, code)
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0)
     st = lib.deltaproduct_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state), _ptr(do),
                                     _ptr(dfinal_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
-                                    _ptr(ds0), B, H, T, r, Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code,
+                                    _ptr(ds0), B, H, T, r, Dk, Dv, float(scale), flags,
+                                    code,
                                     _ptr(workspace), ws_bytes, _stream(stream))
     _raise("deltaproduct_chunk_bwd", st)
     return dq, dk, dv, dbeta, dg, ds0
 
 
 def masked_deltaproduct_chunk_bwd(q, k, v, beta, g, mask, do, initial_state=None, dfinal_state=None, scale=1.0,
-                                  l2norm=False, need_dinitial=False, workspace=None, stream=None):
+                                  l2norm=False, need_dinitial=False, workspace=None, stream=None, simt=False):
     """Backward of masked_deltaproduct_chunk_fwd.  Returns (dq, dk, dv, dbeta,
     dg, dinitial_state or None); dq, dk, dv in the inputs' dtype, the rest fp32."""
     B, H, T, Dk = q.shape
@@ -507,17 +513,19 @@ def masked_deltaproduct_chunk_bwd(q, k, v, beta, g, mask, do, initial_state=None
         need = lib.masked_deltaproduct_chunk_bwd_workspace_bytes(B, H, T, r, Dk, Dv, code)
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0)
     st = lib.masked_deltaproduct_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(mask),
                                            _ptr(initial_state), _ptr(do), _ptr(dfinal_state), _ptr(dq), _ptr(dk),
                                            _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(ds0), B, H, T, r, Dk, Dv,
-                                           float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace),
+                                           float(scale), flags,
+                                           code, _ptr(workspace),
                                            ws_bytes, _stream(stream))
     _raise("masked_deltaproduct_chunk_bwd", st)
     return dq, dk, dv, dbeta, dg, ds0
 
 
 def gdn_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, scale=1.0, l2norm=False,
-                  need_dinitial=False, workspace=None, stream=None):
+                  need_dinitial=False, workspace=None, stream=None, simt=False):
     """Backward of gdn_chunk_fwd.  Returns (dq, dk, dv, dbeta, dg,
     dinitial_state or None); dq, dk, dv in the inputs' dtype, the rest fp32."""
     B, H, T, Dk = q.shape
@@ -543,10 +551,11 @@ def gdn_chunk_bwd(q, k, v, beta, g, do, initial_state=None, dfinal_state=None, s
         need = lib.gdn_chunk_bwd_workspace_bytes(B, H, T, 1, Dk, Dv, code)
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PATH_SIMT if simt else 0)
     st = lib.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(initial_state), _ptr(do),
                            _ptr(dfinal_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(ds0), B, H, T,
-                           Dk, Dv, float(scale), GDN_QK_L2NORM if l2norm else 0, code, _ptr(workspace), ws_bytes,
-                           _stream(stream))
+                           Dk, Dv, float(scale), flags,
+                           code, _ptr(workspace), ws_bytes, _stream(stream))
     _raise("gdn_chunk_bwd", st)
     return dq, dk, dv, dbeta, dg, ds0
 

@@ -177,7 +177,7 @@ int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, c
                                   void *stream_v) {
     if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
     if (chunk != 16 && chunk != 32 && chunk != 64) return chunk <= 0 ? GDN_ERR_INVALID_ARG : GDN_ERR_UNSUPPORTED;
     if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
     if (r > 8 || Dk % r != 0 || chunk % r != 0) return GDN_ERR_UNSUPPORTED;
@@ -452,7 +452,7 @@ int masked_deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, c
                                   unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
     if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-    if (flags & ~GDN_QK_L2NORM) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
     if ((Dk != 64 && Dk != 128) || (Dv != 64 && Dv != 128)) return GDN_ERR_UNSUPPORTED;
     if (r > 8 || 64 % r != 0 || Dk % r != 0) return GDN_ERR_UNSUPPORTED;
     if ((long long)B * H > 65535 || (long long)T * r >= (1LL << 31)) return GDN_ERR_UNSUPPORTED;
@@ -489,7 +489,11 @@ int gdn_get_device_error(void *stream) {
     const int b = gdn::cam_prep_read_clear_error();
     const int c = gdn::cam_scan_read_clear_error();
     const int d = gdn::cam_scan_bwd_read_clear_error();
-    return a != GDN_OK ? a : (b != GDN_OK ? b : (c != GDN_OK ? c : d));
+    const int e = gdn::wy_chain_tc_read_clear_error();
+    const int r[] = {a, b, c, d, e};
+    for (int x : r)
+        if (x != GDN_OK) return x;
+    return GDN_OK;
 }
 
 unsigned long long gdn_launch_count(void) { return gdn::g_launches.load(); }

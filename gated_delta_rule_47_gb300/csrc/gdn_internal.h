@@ -203,6 +203,23 @@ struct MaskedBwdArgs {
 size_t masked_bwd_workspace_bytes(const MaskedBwdArgs &a);
 int launch_masked_bwd(const MaskedBwdArgs &a, cudaStream_t stream);
 
+// The sequential chains of the chunkwise WY form on tcgen05 (wy_chain_tc.cu),
+// for Dk = Dv = 128 and 64-row chunks; per (head, chunk) ci = head * NT + c.
+// roles = 1 runs the forward state chain only, 2 also the reverse gradient
+// chain (a second CTA per head).
+struct WyChainTcArgs {
+    const float *s0, *dsf;  // [BH][128][128] initial state / final state's gradient, or null (zero)
+    float *sf, *ds0;        // [BH][128][128] final state / initial state's gradient, or null (not wanted)
+    float *Sw, *dSw;        // [ci][128][128] state entering / gradient leaving each chunk
+    float *Vnw;             // [ci][64][128] Vn of each chunk (forward chain)
+    const unsigned char *Wimg, *Kdimg;  // [ci] 32 KB bf16 hi | lo images of W and Kd (write_chain_image)
+    const float *Uw, *Bw, *Gw;          // [ci][64][128] U, [ci][128][128] B (reverse), [ci][64] gamma
+    int BH, NT, roles;
+};
+int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t stream);
+// Reads and clears the error word of the chain kernel (GDN_OK or GDN_ERR_TIMEOUT).
+int wy_chain_tc_read_clear_error();
+
 // Counts one kernel launch (thread-safe); read by gdn_launch_count().
 void note_launch();
 

@@ -22,6 +22,8 @@
 // gradient), wy_chain_kernel (both chains), mbwd_grad_kernel.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "gdn_internal.h"
 #include "simt_tile.cuh"
 #include "tri_inverse.cuh"
@@ -44,6 +46,7 @@ struct MbParams {
     int T, r, lr, lsl, Ct, NT;                              // lr = log2 r, lsl = log2 (Dk / r)
     float scale;
     int l2;
+    int img;  // W and Kd stored as the tensor-core chain's bf16 hi | lo images, not in fp32
 };
 
 struct MbChunk {
@@ -194,12 +197,13 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
 #pragma unroll
             for (int j = 0; j < DK / 16; ++j) {
                 const int m = ty + 32 * i, n = tx + 16 * j;
-                Wg[m * DK + n] = accW[i][j];
+                if (!p.img) Wg[m * DK + n] = accW[i][j];
                 Kt[m * LX + n] = accW[i][j];  // W
             }
         const float gl = gam[kC - 1];
         float *Kdg = p.Kdw + ch.ci * kC * DK;
-        for (int e = tid; e < kC * DK; e += kThr) Kdg[e] = expf(gl - gam[e / DK]) * Kw[(e / DK) * LK + e % DK];
+        if (!p.img)
+            for (int e = tid; e < kC * DK; e += kThr) Kdg[e] = expf(gl - gam[e / DK]) * Kw[(e / DK) * LK + e % DK];
         if (tid < kC) p.Gw[ch.ci * kC + tid] = gam[tid];
     }
     load_rows<T, DV>(Vs, (const T *)p.dout + ch.htok * DV, ch.ntok, false, nullptr);  // dO by query
@@ -220,6 +224,15 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
             }
     }
     __syncthreads();
+    if constexpr (DK == 128) {
+        if (p.img) {  // W (in Kt) and Kd = diag(e^{gl - gamma}) Kw as the chain's operand images
+            const float gl = gam[kC - 1];
+            write_chain_image<kThr>(reinterpret_cast<unsigned char *>(p.Ww + ch.ci * kC * DK), Kt, LX,
+                                    [](int) { return 1.f; });
+            write_chain_image<kThr>(reinterpret_cast<unsigned char *>(p.Kdw + ch.ci * kC * DK), Kw, LK,
+                                    [&](int m) { return expf(gl - gam[m]); });
+        }
+    }
     {  // Kr = -P^^T dO; dO rows scaled by scale e^{gamma_t}
         float acc[2][DV / 16];
         zero(acc);
@@ -648,11 +661,35 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
         cudaFuncSetAttribute(mbwd_grad_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3) !=
             cudaSuccess)
         return GDN_ERR_CUDA;
+    // the chains on tcgen05 for bf16 at Dk = Dv = 128 (W and Kd then travel as operand images)
+    const bool tc_chain = std::is_same<T, __nv_bfloat16>::value && DK == 128 && DV == 128 &&
+                          !(a.flags & GDN_PATH_SIMT) && sm100_family();
+    p.img = tc_chain ? 1 : 0;
     mbwd_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
     note_launch();
-    WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};
-    wy_chain_kernel<DK, DV, kSlice><<<dim3((unsigned)(DV / kSlice), (unsigned)BH, 2), kChainThr, s2, st>>>(cp);
-    note_launch();
+    if (tc_chain) {
+        WyChainTcArgs ca{};
+        ca.s0 = p.s0;
+        ca.dsf = p.dsf;
+        ca.ds0 = p.ds0;
+        ca.Sw = p.Sw;
+        ca.dSw = p.dSw;
+        ca.Vnw = p.Vnw;
+        ca.Wimg = reinterpret_cast<const unsigned char *>(p.Ww);
+        ca.Kdimg = reinterpret_cast<const unsigned char *>(p.Kdw);
+        ca.Uw = p.Uw;
+        ca.Bw = p.Bw;
+        ca.Gw = p.Gw;
+        ca.BH = BH;
+        ca.NT = NT;
+        ca.roles = 2;
+        const int rc = launch_wy_chain_tc(ca, st);
+        if (rc != GDN_OK) return rc;
+    } else {
+        WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};
+        wy_chain_kernel<DK, DV, kSlice><<<dim3((unsigned)(DV / kSlice), (unsigned)BH, 2), kChainThr, s2, st>>>(cp);
+        note_launch();
+    }
     mbwd_grad_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s3, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

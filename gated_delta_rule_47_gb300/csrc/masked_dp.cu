@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "gdn_internal.h"
 #include "simt_tile.cuh"
 #include "tri_inverse.cuh"
@@ -51,6 +53,7 @@ struct MdpParams {
     int T, r, Ct, NT;
     float scale;
     int l2;
+    int img;  // W and Kd stored as the tensor-core chain's bf16 hi | lo images, not in fp32
 };
 
 struct MChunk {
@@ -148,7 +151,12 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int j = 0; j < DK / 16; ++j) Wg[(ty + 32 * i) * DK + tx + 16 * j] = acc[i][j];
+            for (int j = 0; j < DK / 16; ++j) {
+                if (p.img)
+                    Kt[(ty + 32 * i) * LK + tx + 16 * j] = acc[i][j];  // the token keys are no longer needed
+                else
+                    Wg[(ty + 32 * i) * DK + tx + 16 * j] = acc[i][j];
+            }
     }
     {
         float acc[2][DV / 16];
@@ -163,7 +171,8 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
     {
         const float gl = gam[kC - 1];
         float *Kdg = p.Kdw + ch.ci * kC * DK;
-        for (int e = tid; e < kC * DK; e += kThr) Kdg[e] = expf(gl - gam[e / DK]) * Kw[(e / DK) * LK + e % DK];
+        if (!p.img)
+            for (int e = tid; e < kC * DK; e += kThr) Kdg[e] = expf(gl - gam[e / DK]) * Kw[(e / DK) * LK + e % DK];
         if (tid < kC) p.Gw[ch.ci * kC + tid] = gam[tid];
     }
     // the output factors P[t][b] over the sub-rows of tokens up to t
@@ -179,6 +188,16 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
                 const int t = ty + 32 * i, b = tx + 16 * j;
                 Pg[t * kC + b] = (t < ch.ntok && b / r <= t) ? p.scale * expf(gam[t * r] - gam[b]) * acc[i][j] : 0.f;
             }
+    }
+    if constexpr (DK == 128) {
+        if (p.img) {  // W (in Kt) and Kd = diag(e^{gl - gamma}) Kw as the chain's operand images
+            __syncthreads();
+            const float gl = gam[kC - 1];
+            write_chain_image<kThr>(reinterpret_cast<unsigned char *>(p.Ww + ch.ci * kC * DK), Kt, LK,
+                                    [](int) { return 1.f; });
+            write_chain_image<kThr>(reinterpret_cast<unsigned char *>(p.Kdw + ch.ci * kC * DK), Kw, LK,
+                                    [&](int m) { return expf(gl - gam[m]); });
+        }
     }
 }
 
@@ -267,11 +286,32 @@ int run(const MaskedDpArgs &a, cudaStream_t st) {
         cudaFuncSetAttribute(mdp_out_kernel<T, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s3) !=
             cudaSuccess)
         return GDN_ERR_CUDA;
+    // the state chain on tcgen05 for bf16 at Dk = Dv = 128 (W and Kd then travel as operand images)
+    const bool tc_chain = std::is_same<T, __nv_bfloat16>::value && DK == 128 && DV == 128 &&
+                          !(a.flags & GDN_PATH_SIMT) && sm100_family();
+    p.img = tc_chain ? 1 : 0;
     mdp_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
     note_launch();
-    WyChainParams cp{a.s0, nullptr, a.sf, nullptr, p.Sw, nullptr, p.Ww, p.Kdw, p.Uw, p.Vnw, nullptr, p.Gw, NT};
-    wy_chain_kernel<DK, DV, kMSlice><<<dim3((unsigned)(DV / kMSlice), (unsigned)BH, 1), kChainThr, s2, st>>>(cp);
-    note_launch();
+    if (tc_chain) {
+        WyChainTcArgs ca{};
+        ca.s0 = a.s0;
+        ca.sf = a.sf;
+        ca.Sw = p.Sw;
+        ca.Vnw = p.Vnw;
+        ca.Wimg = reinterpret_cast<const unsigned char *>(p.Ww);
+        ca.Kdimg = reinterpret_cast<const unsigned char *>(p.Kdw);
+        ca.Uw = p.Uw;
+        ca.Gw = p.Gw;
+        ca.BH = BH;
+        ca.NT = NT;
+        ca.roles = 1;
+        const int rc = launch_wy_chain_tc(ca, st);
+        if (rc != GDN_OK) return rc;
+    } else {
+        WyChainParams cp{a.s0, nullptr, a.sf, nullptr, p.Sw, nullptr, p.Ww, p.Kdw, p.Uw, p.Vnw, nullptr, p.Gw, NT};
+        wy_chain_kernel<DK, DV, kMSlice><<<dim3((unsigned)(DV / kMSlice), (unsigned)BH, 1), kChainThr, s2, st>>>(cp);
+        note_launch();
+    }
     mdp_out_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s3, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

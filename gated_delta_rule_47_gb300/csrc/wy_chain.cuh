@@ -10,6 +10,7 @@
 #pragma once
 
 #include "simt_tile.cuh"
+#include "tc_util.cuh"
 
 namespace gdn {
 namespace {
@@ -24,6 +25,30 @@ struct WyChainParams {
     float *Sw, *dSw, *Ww, *Kdw, *Uw, *Vnw, *Bw, *Gw;
     int NT;  // chunks per head
 };
+
+// Rows 0..63 of an fp32 tile of 128 columns (row m at src + m * ld, scaled by
+// rs(m)) as the tensor-core chain's bf16 hi | lo operand image (32 KB):
+// element (m, c) in the 8 KB block c / 64, at row m and 16-byte chunk
+// (c % 64) / 8 of the 128-byte row, the chunk index XORed with m % 8 (the
+// 128-byte swizzle); hi at +0, lo = x - hi at +16 KB.  The same bytes serve
+// the chain's MMAs as a K-major (rows) and as an MN-major (columns) operand.
+template <int NTHR, typename RowScale>
+__device__ __forceinline__ void write_chain_image(unsigned char *img, const float *src, int ld, RowScale rs) {
+    for (int e = threadIdx.x; e < tile::kC * 16; e += NTHR) {
+        const int m = e >> 4, c8 = (e & 15) * 8;
+        const float f = rs(m);
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = f * src[m * ld + c8 + 2 * i], x1 = f * src[m * ld + c8 + 2 * i + 1];
+            h[i] = tc::pack_bf16(x0, x1);
+            l[i] = tc::pack_bf16(x0 - __uint_as_float(h[i] << 16), x1 - __uint_as_float(h[i] & 0xffff0000u));
+        }
+        const uint32_t off = (uint32_t)(c8 >> 6) * 8192u + tc::sw128_offset((uint32_t)m, (uint32_t)(c8 & 63));
+        *reinterpret_cast<uint4 *>(img + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(img + 16384 + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
 
 template <int DK, int SLICE>
 constexpr size_t wy_chain_smem() {

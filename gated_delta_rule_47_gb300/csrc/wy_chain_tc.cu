@@ -1,0 +1,312 @@
+// wy_chain_tc.cu -- the sequential state chains of the chunkwise WY form on
+// tcgen05, for Dk = Dv = 128 and 64-row chunks (gated_deltaproduct test.py:
+// the state loop of `gated_chunk_delta_rule_fwd_kernel_h` forward and of
+// `gated_chunk_delta_rule_bwd_kernel_dhu` in reverse).  One CTA per head and
+// chain:
+//   forward:  Vn = U - W S,  S <- e^{gl} S + Kd^T Vn    (S entering each chunk and Vn kept)
+//   reverse:  dS <- e^{gl} dS' - W^T (Kd dS') + B_c     (dS' leaving each chunk kept)
+// The state lives in tensor memory as X^T (128 value lanes x 128 key columns,
+// fp32).  Per chunk:
+//   1. eight epilogue warps read X^T, write it out (the chunk's snapshot),
+//      split it into bf16 hi + lo operand tiles in shared memory, and put
+//      e^{gl} X^T (+ B_c^T on the reverse chain) back;
+//   2. one thread issues Z^T = X^T M1^T (M1 = W forward, Kd reverse) as the
+//      products hi.hi + hi.lo + lo.hi (24 MMAs, M = 128, N = 64);
+//   3. the epilogue warps read Z^T, form Vn = U - Z (forward, written out) or
+//      Y = Z (reverse), and split it into hi + lo operand tiles;
+//   4. the thread issues X^T += Z'^T M2 (forward, M2 = Kd) or X^T -= Z'^T M2
+//      (reverse, M2 = W), again as three products (12 MMAs, N = 128).
+// The split products carry about 2^-16 relative error, against 2^-8 for a
+// plain bf16 product.  W and Kd arrive as bf16 hi | lo operand images written
+// by the WY kernels (wy_chain.cuh, write_chain_image), two 32 KB bulk copies
+// per chunk, double-buffered.  Every wait is bounded; a CTA that gives up sets
+// the error word, which gdn_get_device_error reads.
+#include <cuda.h>
+#include <stdint.h>
+
+#include "gdn_internal.h"
+#include "tc_util.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace tc;
+
+constexpr int kRows = 64;    // rows of a chunk
+constexpr int kCThr = 384;   // warp 0 issues, warp 1 holds TMEM, warp 2 loads, warps 4..11 epilogue
+constexpr uint32_t C_SLOT = 65536;         // one chunk's W hi | W lo | Kd hi | Kd lo, 16 KB each
+constexpr uint32_t C_XOP = 2 * C_SLOT;     // X^T hi | lo: K-major [2 key blocks][128 value rows][128 B]
+constexpr uint32_t C_ZOP = C_XOP + 65536;  // Z'^T hi | lo: K-major [128 value rows][128 B]
+constexpr uint32_t C_BAR = C_ZOP + 32768;
+enum { CB_FULL = 0, CB_FREE = 2, CB_XREADY = 4, CB_ZDONE, CB_ZREADY, CB_XDONE, CB_DRAIN, CB_NUM };
+constexpr uint32_t C_TSLOT = C_BAR + 8 * CB_NUM;
+constexpr uint32_t C_SMEM = C_TSLOT + 16 + 1024;  // + slack to align the base to 1024 bytes
+static_assert(C_SMEM <= 232448, "chain kernel fits the shared memory of one CTA");
+constexpr uint32_t TM_X = 0, TM_Z = 128, kTmemCols = 256;
+
+__device__ unsigned int g_wyc_error = 0;  // set when a bounded wait of the chain kernel gives up
+constexpr unsigned long long kWycWaitNs = 1000000000ull;
+constexpr unsigned long long kWycDrainNs = 200000000ull;
+
+__device__ __forceinline__ bool wyc_wait(uint64_t *bar, uint32_t parity, unsigned code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*reinterpret_cast<volatile unsigned *>(&g_wyc_error) != 0u) return false;
+        if (global_timer_ns() - t0 > kWycWaitNs) {
+            atomicOr(&g_wyc_error, code);
+            return false;
+        }
+    }
+}
+
+// A wait's outcome made uniform across the warp, so that the warp's
+// .sync.aligned TMEM accesses that follow are reached by all of its lanes.
+__device__ __forceinline__ bool warp_ok(bool ok) { return __all_sync(0xffffffffu, ok) != 0; }
+
+// x[0..7] as bf16 hi and lo = x - hi, 16 bytes each
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+        l[i] = pack_bf16(x[2 * i] - __uint_as_float(h[i] << 16), x[2 * i + 1] - __uint_as_float(h[i] & 0xffff0000u));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_TSLOT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x, role = blockIdx.y, NT = p.NT;
+    const size_t ci0 = (size_t)bh * NT;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < CB_NUM; ++i) mbar_init(&bars[i], (i == CB_XREADY || i == CB_ZREADY) ? 256u : 1u);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idZ = idesc_bf16(128, 64, false, false);
+            const uint32_t idX = idesc_bf16(128, 128, false, true, role == 1);
+            const uint32_t m1 = role == 0 ? 0u : 32768u, m2 = role == 0 ? 32768u : 0u;
+            for (int s = 0; s < NT; ++s) {
+                const int b = s & 1;
+                const uint32_t slot = sb + (uint32_t)b * C_SLOT;
+                if (!wyc_wait(&bars[CB_FULL + b], (s >> 1) & 1, 1u)) break;
+                if (!wyc_wait(&bars[CB_XREADY], s & 1, 1u)) break;
+                tc_fence_after_sync();
+                // Z^T = X^T M1^T over the 128 keys: hi.hi, hi.lo, lo.hi
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {
+                    const uint32_t xa = sb + C_XOP + (pr == 2 ? 32768u : 0u);
+                    const uint32_t mb = slot + m1 + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem + TM_Z, smem_desc(xa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    smem_desc(mb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idZ,
+                                    (pr | ks) != 0);
+                }
+                mma_commit(&bars[CB_ZDONE]);
+                if (!wyc_wait(&bars[CB_ZREADY], s & 1, 1u)) break;
+                tc_fence_after_sync();
+                // X^T +/-= Z'^T M2 over the 64 rows
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {
+                    const uint32_t za = sb + C_ZOP + (pr == 2 ? 16384u : 0u);
+                    const uint32_t nb = slot + m2 + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ss(tmem + TM_X, smem_desc(za + ks * 32, 16, 1024), smem_desc(nb + ks * 2048, 8192, 1024),
+                                    idX, 1u);
+                }
+                mma_commit(&bars[CB_XDONE]);
+                mma_commit(&bars[CB_FREE + b]);
+            }
+            mma_commit(&bars[CB_DRAIN]);
+            mbar_wait(&bars[CB_DRAIN], 0, kWycDrainNs);
+        }
+    } else if (warp == 2) {
+        // ----------------------------------------- W and Kd images, bulk copies
+        if (lane == 0) {
+            int armed[2] = {0, 0};
+            for (int s = 0; s < NT; ++s) {
+                const int b = s & 1;
+                // slot b held chunk s-2, whose MMAs are complete when CB_FREE + b completes
+                if (s >= 2 && !wyc_wait(&bars[CB_FREE + b], ((s - 2) >> 1) & 1, 2u)) break;
+                const size_t ci = ci0 + (size_t)(role == 0 ? s : NT - 1 - s);
+                mbar_arrive_expect_tx(&bars[CB_FULL + b], 65536u);
+                bulk_load_global(sm + b * C_SLOT, p.Wimg + ci * 32768, 32768u, &bars[CB_FULL + b]);
+                bulk_load_global(sm + b * C_SLOT + 32768, p.Kdimg + ci * 32768, 32768u, &bars[CB_FULL + b]);
+                armed[b]++;
+            }
+            for (int b = 0; b < 2; ++b)
+                if (armed[b]) mbar_wait(&bars[CB_FULL + b], (armed[b] - 1) & 1, kWycDrainNs);
+        }
+    } else if (warp >= 4) {
+        // --------------------------------------------------------- epilogue
+        // thread = value index dv (its TMEM lane); hh picks the half of the key
+        // columns of X^T (and of the rows of Z^T) it handles
+        const int q = warp & 3, hh = (warp - 4) >> 2;
+        const int dv = 32 * q + lane;
+        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        const float *init = role == 0 ? p.s0 : p.dsf;
+        float *snap = role == 0 ? p.Sw : p.dSw;
+        bool ok = true;
+        for (int s = 0; s < NT; ++s) {
+            const size_t ci = ci0 + (size_t)(role == 0 ? s : NT - 1 - s);
+            const float el = expf(p.Gw[ci * kRows + kRows - 1]);
+            // forward: U[t][dv] for the rows 32hh..32hh+31; reverse: B[dk][dv] for
+            // the keys 64hh..64hh+63 (loaded ahead of the waits)
+            float pre[64];
+            if (role == 0) {
+                const float *Ug = p.Uw + ci * (kRows * 128) + (size_t)(32 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pre[i] = Ug[(size_t)i * 128];
+            } else {
+                const float *Bg = p.Bw + ci * 16384 + (size_t)(64 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) pre[i] = Bg[(size_t)i * 128];
+            }
+            float x[64];
+            if (s == 0) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    x[i] = init ? init[((size_t)bh * 128 + 64 * hh + i) * 128 + dv] : 0.f;
+            } else {
+                ok = warp_ok(wyc_wait(&bars[CB_XDONE], (s - 1) & 1, 4u));
+                if (!ok) break;
+                tc_fence_after_sync();
+                uint32_t r[4][16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld16(tmem + lb + TM_X + 64 * hh + 16 * j, r[j]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) x[16 * j + i] = __uint_as_float(r[j][i]);
+            }
+            {  // the snapshot, and X^T as its hi | lo operand (key block hh)
+                float *sn = snap + ci * 16384 + (size_t)(64 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) sn[(size_t)i * 128] = x[i];
+                uint8_t *xo = sm + C_XOP + hh * 16384;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 hi, lo;
+                    split8(x + 8 * c, hi, lo);
+                    const uint32_t off = sw128_offset((uint32_t)dv, (uint32_t)(8 * c));
+                    *reinterpret_cast<uint4 *>(xo + off) = hi;
+                    *reinterpret_cast<uint4 *>(xo + 32768 + off) = lo;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&bars[CB_XREADY]);
+            }
+            // e^{gl} X^T (+ B^T) back into TMEM for the update (the Z product
+            // reads only the operand tiles)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    r[i] = __float_as_uint(role == 0 ? el * x[16 * j + i] : el * x[16 * j + i] + pre[16 * j + i]);
+                tmem_st16(tmem + lb + TM_X + 64 * hh + 16 * j, r);
+            }
+            ok = warp_ok(wyc_wait(&bars[CB_ZDONE], s & 1, 4u));
+            if (!ok) break;
+            tc_fence_after_sync();
+            float z[32];
+            {
+                uint32_t r[2][16];
+                tmem_ld16(tmem + lb + TM_Z + 32 * hh, r[0]);
+                tmem_ld16(tmem + lb + TM_Z + 32 * hh + 16, r[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i >> 4][i & 15]);
+            }
+            if (role == 0) {  // Vn = U - W S, kept
+                float *Vg = p.Vnw + ci * (kRows * 128) + (size_t)(32 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    z[i] = pre[i] - z[i];
+                    Vg[(size_t)i * 128] = z[i];
+                }
+            }
+            {  // Z'^T as its hi | lo operand (rows 32hh.. of the chunk)
+                uint8_t *zo = sm + C_ZOP;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 hi, lo;
+                    split8(z + 8 * c, hi, lo);
+                    const uint32_t off = sw128_offset((uint32_t)dv, (uint32_t)(32 * hh + 8 * c));
+                    *reinterpret_cast<uint4 *>(zo + off) = hi;
+                    *reinterpret_cast<uint4 *>(zo + 16384 + off) = lo;
+                }
+            }
+            tmem_wait_st();  // the decayed state is in place before the update reads it
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&bars[CB_ZREADY]);
+        }
+        float *out = role == 0 ? p.sf : p.ds0;
+        if (ok && NT > 0) {
+            ok = warp_ok(wyc_wait(&bars[CB_XDONE], (NT - 1) & 1, 4u));
+            if (ok && out) {
+                tc_fence_after_sync();
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lb + TM_X + 64 * hh + 16 * j, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        out[((size_t)bh * 128 + 64 * hh + 16 * j + i) * 128 + dv] = __uint_as_float(r[i]);
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t st) {
+    if (a.BH <= 0 || a.NT <= 0 || a.roles < 1 || a.roles > 2) return GDN_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(wy_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    wy_chain_tc_kernel<<<dim3((unsigned)a.BH, (unsigned)a.roles), kCThr, C_SMEM, st>>>(a);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int wy_chain_tc_read_clear_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wyc_error, sizeof(v)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_wyc_error, &zero, sizeof(zero)) != cudaSuccess) return GDN_ERR_CUDA;
+    return v ? GDN_ERR_TIMEOUT : GDN_OK;
+}
+
+}  // namespace gdn

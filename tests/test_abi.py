@@ -151,7 +151,7 @@ def test_masked_deltaproduct_argument_checks(lib):
     assert call(r=16, Dk=128) == 2  # r <= 8
     assert call(chunk=48) == 2
     assert call(chunk=0) == 1
-    assert call(flags=2) == 1      # only GDN_QK_L2NORM
+    assert call(flags=4) == 1      # GDN_QK_L2NORM and GDN_PATH_SIMT only
     assert call(mask=None) == 1
     assert call(q=u + 4) == 3
     assert call(dtype=3) == 1
@@ -264,7 +264,7 @@ def test_masked_bwd_argument_checks(lib):
 
     assert call(r=3) == 2          # r must divide 64 and Dk
     assert call(r=16) == 2
-    assert call(flags=2) == 1      # only GDN_QK_L2NORM
+    assert call(flags=4) == 1      # GDN_QK_L2NORM and GDN_PATH_SIMT only
     assert call(Dk=96) == 2
     assert call(dtype=4) == 1
     assert call(mask=None) == 1

@@ -168,3 +168,31 @@ def test_split_and_resume(cut):
         joined = torch.cat([gh[i], gt[i]], dim=2)
         assert rel_err(joined, full[i].double().cpu().numpy()) <= TOL_F32, name
     assert rel_err(gh[5], full[5].double().cpu().numpy()) <= TOL_F32
+
+
+@pytest.mark.parametrize("r,T", [(1, 300), (2, 130), (4, 70)])
+def test_tensor_core_chain_matches_the_cuda_core_chain(r, T):
+    """bf16 tensors at Dk = Dv = 128 run both state chains on tcgen05 (bf16
+    hi / lo split products, fp32 state in tensor memory); the fp32 CUDA-core
+    chains give the same gradients to within the split products' ~2^-16
+    relative error, over several chunks with a ragged tail, an initial state
+    and a final-state gradient.  The bf16 gradients may differ by one rounding
+    of the output (2^-8 of an element); the fp32 ones only by the chains'
+    arithmetic."""
+    inp, do, dsf = grads_case(1, 3, T, 128, 128, "bf16", True, r=(r if r > 1 else None), seed=40 + r)
+    d = to_dev(inp)
+
+    def run(simt):
+        if r == 1:
+            return binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"],
+                                         dsf.cuda(), l2norm=True, need_dinitial=True, simt=simt)
+        return binding.deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(),
+                                              d["initial_state"], dsf.cuda(), l2norm=True, need_dinitial=True,
+                                              simt=simt)
+
+    tc, simt = run(False), run(True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    for name, x, y in zip(NAMES, tc, simt):
+        tol = 5e-3 if x.dtype == torch.bfloat16 else 2e-4
+        assert rel_err(x, y.double().cpu().numpy()) <= tol, name

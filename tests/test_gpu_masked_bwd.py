@@ -94,3 +94,24 @@ def test_full_size_sampled_heads():
                                          heads(do, idx))
     for name, x, y in zip(NAMES[:5], got[:5], ref[:5]):
         assert rel_err(heads(x, idx).cpu(), y) <= TOL_BF16, name
+
+
+@pytest.mark.parametrize("r,T", [(2, 100), (4, 40)])
+def test_tensor_core_chain_matches_the_cuda_core_chain(r, T):
+    """bf16 at D = 128 runs the chains on tcgen05 (bf16 hi / lo split
+    products); the fp32 CUDA-core chains agree to within one rounding of the
+    bf16 gradients and ~2e-4 on the fp32 ones."""
+    inp, do, dsf = case(T, 128, r, "bf16", True, seed=60 + r, general_mask=True)
+    d = to_dev(inp)
+
+    def run(simt):
+        return binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"], do.cuda(),
+                                                     d["initial_state"], dsf.cuda(), l2norm=True, need_dinitial=True,
+                                                     simt=simt)
+
+    tc, simt = run(False), run(True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    for name, x, y in zip(NAMES, tc, simt):
+        tol = 5e-3 if x.dtype == torch.bfloat16 else 2e-4
+        assert rel_err(x, y.double().cpu().numpy()) <= tol, name

@@ -79,3 +79,24 @@ def test_full_size_workload_sampled_heads():
     sub = {k: (heads(v, idx) if k != "mask" else v) for k, v in inp.items()}
     ro, _ = oracle.masked_deltaproduct_fwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], sub["mask"])
     assert rel_err(heads(o, idx).cpu(), ro) <= TOL_BF16
+
+
+@pytest.mark.parametrize("r", [2, 4])
+def test_tensor_core_chain_matches_the_cuda_core_chain(r):
+    """bf16 at D = 128 runs the state chain on tcgen05 (bf16 hi / lo split
+    products, fp32 state in tensor memory); the fp32 CUDA-core chain gives the
+    same output to within one bf16 rounding and the same final state to ~2e-4."""
+    inp = gdn_inputs(1, 3, 150, 128, 128, seed=70 + r, dtype="bf16", initial_state=True, normalise_qk=False)
+    g = torch.Generator().manual_seed(r)
+    inp["mask"] = (torch.randn(r, r, generator=g) * 0.5).contiguous()
+    d = to_dev(inp)
+    outs = []
+    for simt in (False, True):
+        outs.append(binding.masked_deltaproduct_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"],
+                                                          d["initial_state"], output_final_state=True, l2norm=True,
+                                                          simt=simt))
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    (o1, s1), (o2, s2) = outs
+    assert rel_err(o1, o2.double().cpu().numpy()) <= 5e-3
+    assert rel_err(s1, s2.double().cpu().numpy()) <= 2e-4
