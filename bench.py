@@ -445,7 +445,7 @@ def secondary(args, dev):
                      "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del d, o, wsw
         torch.cuda.empty_cache()
-    # the block-masked DeltaProduct variant (CUDA-core path)
+    # the block-masked DeltaProduct variant (chunk-local kernels on the CUDA cores, chain on tcgen05)
     w = WORKLOADS["masked_dp_r2_b4h16t4096d128_bf16"]
     d = {k: v.to(dev) for k, v in w.make().items()}
     o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
@@ -455,7 +455,8 @@ def secondary(args, dev):
                                                               chunk=w.chunk, o=o, workspace=wsm))
     nbytes = w.B * w.H * w.T * gdn_bytes_per_token_head(w.D)
     out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
-                   "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "path": "CUDA cores, fp32",
+                   "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                   "path": "chunk-local kernels on the CUDA cores (fp32), state chains on tcgen05",
                    "launches_per_call": 3}
     # its backward
     gom = torch.randn(w.B, w.H, w.T, w.D, device=dev).to(torch.bfloat16)
@@ -464,10 +465,11 @@ def secondary(args, dev):
     ms = timeit(lambda: binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"],
                                                               gom, workspace=wsmb))
     out["masked_dp_bwd_r2_b4h16t4096d128_bf16"] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
-                                                   "path": "CUDA cores, fp32", "launches_per_call": 3}
+                                                   "path": "chunk-local kernels on the CUDA cores (fp32), state chains on tcgen05",
+                                                   "launches_per_call": 3}
     del d, o, wsm, gom, wsmb
     torch.cuda.empty_cache()
-    # the chunkwise GDN backward on the headline's shape (CUDA cores, fp32 arithmetic)
+    # the chunkwise GDN backward on the headline's shape (chunk-local kernels on the CUDA cores, chains on tcgen05)
     w = WORKLOADS["gdn_b4h16t4096d128_bf16"]
     d = {k: v.to(dev) for k, v in w.make().items()}
     gen = torch.Generator(device=dev).manual_seed(3)
@@ -478,7 +480,8 @@ def secondary(args, dev):
     nbytes = w.B * w.H * w.T * (14 * w.D + 14)  # q, k, v, beta, g, do in; dq, dk, dv, dbeta, dg out
     out["gdn_bwd_b4h16t4096d128_bf16"] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
                                           "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                          "launches_per_call": 3, "path": "CUDA cores, fp32"}
+                                          "launches_per_call": 3,
+                                          "path": "chunk-local kernels on the CUDA cores (fp32), state chains on tcgen05"}
     del d, go, wsg
     torch.cuda.empty_cache()
     w = WORKLOADS["cam_b2n32760h16d128_bf16"]

@@ -1,5 +1,5 @@
-// chunk_bwd.cu -- backward of the chunkwise GDN / DeltaProduct forward on the
-// CUDA cores, fp32 arithmetic (gated_deltaproduct test.py computes the same
+// chunk_bwd.cu -- backward of the chunkwise GDN / DeltaProduct forward, the
+// chunk-local kernels on the CUDA cores in fp32 (gated_deltaproduct test.py computes the same
 // gradients with `gated_chunk_delta_rule_bwd_kernel_dhu` for the state
 // gradient, `gated_chunk_delta_rule_bwd_kernel_dqkw` and
 // `gated_bwd_prepare_wy_repr_kernel` for the chunk-local ones).
@@ -29,11 +29,14 @@
 //
 // Three launches:
 //   1. bwd_wy_kernel (one CTA per chunk): T, W, U, Kd, gamma and B to the workspace.
-//   2. wy_chain_kernel: the forward state chain (S entering each chunk, and
-//      Vn) and the reverse gradient chain (dS' of each chunk, and the initial
-//      state's gradient) run side by side; each CTA holds 64 value columns of
-//      one head's state, since the columns of both chains are independent
-//      (64 heads of 128 columns make 256 CTAs, one wave at two per SM).
+//   2. the forward state chain (S entering each chunk, and Vn) and the
+//      reverse gradient chain (dS' of each chunk, and the initial state's
+//      gradient) side by side: for bf16 at Dk = Dv = 128 wy_chain_tc_kernel
+//      (tcgen05, one CTA per head and chain, the fp32 state in tensor memory;
+//      the WY kernel then writes W and Kd as its bf16 hi / lo operand images
+//      instead of fp32), otherwise wy_chain_kernel (CUDA cores, fp32; each CTA
+//      holds 64 value columns of one head's state, since the columns of both
+//      chains are independent).
 //   3. bwd_grad_kernel (one CTA per chunk): every input gradient.
 #include <cuda_bf16.h>
 

@@ -1,7 +1,8 @@
 // masked_bwd.cu -- backward of the block-masked DeltaProduct forward
 // (gated_deltaproduct test.py: `gated_chunk_delta_rule_bwd_kernel_dhu`,
 // `gated_chunk_delta_rule_bwd_kernel_dqkw` and `gated_bwd_prepare_wy_repr_kernel`
-// for the mask_ij variant) on the CUDA cores, fp32 arithmetic.
+// for the mask_ij variant): the chunk-local kernels on the CUDA cores in fp32,
+// the chains on tcgen05 for bf16 at D = 128 (wy_chain_tc.cu).
 //
 // The sub-rows a = (t, i) of a 64-row chunk (64 / r tokens) carry the read key
 // kr_a = k_t masked slice-wise by mask[i][:] and the write key kw_a = slice i
@@ -19,7 +20,9 @@
 // D_a = mask[i][j(c)] dKr_a[c] + [j(c) = i] dKw_a[c] as it goes, and the
 // token sums its rows at the end.  Three launches, as the chunk backward:
 // mbwd_wy_kernel (T, W, U, Kd, gamma and the chunk's term B of the state
-// gradient), wy_chain_kernel (both chains), mbwd_grad_kernel.
+// gradient), the two chains (wy_chain_tc_kernel for bf16 at Dk = Dv = 128,
+// with W and Kd handed over as operand images; wy_chain_kernel otherwise),
+// mbwd_grad_kernel.
 #include <cuda_bf16.h>
 
 #include <type_traits>

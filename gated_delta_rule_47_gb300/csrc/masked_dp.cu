@@ -1,5 +1,5 @@
-// masked_dp.cu -- block-masked DeltaProduct forward on the CUDA cores, fp32
-// arithmetic (gated_deltaproduct test.py: the mask_ij coupling of
+// masked_dp.cu -- block-masked DeltaProduct forward, the chunk-local kernels on
+// the CUDA cores in fp32 (gated_deltaproduct test.py: the mask_ij coupling of
 // `gated_chunk_scaled_dot_kkt_fwd_kernel` and `gated_fwd_recompute_w_u_kernel`,
 // the per-slice state update of `gated_chunk_delta_rule_fwd_kernel_h`, and the
 // sum over r of `gated_chunk_fwd_o_fn`).
@@ -20,8 +20,10 @@
 //   1. mdp_wy_kernel (one CTA per chunk): the keys, A, T, W, U,
 //      Kd = diag(e^{gamma_last - gamma}) Kw, and the output factors
 //      P[t][b] = scale e^{gamma_t - gamma_b} q_t . kw_b (token(b) <= t).
-//   2. wy_chain_kernel, forward: the state entering each chunk and Vn (32
-//      value columns per CTA), and the final state.
+//   2. the state chain: the state entering each chunk and Vn, and the final
+//      state; wy_chain_tc_kernel (tcgen05, one CTA per head) for bf16 at
+//      Dk = Dv = 128, with W and Kd handed over as operand images, else
+//      wy_chain_kernel (CUDA cores, fp32, 32 value columns per CTA).
 //   3. mdp_out_kernel (one CTA per chunk): o = diag(scale e^gamma) Q S + P Vn.
 // Tokens past the end of the sequence have k = v = beta = 0 and g = 0, so
 // they change nothing.

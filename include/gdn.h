@@ -191,9 +191,13 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
  *   chunk   16, 32 or 64, a multiple of r (accepted for symmetry with the other
  *           entry points: the kernels work on 64 sub-rows, 64 / r tokens, per
  *           chunk, and results do not depend on the chunk beyond rounding)
- *   flags   0 or GDN_QK_L2NORM.  CUDA-core path, fp32 arithmetic: the chunks'
- *           WY factors in parallel, the state chain by 32 value columns per
- *           CTA, then the outputs in parallel (three launches).
+ *   flags   0, or GDN_QK_L2NORM and GDN_PATH_SIMT.  Three launches: the
+ *           chunks' WY factors in parallel (CUDA cores, fp32), the state
+ *           chain, then the outputs in parallel (CUDA cores, fp32).  With bf16
+ *           tensors at Dk = Dv = 128 the chain runs on tcgen05 (one CTA per
+ *           head, fp32 state in tensor memory, bf16 hi / lo split products of
+ *           about 2^-16 relative error); otherwise, or with GDN_PATH_SIMT, on
+ *           the CUDA cores by 32 value columns per CTA.
  *   workspace: masked_deltaproduct_chunk_fwd_workspace_bytes(...) bytes,
  *           16-byte aligned (GDN_ERR_WORKSPACE when missing or short); no
  *           initialisation needed, contents not meaningful afterwards.
@@ -224,8 +228,8 @@ size_t masked_deltaproduct_chunk_bwd_workspace_bytes(int B, int H, int T, int r,
  *     w_i = G^T kw_i;  dv = beta sum_i w_i;  dbeta = sum_i kw_i . (G e_i)
  *     dkw_i = beta G e_i;  dkr_i = -beta D w_i;  dD = G - beta sum_i kr_i w_i^T
  * slice j of dk = slice j of (dkw_j + sum_i mask[i][j] dkr_i), dg = <dD, D>,
- * and the state entering the token gets exp(g) dD; computed chunk-wise
- * (CUDA cores, fp32, three launches as gdn_chunk_bwd).
+ * and the state entering the token gets exp(g) dD; computed chunk-wise in
+ * three launches as gdn_chunk_bwd (flags: GDN_QK_L2NORM, GDN_PATH_SIMT).
  *   q, k, v, beta, g, mask, initial_state, scale, flags, dtype, Dk, Dv, r: as
  *           given to masked_deltaproduct_chunk_fwd (r in {1, 2, 4, 8})
  *   dout [B,H,T,Dv] dtype;  dfinal_state [B,H,Dk,Dv] fp32 or NULL (= zero)
@@ -363,13 +367,16 @@ size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int r, int Dk, int Dv,
  *     G += scale q do^T;  dq = scale S do;  e = v - X^T k,  w = G^T k
  *     dv = beta w;  dbeta = k.(G e);  dk = beta (G e - X w);  G <- G - beta k w^T
  *     dg = <G, X>;  G <- exp(g) G
- * computed chunk-wise in the WY form (64-row chunks, fp32 arithmetic on the
- * CUDA cores, three launches: the chunk factors, the forward state chain and
- * the reverse gradient chain side by side, then the input gradients).
+ * computed chunk-wise in the WY form (64-row chunks) in three launches: the
+ * chunk factors (CUDA cores, fp32); the forward state chain and the reverse
+ * gradient chain side by side; the input gradients (CUDA cores, fp32).  With
+ * bf16 tensors at Dk = Dv = 128 the two chains run on tcgen05 (one CTA per
+ * head and chain, fp32 state in tensor memory, bf16 hi / lo split products of
+ * about 2^-16 relative error); otherwise, or with GDN_PATH_SIMT, on the CUDA
+ * cores in fp32 by 64 value columns per CTA.
  *
  *   q, k, v, beta, g, initial_state, scale, dtype, Dk, Dv: as given to
- *           gdn_chunk_fwd (flags: GDN_QK_L2NORM and GDN_PATH_SIMT, which
- *           changes nothing: this is the only path)
+ *           gdn_chunk_fwd (flags: GDN_QK_L2NORM and GDN_PATH_SIMT)
  *   dout    [B,H,T,Dv] dtype;  dfinal_state [B,H,Dk,Dv] fp32 or NULL (= zero)
  *   dq, dk [B,H,T,Dk], dv [B,H,T,Dv] dtype (written);  dbeta [B,H,T] fp32;
  *   dg [B,H,T] fp32;  dinitial_state [B,H,Dk,Dv] fp32 or NULL (not wanted)
