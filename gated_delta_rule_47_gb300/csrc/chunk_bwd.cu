@@ -92,16 +92,16 @@ __device__ __forceinline__ Chunk chunk_of(const BwdParams &p) {
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LV = DV + 1;
+    constexpr int LK = DK + 4, LV = DV + 1;  // the key-side tiles are read by mm_nt
     float *Ks = sm, *Vs = Ks + kC * LK, *Qs = Vs + kC * LV, *dOs = Qs + kC * LK, *Ws = dOs + kC * LV;
     float *Xa = Ws + kC * LK, *Xb = Xa + kC * LC, *X4 = Xb + kC * LC;
     float *gam = X4 + kC * kC / 4, *eg = gam + kC, *bet = eg + kC, *nrm = bet + kC;
     const Chunk ch = chunk_of(p);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, r = p.r;
 
-    load_rows<T, DK>(Ks, (const T *)p.k + ch.hrow * DK, ch.nrows, p.l2 != 0, nrm);
+    load_rows<T, DK, LK>(Ks, (const T *)p.k + ch.hrow * DK, ch.nrows, p.l2 != 0, nrm);
     load_rows<T, DV>(Vs, (const T *)p.v + ch.hrow * DV, ch.nrows, false, nullptr);
-    load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    load_rows<T, DK, LK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
     load_rows<T, DV>(dOs, (const T *)p.dout + ch.htok * DV, ch.ntok, false, nullptr);
     if (tid < kC) bet[tid] = tid < ch.nrows ? ld_f((const T *)p.beta + ch.hrow + tid) : 0.f;
     if (tid < 32) {  // gamma: inclusive cumulative sum of the rows' log-decays
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
     {
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, Ks, LK, 1, Ks, 1, LK, DK);
+        mm_nt<kThr, 2, 4>(acc, Ks, LK, Ks, LK, DK);
         float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
     {
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, Qs, LK, 1, Ks, 1, LK, DK);
+        mm_nt<kThr, 2, 4>(acc, Qs, LK, Ks, LK, DK);
         float *Pg = p.Pw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_wy_kernel(BwdParams p) {
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LV = DV + 1, TK = DK / 16, TV = DV / 16, NH = DK / 64;
+    // the value-side tiles are read by mm_nt (row stride 4 mod 32 words)
+    constexpr int LK = DK + 1, LV = DV + 4, TK = DK / 16, TV = DV / 16, NH = DK / 64;
     float *Ks = sm, *Qs = Ks + kC * LK, *Vns = Qs + kC * LK, *dOs = Vns + kC * LV, *Hs = dOs + kC * LV;
     float *Xa = Hs + kC * LV, *Xb = Xa + kC * LC;
     float *gam = Xb + kC * LC, *eg = gam + kC, *bet = eg + kC, *nk = bet + kC, *nq = nk + kC;
@@ -270,8 +271,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
 
     load_rows<T, DK>(Ks, (const T *)p.k + ch.hrow * DK, nrows, p.l2 != 0, nk);
     load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ntok, p.l2 != 0, nq);
-    load_rows<T, DV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
-    load_rows<float, DV>(Vns, p.Vnw + ch.ci * kC * DV, kC, false, nullptr);
+    load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
+    load_rows<float, DV, LV>(Vns, p.Vnw + ch.ci * kC * DV, kC, false, nullptr);
     if (tid < kC) {
         gam[tid] = p.Gw[ch.ci * kC + tid];
         eg[tid] = expf(gam[tid]);
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         mm<kThr, 2, TV>(accKdS, Ks + 64 * h, LK, 1, Hs, LV, 1, 64);
         float tz[2][4];
         zero(tz);
-        mm<kThr, 2, 4>(tz, Vns, LV, 1, Hs, 1, LV, DV);
+        mm_nt<kThr, 2, 4>(tz, Vns, LV, Hs, LV, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const float s = expf(gl - gam[ty + 32 * i]);
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     {
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, dOs, LV, 1, Vns, 1, LV, DV);
+        mm_nt<kThr, 2, 4>(acc, dOs, LV, Vns, LV, DV);
         float col[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     {
         float ta[2][4], tk[2][4];
         zero(ta);
-        mm<kThr, 2, 4>(ta, Hs, LV, 1, Vns, 1, LV, DV);
+        mm_nt<kThr, 2, 4>(ta, Hs, LV, Vns, LV, DV);
         {  // K K^T, formed by the WY kernel
             const float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
@@ -454,8 +455,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        mm<kThr, 2, 4>(t1, dOs, LV, 1, Vns, 1, LV, DV);
-        mm<kThr, 2, 4>(t2, Hs, LV, 1, Vns, 1, LV, DV);
+        mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LV, DV);
+        mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LV, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int m = ty + 32 * i;
@@ -547,10 +548,10 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
 }
 
 constexpr size_t wy_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)3 * kC * (DK + 1) + 2 * kC * (DV + 1) + 2 * kC * LC + kC * kC / 4 + 4 * kC);
+    return sizeof(float) * ((size_t)3 * kC * (DK + 4) + 2 * kC * (DV + 1) + 2 * kC * LC + kC * kC / 4 + 4 * kC);
 }
 constexpr size_t grad_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)2 * kC * (DK + 1) + 3 * kC * (DV + 1) + 2 * kC * LC + 9 * kC + 32 * kC + 16);
+    return sizeof(float) * ((size_t)2 * kC * (DK + 1) + 3 * kC * (DV + 4) + 2 * kC * LC + 9 * kC + 32 * kC + 16);
 }
 
 // Workspace floats per (head, chunk).

@@ -104,7 +104,8 @@ struct Sm {
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
     extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LV = DV + 1, LX = (DK > DV ? DK : DV) + 1;
+    // the key tiles are read by mm_nt (row strides 4 mod 32 words)
+    constexpr int LK = DK + 4, LV = DV + 1, LX = (DK > DV ? DK : DV) + 4;
     float *Kt = sm;               // [64][LX] token keys, then W
     float *Kr = Kt + kC * LX;     // [64][LX] read keys, then -P^^T dO
     float *Kw = Kr + kC * LX;     // [64][LK] write keys
@@ -115,9 +116,9 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
     const MbChunk ch = mbchunk(p);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, r = p.r;
 
-    // token keys into Kt with the row stride LX (load_rows writes stride D + 1)
-    load_rows<T, DK>(Kw, (const T *)p.k + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
-    load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    // token keys into Kt with the row stride LX (loaded with the stride LK first)
+    load_rows<T, DK, LK>(Kw, (const T *)p.k + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    load_rows<T, DK, LK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
     for (int e = tid; e < kC * DV; e += kThr) {
         const int a = e / DV, c = e % DV;
         Vs[a * LV + c] = a < ch.nrows ? ld_f((const T *)p.v + (ch.htok + (a >> p.lr)) * DV + c) : 0.f;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
     {  // A over the sub-rows of earlier tokens
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, Kr, LX, 1, Kw, 1, LK, DK);
+        mm_nt<kThr, 2, 4>(acc, Kr, LX, Kw, LK, DK);
         float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
     {  // P^ = scale e^{gamma_t - gamma_b} q_t . kw_b over the sub-rows of tokens up to t
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, Qs, LK, 1, Kw, 1, LK, DK);
+        mm_nt<kThr, 2, 4>(acc, Qs, LK, Kw, LK, DK);
         float *Pg = p.Pw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -268,8 +269,9 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LV = DV + 1, TK = DK / 16, TV = DV / 16, NH = DK / 64;
-    constexpr int LX = (DK > DV ? DK : DV) + 1;
+    // the value-side tiles are read by mm_nt (row strides 4 mod 32 words)
+    constexpr int LK = DK + 1, LV = DV + 4, TK = DK / 16, TV = DV / 16, NH = DK / 64;
+    constexpr int LX = (DK > DV ? DK : DV) + 4;
     float *Kt = sm, *Qs = Kt + kC * LK, *Vns = Qs + kC * LK, *dOs = Vns + kC * LX, *Hs = dOs + kC * LV;
     float *Xa = Hs + kC * LV, *Xb = Xa + kC * LC;
     float *gam = Xb + kC * LC, *eg = gam + kC, *bet = eg + kC, *nk = bet + kC, *nq = nk + kC;
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
 
     load_rows<T, DK>(Kt, (const T *)p.k + ch.htok * DK, ntok, p.l2 != 0, nk);
     load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ntok, p.l2 != 0, nq);
-    load_rows<T, DV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
+    load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
     for (int e = tid; e < kC * DV; e += kThr) Vns[(e / DV) * LX + e % DV] = p.Vnw[ch.ci * kC * DV + e];
     if (tid < kC) {
         gam[tid] = p.Gw[ch.ci * kC + tid];
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         mm_f<kThr, 2, TV>(accKdS, Off<SubKey<true>>{KW, 64 * h}, Sm{Hs, LV, 1}, 64);
         float tz[2][4];
         zero(tz);
-        mm<kThr, 2, 4>(tz, Vns, LX, 1, Hs, 1, LV, DV);
+        mm_nt<kThr, 2, 4>(tz, Vns, LX, Hs, LV, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int a = ty + 32 * i;
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     {
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, dOs, LV, 1, Vns, 1, LX, DV);
+        mm_nt<kThr, 2, 4>(acc, dOs, LV, Vns, LX, DV);
         float col[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     {
         float ta[2][4], tk[2][4];
         zero(ta);
-        mm<kThr, 2, 4>(ta, Hs, LV, 1, Vns, 1, LX, DV);
+        mm_nt<kThr, 2, 4>(ta, Hs, LV, Vns, LX, DV);
         {  // Kr Kw^T, formed by the WY kernel
             const float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
@@ -476,8 +478,8 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        mm<kThr, 2, 4>(t1, dOs, LV, 1, Vns, 1, LX, DV);
-        mm<kThr, 2, 4>(t2, Hs, LV, 1, Vns, 1, LX, DV);
+        mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LX, DV);
+        mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LX, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int m = ty + 32 * i;
@@ -598,11 +600,11 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
 }
 
 constexpr size_t mwy_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)2 * kC * ((DK > DV ? DK : DV) + 1) + 2 * kC * (DK + 1) + kC * (DV + 1) +
+    return sizeof(float) * ((size_t)2 * kC * ((DK > DV ? DK : DV) + 4) + 2 * kC * (DK + 4) + kC * (DV + 1) +
                             2 * kC * LC + kC * kC / 4 + 4 * kC + 64);
 }
 constexpr size_t mgrad_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)2 * kC * (DK + 1) + kC * ((DK > DV ? DK : DV) + 1) + 2 * kC * (DV + 1) +
+    return sizeof(float) * ((size_t)2 * kC * (DK + 1) + kC * ((DK > DV ? DK : DV) + 4) + 2 * kC * (DV + 4) +
                             2 * kC * LC + 9 * kC + 32 * kC + 16 + 64);
 }
 

@@ -1,7 +1,8 @@
 // simt_tile.cuh -- CUDA-core building blocks of the backward kernels: fp32
 // tiles of 64 rows in shared memory (leading dimension = columns + 1, odd, so
-// that rows and columns are both read without bank conflicts), a register-
-// tiled block product over them, and row / warp reductions.
+// that rows and columns are both read without bank conflicts; columns + 4 for
+// tiles that mm_nt reads with 16-byte loads), register-tiled block products
+// over them, and row / warp reductions.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -39,6 +40,37 @@ __device__ __forceinline__ void mm(float (&acc)[TI][TJ], const float *A, int am,
         for (int i = 0; i < TI; ++i)
 #pragma unroll
             for (int j = 0; j < TJ; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+}
+
+// As mm for operands that are both contiguous in k: A(m, k) = A[m lda + k] and
+// B(k, n) = B[n ldb + k], read four k at a time with 16-byte loads.  A and B
+// 16-byte aligned, lda and ldb multiples of 4 (a row stride of 4 mod 32 words
+// keeps the loads free of bank conflicts: the 16 rows a warp reads then cover
+// every bank twice), K a multiple of 4.  Each accumulator sums over k in
+// increasing order, as mm does, so the two give the same bits.
+template <int NTHR, int TI, int TJ>
+__device__ __forceinline__ void mm_nt(float (&acc)[TI][TJ], const float *A, int lda, const float *B, int ldb, int K) {
+    constexpr int RS = NTHR / 16;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const float *a0 = A + ty * lda;
+    const float *b0 = B + tx * ldb;
+#pragma unroll 1
+    for (int k = 0; k < K; k += 4) {
+        float4 a[TI], b[TJ];
+#pragma unroll
+        for (int i = 0; i < TI; ++i) a[i] = *reinterpret_cast<const float4 *>(a0 + RS * i * lda + k);
+#pragma unroll
+        for (int j = 0; j < TJ; ++j) b[j] = *reinterpret_cast<const float4 *>(b0 + 16 * j * ldb + k);
+#pragma unroll
+        for (int i = 0; i < TI; ++i)
+#pragma unroll
+            for (int j = 0; j < TJ; ++j) {
+                acc[i][j] = fmaf(a[i].x, b[j].x, acc[i][j]);
+                acc[i][j] = fmaf(a[i].y, b[j].y, acc[i][j]);
+                acc[i][j] = fmaf(a[i].z, b[j].z, acc[i][j]);
+                acc[i][j] = fmaf(a[i].w, b[j].w, acc[i][j]);
+            }
     }
 }
 
@@ -95,10 +127,10 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// dst[a][0..D) (leading dimension D + 1) = row a of src for a < nvalid, else 0,
-// for the 64 rows of a chunk.  With norm, each row is divided by max(|row|,
-// 1e-12) and its plain norm kept in nrm[a].
-template <typename T, int D>
+// dst[a][0..D) (leading dimension LD, D + 1 unless given) = row a of src for
+// a < nvalid, else 0, for the 64 rows of a chunk.  With norm, each row is
+// divided by max(|row|, 1e-12) and its plain norm kept in nrm[a].
+template <typename T, int D, int LD = D + 1>
 __device__ void load_rows(float *dst, const T *src, int nvalid, bool norm, float *nrm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int a = warp; a < kC; a += kThr / 32) {
@@ -118,7 +150,7 @@ __device__ void load_rows(float *dst, const T *src, int nvalid, bool norm, float
             if (lane == 0) nrm[a] = n;
         }
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) dst[a * (D + 1) + lane + 32 * u] = x[u];
+        for (int u = 0; u < D / 32; ++u) dst[a * LD + lane + 32 * u] = x[u];
     }
 }
 
