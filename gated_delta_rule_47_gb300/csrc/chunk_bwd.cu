@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     zero(accKdS);
     zero(accDK);
     for (int h = 0; h < NH; ++h) {
-        for (int e = tid; e < 64 * DV; e += kThr) Hs[(e / DV) * LV + e % DV] = dSg[(size_t)64 * h * DV + e];
+        stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
         __syncthreads();
         mm<kThr, 2, TV>(accKdS, Ks + 64 * h, LK, 1, Hs, LV, 1, 64);
         float tz[2][4];
@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     }
     {  // <dS', S>
         float s = 0.f;
+#pragma unroll 8
         for (int e = tid; e < DK * DV; e += kThr) s += dSg[e] * Sg[e];
         s = warp_sum(s);
         if ((tid & 31) == 0) red[tid >> 5] = s;
@@ -327,10 +328,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     // 2. P^ (formed by the WY kernel) into Xa, T into Xb
     {
         const float *Pg = p.Pw + ch.ci * kC * kC, *Tg = p.Tw + ch.ci * kC * kC;
-        for (int e = tid; e < kC * kC; e += kThr) {
-            Xa[(e / kC) * LC + e % kC] = Pg[e];
-            Xb[(e / kC) * LC + e % kC] = Tg[e];
-        }
+        stage_rows<kC, kC>(Xa, LC, Pg);
+        stage_rows<kC, kC>(Xb, LC, Tg);
     }
     __syncthreads();
 
@@ -450,7 +449,7 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     //    (S^T q_i).do_i = q_i.(S do_i) and (S^T k_b).dR_b = k_b.(S dR_b).
     float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
     for (int h = 0; h < NH; ++h) {
-        for (int e = tid; e < 64 * DV; e += kThr) Vns[(e / DV) * LV + e % DV] = Sg[(size_t)64 * h * DV + e];
+        stage_rows<64, DV>(Vns, LV, Sg + (size_t)64 * h * DV);
         __syncthreads();
         float t1[2][4], t2[2][4];
         zero(t1);

@@ -119,10 +119,12 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_wy_kernel(MbParams p) {
     // token keys into Kt with the row stride LX (loaded with the stride LK first)
     load_rows<T, DK, LK>(Kw, (const T *)p.k + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
     load_rows<T, DK, LK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
-    for (int e = tid; e < kC * DV; e += kThr) {
-        const int a = e / DV, c = e % DV;
-        Vs[a * LV + c] = a < ch.nrows ? ld_f((const T *)p.v + (ch.htok + (a >> p.lr)) * DV + c) : 0.f;
-    }
+    staged<kC * DV / kThr>(
+        [&](int e) {
+            const int a = e / DV;
+            return a < ch.nrows ? ld_f((const T *)p.v + (ch.htok + (a >> p.lr)) * DV + e % DV) : 0.f;
+        },
+        [&](int e, float x) { Vs[(e / DV) * LV + e % DV] = x; });
     if (tid < kC) bet[tid] = tid < ch.nrows ? ld_f((const T *)p.beta + ch.htok + (tid >> p.lr)) : 0.f;
     if (tid < r * r) msk[tid] = p.mask[tid];
     if (tid < 32) {  // gamma per sub-row: the token's g enters on its first sub-row
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     load_rows<T, DK>(Kt, (const T *)p.k + ch.htok * DK, ntok, p.l2 != 0, nk);
     load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ntok, p.l2 != 0, nq);
     load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
-    for (int e = tid; e < kC * DV; e += kThr) Vns[(e / DV) * LX + e % DV] = p.Vnw[ch.ci * kC * DV + e];
+    stage_rows<kC, DV>(Vns, LX, p.Vnw + ch.ci * kC * DV);
     if (tid < kC) {
         gam[tid] = p.Gw[ch.ci * kC + tid];
         eg[tid] = expf(gam[tid]);
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     zero(accKdS);
     zero(accD);
     for (int h = 0; h < NH; ++h) {
-        for (int e = tid; e < 64 * DV; e += kThr) Hs[(e / DV) * LV + e % DV] = dSg[(size_t)64 * h * DV + e];
+        stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
         __syncthreads();
         mm_f<kThr, 2, TV>(accKdS, Off<SubKey<true>>{KW, 64 * h}, Sm{Hs, LV, 1}, 64);
         float tz[2][4];
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     }
     {  // <dS', S>
         float s = 0.f;
+#pragma unroll 8
         for (int e = tid; e < DK * DV; e += kThr) s += dSg[e] * Sg[e];
         s = warp_sum(s);
         if ((tid & 31) == 0) red[tid >> 5] = s;
@@ -348,10 +351,8 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     // 2. P^ (formed by the WY kernel) into Xa, T into Xb
     {
         const float *Pg = p.Pw + ch.ci * kC * kC, *Tg = p.Tw + ch.ci * kC * kC;
-        for (int e = tid; e < kC * kC; e += kThr) {
-            Xa[(e / kC) * LC + e % kC] = Pg[e];
-            Xb[(e / kC) * LC + e % kC] = Tg[e];
-        }
+        stage_rows<kC, kC>(Xa, LC, Pg);
+        stage_rows<kC, kC>(Xb, LC, Tg);
     }
     __syncthreads();
     // 3. dVn = Kd dS' + P^^T dO into Hs
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     //    products give (S^T q_t).do_t = q_t.(S do_t) and (S^T kr_b).dR_b = kr_b.(S dR_b).
     float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
     for (int h = 0; h < NH; ++h) {
-        for (int e = tid; e < 64 * DV; e += kThr) Vns[(e / DV) * LX + e % DV] = Sg[(size_t)64 * h * DV + e];
+        stage_rows<64, DV>(Vns, LX, Sg + (size_t)64 * h * DV);
         __syncthreads();
         float t1[2][4], t2[2][4];
         zero(t1);

@@ -77,7 +77,7 @@ __device__ __forceinline__ MChunk mchunk(const MdpParams &p) {
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
     extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LV = DV + 1;
+    constexpr int LK = DK + 4, LV = DV + 1;  // the key tiles are read by mm_nt (row stride 4 mod 32 words)
     float *Kt = sm;                // [64][LK] token keys (unit when asked)
     float *Kr = Kt + kC * LK;      // [64][LK] read keys of the sub-rows
     float *Kw = Kr + kC * LK;      // [64][LK] write keys of the sub-rows
@@ -88,12 +88,14 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
     const MChunk ch = mchunk(p);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, r = p.r, sl = DK / r;
 
-    load_rows<T, DK>(Kt, (const T *)p.k + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
-    load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
-    for (int e = tid; e < kC * DV; e += kThr) {
-        const int a = e / DV, c = e % DV;
-        Vs[a * LV + c] = a < ch.nrows ? ld_f((const T *)p.v + (ch.htok + a / r) * DV + c) : 0.f;
-    }
+    load_rows<T, DK, LK>(Kt, (const T *)p.k + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    load_rows<T, DK, LK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    staged<kC * DV / kThr>(
+        [&](int e) {
+            const int a = e / DV;
+            return a < ch.nrows ? ld_f((const T *)p.v + (ch.htok + a / r) * DV + e % DV) : 0.f;
+        },
+        [&](int e, float x) { Vs[(e / DV) * LV + e % DV] = x; });
     if (tid < kC) bet[tid] = tid < ch.nrows ? ld_f((const T *)p.beta + ch.htok + tid / r) : 0.f;
     if (tid < r * r) msk[tid] = p.mask[tid];
     if (tid < 32) {  // gamma per sub-row: the token's g enters on its first sub-row
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
     {
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, Kr, LK, 1, Kw, 1, LK, DK);
+        mm_nt<kThr, 2, 4>(acc, Kr, LK, Kw, LK, DK);
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
     {
         float acc[2][4];
         zero(acc);
-        mm<kThr, 2, 4>(acc, Qs, LK, 1, Kw, 1, LK, DK);
+        mm_nt<kThr, 2, 4>(acc, Qs, LK, Kw, LK, DK);
         float *Pg = p.Pw + ch.ci * kC * kC;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -207,30 +209,34 @@ __global__ void __launch_bounds__(kThr, 1) mdp_wy_kernel(MdpParams p) {
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr, 1) mdp_out_kernel(MdpParams p) {
     extern __shared__ float sm[];
-    constexpr int LK = DK + 1, LV = DV + 1, NH = DK / 64;
+    // both products read their operands along k with 16-byte loads (mm_nt), so
+    // Vn and the blocks of S are staged transposed; row strides 4 mod 32 words
+    constexpr int LK = DK + 4, LT = kC + 4, NH = DK / 64;
     float *Qs = sm;              // [64][LK]
-    float *Vn = Qs + kC * LK;    // [64][LV]
-    float *Hs = Vn + kC * LV;    // [64][LV] a 64-row block of S
-    float *Ps = Hs + kC * LV;    // [64][LC]
-    float *gam = Ps + kC * LC, *nrm = gam + kC;
+    float *VnT = Qs + kC * LK;   // [DV][LT] Vn transposed
+    float *HsT = VnT + DV * LT;  // [DV][LT] a 64-row block of S, transposed
+    float *Ps = HsT + DV * LT;   // [64][LT]
+    float *gam = Ps + kC * LT, *nrm = gam + kC;
     const MChunk ch = mchunk(p);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, r = p.r;
     const float *Sg = p.Sw + ch.ci * DK * DV;
 
-    load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
-    load_rows<float, DV>(Vn, p.Vnw + ch.ci * kC * DV, kC, false, nullptr);
-    for (int e = tid; e < kC * kC; e += kThr) Ps[(e / kC) * LC + e % kC] = p.Pw[ch.ci * kC * kC + e];
+    load_rows<T, DK, LK>(Qs, (const T *)p.q + ch.htok * DK, ch.ntok, p.l2 != 0, nrm);
+    const float *Vg = p.Vnw + ch.ci * kC * DV;
+    staged<kC * DV / kThr>([&](int e) { return Vg[e]; }, [&](int e, float x) { VnT[(e % DV) * LT + e / DV] = x; });
+    stage_rows<kC, kC>(Ps, LT, p.Pw + ch.ci * kC * kC);
     if (tid < kC) gam[tid] = p.Gw[ch.ci * kC + tid];
     float accQS[2][DV / 16], accPV[2][DV / 16];
     zero(accQS);
     zero(accPV);
     for (int h = 0; h < NH; ++h) {
         __syncthreads();
-        for (int e = tid; e < 64 * DV; e += kThr) Hs[(e / DV) * LV + e % DV] = Sg[(size_t)64 * h * DV + e];
+        const float *Sb = Sg + (size_t)64 * h * DV;
+        staged<64 * DV / kThr>([&](int e) { return Sb[e]; }, [&](int e, float x) { HsT[(e % DV) * LT + e / DV] = x; });
         __syncthreads();
-        mm<kThr, 2, DV / 16>(accQS, Qs + 64 * h, LK, 1, Hs, LV, 1, 64);
+        mm_nt<kThr, 2, DV / 16>(accQS, Qs + 64 * h, LK, HsT, LT, 64);
     }
-    mm<kThr, 2, DV / 16>(accPV, Ps, LC, 1, Vn, LV, 1, kC);
+    mm_nt<kThr, 2, DV / 16>(accPV, Ps, LT, VnT, LT, kC);
     T *op = (T *)p.o + ch.htok * DV;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -244,10 +250,10 @@ __global__ void __launch_bounds__(kThr, 1) mdp_out_kernel(MdpParams p) {
 }
 
 constexpr size_t wy_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)4 * kC * (DK + 1) + kC * (DV + 1) + 2 * kC * LC + kC * kC / 4 + 4 * kC + 64);
+    return sizeof(float) * ((size_t)4 * kC * (DK + 4) + kC * (DV + 1) + 2 * kC * LC + kC * kC / 4 + 4 * kC + 64);
 }
 constexpr size_t out_smem(int DK, int DV) {
-    return sizeof(float) * ((size_t)kC * (DK + 1) + 2 * kC * (DV + 1) + kC * LC + 2 * kC);
+    return sizeof(float) * ((size_t)kC * (DK + 4) + 2 * (size_t)DV * (kC + 4) + kC * (kC + 4) + 2 * kC);
 }
 
 size_t per_chunk_floats(int Dk, int Dv) {

@@ -127,30 +127,59 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// Element u of this thread's share of a kThr-strided pass, e = thread + u kThr
+// for u < N: all N values are loaded (load(e)) before any is stored
+// (store(e, x)), so that a pass over global memory waits for one round trip,
+// not N.
+template <int N, class Load, class Store>
+__device__ __forceinline__ void staged(const Load &load, const Store &store) {
+    float x[N];
+#pragma unroll
+    for (int u = 0; u < N; ++u) x[u] = load((int)threadIdx.x + u * kThr);
+#pragma unroll
+    for (int u = 0; u < N; ++u) store((int)threadIdx.x + u * kThr, x[u]);
+}
+
+// dst[(e / C) ld + e % C] = src[e] for the R x C row-major values of src (R C a
+// multiple of kThr), every load in flight before the stores.
+template <int R, int C, typename T>
+__device__ __forceinline__ void stage_rows(float *dst, int ld, const T *src) {
+    static_assert(R * C % kThr == 0, "whole passes");
+    staged<R * C / kThr>([&](int e) { return ld_f(src + e); },
+                         [&](int e, float x) { dst[(e / C) * ld + e % C] = x; });
+}
+
 // dst[a][0..D) (leading dimension LD, D + 1 unless given) = row a of src for
-// a < nvalid, else 0, for the 64 rows of a chunk.  With norm, each row is
-// divided by max(|row|, 1e-12) and its plain norm kept in nrm[a].
+// a < nvalid, else 0, for the 64 rows of a chunk (each warp loads all its rows
+// before it stores any).  With norm, each row is divided by max(|row|, 1e-12)
+// and its plain norm kept in nrm[a].
 template <typename T, int D, int LD = D + 1>
 __device__ void load_rows(float *dst, const T *src, int nvalid, bool norm, float *nrm) {
+    constexpr int NW = kThr / 32, NR = kC / NW;  // warps, rows per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int a = warp; a < kC; a += kThr / 32) {
-        float x[D / 32];
-        float ss = 0.f;
+    float x[NR][D / 32];
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) {
-            x[u] = a < nvalid ? ld_f(src + (size_t)a * D + lane + 32 * u) : 0.f;
-            ss += x[u] * x[u];
-        }
+    for (int j = 0; j < NR; ++j) {
+        const int a = warp + NW * j;
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) x[j][u] = a < nvalid ? ld_f(src + (size_t)a * D + lane + 32 * u) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        const int a = warp + NW * j;
         if (norm) {
+            float ss = 0.f;
+#pragma unroll
+            for (int u = 0; u < D / 32; ++u) ss += x[j][u] * x[j][u];
             ss = warp_sum(ss);
             const float n = sqrtf(ss);
             const float inv = 1.f / fmaxf(n, 1e-12f);
 #pragma unroll
-            for (int u = 0; u < D / 32; ++u) x[u] *= inv;
+            for (int u = 0; u < D / 32; ++u) x[j][u] *= inv;
             if (lane == 0) nrm[a] = n;
         }
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) dst[a * LD + lane + 32 * u] = x[u];
+        for (int u = 0; u < D / 32; ++u) dst[a * LD + lane + 32 * u] = x[j][u];
     }
 }
 
