@@ -46,6 +46,8 @@ size_t scan_tc_workspace_bytes(const ScanArgs &a);
 int launch_scan_tc(const ScanArgs &a, cudaStream_t stream);
 int scan_tc_read_clear_error(cudaStream_t stream);
 int scan_tc_set_wait_limit(unsigned long long polls);
+// The bounded-wait limit gdn_set_wait_limit last set, in ns.
+unsigned long long wait_limit_ns();
 // Cluster shape of the tcgen05 path (heads and WY CTAs per cluster); 0, 0 = automatic.
 int scan_tc_set_cluster_shape(int hc, int nwy);
 // Device address and size of the fixed scratch array behind
@@ -215,6 +217,7 @@ struct WyChainTcArgs {
     const unsigned char *Wimg, *Kdimg;  // [ci] 32 KB bf16 hi | lo images of W and Kd (write_chain_image)
     const float *Uw, *Bw, *Gw;          // [ci][64][128] U, [ci][128][128] B (reverse), [ci][64] gamma
     int BH, NT, roles;
+    unsigned long long timeout_ns;  // bounded-wait limit (set by the launcher)
 };
 int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the chain kernel (GDN_OK or GDN_ERR_TIMEOUT).

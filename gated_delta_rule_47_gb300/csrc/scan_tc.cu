@@ -1601,4 +1601,6 @@ int scan_tc_set_wait_limit(unsigned long long us) {
     return GDN_OK;
 }
 
+unsigned long long wait_limit_ns() { return g_timeout_ns; }
+
 }  // namespace gdn

@@ -45,16 +45,17 @@ static_assert(C_SMEM <= 232448, "chain kernel fits the shared memory of one CTA"
 constexpr uint32_t TM_X = 0, TM_Z = 128, kTmemCols = 256;
 
 __device__ unsigned int g_wyc_error = 0;  // set when a bounded wait of the chain kernel gives up
-constexpr unsigned long long kWycWaitNs = 1000000000ull;
 constexpr unsigned long long kWycDrainNs = 200000000ull;
 
-__device__ __forceinline__ bool wyc_wait(uint64_t *bar, uint32_t parity, unsigned code) {
+// Waits for the phase of the given parity for at most limit ns; gives up at
+// once when another CTA has set the error word.
+__device__ __forceinline__ bool wyc_wait(uint64_t *bar, uint32_t parity, unsigned code, unsigned long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*reinterpret_cast<volatile unsigned *>(&g_wyc_error) != 0u) return false;
-        if (global_timer_ns() - t0 > kWycWaitNs) {
+        if (global_timer_ns() - t0 > limit) {
             atomicOr(&g_wyc_error, code);
             return false;
         }
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x, role = blockIdx.y, NT = p.NT;
     const size_t ci0 = (size_t)bh * NT;
+    const unsigned long long tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < CB_NUM; ++i) mbar_init(&bars[i], (i == CB_XREADY || i == CB_ZREADY) ? 256u : 1u);
@@ -109,8 +111,8 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
             for (int s = 0; s < NT; ++s) {
                 const int b = s & 1;
                 const uint32_t slot = sb + (uint32_t)b * C_SLOT;
-                if (!wyc_wait(&bars[CB_FULL + b], (s >> 1) & 1, 1u)) break;
-                if (!wyc_wait(&bars[CB_XREADY], s & 1, 1u)) break;
+                if (!wyc_wait(&bars[CB_FULL + b], (s >> 1) & 1, 1u, tmo)) break;
+                if (!wyc_wait(&bars[CB_XREADY], s & 1, 1u, tmo)) break;
                 tc_fence_after_sync();
                 // Z^T = X^T M1^T over the 128 keys: hi.hi, hi.lo, lo.hi
 #pragma unroll
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
                                     (pr | ks) != 0);
                 }
                 mma_commit(&bars[CB_ZDONE]);
-                if (!wyc_wait(&bars[CB_ZREADY], s & 1, 1u)) break;
+                if (!wyc_wait(&bars[CB_ZREADY], s & 1, 1u, tmo)) break;
                 tc_fence_after_sync();
                 // X^T +/-= Z'^T M2 over the 64 rows
 #pragma unroll
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
             for (int s = 0; s < NT; ++s) {
                 const int b = s & 1;
                 // slot b held chunk s-2, whose MMAs are complete when CB_FREE + b completes
-                if (s >= 2 && !wyc_wait(&bars[CB_FREE + b], ((s - 2) >> 1) & 1, 2u)) break;
+                if (s >= 2 && !wyc_wait(&bars[CB_FREE + b], ((s - 2) >> 1) & 1, 2u, tmo)) break;
                 const size_t ci = ci0 + (size_t)(role == 0 ? s : NT - 1 - s);
                 mbar_arrive_expect_tx(&bars[CB_FULL + b], 65536u);
                 bulk_load_global(sm + b * C_SLOT, p.Wimg + ci * 32768, 32768u, &bars[CB_FULL + b]);
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
                 for (int i = 0; i < 64; ++i)
                     x[i] = init ? init[((size_t)bh * 128 + 64 * hh + i) * 128 + dv] : 0.f;
             } else {
-                ok = warp_ok(wyc_wait(&bars[CB_XDONE], (s - 1) & 1, 4u));
+                ok = warp_ok(wyc_wait(&bars[CB_XDONE], (s - 1) & 1, 4u, tmo));
                 if (!ok) break;
                 tc_fence_after_sync();
                 uint32_t r[4][16];
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
                     r[i] = __float_as_uint(role == 0 ? el * x[16 * j + i] : el * x[16 * j + i] + pre[16 * j + i]);
                 tmem_st16(tmem + lb + TM_X + 64 * hh + 16 * j, r);
             }
-            ok = warp_ok(wyc_wait(&bars[CB_ZDONE], s & 1, 4u));
+            ok = warp_ok(wyc_wait(&bars[CB_ZDONE], s & 1, 4u, tmo));
             if (!ok) break;
             tc_fence_after_sync();
             float z[32];
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
         }
         float *out = role == 0 ? p.sf : p.ds0;
         if (ok && NT > 0) {
-            ok = warp_ok(wyc_wait(&bars[CB_XDONE], (NT - 1) & 1, 4u));
+            ok = warp_ok(wyc_wait(&bars[CB_XDONE], (NT - 1) & 1, 4u, tmo));
             if (ok && out) {
                 tc_fence_after_sync();
 #pragma unroll 1
@@ -294,10 +296,12 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
 
 int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t st) {
     if (a.BH <= 0 || a.NT <= 0 || a.roles < 1 || a.roles > 2) return GDN_ERR_INVALID_ARG;
+    WyChainTcArgs p = a;
+    p.timeout_ns = wait_limit_ns();
     if (cudaFuncSetAttribute(wy_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
-    wy_chain_tc_kernel<<<dim3((unsigned)a.BH, (unsigned)a.roles), kCThr, C_SMEM, st>>>(a);
+    wy_chain_tc_kernel<<<dim3((unsigned)a.BH, (unsigned)a.roles), kCThr, C_SMEM, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -488,10 +488,13 @@ unsigned long long gdn_launch_count(void);
 
 /*
  * Test hook for the bounded-wait path: sets the wall-clock limit, in
- * microseconds, of every bounded device wait in later launches (0 restores
- * the default of one second).  A wait that runs out sets GDN_ERR_TIMEOUT in
- * the device error word and its kernel stops early; the outputs of that
- * call are then undefined, but the context stays usable.
+ * microseconds, of the bounded device waits in later launches of the
+ * tensor-core scan (gdn_chunk_fwd, deltaproduct_chunk_fwd) and of the
+ * tensor-core state chains (the chunk backward passes
+ * and the block-masked forward); 0 restores the default of one second.  The
+ * other tensor-core kernels keep a one-second limit.  A wait that runs out
+ * sets GDN_ERR_TIMEOUT in the device error word and its kernel stops early;
+ * the outputs of that call are then undefined, but the context stays usable.
  */
 int gdn_set_wait_limit(unsigned long long polls);
 

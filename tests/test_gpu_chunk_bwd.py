@@ -196,3 +196,28 @@ def test_tensor_core_chain_matches_the_cuda_core_chain(r, T):
     for name, x, y in zip(NAMES, tc, simt):
         tol = 5e-3 if x.dtype == torch.bfloat16 else 2e-4
         assert rel_err(x, y.double().cpu().numpy()) <= tol, name
+
+
+def test_chain_bounded_wait_gives_up_and_context_survives():
+    """A 1-microsecond wait limit makes the tensor-core chains' waits run out:
+    the call reports GDN_ERR_TIMEOUT through the device error word, and with
+    the default limit restored the next call is correct."""
+    inp, do, dsf = grads_case(1, 2, 1024, 128, 128, "bf16", False, seed=50)
+    d = to_dev(inp)
+    assert binding.device_error() == 0
+    try:
+        binding.set_wait_limit(1)
+        binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"], dsf.cuda(),
+                              need_dinitial=True)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 6
+    finally:
+        binding.set_wait_limit(0)
+    assert binding.device_error() == 0
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"],
+                                dsf.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name
