@@ -635,10 +635,20 @@ __global__ void __launch_bounds__(512) cam_prep_bwd_kernel(CamBwdParams p) {
     const int c0 = 8 * threadIdx.x;
     const bool act = c0 < C;
     const int h = act ? c0 / p.D : 0, d0 = act ? c0 % p.D : 0;
-    float q[8] = {0}, k[8] = {0};
+    // the token's streamed loads are all issued before the first block
+    // reduction, so that the CTA waits for one memory round trip
+    float q[8] = {0}, k[8] = {0}, dy[3][8];
+    float gpre = 0.f, gpost = 0.f;
+    const size_t ob = (((size_t)b * p.H + h) * p.N + n) * p.D + d0;
     if (act) {
         ld8(static_cast<const T *>(p.q_raw) + bn * C + c0, q);
         ld8(static_cast<const T *>(p.k_raw) + bn * C + c0, k);
+        ld8(static_cast<const T *>(p.dq_out) + ob, dy[0]);
+        ld8(static_cast<const T *>(p.dk_out) + ob, dy[1]);
+        ld8(static_cast<const T *>(p.dv_out) + ob, dy[2]);
+        const size_t si = ((size_t)b * p.H + h) * p.N + n;
+        gpre = p.dpre ? p.dpre[si] : 0.f;
+        gpost = p.dpost ? p.dpost[si] : 0.f;
     }
     float sq = 0.f, sk = 0.f;
 #pragma unroll
@@ -656,10 +666,7 @@ __global__ void __launch_bounds__(512) cam_prep_bwd_kernel(CamBwdParams p) {
     }
     float dxq[8] = {0}, dxk[8] = {0}, dav[8] = {0};
     if (act) {
-        const size_t ob = (((size_t)b * p.H + h) * p.N + n) * p.D + d0;
-        const size_t si = ((size_t)b * p.H + h) * p.N + n;
-        const float gpre = p.dpre ? p.dpre[si] : 0.f, gpost = p.dpost ? p.dpost[si] : 0.f;
-        float P[2][16];
+        float P[2][16];  // the token's projections (the same for every thread: cached loads)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             P[0][e] = p.proj_q[bn * 16 + e];
@@ -706,10 +713,6 @@ __global__ void __launch_bounds__(512) cam_prep_bwd_kernel(CamBwdParams p) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) ko[e] = ak[e] * cs[e] + ak[e ^ 1] * sn[e];
         }
-        float dy[3][8];
-        ld8(static_cast<const T *>(p.dq_out) + ob, dy[0]);
-        ld8(static_cast<const T *>(p.dk_out) + ob, dy[1]);
-        ld8(static_cast<const T *>(p.dv_out) + ob, dy[2]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) dy[1][e] += 2.f * ko[e] * gpost;
         float da[3][8];
