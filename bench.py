@@ -534,7 +534,7 @@ def secondary(args, dev):
     bms = timeit(lambda: binding.cam_scan_bwd(outs[0], outs[1], outs[2], beta_f, decay_f, gob, l2norm=True,
                                               workspace=wsb))
     out["cam_frames_bwd_b2f21s1560h16d128_bf16"] = {"ms": bms, "tokens_per_s": w.B * w.T / (bms * 1e-3),
-                                                    "path": "tcgen05 for the frame products and token gradients, CUDA-core chains"}
+                                                    "path": "tcgen05 for the frame products, the chains and the token gradients"}
     del gob, wsb
     # the prep fused into the frame scan: raw q, k, v in, o out, one call
     wsx = torch.empty(binding.cam_prep_scan_workspace_bytes(w.B, w.T, w.H, w.D, F), dtype=torch.uint8, device=dev)
@@ -554,7 +554,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--ref-heads", type=int, default=64,
                     help="heads of the workload the CPU oracle runs per sample")

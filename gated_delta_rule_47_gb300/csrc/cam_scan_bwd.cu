@@ -18,9 +18,11 @@
 // Four launches:
 //   1. fb_frame_kernel (one CTA per frame, head and product): G_f, H_f and P_f
 //      as sums over the frame's 64-token tiles.
-//   2. fb_chain_kernel: the states E_f (forward) and the gradients dX_f
-//      (reverse, down to the initial state's) side by side, each CTA holding
-//      32 value columns of one head.
+//   2. the states E_f (forward) and the gradients dX_f (reverse, down to the
+//      initial state's) side by side: fb_chain_tc_kernel (bf16, Dk = Dv = 128,
+//      one CTA per head and chain, the product G_f X on tcgen05 with G_f as
+//      the bf16 hi | lo image the frame kernel writes), else fb_chain_kernel
+//      (CUDA cores, each CTA holding 32 value columns of one head).
 //   3. the token gradients, and each tile's share of ddecay:
 //      fb_token_tc_kernel (bf16, Dk = Dv = 128, one CTA per 128-token tile):
 //      K and dO tiles by TMA, the frame's E_f, dX_f and X_f as bf16 hi / lo
@@ -63,6 +65,10 @@ struct FbParams {
     int F, S, N, tiles, BH;
     float scale;
     int l2;
+    // 1 when the frame kernel writes G_f as the tensor-core chain's bf16 hi | lo
+    // operand image (K-major: two 64-column blocks of 128 swizzled rows, hi then
+    // lo) in place of its fp32 copy
+    int gimg;
 };
 
 // ======================================== 1. the frame products G, H and P
@@ -916,16 +922,228 @@ __global__ void __launch_bounds__(kFrThr, 1)
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
             const float sc = part == 2 ? p.scale : 1.f;
             float *out = (part == 0 ? p.Gw : (part == 1 ? p.Hw : p.Pw)) + fi * 16384 + (size_t)r * 128;
+            if (part == 0 && p.gimg) {
+                // G_f as the chain's operand image: row r, 16-byte chunks of 8 columns
+                uint8_t *img = reinterpret_cast<uint8_t *>(p.Gw + fi * 16384);
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                uint32_t x[16];
-                tmem_ld16(tmem + lb + 16 * cc, x);
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t x[16];
+                    tmem_ld16(tmem + lb + 16 * cc, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[e] = __uint_as_float(x[8 * g + e]);
+                        uint4 hi, lo;
+                        split8(y, hi, lo);
+                        const int c = 16 * cc + 8 * g;
+                        const uint32_t off = (uint32_t)(c >> 6) * 16384u + sw128_offset((uint32_t)r, (uint32_t)(c & 63));
+                        *reinterpret_cast<uint4 *>(img + off) = hi;
+                        *reinterpret_cast<uint4 *>(img + 32768 + off) = lo;
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t x[16];
+                    tmem_ld16(tmem + lb + 16 * cc, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<float4 *>(out + 16 * cc + 4 * j) =
+                            make_float4(sc * __uint_as_float(x[4 * j]), sc * __uint_as_float(x[4 * j + 1]),
+                                        sc * __uint_as_float(x[4 * j + 2]), sc * __uint_as_float(x[4 * j + 3]));
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ================================== 2'. the chains on tcgen05 (bf16, D = 128)
+// fb_chain_tc_kernel: one CTA per head and direction (blockIdx.y: 0 = the
+// states E_f, 1 = the gradients dX_f), the 128 x 128 state held transposed in
+// the registers of sixteen epilogue warps (thread = value index dv, and a
+// quarter hh of the key indices).  Per frame each thread writes its part of the fp32
+// snapshot, of the token kernel's bf16 hi | lo image and of the state's own
+// hi | lo operand (K-major, value rows); one thread issues
+// Z^T = X^T G_f^T as hi.hi + hi.lo + lo.hi (24 MMAs, M = N = 128) into TMEM,
+// and the threads form E_{f+1} = d_f (E_f - G_f E_f) + H_f, or
+// dE_f = d_f (dX_f - G_f dX_f) with dX_f = dE_{f+1} + P_f.  G_f arrives as the
+// bf16 hi | lo image the frame kernel writes in place of its fp32 copy,
+// double-buffered with bulk copies.
+constexpr int kFcThr = 640;           // warp 0 issues, warp 1 holds TMEM, warp 2 loads, warps 4..19 epilogue
+constexpr int kFcEpi = 512;           // epilogue threads
+constexpr uint32_t FC_G = 0;          // two slots of G_f hi | lo (64 KB each)
+constexpr uint32_t FC_X = 131072;     // X^T hi | lo: K-major [2 key blocks][128 value rows][128 B]
+constexpr uint32_t FC_BAR = FC_X + 65536;
+enum { FCB_FULL = 0, FCB_FREE = 2, FCB_XREADY = 4, FCB_ZDONE, FCB_DRAIN, FCB_NUM };
+constexpr uint32_t FC_TSLOT = FC_BAR + 8 * FCB_NUM;
+constexpr uint32_t FC_SMEM = FC_TSLOT + 16 + 1024;  // + alignment of the base to 1024 bytes
+static_assert(FC_SMEM <= 232448, "frame chain kernel fits the shared memory of one CTA");
+
+// This thread's column dv of rows 32 hh .. 32 hh + 31 of a 128 x 128 matrix
+// into its bf16 hi | lo image (as write_image lays it out).
+__device__ __forceinline__ void write_col_image(uint8_t *img, const float (&x)[32], int hh, int dv) {
+    uint8_t *base = img + (uint32_t)(dv >> 6) * 16384u;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t off = tc::sw128_offset((uint32_t)(32 * hh + i), (uint32_t)(dv & 63));
+        const __nv_bfloat16 h = __float2bfloat16_rn(x[i]);
+        *reinterpret_cast<__nv_bfloat16 *>(base + off) = h;
+        *reinterpret_cast<__nv_bfloat16 *>(base + 32768 + off) = __float2bfloat16_rn(x[i] - __bfloat162float(h));
+    }
+}
+
+__global__ void __launch_bounds__(kFcThr, 1) fb_chain_tc_kernel(FbParams p) {
+    using namespace tc;
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + FC_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + FC_TSLOT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x, role = blockIdx.y, F = p.F;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < FCB_NUM; ++i) mbar_init(&bars[i], i == FCB_XREADY ? (uint32_t)kFcEpi : 1u);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id = idesc_bf16(128, 128, false, false);
+            for (int s = 0; s < F; ++s) {
+                const int b = s & 1;
+                if (!fb_wait(&bars[FCB_FULL + b], (s >> 1) & 1, 32u)) break;
+                if (!fb_wait(&bars[FCB_XREADY], s & 1, 32u)) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int pr = 0; pr < 3; ++pr) {
+                    const uint32_t xa = sb + FC_X + (pr == 2 ? 32768u : 0u);
+                    const uint32_t gb = sb + FC_G + (uint32_t)b * 65536u + (pr == 1 ? 32768u : 0u);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem, smem_desc(xa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    smem_desc(gb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id, (pr | ks) != 0);
+                }
+                mma_commit(&bars[FCB_ZDONE]);
+                mma_commit(&bars[FCB_FREE + b]);
+            }
+            mma_commit(&bars[FCB_DRAIN]);
+            mbar_wait(&bars[FCB_DRAIN], 0, 200000000ull);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------- G_f images, bulk copies
+        if (lane == 0) {
+            int armed[2] = {0, 0};
+            for (int s = 0; s < F; ++s) {
+                const int b = s & 1;
+                // slot b held frame s-2, whose MMAs are complete when FCB_FREE + b completes
+                if (s >= 2 && !fb_wait(&bars[FCB_FREE + b], ((s - 2) >> 1) & 1, 33u)) break;
+                const size_t fi = (size_t)bh * F + (role == 0 ? s : F - 1 - s);
+                const uint8_t *g = reinterpret_cast<const uint8_t *>(p.Gw + fi * 16384);
+                mbar_arrive_expect_tx(&bars[FCB_FULL + b], 65536u);
+                bulk_load_global(sm + FC_G + b * 65536, g, 32768u, &bars[FCB_FULL + b]);
+                bulk_load_global(sm + FC_G + b * 65536 + 32768, g + 32768, 32768u, &bars[FCB_FULL + b]);
+                armed[b]++;
+            }
+            for (int b = 0; b < 2; ++b)
+                if (armed[b]) mbar_wait(&bars[FCB_FULL + b], (armed[b] - 1) & 1, 200000000ull);
+        }
+    } else if (warp >= 4) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3, hh = (warp - 4) >> 2;
+        const int dv = 32 * q + lane;
+        const uint32_t lb = (uint32_t)(32 * q) << 16;
+        const float *init = role == 0 ? p.s0 : p.dsf;
+        float x[32], pre[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = init ? init[((size_t)bh * 128 + 32 * hh + i) * 128 + dv] : 0.f;
+        // H_f (states: added after this frame's product) or P_f (gradients: added
+        // before it, so loaded one frame ahead), rows 32 hh.., column dv
+        auto load_pre = [&](int f) {
+            const float *src = (role == 0 ? p.Hw : p.Pw) + ((size_t)bh * F + f) * 16384 + (size_t)(32 * hh) * 128 + dv;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pre[i] = src[(size_t)i * 128];
+        };
+        if (role == 1 && F > 0) load_pre(F - 1);
+        bool ok = true;
+        for (int s = 0; s < F; ++s) {
+            const int f = role == 0 ? s : F - 1 - s;
+            const size_t fi = (size_t)bh * F + f;
+            const float d = p.decay[fi];
+            if (role == 1) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] += pre[i];  // dX_f = dE_{f+1} + P_f
+            }
+            {  // the snapshot, the token kernel's image, and X^T as the MMA operand
+                const size_t slot = role == 0 ? (size_t)bh * (F + 1) + f : fi;
+                float *sn = (role == 0 ? p.Ew : p.dXw) + slot * 16384 + (size_t)(32 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sn[(size_t)i * 128] = x[i];
+                write_col_image((role == 0 ? p.Eimg : p.dXimg) + slot * kImg, x, hh, dv);
+                uint8_t *xo = sm + FC_X + (hh >> 1) * 16384;  // key block of rows 32 hh..
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = x[8 * c + e];
+                    uint4 hi, lo;
+                    split8(y, hi, lo);
+                    const uint32_t off = sw128_offset((uint32_t)dv, (uint32_t)(32 * (hh & 1) + 8 * c));
+                    *reinterpret_cast<uint4 *>(xo + off) = hi;
+                    *reinterpret_cast<uint4 *>(xo + 32768 + off) = lo;
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&bars[FCB_XREADY]);
+            }
+            if (role == 0)
+                load_pre(f);
+            else if (s + 1 < F)
+                load_pre(f - 1);
+            ok = warp_all_ok(fb_wait(&bars[FCB_ZDONE], s & 1, 34u));
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t z[16];
+                tmem_ld16(tmem + lb + 32 * hh + 16 * j, z);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<float4 *>(out + 16 * cc + 4 * j) =
-                        make_float4(sc * __uint_as_float(x[4 * j]), sc * __uint_as_float(x[4 * j + 1]),
-                                    sc * __uint_as_float(x[4 * j + 2]), sc * __uint_as_float(x[4 * j + 3]));
+                for (int i = 0; i < 16; ++i) {
+                    const float gx = __uint_as_float(z[i]);
+                    x[16 * j + i] = role == 0 ? d * (x[16 * j + i] - gx) + pre[16 * j + i] : d * (x[16 * j + i] - gx);
+                }
+            }
+            tc_fence_before_sync();  // the TMEM reads complete before the next frame's MMAs (after FCB_XREADY)
+        }
+        if (ok) {
+            if (role == 0) {  // the state after the last frame
+                const size_t slot = (size_t)bh * (F + 1) + F;
+                float *sn = p.Ew + slot * 16384 + (size_t)(32 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sn[(size_t)i * 128] = x[i];
+                write_col_image(p.Eimg + slot * kImg, x, hh, dv);
+            } else if (p.ds0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) p.ds0[((size_t)bh * 128 + 32 * hh + i) * 128 + dv] = x[i];
             }
         }
     }
@@ -1025,12 +1243,20 @@ int run(const CamScanBwdArgs &a, cudaStream_t st) {
         if (cudaFuncSetAttribute(fb_frame_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FR_SMEM) !=
             cudaSuccess)
             return GDN_ERR_CUDA;
+        p.gimg = 1;  // G_f as the tensor-core chain's operand image
         fb_frame_tc_kernel<<<dim3((unsigned)a.F, (unsigned)BH, 3), kFrThr, FR_SMEM, st>>>(mK, mV, mQ, mDO, p);
     } else {
         fb_frame_kernel<T, DK, DV><<<dim3((unsigned)a.F, (unsigned)BH, 3), kThr, s1, st>>>(p);
     }
     note_launch();
-    fb_chain_kernel<DK, DV><<<dim3((unsigned)(DV / kSl), (unsigned)BH, 2), kFChainThr, s2, st>>>(p);
+    if (p.gimg) {
+        if (cudaFuncSetAttribute(fb_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FC_SMEM) !=
+            cudaSuccess)
+            return GDN_ERR_CUDA;
+        fb_chain_tc_kernel<<<dim3((unsigned)BH, 2), kFcThr, FC_SMEM, st>>>(p);
+    } else {
+        fb_chain_kernel<DK, DV><<<dim3((unsigned)(DV / kSl), (unsigned)BH, 2), kFChainThr, s2, st>>>(p);
+    }
     note_launch();
     if (tc) {
         p.tiles = (a.S + kTcRows - 1) / kTcRows;

@@ -434,13 +434,14 @@ size_t cam_scan_bwd_workspace_bytes(int B, int H, int F, int S, int Dk, int Dv, 
  *           CUDA cores
  *   workspace: cam_scan_bwd_workspace_bytes bytes, 16-byte aligned.
  * Four launches: the frame products (one CTA per frame, head and product),
- * the forward state chain and the reverse gradient chain side by side (32
- * value columns per CTA, fp32 on the CUDA cores), the token gradients, then
- * each frame's ddecay.  For bf16 with Dk = Dv = 128 on an sm_10x device the
- * frame products and the token gradients run on tcgen05 (fp32 accumulators
- * in TMEM; the fp32 operands split into bf16 hi + lo, products formed as
+ * the forward state chain and the reverse gradient chain side by side, the
+ * token gradients, then each frame's ddecay.  For bf16 with Dk = Dv = 128 on
+ * an sm_10x device the frame products, the chains (one CTA per head and
+ * chain) and the token gradients run on tcgen05 (fp32 accumulators in TMEM;
+ * the fp32 operands split into bf16 hi + lo, products formed as
  * hi.hi + hi.lo + lo.hi; the token kernel persistent over 128-token tiles);
- * otherwise on the CUDA cores in fp32 (64-token tiles).
+ * otherwise on the CUDA cores in fp32 (chains by 32 value columns per CTA,
+ * 64-token tiles).
  */
 int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, const float *decay,
                  const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
