@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
+#include "simt_tile.cuh"
 #include "tri_inverse.cuh"
 
 namespace gdn {
@@ -44,7 +45,9 @@ struct SimtParams {
 
 template <int DK, int C>
 struct SimtSmem {
-    static constexpr int KP = DK + 1, VP = kBV + 1, CP = C + 1;
+    // the key and query tiles have a row stride of DK + 4 (4 mod 32 words), so
+    // that the K K^T and Q K^T products read them with 16-byte loads
+    static constexpr int KP = DK + 4, VP = kBV + 1, CP = C + 1;
     static constexpr int floats = 2 * C * KP + C * VP + DK * VP + 3 * C * CP + 2 * C * VP + 3 * C + C * C / 4;
     static constexpr size_t bytes = sizeof(float) * floats;
 };
@@ -82,16 +85,18 @@ __device__ void unit_rows(float *X, int stride, int nrows, int warp, int lane, i
 }
 
 template <typename Tin, int DK, int C>
-__global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
+__global__ void __launch_bounds__(kThreads, 1) scan_simt_kernel(SimtParams p) {
     using L = SimtSmem<DK, C>;
     constexpr int KP = L::KP, VP = L::VP, CP = L::CP;
-    extern __shared__ float smem[];
+    constexpr int TC = C / 16;   // 16-row blocks of a chunk a thread covers (rows ty + 16 i)
+    constexpr int TD = DK / 16;  // 16-row blocks of the state
+    extern __shared__ __align__(16) float smem[];
     float *Ks = smem;            // [C][KP]   keys of the chunk
     float *Qs = Ks + C * KP;     // [C][KP]   queries (C/r rows used)
     float *Vs = Qs + C * KP;     // [C][VP]   value tile
     float *Ss = Vs + C * VP;     // [DK][VP]  fp32 state tile
     float *As = Ss + DK * VP;    // [C][CP]   A (strictly lower)
-    float *Ts = As + C * CP;     // [C][CP]   (I + A)^-1
+    float *Ts = As + C * CP;     // [C][CP]   (I + A)^-1 (zero above the diagonal)
     float *Ps = Ts + C * CP;     // [C][CP]   decay-masked q.k, s <= t
     float *Rs = Ps + C * CP;     // [C][VP]   R
     float *Ds = Rs + C * VP;     // [C][VP]   Delta
@@ -100,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
     float *eS = bet + C;         // [C] exp(gam_last - gam_s)
     float *Xs = eS + C;          // [C*C/4] scratch of the blocked inverse
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, tx = tid & 15, ty = tid >> 4;
     const int vt = blockIdx.x;
     const size_t head = blockIdx.y;
     const int r = p.r, Dv = p.Dv, T = p.T;
@@ -119,6 +124,8 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
         const int d = i / kBV, j = i % kBV;
         Ss[d * VP + j] = p.s0 ? p.s0[(head * DK + d) * Dv + vt * kBV + j] : 0.f;
     }
+    // the inverse writes only the lower triangle of T; its product reads all of it
+    for (int i = tid; i < C * CP; i += kThreads) Ts[i] = 0.f;
 
     for (long c0 = 0; c0 < rows; c0 += Ce) {
         const int Lr = (int)min((long)Ce, rows - c0);  // valid rows (a multiple of r)
@@ -149,68 +156,90 @@ __global__ void __launch_bounds__(kThreads) scan_simt_kernel(SimtParams p) {
         const float glast = gam[C - 1];
         if (tid < C) eS[tid] = expf(glast - gam[tid]);
 
-        // A (strictly lower) and the decay-masked query-key scores.
-        for (int i = tid; i < C * C; i += kThreads) {
-            const int t = i / C, s = i % C;
-            float a = 0.f;
-            if (s < t) {
-                float acc = 0.f;
-#pragma unroll 8
-                for (int d = 0; d < DK; ++d) acc += Ks[t * KP + d] * Ks[s * KP + d];
-                a = bet[t] * expf(gam[t] - gam[s]) * acc;
-            }
-            As[t * CP + s] = a;
-            float pv = 0.f;
-            if (t < CQ) {
-                const int row = t * r + r - 1;
-                if (s <= row) {
-                    float acc = 0.f;
-#pragma unroll 8
-                    for (int d = 0; d < DK; ++d) acc += Qs[t * KP + d] * Ks[s * KP + d];
-                    pv = expf(gam[row] - gam[s]) * acc;
+        // A (strictly lower) and the decay-masked query-key scores, from the
+        // block products K K^T and Q K^T
+        {
+            float acc[TC][TC];
+            tile::zero(acc);
+            tile::mm_nt<kThreads, TC, TC>(acc, Ks, KP, Ks, KP, DK);
+#pragma unroll
+            for (int i = 0; i < TC; ++i)
+#pragma unroll
+                for (int j = 0; j < TC; ++j) {
+                    const int t = ty + 16 * i, s = tx + 16 * j;
+                    As[t * CP + s] = s < t ? bet[t] * expf(gam[t] - gam[s]) * acc[i][j] : 0.f;
                 }
-            }
-            Ps[t * CP + s] = pv;
+            tile::zero(acc);
+            tile::mm_nt<kThreads, TC, TC>(acc, Qs, KP, Ks, KP, DK);
+#pragma unroll
+            for (int i = 0; i < TC; ++i)
+#pragma unroll
+                for (int j = 0; j < TC; ++j) {
+                    const int t = ty + 16 * i, s = tx + 16 * j, row = t * r + r - 1;
+                    Ps[t * CP + s] = (t < CQ && s <= row) ? expf(gam[row] - gam[s]) * acc[i][j] : 0.f;
+                }
         }
         // R = diag(beta) (V - diag(exp(gam)) K S)
-        for (int i = tid; i < C * kBV; i += kThreads) {
-            const int t = i / kBV, j = i % kBV;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < DK; ++d) acc += Ks[t * KP + d] * Ss[d * VP + j];
-            Rs[t * VP + j] = bet[t] * (Vs[t * VP + j] - expf(gam[t]) * acc);
+        {
+            float acc[TC][4];
+            tile::zero(acc);
+            tile::mm<kThreads, TC, 4>(acc, Ks, KP, 1, Ss, VP, 1, DK);
+#pragma unroll
+            for (int i = 0; i < TC; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = ty + 16 * i, c = tx + 16 * j;
+                    Rs[t * VP + c] = bet[t] * (Vs[t * VP + c] - expf(gam[t]) * acc[i][j]);
+                }
         }
         __syncthreads();
         // (I + A)^-1: 16 x 16 diagonal blocks, then the 16- and 32-level merges
         unit_lower_inverse<C, kThreads>(As, Ts, Xs, CP);
         // Delta = (I + A)^-1 R
-        for (int i = tid; i < C * kBV; i += kThreads) {
-            const int t = i / kBV, j = i % kBV;
-            float acc = 0.f;
-            for (int s = 0; s <= t; ++s) acc += Ts[t * CP + s] * Rs[s * VP + j];
-            Ds[t * VP + j] = acc;
+        {
+            float acc[TC][4];
+            tile::zero(acc);
+            tile::mm<kThreads, TC, 4>(acc, Ts, CP, 1, Rs, VP, 1, C);
+#pragma unroll
+            for (int i = 0; i < TC; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) Ds[(ty + 16 * i) * VP + tx + 16 * j] = acc[i][j];
         }
         __syncthreads();
         // Outputs of the chunk's tokens (read the state before this chunk's update).
-        for (int i = tid; i < LQ * kBV; i += kThreads) {
-            const int t = i / kBV, j = i % kBV;
-            const int row = t * r + r - 1;
-            float inter = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < DK; ++d) inter += Qs[t * KP + d] * Ss[d * VP + j];
-            float intra = 0.f;
-            for (int s = 0; s <= row; ++s) intra += Ps[t * CP + s] * Ds[s * VP + j];
-            from_f32(op + (tok0 + t) * Dv + j, p.scale * (expf(gam[row]) * inter + intra));
+        {
+            float inter[TC][4], intra[TC][4];
+            tile::zero(inter);
+            tile::zero(intra);
+            tile::mm<kThreads, TC, 4>(inter, Qs, KP, 1, Ss, VP, 1, DK);
+            tile::mm<kThreads, TC, 4>(intra, Ps, CP, 1, Ds, VP, 1, C);
+#pragma unroll
+            for (int i = 0; i < TC; ++i) {
+                const int t = ty + 16 * i;
+                if (t < LQ) {
+                    const float eg = expf(gam[t * r + r - 1]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        from_f32(op + (tok0 + t) * Dv + tx + 16 * j, p.scale * (eg * inter[i][j] + intra[i][j]));
+                }
+            }
         }
         __syncthreads();
-        // State update.
-        const float dl = expf(glast);
-        for (int i = tid; i < DK * kBV; i += kThreads) {
-            const int d = i / kBV, j = i % kBV;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int s = 0; s < C; ++s) acc += Ks[s * KP + d] * eS[s] * Ds[s * VP + j];
-            Ss[d * VP + j] = dl * Ss[d * VP + j] + acc;
+        // State update S <- exp(gam_last) S + K^T diag(exp(gam_last - gam)) Delta
+        for (int i = tid; i < C * kBV; i += kThreads) Ds[(i / kBV) * VP + i % kBV] *= eS[i / kBV];
+        __syncthreads();
+        {
+            const float dl = expf(glast);
+            float acc[TD][4];
+            tile::zero(acc);
+            tile::mm<kThreads, TD, 4>(acc, Ks, 1, KP, Ds, VP, 1, C);
+#pragma unroll
+            for (int i = 0; i < TD; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int d = ty + 16 * i, c = tx + 16 * j;
+                    Ss[d * VP + c] = dl * Ss[d * VP + c] + acc[i][j];
+                }
         }
     }
     __syncthreads();
