@@ -321,30 +321,15 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         const float *t64 = reinterpret_cast<const float *>(sm + GR_T64);
         int j = 0;
         bool ok = true;
-        // beta of this thread's token row, loaded one tile ahead of its use
-        // (with the fused prep, whose per-token loads fill the registers, at the
-        // start of the tile)
-        auto load_beta = [&](int it2, int i2) {
-            const int t2 = 64 * i2 + r;
-            return (it2 < items && t2 < p.S)
-                       ? bf16_bits_to_float(p.beta[(size_t)(it2 / p.F) * p.N + (size_t)(it2 % p.F) * p.S + t2])
-                       : 0.f;
-        };
-        float beta_next = PREP ? 0.f : load_beta(blockIdx.x, 0);
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             const int bh = it / p.F, f = it % p.F;
+            const unsigned short *brow = p.beta + (size_t)bh * p.N + (size_t)f * p.S;
             const float *wk = (PREP && p.pp.wk) ? p.pp.wk + 128 * (bh % p.pp.H) : nullptr;
             for (int i = 0; i < nt; ++i, ++j) {
                 const int s = j % kGramStages, x = j & 1;
                 const int t = 64 * i + r;  // token within the frame
                 const bool valid = t < p.S;
-                float beta;
-                if (PREP) {
-                    beta = load_beta(it, i);
-                } else {
-                    beta = beta_next;
-                    beta_next = i + 1 < nt ? load_beta(it, i + 1) : load_beta(it + (int)gridDim.x, 0);
-                }
+                const float beta = valid ? bf16_bits_to_float(brow[t]) : 0.f;
                 // the prep's per-token values, loaded before the wait
                 float P[16], rk = 0.f;
                 if (PREP && valid) {
