@@ -1,7 +1,12 @@
 // gdn_api.cu -- the extern "C" boundary of libgdn.so: host-side argument
 // checks, dispatch between the tcgen05 and SIMT scan paths, status strings.
-// No allocation, no synchronisation, no exception crosses this file.
+// No allocation, no synchronisation, no exception crosses this file.  Every
+// compute entry point opens an NVTX range named after itself around its
+// checks and launches (header-only NVTX 3: a no-op unless a tool such as
+// Nsight Compute or Nsight Systems is attached), so a profiler can select a
+// call's kernels by range (ncu --nvtx --nvtx-include "gdn_chunk_fwd/").
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -16,6 +21,14 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace gdn
 
 namespace {
+
+// An NVTX range over the enclosing scope.
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -121,6 +134,7 @@ int gdn_chunk_fwd(const void *q, const void *k, const void *v, const void *beta,
                   int B, int H, int T, int Dk, int Dv, int chunk, float scale,
                   unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
                   void *stream) {
+    const Range nvtx_range("gdn_chunk_fwd");
     gdn::ScanArgs a{q, k, v, beta, g, initial_state, o, final_state, B, H, T, 1, Dk, Dv,
                     chunk, scale, flags, dtype, workspace, workspace_bytes};
     return run_scan(a, stream);
@@ -130,6 +144,7 @@ int gdn_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const voi
                           const float *g, const float *initial_state, void *o, float *final_state,
                           int B, int H, int T, int Dk, int Dv, int chunk, float scale,
                           unsigned flags, int dtype, void *stream) {
+    const Range nvtx_range("gdn_chunk_fwd_noalloc");
     // gdn_chunk_fwd with the library's own fixed scratch in place of a
     // caller-provided workspace; nothing is allocated
     gdn::ScanArgs a{q, k, v, beta, g, initial_state, o, final_state, B, H, T, 1, Dk, Dv,
@@ -156,6 +171,7 @@ int deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, const vo
                            float *final_state, int B, int H, int T, int r, int Dk, int Dv,
                            int chunk, float scale, unsigned flags, int dtype, void *workspace,
                            size_t workspace_bytes, void *stream) {
+    const Range nvtx_range("deltaproduct_chunk_fwd");
     gdn::ScanArgs a{q, k, v, beta, g, initial_state, o, final_state, B, H, T, r, Dk, Dv,
                     chunk, scale, flags, dtype, workspace, workspace_bytes};
     return run_scan(a, stream);
@@ -175,6 +191,7 @@ int masked_deltaproduct_chunk_fwd(const void *q, const void *k, const void *v, c
                                   float *final_state, int B, int H, int T, int r, int Dk, int Dv, int chunk,
                                   float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
                                   void *stream_v) {
+    const Range nvtx_range("masked_deltaproduct_chunk_fwd");
     if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
@@ -222,6 +239,7 @@ int cam_scan_fwd(const void *q, const void *k, const void *v, const void *beta, 
                  const float *initial_state, void *o, float *final_state, int B, int H, int F, int S,
                  int Dk, int Dv, float scale, unsigned flags, int dtype, void *workspace,
                  size_t workspace_bytes, void *stream_v) {
+    const Range nvtx_range("cam_scan_fwd");
     gdn::CamScanArgs a{q, k, v, beta, decay, initial_state, o, final_state, B, H, F, S, Dk, Dv,
                        scale, flags, dtype, workspace, workspace_bytes};
     const int st = check_cam_scan(a);
@@ -256,6 +274,7 @@ int cam_prep_scan_fwd(const void *q_raw, const void *k_raw, const void *v_raw, c
                       const void *beta, const float *decay, const float *initial_state, void *o,
                       float *final_state, int B, int N, int H, int D, int F, float k_scale, float eps, float scale,
                       unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream_v) {
+    const Range nvtx_range("cam_prep_scan_fwd");
     if (B < 0 || N < 0 || H < 1 || F < 1) return GDN_ERR_INVALID_ARG;
     if (N % F != 0 || (N > 0 && N / F == 0)) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
@@ -286,6 +305,7 @@ int cam_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
                  const float *rope_cos, const float *rope_sin, float rope_base, void *q_out,
                  void *k_out, void *v_out, float *k_pre_sq, float *k_post_sq, int B, int N,
                  int H, int D, float k_scale, float eps, int dtype, void *stream) {
+    const Range nvtx_range("cam_prep_fwd");
     if (B < 0 || N < 0 || H < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if ((rope_cos == nullptr) != (rope_sin == nullptr)) return GDN_ERR_INVALID_ARG;
@@ -321,6 +341,7 @@ int cam_scan_bwd(const void *q, const void *k, const void *v, const void *beta, 
                  void *dv, float *dbeta, float *ddecay, float *dinitial_state, int B, int H, int F, int S, int Dk,
                  int Dv, float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes,
                  void *stream) {
+    const Range nvtx_range("cam_scan_bwd");
     if (B < 0 || H < 0 || F < 0 || S < 0 || (F > 0 && S == 0)) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (flags & ~(GDN_QK_L2NORM | GDN_CAM_REVERSE | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
@@ -360,6 +381,7 @@ int cam_prep_bwd(const void *q_raw, const void *k_raw, const float *q_norm_w, co
                  float rope_base, const void *dq_out, const void *dk_out, const void *dv_out,
                  const float *dk_pre_sq, const float *dk_post_sq, void *dq_raw, void *dk_raw, void *dv_raw, int B,
                  int N, int H, int D, float k_scale, float eps, int dtype, void *stream) {
+    const Range nvtx_range("cam_prep_bwd");
     if (B < 0 || N < 0 || H < 0 || D <= 0) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if ((rope_cos == nullptr) != (rope_sin == nullptr)) return GDN_ERR_INVALID_ARG;
@@ -394,6 +416,7 @@ int deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, const vo
                            void *dk, void *dv, float *dbeta, float *dg, float *dinitial_state, int B, int H, int T,
                            int r, int Dk, int Dv, float scale, unsigned flags, int dtype, void *workspace,
                            size_t workspace_bytes, void *stream) {
+    const Range nvtx_range("deltaproduct_chunk_bwd");
     if (B < 0 || H < 0 || T < 0 || r < 1 || r > 8) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
@@ -431,6 +454,7 @@ int gdn_chunk_bwd(const void *q, const void *k, const void *v, const void *beta,
                   const float *initial_state, const void *dout, const float *dfinal_state, void *dq, void *dk,
                   void *dv, float *dbeta, float *dg, float *dinitial_state, int B, int H, int T, int Dk, int Dv,
                   float scale, unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    const Range nvtx_range("gdn_chunk_bwd");
     return deltaproduct_chunk_bwd(q, k, v, beta, g, initial_state, dout, dfinal_state, dq, dk, dv, dbeta, dg,
                                   dinitial_state, B, H, T, 1, Dk, Dv, scale, flags, dtype, workspace,
                                   workspace_bytes, stream);
@@ -450,6 +474,7 @@ int masked_deltaproduct_chunk_bwd(const void *q, const void *k, const void *v, c
                                   const float *dfinal_state, void *dq, void *dk, void *dv, float *dbeta, float *dg,
                                   float *dinitial_state, int B, int H, int T, int r, int Dk, int Dv, float scale,
                                   unsigned flags, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    const Range nvtx_range("masked_deltaproduct_chunk_bwd");
     if (B < 0 || H < 0 || T < 0 || r < 1) return GDN_ERR_INVALID_ARG;
     if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
     if (flags & ~(GDN_QK_L2NORM | GDN_PATH_SIMT)) return GDN_ERR_INVALID_ARG;
