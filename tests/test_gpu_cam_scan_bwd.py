@@ -77,3 +77,22 @@ def test_camera_workload_shape_sampled_heads():
     ref = oracle.cam_scan_bwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["decay"], heads(do, idx), l2norm=True)
     for name, x, y in zip(("dq", "dk", "dv", "dbeta", "ddecay"), got[:5], ref[:5]):
         assert rel_err(heads(x, idx).cpu(), y) <= TOL_BF16, name
+
+
+@pytest.mark.parametrize("F,S", [(1, 50), (1, 128), (2, 1)])
+def test_single_frame_and_single_token_frames(F, S):
+    """The tensor-core frame products and chains at their edges (bf16, D 128):
+    one frame (the chains take a single step each way, so the reverse chain's
+    one-frame-ahead load of P never runs) and frames of one token."""
+    inp = cam_scan_inputs(1, 2, F, S, 128, 128, seed=40 + F * S, dtype="bf16", initial_state=True)
+    g = torch.Generator().manual_seed(11)
+    do = torch.randn(1, 2, F * S, 128, generator=g).to(torch.bfloat16)
+    dsf = torch.randn(1, 2, 128, 128, generator=g)
+    d = to_dev(inp)
+    got = binding.cam_scan_bwd(d["q"], d["k"], d["v"], d["beta"], d["decay"], do.cuda(), d["initial_state"],
+                               dsf.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.cam_scan_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["decay"], do, inp["initial_state"], dsf)
+    for name, x, y in zip(("dq", "dk", "dv", "dbeta", "ddecay", "ds0"), got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name

@@ -221,3 +221,19 @@ def test_chain_bounded_wait_gives_up_and_context_survives():
     ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf)
     for name, x, y in zip(NAMES, got, ref):
         assert rel_err(x, y) <= TOL_BF16, name
+
+
+@pytest.mark.parametrize("T", [1, 40, 64, 65])
+def test_tensor_core_chain_single_chunk_and_ragged(T):
+    """The tensor-core chains (bf16, D 128) over one chunk (T <= 64: each chain
+    takes one step, the final state comes from the initial one) and over one
+    full chunk plus one token, against the oracle."""
+    inp, do, dsf = grads_case(1, 2, T, 128, 128, "bf16", False, seed=70 + T)
+    d = to_dev(inp)
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"],
+                                dsf.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name

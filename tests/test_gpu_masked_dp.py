@@ -100,3 +100,15 @@ def test_tensor_core_chain_matches_the_cuda_core_chain(r):
     (o1, s1), (o2, s2) = outs
     assert rel_err(o1, o2.double().cpu().numpy()) <= 5e-3
     assert rel_err(s1, s2.double().cpu().numpy()) <= 2e-4
+
+
+@pytest.mark.parametrize("T", [1, 32, 33])
+def test_tensor_core_chain_single_chunk(T):
+    """The block-masked forward's tensor-core chain (bf16, D 128, r = 2: 32
+    tokens per chunk) over one chunk and one chunk plus a token."""
+    inp = gdn_inputs(1, 2, T, 128, 128, seed=90 + T, dtype="bf16", initial_state=True)
+    inp["mask"] = slice_mask(2, seed=2)
+    o, sf = run(inp)
+    ro, rs = ref(inp)
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
