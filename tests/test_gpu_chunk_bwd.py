@@ -237,3 +237,21 @@ def test_tensor_core_chain_single_chunk_and_ragged(T):
     ref = oracle.gdn_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf)
     for name, x, y in zip(NAMES, got, ref):
         assert rel_err(x, y) <= TOL_BF16, name
+
+
+def test_full_size_fp32_sampled_heads():
+    """The fp32 backward (CUDA-core chains) over 64 chunks per head: every head
+    on the GPU, two heads against the oracle at the fp32 bound."""
+    B, H, T = 2, 8, 4096
+    inp, do, dsf = grads_case(B, H, T, 128, 128, "f32", False, seed=33)
+    d = to_dev(inp)
+    got = binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"],
+                                dsf.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    idx = [0, 13]
+    sub = {k: heads(v, idx) for k, v in inp.items()}
+    ref = oracle.gdn_bwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], heads(do, idx),
+                         sub["initial_state"], heads(dsf, idx))
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(heads(x, idx).cpu(), y) <= TOL_F32, name

@@ -347,3 +347,19 @@ def test_graph_replays_reuse_one_workspace():
     assert torch.equal(o2, o_eager) and torch.equal(s2, s_eager)
     ro, _ = ref_gdn(inp)
     assert rel_err(o_eager, ro) <= TOL_BF16
+
+
+def test_full_size_fp32_sampled_heads():
+    """The fp32 path at the headline's size (B4 H16 T4096 D128, 64 chunks per
+    head, CUDA cores): sampled heads against the oracle at the fp32 bound."""
+    inp = gdn_inputs(4, 16, 4096, 128, 128, seed=31, dtype="f32", initial_state=True)
+    d = to_dev(inp)
+    o, sf = binding.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["initial_state"],
+                                  output_final_state=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    idx = sample_heads(4, 16, 2, seed=31)
+    sub = {k: heads(v, idx) for k, v in inp.items()}
+    ro, rs = oracle.gdn_fwd(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], sub["initial_state"])
+    assert rel_err(heads(o, idx).cpu(), ro) <= TOL_F32
+    assert rel_err(heads(sf, idx).cpu(), rs) <= TOL_F32
