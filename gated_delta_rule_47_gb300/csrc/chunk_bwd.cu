@@ -61,7 +61,8 @@ struct BwdParams {
     float *dbeta, *dg, *ds0;
     // workspace, per (head, chunk): T [64][64], W [64][Dk], U [64][Dv], Kd [64][Dk],
     // B [Dk][Dv], S [Dk][Dv], dS' [Dk][Dv], Vn [64][Dv], gamma [64], and the
-    // products P^ [64][64] and K K^T [64][64] for the gradient kernel
+    // products P^ [64][64] and K K^T [64][64] for the gradient kernel; with the
+    // tensor-core chains (img) the first half of B then holds Y = Kd dS' [64][Dv]
     float *Tw, *Ww, *Uw, *Kdw, *Bw, *Sw, *dSw, *Vnw, *Gw, *Pw, *KKw;
     int T, r, Ct, NT;
     float scale;
@@ -285,14 +286,15 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     __syncthreads();
     const float gl = gam[kC - 1];
 
-    // 1. through the state leaving the chunk: K dS', and Vn dS'^T into dk
+    // 1. through the state leaving the chunk: Kd dS' (from the tensor-core chain,
+    //    which forms it, when the chain ran there), and Vn dS'^T into dk
     float accKdS[2][TV], accDK[2][TK];
     zero(accKdS);
     zero(accDK);
     for (int h = 0; h < NH; ++h) {
         stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
         __syncthreads();
-        mm<kThr, 2, TV>(accKdS, Ks + 64 * h, LK, 1, Hs, LV, 1, 64);
+        if (!p.img) mm<kThr, 2, TV>(accKdS, Ks + 64 * h, LK, 1, Hs, LV, 1, 64);
         float tz[2][4];
         zero(tz);
         mm_nt<kThr, 2, 4>(tz, Vns, LV, Hs, LV, DV);
@@ -311,15 +313,28 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         s = warp_sum(s);
         if ((tid & 31) == 0) red[tid >> 5] = s;
     }
+    if (p.img) {  // Y = Kd dS', over the first half of the chunk's B slot
+        const float *Yg = p.Bw + ch.ci * DK * DV;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TV; ++j) accKdS[i][j] = Yg[(ty + 32 * i) * DV + tx + 16 * j];
+    } else {  // K dS' -> Kd dS'
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float s = expf(gl - gam[ty + 32 * i]);
+#pragma unroll
+            for (int j = 0; j < TV; ++j) accKdS[i][j] *= s;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {  // decay gradients of the state's update
         const int b = ty + 32 * i;
-        float d = 0.f;
+        float w = 0.f;
 #pragma unroll
-        for (int j = 0; j < TV; ++j) d += accKdS[i][j] * Vns[b * LV + tx + 16 * j];
-        d = row_sum16(d);
+        for (int j = 0; j < TV; ++j) w += accKdS[i][j] * Vns[b * LV + tx + 16 * j];
+        w = row_sum16(w);
         if (tx == 0) {
-            const float w = expf(gl - gam[b]) * d;
             rowg[b] -= w;
             lastg[b] = w;
         }
@@ -334,12 +349,6 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     __syncthreads();
 
     // 3. dVn = Kd dS' + P^^T dO into Hs
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float s = expf(gl - gam[ty + 32 * i]);
-#pragma unroll
-        for (int j = 0; j < TV; ++j) accKdS[i][j] *= s;
-    }
     mm<kThr, 2, TV>(accKdS, Xa, 1, LC, dOs, LV, 1, kC);
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -623,6 +632,7 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
         ca.Uw = p.Uw;
         ca.Bw = p.Bw;
         ca.Gw = p.Gw;
+        ca.Yw = p.Bw;  // Y = Kd dS' for the gradient kernel
         ca.BH = BH;
         ca.NT = NT;
         ca.roles = 2;

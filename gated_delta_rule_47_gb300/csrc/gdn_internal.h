@@ -216,6 +216,9 @@ struct WyChainTcArgs {
     float *Vnw;             // [ci][64][128] Vn of each chunk (forward chain)
     const unsigned char *Wimg, *Kdimg;  // [ci] 32 KB bf16 hi | lo images of W and Kd (write_chain_image)
     const float *Uw, *Bw, *Gw;          // [ci][64][128] U, [ci][128][128] B (reverse), [ci][64] gamma
+    // or null: [ci] Y = Kd dS' of each chunk ([64][128], reverse chain), written over the first half
+    // of that chunk's B once the chain has read it
+    float *Yw;
     int BH, NT, roles;
     unsigned long long timeout_ns;  // bounded-wait limit (set by the launcher)
 };

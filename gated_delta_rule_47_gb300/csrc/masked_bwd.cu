@@ -308,14 +308,15 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     auto wr = [&](int a, int c) { return msk[(a & (r - 1)) * r + (c >> lsl)]; };
     auto ww = [&](int a, int c) { return (c >> lsl) == (a & (r - 1)) ? 1.f : 0.f; };
 
-    // 1. through the state leaving the chunk: Kw dS', and Vn dS'^T (write keys)
+    // 1. through the state leaving the chunk: Kd dS' (from the tensor-core chain,
+    //    which forms it, when the chain ran there), and Vn dS'^T (write keys)
     float accKdS[2][TV], accD[2][TK];
     zero(accKdS);
     zero(accD);
     for (int h = 0; h < NH; ++h) {
         stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
         __syncthreads();
-        mm_f<kThr, 2, TV>(accKdS, Off<SubKey<true>>{KW, 64 * h}, Sm{Hs, LV, 1}, 64);
+        if (!p.img) mm_f<kThr, 2, TV>(accKdS, Off<SubKey<true>>{KW, 64 * h}, Sm{Hs, LV, 1}, 64);
         float tz[2][4];
         zero(tz);
         mm_nt<kThr, 2, 4>(tz, Vns, LX, Hs, LV, DV);
@@ -335,15 +336,28 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         s = warp_sum(s);
         if ((tid & 31) == 0) red[tid >> 5] = s;
     }
+    if (p.img) {  // Y = Kd dS', over the first half of the chunk's B slot
+        const float *Yg = p.Bw + ch.ci * DK * DV;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TV; ++j) accKdS[i][j] = Yg[(ty + 32 * i) * DV + tx + 16 * j];
+    } else {  // Kw dS' -> Kd dS'
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float s = expf(gl - gam[ty + 32 * i]);
+#pragma unroll
+            for (int j = 0; j < TV; ++j) accKdS[i][j] *= s;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int b = ty + 32 * i;
-        float d = 0.f;
+        float w = 0.f;
 #pragma unroll
-        for (int j = 0; j < TV; ++j) d += accKdS[i][j] * Vns[b * LX + tx + 16 * j];
-        d = row_sum16(d);
+        for (int j = 0; j < TV; ++j) w += accKdS[i][j] * Vns[b * LX + tx + 16 * j];
+        w = row_sum16(w);
         if (tx == 0) {
-            const float w = expf(gl - gam[b]) * d;
             rowg[b] -= w;
             lastg[b] = w;
         }
@@ -356,12 +370,6 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     }
     __syncthreads();
     // 3. dVn = Kd dS' + P^^T dO into Hs
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float s = expf(gl - gam[ty + 32 * i]);
-#pragma unroll
-        for (int j = 0; j < TV; ++j) accKdS[i][j] *= s;
-    }
     mm<kThr, 2, TV>(accKdS, Xa, 1, LC, dOs, LV, 1, kC);
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -686,6 +694,7 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
         ca.Uw = p.Uw;
         ca.Bw = p.Bw;
         ca.Gw = p.Gw;
+        ca.Yw = p.Bw;  // Y = Kd dS' for the gradient kernel
         ca.BH = BH;
         ca.NT = NT;
         ca.roles = 2;

@@ -250,6 +250,12 @@ __global__ void __launch_bounds__(kCThr, 1) wy_chain_tc_kernel(WyChainTcArgs p) 
                     z[i] = pre[i] - z[i];
                     Vg[(size_t)i * 128] = z[i];
                 }
+            } else if (p.Yw) {
+                // Y = Kd dS', kept for the gradient kernel over this chunk's B, which every
+                // thread loaded before arriving on CB_XREADY (ordered before this write)
+                float *Yg = p.Yw + ci * 16384 + (size_t)(32 * hh) * 128 + dv;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) Yg[(size_t)i * 128] = z[i];
             }
             {  // Z'^T as its hi | lo operand (rows 32hh.. of the chunk)
                 uint8_t *zo = sm + C_ZOP;
