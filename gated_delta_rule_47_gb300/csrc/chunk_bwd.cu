@@ -27,7 +27,7 @@
 //   with P~[i][b] = scale e^{gamma_rho - gamma_b} do_i.vn_b (b <= rho), L = dA o beta E,
 //   and dgamma collected term by term, then dg the reverse cumulative sum.
 //
-// Three launches:
+// Three launches (four with the tensor-core chains):
 //   1. bwd_wy_kernel (one CTA per chunk): T, W, U, Kd, gamma and B to the workspace.
 //   2. the forward state chain (S entering each chunk, and Vn) and the
 //      reverse gradient chain (dS' of each chunk, and the initial state's
@@ -37,7 +37,9 @@
 //      instead of fp32), otherwise wy_chain_kernel (CUDA cores, fp32; each CTA
 //      holds 64 value columns of one head's state, since the columns of both
 //      chains are independent).
-//   3. bwd_grad_kernel (one CTA per chunk): every input gradient.
+//   3. (tensor-core chains only) state_products_tc_kernel: Z = Vn dS'^T,
+//      t1 = dO S^T and <dS', S> per chunk on tcgen05, over the dS' slot.
+//   4. bwd_grad_kernel (one CTA per chunk): every input gradient.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -286,27 +288,38 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     __syncthreads();
     const float gl = gam[kC - 1];
 
-    // 1. through the state leaving the chunk: Kd dS' (from the tensor-core chain,
-    //    which forms it, when the chain ran there), and Vn dS'^T into dk
+    // 1. through the state leaving the chunk: Kd dS' and Z = Vn dS'^T into dk.
+    //    With the tensor-core chains the chunk's dS' slot holds Z (and t1 = dO S^T,
+    //    step 8) from the state-products kernel, the first half of its B slot
+    //    holds Kd dS' (from the reverse chain), and float 8192 of B holds <dS', S>.
     float accKdS[2][TV], accDK[2][TK];
     zero(accKdS);
     zero(accDK);
-    for (int h = 0; h < NH; ++h) {
-        stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
-        __syncthreads();
-        if (!p.img) mm<kThr, 2, TV>(accKdS, Ks + 64 * h, LK, 1, Hs, LV, 1, 64);
-        float tz[2][4];
-        zero(tz);
-        mm_nt<kThr, 2, 4>(tz, Vns, LV, Hs, LV, DV);
+    if (p.img) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const float s = expf(gl - gam[ty + 32 * i]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) accDK[i][4 * h + j] += s * tz[i][j];
+            for (int j = 0; j < TK; ++j) accDK[i][j] += s * dSg[(ty + 32 * i) * DK + tx + 16 * j];
         }
-        __syncthreads();
-    }
-    {  // <dS', S>
+        if (tid < kThr / 32) red[tid] = tid == 0 ? p.Bw[ch.ci * DK * DV + 8192] : 0.f;
+    } else {
+        for (int h = 0; h < NH; ++h) {
+            stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
+            __syncthreads();
+            mm<kThr, 2, TV>(accKdS, Ks + 64 * h, LK, 1, Hs, LV, 1, 64);
+            float tz[2][4];
+            zero(tz);
+            mm_nt<kThr, 2, 4>(tz, Vns, LV, Hs, LV, DV);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float s = expf(gl - gam[ty + 32 * i]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) accDK[i][4 * h + j] += s * tz[i][j];
+            }
+            __syncthreads();
+        }
+        // <dS', S>
         float s = 0.f;
 #pragma unroll 8
         for (int e = tid; e < DK * DV; e += kThr) s += dSg[e] * Sg[e];
@@ -463,7 +476,17 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LV, DV);
+        if (p.img) {  // t1 = dO S^T from the state-products kernel
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int m = ty + 32 * i;
+                    t1[i][j] = m < ntok ? dSg[8192 + m * DK + 64 * h + tx + 16 * j] : 0.f;
+                }
+        } else {
+            mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LV, DV);
+        }
         mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LV, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -636,7 +659,19 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
         ca.BH = BH;
         ca.NT = NT;
         ca.roles = 2;
-        const int rc = launch_wy_chain_tc(ca, st);
+        int rc = launch_wy_chain_tc(ca, st);
+        if (rc != GDN_OK) return rc;
+        StateProductsTcArgs sa{};
+        sa.Sw = p.Sw;
+        sa.Vnw = p.Vnw;
+        sa.dSw = p.dSw;
+        sa.Bw = p.Bw;
+        sa.dout = static_cast<const unsigned short *>(a.dout);
+        sa.BH = BH;
+        sa.NT = NT;
+        sa.T = a.T;
+        sa.Ct = Ct;
+        rc = launch_state_products_tc(sa, st);
         if (rc != GDN_OK) return rc;
     } else {
         WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};

@@ -223,6 +223,19 @@ struct WyChainTcArgs {
     unsigned long long timeout_ns;  // bounded-wait limit (set by the launcher)
 };
 int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t stream);
+// The state products of the chunk backward's gradient kernel on tcgen05
+// (wy_chain_tc.cu), per (head, chunk) after both chains: Z = Vn dS'^T over
+// floats 0..8191 and t1 = dO S^T ([Ct][128]) over floats 8192.. of the chunk's
+// dS' slot, and <dS', S> to float 8192 of its B slot.
+struct StateProductsTcArgs {
+    const float *Sw, *Vnw;           // [ci][128][128] S entering the chunk, [ci][64][128] Vn
+    float *dSw, *Bw;                 // [ci][128][128] dS' (then Z | t1), [ci][128][128] B (float 8192: the dot)
+    const unsigned short *dout;      // [BH][T][128] bf16 bits of dO
+    int BH, NT, T, Ct;               // Ct: query rows (tokens) per chunk
+    int nq2;                         // set by the launcher
+    unsigned long long timeout_ns;   // set by the launcher
+};
+int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the chain kernel (GDN_OK or GDN_ERR_TIMEOUT).
 int wy_chain_tc_read_clear_error();
 

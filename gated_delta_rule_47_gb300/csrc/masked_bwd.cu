@@ -313,23 +313,36 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     float accKdS[2][TV], accD[2][TK];
     zero(accKdS);
     zero(accD);
-    for (int h = 0; h < NH; ++h) {
-        stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
-        __syncthreads();
-        if (!p.img) mm_f<kThr, 2, TV>(accKdS, Off<SubKey<true>>{KW, 64 * h}, Sm{Hs, LV, 1}, 64);
-        float tz[2][4];
-        zero(tz);
-        mm_nt<kThr, 2, 4>(tz, Vns, LX, Hs, LV, DV);
+    if (p.img) {  // Z = Vn dS'^T over the dS' slot, <dS', S> at float 8192 of B (state-products kernel)
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int a = ty + 32 * i;
             const float s = expf(gl - gam[a]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) accD[i][4 * h + j] += ww(a, 64 * h + tx + 16 * j) * s * tz[i][j];
+            for (int j = 0; j < TK; ++j) {
+                const int c = tx + 16 * j;
+                accD[i][j] += ww(a, c) * s * dSg[a * DK + c];
+            }
         }
-        __syncthreads();
-    }
-    {  // <dS', S>
+        if (tid < kThr / 32) red[tid] = tid == 0 ? p.Bw[ch.ci * DK * DV + 8192] : 0.f;
+    } else {
+        for (int h = 0; h < NH; ++h) {
+            stage_rows<64, DV>(Hs, LV, dSg + (size_t)64 * h * DV);
+            __syncthreads();
+            mm_f<kThr, 2, TV>(accKdS, Off<SubKey<true>>{KW, 64 * h}, Sm{Hs, LV, 1}, 64);
+            float tz[2][4];
+            zero(tz);
+            mm_nt<kThr, 2, 4>(tz, Vns, LX, Hs, LV, DV);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int a = ty + 32 * i;
+                const float s = expf(gl - gam[a]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) accD[i][4 * h + j] += ww(a, 64 * h + tx + 16 * j) * s * tz[i][j];
+            }
+            __syncthreads();
+        }
+        // <dS', S>
         float s = 0.f;
 #pragma unroll 8
         for (int e = tid; e < DK * DV; e += kThr) s += dSg[e] * Sg[e];
@@ -487,7 +500,17 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LX, DV);
+        if (p.img) {  // t1 = dO S^T from the state-products kernel
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int m = ty + 32 * i;
+                    t1[i][j] = m < ntok ? dSg[8192 + m * DK + 64 * h + tx + 16 * j] : 0.f;
+                }
+        } else {
+            mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LX, DV);
+        }
         mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LX, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -698,7 +721,19 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
         ca.BH = BH;
         ca.NT = NT;
         ca.roles = 2;
-        const int rc = launch_wy_chain_tc(ca, st);
+        int rc = launch_wy_chain_tc(ca, st);
+        if (rc != GDN_OK) return rc;
+        StateProductsTcArgs sa{};
+        sa.Sw = p.Sw;
+        sa.Vnw = p.Vnw;
+        sa.dSw = p.dSw;
+        sa.Bw = p.Bw;
+        sa.dout = static_cast<const unsigned short *>(a.dout);
+        sa.BH = BH;
+        sa.NT = NT;
+        sa.T = a.T;
+        sa.Ct = p.Ct;
+        rc = launch_state_products_tc(sa, st);
         if (rc != GDN_OK) return rc;
     } else {
         WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};

@@ -319,4 +319,170 @@ int wy_chain_tc_read_clear_error() {
     return v ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
+
+// ======================= the state products of the gradient kernels (tcgen05)
+// state_products_tc_kernel: per (head, chunk), after both chains, with S the
+// state entering the chunk, dS' the gradient leaving it, Vn [64][128] and the
+// chunk's nq query rows of dO [nq][128] (bf16):
+//   Z  = Vn dS'^T      [64][128]   (3 split products: both operands fp32)
+//   t1 = dO S^T        [nq][128]   (2 split products: dO is exact in bf16)
+//   <dS', S>
+// Z and t1 go over the chunk's dS' slot (Z in floats 0 .. 8191, t1 in
+// 8192 ..), which no later kernel reads, and <dS', S> to float 8192 of the
+// chunk's B slot (whose first half holds Y).  One CTA per chunk: 256 threads
+// split the fp32 operands into bf16 hi | lo K-major tiles, thread 0 issues
+// Z^T = dS' Vn^T and t1^T = S dO^T (M = 128 key rows) into TMEM, and the
+// threads write the transposes back.
+namespace {
+
+constexpr int kSpThr = 256;
+constexpr uint32_t SP_A1 = 0;        // dS' hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each
+constexpr uint32_t SP_A2 = 65536;    // S hi | lo, likewise
+constexpr uint32_t SP_B1 = 131072;   // Vn hi | lo: [2 value blocks][64 rows][128 B], 16 KB each
+constexpr uint32_t SP_B2 = 163840;   // dO: [2 value blocks][nq2 rows][128 B], 16 KB at most
+constexpr uint32_t SP_BAR = 180224;
+constexpr uint32_t SP_MISC = SP_BAR + 16;  // TMEM address, then 8 warp sums
+constexpr uint32_t SP_SMEM = SP_MISC + 48 + 1024;
+
+__global__ void __launch_bounds__(kSpThr, 1) state_products_tc_kernel(StateProductsTcArgs p) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + SP_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SP_MISC);
+    float *wsum = reinterpret_cast<float *>(sm + SP_MISC + 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const size_t ci = (size_t)bh * p.NT + c;
+    const int nq2 = p.nq2;  // query rows of the t1 product (a multiple of 16; rows past the chunk are zero)
+    const int t0 = c * p.Ct, ntok = min(p.Ct, p.T - t0);
+
+    if (tid == 0) {
+        mbar_init(bar, 1u);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 128);
+        tmem_relinquish();
+    }
+    // the operands: 8-element groups, hi at +0 and lo at +32 KB (A) / +16 KB (B)
+    const float *Sg = p.Sw + ci * 16384, *dSg = p.dSw + ci * 16384;
+    float dot = 0.f;
+    for (int e = tid; e < 128 * 16; e += kSpThr) {  // S and dS': row m, columns 8 g ..
+        const int m = e >> 4, g = e & 15, k0 = 8 * g;
+        const float4 a0 = *reinterpret_cast<const float4 *>(dSg + m * 128 + k0);
+        const float4 a1 = *reinterpret_cast<const float4 *>(dSg + m * 128 + k0 + 4);
+        const float4 b0 = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0);
+        const float4 b1 = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0 + 4);
+        const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float y[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dot += x[i] * y[i];
+        const uint32_t off = (uint32_t)(k0 >> 6) * 16384u + sw128_offset((uint32_t)m, (uint32_t)(k0 & 63));
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + SP_A1 + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + SP_A1 + 32768 + off) = lo;
+        split8(y, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + SP_A2 + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + SP_A2 + 32768 + off) = lo;
+    }
+    const float *Vg = p.Vnw + ci * 8192;
+    for (int e = tid; e < 64 * 16; e += kSpThr) {  // Vn: row t, columns 8 g ..
+        const int t = e >> 4, g = e & 15, k0 = 8 * g;
+        const float4 a0 = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0);
+        const float4 a1 = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0 + 4);
+        const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t off = (uint32_t)(k0 >> 6) * 8192u + sw128_offset((uint32_t)t, (uint32_t)(k0 & 63));
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + SP_B1 + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + SP_B1 + 16384 + off) = lo;
+    }
+    const unsigned short *dO = p.dout + ((size_t)bh * p.T + t0) * 128;
+    for (int e = tid; e < nq2 * 16; e += kSpThr) {  // dO: query row q, columns 8 g .. (exact in bf16)
+        const int q = e >> 4, g = e & 15, k0 = 8 * g;
+        const uint4 v = q < ntok ? *reinterpret_cast<const uint4 *>(dO + (size_t)q * 128 + k0) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + SP_B2 + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
+                                   sw128_offset((uint32_t)q, (uint32_t)(k0 & 63))) = v;
+    }
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) wsum[warp] = dot;
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) {
+        float d = 0.f;
+        for (int w = 0; w < kSpThr / 32; ++w) d += wsum[w];
+        p.Bw[ci * 16384 + 8192] = d;
+        // Z^T = dS' Vn^T (columns 0..63), t1^T = S dO^T (columns 64..)
+        const uint32_t idZ = idesc_bf16(128, 64, false, false), idT = idesc_bf16(128, nq2, false, false);
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t a = sb + SP_A1 + (pr == 2 ? 32768u : 0u), b = sb + SP_B1 + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tmem, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                            smem_desc(b + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idZ, (pr | ks) != 0);
+        }
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t a = sb + SP_A2 + (pr == 1 ? 32768u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tmem + 64, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                            smem_desc(sb + SP_B2 + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), idT,
+                            (pr | ks) != 0);
+        }
+        mma_commit(bar);
+    }
+    // every thread: key row m = TMEM lane (warp quarter), half of the columns
+    const bool ok = warp_ok(wyc_wait(bar, 0, 8u, p.timeout_ns));
+    if (ok) {
+        tc_fence_after_sync();
+        const int q4 = warp & 3, half = warp >> 2;
+        const int m = 32 * q4 + lane;
+        const uint32_t lb = (uint32_t)(32 * q4) << 16;
+        float *out = p.dSw + ci * 16384;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // Z rows t = 32 half + 16 j ..
+            uint32_t r[16];
+            tmem_ld16(tmem + lb + 32 * half + 16 * j, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[(size_t)(32 * half + 16 * j + i) * 128 + m] = __uint_as_float(r[i]);
+        }
+        for (int j = half; j < nq2 / 16; j += 2) {  // t1 rows q = 16 j ..
+            uint32_t r[16];
+            tmem_ld16(tmem + lb + 64 + 16 * j, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[8192 + (size_t)(16 * j + i) * 128 + m] = __uint_as_float(r[i]);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+
+int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t st) {
+    if (a.BH <= 0 || a.NT <= 0 || a.Ct <= 0 || a.Ct > 64) return GDN_ERR_INVALID_ARG;
+    StateProductsTcArgs p = a;
+    p.nq2 = (a.Ct + 15) / 16 * 16;
+    p.timeout_ns = wait_limit_ns();
+    if (cudaFuncSetAttribute(state_products_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SP_SMEM) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    state_products_tc_kernel<<<dim3((unsigned)a.NT, (unsigned)a.BH), kSpThr, SP_SMEM, st>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 }  // namespace gdn
