@@ -236,6 +236,24 @@ struct StateProductsTcArgs {
     unsigned long long timeout_ns;   // set by the launcher
 };
 int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t stream);
+
+// Chunk-local kernels of the block-masked DeltaProduct forward on tcgen05
+// (bf16, Dk = Dv = 128, 64-row chunks of Ct = 64 / r tokens), around the
+// tensor-core state chain.  The WY kernel writes, per (head, chunk) ci, W and
+// Kd as the chain's bf16 hi | lo operand images (32 KB each, in the W and Kd
+// slots), U [64][128], P [64][64] and gamma [64] in fp32; the output kernel
+// reads S [128][128], Vn [64][128], P and gamma and writes o.
+struct MaskedTcArgs {
+    const unsigned short *q, *k, *v, *beta;  // bf16 bits: [BH][T][128], beta [BH][T]
+    const float *g, *mask;                   // [BH][T] log-decays, [r][r]
+    unsigned short *o;                       // [BH][T][128] bf16 bits
+    float *Ww, *Kdw, *Uw, *Vnw, *Sw, *Pw, *Gw;
+    int BH, T, r, Ct, NT, l2;
+    float scale;
+    unsigned long long timeout_ns;  // set by the launchers
+};
+int launch_masked_wy_tc(const MaskedTcArgs &a, cudaStream_t stream);
+int launch_masked_out_tc(const MaskedTcArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the chain kernel (GDN_OK or GDN_ERR_TIMEOUT).
 int wy_chain_tc_read_clear_error();
 

@@ -298,8 +298,36 @@ int run(const MaskedDpArgs &a, cudaStream_t st) {
     const bool tc_chain = std::is_same<T, __nv_bfloat16>::value && DK == 128 && DV == 128 &&
                           !(a.flags & GDN_PATH_SIMT) && sm100_family();
     p.img = tc_chain ? 1 : 0;
-    mdp_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
-    note_launch();
+    // with the tensor-core chain the chunk-local kernels run on tcgen05 too
+    MaskedTcArgs ta{};
+    if (tc_chain) {
+        ta.q = static_cast<const unsigned short *>(a.q);
+        ta.k = static_cast<const unsigned short *>(a.k);
+        ta.v = static_cast<const unsigned short *>(a.v);
+        ta.beta = static_cast<const unsigned short *>(a.beta);
+        ta.g = a.g;
+        ta.mask = a.mask;
+        ta.o = static_cast<unsigned short *>(a.o);
+        ta.Ww = p.Ww;
+        ta.Kdw = p.Kdw;
+        ta.Uw = p.Uw;
+        ta.Vnw = p.Vnw;
+        ta.Sw = p.Sw;
+        ta.Pw = p.Pw;
+        ta.Gw = p.Gw;
+        ta.BH = BH;
+        ta.T = a.T;
+        ta.r = a.r;
+        ta.Ct = Ct;
+        ta.NT = NT;
+        ta.l2 = p.l2;
+        ta.scale = a.scale;
+        const int rc = launch_masked_wy_tc(ta, st);
+        if (rc != GDN_OK) return rc;
+    } else {
+        mdp_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
+        note_launch();
+    }
     if (tc_chain) {
         WyChainTcArgs ca{};
         ca.s0 = a.s0;
@@ -320,6 +348,7 @@ int run(const MaskedDpArgs &a, cudaStream_t st) {
         wy_chain_kernel<DK, DV, kMSlice><<<dim3((unsigned)(DV / kMSlice), (unsigned)BH, 1), kChainThr, s2, st>>>(cp);
         note_launch();
     }
+    if (tc_chain) return launch_masked_out_tc(ta, st);
     mdp_out_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s3, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

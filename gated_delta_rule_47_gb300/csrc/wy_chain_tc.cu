@@ -22,10 +22,12 @@
 // per chunk, double-buffered.  Every wait is bounded; a CTA that gives up sets
 // the error word, which gdn_get_device_error reads.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "gdn_internal.h"
 #include "tc_util.cuh"
+#include "tri_inverse.cuh"
 
 namespace gdn {
 namespace {
@@ -481,6 +483,563 @@ int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t st) {
         cudaSuccess)
         return GDN_ERR_CUDA;
     state_products_tc_kernel<<<dim3((unsigned)a.NT, (unsigned)a.BH), kSpThr, SP_SMEM, st>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+
+// ---------------------------------------------------------------------------
+// Block-masked DeltaProduct forward, the chunk-local kernels on tcgen05 for
+// bf16 at Dk = Dv = 128 (gated_deltaproduct test.py: the mask_ij coupling of
+// `gated_chunk_scaled_dot_kkt_fwd_kernel`, `gated_fwd_recompute_w_u_kernel`
+// and the chunk output of `gated_chunk_fwd_o_fn`).  Sub-row b = (token t_b,
+// slice i_b) of a 64-row chunk of Ct = 64 / r tokens; kw_b is slice i_b of
+// k_{t_b} (zero elsewhere) and kr_b is k_{t_b} with slice j scaled by
+// mask[i_b][j].  With the unit-norm flag n_t = 1/||k_t|| and m_t = 1/||q_t||
+// (else 1) stay scalar factors, so the raw bf16 keys and queries enter the
+// products exactly.
+//
+// masked_wy_tc_kernel, one CTA of 256 threads per chunk (two per SM):
+//   1. [K; Q] Kw^T as one exact product (M = 128: the chunk's token keys in
+//      rows 0..63, its queries in rows 64..127; N = 64 sub-rows), since
+//      k_t . kw_b is the dot product of slice i_b of k_t and of k_{t_b};
+//   2. A[a][b] = beta_a e^{gamma_a - gamma_b} mask[i_a][i_b] n_{t_a} n_{t_b}
+//      k_{t_a} . kw_b for t_b < t_a, and the output factors
+//      P[t][b] = scale e^{gamma_{t r} - gamma_b} m_t n_{t_b} q_t . kw_b for
+//      t_b <= t (to the workspace);
+//   3. T = (I + A)^-1 on the CUDA cores (tri_inverse.cuh);
+//   4. W = T diag(beta e^gamma) Kr as three split products (both operands
+//      rounded) and U = T diag(beta) V as two (v is exact), M = 128 with rows
+//      0..63 used, N = 128;
+//   5. W and Kd = diag(e^{gl - gamma} n) Kw as the chain's operand images, U
+//      and gamma in fp32.
+// masked_out_tc_kernel, one CTA of 256 threads per chunk, with S the state
+// entering it:  o_t = scale e^{gamma_{t r}} m_t q_t S + (P Vn)_t, as
+// o^T = S^T Q^T (two split products: q is exact) + Vn^T P^T (three), M = 128
+// value rows, N = the chunk's query rows rounded up to 16.
+namespace {
+
+constexpr int kMwThr = 256;  // two CTAs per SM
+// One 97 KB region reused by the phases (byte offsets):
+//   loads, [K; Q] Kw^T:  X = [sub-row keys k_{t_a}, rows 0..63 | queries q_t, rows 64..127] K-major,
+//                        2 key blocks of 16 KB, at 0; Kw [2 key blocks][64 sub-rows][128 B] (exact)
+//                        at 32768; Kd's image (hi | lo), staged for one bulk copy, at 49152
+//   A, the inverse:      A, T fp32 [64][68] at 0 and 17408, scratch (1024 floats) at 34816;
+//                        P's rows (68-float stride), staged for bulk copies, at 81920
+//   W and U:             Tw hi | Tw lo | Tu hi | Tu lo [64 rows][128 B] K-major (8 KB each) at 0,
+//                        Kr hi | lo [2 key blocks][64 sub-rows][128 B] at 32768,
+//                        the sub-rows' values [2 value blocks][64 sub-rows][128 B] (exact) at 65536
+//   the results:         W's image at 0, U's rows (132-float stride) at 32768, both for bulk copies
+// The padded row strides keep the row-per-lane stores of the staging free of
+// bank conflicts.
+constexpr uint32_t MW_X = 0, MW_KW = 32768, MW_KD = 49152;
+constexpr int kMwLA = 68;  // fp32 row stride of A and T (16-byte aligned rows)
+constexpr uint32_t MW_AF = 0, MW_TF = 64 * kMwLA * 4, MW_X4 = 2 * 64 * kMwLA * 4, MW_PS = 81920;
+constexpr uint32_t MW_TW = 0, MW_KR = 32768, MW_VS = 65536;
+constexpr uint32_t MW_WS = 0, MW_US = 32768;
+constexpr int kMwLP = 68, kMwLU = 132;  // staging row strides (floats)
+constexpr uint32_t MW_VEC = 99328;      // gamma, beta, n (per sub-row), m, mask: 64 floats each
+constexpr uint32_t MW_BAR = MW_VEC + 5 * 256;
+constexpr uint32_t MW_SMEM = MW_BAR + 16 + 1024;
+// The M = 128 products read A rows 64..127 from the 8 KB after the start of
+// their 64-row operand: W's rows past Tw are Tw lo and Tu hi, and U's
+// operand starts 8 KB before Tu hi (lo), so that Tu sits in rows 64..127 and
+// U lands in TMEM lanes 64..127; every row read is finite and the rows not
+// wanted are not used.
+static_assert(MW_X4 + 4096 <= MW_PS && MW_KD + 32768 <= MW_PS && MW_PS + 64 * kMwLP * 4 <= MW_VEC &&
+                  MW_VS + 16384 <= MW_PS && MW_US + 64 * kMwLU * 4 <= MW_PS,
+              "masked WY map");
+static_assert(2 * (MW_SMEM + 1024) <= 233472, "two masked WY CTAs fit the shared memory of one SM");
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float *x) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(u[i] << 16);
+        x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float sum16(float x) {  // over the 16 lanes that differ in bits 0..3
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ uint4 ldg16(const unsigned short *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+template <int R>
+__global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p) {
+    constexpr int Ct = 64 / R;
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    float *Af = reinterpret_cast<float *>(sm + MW_AF), *Tf = reinterpret_cast<float *>(sm + MW_TF);
+    float *X4 = reinterpret_cast<float *>(sm + MW_X4), *Ps = reinterpret_cast<float *>(sm + MW_PS);
+    float *Us = reinterpret_cast<float *>(sm + MW_US);
+    float *gam = reinterpret_cast<float *>(sm + MW_VEC), *bet = gam + 64, *nk = bet + 64, *mq = nk + 64,
+          *msk = mq + 64;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + MW_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + MW_BAR + 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const int t0 = c * Ct, ntok = min(Ct, p.T - t0), nrows = ntok * R;
+    const size_t htok = (size_t)bh * p.T + t0, ci = (size_t)bh * p.NT + c;
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+
+    if (tid == 0) {
+        mbar_init(bar, 1u);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
+    if (tid < 64) {
+        bet[tid] = tid < nrows ? __uint_as_float((uint32_t)p.beta[htok + tid / R] << 16) : 0.f;
+        if (tid < R * R) msk[tid] = p.mask[tid];
+    }
+    if (warp == 1) {  // gamma: inclusive cumulative sum over the sub-rows; g_t enters on (t, 0)
+        const int a0 = lane, a1 = lane + 32;
+        float x0 = (a0 < nrows && a0 % R == 0) ? p.g[htok + a0 / R] : 0.f;
+        float x1 = (a1 < nrows && a1 % R == 0) ? p.g[htok + a1 / R] : 0.f;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (lane >= o) {
+                x0 += y0;
+                x1 += y1;
+            }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        gam[a0] = x0;
+        gam[a1] = x1;
+    }
+    // X: sub-row a's key k_{a / R} in row a, query t in row 64 + t (zero past
+    // the sequence), and the norms; element e: matrix e / 1024, row (e / 16) % 64,
+    // 8-column group e % 16
+    {
+        uint4 w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + kMwThr * u, mat = e >> 10, row = (e >> 4) & 63, g = e & 15;
+            const int t = mat ? row : row / R;
+            w[u] = t < ntok ? ldg16((mat ? p.q : p.k) + (htok + t) * 128 + 8 * g) : z4;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + kMwThr * u, mat = e >> 10, row = (e >> 4) & 63, g = e & 15;
+            float x[8];
+            unpack8(w[u], x);
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
+            ss = sum16(ss);
+            if (g == 0) (mat ? mq : nk)[row] = p.l2 ? 1.f / fmaxf(sqrtf(ss), 1e-12f) : 1.f;
+            *reinterpret_cast<uint4 *>(sm + MW_X + (uint32_t)(g >> 3) * 16384u +
+                                       sw128_offset((uint32_t)(row + 64 * mat), (uint32_t)((8 * g) & 63))) = w[u];
+        }
+    }
+    __syncthreads();
+    // Kw (exact) and Kd = diag(e^{gl - gamma} n) Kw's image (hi | lo), staged;
+    // element e: sub-row e / 16, 8-column group e % 16 (in slice g R / 16)
+    {
+        const float gl = gam[63];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kMwThr * u, b = e >> 4, g = e & 15, ib = b % R, j = (g * R) >> 4;
+            const uint32_t off = (uint32_t)(g >> 3) * 8192u + sw128_offset((uint32_t)b, (uint32_t)((8 * g) & 63));
+            const uint4 kx = *reinterpret_cast<const uint4 *>(sm + MW_X + (uint32_t)(g >> 3) * 16384u +
+                                                              sw128_offset((uint32_t)b, (uint32_t)((8 * g) & 63)));
+            *reinterpret_cast<uint4 *>(sm + MW_KW + off) = j == ib ? kx : z4;
+            float x[8];
+            unpack8(kx, x);
+            const float fd = j == ib ? expf(gl - gam[b]) * nk[b] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] *= fd;
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4 *>(sm + MW_KD + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + MW_KD + 16384 + off) = lo;
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) {  // Kd's image out; [K; Q] Kw^T into columns 0..63
+        bulk_store_global(p.Kdw + ci * 8192, sm + MW_KD, 32768u);
+        tma_store_commit();
+        const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16_ss(tmem, smem_desc(sb + MW_X + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                        smem_desc(sb + MW_KW + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id, ks > 0);
+        mma_commit(bar);
+    }
+    bool ok = warp_ok(wyc_wait(bar, 0, 16u, p.timeout_ns));
+    if (ok) {  // warp: TMEM lanes 32 (warp % 4) .., columns 32 (warp / 4) ..  (A is written over X)
+        tc_fence_after_sync();
+        const int q4 = warp & 3, c0 = 32 * (warp >> 2);
+        uint32_t x[32];
+        tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + c0, *reinterpret_cast<uint32_t(*)[16]>(x));
+        tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(x + 16));
+        tmem_wait_ld();
+        if (q4 < 2) {  // row a of A
+            const int a = 32 * q4 + lane, ta = a / R, ia = a % R;
+            const float fa = bet[a] * nk[a], ga = gam[a];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int b = c0 + jj;
+                Af[a * kMwLA + b] = b / R < ta ? fa * msk[ia * R + b % R] * nk[b] * expf(ga - gam[b]) *
+                                                     __uint_as_float(x[jj])
+                                               : 0.f;
+            }
+        } else {  // token t's query: row t of P, staged
+            const int t = 32 * (q4 - 2) + lane;
+            const bool live = t < ntok;
+            const float ga = live ? gam[t * R] : 0.f, fq = p.scale * mq[t];
+            float4 *Pr = reinterpret_cast<float4 *>(Ps + t * kMwLP + c0);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                float o[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int b = c0 + 4 * h + jj;
+                    o[jj] = (live && b / R <= t) ? fq * nk[b] * expf(ga - gam[b]) * __uint_as_float(x[4 * h + jj])
+                                                 : 0.f;
+                }
+                Pr[h] = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {  // P's rows out (lane: rows lane, lane + 32)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = lane + 32 * h;
+            bulk_store_global(p.Pw + ci * 4096 + (size_t)t * 64, Ps + t * kMwLP, 256u);
+        }
+        tma_store_commit();
+    }
+    unit_lower_inverse64_v4<kMwThr>(Af, Tf, X4, kMwLA);
+    // Tw = T diag(beta e^gamma) and Tu = T diag(beta) (rows a, columns 8 g ..,
+    // item e: a = e / 8, g = e % 8) and the global loads of the sub-rows'
+    // keys and values, all held in registers until T has been read
+    uint4 th[2][4];
+    uint4 kg[4], vg[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = tid + kMwThr * u, b = e >> 4, g = e & 15;
+        kg[u] = b < nrows ? ldg16(p.k + (htok + b / R) * 128 + 8 * g) : z4;
+        vg[u] = b < nrows ? ldg16(p.v + (htok + b / R) * 128 + 8 * g) : z4;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int e = tid + kMwThr * u, a = e >> 3, g = e & 7;
+        float w8[8], u8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int b = 8 * g + i;
+            const float t = b <= a ? Tf[a * kMwLA + b] : 0.f;
+            u8[i] = t * bet[b];
+            w8[i] = u8[i] * expf(gam[b]);
+        }
+        split8(w8, th[u][0], th[u][1]);
+        split8(u8, th[u][2], th[u][3]);
+    }
+    if (tid == 0) tma_store_wait_read<0>();  // Kd's staging is overwritten below
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int e = tid + kMwThr * u, a = e >> 3, g = e & 7;
+        const uint32_t off = sw128_offset((uint32_t)a, (uint32_t)(8 * g));
+#pragma unroll
+        for (int h = 0; h < 4; ++h) *reinterpret_cast<uint4 *>(sm + MW_TW + 8192u * h + off) = th[u][h];
+    }
+    // Kr (hi | lo) and the sub-rows' values
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = tid + kMwThr * u, b = e >> 4, g = e & 15, ib = b % R, j = (g * R) >> 4;
+        const uint32_t off = (uint32_t)(g >> 3) * 8192u + sw128_offset((uint32_t)b, (uint32_t)((8 * g) & 63));
+        *reinterpret_cast<uint4 *>(sm + MW_VS + off) = vg[u];
+        float x[8];
+        unpack8(kg[u], x);
+        const float fr = nk[b] * msk[ib * R + j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= fr;
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + MW_KR + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + MW_KR + 16384 + off) = lo;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (tid == 0) {  // W = Tw Kr into columns 0..127 (lanes 0..63), U = Tu V into 128..255 (lanes 64..127)
+        const uint32_t id = idesc_bf16(128, 128, false, true);
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t a = sb + MW_TW + (pr == 2 ? 8192u : 0u), b = sb + MW_KR + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem, smem_desc(a + ks * 32, 16, 1024), smem_desc(b + ks * 2048, 8192, 1024), id,
+                            (pr | ks) != 0);
+        }
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t a = sb + MW_TW + 8192u + 8192u * pr;  // rows 64..127: Tu hi, then Tu lo
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem + 128, smem_desc(a + ks * 32, 16, 1024), smem_desc(sb + MW_VS + ks * 2048, 8192, 1024),
+                            id, (pr | ks) != 0);
+        }
+        mma_commit(bar);
+    }
+    ok = warp_ok(wyc_wait(bar, 1, 16u, p.timeout_ns));
+    if (ok) {  // warp: lanes 32 (warp % 4) .. (W rows for quarters 0, 1; U rows for 2, 3), columns 64 (warp / 4) ..
+        tc_fence_after_sync();
+        const int q4 = warp & 3, c0 = 64 * (warp >> 2), a = 32 * (q4 & 1) + lane;
+        const uint32_t lb = (uint32_t)(32 * q4) << 16;
+        uint32_t x[64];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            tmem_ld16(tmem + lb + (q4 < 2 ? 0u : 128u) + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(x + 16 * h));
+        tmem_wait_ld();
+        if (q4 < 2) {  // W's image, staged
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                float y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(x[8 * h + i]);
+                uint4 hi, lo;
+                split8(y, hi, lo);
+                const int c8 = c0 + 8 * h;
+                const uint32_t off = (uint32_t)(c8 >> 6) * 8192u + sw128_offset((uint32_t)a, (uint32_t)(c8 & 63));
+                *reinterpret_cast<uint4 *>(sm + MW_WS + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + MW_WS + 16384 + off) = lo;
+            }
+        } else {  // U's row a, staged
+            float4 *Ur = reinterpret_cast<float4 *>(Us + a * kMwLU + c0);
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+                Ur[h] = make_float4(__uint_as_float(x[4 * h]), __uint_as_float(x[4 * h + 1]),
+                                    __uint_as_float(x[4 * h + 2]), __uint_as_float(x[4 * h + 3]));
+        }
+    }
+    if (tid < 64) p.Gw[ci * 64 + tid] = gam[tid];
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {  // W's image and U's rows out (lane: rows lane, lane + 32), then drain
+        if (lane == 0) bulk_store_global(p.Ww + ci * 8192, sm + MW_WS, 32768u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = lane + 32 * h;
+            bulk_store_global(p.Uw + ci * 8192 + (size_t)r * 128, Us + r * kMwLU, 512u);
+        }
+        tma_store_commit();
+        tma_store_wait_all<0>();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+constexpr int kMoThr = 256;
+constexpr uint32_t MO_S = 0;         // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each
+constexpr uint32_t MO_VN = 65536;    // Vn hi | lo: [2 value blocks][64 sub-rows][128 B], 16 KB each
+constexpr uint32_t MO_Q = 98304;     // Q: [2 key blocks][nq2 query rows][128 B] (exact), 16 KB at most
+constexpr uint32_t MO_P = 114688;    // P hi | lo: [nq2 query rows][128 B], 8 KB each
+constexpr uint32_t MO_VEC = 131072;  // gamma (64), query norms, then output row scales (64)
+constexpr uint32_t MO_BAR = MO_VEC + 512;
+constexpr uint32_t MO_SMEM = MO_BAR + 16 + 1024;
+
+__global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(MaskedTcArgs p) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    float *gam = reinterpret_cast<float *>(sm + MO_VEC), *sc = gam + 64;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + MO_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + MO_BAR + 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, bh = blockIdx.y, r = p.r, Ct = p.Ct, nq2 = (Ct + 15) / 16 * 16;
+    const int t0 = c * Ct, ntok = min(Ct, p.T - t0);
+    const size_t htok = (size_t)bh * p.T + t0, ci = (size_t)bh * p.NT + c;
+
+    if (tid == 0) {
+        mbar_init(bar, 1u);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 128);
+        tmem_relinquish();
+    }
+    if (tid < 64) gam[tid] = p.Gw[ci * 64 + tid];
+    {  // S: key row m, value columns 8 g .. (element e: m = e / 16, g = e % 16)
+        const float *Sg = p.Sw + ci * 16384;
+        float4 v[16];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + kMoThr * u, m = e >> 4, k0 = 8 * (e & 15);
+            v[2 * u] = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0);
+            v[2 * u + 1] = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0 + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + kMoThr * u, m = e >> 4, k0 = 8 * (e & 15);
+            const float x[8] = {v[2 * u].x,     v[2 * u].y,     v[2 * u].z,     v[2 * u].w,
+                                v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            const uint32_t off = (uint32_t)(k0 >> 6) * 16384u + sw128_offset((uint32_t)m, (uint32_t)(k0 & 63));
+            *reinterpret_cast<uint4 *>(sm + MO_S + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + MO_S + 32768 + off) = lo;
+        }
+    }
+    {  // Vn (sub-row b, value columns 8 g ..), P (query row t < nq2, columns 8 g ..) and Q
+        const float *Vg = p.Vnw + ci * 8192, *Pg = p.Pw + ci * 4096;
+        float4 v[8], pv[4];
+        uint4 qw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kMoThr * u, b = e >> 4, k0 = 8 * (e & 15);
+            v[2 * u] = *reinterpret_cast<const float4 *>(Vg + b * 128 + k0);
+            v[2 * u + 1] = *reinterpret_cast<const float4 *>(Vg + b * 128 + k0 + 4);
+            const int q = e >> 4;  // query row of Q (16 groups of 8 per row)
+            qw[u] = q < ntok ? ldg16(p.q + (htok + q) * 128 + k0) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + kMoThr * u, t = e >> 3, k0 = 8 * (e & 7);
+            const bool in = t < nq2;
+            pv[2 * u] = in ? *reinterpret_cast<const float4 *>(Pg + t * 64 + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
+            pv[2 * u + 1] = in ? *reinterpret_cast<const float4 *>(Pg + t * 64 + k0 + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kMoThr * u, b = e >> 4, k0 = 8 * (e & 15);
+            const float x[8] = {v[2 * u].x,     v[2 * u].y,     v[2 * u].z,     v[2 * u].w,
+                                v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            const uint32_t off = (uint32_t)(k0 >> 6) * 8192u + sw128_offset((uint32_t)b, (uint32_t)(k0 & 63));
+            *reinterpret_cast<uint4 *>(sm + MO_VN + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + MO_VN + 16384 + off) = lo;
+            // Q row q = b and the query's norm
+            const int q = b;
+            float y[8];
+            unpack8(qw[u], y);
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss += y[i] * y[i];
+            ss = sum16(ss);
+            if ((e & 15) == 0) sc[q] = p.l2 ? 1.f / fmaxf(sqrtf(ss), 1e-12f) : 1.f;  // m_q; the scale follows
+            if (q < nq2)
+                *reinterpret_cast<uint4 *>(sm + MO_Q + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
+                                           sw128_offset((uint32_t)q, (uint32_t)(k0 & 63))) = qw[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + kMoThr * u, t = e >> 3, k0 = 8 * (e & 7);
+            if (t < nq2) {
+                const float x[8] = {pv[2 * u].x,     pv[2 * u].y,     pv[2 * u].z,     pv[2 * u].w,
+                                    pv[2 * u + 1].x, pv[2 * u + 1].y, pv[2 * u + 1].z, pv[2 * u + 1].w};
+                uint4 hi, lo;
+                split8(x, hi, lo);
+                const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)k0);
+                *reinterpret_cast<uint4 *>(sm + MO_P + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + MO_P + 8192 + off) = lo;
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) {  // S^T Q^T into columns 0.., Vn^T P^T into 64..
+        const uint32_t id = idesc_bf16(128, nq2, true, false);
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t a = sb + MO_S + 32768u * pr;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tmem, smem_desc(a + ks * 2048, 16384, 1024),
+                            smem_desc(sb + MO_Q + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), id,
+                            (pr | ks) != 0);
+        }
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t a = sb + MO_VN + (pr == 2 ? 16384u : 0u), b = sb + MO_P + (pr == 1 ? 8192u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem + 64, smem_desc(a + ks * 2048, 8192, 1024), smem_desc(b + ks * 32, 16, 1024), id,
+                            (pr | ks) != 0);
+        }
+        mma_commit(bar);
+    }
+    if (tid < 64) sc[tid] = tid < ntok ? p.scale * expf(gam[tid * r]) * sc[tid] : 0.f;  // row scales
+    __syncthreads();
+    const bool ok = warp_ok(wyc_wait(bar, 0, 16u, p.timeout_ns));
+    if (ok) {  // value row dv = TMEM lane; query columns 16 j .. for j = warp / 4, + 2, ..
+        tc_fence_after_sync();
+        const int q4 = warp & 3, dv = 32 * q4 + lane;
+        const uint32_t lb = (uint32_t)(32 * q4) << 16;
+        unsigned short *op = p.o + htok * 128 + dv;
+        for (int j = warp >> 2; j < nq2 / 16; j += 2) {
+            uint32_t x1[16], x2[16];
+            tmem_ld16(tmem + lb + 16 * j, x1);
+            tmem_ld16(tmem + lb + 64 + 16 * j, x2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * j + i;
+                if (t < ntok)
+                    op[(size_t)t * 128] = __bfloat16_as_ushort(
+                        __float2bfloat16_rn(sc[t] * __uint_as_float(x1[i]) + __uint_as_float(x2[i])));
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+bool masked_tc_args_ok(const MaskedTcArgs &a) {
+    return a.BH > 0 && a.NT > 0 && a.r >= 1 && a.r <= 8 && 64 % a.r == 0 && a.Ct == 64 / a.r;
+}
+
+}  // namespace
+
+int launch_masked_wy_tc(const MaskedTcArgs &a, cudaStream_t st) {
+    if (!masked_tc_args_ok(a)) return GDN_ERR_INVALID_ARG;
+    MaskedTcArgs p = a;
+    p.timeout_ns = wait_limit_ns();
+    void (*kern)(MaskedTcArgs) = a.r == 1   ? masked_wy_tc_kernel<1>
+                                 : a.r == 2 ? masked_wy_tc_kernel<2>
+                                 : a.r == 4 ? masked_wy_tc_kernel<4>
+                                            : masked_wy_tc_kernel<8>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MW_SMEM) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    kern<<<dim3((unsigned)a.NT, (unsigned)a.BH), kMwThr, MW_SMEM, st>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int launch_masked_out_tc(const MaskedTcArgs &a, cudaStream_t st) {
+    if (!masked_tc_args_ok(a)) return GDN_ERR_INVALID_ARG;
+    MaskedTcArgs p = a;
+    p.timeout_ns = wait_limit_ns();
+    if (cudaFuncSetAttribute(masked_out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MO_SMEM) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    masked_out_tc_kernel<<<dim3((unsigned)a.NT, (unsigned)a.BH), kMoThr, MO_SMEM, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

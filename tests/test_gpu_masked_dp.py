@@ -112,3 +112,43 @@ def test_tensor_core_chain_single_chunk(T):
     ro, rs = ref(inp)
     assert rel_err(o, ro) <= TOL_BF16
     assert rel_err(sf, rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("r", [2, 4, 8])
+def test_tensor_core_kernels_general_mask_unit_norm(r):
+    """bf16 at D = 128 runs the chunk-local kernels on tcgen05 as well (exact
+    bf16 key / query products, split products for W, U and the output): a
+    general real mask, unnormalised keys with the unit-norm flag, a ragged
+    tail, against the oracle."""
+    inp = gdn_inputs(1, 2, 200, 128, 128, seed=110 + r, dtype="bf16", initial_state=True, normalise_qk=False)
+    g = torch.Generator().manual_seed(20 + r)
+    inp["mask"] = (torch.randn(r, r, generator=g) * 0.5).contiguous()
+    o, sf = run(inp, l2norm=True, scale=0.6)
+    ro, rs = ref(inp, l2norm=True, scale=0.6)
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
+@pytest.mark.parametrize("r", [2, 4])
+def test_tensor_core_kernels_strong_decay(r):
+    """Log-decays near -2 per token (over 60 nats per chunk): the decay
+    factors of A, P, W and Kd are formed per element, so nothing overflows."""
+    inp = gdn_inputs(1, 2, 140, 128, 128, seed=130 + r, dtype="bf16", g_mu=-2.0, g_div=1.0, initial_state=True)
+    inp["mask"] = slice_mask(r, seed=r)
+    o, sf = run(inp)
+    ro, rs = ref(inp)
+    assert torch.isfinite(o).all() and torch.isfinite(sf).all()
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
+
+
+def test_tensor_core_path_is_deterministic():
+    """Two CTAs of the WY kernel share each SM and every kernel of the path
+    stages through shared memory: two runs over 2048 chunks give the same
+    bits (a race between a CTA's phases would show up as differences in a few
+    chunks)."""
+    inp = gdn_inputs(1, 16, 4096, 128, 128, seed=150, dtype="bf16", initial_state=True)
+    inp["mask"] = slice_mask(2, seed=2)
+    o1, s1 = run(inp)
+    o2, s2 = run(inp)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
