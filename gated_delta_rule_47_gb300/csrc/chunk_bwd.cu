@@ -640,8 +640,38 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
     const bool tc_chain = std::is_same<T, __nv_bfloat16>::value && DK == 128 && DV == 128 &&
                           !(a.flags & GDN_PATH_SIMT) && sm100_family();
     p.img = tc_chain ? 1 : 0;
-    bwd_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
-    note_launch();
+    if (tc_chain && 64 % a.r == 0 && a.r <= 8) {  // the WY factors on tcgen05 as well
+        WyTcArgs ta{};
+        ta.q = static_cast<const unsigned short *>(a.q);
+        ta.k = static_cast<const unsigned short *>(a.k);
+        ta.v = static_cast<const unsigned short *>(a.v);
+        ta.beta = static_cast<const unsigned short *>(a.beta);
+        ta.dout = static_cast<const unsigned short *>(a.dout);
+        ta.g = a.g;
+        ta.mask = nullptr;
+        ta.Tw = p.Tw;
+        ta.Ww = p.Ww;
+        ta.Uw = p.Uw;
+        ta.Kdw = p.Kdw;
+        ta.Bw = p.Bw;
+        ta.Pw = p.Pw;
+        ta.KKw = p.KKw;
+        ta.Gw = p.Gw;
+        ta.BH = BH;
+        ta.T = a.T;
+        ta.r = a.r;
+        ta.Ct = Ct;
+        ta.NT = NT;
+        ta.l2 = p.l2;
+        ta.masked = 0;
+        ta.bwd = 1;
+        ta.scale = a.scale;
+        const int rc = launch_wy_tc(ta, st);
+        if (rc != GDN_OK) return rc;
+    } else {
+        bwd_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);
+        note_launch();
+    }
     if (tc_chain) {
         WyChainTcArgs ca{};
         ca.s0 = p.s0;

@@ -237,23 +237,28 @@ struct StateProductsTcArgs {
 };
 int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t stream);
 
-// Chunk-local kernels of the block-masked DeltaProduct forward on tcgen05
-// (bf16, Dk = Dv = 128, 64-row chunks of Ct = 64 / r tokens), around the
-// tensor-core state chain.  The WY kernel writes, per (head, chunk) ci, W and
-// Kd as the chain's bf16 hi | lo operand images (32 KB each, in the W and Kd
-// slots), U [64][128], P [64][64] and gamma [64] in fp32; the output kernel
-// reads S [128][128], Vn [64][128], P and gamma and writes o.
-struct MaskedTcArgs {
-    const unsigned short *q, *k, *v, *beta;  // bf16 bits: [BH][T][128], beta [BH][T]
-    const float *g, *mask;                   // [BH][T] log-decays, [r][r]
-    unsigned short *o;                       // [BH][T][128] bf16 bits
-    float *Ww, *Kdw, *Uw, *Vnw, *Sw, *Pw, *Gw;
-    int BH, T, r, Ct, NT, l2;
+// Chunk-local WY factors on tcgen05 (bf16, Dk = Dv = 128, 64-row chunks of
+// Ct = 64 / r tokens, r in {1, 2, 4, 8}), for the block-masked DeltaProduct
+// forward (masked = 1, bwd = 0) and for the backward passes of the chunk GDN /
+// DeltaProduct (masked = 0, bwd = 1) and of the block-masked variant (masked =
+// 1, bwd = 1).  Per (head, chunk) ci it writes W and Kd as the tensor-core
+// chain's bf16 hi | lo operand images (32 KB each, in the W and Kd slots), U
+// [64][128], P [64][64] and gamma [64] in fp32; the backward also T [64][64],
+// K K^T (read keys against write keys) [64][64] and B [128][128].  The
+// output kernel of the block-masked forward reads S [128][128], Vn [64][128],
+// P and gamma and writes o.
+struct WyTcArgs {
+    const unsigned short *q, *k, *v, *beta;  // bf16 bits; k, v, beta per sub-row (GDN / DeltaProduct) or per token
+    const unsigned short *dout;              // [BH][T][128] bf16 bits (backward)
+    const float *g, *mask;                   // [BH][T] log-decays, [r][r] (block-masked)
+    unsigned short *o;                       // [BH][T][128] bf16 bits (block-masked output kernel)
+    float *Tw, *Ww, *Uw, *Kdw, *Bw, *Vnw, *Sw, *Pw, *KKw, *Gw;
+    int BH, T, r, Ct, NT, l2, masked, bwd;
     float scale;
     unsigned long long timeout_ns;  // set by the launchers
 };
-int launch_masked_wy_tc(const MaskedTcArgs &a, cudaStream_t stream);
-int launch_masked_out_tc(const MaskedTcArgs &a, cudaStream_t stream);
+int launch_wy_tc(const WyTcArgs &a, cudaStream_t stream);
+int launch_masked_out_tc(const WyTcArgs &a, cudaStream_t stream);
 // Reads and clears the error word of the chain kernel (GDN_OK or GDN_ERR_TIMEOUT).
 int wy_chain_tc_read_clear_error();
 

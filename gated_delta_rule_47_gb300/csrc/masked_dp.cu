@@ -299,7 +299,7 @@ int run(const MaskedDpArgs &a, cudaStream_t st) {
                           !(a.flags & GDN_PATH_SIMT) && sm100_family();
     p.img = tc_chain ? 1 : 0;
     // with the tensor-core chain the chunk-local kernels run on tcgen05 too
-    MaskedTcArgs ta{};
+    WyTcArgs ta{};
     if (tc_chain) {
         ta.q = static_cast<const unsigned short *>(a.q);
         ta.k = static_cast<const unsigned short *>(a.k);
@@ -322,7 +322,8 @@ int run(const MaskedDpArgs &a, cudaStream_t st) {
         ta.NT = NT;
         ta.l2 = p.l2;
         ta.scale = a.scale;
-        const int rc = launch_masked_wy_tc(ta, st);
+        ta.masked = 1;
+        const int rc = launch_wy_tc(ta, st);
         if (rc != GDN_OK) return rc;
     } else {
         mdp_wy_kernel<T, DK, DV><<<dim3((unsigned)NT, (unsigned)BH), kThr, s1, st>>>(p);

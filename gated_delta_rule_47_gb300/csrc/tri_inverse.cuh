@@ -56,17 +56,19 @@ __device__ __forceinline__ void unit_lower_inverse(const float *A, float *T, flo
     }
 }
 
-// As unit_lower_inverse for C = 64 and NT = 256, for tiles whose rows are
-// 16-byte aligned (A and T 16-byte aligned, stride a multiple of 4): T is
-// cleared first, so that the merges can run over whole blocks, and each
-// merge thread keeps a column of a 2- or 4-row tile in registers, reading the
-// left factor's rows four k at a time with 16-byte loads (one broadcast
-// wavefront each) and the right factor's column once per k.  X: scratch of
-// 1024 floats (16-byte aligned).  Ends with the CTA synchronised.
+// As unit_lower_inverse for C = 64 (NT >= 256 threads, the merges on the
+// first 256), for tiles whose rows are 16-byte aligned (A and T 16-byte
+// aligned, stride a multiple of 4): T is cleared first, so that the merges can
+// run over whole blocks, and each merge thread keeps a column of a 2- or
+// 4-row tile in registers, reading the left factor's rows four k at a time
+// with 16-byte loads (one broadcast wavefront each) and the right factor's
+// column once per k.  X: scratch of 1024 floats (16-byte aligned).  Ends with
+// the CTA synchronised.
 template <int NT>
 __device__ __forceinline__ void unit_lower_inverse64_v4(const float *A, float *T, float *X, int stride) {
-    static_assert(NT == 256, "the tiles of the merges assume 256 threads");
+    static_assert(NT >= 256 && NT % 32 == 0, "the merges' tiles take 256 threads");
     const int tid = threadIdx.x;
+    const bool act = tid < 256;
     for (int e = tid; e < 64 * stride / 4; e += NT) reinterpret_cast<float4 *>(T)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
     // 1. diagonal 16 x 16 blocks: thread (block b, column c)
@@ -89,66 +91,75 @@ __device__ __forceinline__ void unit_lower_inverse64_v4(const float *A, float *T
     //    then T[o+16.., o..] = -T[o+16.., o+16..] Y.  Thread: pair tid / 128, rows 2 ((tid / 16) % 8) + {0, 1},
     //    column tid % 16.
     {
-        const int pp = tid >> 7, i0 = 2 * ((tid >> 4) & 7), j = tid & 15, o = 32 * pp;
-        float y[2] = {0.f, 0.f};
+        const int pp = (tid >> 7) & 1, i0 = 2 * ((tid >> 4) & 7), j = tid & 15, o = 32 * pp;
+        if (act) {
+            float y[2] = {0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-            float4 a[2];
+            for (int k = 0; k < 16; k += 4) {
+                float4 a[2];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) a[r] = *reinterpret_cast<const float4 *>(A + (o + 16 + i0 + r) * stride + o + k);
-            const float t0 = T[(o + k) * stride + o + j], t1 = T[(o + k + 1) * stride + o + j];
-            const float t2 = T[(o + k + 2) * stride + o + j], t3 = T[(o + k + 3) * stride + o + j];
+                for (int r = 0; r < 2; ++r) a[r] = *reinterpret_cast<const float4 *>(A + (o + 16 + i0 + r) * stride + o + k);
+                const float t0 = T[(o + k) * stride + o + j], t1 = T[(o + k + 1) * stride + o + j];
+                const float t2 = T[(o + k + 2) * stride + o + j], t3 = T[(o + k + 3) * stride + o + j];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) y[r] += a[r].x * t0 + a[r].y * t1 + a[r].z * t2 + a[r].w * t3;
+                for (int r = 0; r < 2; ++r) y[r] += a[r].x * t0 + a[r].y * t1 + a[r].z * t2 + a[r].w * t3;
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) X[pp * 256 + (i0 + r) * 16 + j] = y[r];
         }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) X[pp * 256 + (i0 + r) * 16 + j] = y[r];
         __syncthreads();
-        float z[2] = {0.f, 0.f};
+        if (act) {
+            float z[2] = {0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-            float4 a[2];
+            for (int k = 0; k < 16; k += 4) {
+                float4 a[2];
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
-                a[r] = *reinterpret_cast<const float4 *>(T + (o + 16 + i0 + r) * stride + o + 16 + k);
-            const float *Y = X + pp * 256 + k * 16 + j;
+                for (int r = 0; r < 2; ++r)
+                    a[r] = *reinterpret_cast<const float4 *>(T + (o + 16 + i0 + r) * stride + o + 16 + k);
+                const float *Y = X + pp * 256 + k * 16 + j;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) z[r] += a[r].x * Y[0] + a[r].y * Y[16] + a[r].z * Y[32] + a[r].w * Y[48];
+                for (int r = 0; r < 2; ++r) z[r] += a[r].x * Y[0] + a[r].y * Y[16] + a[r].z * Y[32] + a[r].w * Y[48];
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) T[(o + 16 + i0 + r) * stride + o + j] = -z[r];
         }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) T[(o + 16 + i0 + r) * stride + o + j] = -z[r];
         __syncthreads();
     }
     // 3. the 32-level merge: Y = A[32.., 0..] T[0.., 0..], T[32.., 0..] = -T[32.., 32..] Y.
     //    Thread: rows 4 (tid / 32) + {0..3}, column tid % 32.
     {
-        const int i0 = 4 * (tid >> 5), j = tid & 31;
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        const int i0 = 4 * ((tid >> 5) & 7), j = tid & 31;
+        if (act) {
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
-        for (int k = 0; k < 32; k += 4) {
-            float4 a[4];
+            for (int k = 0; k < 32; k += 4) {
+                float4 a[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(A + (32 + i0 + r) * stride + k);
-            const float t0 = T[k * stride + j], t1 = T[(k + 1) * stride + j];
-            const float t2 = T[(k + 2) * stride + j], t3 = T[(k + 3) * stride + j];
+                for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(A + (32 + i0 + r) * stride + k);
+                const float t0 = T[k * stride + j], t1 = T[(k + 1) * stride + j];
+                const float t2 = T[(k + 2) * stride + j], t3 = T[(k + 3) * stride + j];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) y[r] += a[r].x * t0 + a[r].y * t1 + a[r].z * t2 + a[r].w * t3;
+                for (int r = 0; r < 4; ++r) y[r] += a[r].x * t0 + a[r].y * t1 + a[r].z * t2 + a[r].w * t3;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) X[(i0 + r) * 32 + j] = y[r];
         }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) X[(i0 + r) * 32 + j] = y[r];
         __syncthreads();
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
+        if (act) {
+            float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
-        for (int k = 0; k < 32; k += 4) {
-            float4 a[4];
+            for (int k = 0; k < 32; k += 4) {
+                float4 a[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4 *>(T + (32 + i0 + r) * stride + 32 + k);
-            const float *Y = X + k * 32 + j;
+                for (int r = 0; r < 4; ++r)
+                    a[r] = *reinterpret_cast<const float4 *>(T + (32 + i0 + r) * stride + 32 + k);
+                const float *Y = X + k * 32 + j;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) z[r] += a[r].x * Y[0] + a[r].y * Y[32] + a[r].z * Y[64] + a[r].w * Y[96];
+                for (int r = 0; r < 4; ++r) z[r] += a[r].x * Y[0] + a[r].y * Y[32] + a[r].z * Y[64] + a[r].w * Y[96];
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) T[(32 + i0 + r) * stride + j] = -z[r];
         }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) T[(32 + i0 + r) * stride + j] = -z[r];
         __syncthreads();
     }
 }

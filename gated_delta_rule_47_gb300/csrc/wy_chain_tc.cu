@@ -489,39 +489,45 @@ int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t st) {
 
 
 // ---------------------------------------------------------------------------
-// Block-masked DeltaProduct forward, the chunk-local kernels on tcgen05 for
-// bf16 at Dk = Dv = 128 (gated_deltaproduct test.py: the mask_ij coupling of
-// `gated_chunk_scaled_dot_kkt_fwd_kernel`, `gated_fwd_recompute_w_u_kernel`
-// and the chunk output of `gated_chunk_fwd_o_fn`).  Sub-row b = (token t_b,
-// slice i_b) of a 64-row chunk of Ct = 64 / r tokens; kw_b is slice i_b of
-// k_{t_b} (zero elsewhere) and kr_b is k_{t_b} with slice j scaled by
-// mask[i_b][j].  With the unit-norm flag n_t = 1/||k_t|| and m_t = 1/||q_t||
-// (else 1) stay scalar factors, so the raw bf16 keys and queries enter the
-// products exactly.
+// The chunk-local WY factors on tcgen05 for bf16 at Dk = Dv = 128, for the
+// block-masked DeltaProduct forward and for the backward passes of the chunk
+// GDN / DeltaProduct and of the block-masked variant (gated_deltaproduct
+// test.py: `gated_chunk_scaled_dot_kkt_fwd_kernel` with its mask_ij coupling,
+// the triangular solve, `gated_fwd_recompute_w_u_kernel`,
+// `gated_bwd_prepare_wy_repr_kernel` and the chunk output of
+// `gated_chunk_fwd_o_fn`).  Sub-row b of a 64-row chunk of Ct = 64 / r tokens
+// belongs to token t_b = b / r.  GDN / DeltaProduct: sub-row b has its own key
+// (read and write key alike), value and beta.  Block-masked: kw_b is slice
+// i_b = b % r of k_{t_b} (zero elsewhere) and kr_b is k_{t_b} with slice j
+// scaled by mask[i_b][j].  With the unit-norm flag n_b = 1/||key of b|| and
+// m_t = 1/||q_t|| (else 1) stay scalar factors, so the raw bf16 keys and
+// queries enter the products exactly.
 //
-// masked_wy_tc_kernel, one CTA of 256 threads per chunk (two per SM):
-//   1. [K; Q] Kw^T as one exact product (M = 128: the chunk's token keys in
-//      rows 0..63, its queries in rows 64..127; N = 64 sub-rows), since
-//      k_t . kw_b is the dot product of slice i_b of k_t and of k_{t_b};
-//   2. A[a][b] = beta_a e^{gamma_a - gamma_b} mask[i_a][i_b] n_{t_a} n_{t_b}
-//      k_{t_a} . kw_b for t_b < t_a, and the output factors
-//      P[t][b] = scale e^{gamma_{t r} - gamma_b} m_t n_{t_b} q_t . kw_b for
-//      t_b <= t (to the workspace);
+// wy_tc_kernel, one CTA per chunk:
+//   1. [K; Q] Kw^T as one exact product (M = 128: the sub-rows' raw read keys
+//      in rows 0..63, the queries in rows 64..127; N = 64 sub-rows), since
+//      kr_a . kw_b is mask[i_a][i_b] times the dot product of k_{t_a} and kw_b;
+//   2. A[a][b] = beta_a e^{gamma_a - gamma_b} kr_a . kw_b below the diagonal
+//      (earlier tokens for the block-masked variant), the output factors
+//      P[t][b] = scale e^{gamma_{t r} - gamma_b} m_t q_t . kw_b for t_b <= t,
+//      and for the backward kr_a . kw_b itself;
 //   3. T = (I + A)^-1 on the CUDA cores (tri_inverse.cuh);
 //   4. W = T diag(beta e^gamma) Kr as three split products (both operands
 //      rounded) and U = T diag(beta) V as two (v is exact), M = 128 with rows
 //      0..63 used, N = 128;
-//   5. W and Kd = diag(e^{gl - gamma} n) Kw as the chain's operand images, U
-//      and gamma in fp32.
+//   5. W and Kd = diag(e^{gl - gamma}) Kw as the chain's operand images, U, P,
+//      gamma in fp32; the backward also T, kr . kw and the chunk's term of the
+//      state gradient B = Q^T diag(scale e^{gamma_{t r}} m) dO - W^T P^T dO, as
+//      B^T = dO^T Q' (two split products: dO is exact) - Y^T W (three), with
+//      Y^T = dO^T P formed while T is inverted.
 // masked_out_tc_kernel, one CTA of 256 threads per chunk, with S the state
 // entering it:  o_t = scale e^{gamma_{t r}} m_t q_t S + (P Vn)_t, as
 // o^T = S^T Q^T (two split products: q is exact) + Vn^T P^T (three), M = 128
 // value rows, N = the chunk's query rows rounded up to 16.
 namespace {
 
-constexpr int kMwThr = 256;  // two CTAs per SM
-// One 97 KB region reused by the phases (byte offsets):
-//   loads, [K; Q] Kw^T:  X = [sub-row keys k_{t_a}, rows 0..63 | queries q_t, rows 64..127] K-major,
+// Shared memory of wy_tc_kernel, reused by the phases (byte offsets):
+//   loads, [K; Q] Kw^T:  X = [sub-row read keys, rows 0..63 | queries q_t, rows 64..127] K-major,
 //                        2 key blocks of 16 KB, at 0; Kw [2 key blocks][64 sub-rows][128 B] (exact)
 //                        at 32768; Kd's image (hi | lo), staged for one bulk copy, at 49152
 //   A, the inverse:      A, T fp32 [64][68] at 0 and 17408, scratch (1024 floats) at 34816;
@@ -530,26 +536,33 @@ constexpr int kMwThr = 256;  // two CTAs per SM
 //                        Kr hi | lo [2 key blocks][64 sub-rows][128 B] at 32768,
 //                        the sub-rows' values [2 value blocks][64 sub-rows][128 B] (exact) at 65536
 //   the results:         W's image at 0, U's rows (132-float stride) at 32768, both for bulk copies
-// The padded row strides keep the row-per-lane stores of the staging free of
-// bank conflicts.
+// and for the backward, from 99328 on: K K^T's rows (68-float stride, staged),
+// P as an MN-major operand (rows t, hi | lo), dO (rows t, 2 value blocks,
+// exact), Q' = diag(scale e^gamma m) Q (rows t, 2 key blocks, hi | lo), and Y^T
+// = (P^T dO)^T as a K-major operand (rows dv, hi | lo) over the staging of P
+// and K K^T once those have left.  The padded row strides keep the
+// row-per-lane stores of the staging free of bank conflicts.
 constexpr uint32_t MW_X = 0, MW_KW = 32768, MW_KD = 49152;
 constexpr int kMwLA = 68;  // fp32 row stride of A and T (16-byte aligned rows)
 constexpr uint32_t MW_AF = 0, MW_TF = 64 * kMwLA * 4, MW_X4 = 2 * 64 * kMwLA * 4, MW_PS = 81920;
 constexpr uint32_t MW_TW = 0, MW_KR = 32768, MW_VS = 65536;
 constexpr uint32_t MW_WS = 0, MW_US = 32768;
 constexpr int kMwLP = 68, kMwLU = 132;  // staging row strides (floats)
-constexpr uint32_t MW_VEC = 99328;      // gamma, beta, n (per sub-row), m, mask: 64 floats each
-constexpr uint32_t MW_BAR = MW_VEC + 5 * 256;
-constexpr uint32_t MW_SMEM = MW_BAR + 16 + 1024;
+constexpr uint32_t MW_KKS = 99328, MW_PI = 116736, MW_DOI = 133120, MW_QP = 149504, MW_YI = 81920;
+__host__ __device__ constexpr uint32_t mw_vec(bool bwd) { return bwd ? 182272u : 99328u; }  // gamma, beta, n, m, mask: 64 floats each
+__host__ __device__ constexpr uint32_t mw_bar(bool bwd) { return mw_vec(bwd) + 5 * 256; }     // 4 mbarriers, then the TMEM address
+__host__ __device__ constexpr uint32_t mw_smem(bool bwd) { return mw_bar(bwd) + 48 + 1024; }
 // The M = 128 products read A rows 64..127 from the 8 KB after the start of
 // their 64-row operand: W's rows past Tw are Tw lo and Tu hi, and U's
 // operand starts 8 KB before Tu hi (lo), so that Tu sits in rows 64..127 and
 // U lands in TMEM lanes 64..127; every row read is finite and the rows not
 // wanted are not used.
-static_assert(MW_X4 + 4096 <= MW_PS && MW_KD + 32768 <= MW_PS && MW_PS + 64 * kMwLP * 4 <= MW_VEC &&
-                  MW_VS + 16384 <= MW_PS && MW_US + 64 * kMwLU * 4 <= MW_PS,
-              "masked WY map");
-static_assert(2 * (MW_SMEM + 1024) <= 233472, "two masked WY CTAs fit the shared memory of one SM");
+static_assert(MW_X4 + 4096 <= MW_PS && MW_KD + 32768 <= MW_PS && MW_PS + 64 * kMwLP * 4 <= MW_KKS &&
+                  MW_VS + 16384 <= MW_PS && MW_US + 64 * kMwLU * 4 <= MW_PS && MW_KKS + 64 * kMwLP * 4 <= MW_PI &&
+                  MW_PI + 16384 <= MW_DOI && MW_DOI + 16384 <= MW_QP && MW_QP + 32768 <= mw_vec(true) &&
+                  MW_YI + 32768 <= MW_PI && mw_vec(false) >= MW_PS + 64 * kMwLP * 4,
+              "WY map");
+static_assert(2 * (mw_smem(false) + 1024) <= 233472 && mw_smem(true) <= 232448, "WY kernels fit shared memory");
 
 __device__ __forceinline__ void unpack8(const uint4 &w, float *x) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -568,36 +581,41 @@ __device__ __forceinline__ float sum16(float x) {  // over the 16 lanes that dif
 
 __device__ __forceinline__ uint4 ldg16(const unsigned short *p) { return *reinterpret_cast<const uint4 *>(p); }
 
-template <int R>
-__global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p) {
-    constexpr int Ct = 64 / R;
+// wy_tc_kernel<R, MASKED, BWD>: one CTA per chunk; 256 threads and two CTAs
+// per SM for the forward, 512 threads and one CTA per SM for the backward.
+// MASKED: the sub-rows' keys are the token keys' slices (read keys scaled by
+// the mask); otherwise each sub-row has its own key, value and beta.
+template <int R, bool MASKED, bool BWD>
+__global__ void __launch_bounds__(BWD ? 512 : 256, BWD ? 1 : 2) wy_tc_kernel(WyTcArgs p) {
+    constexpr int NT = BWD ? 512 : 256, CG = NT / 128, Ct = 64 / R, NQ2 = (Ct + 15) / 16 * 16;
+    constexpr uint32_t VEC = mw_vec(BWD), BAR = mw_bar(BWD), TCOLS = BWD ? 512u : 256u;
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     float *Af = reinterpret_cast<float *>(sm + MW_AF), *Tf = reinterpret_cast<float *>(sm + MW_TF);
     float *X4 = reinterpret_cast<float *>(sm + MW_X4), *Ps = reinterpret_cast<float *>(sm + MW_PS);
-    float *Us = reinterpret_cast<float *>(sm + MW_US);
-    float *gam = reinterpret_cast<float *>(sm + MW_VEC), *bet = gam + 64, *nk = bet + 64, *mq = nk + 64,
-          *msk = mq + 64;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + MW_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + MW_BAR + 8);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *Us = reinterpret_cast<float *>(sm + MW_US), *KKs = reinterpret_cast<float *>(sm + MW_KKS);
+    float *gam = reinterpret_cast<float *>(sm + VEC), *bet = gam + 64, *nk = bet + 64, *mq = nk + 64, *msk = mq + 64;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + BAR);  // [K; Q] Kw^T | W, U (and Y) | B
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + BAR + 32);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q4 = warp & 3;
+    const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
     const int c = blockIdx.x, bh = blockIdx.y;
     const int t0 = c * Ct, ntok = min(Ct, p.T - t0), nrows = ntok * R;
-    const size_t htok = (size_t)bh * p.T + t0, ci = (size_t)bh * p.NT + c;
+    const size_t htok = (size_t)bh * p.T + t0, hrow = htok * R, ci = (size_t)bh * p.NT + c;
     const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
 
     if (tid == 0) {
-        mbar_init(bar, 1u);
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1u);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tslot, 256);
+        tmem_alloc(tslot, TCOLS);
         tmem_relinquish();
     }
     if (tid < 64) {
-        bet[tid] = tid < nrows ? __uint_as_float((uint32_t)p.beta[htok + tid / R] << 16) : 0.f;
-        if (tid < R * R) msk[tid] = p.mask[tid];
+        bet[tid] = tid < nrows ? __uint_as_float((uint32_t)p.beta[MASKED ? htok + tid / R : hrow + tid] << 16) : 0.f;
+        if (MASKED && tid < R * R) msk[tid] = p.mask[tid];
     }
     if (warp == 1) {  // gamma: inclusive cumulative sum over the sub-rows; g_t enters on (t, 0)
         const int a0 = lane, a1 = lane + 32;
@@ -614,20 +632,21 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
         gam[a0] = x0;
         gam[a1] = x1;
     }
-    // X: sub-row a's key k_{a / R} in row a, query t in row 64 + t (zero past
-    // the sequence), and the norms; element e: matrix e / 1024, row (e / 16) % 64,
+    // X: sub-row a's read key in row a, query t in row 64 + t (zero past the
+    // sequence), and the norms; element e: matrix e / 1024, row (e / 16) % 64,
     // 8-column group e % 16
     {
-        uint4 w[8];
+        constexpr int U = 2048 / NT;
+        uint4 w[U];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + kMwThr * u, mat = e >> 10, row = (e >> 4) & 63, g = e & 15;
-            const int t = mat ? row : row / R;
-            w[u] = t < ntok ? ldg16((mat ? p.q : p.k) + (htok + t) * 128 + 8 * g) : z4;
+        for (int u = 0; u < U; ++u) {
+            const int e = tid + NT * u, mat = e >> 10, row = (e >> 4) & 63, g = e & 15;
+            const size_t src = mat ? htok + row : (MASKED ? htok + row / R : hrow + row);
+            w[u] = (mat ? row : row / R) < ntok ? ldg16((mat ? p.q : p.k) + src * 128 + 8 * g) : z4;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + kMwThr * u, mat = e >> 10, row = (e >> 4) & 63, g = e & 15;
+        for (int u = 0; u < U; ++u) {
+            const int e = tid + NT * u, mat = e >> 10, row = (e >> 4) & 63, g = e & 15;
             float x[8];
             unpack8(w[u], x);
             float ss = 0.f;
@@ -639,27 +658,57 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
                                        sw128_offset((uint32_t)(row + 64 * mat), (uint32_t)((8 * g) & 63))) = w[u];
         }
     }
+    if constexpr (BWD) {  // dO rows t (exact) as an MN-major operand: [2 value blocks][64 rows][128 B]
+        constexpr int U = 1024 / NT;
+        uint4 w[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = tid + NT * u, t = e >> 4, g = e & 15;
+            w[u] = t < ntok ? ldg16(p.dout + (htok + t) * 128 + 8 * g) : z4;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = tid + NT * u, t = e >> 4, g = e & 15;
+            *reinterpret_cast<uint4 *>(sm + MW_DOI + (uint32_t)(g >> 3) * 8192u +
+                                       sw128_offset((uint32_t)t, (uint32_t)((8 * g) & 63))) = w[u];
+        }
+    }
     __syncthreads();
     // Kw (exact) and Kd = diag(e^{gl - gamma} n) Kw's image (hi | lo), staged;
-    // element e: sub-row e / 16, 8-column group e % 16 (in slice g R / 16)
+    // element e: sub-row e / 16, 8-column group e % 16 (in slice g R / 16).  The
+    // backward also forms Q' = diag(scale e^{gamma_{t r}} m) Q (hi | lo).
     {
         const float gl = gam[63];
+        constexpr int U = 1024 / NT;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + kMwThr * u, b = e >> 4, g = e & 15, ib = b % R, j = (g * R) >> 4;
+        for (int u = 0; u < U; ++u) {
+            const int e = tid + NT * u, b = e >> 4, g = e & 15;
+            const bool own = !MASKED || ((g * R) >> 4) == b % R;
             const uint32_t off = (uint32_t)(g >> 3) * 8192u + sw128_offset((uint32_t)b, (uint32_t)((8 * g) & 63));
             const uint4 kx = *reinterpret_cast<const uint4 *>(sm + MW_X + (uint32_t)(g >> 3) * 16384u +
                                                               sw128_offset((uint32_t)b, (uint32_t)((8 * g) & 63)));
-            *reinterpret_cast<uint4 *>(sm + MW_KW + off) = j == ib ? kx : z4;
+            *reinterpret_cast<uint4 *>(sm + MW_KW + off) = own ? kx : z4;
             float x[8];
             unpack8(kx, x);
-            const float fd = j == ib ? expf(gl - gam[b]) * nk[b] : 0.f;
+            const float fd = own ? expf(gl - gam[b]) * nk[b] : 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] *= fd;
             uint4 hi, lo;
             split8(x, hi, lo);
             *reinterpret_cast<uint4 *>(sm + MW_KD + off) = hi;
             *reinterpret_cast<uint4 *>(sm + MW_KD + 16384 + off) = lo;
+            if constexpr (BWD) {  // query row t = b
+                const int t = b;
+                const uint4 qx = *reinterpret_cast<const uint4 *>(
+                    sm + MW_X + (uint32_t)(g >> 3) * 16384u + sw128_offset((uint32_t)(64 + t), (uint32_t)((8 * g) & 63)));
+                unpack8(qx, x);
+                const float fq = t < ntok ? p.scale * expf(gam[t * R]) * mq[t] : 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] *= fq;
+                split8(x, hi, lo);
+                *reinterpret_cast<uint4 *>(sm + MW_QP + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + MW_QP + 16384 + off) = lo;
+            }
         }
     }
     fence_proxy_async_smem();
@@ -675,70 +724,94 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
         for (int ks = 0; ks < 8; ++ks)
             mma_bf16_ss(tmem, smem_desc(sb + MW_X + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                         smem_desc(sb + MW_KW + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id, ks > 0);
-        mma_commit(bar);
+        mma_commit(&bar[0]);
     }
-    bool ok = warp_ok(wyc_wait(bar, 0, 16u, p.timeout_ns));
-    if (ok) {  // warp: TMEM lanes 32 (warp % 4) .., columns 32 (warp / 4) ..  (A is written over X)
+    bool ok = warp_ok(wyc_wait(&bar[0], 0, 16u, p.timeout_ns));
+    if (ok) {  // warp: TMEM lanes 32 (warp % 4) .., columns CW (warp / 4) ..  (A is written over X)
+        constexpr int CW = 64 / CG;
         tc_fence_after_sync();
-        const int q4 = warp & 3, c0 = 32 * (warp >> 2);
-        uint32_t x[32];
-        tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + c0, *reinterpret_cast<uint32_t(*)[16]>(x));
-        tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(x + 16));
-        tmem_wait_ld();
-        if (q4 < 2) {  // row a of A
-            const int a = 32 * q4 + lane, ta = a / R, ia = a % R;
-            const float fa = bet[a] * nk[a], ga = gam[a];
+        const int c0 = CW * (warp >> 2);
+        uint32_t x[CW];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
+        for (int h = 0; h < CW / 16; ++h)
+            tmem_ld16(tmem + lb + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(x + 16 * h));
+        tmem_wait_ld();
+        if (q4 < 2) {  // row a of A (and of the read keys against the write keys)
+            const int a = 32 * q4 + lane, ta = a / R, ia = a % R;
+            const float fa = bet[a], na = nk[a], ga = gam[a];
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
                 const int b = c0 + jj;
-                Af[a * kMwLA + b] = b / R < ta ? fa * msk[ia * R + b % R] * nk[b] * expf(ga - gam[b]) *
-                                                     __uint_as_float(x[jj])
-                                               : 0.f;
+                const float kk = (MASKED ? msk[ia * R + b % R] : 1.f) * na * nk[b] * __uint_as_float(x[jj]);
+                Af[a * kMwLA + b] = (MASKED ? b / R < ta : b < a) ? fa * expf(ga - gam[b]) * kk : 0.f;
+                if constexpr (BWD) KKs[a * kMwLP + b] = kk;
             }
-        } else {  // token t's query: row t of P, staged
+        } else {  // token t's query: row t of P, staged (and, for the backward, as an operand)
             const int t = 32 * (q4 - 2) + lane;
             const bool live = t < ntok;
             const float ga = live ? gam[t * R] : 0.f, fq = p.scale * mq[t];
+            float pv[CW];
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+                const int b = c0 + jj;
+                pv[jj] = (live && b / R <= t) ? fq * nk[b] * expf(ga - gam[b]) * __uint_as_float(x[jj]) : 0.f;
+            }
             float4 *Pr = reinterpret_cast<float4 *>(Ps + t * kMwLP + c0);
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                float o[4];
+            for (int h = 0; h < CW / 4; ++h) Pr[h] = make_float4(pv[4 * h], pv[4 * h + 1], pv[4 * h + 2], pv[4 * h + 3]);
+            if constexpr (BWD) {
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int b = c0 + 4 * h + jj;
-                    o[jj] = (live && b / R <= t) ? fq * nk[b] * expf(ga - gam[b]) * __uint_as_float(x[4 * h + jj])
-                                                 : 0.f;
+                for (int h = 0; h < CW / 8; ++h) {
+                    uint4 hi, lo;
+                    split8(pv + 8 * h, hi, lo);
+                    const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)(c0 + 8 * h));
+                    *reinterpret_cast<uint4 *>(sm + MW_PI + off) = hi;
+                    *reinterpret_cast<uint4 *>(sm + MW_PI + 8192 + off) = lo;
                 }
-                Pr[h] = make_float4(o[0], o[1], o[2], o[3]);
             }
         }
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) {  // P's rows out (lane: rows lane, lane + 32)
+    if (warp == 0) {  // P's rows (and K K^T's) out (lane: rows lane, lane + 32)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int t = lane + 32 * h;
             bulk_store_global(p.Pw + ci * 4096 + (size_t)t * 64, Ps + t * kMwLP, 256u);
+            if constexpr (BWD) bulk_store_global(p.KKw + ci * 4096 + (size_t)t * 64, KKs + t * kMwLP, 256u);
         }
         tma_store_commit();
     }
-    unit_lower_inverse64_v4<kMwThr>(Af, Tf, X4, kMwLA);
+    unit_lower_inverse64_v4<NT>(Af, Tf, X4, kMwLA);
+    if constexpr (BWD) {  // T's rows out
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int t = lane + 32 * h;
+                bulk_store_global(p.Tw + ci * 4096 + (size_t)t * 64, Tf + t * kMwLA, 256u);
+            }
+            tma_store_commit();
+        }
+    }
     // Tw = T diag(beta e^gamma) and Tu = T diag(beta) (rows a, columns 8 g ..,
     // item e: a = e / 8, g = e % 8) and the global loads of the sub-rows'
     // keys and values, all held in registers until T has been read
-    uint4 th[2][4];
-    uint4 kg[4], vg[4];
+    constexpr int UT = 512 / NT, UK = 1024 / NT;
+    uint4 th[UT][4];
+    uint4 kg[UK], vg[UK];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int e = tid + kMwThr * u, b = e >> 4, g = e & 15;
-        kg[u] = b < nrows ? ldg16(p.k + (htok + b / R) * 128 + 8 * g) : z4;
-        vg[u] = b < nrows ? ldg16(p.v + (htok + b / R) * 128 + 8 * g) : z4;
+    for (int u = 0; u < UK; ++u) {
+        const int e = tid + NT * u, b = e >> 4, g = e & 15;
+        const size_t src = MASKED ? htok + b / R : hrow + b;
+        kg[u] = b < nrows ? ldg16(p.k + src * 128 + 8 * g) : z4;
+        vg[u] = b < nrows ? ldg16(p.v + src * 128 + 8 * g) : z4;
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int e = tid + kMwThr * u, a = e >> 3, g = e & 7;
+    for (int u = 0; u < UT; ++u) {
+        const int e = tid + NT * u, a = e >> 3, g = e & 7;
         float w8[8], u8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -750,24 +823,24 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
         split8(w8, th[u][0], th[u][1]);
         split8(u8, th[u][2], th[u][3]);
     }
-    if (tid == 0) tma_store_wait_read<0>();  // Kd's staging is overwritten below
+    if (warp == 0) tma_store_wait_read<0>();  // the staged Kd, P (K K^T, T) are overwritten below
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int e = tid + kMwThr * u, a = e >> 3, g = e & 7;
+    for (int u = 0; u < UT; ++u) {
+        const int e = tid + NT * u, a = e >> 3, g = e & 7;
         const uint32_t off = sw128_offset((uint32_t)a, (uint32_t)(8 * g));
 #pragma unroll
         for (int h = 0; h < 4; ++h) *reinterpret_cast<uint4 *>(sm + MW_TW + 8192u * h + off) = th[u][h];
     }
     // Kr (hi | lo) and the sub-rows' values
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int e = tid + kMwThr * u, b = e >> 4, g = e & 15, ib = b % R, j = (g * R) >> 4;
+    for (int u = 0; u < UK; ++u) {
+        const int e = tid + NT * u, b = e >> 4, g = e & 15;
         const uint32_t off = (uint32_t)(g >> 3) * 8192u + sw128_offset((uint32_t)b, (uint32_t)((8 * g) & 63));
         *reinterpret_cast<uint4 *>(sm + MW_VS + off) = vg[u];
         float x[8];
         unpack8(kg[u], x);
-        const float fr = nk[b] * msk[ib * R + j];
+        const float fr = nk[b] * (MASKED ? msk[(b % R) * R + ((g * R) >> 4)] : 1.f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] *= fr;
         uint4 hi, lo;
@@ -797,21 +870,30 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
                 mma_bf16_ss(tmem + 128, smem_desc(a + ks * 32, 16, 1024), smem_desc(sb + MW_VS + ks * 2048, 8192, 1024),
                             id, (pr | ks) != 0);
         }
-        mma_commit(bar);
-    }
-    ok = warp_ok(wyc_wait(bar, 1, 16u, p.timeout_ns));
-    if (ok) {  // warp: lanes 32 (warp % 4) .. (W rows for quarters 0, 1; U rows for 2, 3), columns 64 (warp / 4) ..
-        tc_fence_after_sync();
-        const int q4 = warp & 3, c0 = 64 * (warp >> 2), a = 32 * (q4 & 1) + lane;
-        const uint32_t lb = (uint32_t)(32 * q4) << 16;
-        uint32_t x[64];
+        if constexpr (BWD) {  // Y^T = dO^T P (P^ hi | lo) into columns 256..319
+            const uint32_t idy = idesc_bf16(128, 64, true, true);
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+            for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+                for (int ks = 0; ks < NQ2 / 16; ++ks)
+                    mma_bf16_ss(tmem + 256, smem_desc(sb + MW_DOI + ks * 2048, 8192, 1024),
+                                smem_desc(sb + MW_PI + 8192u * pr + ks * 2048, 8192, 1024), idy, (pr | ks) != 0);
+        }
+        mma_commit(&bar[1]);
+    }
+    ok = warp_ok(wyc_wait(&bar[1], 0, 16u, p.timeout_ns));
+    if (ok) {  // warp: lanes 32 (warp % 4) .. (W rows for quarters 0, 1; U rows for 2, 3), columns CW (warp / 4) ..
+        constexpr int CW = 128 / CG;
+        tc_fence_after_sync();
+        const int c0 = CW * (warp >> 2), a = 32 * (q4 & 1) + lane;
+        uint32_t x[CW];
+#pragma unroll
+        for (int h = 0; h < CW / 16; ++h)
             tmem_ld16(tmem + lb + (q4 < 2 ? 0u : 128u) + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(x + 16 * h));
         tmem_wait_ld();
         if (q4 < 2) {  // W's image, staged
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
+            for (int h = 0; h < CW / 8; ++h) {
                 float y[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) y[i] = __uint_as_float(x[8 * h + i]);
@@ -825,16 +907,32 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
         } else {  // U's row a, staged
             float4 *Ur = reinterpret_cast<float4 *>(Us + a * kMwLU + c0);
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
+            for (int h = 0; h < CW / 4; ++h)
                 Ur[h] = make_float4(__uint_as_float(x[4 * h]), __uint_as_float(x[4 * h + 1]),
                                     __uint_as_float(x[4 * h + 2]), __uint_as_float(x[4 * h + 3]));
         }
+        if constexpr (BWD) {  // Y^T row dv = lane of this quarter, columns 16 (warp / 4) ..: K-major operand
+            uint32_t y[16];
+            const int dv = 32 * q4 + lane, cy = 16 * (warp >> 2);
+            tmem_ld16(tmem + lb + 256 + cy, y);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(y[8 * h + i]);
+                uint4 hi, lo;
+                split8(f, hi, lo);
+                const uint32_t off = sw128_offset((uint32_t)dv, (uint32_t)(cy + 8 * h));
+                *reinterpret_cast<uint4 *>(sm + MW_YI + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + MW_YI + 16384 + off) = lo;
+            }
+        }
     }
-    if (tid < 64) p.Gw[ci * 64 + tid] = gam[tid];
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) {  // W's image and U's rows out (lane: rows lane, lane + 32), then drain
+    if (warp == 0) {  // W's image and U's rows out (lane: rows lane, lane + 32)
         if (lane == 0) bulk_store_global(p.Ww + ci * 8192, sm + MW_WS, 32768u);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -842,9 +940,49 @@ __global__ void __launch_bounds__(kMwThr, 2) masked_wy_tc_kernel(MaskedTcArgs p)
             bulk_store_global(p.Uw + ci * 8192 + (size_t)r * 128, Us + r * kMwLU, 512u);
         }
         tma_store_commit();
+    }
+    if constexpr (BWD) {
+        tc_fence_after_sync();
+        if (tid == 0) {  // B^T = dO^T Q' - Y^T W into columns 384..511
+            const uint32_t id1 = idesc_bf16(128, 128, true, true), id2 = idesc_bf16(128, 128, false, true, true);
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+                for (int ks = 0; ks < NQ2 / 16; ++ks)
+                    mma_bf16_ss(tmem + 384, smem_desc(sb + MW_DOI + ks * 2048, 8192, 1024),
+                                smem_desc(sb + MW_QP + 16384u * pr + ks * 2048, 8192, 1024), id1, (pr | ks) != 0);
+#pragma unroll
+            for (int pr = 0; pr < 3; ++pr) {
+                const uint32_t a = sb + MW_YI + (pr == 2 ? 16384u : 0u), b = sb + MW_WS + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ss(tmem + 384, smem_desc(a + ks * 32, 16, 1024), smem_desc(b + ks * 2048, 8192, 1024),
+                                id2, 1u);
+            }
+            mma_commit(&bar[2]);
+        }
+        ok = warp_ok(wyc_wait(&bar[2], 0, 16u, p.timeout_ns));
+        if (ok) {  // B^T row dv = lane of this quarter, key columns 32 (warp / 4) ..: B[dk][dv]
+            tc_fence_after_sync();
+            const int dv = 32 * q4 + lane, k0 = 32 * (warp >> 2);
+            float *Bg = p.Bw + ci * 16384 + dv;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t y[16];
+                tmem_ld16(tmem + lb + 384 + k0 + 16 * h, y);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Bg[(size_t)(k0 + 16 * h + i) * 128] = __uint_as_float(y[i]);
+            }
+        }
+    }
+    if (tid < 64) p.Gw[ci * 64 + tid] = gam[tid];
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
         tma_store_wait_all<0>();
         tc_fence_after_sync();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, TCOLS);
     }
 }
 
@@ -857,7 +995,7 @@ constexpr uint32_t MO_VEC = 131072;  // gamma (64), query norms, then output row
 constexpr uint32_t MO_BAR = MO_VEC + 512;
 constexpr uint32_t MO_SMEM = MO_BAR + 16 + 1024;
 
-__global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(MaskedTcArgs p) {
+__global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(WyTcArgs p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
@@ -1011,30 +1149,38 @@ __global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(MaskedTcArgs p
     }
 }
 
-bool masked_tc_args_ok(const MaskedTcArgs &a) {
+bool wy_tc_args_ok(const WyTcArgs &a) {
     return a.BH > 0 && a.NT > 0 && a.r >= 1 && a.r <= 8 && 64 % a.r == 0 && a.Ct == 64 / a.r;
+}
+
+template <bool MASKED, bool BWD>
+void (*wy_tc_pick(int r))(WyTcArgs) {
+    return r == 1 ? wy_tc_kernel<1, MASKED, BWD>
+           : r == 2 ? wy_tc_kernel<2, MASKED, BWD>
+           : r == 4 ? wy_tc_kernel<4, MASKED, BWD>
+                    : wy_tc_kernel<8, MASKED, BWD>;
 }
 
 }  // namespace
 
-int launch_masked_wy_tc(const MaskedTcArgs &a, cudaStream_t st) {
-    if (!masked_tc_args_ok(a)) return GDN_ERR_INVALID_ARG;
-    MaskedTcArgs p = a;
+int launch_wy_tc(const WyTcArgs &a, cudaStream_t st) {
+    if (!wy_tc_args_ok(a)) return GDN_ERR_INVALID_ARG;
+    if (!a.masked && !a.bwd) return GDN_ERR_UNSUPPORTED;  // the GDN / DeltaProduct forward is fused (scan_tc.cu)
+    WyTcArgs p = a;
     p.timeout_ns = wait_limit_ns();
-    void (*kern)(MaskedTcArgs) = a.r == 1   ? masked_wy_tc_kernel<1>
-                                 : a.r == 2 ? masked_wy_tc_kernel<2>
-                                 : a.r == 4 ? masked_wy_tc_kernel<4>
-                                            : masked_wy_tc_kernel<8>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MW_SMEM) != cudaSuccess)
+    void (*kern)(WyTcArgs) = a.bwd ? (a.masked ? wy_tc_pick<true, true>(a.r) : wy_tc_pick<false, true>(a.r))
+                                   : wy_tc_pick<true, false>(a.r);
+    const uint32_t smem = mw_smem(a.bwd != 0);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_CUDA;
-    kern<<<dim3((unsigned)a.NT, (unsigned)a.BH), kMwThr, MW_SMEM, st>>>(p);
+    kern<<<dim3((unsigned)a.NT, (unsigned)a.BH), a.bwd ? 512 : 256, smem, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-int launch_masked_out_tc(const MaskedTcArgs &a, cudaStream_t st) {
-    if (!masked_tc_args_ok(a)) return GDN_ERR_INVALID_ARG;
-    MaskedTcArgs p = a;
+int launch_masked_out_tc(const WyTcArgs &a, cudaStream_t st) {
+    if (!wy_tc_args_ok(a)) return GDN_ERR_INVALID_ARG;
+    WyTcArgs p = a;
     p.timeout_ns = wait_limit_ns();
     if (cudaFuncSetAttribute(masked_out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MO_SMEM) !=
         cudaSuccess)

@@ -255,3 +255,32 @@ def test_full_size_fp32_sampled_heads():
                          sub["initial_state"], heads(dsf, idx))
     for name, x, y in zip(NAMES, got, ref):
         assert rel_err(heads(x, idx).cpu(), y) <= TOL_F32, name
+
+
+@pytest.mark.parametrize("r,T", [(2, 150), (4, 90), (8, 40)])
+def test_tensor_core_wy_deltaproduct_unit_norm(r, T):
+    """bf16 DeltaProduct at D = 128 forms the WY factors, T, K K^T, P and B on
+    tcgen05: unnormalised sub-step keys under the unit-norm flag, against the
+    oracle."""
+    inp, do, dsf = grads_case(1, 2, T, 128, 128, "bf16", True, r=r, seed=70 + r)
+    d = to_dev(inp)
+    got = binding.deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do.cuda(), d["initial_state"],
+                                         dsf.cuda(), scale=0.6, l2norm=True, need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.deltaproduct_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], do, inp["initial_state"], dsf,
+                                  scale=0.6, l2norm=True)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name
+
+
+def test_tensor_core_path_is_deterministic():
+    """Two runs of the bf16 GDN backward over 512 chunks give the same bits."""
+    inp, do, dsf = grads_case(1, 16, 2048, 128, 128, "bf16", False, seed=81)
+    d = to_dev(inp)
+    do, dsf = do.cuda(), dsf.cuda()
+    outs = [binding.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], do, d["initial_state"], dsf,
+                                  need_dinitial=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)

@@ -115,3 +115,37 @@ def test_tensor_core_chain_matches_the_cuda_core_chain(r, T):
     for name, x, y in zip(NAMES, tc, simt):
         tol = 5e-3 if x.dtype == torch.bfloat16 else 2e-4
         assert rel_err(x, y.double().cpu().numpy()) <= tol, name
+
+
+@pytest.mark.parametrize("r", [2, 4, 8])
+def test_tensor_core_wy_general_mask_unit_norm(r):
+    """bf16 at D = 128 forms the WY factors, T, K K^T, P and the state-gradient
+    term B on tcgen05: a general real mask, unnormalised keys under the
+    unit-norm flag and a ragged tail, against the oracle."""
+    inp, do, dsf = case(150, 128, r, "bf16", True, seed=40 + r, general_mask=True)
+    d = to_dev(inp)
+    got = binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"], do.cuda(),
+                                                d["initial_state"], dsf.cuda(), scale=0.7, l2norm=True,
+                                                need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.masked_deltaproduct_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["mask"], do,
+                                         inp["initial_state"], dsf, scale=0.7, l2norm=True)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name
+
+
+def test_tensor_core_path_is_deterministic():
+    """Two runs of the bf16 backward over 512 chunks give the same bits."""
+    inp, do, dsf = case(2048, 128, 2, "bf16", False, seed=61)
+    inp = {k: (v.repeat(1, 4, *([1] * (v.dim() - 2))) if k != "mask" else v) for k, v in inp.items()}
+    d = to_dev(inp)
+    do = do.repeat(1, 4, 1, 1).cuda()
+    dsf = dsf.repeat(1, 4, 1, 1).cuda()
+    outs = []
+    for _ in range(2):
+        outs.append(binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"], do,
+                                                          d["initial_state"], dsf, need_dinitial=True))
+    torch.cuda.synchronize()
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
