@@ -27,6 +27,9 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# the backward passes on bf16 at D = 128: what runs where
+BWD_PATH = "WY factors, state chains and state products on tcgen05; input gradients on the CUDA cores (fp32)"
+
 WORKLOAD = "gdn_b4h16t4096d128_bf16"
 METRIC = "GDN fwd tokens/s (B4,H16,T4096,D128 bf16) + % of binding roofline"
 UNIT = "tokens/s"
@@ -445,7 +448,7 @@ def secondary(args, dev):
                      "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del d, o, wsw
         torch.cuda.empty_cache()
-    # the block-masked DeltaProduct variant (chunk-local kernels on the CUDA cores, chain on tcgen05)
+    # the block-masked DeltaProduct variant (WY factors, state chain and output on tcgen05)
     w = WORKLOADS["masked_dp_r2_b4h16t4096d128_bf16"]
     d = {k: v.to(dev) for k, v in w.make().items()}
     o = torch.empty(w.B, w.H, w.T, w.D, dtype=torch.bfloat16, device=dev)
@@ -456,7 +459,7 @@ def secondary(args, dev):
     nbytes = w.B * w.H * w.T * gdn_bytes_per_token_head(w.D)
     out[w.name] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
                    "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                   "path": "chunk-local kernels on the CUDA cores (fp32), state chains on tcgen05",
+                   "path": "WY factors, state chain and output on tcgen05",
                    "launches_per_call": 3}
     # its backward
     gom = torch.randn(w.B, w.H, w.T, w.D, device=dev).to(torch.bfloat16)
@@ -464,12 +467,13 @@ def secondary(args, dev):
                        dtype=torch.uint8, device=dev)
     ms = timeit(lambda: binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"],
                                                               gom, workspace=wsmb))
+    nbytes = w.B * w.H * w.T * (14 * w.D + 14)  # q, k, v, beta, g, do in; dq, dk, dv, dbeta, dg out
     out["masked_dp_bwd_r2_b4h16t4096d128_bf16"] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
-                                                   "path": "chunk-local kernels on the CUDA cores (fp32), state chains on tcgen05",
-                                                   "launches_per_call": 3}
+                                                   "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                                   "path": BWD_PATH, "launches_per_call": 4}
     del d, o, wsm, gom, wsmb
     torch.cuda.empty_cache()
-    # the chunkwise GDN backward on the headline's shape (chunk-local kernels on the CUDA cores, chains on tcgen05)
+    # the chunkwise GDN backward on the headline's shape
     w = WORKLOADS["gdn_b4h16t4096d128_bf16"]
     d = {k: v.to(dev) for k, v in w.make().items()}
     gen = torch.Generator(device=dev).manual_seed(3)
@@ -480,8 +484,7 @@ def secondary(args, dev):
     nbytes = w.B * w.H * w.T * (14 * w.D + 14)  # q, k, v, beta, g, do in; dq, dk, dv, dbeta, dg out
     out["gdn_bwd_b4h16t4096d128_bf16"] = {"ms": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
                                           "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                          "launches_per_call": 3,
-                                          "path": "chunk-local kernels on the CUDA cores (fp32), state chains on tcgen05"}
+                                          "launches_per_call": 4, "path": BWD_PATH}
     del d, go, wsg
     torch.cuda.empty_cache()
     w = WORKLOADS["cam_b2n32760h16d128_bf16"]
