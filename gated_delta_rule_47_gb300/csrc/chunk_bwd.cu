@@ -37,8 +37,9 @@
 //      instead of fp32), otherwise wy_chain_kernel (CUDA cores, fp32; each CTA
 //      holds 64 value columns of one head's state, since the columns of both
 //      chains are independent).
-//   3. (tensor-core chains only) state_products_tc_kernel: Z = Vn dS'^T,
-//      t1 = dO S^T and <dS', S> per chunk on tcgen05, over the dS' slot.
+//   3. (tensor-core chains only) chunk_products_tc_kernel: Z = Vn dS'^T,
+//      t1 = dO S^T, dR = T^T dVn, dR Vn^T, t2 = dR S^T, dO Vn^T, <dS', S> and
+//      each row's (Kd dS') . Vn per chunk on tcgen05, over dead slots.
 //   4. bwd_grad_kernel (one CTA per chunk): every input gradient.
 #include <cuda_bf16.h>
 
@@ -274,8 +275,10 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
 
     load_rows<T, DK>(Ks, (const T *)p.k + ch.hrow * DK, nrows, p.l2 != 0, nk);
     load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ntok, p.l2 != 0, nq);
-    load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
-    load_rows<float, DV, LV>(Vns, p.Vnw + ch.ci * kC * DV, kC, false, nullptr);
+    if (!p.img) {  // with the tensor-core products, dO and Vn enter only through them
+        load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
+        load_rows<float, DV, LV>(Vns, p.Vnw + ch.ci * kC * DV, kC, false, nullptr);
+    }
     if (tid < kC) {
         gam[tid] = p.Gw[ch.ci * kC + tid];
         eg[tid] = expf(gam[tid]);
@@ -289,9 +292,11 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     const float gl = gam[kC - 1];
 
     // 1. through the state leaving the chunk: Kd dS' and Z = Vn dS'^T into dk.
-    //    With the tensor-core chains the chunk's dS' slot holds Z (and t1 = dO S^T,
-    //    step 8) from the state-products kernel, the first half of its B slot
-    //    holds Kd dS' (from the reverse chain), and float 8192 of B holds <dS', S>.
+    //    With the tensor-core chains the products kernel has left (layout with
+    //    ChunkProductsTcArgs): Z and t1 = dO S^T in the dS' slot, dR and t2 = dR S^T
+    //    in the S slot, dR Vn^T and DOV = dO Vn^T in the Vn slot, <dS', S> and
+    //    each row's (Kd dS') . Vn in the B slot; the steps below read them.
+    const float *Vg = p.Vnw + ch.ci * kC * DV;
     float accKdS[2][TV], accDK[2][TK];
     zero(accKdS);
     zero(accDK);
@@ -326,30 +331,34 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         s = warp_sum(s);
         if ((tid & 31) == 0) red[tid >> 5] = s;
     }
-    if (p.img) {  // Y = Kd dS', over the first half of the chunk's B slot
-        const float *Yg = p.Bw + ch.ci * DK * DV;
+    if (p.img) {  // (Kd dS') . Vn of each row from the products kernel
+        if (tx == 0) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < TV; ++j) accKdS[i][j] = Yg[(ty + 32 * i) * DV + tx + 16 * j];
-    } else {  // K dS' -> Kd dS'
+            for (int i = 0; i < 2; ++i) {
+                const int b = ty + 32 * i;
+                const float w = p.Bw[ch.ci * DK * DV + 8256 + b];
+                rowg[b] -= w;
+                lastg[b] = w;
+            }
+        }
+    } else {  // K dS' -> Kd dS', and the decay gradients of the state's update
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const float s = expf(gl - gam[ty + 32 * i]);
 #pragma unroll
             for (int j = 0; j < TV; ++j) accKdS[i][j] *= s;
         }
-    }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {  // decay gradients of the state's update
-        const int b = ty + 32 * i;
-        float w = 0.f;
+        for (int i = 0; i < 2; ++i) {
+            const int b = ty + 32 * i;
+            float w = 0.f;
 #pragma unroll
-        for (int j = 0; j < TV; ++j) w += accKdS[i][j] * Vns[b * LV + tx + 16 * j];
-        w = row_sum16(w);
-        if (tx == 0) {
-            rowg[b] -= w;
-            lastg[b] = w;
+            for (int j = 0; j < TV; ++j) w += accKdS[i][j] * Vns[b * LV + tx + 16 * j];
+            w = row_sum16(w);
+            if (tx == 0) {
+                rowg[b] -= w;
+                lastg[b] = w;
+            }
         }
     }
 
@@ -357,25 +366,36 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     {
         const float *Pg = p.Pw + ch.ci * kC * kC, *Tg = p.Tw + ch.ci * kC * kC;
         stage_rows<kC, kC>(Xa, LC, Pg);
-        stage_rows<kC, kC>(Xb, LC, Tg);
+        if (p.img)
+            stage_rows<64, DV>(Hs, LV, Sg);  // dR, from the products kernel
+        else
+            stage_rows<kC, kC>(Xb, LC, Tg);
     }
     __syncthreads();
 
-    // 3. dVn = Kd dS' + P^^T dO into Hs
-    mm<kThr, 2, TV>(accKdS, Xa, 1, LC, dOs, LV, 1, kC);
+    T *dvp = (T *)p.dv + ch.hrow * DV;
+    if (p.img) {  // dv = beta dR
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int j = 0; j < TV; ++j) Hs[(ty + 32 * i) * LV + tx + 16 * j] = accKdS[i][j];
-    __syncthreads();
+            for (int j = 0; j < TV; ++j) {
+                const int m = ty + 32 * i, n = tx + 16 * j;
+                if (m < nrows) st_f(dvp + (size_t)m * DV + n, bet[m] * Hs[m * LV + n]);
+            }
+    } else {
+        // 3. dVn = Kd dS' + P^^T dO into Hs
+        mm<kThr, 2, TV>(accKdS, Xa, 1, LC, dOs, LV, 1, kC);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TV; ++j) Hs[(ty + 32 * i) * LV + tx + 16 * j] = accKdS[i][j];
+        __syncthreads();
 
-    // 4. dR = T^T dVn into Hs; dv = beta dR
-    {
+        // 4. dR = T^T dVn into Hs; dv = beta dR
         float acc[2][TV];
         zero(acc);
         mm<kThr, 2, TV>(acc, Xb, 1, LC, Hs, LV, 1, kC);
         __syncthreads();
-        T *dvp = (T *)p.dv + ch.hrow * DV;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -384,14 +404,22 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
                 Hs[m * LV + n] = acc[i][j];
                 if (m < nrows) st_f(dvp + (size_t)m * DV + n, bet[m] * acc[i][j]);
             }
+        __syncthreads();
     }
-    __syncthreads();
 
     // 5. DOV = dO Vn^T: the output's decay gradients, and P~ into Xa
     {
         float acc[2][4];
         zero(acc);
-        mm_nt<kThr, 2, 4>(acc, dOs, LV, Vns, LV, DV);
+        if (p.img) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[i][j] = ty + 32 * i < ntok ? Vg[4096 + (ty + 32 * i) * kC + tx + 16 * j] : 0.f;
+        } else {
+            mm_nt<kThr, 2, 4>(acc, dOs, LV, Vns, LV, DV);
+        }
         float col[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -417,7 +445,14 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     {
         float ta[2][4], tk[2][4];
         zero(ta);
-        mm_nt<kThr, 2, 4>(ta, Hs, LV, Vns, LV, DV);
+        if (p.img) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ta[i][j] = Vg[(ty + 32 * i) * kC + tx + 16 * j];
+        } else {
+            mm_nt<kThr, 2, 4>(ta, Hs, LV, Vns, LV, DV);
+        }
         {  // K K^T, formed by the WY kernel
             const float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
@@ -471,23 +506,24 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     //    (S^T q_i).do_i = q_i.(S do_i) and (S^T k_b).dR_b = k_b.(S dR_b).
     float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
     for (int h = 0; h < NH; ++h) {
-        stage_rows<64, DV>(Vns, LV, Sg + (size_t)64 * h * DV);
+        if (!p.img) stage_rows<64, DV>(Vns, LV, Sg + (size_t)64 * h * DV);
         __syncthreads();
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        if (p.img) {  // t1 = dO S^T from the state-products kernel
+        if (p.img) {  // t1 = dO S^T and t2 = dR S^T from the products kernel
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int m = ty + 32 * i;
-                    t1[i][j] = m < ntok ? dSg[8192 + m * DK + 64 * h + tx + 16 * j] : 0.f;
+                    const int m = ty + 32 * i, c = 64 * h + tx + 16 * j;
+                    t1[i][j] = m < ntok ? dSg[8192 + m * DK + c] : 0.f;
+                    t2[i][j] = Sg[8192 + m * DK + c];
                 }
         } else {
             mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LV, DV);
+            mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LV, DV);
         }
-        mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LV, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int m = ty + 32 * i;
@@ -691,17 +727,19 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
         ca.roles = 2;
         int rc = launch_wy_chain_tc(ca, st);
         if (rc != GDN_OK) return rc;
-        StateProductsTcArgs sa{};
+        ChunkProductsTcArgs sa{};
         sa.Sw = p.Sw;
         sa.Vnw = p.Vnw;
         sa.dSw = p.dSw;
         sa.Bw = p.Bw;
+        sa.Pw = p.Pw;
+        sa.Tw = p.Tw;
         sa.dout = static_cast<const unsigned short *>(a.dout);
         sa.BH = BH;
         sa.NT = NT;
         sa.T = a.T;
         sa.Ct = Ct;
-        rc = launch_state_products_tc(sa, st);
+        rc = launch_chunk_products_tc(sa, st);
         if (rc != GDN_OK) return rc;
     } else {
         WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};

@@ -223,19 +223,25 @@ struct WyChainTcArgs {
     unsigned long long timeout_ns;  // bounded-wait limit (set by the launcher)
 };
 int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t stream);
-// The state products of the chunk backward's gradient kernel on tcgen05
-// (wy_chain_tc.cu), per (head, chunk) after both chains: Z = Vn dS'^T over
-// floats 0..8191 and t1 = dO S^T ([Ct][128]) over floats 8192.. of the chunk's
-// dS' slot, and <dS', S> to float 8192 of its B slot.
-struct StateProductsTcArgs {
-    const float *Sw, *Vnw;           // [ci][128][128] S entering the chunk, [ci][64][128] Vn
-    float *dSw, *Bw;                 // [ci][128][128] dS' (then Z | t1), [ci][128][128] B (float 8192: the dot)
+// The products the backward's gradient kernels need that involve no
+// per-row reduction, on tcgen05 (wy_chain_tc.cu), per (head, chunk) ci after
+// both chains, written over slots that nothing reads afterwards:
+//   dS' slot: Z = Vn dS'^T [64][128] (floats 0..8191), t1 = dO S^T [Ct][128] (8192..)
+//   S slot:   dR = T^T dVn [64][128] (0..8191), t2 = dR S^T [64][128] (8192..)
+//   Vn slot:  dR Vn^T [64][64] (0..4095), DOV = dO Vn^T [64][64] (4096..; rows
+//             past the chunk's queries undefined)
+//   B slot:   <dS', S> at float 8192, each row's Y . Vn at floats 8256..8319
+// with dVn = Y + P^^T dO, Y = Kd dS' (the first half of the B slot, from the
+// reverse chain), P^ and T from the WY kernel.
+struct ChunkProductsTcArgs {
+    float *Sw, *Vnw, *dSw, *Bw;      // [ci][128][128], [ci][64][128], [ci][128][128], [ci][128][128]
+    const float *Pw, *Tw;            // [ci][64][64]
     const unsigned short *dout;      // [BH][T][128] bf16 bits of dO
     int BH, NT, T, Ct;               // Ct: query rows (tokens) per chunk
     int nq2;                         // set by the launcher
     unsigned long long timeout_ns;   // set by the launcher
 };
-int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t stream);
+int launch_chunk_products_tc(const ChunkProductsTcArgs &a, cudaStream_t stream);
 
 // Chunk-local WY factors on tcgen05 (bf16, Dk = Dv = 128, 64-row chunks of
 // Ct = 64 / r tokens, r in {1, 2, 4, 8}), for the block-masked DeltaProduct

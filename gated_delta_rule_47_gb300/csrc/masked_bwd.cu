@@ -288,8 +288,11 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
 
     load_rows<T, DK>(Kt, (const T *)p.k + ch.htok * DK, ntok, p.l2 != 0, nk);
     load_rows<T, DK>(Qs, (const T *)p.q + ch.htok * DK, ntok, p.l2 != 0, nq);
-    load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
-    stage_rows<kC, DV>(Vns, LX, p.Vnw + ch.ci * kC * DV);
+    if (!p.img) {  // with the tensor-core products, dO and Vn enter only through them
+        load_rows<T, DV, LV>(dOs, (const T *)p.dout + ch.htok * DV, ntok, false, nullptr);
+        stage_rows<kC, DV>(Vns, LX, p.Vnw + ch.ci * kC * DV);
+    }
+    const float *Vg = p.Vnw + ch.ci * kC * DV;
     if (tid < kC) {
         gam[tid] = p.Gw[ch.ci * kC + tid];
         eg[tid] = expf(gam[tid]);
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     float accKdS[2][TV], accD[2][TK];
     zero(accKdS);
     zero(accD);
-    if (p.img) {  // Z = Vn dS'^T over the dS' slot, <dS', S> at float 8192 of B (state-products kernel)
+    if (p.img) {  // from the products kernel (layout with ChunkProductsTcArgs): Z, <dS', S>
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int a = ty + 32 * i;
@@ -349,48 +352,55 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         s = warp_sum(s);
         if ((tid & 31) == 0) red[tid >> 5] = s;
     }
-    if (p.img) {  // Y = Kd dS', over the first half of the chunk's B slot
-        const float *Yg = p.Bw + ch.ci * DK * DV;
+    if (p.img) {  // (Kd dS') . Vn of each row from the products kernel
+        if (tx == 0) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < TV; ++j) accKdS[i][j] = Yg[(ty + 32 * i) * DV + tx + 16 * j];
-    } else {  // Kw dS' -> Kd dS'
+            for (int i = 0; i < 2; ++i) {
+                const int b = ty + 32 * i;
+                const float w = p.Bw[ch.ci * DK * DV + 8256 + b];
+                rowg[b] -= w;
+                lastg[b] = w;
+            }
+        }
+    } else {  // Kw dS' -> Kd dS', and the decay gradients of the state's update
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const float s = expf(gl - gam[ty + 32 * i]);
 #pragma unroll
             for (int j = 0; j < TV; ++j) accKdS[i][j] *= s;
         }
-    }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int b = ty + 32 * i;
-        float w = 0.f;
+        for (int i = 0; i < 2; ++i) {
+            const int b = ty + 32 * i;
+            float w = 0.f;
 #pragma unroll
-        for (int j = 0; j < TV; ++j) w += accKdS[i][j] * Vns[b * LX + tx + 16 * j];
-        w = row_sum16(w);
-        if (tx == 0) {
-            rowg[b] -= w;
-            lastg[b] = w;
+            for (int j = 0; j < TV; ++j) w += accKdS[i][j] * Vns[b * LX + tx + 16 * j];
+            w = row_sum16(w);
+            if (tx == 0) {
+                rowg[b] -= w;
+                lastg[b] = w;
+            }
         }
     }
-    // 2. P^ (formed by the WY kernel) into Xa, T into Xb
+    // 2. P^ (formed by the WY kernel) into Xa, T into Xb (dR from the products kernel into Hs)
     {
         const float *Pg = p.Pw + ch.ci * kC * kC, *Tg = p.Tw + ch.ci * kC * kC;
         stage_rows<kC, kC>(Xa, LC, Pg);
-        stage_rows<kC, kC>(Xb, LC, Tg);
+        if (p.img)
+            stage_rows<64, DV>(Hs, LV, Sg);
+        else
+            stage_rows<kC, kC>(Xb, LC, Tg);
     }
     __syncthreads();
-    // 3. dVn = Kd dS' + P^^T dO into Hs
-    mm<kThr, 2, TV>(accKdS, Xa, 1, LC, dOs, LV, 1, kC);
+    if (!p.img) {
+        // 3. dVn = Kd dS' + P^^T dO into Hs
+        mm<kThr, 2, TV>(accKdS, Xa, 1, LC, dOs, LV, 1, kC);
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int j = 0; j < TV; ++j) Hs[(ty + 32 * i) * LV + tx + 16 * j] = accKdS[i][j];
-    __syncthreads();
-    // 4. dR = T^T dVn into Hs
-    {
+            for (int j = 0; j < TV; ++j) Hs[(ty + 32 * i) * LV + tx + 16 * j] = accKdS[i][j];
+        __syncthreads();
+        // 4. dR = T^T dVn into Hs
         float acc[2][TV];
         zero(acc);
         mm<kThr, 2, TV>(acc, Xb, 1, LC, Hs, LV, 1, kC);
@@ -399,13 +409,21 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < TV; ++j) Hs[(ty + 32 * i) * LV + tx + 16 * j] = acc[i][j];
+        __syncthreads();
     }
-    __syncthreads();
     // 5. DOV = dO Vn^T: the output's decay gradients, and P~ into Xa
     {
         float acc[2][4];
         zero(acc);
-        mm_nt<kThr, 2, 4>(acc, dOs, LV, Vns, LX, DV);
+        if (p.img) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[i][j] = ty + 32 * i < ntok ? Vg[4096 + (ty + 32 * i) * kC + tx + 16 * j] : 0.f;
+        } else {
+            mm_nt<kThr, 2, 4>(acc, dOs, LV, Vns, LX, DV);
+        }
         float col[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -431,7 +449,14 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     {
         float ta[2][4], tk[2][4];
         zero(ta);
-        mm_nt<kThr, 2, 4>(ta, Hs, LV, Vns, LX, DV);
+        if (p.img) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ta[i][j] = Vg[(ty + 32 * i) * kC + tx + 16 * j];
+        } else {
+            mm_nt<kThr, 2, 4>(ta, Hs, LV, Vns, LX, DV);
+        }
         {  // Kr Kw^T, formed by the WY kernel
             const float *KKg = p.KKw + ch.ci * kC * kC;
 #pragma unroll
@@ -495,23 +520,24 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     //    products give (S^T q_t).do_t = q_t.(S do_t) and (S^T kr_b).dR_b = kr_b.(S dR_b).
     float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
     for (int h = 0; h < NH; ++h) {
-        stage_rows<64, DV>(Vns, LX, Sg + (size_t)64 * h * DV);
+        if (!p.img) stage_rows<64, DV>(Vns, LX, Sg + (size_t)64 * h * DV);
         __syncthreads();
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        if (p.img) {  // t1 = dO S^T from the state-products kernel
+        if (p.img) {  // t1 = dO S^T and t2 = dR S^T from the products kernel
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int m = ty + 32 * i;
-                    t1[i][j] = m < ntok ? dSg[8192 + m * DK + 64 * h + tx + 16 * j] : 0.f;
+                    const int m = ty + 32 * i, c = 64 * h + tx + 16 * j;
+                    t1[i][j] = m < ntok ? dSg[8192 + m * DK + c] : 0.f;
+                    t2[i][j] = Sg[8192 + m * DK + c];
                 }
         } else {
             mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LX, DV);
+            mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LX, DV);
         }
-        mm_nt<kThr, 2, 4>(t2, Hs, LV, Vns, LX, DV);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int m = ty + 32 * i;
@@ -753,7 +779,7 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
         ca.roles = 2;
         int rc = launch_wy_chain_tc(ca, st);
         if (rc != GDN_OK) return rc;
-        StateProductsTcArgs sa{};
+        ChunkProductsTcArgs sa{};
         sa.Sw = p.Sw;
         sa.Vnw = p.Vnw;
         sa.dSw = p.dSw;
@@ -763,7 +789,9 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
         sa.NT = NT;
         sa.T = a.T;
         sa.Ct = p.Ct;
-        rc = launch_state_products_tc(sa, st);
+        sa.Pw = p.Pw;
+        sa.Tw = p.Tw;
+        rc = launch_chunk_products_tc(sa, st);
         if (rc != GDN_OK) return rc;
     } else {
         WyChainParams cp{p.s0, p.dsf, nullptr, p.ds0, p.Sw, p.dSw, p.Ww, p.Kdw, p.Uw, p.Vnw, p.Bw, p.Gw, NT};

@@ -323,55 +323,69 @@ int wy_chain_tc_read_clear_error() {
 
 
 // ======================= the state products of the gradient kernels (tcgen05)
-// state_products_tc_kernel: per (head, chunk), after both chains, with S the
-// state entering the chunk, dS' the gradient leaving it, Vn [64][128] and the
-// chunk's nq query rows of dO [nq][128] (bf16):
-//   Z  = Vn dS'^T      [64][128]   (3 split products: both operands fp32)
-//   t1 = dO S^T        [nq][128]   (2 split products: dO is exact in bf16)
-//   <dS', S>
-// Z and t1 go over the chunk's dS' slot (Z in floats 0 .. 8191, t1 in
-// 8192 ..), which no later kernel reads, and <dS', S> to float 8192 of the
-// chunk's B slot (whose first half holds Y).  One CTA per chunk: 256 threads
-// split the fp32 operands into bf16 hi | lo K-major tiles, thread 0 issues
-// Z^T = dS' Vn^T and t1^T = S dO^T (M = 128 key rows) into TMEM, and the
-// threads write the transposes back.
+// chunk_products_tc_kernel: per (head, chunk), after both chains, with S the
+// state entering the chunk, dS' the gradient leaving it, Vn [64][128], the
+// chunk's nq query rows of dO (bf16), P^ and T [64][64] from the WY kernel
+// and Y = Kd dS' from the reverse chain, three rounds of MMAs (M = 128):
+//   1. Z^T = dS' Vn^T and t1^T = S dO^T, Yw^T = dO^T P^ and DOV^T = Vn dO^T;
+//   2. dR^T = dVn^T T, with dVn^T = Y^T + Yw^T as a K-major operand;
+//   3. dR Vn^T (dR^T's image read as an MN-major operand) and t2^T = S dR^T.
+// Each fp32 operand is split into bf16 hi | lo tiles (hi.hi + hi.lo + lo.hi,
+// about 2^-16 relative; two terms where the other operand, dO, is exact).
+// The results go over slots that nothing reads afterwards (the layout is
+// listed with ChunkProductsTcArgs); <dS', S> and each row's Y . Vn as well.
 namespace {
 
-constexpr int kSpThr = 256;
-constexpr uint32_t SP_A1 = 0;        // dS' hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each
-constexpr uint32_t SP_A2 = 65536;    // S hi | lo, likewise
-constexpr uint32_t SP_B1 = 131072;   // Vn hi | lo: [2 value blocks][64 rows][128 B], 16 KB each
-constexpr uint32_t SP_B2 = 163840;   // dO: [2 value blocks][nq2 rows][128 B], 16 KB at most
-constexpr uint32_t SP_BAR = 180224;
-constexpr uint32_t SP_MISC = SP_BAR + 16;  // TMEM address, then 8 warp sums
-constexpr uint32_t SP_SMEM = SP_MISC + 48 + 1024;
+constexpr int kCpThr = 256;
+constexpr uint32_t CP_S = 0;          // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each
+constexpr uint32_t CP_DS = 65536;     // dS' hi | lo, likewise; after round 1 dVn^T hi | lo [128 value rows][128 B]
+constexpr uint32_t CP_DR = 98304;     //   and then dR^T hi | lo [128 value rows][128 B] (over dS' lo)
+constexpr uint32_t CP_VN = 131072;    // Vn hi | lo: [2 value blocks][64 rows][128 B], 16 KB each
+constexpr uint32_t CP_DO = 163840;    // dO: [2 value blocks][nq2 rows][128 B], 16 KB at most
+constexpr uint32_t CP_P = 180224;     // P^ hi | lo as an MN-major operand: [64 query rows][128 B], 8 KB each
+constexpr uint32_t CP_T = 196608;     // T hi | lo as an MN-major operand: [64 rows][128 B], 8 KB each
+constexpr uint32_t CP_BAR = 212992;   // 3 mbarriers
+constexpr uint32_t CP_MISC = CP_BAR + 32;  // TMEM address, then 8 warp sums
+constexpr uint32_t CP_SMEM = CP_MISC + 48 + 1024;
+// The M = 128 products whose operand has 64 rows (DOV^T from Vn, dR Vn^T from
+// dR^T's second atom) read the next 8 / 16 KB for rows 64..127: Vn's other
+// block, Vn lo, dO, or dR^T lo and Vn hi, all finite; those rows are not used.
+static_assert(CP_DR + 32768 == CP_VN && CP_VN + 32768 == CP_DO && CP_T + 16384 <= CP_BAR, "products map");
+constexpr uint32_t CT_Z = 0, CT_T1 = 64, CT_YW = 128, CT_DOV = 192, CT_DR = 256, CT_DA = 320, CT_T2 = 384;
 
-__global__ void __launch_bounds__(kSpThr, 1) state_products_tc_kernel(StateProductsTcArgs p) {
+__device__ __forceinline__ float sum16p(float x) {  // over the 16 lanes that differ in bits 0..3
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProductsTcArgs p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + SP_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + SP_MISC);
-    float *wsum = reinterpret_cast<float *>(sm + SP_MISC + 16);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + CP_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CP_MISC);
+    float *wsum = reinterpret_cast<float *>(sm + CP_MISC + 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q4 = warp & 3, half = warp >> 2;
+    const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
     const int c = blockIdx.x, bh = blockIdx.y;
     const size_t ci = (size_t)bh * p.NT + c;
-    const int nq2 = p.nq2;  // query rows of the t1 product (a multiple of 16; rows past the chunk are zero)
+    const int nq2 = p.nq2;  // query rows of the dO products (a multiple of 16; rows past the chunk are zero)
     const int t0 = c * p.Ct, ntok = min(p.Ct, p.T - t0);
+    float *Sg = p.Sw + ci * 16384, *dSg = p.dSw + ci * 16384, *Vg = p.Vnw + ci * 8192, *Bg = p.Bw + ci * 16384;
 
     if (tid == 0) {
-        mbar_init(bar, 1u);
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1u);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tslot, 128);
+        tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    // the operands: 8-element groups, hi at +0 and lo at +32 KB (A) / +16 KB (B)
-    const float *Sg = p.Sw + ci * 16384, *dSg = p.dSw + ci * 16384;
+    // S and dS' split (row m, columns 8 g ..: hi at +0, lo at +32 KB), with <dS', S>
     float dot = 0.f;
-    for (int e = tid; e < 128 * 16; e += kSpThr) {  // S and dS': row m, columns 8 g ..
-        const int m = e >> 4, g = e & 15, k0 = 8 * g;
+    for (int e = tid; e < 128 * 16; e += kCpThr) {
+        const int m = e >> 4, k0 = 8 * (e & 15);
         const float4 a0 = *reinterpret_cast<const float4 *>(dSg + m * 128 + k0);
         const float4 a1 = *reinterpret_cast<const float4 *>(dSg + m * 128 + k0 + 4);
         const float4 b0 = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0);
@@ -383,30 +397,58 @@ __global__ void __launch_bounds__(kSpThr, 1) state_products_tc_kernel(StateProdu
         const uint32_t off = (uint32_t)(k0 >> 6) * 16384u + sw128_offset((uint32_t)m, (uint32_t)(k0 & 63));
         uint4 hi, lo;
         split8(x, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + SP_A1 + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + SP_A1 + 32768 + off) = lo;
+        *reinterpret_cast<uint4 *>(sm + CP_DS + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + CP_DS + 32768 + off) = lo;
         split8(y, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + SP_A2 + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + SP_A2 + 32768 + off) = lo;
+        *reinterpret_cast<uint4 *>(sm + CP_S + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + CP_S + 32768 + off) = lo;
     }
-    const float *Vg = p.Vnw + ci * 8192;
-    for (int e = tid; e < 64 * 16; e += kSpThr) {  // Vn: row t, columns 8 g ..
-        const int t = e >> 4, g = e & 15, k0 = 8 * g;
+    // Vn split (row b, columns 8 g ..), with Y_b . Vn_b (the 16 lanes of a row)
+    for (int e = tid; e < 64 * 16; e += kCpThr) {
+        const int t = e >> 4, k0 = 8 * (e & 15);
         const float4 a0 = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0);
         const float4 a1 = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0 + 4);
+        const float4 y0 = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0);
+        const float4 y1 = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0 + 4);
         const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float yv = y0.x * a0.x + y0.y * a0.y + y0.z * a0.z + y0.w * a0.w + y1.x * a1.x + y1.y * a1.y +
+                   y1.z * a1.z + y1.w * a1.w;
+        yv = sum16p(yv);
+        if ((e & 15) == 0) Bg[8256 + t] = yv;
         const uint32_t off = (uint32_t)(k0 >> 6) * 8192u + sw128_offset((uint32_t)t, (uint32_t)(k0 & 63));
         uint4 hi, lo;
         split8(x, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + SP_B1 + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + SP_B1 + 16384 + off) = lo;
+        *reinterpret_cast<uint4 *>(sm + CP_VN + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + CP_VN + 16384 + off) = lo;
     }
     const unsigned short *dO = p.dout + ((size_t)bh * p.T + t0) * 128;
-    for (int e = tid; e < nq2 * 16; e += kSpThr) {  // dO: query row q, columns 8 g .. (exact in bf16)
-        const int q = e >> 4, g = e & 15, k0 = 8 * g;
+    for (int e = tid; e < nq2 * 16; e += kCpThr) {  // dO: query row q, columns 8 g .. (exact in bf16)
+        const int q = e >> 4, k0 = 8 * (e & 15);
         const uint4 v = q < ntok ? *reinterpret_cast<const uint4 *>(dO + (size_t)q * 128 + k0) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sm + SP_B2 + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
+        *reinterpret_cast<uint4 *>(sm + CP_DO + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
                                    sw128_offset((uint32_t)q, (uint32_t)(k0 & 63))) = v;
+    }
+    {  // T (row b) and P^ (query row t < nq2), columns 8 g .., split as MN-major operands
+        const float *Tg = p.Tw + ci * 4096, *Pg = p.Pw + ci * 4096;
+        for (int e = tid; e < 64 * 8; e += kCpThr) {
+            const int r = e >> 3, k0 = 8 * (e & 7);
+            const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)k0);
+            float4 a0 = *reinterpret_cast<const float4 *>(Tg + r * 64 + k0);
+            float4 a1 = *reinterpret_cast<const float4 *>(Tg + r * 64 + k0 + 4);
+            float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4 *>(sm + CP_T + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + CP_T + 8192 + off) = lo;
+            if (r < nq2) {
+                a0 = *reinterpret_cast<const float4 *>(Pg + r * 64 + k0);
+                a1 = *reinterpret_cast<const float4 *>(Pg + r * 64 + k0 + 4);
+                const float y[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                split8(y, hi, lo);
+                *reinterpret_cast<uint4 *>(sm + CP_P + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + CP_P + 8192 + off) = lo;
+            }
+        }
     }
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     if (lane == 0) wsum[warp] = dot;
@@ -417,76 +459,203 @@ __global__ void __launch_bounds__(kSpThr, 1) state_products_tc_kernel(StateProdu
     const uint32_t tmem = *tslot;
     if (tid == 0) {
         float d = 0.f;
-        for (int w = 0; w < kSpThr / 32; ++w) d += wsum[w];
-        p.Bw[ci * 16384 + 8192] = d;
-        // Z^T = dS' Vn^T (columns 0..63), t1^T = S dO^T (columns 64..)
+        for (int w = 0; w < kCpThr / 32; ++w) d += wsum[w];
+        Bg[8192] = d;
+        // Z^T = dS' Vn^T, t1^T = S dO^T
         const uint32_t idZ = idesc_bf16(128, 64, false, false), idT = idesc_bf16(128, nq2, false, false);
 #pragma unroll
         for (int pr = 0; pr < 3; ++pr) {
-            const uint32_t a = sb + SP_A1 + (pr == 2 ? 32768u : 0u), b = sb + SP_B1 + (pr == 1 ? 16384u : 0u);
+            const uint32_t a = sb + CP_DS + (pr == 2 ? 32768u : 0u), b = sb + CP_VN + (pr == 1 ? 16384u : 0u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ss(tmem, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                mma_bf16_ss(tmem + CT_Z, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                             smem_desc(b + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idZ, (pr | ks) != 0);
         }
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
-            const uint32_t a = sb + SP_A2 + (pr == 1 ? 32768u : 0u);
+            const uint32_t a = sb + CP_S + (pr == 1 ? 32768u : 0u);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ss(tmem + 64, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                            smem_desc(sb + SP_B2 + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), idT,
+                mma_bf16_ss(tmem + CT_T1, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                            smem_desc(sb + CP_DO + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), idT,
                             (pr | ks) != 0);
         }
-        mma_commit(bar);
+        // Yw^T = dO^T P^ (dO as an MN-major operand: K = query rows, M = value columns)
+        const uint32_t idY = idesc_bf16(128, 64, true, true);
+        for (int pr = 0; pr < 2; ++pr)
+            for (int ks = 0; ks < nq2 / 16; ++ks)
+                mma_bf16_ss(tmem + CT_YW, smem_desc(sb + CP_DO + ks * 2048, nq2 * 128, 1024),
+                            smem_desc(sb + CP_P + 8192u * pr + ks * 2048, 8192, 1024), idY, (pr | ks) != 0);
+        // DOV^T = Vn dO^T (rows 0..63 of the product)
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t a = sb + CP_VN + 16384u * pr;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tmem + CT_DOV, smem_desc(a + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                            smem_desc(sb + CP_DO + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), idT,
+                            (pr | ks) != 0);
+        }
+        mma_commit(&bar[0]);
     }
-    // every thread: key row m = TMEM lane (warp quarter), half of the columns
-    const bool ok = warp_ok(wyc_wait(bar, 0, 8u, p.timeout_ns));
+    bool ok = warp_ok(wyc_wait(&bar[0], 0, 8u, p.timeout_ns));
+    const int m = 32 * q4 + lane;  // TMEM lane: key row (Z, t1, t2), value row (Yw, dR) or row (DOV, dR Vn^T)
     if (ok) {
         tc_fence_after_sync();
-        const int q4 = warp & 3, half = warp >> 2;
-        const int m = 32 * q4 + lane;
-        const uint32_t lb = (uint32_t)(32 * q4) << 16;
-        float *out = p.dSw + ci * 16384;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {  // Z rows t = 32 half + 16 j ..
             uint32_t r[16];
-            tmem_ld16(tmem + lb + 32 * half + 16 * j, r);
+            tmem_ld16(tmem + lb + CT_Z + 32 * half + 16 * j, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) out[(size_t)(32 * half + 16 * j + i) * 128 + m] = __uint_as_float(r[i]);
+            for (int i = 0; i < 16; ++i) dSg[(size_t)(32 * half + 16 * j + i) * 128 + m] = __uint_as_float(r[i]);
         }
         for (int j = half; j < nq2 / 16; j += 2) {  // t1 rows q = 16 j ..
             uint32_t r[16];
-            tmem_ld16(tmem + lb + 64 + 16 * j, r);
+            tmem_ld16(tmem + lb + CT_T1 + 16 * j, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) out[8192 + (size_t)(16 * j + i) * 128 + m] = __uint_as_float(r[i]);
+            for (int i = 0; i < 16; ++i) dSg[8192 + (size_t)(16 * j + i) * 128 + m] = __uint_as_float(r[i]);
         }
+        {  // dVn^T row dv = m, columns b = 32 half ..: Y^T + Yw^T as a K-major operand (over dS' hi)
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tmem + lb + CT_YW + 32 * half, r0);
+            tmem_ld16(tmem + lb + CT_YW + 32 * half + 16, r1);
+            tmem_wait_ld();
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                x[i] = Bg[(size_t)(32 * half + i) * 128 + m] + __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint4 hi, lo;
+                split8(x + 8 * h, hi, lo);
+                const uint32_t off = sw128_offset((uint32_t)m, (uint32_t)(32 * half + 8 * h));
+                *reinterpret_cast<uint4 *>(sm + CP_DS + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + CP_DS + 16384 + off) = lo;
+            }
+        }
+        if (q4 < 2) {  // DOV^T rows b = m, query columns q = 16 j .. -> DOV[q][b] (Vn slot, float 4096 on)
+            for (int j = half; j < nq2 / 16; j += 2) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lb + CT_DOV + 16 * j, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Vg[4096 + (size_t)(16 * j + i) * 64 + m] = __uint_as_float(r[i]);
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (tid == 0) {  // dR^T = dVn^T T
+        const uint32_t id = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t a = sb + CP_DS + (pr == 2 ? 16384u : 0u), b = sb + CP_T + (pr == 1 ? 8192u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(tmem + CT_DR, smem_desc(a + ks * 32, 16, 1024), smem_desc(b + ks * 2048, 8192, 1024), id,
+                            (pr | ks) != 0);
+        }
+        mma_commit(&bar[1]);
+    }
+    ok = warp_ok(wyc_wait(&bar[1], 0, 8u, p.timeout_ns));
+    if (ok) {  // dR^T row dv = m, columns a = 32 half ..: dR[a][dv] over S's slot, and dR^T's image
+        tc_fence_after_sync();
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tmem + lb + CT_DR + 32 * half, r0);
+        tmem_ld16(tmem + lb + CT_DR + 32 * half + 16, r1);
+        tmem_wait_ld();
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            x[i] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+            Sg[(size_t)(32 * half + i) * 128 + m] = x[i];
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            uint4 hi, lo;
+            split8(x + 8 * h, hi, lo);
+            const uint32_t off = sw128_offset((uint32_t)m, (uint32_t)(32 * half + 8 * h));
+            *reinterpret_cast<uint4 *>(sm + CP_DR + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + CP_DR + 16384 + off) = lo;
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (tid == 0) {
+        // dR Vn^T: dR^T's image as an MN-major operand (K = value rows, M = a; the second atom is not used)
+        const uint32_t idA = idesc_bf16(128, 64, true, false), idT2 = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t a = sb + CP_DR + (pr == 2 ? 16384u : 0u), b = sb + CP_VN + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tmem + CT_DA, smem_desc(a + ks * 2048, 16384, 1024),
+                            smem_desc(b + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idA, (pr | ks) != 0);
+        }
+        // t2^T = S dR^T (dR^T's image as an MN-major operand: K = value rows, N = a)
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t a = sb + CP_S + (pr == 2 ? 32768u : 0u), b = sb + CP_DR + (pr == 1 ? 16384u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ss(tmem + CT_T2, smem_desc(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                            smem_desc(b + ks * 2048, 8192, 1024), idT2, (pr | ks) != 0);
+        }
+        mma_commit(&bar[2]);
+    }
+    ok = warp_ok(wyc_wait(&bar[2], 0, 8u, p.timeout_ns));
+    if (ok) {
+        tc_fence_after_sync();
+        uint32_t r0[16], r1[16];
+        if (q4 < 2) {  // row a = m of dR Vn^T, columns 32 half .. -> Vn slot [a][c]
+            tmem_ld16(tmem + lb + CT_DA + 32 * half, r0);
+            tmem_ld16(tmem + lb + CT_DA + 32 * half + 16, r1);
+            tmem_wait_ld();
+            float4 *dst = reinterpret_cast<float4 *>(Vg + (size_t)m * 64 + 32 * half);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t *r = h < 4 ? r0 : r1;
+                const int i = 4 * (h & 3);
+                dst[h] = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                     __uint_as_float(r[i + 3]));
+            }
+        }
+        // t2^T row dk = m, columns a = 32 half .. -> t2[a][dk] (S slot, float 8192 on)
+        tmem_ld16(tmem + lb + CT_T2 + 32 * half, r0);
+        tmem_ld16(tmem + lb + CT_T2 + 32 * half + 16, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            Sg[8192 + (size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
     }
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 512);
     }
 }
 
 }  // namespace
 
-int launch_state_products_tc(const StateProductsTcArgs &a, cudaStream_t st) {
+int launch_chunk_products_tc(const ChunkProductsTcArgs &a, cudaStream_t st) {
     if (a.BH <= 0 || a.NT <= 0 || a.Ct <= 0 || a.Ct > 64) return GDN_ERR_INVALID_ARG;
-    StateProductsTcArgs p = a;
+    ChunkProductsTcArgs p = a;
     p.nq2 = (a.Ct + 15) / 16 * 16;
     p.timeout_ns = wait_limit_ns();
-    if (cudaFuncSetAttribute(state_products_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SP_SMEM) !=
+    if (cudaFuncSetAttribute(chunk_products_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CP_SMEM) !=
         cudaSuccess)
         return GDN_ERR_CUDA;
-    state_products_tc_kernel<<<dim3((unsigned)a.NT, (unsigned)a.BH), kSpThr, SP_SMEM, st>>>(p);
+    chunk_products_tc_kernel<<<dim3((unsigned)a.NT, (unsigned)a.BH), kCpThr, CP_SMEM, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
-
 
 // ---------------------------------------------------------------------------
 // The chunk-local WY factors on tcgen05 for bf16 at Dk = Dv = 128, for the
