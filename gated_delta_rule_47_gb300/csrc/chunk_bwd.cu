@@ -491,13 +491,26 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     }
     __syncthreads();
 
-    // 7. dk += P~^T Q + (L + L^T) K;  dq = P~ K
+    // 7. dk += P~^T Q + (L + L^T) K;  dq = P~ K  (X1 = P~^T Q + L^T K, X2 = L K and
+    //    P~ K from the products kernel with the tensor-core chains)
     float accDQ[2][TK];
     zero(accDQ);
-    mm<kThr, 2, TK>(accDK, Xa, 1, LC, Qs, LK, 1, kC);
-    mm<kThr, 2, TK>(accDK, Xb, LC, 1, Ks, LK, 1, kC);
-    mm<kThr, 2, TK>(accDK, Xb, 1, LC, Ks, LK, 1, kC);
-    mm<kThr, 2, TK>(accDQ, Xa, LC, 1, Ks, LK, 1, kC);
+    if (p.img) {
+        const float *X1 = p.Bw + ch.ci * DK * DV, *X2 = p.Uw + ch.ci * kC * DV, *DQ = p.Ww + ch.ci * kC * DK;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TK; ++j) {
+                const int m = ty + 32 * i, n = tx + 16 * j;
+                accDK[i][j] += X1[m * DK + n] + X2[m * DK + n];
+                accDQ[i][j] = m < ntok ? DQ[m * DK + n] : 0.f;
+            }
+    } else {
+        mm<kThr, 2, TK>(accDK, Xa, 1, LC, Qs, LK, 1, kC);
+        mm<kThr, 2, TK>(accDK, Xb, LC, 1, Ks, LK, 1, kC);
+        mm<kThr, 2, TK>(accDK, Xb, 1, LC, Ks, LK, 1, kC);
+        mm<kThr, 2, TK>(accDQ, Xa, LC, 1, Ks, LK, 1, kC);
+    }
     __syncthreads();
 
     // 8. through the state entering the chunk (staged in 64-row blocks of Dk in Vns):
@@ -732,9 +745,18 @@ int run(const ChunkBwdArgs &a, cudaStream_t st) {
         sa.Vnw = p.Vnw;
         sa.dSw = p.dSw;
         sa.Bw = p.Bw;
+        sa.Uw = p.Uw;
+        sa.Ww = p.Ww;
         sa.Pw = p.Pw;
         sa.Tw = p.Tw;
+        sa.Gw = p.Gw;
+        sa.q = static_cast<const unsigned short *>(a.q);
+        sa.k = static_cast<const unsigned short *>(a.k);
+        sa.beta = static_cast<const unsigned short *>(a.beta);
         sa.dout = static_cast<const unsigned short *>(a.dout);
+        sa.r = a.r;
+        sa.l2 = p.l2;
+        sa.scale = a.scale;
         sa.BH = BH;
         sa.NT = NT;
         sa.T = a.T;

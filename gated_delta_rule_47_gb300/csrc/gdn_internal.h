@@ -223,23 +223,31 @@ struct WyChainTcArgs {
     unsigned long long timeout_ns;  // bounded-wait limit (set by the launcher)
 };
 int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t stream);
-// The products the backward's gradient kernels need that involve no
-// per-row reduction, on tcgen05 (wy_chain_tc.cu), per (head, chunk) ci after
-// both chains, written over slots that nothing reads afterwards:
+// The products the backward's gradient kernels need, on tcgen05
+// (wy_chain_tc.cu), per (head, chunk) ci after both chains, written over
+// slots that nothing reads afterwards:
 //   dS' slot: Z = Vn dS'^T [64][128] (floats 0..8191), t1 = dO S^T [Ct][128] (8192..)
 //   S slot:   dR = T^T dVn [64][128] (0..8191), t2 = dR S^T [64][128] (8192..)
 //   Vn slot:  dR Vn^T [64][64] (0..4095), DOV = dO Vn^T [64][64] (4096..; rows
 //             past the chunk's queries undefined)
-//   B slot:   <dS', S> at float 8192, each row's Y . Vn at floats 8256..8319
+//   B slot:   X1 = P~^T Q + L^T Kr [64][128] (0..8191), <dS', S> at float 8192,
+//             each row's Y . Vn at floats 8256..8319
+//   U slot:   X2 = L Kw [64][128];  W slot: P~ Kw [Ct][128]
 // with dVn = Y + P^^T dO, Y = Kd dS' (the first half of the B slot, from the
-// reverse chain), P^ and T from the WY kernel.
+// reverse chain), P^ and T from the WY kernel, and the gradient kernel's
+// P~ = the decay-masked scale dO Vn^T and L = -(dR Vn^T) diag(beta) E below
+// the diagonal (earlier tokens for the block-masked variant); Q, Kr and Kw
+// the unit-normalised queries, read keys and write keys when asked.
 struct ChunkProductsTcArgs {
-    float *Sw, *Vnw, *dSw, *Bw;      // [ci][128][128], [ci][64][128], [ci][128][128], [ci][128][128]
-    const float *Pw, *Tw;            // [ci][64][64]
-    const unsigned short *dout;      // [BH][T][128] bf16 bits of dO
-    int BH, NT, T, Ct;               // Ct: query rows (tokens) per chunk
-    int nq2;                         // set by the launcher
-    unsigned long long timeout_ns;   // set by the launcher
+    float *Sw, *Vnw, *dSw, *Bw, *Uw, *Ww;  // [ci][128][128], [ci][64][128], [ci][128][128] x 2, [ci][64][128] x 2
+    const float *Pw, *Tw, *Gw;             // [ci][64][64] x 2, [ci][64]
+    const unsigned short *q, *k, *beta;    // bf16 bits: k and beta per sub-row (GDN / DeltaProduct) or per token
+    const unsigned short *dout;            // [BH][T][128] bf16 bits of dO
+    const float *mask;                     // [r][r] (block-masked)
+    int BH, NT, T, Ct, r, masked, l2;      // Ct: query rows (tokens) per chunk, Ct = 64 / r
+    float scale;
+    int nq2;                               // set by the launcher
+    unsigned long long timeout_ns;         // set by the launcher
 };
 int launch_chunk_products_tc(const ChunkProductsTcArgs &a, cudaStream_t stream);
 

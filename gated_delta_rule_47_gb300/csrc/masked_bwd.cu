@@ -494,8 +494,22 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         for (int j = 0; j < 4; ++j) colg[ty * kC + tx + 16 * j] -= cs[j];
     }
     __syncthreads();
-    // 7. dKw += P~^T Q + L^T Kr, dKr += L Kw (weighted into D); dq = P~ Kw
-    {
+    // 7. dKw += P~^T Q + L^T Kr, dKr += L Kw (weighted into D); dq = P~ Kw  (X1 =
+    //    P~^T Q + L^T Kr, X2 = L Kw and P~ Kw from the products kernel with the
+    //    tensor-core chains)
+    float accDQ[2][TK];
+    zero(accDQ);
+    if (p.img) {
+        const float *X1 = p.Bw + ch.ci * DK * DV, *X2 = p.Uw + ch.ci * kC * DV, *DQ = p.Ww + ch.ci * kC * DK;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < TK; ++j) {
+                const int a = ty + 32 * i, c = tx + 16 * j;
+                accD[i][j] += ww(a, c) * X1[a * DK + c] + wr(a, c) * X2[a * DK + c];
+                accDQ[i][j] = a < ntok ? DQ[a * DK + c] : 0.f;
+            }
+    } else {
         float t1[2][TK];
         zero(t1);
         mm<kThr, 2, TK>(t1, Xa, 1, LC, Qs, LK, 1, kC);
@@ -510,10 +524,8 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < TK; ++j) accD[i][j] += wr(ty + 32 * i, tx + 16 * j) * t1[i][j];
+        mm_f<kThr, 2, TK>(accDQ, Sm{Xa, LC, 1}, KW, kC);
     }
-    float accDQ[2][TK];
-    zero(accDQ);
-    mm_f<kThr, 2, TK>(accDQ, Sm{Xa, LC, 1}, KW, kC);
     __syncthreads();
     // 8. through the state entering the chunk (staged in 64-row blocks of Dk in Vns):
     //    dq += diag(scale e^{gamma}) dO S^T and dKr -= diag(beta e^gamma) dR S^T; the same
@@ -789,8 +801,19 @@ int run(const MaskedBwdArgs &a, cudaStream_t st) {
         sa.NT = NT;
         sa.T = a.T;
         sa.Ct = p.Ct;
+        sa.Uw = p.Uw;
+        sa.Ww = p.Ww;
         sa.Pw = p.Pw;
         sa.Tw = p.Tw;
+        sa.Gw = p.Gw;
+        sa.q = static_cast<const unsigned short *>(a.q);
+        sa.k = static_cast<const unsigned short *>(a.k);
+        sa.beta = static_cast<const unsigned short *>(a.beta);
+        sa.mask = a.mask;
+        sa.r = a.r;
+        sa.masked = 1;
+        sa.l2 = p.l2;
+        sa.scale = a.scale;
         rc = launch_chunk_products_tc(sa, st);
         if (rc != GDN_OK) return rc;
     } else {

@@ -326,32 +326,40 @@ int wy_chain_tc_read_clear_error() {
 // chunk_products_tc_kernel: per (head, chunk), after both chains, with S the
 // state entering the chunk, dS' the gradient leaving it, Vn [64][128], the
 // chunk's nq query rows of dO (bf16), P^ and T [64][64] from the WY kernel
-// and Y = Kd dS' from the reverse chain, three rounds of MMAs (M = 128):
-//   1. Z^T = dS' Vn^T and t1^T = S dO^T, Yw^T = dO^T P^ and DOV^T = Vn dO^T;
+// and Y = Kd dS' from the reverse chain, four rounds of MMAs (M = 128):
+//   1. Z^T = dS' Vn^T and t1^T = S dO^T, Yw^T = dO^T P^ and DOV = dO Vn^T;
 //   2. dR^T = dVn^T T, with dVn^T = Y^T + Yw^T as a K-major operand;
-//   3. dR Vn^T (dR^T's image read as an MN-major operand) and t2^T = S dR^T.
+//   3. dR Vn^T (dR^T's image read as an MN-major operand) and t2^T = S dR^T;
+//   4. X1^T = Q^T P~ + Kr^T L, X2^T = Kw^T L^T and (P~ Kw)^T, with P~ formed
+//      from DOV and L from dR Vn^T (both decay-masked, as the gradient kernels
+//      define them) and the unit-normalised queries and keys.
 // Each fp32 operand is split into bf16 hi | lo tiles (hi.hi + hi.lo + lo.hi,
 // about 2^-16 relative; two terms where the other operand, dO, is exact).
-// The results go over slots that nothing reads afterwards (the layout is
-// listed with ChunkProductsTcArgs); <dS', S> and each row's Y . Vn as well.
+// P~ and L serve as MN-major operands (rows K) and as K-major ones (rows N) in
+// the same bytes.  The results go over slots that nothing reads afterwards
+// (the layout is listed with ChunkProductsTcArgs).
 namespace {
 
 constexpr int kCpThr = 256;
-constexpr uint32_t CP_S = 0;          // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each
-constexpr uint32_t CP_DS = 65536;     // dS' hi | lo, likewise; after round 1 dVn^T hi | lo [128 value rows][128 B]
-constexpr uint32_t CP_DR = 98304;     //   and then dR^T hi | lo [128 value rows][128 B] (over dS' lo)
+constexpr uint32_t CP_S = 0;          // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each;
+                                      //   round 4: Kr hi | lo [2 key blocks][64 rows][128 B] (at 0), Kw (at 32768)
+constexpr uint32_t CP_DS = 65536;     // dS' hi | lo, likewise; after round 1 dVn^T hi | lo [128 value rows][128 B],
+                                      //   after round 2 Q hi | lo [2 key blocks][64 rows][128 B]
+constexpr uint32_t CP_DR = 98304;     // dR^T hi | lo [128 value rows][128 B] (over dS' lo)
 constexpr uint32_t CP_VN = 131072;    // Vn hi | lo: [2 value blocks][64 rows][128 B], 16 KB each
-constexpr uint32_t CP_DO = 163840;    // dO: [2 value blocks][nq2 rows][128 B], 16 KB at most
-constexpr uint32_t CP_P = 180224;     // P^ hi | lo as an MN-major operand: [64 query rows][128 B], 8 KB each
+constexpr uint32_t CP_DO = 163840;    // dO: [2 value blocks][nq2 rows][128 B], 16 KB at most; then P~ hi | lo [64 rows][128 B]
+constexpr uint32_t CP_P = 180224;     // P^ hi | lo as an MN-major operand: [64 query rows][128 B]; then L hi | lo
 constexpr uint32_t CP_T = 196608;     // T hi | lo as an MN-major operand: [64 rows][128 B], 8 KB each
-constexpr uint32_t CP_BAR = 212992;   // 3 mbarriers
-constexpr uint32_t CP_MISC = CP_BAR + 32;  // TMEM address, then 8 warp sums
+constexpr uint32_t CP_BAR = 212992;   // 4 mbarriers
+constexpr uint32_t CP_VEC = CP_BAR + 32;   // gamma, beta (per sub-row), n (per sub-row), m (per query), mask
+constexpr uint32_t CP_MISC = CP_VEC + 5 * 256;  // TMEM address, then 8 warp sums
 constexpr uint32_t CP_SMEM = CP_MISC + 48 + 1024;
-// The M = 128 products whose operand has 64 rows (DOV^T from Vn, dR Vn^T from
-// dR^T's second atom) read the next 8 / 16 KB for rows 64..127: Vn's other
-// block, Vn lo, dO, or dR^T lo and Vn hi, all finite; those rows are not used.
+// The M = 128 products whose operand has fewer than 128 rows read past it for
+// the rest (the next block or region, or stale staging); those rows of the
+// product are not used.
 static_assert(CP_DR + 32768 == CP_VN && CP_VN + 32768 == CP_DO && CP_T + 16384 <= CP_BAR, "products map");
 constexpr uint32_t CT_Z = 0, CT_T1 = 64, CT_YW = 128, CT_DOV = 192, CT_DR = 256, CT_DA = 320, CT_T2 = 384;
+constexpr uint32_t CT_X1 = 0, CT_X2 = 64, CT_DQ = 128;  // round 4, over columns read in round 1's epilogue
 
 __device__ __forceinline__ float sum16p(float x) {  // over the 16 lanes that differ in bits 0..3
 #pragma unroll
@@ -359,91 +367,144 @@ __device__ __forceinline__ float sum16p(float x) {  // over the 16 lanes that di
     return x;
 }
 
+__device__ __forceinline__ void unpack8p(const uint4 &w, float *x) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(u[i] << 16);
+        x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 ldg16p(const unsigned short *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+template <bool MASKED>
 __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProductsTcArgs p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + CP_BAR);
+    float *gam = reinterpret_cast<float *>(sm + CP_VEC), *bet = gam + 64, *nk = bet + 64, *mq = nk + 64, *msk = mq + 64;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CP_MISC);
     float *wsum = reinterpret_cast<float *>(sm + CP_MISC + 16);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q4 = warp & 3, half = warp >> 2;
     const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
-    const int c = blockIdx.x, bh = blockIdx.y;
+    const int c = blockIdx.x, bh = blockIdx.y, r = p.r;
     const size_t ci = (size_t)bh * p.NT + c;
     const int nq2 = p.nq2;  // query rows of the dO products (a multiple of 16; rows past the chunk are zero)
-    const int t0 = c * p.Ct, ntok = min(p.Ct, p.T - t0);
+    const int t0 = c * p.Ct, ntok = min(p.Ct, p.T - t0), nrows = ntok * r;
+    const size_t htok = (size_t)bh * p.T + t0, hrow = htok * r;
     float *Sg = p.Sw + ci * 16384, *dSg = p.dSw + ci * 16384, *Vg = p.Vnw + ci * 8192, *Bg = p.Bw + ci * 16384;
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
 
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1u);
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1u);
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    // S and dS' split (row m, columns 8 g ..: hi at +0, lo at +32 KB), with <dS', S>
+    if (tid < 64) {
+        gam[tid] = p.Gw[ci * 64 + tid];
+        bet[tid] = tid < nrows ? __uint_as_float((uint32_t)p.beta[MASKED ? htok + tid / r : hrow + tid] << 16) : 0.f;
+        if (MASKED && tid < r * r) msk[tid] = p.mask[tid];
+    }
+    // S and dS' split (row m, columns 8 g ..: hi at +0, lo at +32 KB), with <dS', S>;
+    // every pass issues a batch of loads before its shared stores
     float dot = 0.f;
-    for (int e = tid; e < 128 * 16; e += kCpThr) {
-        const int m = e >> 4, k0 = 8 * (e & 15);
-        const float4 a0 = *reinterpret_cast<const float4 *>(dSg + m * 128 + k0);
-        const float4 a1 = *reinterpret_cast<const float4 *>(dSg + m * 128 + k0 + 4);
-        const float4 b0 = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0);
-        const float4 b1 = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0 + 4);
-        const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float y[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll 1
+    for (int e0 = tid; e0 < 128 * 16; e0 += 4 * kCpThr) {
+        float4 v[4][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dot += x[i] * y[i];
-        const uint32_t off = (uint32_t)(k0 >> 6) * 16384u + sw128_offset((uint32_t)m, (uint32_t)(k0 & 63));
-        uint4 hi, lo;
-        split8(x, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + CP_DS + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + CP_DS + 32768 + off) = lo;
-        split8(y, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + CP_S + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + CP_S + 32768 + off) = lo;
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + kCpThr * u, m2 = e >> 4, k0 = 8 * (e & 15);
+            v[u][0] = *reinterpret_cast<const float4 *>(dSg + m2 * 128 + k0);
+            v[u][1] = *reinterpret_cast<const float4 *>(dSg + m2 * 128 + k0 + 4);
+            v[u][2] = *reinterpret_cast<const float4 *>(Sg + m2 * 128 + k0);
+            v[u][3] = *reinterpret_cast<const float4 *>(Sg + m2 * 128 + k0 + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + kCpThr * u, m2 = e >> 4, k0 = 8 * (e & 15);
+            const float x[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+            const float y[8] = {v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w, v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dot += x[i] * y[i];
+            const uint32_t off = (uint32_t)(k0 >> 6) * 16384u + sw128_offset((uint32_t)m2, (uint32_t)(k0 & 63));
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4 *>(sm + CP_DS + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + CP_DS + 32768 + off) = lo;
+            split8(y, hi, lo);
+            *reinterpret_cast<uint4 *>(sm + CP_S + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + CP_S + 32768 + off) = lo;
+        }
     }
-    // Vn split (row b, columns 8 g ..), with Y_b . Vn_b (the 16 lanes of a row)
-    for (int e = tid; e < 64 * 16; e += kCpThr) {
-        const int t = e >> 4, k0 = 8 * (e & 15);
-        const float4 a0 = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0);
-        const float4 a1 = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0 + 4);
-        const float4 y0 = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0);
-        const float4 y1 = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0 + 4);
-        const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float yv = y0.x * a0.x + y0.y * a0.y + y0.z * a0.z + y0.w * a0.w + y1.x * a1.x + y1.y * a1.y +
-                   y1.z * a1.z + y1.w * a1.w;
-        yv = sum16p(yv);
-        if ((e & 15) == 0) Bg[8256 + t] = yv;
-        const uint32_t off = (uint32_t)(k0 >> 6) * 8192u + sw128_offset((uint32_t)t, (uint32_t)(k0 & 63));
-        uint4 hi, lo;
-        split8(x, hi, lo);
-        *reinterpret_cast<uint4 *>(sm + CP_VN + off) = hi;
-        *reinterpret_cast<uint4 *>(sm + CP_VN + 16384 + off) = lo;
+    {  // Vn split (row b, columns 8 g ..), with Y_b . Vn_b (the 16 lanes of a row)
+        float4 v[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kCpThr * u, t = e >> 4, k0 = 8 * (e & 15);
+            v[u][0] = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0);
+            v[u][1] = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0 + 4);
+            v[u][2] = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0);
+            v[u][3] = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0 + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kCpThr * u, t = e >> 4, k0 = 8 * (e & 15);
+            const float4 a0 = v[u][0], a1 = v[u][1], y0 = v[u][2], y1 = v[u][3];
+            const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float yv = y0.x * a0.x + y0.y * a0.y + y0.z * a0.z + y0.w * a0.w + y1.x * a1.x + y1.y * a1.y +
+                       y1.z * a1.z + y1.w * a1.w;
+            yv = sum16p(yv);
+            if ((e & 15) == 0) Bg[8256 + t] = yv;
+            const uint32_t off = (uint32_t)(k0 >> 6) * 8192u + sw128_offset((uint32_t)t, (uint32_t)(k0 & 63));
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4 *>(sm + CP_VN + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + CP_VN + 16384 + off) = lo;
+        }
     }
-    const unsigned short *dO = p.dout + ((size_t)bh * p.T + t0) * 128;
-    for (int e = tid; e < nq2 * 16; e += kCpThr) {  // dO: query row q, columns 8 g .. (exact in bf16)
-        const int q = e >> 4, k0 = 8 * (e & 15);
-        const uint4 v = q < ntok ? *reinterpret_cast<const uint4 *>(dO + (size_t)q * 128 + k0) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sm + CP_DO + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
-                                   sw128_offset((uint32_t)q, (uint32_t)(k0 & 63))) = v;
+    const unsigned short *dO = p.dout + htok * 128;
+    {  // dO: query row q < nq2, columns 8 g .. (exact in bf16)
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kCpThr * u, q = e >> 4, k0 = 8 * (e & 15);
+            w[u] = q < ntok ? *reinterpret_cast<const uint4 *>(dO + (size_t)q * 128 + k0) : z4;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kCpThr * u, q = e >> 4, k0 = 8 * (e & 15);
+            if (q < nq2)
+                *reinterpret_cast<uint4 *>(sm + CP_DO + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
+                                           sw128_offset((uint32_t)q, (uint32_t)(k0 & 63))) = w[u];
+        }
     }
     {  // T (row b) and P^ (query row t < nq2), columns 8 g .., split as MN-major operands
         const float *Tg = p.Tw + ci * 4096, *Pg = p.Pw + ci * 4096;
-        for (int e = tid; e < 64 * 8; e += kCpThr) {
-            const int r = e >> 3, k0 = 8 * (e & 7);
-            const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)k0);
-            float4 a0 = *reinterpret_cast<const float4 *>(Tg + r * 64 + k0);
-            float4 a1 = *reinterpret_cast<const float4 *>(Tg + r * 64 + k0 + 4);
-            float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float4 v[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + kCpThr * u, rr = e >> 3, k0 = 8 * (e & 7);
+            v[u][0] = *reinterpret_cast<const float4 *>(Tg + rr * 64 + k0);
+            v[u][1] = *reinterpret_cast<const float4 *>(Tg + rr * 64 + k0 + 4);
+            v[u][2] = *reinterpret_cast<const float4 *>(Pg + rr * 64 + k0);
+            v[u][3] = *reinterpret_cast<const float4 *>(Pg + rr * 64 + k0 + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + kCpThr * u, rr = e >> 3, k0 = 8 * (e & 7);
+            const uint32_t off = sw128_offset((uint32_t)rr, (uint32_t)k0);
+            const float x[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
             uint4 hi, lo;
             split8(x, hi, lo);
             *reinterpret_cast<uint4 *>(sm + CP_T + off) = hi;
             *reinterpret_cast<uint4 *>(sm + CP_T + 8192 + off) = lo;
-            if (r < nq2) {
-                a0 = *reinterpret_cast<const float4 *>(Pg + r * 64 + k0);
-                a1 = *reinterpret_cast<const float4 *>(Pg + r * 64 + k0 + 4);
-                const float y[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            if (rr < nq2) {
+                const float y[8] = {v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w, v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
                 split8(y, hi, lo);
                 *reinterpret_cast<uint4 *>(sm + CP_P + off) = hi;
                 *reinterpret_cast<uint4 *>(sm + CP_P + 8192 + off) = lo;
@@ -486,36 +547,36 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
             for (int ks = 0; ks < nq2 / 16; ++ks)
                 mma_bf16_ss(tmem + CT_YW, smem_desc(sb + CP_DO + ks * 2048, nq2 * 128, 1024),
                             smem_desc(sb + CP_P + 8192u * pr + ks * 2048, 8192, 1024), idY, (pr | ks) != 0);
-        // DOV^T = Vn dO^T (rows 0..63 of the product)
+        // DOV = dO Vn^T (rows: the query rows of dO)
+        const uint32_t idV = idesc_bf16(128, 64, false, false);
 #pragma unroll
         for (int pr = 0; pr < 2; ++pr) {
-            const uint32_t a = sb + CP_VN + 16384u * pr;
+            const uint32_t b = sb + CP_VN + 16384u * pr;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ss(tmem + CT_DOV, smem_desc(a + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                            smem_desc(sb + CP_DO + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), idT,
-                            (pr | ks) != 0);
+                mma_bf16_ss(tmem + CT_DOV, smem_desc(sb + CP_DO + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024),
+                            smem_desc(b + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idV, (pr | ks) != 0);
         }
         mma_commit(&bar[0]);
     }
     bool ok = warp_ok(wyc_wait(&bar[0], 0, 8u, p.timeout_ns));
-    const int m = 32 * q4 + lane;  // TMEM lane: key row (Z, t1, t2), value row (Yw, dR) or row (DOV, dR Vn^T)
+    const int m = 32 * q4 + lane;  // TMEM lane
     if (ok) {
         tc_fence_after_sync();
 #pragma unroll
         for (int j = 0; j < 2; ++j) {  // Z rows t = 32 half + 16 j ..
-            uint32_t r[16];
-            tmem_ld16(tmem + lb + CT_Z + 32 * half + 16 * j, r);
+            uint32_t rg[16];
+            tmem_ld16(tmem + lb + CT_Z + 32 * half + 16 * j, rg);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dSg[(size_t)(32 * half + 16 * j + i) * 128 + m] = __uint_as_float(r[i]);
+            for (int i = 0; i < 16; ++i) dSg[(size_t)(32 * half + 16 * j + i) * 128 + m] = __uint_as_float(rg[i]);
         }
         for (int j = half; j < nq2 / 16; j += 2) {  // t1 rows q = 16 j ..
-            uint32_t r[16];
-            tmem_ld16(tmem + lb + CT_T1 + 16 * j, r);
+            uint32_t rg[16];
+            tmem_ld16(tmem + lb + CT_T1 + 16 * j, rg);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dSg[8192 + (size_t)(16 * j + i) * 128 + m] = __uint_as_float(r[i]);
+            for (int i = 0; i < 16; ++i) dSg[8192 + (size_t)(16 * j + i) * 128 + m] = __uint_as_float(rg[i]);
         }
         {  // dVn^T row dv = m, columns b = 32 half ..: Y^T + Yw^T as a K-major operand (over dS' hi)
             uint32_t r0[16], r1[16];
@@ -535,13 +596,29 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
                 *reinterpret_cast<uint4 *>(sm + CP_DS + 16384 + off) = lo;
             }
         }
-        if (q4 < 2) {  // DOV^T rows b = m, query columns q = 16 j .. -> DOV[q][b] (Vn slot, float 4096 on)
-            for (int j = half; j < nq2 / 16; j += 2) {
-                uint32_t r[16];
-                tmem_ld16(tmem + lb + CT_DOV + 16 * j, r);
-                tmem_wait_ld();
+        if (q4 < 2) {  // DOV row i = m, columns b = 32 half ..: to the Vn slot (float 4096 on), and P~ (over dO)
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tmem + lb + CT_DOV + 32 * half, r0);
+            tmem_ld16(tmem + lb + CT_DOV + 32 * half + 16, r1);
+            tmem_wait_ld();
+            const int i = m;
+            const bool live = i < ntok;
+            const float gi = live ? gam[i * r] : 0.f;
+            float x[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) Vg[4096 + (size_t)(16 * j + i) * 64 + m] = __uint_as_float(r[i]);
+            for (int j = 0; j < 32; ++j) {
+                const int b = 32 * half + j;
+                const float dv = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+                if (i < nq2) Vg[4096 + (size_t)i * 64 + b] = dv;
+                x[j] = (live && b / r <= i) ? p.scale * expf(gi - gam[b]) * dv : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint4 hi, lo;
+                split8(x + 8 * h, hi, lo);
+                const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)(32 * half + 8 * h));
+                *reinterpret_cast<uint4 *>(sm + CP_DO + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + CP_DO + 8192 + off) = lo;
             }
         }
     }
@@ -560,6 +637,35 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
                             (pr | ks) != 0);
         }
         mma_commit(&bar[1]);
+    }
+    // the keys and queries of round 4 (element e: row e / 16, 8-column group e % 16), loaded while dR forms
+    constexpr int UK = 1024 / kCpThr;
+    uint4 kg[UK], qg4[UK];
+#pragma unroll
+    for (int u = 0; u < UK; ++u) {
+        const int e = tid + kCpThr * u, row = e >> 4, g = e & 15;
+        const size_t ks = MASKED ? htok + row / r : hrow + row;
+        kg[u] = row < nrows ? ldg16p(p.k + ks * 128 + 8 * g) : z4;
+        qg4[u] = row < ntok ? ldg16p(p.q + (htok + row) * 128 + 8 * g) : z4;
+    }
+#pragma unroll
+    for (int u = 0; u < UK; ++u) {  // norms (the 16 lanes of a row)
+        const int e = tid + kCpThr * u, row = e >> 4, g = e & 15;
+        float x[8];
+        unpack8p(kg[u], x);
+        float sk = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sk += x[i] * x[i];
+        unpack8p(qg4[u], x);
+        float sq = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sq += x[i] * x[i];
+        sk = sum16p(sk);
+        sq = sum16p(sq);
+        if (g == 0) {
+            nk[row] = p.l2 ? 1.f / fmaxf(sqrtf(sk), 1e-12f) : 1.f;
+            mq[row] = p.l2 ? 1.f / fmaxf(sqrtf(sq), 1e-12f) : 1.f;
+        }
     }
     ok = warp_ok(wyc_wait(&bar[1], 0, 8u, p.timeout_ns));
     if (ok) {  // dR^T row dv = m, columns a = 32 half ..: dR[a][dv] over S's slot, and dR^T's image
@@ -582,6 +688,21 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
             *reinterpret_cast<uint4 *>(sm + CP_DR + off) = hi;
             *reinterpret_cast<uint4 *>(sm + CP_DR + 16384 + off) = lo;
         }
+    }
+    __syncthreads();  // the norms; dVn^T's image has been read
+#pragma unroll
+    for (int u = 0; u < UK; ++u) {  // Q = diag(m) q (hi | lo) over dVn^T's image
+        const int e = tid + kCpThr * u, row = e >> 4, g = e & 15;
+        float x[8];
+        unpack8p(qg4[u], x);
+        const float f = mq[row];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= f;
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        const uint32_t off = (uint32_t)(g >> 3) * 8192u + sw128_offset((uint32_t)row, (uint32_t)((8 * g) & 63));
+        *reinterpret_cast<uint4 *>(sm + CP_DS + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + CP_DS + 16384 + off) = lo;
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -613,17 +734,27 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     if (ok) {
         tc_fence_after_sync();
         uint32_t r0[16], r1[16];
-        if (q4 < 2) {  // row a = m of dR Vn^T, columns 32 half .. -> Vn slot [a][c]
+        if (q4 < 2) {  // row a = m of dR Vn^T, columns 32 half ..: to the Vn slot [a][c], and L (over P^)
             tmem_ld16(tmem + lb + CT_DA + 32 * half, r0);
             tmem_ld16(tmem + lb + CT_DA + 32 * half + 16, r1);
             tmem_wait_ld();
-            float4 *dst = reinterpret_cast<float4 *>(Vg + (size_t)m * 64 + 32 * half);
+            const int a = m;
+            const float fa = bet[a], ga = gam[a];
+            float x[32];
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const uint32_t *r = h < 4 ? r0 : r1;
-                const int i = 4 * (h & 3);
-                dst[h] = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
-                                     __uint_as_float(r[i + 3]));
+            for (int j = 0; j < 32; ++j) {
+                const int cc = 32 * half + j;
+                const float da = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+                Vg[(size_t)a * 64 + cc] = da;
+                x[j] = (MASKED ? cc / r < a / r : cc < a) ? -da * fa * expf(ga - gam[cc]) : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint4 hi, lo;
+                split8(x + 8 * h, hi, lo);
+                const uint32_t off = sw128_offset((uint32_t)a, (uint32_t)(32 * half + 8 * h));
+                *reinterpret_cast<uint4 *>(sm + CP_P + off) = hi;
+                *reinterpret_cast<uint4 *>(sm + CP_P + 8192 + off) = lo;
             }
         }
         // t2^T row dk = m, columns a = 32 half .. -> t2[a][dk] (S slot, float 8192 on)
@@ -633,6 +764,91 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
 #pragma unroll
         for (int i = 0; i < 32; ++i)
             Sg[8192 + (size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+    }
+    tc_fence_before_sync();
+    __syncthreads();  // S's image has been read
+    // Kr and Kw (hi | lo) of the rows (sub-rows), unit-normalised when asked, over S's image
+#pragma unroll
+    for (int u = 0; u < UK; ++u) {
+        const int e = tid + kCpThr * u, row = e >> 4, g = e & 15;
+        float x[8], y[8];
+        unpack8p(kg[u], x);
+        const float f = nk[row];
+        float fr = f, fw = f;
+        if (MASKED) {
+            const int ib = row % r, j = (g * r) >> 4;
+            fr = f * msk[ib * r + j];
+            fw = j == ib ? f : 0.f;
+        }
+        const uint32_t off = (uint32_t)(g >> 3) * 8192u + sw128_offset((uint32_t)row, (uint32_t)((8 * g) & 63));
+        uint4 hi, lo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = x[i] * fr;
+        split8(y, hi, lo);
+        *reinterpret_cast<uint4 *>(sm + CP_S + off) = hi;
+        *reinterpret_cast<uint4 *>(sm + CP_S + 16384 + off) = lo;
+        if (MASKED) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = x[i] * fw;
+            split8(y, hi, lo);
+            *reinterpret_cast<uint4 *>(sm + CP_S + 32768 + off) = hi;
+            *reinterpret_cast<uint4 *>(sm + CP_S + 49152 + off) = lo;
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (tid == 0) {  // X1^T = Q^T P~ + Kr^T L, X2^T = Kw^T L^T, (P~ Kw)^T
+        const uint32_t kr = sb + CP_S, kw = sb + CP_S + (MASKED ? 32768u : 0u);
+        const uint32_t idMM = idesc_bf16(128, 64, true, true), idMK = idesc_bf16(128, 64, true, false);
+        const uint32_t idQ = idesc_bf16(128, nq2, true, false);
+        int n = 0;
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t pa = pr == 2 ? 16384u : 0u, pb = pr == 1 ? 8192u : 0u;
+            for (int ks = 0; ks < nq2 / 16; ++ks)  // Q^T P~ (K = query rows)
+                mma_bf16_ss(tmem + CT_X1, smem_desc(sb + CP_DS + pa + ks * 2048, 8192, 1024),
+                            smem_desc(sb + CP_DO + pb + ks * 2048, 8192, 1024), idMM, (n++) > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)  // Kr^T L (K = rows)
+                mma_bf16_ss(tmem + CT_X1, smem_desc(kr + pa + ks * 2048, 8192, 1024),
+                            smem_desc(sb + CP_P + pb + ks * 2048, 8192, 1024), idMM, 1u);
+        }
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t pa = pr == 2 ? 16384u : 0u, pb = pr == 1 ? 8192u : 0u;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // Kw^T L^T and Kw^T P~^T (L and P~ as K-major operands)
+                mma_bf16_ss(tmem + CT_X2, smem_desc(kw + pa + ks * 2048, 8192, 1024),
+                            smem_desc(sb + CP_P + pb + ks * 32, 16, 1024), idMK, (pr | ks) != 0);
+                mma_bf16_ss(tmem + CT_DQ, smem_desc(kw + pa + ks * 2048, 8192, 1024),
+                            smem_desc(sb + CP_DO + pb + ks * 32, 16, 1024), idQ, (pr | ks) != 0);
+            }
+        }
+        mma_commit(&bar[3]);
+    }
+    ok = warp_ok(wyc_wait(&bar[3], 0, 8u, p.timeout_ns));
+    if (ok) {  // row dk = m: X1[a][dk] (B slot), X2[a][dk] (U slot), (P~ Kw)[i][dk] (W slot)
+        tc_fence_after_sync();
+        float *X2g = p.Uw + ci * 8192, *DQg = p.Ww + ci * 8192;
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tmem + lb + CT_X1 + 32 * half, r0);
+        tmem_ld16(tmem + lb + CT_X1 + 32 * half + 16, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) Bg[(size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+        tmem_ld16(tmem + lb + CT_X2 + 32 * half, r0);
+        tmem_ld16(tmem + lb + CT_X2 + 32 * half + 16, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) X2g[(size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+        for (int j = half; j < nq2 / 16; j += 2) {
+            tmem_ld16(tmem + lb + CT_DQ + 16 * j, r0);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) DQg[(size_t)(16 * j + i) * 128 + m] = __uint_as_float(r0[i]);
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -645,14 +861,15 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
 }  // namespace
 
 int launch_chunk_products_tc(const ChunkProductsTcArgs &a, cudaStream_t st) {
-    if (a.BH <= 0 || a.NT <= 0 || a.Ct <= 0 || a.Ct > 64) return GDN_ERR_INVALID_ARG;
+    if (a.BH <= 0 || a.NT <= 0 || a.Ct <= 0 || a.Ct > 64 || a.r < 1 || a.Ct * a.r > 64) return GDN_ERR_INVALID_ARG;
+    if (a.masked && (a.r > 8 || 64 % a.r != 0)) return GDN_ERR_INVALID_ARG;
     ChunkProductsTcArgs p = a;
     p.nq2 = (a.Ct + 15) / 16 * 16;
     p.timeout_ns = wait_limit_ns();
-    if (cudaFuncSetAttribute(chunk_products_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CP_SMEM) !=
-        cudaSuccess)
+    void (*kern)(ChunkProductsTcArgs) = a.masked ? chunk_products_tc_kernel<true> : chunk_products_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CP_SMEM) != cudaSuccess)
         return GDN_ERR_CUDA;
-    chunk_products_tc_kernel<<<dim3((unsigned)a.NT, (unsigned)a.BH), kCpThr, CP_SMEM, st>>>(p);
+    kern<<<dim3((unsigned)a.NT, (unsigned)a.BH), kCpThr, CP_SMEM, st>>>(p);
     note_launch();
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
