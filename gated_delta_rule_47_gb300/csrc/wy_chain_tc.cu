@@ -340,7 +340,8 @@ int wy_chain_tc_read_clear_error() {
 // (the layout is listed with ChunkProductsTcArgs).
 namespace {
 
-constexpr int kCpThr = 256;
+constexpr int kCpThr = 512;
+constexpr int kCpCG = kCpThr / 128, kCpCW = 64 / kCpCG;  // epilogue column groups (warp / 4), columns of each
 constexpr uint32_t CP_S = 0;          // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each;
                                       //   round 4: Kr hi | lo [2 key blocks][64 rows][128 B] (at 0), Kw (at 32768)
 constexpr uint32_t CP_DS = 65536;     // dS' hi | lo, likewise; after round 1 dVn^T hi | lo [128 value rows][128 B],
@@ -352,8 +353,8 @@ constexpr uint32_t CP_P = 180224;     // P^ hi | lo as an MN-major operand: [64 
 constexpr uint32_t CP_T = 196608;     // T hi | lo as an MN-major operand: [64 rows][128 B], 8 KB each
 constexpr uint32_t CP_BAR = 212992;   // 4 mbarriers
 constexpr uint32_t CP_VEC = CP_BAR + 32;   // gamma, beta (per sub-row), n (per sub-row), m (per query), mask
-constexpr uint32_t CP_MISC = CP_VEC + 5 * 256;  // TMEM address, then 8 warp sums
-constexpr uint32_t CP_SMEM = CP_MISC + 48 + 1024;
+constexpr uint32_t CP_MISC = CP_VEC + 5 * 256;  // TMEM address, then the warps' sums
+constexpr uint32_t CP_SMEM = CP_MISC + 16 + 4 * (kCpThr / 32) + 1024;
 // The M = 128 products whose operand has fewer than 128 rows read past it for
 // the rest (the next block or region, or stale staging); those rows of the
 // product are not used.
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     float *gam = reinterpret_cast<float *>(sm + CP_VEC), *bet = gam + 64, *nk = bet + 64, *mq = nk + 64, *msk = mq + 64;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + CP_MISC);
     float *wsum = reinterpret_cast<float *>(sm + CP_MISC + 16);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q4 = warp & 3, half = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, q4 = warp & 3, cg = warp >> 2;
     const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
     const int c = blockIdx.x, bh = blockIdx.y, r = p.r;
     const size_t ci = (size_t)bh * p.NT + c;
@@ -442,9 +443,10 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
         }
     }
     {  // Vn split (row b, columns 8 g ..), with Y_b . Vn_b (the 16 lanes of a row)
-        float4 v[4][4];
+        constexpr int U = 1024 / kCpThr;
+        float4 v[U][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int e = tid + kCpThr * u, t = e >> 4, k0 = 8 * (e & 15);
             v[u][0] = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0);
             v[u][1] = *reinterpret_cast<const float4 *>(Vg + t * 128 + k0 + 4);
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
             v[u][3] = *reinterpret_cast<const float4 *>(Bg + t * 128 + k0 + 4);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int e = tid + kCpThr * u, t = e >> 4, k0 = 8 * (e & 15);
             const float4 a0 = v[u][0], a1 = v[u][1], y0 = v[u][2], y1 = v[u][3];
             const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -469,14 +471,15 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     }
     const unsigned short *dO = p.dout + htok * 128;
     {  // dO: query row q < nq2, columns 8 g .. (exact in bf16)
-        uint4 w[4];
+        constexpr int U = 1024 / kCpThr;
+        uint4 w[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int e = tid + kCpThr * u, q = e >> 4, k0 = 8 * (e & 15);
             w[u] = q < ntok ? *reinterpret_cast<const uint4 *>(dO + (size_t)q * 128 + k0) : z4;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int e = tid + kCpThr * u, q = e >> 4, k0 = 8 * (e & 15);
             if (q < nq2)
                 *reinterpret_cast<uint4 *>(sm + CP_DO + (uint32_t)(k0 >> 6) * (uint32_t)(nq2 * 128) +
@@ -485,9 +488,10 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     }
     {  // T (row b) and P^ (query row t < nq2), columns 8 g .., split as MN-major operands
         const float *Tg = p.Tw + ci * 4096, *Pg = p.Pw + ci * 4096;
-        float4 v[2][4];
+        constexpr int U = 512 / kCpThr;
+        float4 v[U][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int e = tid + kCpThr * u, rr = e >> 3, k0 = 8 * (e & 7);
             v[u][0] = *reinterpret_cast<const float4 *>(Tg + rr * 64 + k0);
             v[u][1] = *reinterpret_cast<const float4 *>(Tg + rr * 64 + k0 + 4);
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
             v[u][3] = *reinterpret_cast<const float4 *>(Pg + rr * 64 + k0 + 4);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int e = tid + kCpThr * u, rr = e >> 3, k0 = 8 * (e & 7);
             const uint32_t off = sw128_offset((uint32_t)rr, (uint32_t)k0);
             const float x[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
@@ -564,59 +568,60 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     if (ok) {
         tc_fence_after_sync();
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {  // Z rows t = 32 half + 16 j ..
+        for (int j = 0; j < kCpCW / 16; ++j) {  // Z rows t = CW cg + 16 j ..
             uint32_t rg[16];
-            tmem_ld16(tmem + lb + CT_Z + 32 * half + 16 * j, rg);
+            tmem_ld16(tmem + lb + CT_Z + kCpCW * cg + 16 * j, rg);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dSg[(size_t)(32 * half + 16 * j + i) * 128 + m] = __uint_as_float(rg[i]);
+            for (int i = 0; i < 16; ++i) dSg[(size_t)(kCpCW * cg + 16 * j + i) * 128 + m] = __uint_as_float(rg[i]);
         }
-        for (int j = half; j < nq2 / 16; j += 2) {  // t1 rows q = 16 j ..
+        for (int j = cg; j < nq2 / 16; j += kCpCG) {  // t1 rows q = 16 j ..
             uint32_t rg[16];
             tmem_ld16(tmem + lb + CT_T1 + 16 * j, rg);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) dSg[8192 + (size_t)(16 * j + i) * 128 + m] = __uint_as_float(rg[i]);
         }
-        {  // dVn^T row dv = m, columns b = 32 half ..: Y^T + Yw^T as a K-major operand (over dS' hi)
-            uint32_t r0[16], r1[16];
-            tmem_ld16(tmem + lb + CT_YW + 32 * half, r0);
-            tmem_ld16(tmem + lb + CT_YW + 32 * half + 16, r1);
+        {  // dVn^T row dv = m, columns b = CW cg ..: Y^T + Yw^T as a K-major operand (over dS' hi)
+            uint32_t rg[kCpCW];
+#pragma unroll
+            for (int h = 0; h < kCpCW / 16; ++h)
+                tmem_ld16(tmem + lb + CT_YW + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
             tmem_wait_ld();
-            float x[32];
+            float x[kCpCW];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                x[i] = Bg[(size_t)(32 * half + i) * 128 + m] + __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+            for (int i = 0; i < kCpCW; ++i) x[i] = Bg[(size_t)(kCpCW * cg + i) * 128 + m] + __uint_as_float(rg[i]);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < kCpCW / 8; ++h) {
                 uint4 hi, lo;
                 split8(x + 8 * h, hi, lo);
-                const uint32_t off = sw128_offset((uint32_t)m, (uint32_t)(32 * half + 8 * h));
+                const uint32_t off = sw128_offset((uint32_t)m, (uint32_t)(kCpCW * cg + 8 * h));
                 *reinterpret_cast<uint4 *>(sm + CP_DS + off) = hi;
                 *reinterpret_cast<uint4 *>(sm + CP_DS + 16384 + off) = lo;
             }
         }
-        if (q4 < 2) {  // DOV row i = m, columns b = 32 half ..: to the Vn slot (float 4096 on), and P~ (over dO)
-            uint32_t r0[16], r1[16];
-            tmem_ld16(tmem + lb + CT_DOV + 32 * half, r0);
-            tmem_ld16(tmem + lb + CT_DOV + 32 * half + 16, r1);
+        if (q4 < 2) {  // DOV row i = m, columns b = CW cg ..: to the Vn slot (float 4096 on), and P~ (over dO)
+            uint32_t rg[kCpCW];
+#pragma unroll
+            for (int h = 0; h < kCpCW / 16; ++h)
+                tmem_ld16(tmem + lb + CT_DOV + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
             tmem_wait_ld();
             const int i = m;
             const bool live = i < ntok;
             const float gi = live ? gam[i * r] : 0.f;
-            float x[32];
+            float x[kCpCW];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int b = 32 * half + j;
-                const float dv = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+            for (int j = 0; j < kCpCW; ++j) {
+                const int b = kCpCW * cg + j;
+                const float dv = __uint_as_float(rg[j]);
                 if (i < nq2) Vg[4096 + (size_t)i * 64 + b] = dv;
                 x[j] = (live && b / r <= i) ? p.scale * expf(gi - gam[b]) * dv : 0.f;
             }
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < kCpCW / 8; ++h) {
                 uint4 hi, lo;
                 split8(x + 8 * h, hi, lo);
-                const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)(32 * half + 8 * h));
+                const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)(kCpCW * cg + 8 * h));
                 *reinterpret_cast<uint4 *>(sm + CP_DO + off) = hi;
                 *reinterpret_cast<uint4 *>(sm + CP_DO + 8192 + off) = lo;
             }
@@ -668,23 +673,24 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
         }
     }
     ok = warp_ok(wyc_wait(&bar[1], 0, 8u, p.timeout_ns));
-    if (ok) {  // dR^T row dv = m, columns a = 32 half ..: dR[a][dv] over S's slot, and dR^T's image
+    if (ok) {  // dR^T row dv = m, columns a = CW cg ..: dR[a][dv] over S's slot, and dR^T's image
         tc_fence_after_sync();
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tmem + lb + CT_DR + 32 * half, r0);
-        tmem_ld16(tmem + lb + CT_DR + 32 * half + 16, r1);
-        tmem_wait_ld();
-        float x[32];
+        uint32_t rg[kCpCW];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            x[i] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
-            Sg[(size_t)(32 * half + i) * 128 + m] = x[i];
+        for (int h = 0; h < kCpCW / 16; ++h)
+            tmem_ld16(tmem + lb + CT_DR + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
+        tmem_wait_ld();
+        float x[kCpCW];
+#pragma unroll
+        for (int i = 0; i < kCpCW; ++i) {
+            x[i] = __uint_as_float(rg[i]);
+            Sg[(size_t)(kCpCW * cg + i) * 128 + m] = x[i];
         }
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < kCpCW / 8; ++h) {
             uint4 hi, lo;
             split8(x + 8 * h, hi, lo);
-            const uint32_t off = sw128_offset((uint32_t)m, (uint32_t)(32 * half + 8 * h));
+            const uint32_t off = sw128_offset((uint32_t)m, (uint32_t)(kCpCW * cg + 8 * h));
             *reinterpret_cast<uint4 *>(sm + CP_DR + off) = hi;
             *reinterpret_cast<uint4 *>(sm + CP_DR + 16384 + off) = lo;
         }
@@ -733,37 +739,38 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     ok = warp_ok(wyc_wait(&bar[2], 0, 8u, p.timeout_ns));
     if (ok) {
         tc_fence_after_sync();
-        uint32_t r0[16], r1[16];
-        if (q4 < 2) {  // row a = m of dR Vn^T, columns 32 half ..: to the Vn slot [a][c], and L (over P^)
-            tmem_ld16(tmem + lb + CT_DA + 32 * half, r0);
-            tmem_ld16(tmem + lb + CT_DA + 32 * half + 16, r1);
+        uint32_t rg[kCpCW];
+        if (q4 < 2) {  // row a = m of dR Vn^T, columns CW cg ..: to the Vn slot [a][c], and L (over P^)
+#pragma unroll
+            for (int h = 0; h < kCpCW / 16; ++h)
+                tmem_ld16(tmem + lb + CT_DA + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
             tmem_wait_ld();
             const int a = m;
             const float fa = bet[a], ga = gam[a];
-            float x[32];
+            float x[kCpCW];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int cc = 32 * half + j;
-                const float da = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+            for (int j = 0; j < kCpCW; ++j) {
+                const int cc = kCpCW * cg + j;
+                const float da = __uint_as_float(rg[j]);
                 Vg[(size_t)a * 64 + cc] = da;
                 x[j] = (MASKED ? cc / r < a / r : cc < a) ? -da * fa * expf(ga - gam[cc]) : 0.f;
             }
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < kCpCW / 8; ++h) {
                 uint4 hi, lo;
                 split8(x + 8 * h, hi, lo);
-                const uint32_t off = sw128_offset((uint32_t)a, (uint32_t)(32 * half + 8 * h));
+                const uint32_t off = sw128_offset((uint32_t)a, (uint32_t)(kCpCW * cg + 8 * h));
                 *reinterpret_cast<uint4 *>(sm + CP_P + off) = hi;
                 *reinterpret_cast<uint4 *>(sm + CP_P + 8192 + off) = lo;
             }
         }
-        // t2^T row dk = m, columns a = 32 half .. -> t2[a][dk] (S slot, float 8192 on)
-        tmem_ld16(tmem + lb + CT_T2 + 32 * half, r0);
-        tmem_ld16(tmem + lb + CT_T2 + 32 * half + 16, r1);
+        // t2^T row dk = m, columns a = CW cg .. -> t2[a][dk] (S slot, float 8192 on)
+#pragma unroll
+        for (int h = 0; h < kCpCW / 16; ++h)
+            tmem_ld16(tmem + lb + CT_T2 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            Sg[8192 + (size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
+        for (int i = 0; i < kCpCW; ++i) Sg[8192 + (size_t)(kCpCW * cg + i) * 128 + m] = __uint_as_float(rg[i]);
     }
     tc_fence_before_sync();
     __syncthreads();  // S's image has been read
@@ -832,22 +839,25 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     if (ok) {  // row dk = m: X1[a][dk] (B slot), X2[a][dk] (U slot), (P~ Kw)[i][dk] (W slot)
         tc_fence_after_sync();
         float *X2g = p.Uw + ci * 8192, *DQg = p.Ww + ci * 8192;
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tmem + lb + CT_X1 + 32 * half, r0);
-        tmem_ld16(tmem + lb + CT_X1 + 32 * half + 16, r1);
+        uint32_t rg[kCpCW];
+#pragma unroll
+        for (int h = 0; h < kCpCW / 16; ++h)
+            tmem_ld16(tmem + lb + CT_X1 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) Bg[(size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
-        tmem_ld16(tmem + lb + CT_X2 + 32 * half, r0);
-        tmem_ld16(tmem + lb + CT_X2 + 32 * half + 16, r1);
+        for (int i = 0; i < kCpCW; ++i) Bg[(size_t)(kCpCW * cg + i) * 128 + m] = __uint_as_float(rg[i]);
+#pragma unroll
+        for (int h = 0; h < kCpCW / 16; ++h)
+            tmem_ld16(tmem + lb + CT_X2 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) X2g[(size_t)(32 * half + i) * 128 + m] = __uint_as_float(i < 16 ? r0[i] : r1[i - 16]);
-        for (int j = half; j < nq2 / 16; j += 2) {
-            tmem_ld16(tmem + lb + CT_DQ + 16 * j, r0);
+        for (int i = 0; i < kCpCW; ++i) X2g[(size_t)(kCpCW * cg + i) * 128 + m] = __uint_as_float(rg[i]);
+        for (int j = cg; j < nq2 / 16; j += kCpCG) {
+            uint32_t r16[16];
+            tmem_ld16(tmem + lb + CT_DQ + 16 * j, r16);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) DQg[(size_t)(16 * j + i) * 128 + m] = __uint_as_float(r0[i]);
+            for (int i = 0; i < 16; ++i) DQg[(size_t)(16 * j + i) * 128 + m] = __uint_as_float(r16[i]);
         }
     }
     tc_fence_before_sync();
