@@ -28,7 +28,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 # the backward passes on bf16 at D = 128: what runs where
-BWD_PATH = "WY factors, state chains and state products on tcgen05; input gradients on the CUDA cores (fp32)"
+BWD_PATH = ("WY factors, state chains and every product of the gradient step on tcgen05; "
+            "elementwise gradient terms and row sums on the CUDA cores (fp32)")
 
 WORKLOAD = "gdn_b4h16t4096d128_bf16"
 METRIC = "GDN fwd tokens/s (B4,H16,T4096,D128 bf16) + % of binding roofline"
