@@ -300,13 +300,11 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     float accKdS[2][TV], accDK[2][TK];
     zero(accKdS);
     zero(accDK);
-    if (p.img) {
+    if (p.img) {  // dk's share formed by the products kernel (every term but the unit-norm adjoint)
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float s = expf(gl - gam[ty + 32 * i]);
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int j = 0; j < TK; ++j) accDK[i][j] += s * dSg[(ty + 32 * i) * DK + tx + 16 * j];
-        }
+            for (int j = 0; j < TK; ++j) accDK[i][j] = p.Bw[ch.ci * DK * DV + (ty + 32 * i) * DK + tx + 16 * j];
         if (tid < kThr / 32) red[tid] = tid == 0 ? p.Bw[ch.ci * DK * DV + 8192] : 0.f;
     } else {
         for (int h = 0; h < NH; ++h) {
@@ -495,14 +493,13 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
     //    P~ K from the products kernel with the tensor-core chains)
     float accDQ[2][TK];
     zero(accDQ);
-    if (p.img) {
-        const float *X1 = p.Bw + ch.ci * DK * DV, *X2 = p.Uw + ch.ci * kC * DV, *DQ = p.Ww + ch.ci * kC * DK;
+    if (p.img) {  // P~ K from the products kernel (the dk terms are in its share already)
+        const float *DQ = p.Ww + ch.ci * kC * DK;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < TK; ++j) {
                 const int m = ty + 32 * i, n = tx + 16 * j;
-                accDK[i][j] += X1[m * DK + n] + X2[m * DK + n];
                 accDQ[i][j] = m < ntok ? DQ[m * DK + n] : 0.f;
             }
     } else {
@@ -524,14 +521,13 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        if (p.img) {  // t1 = dO S^T and t2 = dR S^T from the products kernel
+        if (p.img) {  // t1 = dO S^T from the products kernel (t2's terms are folded in there)
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int m = ty + 32 * i, c = 64 * h + tx + 16 * j;
                     t1[i][j] = m < ntok ? dSg[8192 + m * DK + c] : 0.f;
-                    t2[i][j] = Sg[8192 + m * DK + c];
                 }
         } else {
             mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LV, DV);
@@ -563,7 +559,8 @@ __global__ void __launch_bounds__(kThr, 1) bwd_grad_kernel(BwdParams p) {
             rv += Hs[b * LV + n] * (b < nrows ? ld_f(vp + (size_t)b * DV + n) : 0.f);
         }
         rv = row_sum16(rv);
-        const float sq = row_sum16(rq[i]), skd = row_sum16(rk[i]);
+        const float sq = row_sum16(rq[i]), skr = row_sum16(rk[i]);
+        const float skd = p.img ? p.Bw[ch.ci * DK * DV + 8320 + b] : skr;  // k_b . t2_b
         if (tx == 0) {
             dbet[b] += rv - eg[b] * skd;
             rowg[b] -= bet[b] * eg[b] * skd;

@@ -226,14 +226,17 @@ int launch_wy_chain_tc(const WyChainTcArgs &a, cudaStream_t stream);
 // The products the backward's gradient kernels need, on tcgen05
 // (wy_chain_tc.cu), per (head, chunk) ci after both chains, written over
 // slots that nothing reads afterwards:
-//   dS' slot: Z = Vn dS'^T [64][128] (floats 0..8191), t1 = dO S^T [Ct][128] (8192..)
-//   S slot:   dR = T^T dVn [64][128] (0..8191), t2 = dR S^T [64][128] (8192..)
+//   dS' slot: t1 = dO S^T [Ct][128] (floats 8192..)
+//   S slot:   dR = T^T dVn [64][128] (0..8191)
 //   Vn slot:  dR Vn^T [64][64] (0..4095), DOV = dO Vn^T [64][64] (4096..; rows
 //             past the chunk's queries undefined)
-//   B slot:   X1 = P~^T Q + L^T Kr [64][128] (0..8191), <dS', S> at float 8192,
-//             each row's Y . Vn at floats 8256..8319
-//   U slot:   X2 = L Kw [64][128];  W slot: P~ Kw [Ct][128]
-// with dVn = Y + P^^T dO, Y = Kd dS' (the first half of the B slot, from the
+//   B slot:   the rows' dk share [64][128] (0..8191, below), <dS', S> at float
+//             8192, each row's Y . Vn at 8256..8319 and kr . t2 at 8320..8383
+//   W slot:   P~ Kw [Ct][128]
+// with dk's share = ww (e^{gl-gamma} Z + X1) + wr (X2 - diag(beta e^gamma) t2),
+// Z = Vn dS'^T, t2 = dR S^T, X1 = P~^T Q + L^T Kr, X2 = L Kw (ww = wr = 1 but
+// for the block-masked variant's slice weights),
+// dVn = Y + P^^T dO, Y = Kd dS' (the first half of the B slot, from the
 // reverse chain), P^ and T from the WY kernel, and the gradient kernel's
 // P~ = the decay-masked scale dO Vn^T and L = -(dR Vn^T) diag(beta) E below
 // the diagonal (earlier tokens for the block-masked variant); Q, Kr and Kw

@@ -316,17 +316,11 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     float accKdS[2][TV], accD[2][TK];
     zero(accKdS);
     zero(accD);
-    if (p.img) {  // from the products kernel (layout with ChunkProductsTcArgs): Z, <dS', S>
+    if (p.img) {  // from the products kernel (layout with ChunkProductsTcArgs): the rows' dk shares, <dS', S>
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int a = ty + 32 * i;
-            const float s = expf(gl - gam[a]);
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int j = 0; j < TK; ++j) {
-                const int c = tx + 16 * j;
-                accD[i][j] += ww(a, c) * s * dSg[a * DK + c];
-            }
-        }
+            for (int j = 0; j < TK; ++j) accD[i][j] = p.Bw[ch.ci * DK * DV + (ty + 32 * i) * DK + tx + 16 * j];
         if (tid < kThr / 32) red[tid] = tid == 0 ? p.Bw[ch.ci * DK * DV + 8192] : 0.f;
     } else {
         for (int h = 0; h < NH; ++h) {
@@ -499,14 +493,13 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
     //    tensor-core chains)
     float accDQ[2][TK];
     zero(accDQ);
-    if (p.img) {
-        const float *X1 = p.Bw + ch.ci * DK * DV, *X2 = p.Uw + ch.ci * kC * DV, *DQ = p.Ww + ch.ci * kC * DK;
+    if (p.img) {  // P~ Kw from the products kernel (the dk terms are in its shares already)
+        const float *DQ = p.Ww + ch.ci * kC * DK;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < TK; ++j) {
                 const int a = ty + 32 * i, c = tx + 16 * j;
-                accD[i][j] += ww(a, c) * X1[a * DK + c] + wr(a, c) * X2[a * DK + c];
                 accDQ[i][j] = a < ntok ? DQ[a * DK + c] : 0.f;
             }
     } else {
@@ -537,14 +530,13 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
         float t1[2][4], t2[2][4];
         zero(t1);
         zero(t2);
-        if (p.img) {  // t1 = dO S^T and t2 = dR S^T from the products kernel
+        if (p.img) {  // t1 = dO S^T from the products kernel (t2's terms are folded in there)
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int m = ty + 32 * i, c = 64 * h + tx + 16 * j;
                     t1[i][j] = m < ntok ? dSg[8192 + m * DK + c] : 0.f;
-                    t2[i][j] = Sg[8192 + m * DK + c];
                 }
         } else {
             mm_nt<kThr, 2, 4>(t1, dOs, LV, Vns, LX, DV);
@@ -576,7 +568,8 @@ __global__ void __launch_bounds__(kThr, 1) mbwd_grad_kernel(MbParams p) {
             rv += Hs[b * LV + n] * (b < nrows ? ld_f(vp + (size_t)(b >> lr) * DV + n) : 0.f);
         }
         rv = row_sum16(rv);
-        const float sq = row_sum16(rq[i]), skd = row_sum16(rk[i]);
+        const float sq = row_sum16(rq[i]), skr = row_sum16(rk[i]);
+        const float skd = p.img ? p.Bw[ch.ci * DK * DV + 8320 + b] : skr;  // kr_b . t2_b
         if (tx == 0) {
             dbet[b] += rv - eg[b] * skd;
             rowg[b] -= bet[b] * eg[b] * skd;

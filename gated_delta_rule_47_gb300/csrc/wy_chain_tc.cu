@@ -360,7 +360,7 @@ constexpr uint32_t CP_SMEM = CP_MISC + 16 + 4 * (kCpThr / 32) + 1024;
 // product are not used.
 static_assert(CP_DR + 32768 == CP_VN && CP_VN + 32768 == CP_DO && CP_T + 16384 <= CP_BAR, "products map");
 constexpr uint32_t CT_Z = 0, CT_T1 = 64, CT_YW = 128, CT_DOV = 192, CT_DR = 256, CT_DA = 320, CT_T2 = 384;
-constexpr uint32_t CT_X1 = 0, CT_X2 = 64, CT_DQ = 128;  // round 4, over columns read in round 1's epilogue
+constexpr uint32_t CT_X1 = 64, CT_X2 = 128, CT_DQ = 192;  // round 4, over columns read in round 1's epilogue
 
 __device__ __forceinline__ float sum16p(float x) {  // over the 16 lanes that differ in bits 0..3
 #pragma unroll
@@ -567,14 +567,6 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     const int m = 32 * q4 + lane;  // TMEM lane
     if (ok) {
         tc_fence_after_sync();
-#pragma unroll
-        for (int j = 0; j < kCpCW / 16; ++j) {  // Z rows t = CW cg + 16 j ..
-            uint32_t rg[16];
-            tmem_ld16(tmem + lb + CT_Z + kCpCW * cg + 16 * j, rg);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) dSg[(size_t)(kCpCW * cg + 16 * j + i) * 128 + m] = __uint_as_float(rg[i]);
-        }
         for (int j = cg; j < nq2 / 16; j += kCpCG) {  // t1 rows q = 16 j ..
             uint32_t rg[16];
             tmem_ld16(tmem + lb + CT_T1 + 16 * j, rg);
@@ -764,13 +756,6 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
                 *reinterpret_cast<uint4 *>(sm + CP_P + 8192 + off) = lo;
             }
         }
-        // t2^T row dk = m, columns a = CW cg .. -> t2[a][dk] (S slot, float 8192 on)
-#pragma unroll
-        for (int h = 0; h < kCpCW / 16; ++h)
-            tmem_ld16(tmem + lb + CT_T2 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < kCpCW; ++i) Sg[8192 + (size_t)(kCpCW * cg + i) * 128 + m] = __uint_as_float(rg[i]);
     }
     tc_fence_before_sync();
     __syncthreads();  // S's image has been read
@@ -836,22 +821,45 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
         mma_commit(&bar[3]);
     }
     ok = warp_ok(wyc_wait(&bar[3], 0, 8u, p.timeout_ns));
-    if (ok) {  // row dk = m: X1[a][dk] (B slot), X2[a][dk] (U slot), (P~ Kw)[i][dk] (W slot)
+    float *red = reinterpret_cast<float *>(sm + CP_T);  // [4 lane quarters][64 rows] (T's image is dead)
+    if (ok) {  // row dk = m, columns a = CW cg ..: dk's share and the rows' kr . t2; (P~ Kw)[i][dk] (W slot)
         tc_fence_after_sync();
-        float *X2g = p.Uw + ci * 8192, *DQg = p.Ww + ci * 8192;
-        uint32_t rg[kCpCW];
+        float *DQg = p.Ww + ci * 8192;
+        uint32_t z[kCpCW], x1[kCpCW], x2[kCpCW], t2[kCpCW];
 #pragma unroll
-        for (int h = 0; h < kCpCW / 16; ++h)
-            tmem_ld16(tmem + lb + CT_X1 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
+        for (int h = 0; h < kCpCW / 16; ++h) {
+            tmem_ld16(tmem + lb + CT_Z + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(z + 16 * h));
+            tmem_ld16(tmem + lb + CT_X1 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(x1 + 16 * h));
+            tmem_ld16(tmem + lb + CT_X2 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(x2 + 16 * h));
+            tmem_ld16(tmem + lb + CT_T2 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(t2 + 16 * h));
+        }
         tmem_wait_ld();
+        // dk[a][m] = ww (e^{gl - gamma_a} Z + X1) + wr (X2 - beta_a e^{gamma_a} t2), with the
+        // block-masked variant's weights ww (m in slice a % r) and wr = mask[a % r][slice of m]
+        const float gl = gam[63];
+        const int jm = MASKED ? m / (128 / r) : 0;
+        const uint32_t kro = (uint32_t)(m >> 6) * 8192u;
 #pragma unroll
-        for (int i = 0; i < kCpCW; ++i) Bg[(size_t)(kCpCW * cg + i) * 128 + m] = __uint_as_float(rg[i]);
+        for (int i = 0; i < kCpCW; ++i) {
+            const int a = kCpCW * cg + i;
+            float ww = 1.f, wr = 1.f;
+            if (MASKED) {
+                ww = jm == a % r ? 1.f : 0.f;
+                wr = msk[(a % r) * r + jm];
+            }
+            const float t2v = __uint_as_float(t2[i]);
+            Bg[(size_t)a * 128 + m] =
+                ww * (expf(gl - gam[a]) * __uint_as_float(z[i]) + __uint_as_float(x1[i])) +
+                wr * (__uint_as_float(x2[i]) - bet[a] * expf(gam[a]) * t2v);
+            // kr[a][m] from its split image (hi + lo), times t2, summed over the warp's 32 key columns
+            const uint32_t off = kro + sw128_offset((uint32_t)a, (uint32_t)(m & 63));
+            const float kr = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(sm + CP_S + off)) << 16) +
+                             __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(sm + CP_S + 16384 + off)) << 16);
+            float v = kr * t2v;
 #pragma unroll
-        for (int h = 0; h < kCpCW / 16; ++h)
-            tmem_ld16(tmem + lb + CT_X2 + kCpCW * cg + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(rg + 16 * h));
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < kCpCW; ++i) X2g[(size_t)(kCpCW * cg + i) * 128 + m] = __uint_as_float(rg[i]);
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[q4 * 64 + a] = v;
+        }
         for (int j = cg; j < nq2 / 16; j += kCpCG) {
             uint32_t r16[16];
             tmem_ld16(tmem + lb + CT_DQ + 16 * j, r16);
@@ -862,6 +870,7 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (tid < 64) Bg[8320 + tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];  // kr_a . t2_a
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);

@@ -149,3 +149,21 @@ def test_tensor_core_path_is_deterministic():
     torch.cuda.synchronize()
     for x, y in zip(*outs):
         assert torch.equal(x, y)
+
+
+def test_tensor_core_path_strong_decay():
+    """Log-decays near -2 per token on the block-masked backward (bf16, D 128,
+    r = 2): every decay factor of the tensor-core kernels is formed per element."""
+    inp, do, dsf = case(120, 128, 2, "bf16", False, seed=71)
+    inp["g"] = (torch.nn.functional.logsigmoid(torch.randn(1, 2, 120, generator=torch.Generator().manual_seed(72))
+                                               - 2.0)).float()
+    d = to_dev(inp)
+    got = binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"], do.cuda(),
+                                                d["initial_state"], dsf.cuda(), need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.masked_deltaproduct_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["mask"], do,
+                                         inp["initial_state"], dsf)
+    for name, x, y in zip(NAMES, got, ref):
+        assert torch.isfinite(x).all(), name
+        assert rel_err(x, y) <= TOL_BF16, name
