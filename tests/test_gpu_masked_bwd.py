@@ -167,3 +167,20 @@ def test_tensor_core_path_strong_decay():
     for name, x, y in zip(NAMES, got, ref):
         assert torch.isfinite(x).all(), name
         assert rel_err(x, y) <= TOL_BF16, name
+
+
+@pytest.mark.parametrize("r,T", [(1, 70), (2, 1), (2, 33), (8, 9)])
+def test_tensor_core_path_small_and_ragged(r, T):
+    """The tensor-core backward (bf16, D 128) at r = 1 (one sub-row per token),
+    with a single token, one chunk plus a token, and r = 8 (eight tokens per
+    chunk, so the query rows round up to 16 inside the products)."""
+    inp, do, dsf = case(T, 128, r, "bf16", False, seed=200 + 10 * r + T)
+    d = to_dev(inp)
+    got = binding.masked_deltaproduct_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["mask"], do.cuda(),
+                                                d["initial_state"], dsf.cuda(), scale=0.9, need_dinitial=True)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ref = oracle.masked_deltaproduct_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["mask"], do,
+                                         inp["initial_state"], dsf, scale=0.9)
+    for name, x, y in zip(NAMES, got, ref):
+        assert rel_err(x, y) <= TOL_BF16, name

@@ -152,3 +152,15 @@ def test_tensor_core_path_is_deterministic():
     o1, s1 = run(inp)
     o2, s2 = run(inp)
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("r,T", [(1, 1), (4, 17), (8, 8), (8, 9)])
+def test_tensor_core_kernels_small_and_ragged(r, T):
+    """The tensor-core forward kernels (bf16, D 128) on a single token, a
+    ragged first chunk and one chunk exactly, at r = 1, 4 and 8."""
+    inp = gdn_inputs(1, 2, T, 128, 128, seed=300 + 10 * r + T, dtype="bf16", initial_state=True)
+    inp["mask"] = slice_mask(r, seed=r)
+    o, sf = run(inp, scale=0.8)
+    ro, rs = ref(inp, scale=0.8)
+    assert rel_err(o, ro) <= TOL_BF16
+    assert rel_err(sf, rs) <= TOL_BF16
