@@ -925,10 +925,11 @@ int launch_chunk_products_tc(const ChunkProductsTcArgs &a, cudaStream_t st) {
 //      state gradient B = Q^T diag(scale e^{gamma_{t r}} m) dO - W^T P^T dO, as
 //      B^T = dO^T Q' (two split products: dO is exact) - Y^T W (three), with
 //      Y^T = dO^T P formed while T is inverted.
-// masked_out_tc_kernel, one CTA of 256 threads per chunk, with S the state
-// entering it:  o_t = scale e^{gamma_{t r}} m_t q_t S + (P Vn)_t, as
-// o^T = S^T Q^T (two split products: q is exact) + Vn^T P^T (three), M = 128
-// value rows, N = the chunk's query rows rounded up to 16.
+// masked_out_tc_kernel, one CTA of 256 threads per chunk (three per SM), with
+// S the state entering it:  o_t = scale e^{gamma_{t r}} m_t q_t S + (P Vn)_t,
+// as o^T = S^T Q^T + Vn^T P^T with bf16 operands (S, Vn and P rounded once, as
+// in the fused forward; q exact), M = 128 value rows, N = the chunk's query
+// rows rounded up to 16.
 namespace {
 
 // Shared memory of wy_tc_kernel, reused by the phases (byte offsets):
@@ -1391,16 +1392,23 @@ __global__ void __launch_bounds__(BWD ? 512 : 256, BWD ? 1 : 2) wy_tc_kernel(WyT
     }
 }
 
-constexpr int kMoThr = 256;
-constexpr uint32_t MO_S = 0;         // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each
-constexpr uint32_t MO_VN = 65536;    // Vn hi | lo: [2 value blocks][64 sub-rows][128 B], 16 KB each
-constexpr uint32_t MO_Q = 98304;     // Q: [2 key blocks][nq2 query rows][128 B] (exact), 16 KB at most
-constexpr uint32_t MO_P = 114688;    // P hi | lo: [nq2 query rows][128 B], 8 KB each
-constexpr uint32_t MO_VEC = 131072;  // gamma (64), query norms, then output row scales (64)
+constexpr int kMoThr = 256;  // three CTAs per SM
+constexpr uint32_t MO_S = 0;         // S: [2 value blocks][128 key rows][128 B] (bf16), 32 KB
+constexpr uint32_t MO_VN = 32768;    // Vn: [2 value blocks][64 sub-rows][128 B] (bf16), 16 KB
+constexpr uint32_t MO_Q = 49152;     // Q: [2 key blocks][nq2 query rows][128 B] (exact), 16 KB at most
+constexpr uint32_t MO_P = 65536;     // P: [nq2 query rows][128 B] (bf16), 8 KB at most
+constexpr uint32_t MO_VEC = 73728;   // gamma (64), query norms, then output row scales (64)
 constexpr uint32_t MO_BAR = MO_VEC + 512;
 constexpr uint32_t MO_SMEM = MO_BAR + 16 + 1024;
+static_assert(3 * (MO_SMEM + 1024) <= 233472, "three output CTAs fit the shared memory of one SM");
 
-__global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(WyTcArgs p) {
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+
+// The output products take their operands in bf16 as the fused forward does
+// (S, Vn and P rounded once; q exact), with fp32 accumulation.
+__global__ void __launch_bounds__(kMoThr, 3) masked_out_tc_kernel(WyTcArgs p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
@@ -1421,25 +1429,25 @@ __global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(WyTcArgs p) {
         tmem_relinquish();
     }
     if (tid < 64) gam[tid] = p.Gw[ci * 64 + tid];
-    {  // S: key row m, value columns 8 g .. (element e: m = e / 16, g = e % 16)
+    {  // S: key row m, value columns 8 g .. (element e: m = e / 16, g = e % 16), two batches of loads
         const float *Sg = p.Sw + ci * 16384;
-        float4 v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + kMoThr * u, m = e >> 4, k0 = 8 * (e & 15);
-            v[2 * u] = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0);
-            v[2 * u + 1] = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0 + 4);
-        }
+        for (int half = 0; half < 2; ++half) {
+            float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + kMoThr * u, m = e >> 4, k0 = 8 * (e & 15);
-            const float x[8] = {v[2 * u].x,     v[2 * u].y,     v[2 * u].z,     v[2 * u].w,
-                                v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
-            uint4 hi, lo;
-            split8(x, hi, lo);
-            const uint32_t off = (uint32_t)(k0 >> 6) * 16384u + sw128_offset((uint32_t)m, (uint32_t)(k0 & 63));
-            *reinterpret_cast<uint4 *>(sm + MO_S + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + MO_S + 32768 + off) = lo;
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + kMoThr * (4 * half + u), m = e >> 4, k0 = 8 * (e & 15);
+                v[2 * u] = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0);
+                v[2 * u + 1] = *reinterpret_cast<const float4 *>(Sg + m * 128 + k0 + 4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + kMoThr * (4 * half + u), m = e >> 4, k0 = 8 * (e & 15);
+                const float x[8] = {v[2 * u].x,     v[2 * u].y,     v[2 * u].z,     v[2 * u].w,
+                                    v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
+                *reinterpret_cast<uint4 *>(sm + MO_S + (uint32_t)(k0 >> 6) * 16384u +
+                                           sw128_offset((uint32_t)m, (uint32_t)(k0 & 63))) = pack8(x);
+            }
         }
     }
     {  // Vn (sub-row b, value columns 8 g ..), P (query row t < nq2, columns 8 g ..) and Q
@@ -1466,11 +1474,8 @@ __global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(WyTcArgs p) {
             const int e = tid + kMoThr * u, b = e >> 4, k0 = 8 * (e & 15);
             const float x[8] = {v[2 * u].x,     v[2 * u].y,     v[2 * u].z,     v[2 * u].w,
                                 v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
-            uint4 hi, lo;
-            split8(x, hi, lo);
-            const uint32_t off = (uint32_t)(k0 >> 6) * 8192u + sw128_offset((uint32_t)b, (uint32_t)(k0 & 63));
-            *reinterpret_cast<uint4 *>(sm + MO_VN + off) = hi;
-            *reinterpret_cast<uint4 *>(sm + MO_VN + 16384 + off) = lo;
+            *reinterpret_cast<uint4 *>(sm + MO_VN + (uint32_t)(k0 >> 6) * 8192u +
+                                       sw128_offset((uint32_t)b, (uint32_t)(k0 & 63))) = pack8(x);
             // Q row q = b and the query's norm
             const int q = b;
             float y[8];
@@ -1490,11 +1495,7 @@ __global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(WyTcArgs p) {
             if (t < nq2) {
                 const float x[8] = {pv[2 * u].x,     pv[2 * u].y,     pv[2 * u].z,     pv[2 * u].w,
                                     pv[2 * u + 1].x, pv[2 * u + 1].y, pv[2 * u + 1].z, pv[2 * u + 1].w};
-                uint4 hi, lo;
-                split8(x, hi, lo);
-                const uint32_t off = sw128_offset((uint32_t)t, (uint32_t)k0);
-                *reinterpret_cast<uint4 *>(sm + MO_P + off) = hi;
-                *reinterpret_cast<uint4 *>(sm + MO_P + 8192 + off) = lo;
+                *reinterpret_cast<uint4 *>(sm + MO_P + sw128_offset((uint32_t)t, (uint32_t)k0)) = pack8(x);
             }
         }
     }
@@ -1506,22 +1507,13 @@ __global__ void __launch_bounds__(kMoThr, 1) masked_out_tc_kernel(WyTcArgs p) {
     if (tid == 0) {  // S^T Q^T into columns 0.., Vn^T P^T into 64..
         const uint32_t id = idesc_bf16(128, nq2, true, false);
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-            const uint32_t a = sb + MO_S + 32768u * pr;
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16_ss(tmem, smem_desc(sb + MO_S + ks * 2048, 16384, 1024),
+                        smem_desc(sb + MO_Q + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), id, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ss(tmem, smem_desc(a + ks * 2048, 16384, 1024),
-                            smem_desc(sb + MO_Q + (ks >> 2) * (nq2 * 128) + (ks & 3) * 32, 16, 1024), id,
-                            (pr | ks) != 0);
-        }
-#pragma unroll
-        for (int pr = 0; pr < 3; ++pr) {
-            const uint32_t a = sb + MO_VN + (pr == 2 ? 16384u : 0u), b = sb + MO_P + (pr == 1 ? 8192u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16_ss(tmem + 64, smem_desc(a + ks * 2048, 8192, 1024), smem_desc(b + ks * 32, 16, 1024), id,
-                            (pr | ks) != 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16_ss(tmem + 64, smem_desc(sb + MO_VN + ks * 2048, 8192, 1024),
+                        smem_desc(sb + MO_P + ks * 32, 16, 1024), id, ks > 0);
         mma_commit(bar);
     }
     if (tid < 64) sc[tid] = tid < ntok ? p.scale * expf(gam[tid * r]) * sc[tid] : 0.f;  // row scales
