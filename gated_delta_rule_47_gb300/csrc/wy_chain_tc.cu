@@ -326,7 +326,7 @@ int wy_chain_tc_read_clear_error() {
 // chunk_products_tc_kernel: per (head, chunk), after both chains, with S the
 // state entering the chunk, dS' the gradient leaving it, Vn [64][128], the
 // chunk's nq query rows of dO (bf16), P^ and T [64][64] from the WY kernel
-// and Y = Kd dS' from the reverse chain, four rounds of MMAs (M = 128):
+// and Y = Kd dS' from the reverse chain, four batches of MMAs (M = 128):
 //   1. Z^T = dS' Vn^T and t1^T = S dO^T, Yw^T = dO^T P^ and DOV = dO Vn^T;
 //   2. dR^T = dVn^T T, with dVn^T = Y^T + Yw^T as a K-major operand;
 //   3. dR Vn^T (dR^T's image read as an MN-major operand) and t2^T = S dR^T;
@@ -343,9 +343,9 @@ namespace {
 constexpr int kCpThr = 512;
 constexpr int kCpCG = kCpThr / 128, kCpCW = 64 / kCpCG;  // epilogue column groups (warp / 4), columns of each
 constexpr uint32_t CP_S = 0;          // S hi | lo: [2 value blocks][128 key rows][128 B], 32 KB each;
-                                      //   round 4: Kr hi | lo [2 key blocks][64 rows][128 B] (at 0), Kw (at 32768)
-constexpr uint32_t CP_DS = 65536;     // dS' hi | lo, likewise; after round 1 dVn^T hi | lo [128 value rows][128 B],
-                                      //   after round 2 Q hi | lo [2 key blocks][64 rows][128 B]
+                                      //   batch 4: Kr hi | lo [2 key blocks][64 rows][128 B] (at 0), Kw (at 32768)
+constexpr uint32_t CP_DS = 65536;     // dS' hi | lo, likewise; after batch 1 dVn^T hi | lo [128 value rows][128 B],
+                                      //   after batch 2 Q hi | lo [2 key blocks][64 rows][128 B]
 constexpr uint32_t CP_DR = 98304;     // dR^T hi | lo [128 value rows][128 B] (over dS' lo)
 constexpr uint32_t CP_VN = 131072;    // Vn hi | lo: [2 value blocks][64 rows][128 B], 16 KB each
 constexpr uint32_t CP_DO = 163840;    // dO: [2 value blocks][nq2 rows][128 B], 16 KB at most; then P~ hi | lo [64 rows][128 B]
@@ -360,7 +360,7 @@ constexpr uint32_t CP_SMEM = CP_MISC + 16 + 4 * (kCpThr / 32) + 1024;
 // product are not used.
 static_assert(CP_DR + 32768 == CP_VN && CP_VN + 32768 == CP_DO && CP_T + 16384 <= CP_BAR, "products map");
 constexpr uint32_t CT_Z = 0, CT_T1 = 64, CT_YW = 128, CT_DOV = 192, CT_DR = 256, CT_DA = 320, CT_T2 = 384;
-constexpr uint32_t CT_X1 = 64, CT_X2 = 128, CT_DQ = 192;  // round 4, over columns read in round 1's epilogue
+constexpr uint32_t CT_X1 = 64, CT_X2 = 128, CT_DQ = 192;  // batch 4, over columns read in batch 1's epilogue
 
 __device__ __forceinline__ float sum16p(float x) {  // over the 16 lanes that differ in bits 0..3
 #pragma unroll
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kCpThr, 1) chunk_products_tc_kernel(ChunkProdu
         }
         mma_commit(&bar[1]);
     }
-    // the keys and queries of round 4 (element e: row e / 16, 8-column group e % 16), loaded while dR forms
+    // the keys and queries of batch 4 (element e: row e / 16, 8-column group e % 16), loaded while dR forms
     constexpr int UK = 1024 / kCpThr;
     uint4 kg[UK], qg4[UK];
 #pragma unroll
