@@ -513,7 +513,8 @@ def secondary(args, dev):
                                                  d["rope_sin"]))
     bwd_bytes = w.B * w.T * (2 * C * 2 + 3 * C * 2 + 3 * C * 2 + 2 * 16 * 4)  # raw q, k + 3 grads in, 3 out
     out["cam_prep_bwd_b2n32760h16d128_bf16"] = {"ms": bwd_ms, "gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9,
-                                                "hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+                                                "hbm_frac": bwd_bytes / (bwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                                "path": "streamed: persistent CTAs fed by bulk copies"}
     del gq, gk, gv
     # the camera branch's own frame-level scan on the prep output: 21 frames of
     # 30 x 52 tokens, unit-norm q and k, beta / S per token, one decay per frame

@@ -16,7 +16,12 @@
 //    16-byte loads, 8 tokens per CTA, the rotary rows of the 8 positions
 //    staged once in shared memory.
 //
-// The path is HBM-bound: 3 reads + 3 writes of C elements per token.
+// The backward has the same split: cam_prep_bwd_stream_kernel (bf16, C <=
+// 2048, rotary tables given; persistent CTAs fed by bulk copies, four warps
+// per token) and cam_prep_bwd_kernel (one CTA per token) for the rest.
+//
+// The path is HBM-bound: 3 reads + 3 writes of C elements per token (the
+// backward: 5 reads + 3 writes).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -559,8 +564,10 @@ int cam_prep_read_clear_error() {
 namespace {
 
 // Backward of the camera prep (fused_cam_gdn.py, `_cam_prep_bwd_kernel`,
-// continued through the full-C RMSNorm, which the page leaves to torch).  One
-// CTA per token, thread i taking channels 8i .. 8i+7 (head c / D, dims c % D):
+// continued through the full-C RMSNorm, which the page leaves to torch).  The
+// streamed kernel further below takes bf16 rows of C <= 2048 with rotary
+// tables; this one takes the rest.  One CTA per token, thread i taking
+// channels 8i .. 8i+7 (head c / D, dims c % D):
 // the forward values it needs are recomputed, the rotation and projection are
 // transposed, the ||k||^2 terms, K-scale and ReLU mask are applied, and the
 // RMSNorm backward dx_j = r w_j dxhat_j - (r^3 / C) x_j sum_c w_c x_c dxhat_c
@@ -759,6 +766,297 @@ __global__ void __launch_bounds__(512) cam_prep_bwd_kernel(CamBwdParams p) {
     }
 }
 
+// ------------------------------------------------------------------ streamed backward
+// The same backward for bf16 rows of C = H*D <= 2048 elements with rotary
+// tables given, fed by the bulk-copy engine as in the streamed forward: one
+// persistent CTA per SM walks stages of kBTok consecutive positions of one
+// batch row.  A producer warp copies each stage's raw q and k rows, the three
+// output gradients (head-major, so one copy per gradient and head holds the
+// stage's kBTok rows of D), the projections and the rotary rows into one of
+// kBBuf shared-memory buffers; 12 compute warps, four per token (each a
+// quarter of the token's 8-channel groups), form the gradients from there
+// while the next stages' copies are in flight.  Thirteen warps leave each
+// thread 128 registers, which the token's values need without spilling.  The two full-C sums each token needs
+// (the RMS factors, then the RMSNorm backward's dot products) meet through
+// shared memory under a named barrier of the token's four warps.
+constexpr int kBTok = 3;
+constexpr int kBBuf = 3;                                     // stage buffers
+constexpr uint32_t kBRows = kBTok * kMaxC * 2;              // kBTok bf16 rows of C (12 KB)
+constexpr uint32_t kBQ = 0, kBK = kBRows, kBG = 2 * kBRows;  // q rows | k rows | dq, dk, dv blocks
+constexpr uint32_t kBPJ = 5 * kBRows;                        // proj_q [kBTok][16] | proj_kv [kBTok][16]
+constexpr uint32_t kBRT = kBPJ + 2 * kBTok * 64;             // cos [kBTok][Dh] | sin [kBTok][Dh]
+constexpr uint32_t kBStage = kBRT + 2 * kBTok * kMaxDh * 4;
+constexpr int kBWarps = 4 * kBTok;                           // compute warps
+constexpr uint32_t kBSmem = kBBuf * kBStage + 16 * kBBuf + 2 * kBWarps * 2 * 4 + 128;
+static_assert(kBStage % 128 == 0, "stage buffers keep 128-byte alignment");
+
+__device__ __forceinline__ F8 unpack_bf16x8(uint4 u) {
+    F8 r;
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r.x[2 * i] = __uint_as_float(w4[i] << 16);
+        r.x[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
+    }
+    return r;
+}
+
+// NPL = 8-element groups per lane (C <= 1024 * NPL).
+template <int NPL>
+__global__ void __launch_bounds__(32 * (kBWarps + 1), 1) cam_prep_bwd_stream_kernel(CamBwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((128u - (tc::smem_u32(smem_raw) & 127u)) & 127u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + kBBuf * kBStage);  // [kBBuf]
+    uint64_t *empty = full + kBBuf;                                       // [kBBuf]
+    float *part = reinterpret_cast<float *>(empty + kBBuf);               // [2 sums][kBWarps][2] per-warp partials
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int H = p.H, D = p.D, N = p.N;
+    const int C = H * D, Dh = D / 2, G8 = C / 8;
+    const int spb = (N + kBTok - 1) / kBTok;  // stages per batch row
+    const long nst = (long)p.B * spb;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kBBuf; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], kBWarps);
+        }
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (w == kBWarps) {
+        // ---------------------------------------------------------- producer
+        // lane 0 arms the stage's barrier, then the 32 lanes share its copies
+        int j = 0;
+        for (long st = blockIdx.x; st < nst; st += gridDim.x, ++j) {
+            const int buf = j % kBBuf;
+            int ok = 1;
+            if (lane == 0 && j >= kBBuf) ok = cam_wait(&empty[buf], ((j - kBBuf) / kBBuf) & 1) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const int b = (int)(st / spb), n0 = (int)(st % spb) * kBTok;
+            const int nt = min(kBTok, N - n0);
+            const uint32_t rowb = (uint32_t)nt * C * 2, grb = (uint32_t)nt * D * 2;
+            const uint32_t pjb = (uint32_t)nt * 64, rtb = (uint32_t)nt * Dh * 4;
+            if (lane == 0) tc::mbar_arrive_expect_tx(&full[buf], 2 * rowb + 3u * H * grb + 2 * pjb + 2 * rtb);
+            __syncwarp();
+            const uint32_t sb = tc::smem_u32(sm + buf * kBStage);
+            const size_t bn0 = (size_t)b * N + n0;
+            for (int i = lane; i < 3 * H + 6; i += 32) {
+                if (i < 3 * H) {
+                    const int g = i / H, h = i % H;
+                    const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(
+                        g == 0 ? p.dq_out : (g == 1 ? p.dk_out : p.dv_out));
+                    bulk_g2s(sb + kBG + g * kBRows + (uint32_t)h * (kBTok * D * 2),
+                             src + (((size_t)b * H + h) * N + n0) * D, grb, &full[buf]);
+                } else if (i == 3 * H) {
+                    bulk_g2s(sb + kBQ, static_cast<const __nv_bfloat16 *>(p.q_raw) + bn0 * C, rowb, &full[buf]);
+                } else if (i == 3 * H + 1) {
+                    bulk_g2s(sb + kBK, static_cast<const __nv_bfloat16 *>(p.k_raw) + bn0 * C, rowb, &full[buf]);
+                } else if (i == 3 * H + 2) {
+                    bulk_g2s(sb + kBPJ, p.proj_q + bn0 * 16, pjb, &full[buf]);
+                } else if (i == 3 * H + 3) {
+                    bulk_g2s(sb + kBPJ + kBTok * 64, p.proj_kv + bn0 * 16, pjb, &full[buf]);
+                } else if (i == 3 * H + 4) {
+                    bulk_g2s(sb + kBRT, p.rope_cos + (size_t)n0 * Dh, rtb, &full[buf]);
+                } else {
+                    bulk_g2s(sb + kBRT + kBTok * kMaxDh * 4, p.rope_sin + (size_t)n0 * Dh, rtb, &full[buf]);
+                }
+            }
+        }
+        // the last stages' copies land before the CTA leaves
+        if (lane == 0)
+            for (int q = (j >= kBBuf ? j - kBBuf : 0); q < j; ++q) cam_wait(&empty[q % kBBuf], (q / kBBuf) & 1);
+        return;
+    }
+    // -------------------------------------------------------------- compute
+    const int tw = w >> 2, qw = w & 3;  // token of the stage, quarter of its groups
+    int j = 0;
+    for (long st = blockIdx.x; st < nst; st += gridDim.x, ++j) {
+        const int buf = j % kBBuf;
+        if (!cam_wait(&full[buf], (j / kBBuf) & 1)) break;
+        const int b = (int)(st / spb), n = (int)(st % spb) * kBTok + tw;
+        if (n < N) {
+            const size_t bn = (size_t)b * N + n;
+            const uint8_t *sb = sm + buf * kBStage;
+            const __nv_bfloat16 *sq_ = reinterpret_cast<const __nv_bfloat16 *>(sb + kBQ) + (size_t)tw * C;
+            const __nv_bfloat16 *sk_ = reinterpret_cast<const __nv_bfloat16 *>(sb + kBK) + (size_t)tw * C;
+            const float *Pq = reinterpret_cast<const float *>(sb + kBPJ) + tw * 16;
+            const float *Pk = reinterpret_cast<const float *>(sb + kBPJ + kBTok * 64) + tw * 16;
+            const float *cs = reinterpret_cast<const float *>(sb + kBRT) + tw * Dh;
+            const float *sn = reinterpret_cast<const float *>(sb + kBRT + kBTok * kMaxDh * 4) + tw * Dh;
+            // the token's RMS factors
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const int gi = lane + 32 * (4 * i + qw);
+                if (gi < G8) {
+                    const F8 x = unpack_bf16x8(*reinterpret_cast<const uint4 *>(sq_ + gi * 8));
+                    const F8 y = unpack_bf16x8(*reinterpret_cast<const uint4 *>(sk_ + gi * 8));
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        sq += x.x[e] * x.x[e];
+                        sk += y.x[e] * y.x[e];
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            }
+            if (lane == 0) {
+                part[2 * w] = sq;
+                part[2 * w + 1] = sk;
+            }
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + tw) : "memory");  // the token's four warps
+            sq = sk = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                sq += part[2 * (4 * tw + r)];
+                sk += part[2 * (4 * tw + r) + 1];
+            }
+            const float iq = rsqrtf(sq / (float)C + p.eps), ik = rsqrtf(sk / (float)C + p.eps);
+            // gradients of the normalised rows; dv goes out at once
+            float dxq[NPL][8], dxk[NPL][8];
+            float tq = 0.f, tk = 0.f;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const int gi = lane + 32 * (4 * i + qw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dxq[i][e] = dxk[i][e] = 0.f;
+                if (gi >= G8) continue;
+                const int c0 = gi * 8, h = c0 / D, d0 = c0 % D;
+                const F8 q = unpack_bf16x8(*reinterpret_cast<const uint4 *>(sq_ + c0));
+                const F8 k = unpack_bf16x8(*reinterpret_cast<const uint4 *>(sk_ + c0));
+                F8 wq, wk;
+                if (p.q_norm_w) wq = load8(p.q_norm_w + c0);
+                else for (int e = 0; e < 8; ++e) wq.x[e] = 1.f;
+                if (p.k_norm_w) wk = load8(p.k_norm_w + c0);
+                else for (int e = 0; e < 8; ++e) wk.x[e] = 1.f;
+                const uint8_t *gr = sb + kBG + (uint32_t)h * (kBTok * D * 2) + (uint32_t)(tw * D + d0) * 2;
+                F8 dy[3];
+#pragma unroll
+                for (int g = 0; g < 3; ++g) dy[g] = unpack_bf16x8(*reinterpret_cast<const uint4 *>(gr + g * kBRows));
+                const size_t si = ((size_t)b * H + h) * N + n;
+                const float gpre = p.dpre ? p.dpre[si] : 0.f, gpost = p.dpost ? p.dpost[si] : 0.f;
+                float xq[8], xk[8], ak[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    xq[e] = q.x[e] * iq * wq.x[e];
+                    xk[e] = k.x[e] * ik * wk.x[e];
+                    ak[e] = fmaxf(xk[e], 0.f) * p.k_scale;
+                }
+                float cva[8], sva[8];
+                if (d0 >= Dh) {
+                    const int dr = d0 - Dh;  // a multiple of 8: 16-byte aligned rows
+                    const float4 c0v = *reinterpret_cast<const float4 *>(cs + dr);
+                    const float4 c1v = *reinterpret_cast<const float4 *>(cs + dr + 4);
+                    const float4 s0v = *reinterpret_cast<const float4 *>(sn + dr);
+                    const float4 s1v = *reinterpret_cast<const float4 *>(sn + dr + 4);
+                    cva[0] = c0v.x; cva[1] = c0v.y; cva[2] = c0v.z; cva[3] = c0v.w;
+                    cva[4] = c1v.x; cva[5] = c1v.y; cva[6] = c1v.z; cva[7] = c1v.w;
+                    sva[0] = s0v.x; sva[1] = s0v.y; sva[2] = s0v.z; sva[3] = s0v.w;
+                    sva[4] = s1v.x; sva[5] = s1v.y; sva[6] = s1v.z; sva[7] = s1v.w;
+                }
+                // k_out of these dims, for the ||k_out||^2 term
+                float ko[8];
+                if (d0 < Dh) {
+#pragma unroll
+                    for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            ko[4 * gg + r] = Pk[4 * r] * ak[4 * gg] + Pk[4 * r + 1] * ak[4 * gg + 1] +
+                                             Pk[4 * r + 2] * ak[4 * gg + 2] + Pk[4 * r + 3] * ak[4 * gg + 3];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ko[e] = ak[e] * cva[e] + ak[e ^ 1] * sva[e];
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dy[1].x[e] += 2.f * ko[e] * gpost;
+                // transposed projection (first D/2 dims) or rotation (last D/2)
+                F8 da[3];
+#pragma unroll
+                for (int g = 0; g < 3; ++g) {
+                    const float *PP = g == 0 ? Pq : Pk;
+                    if (d0 < Dh) {
+#pragma unroll
+                        for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                da[g].x[4 * gg + c] = PP[c] * dy[g].x[4 * gg] + PP[4 + c] * dy[g].x[4 * gg + 1] +
+                                                      PP[8 + c] * dy[g].x[4 * gg + 2] + PP[12 + c] * dy[g].x[4 * gg + 3];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) da[g].x[e] = dy[g].x[e] * cva[e] + dy[g].x[e ^ 1] * sva[e ^ 1];
+                    }
+                }
+                store8(static_cast<__nv_bfloat16 *>(p.dv_raw) + bn * C + c0, da[2]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    dxq[i][e] = xq[e] > 0.f ? da[0].x[e] : 0.f;
+                    dxk[i][e] = xk[e] > 0.f ? p.k_scale * (da[1].x[e] + 2.f * ak[e] * gpre) : 0.f;
+                    tq += wq.x[e] * q.x[e] * dxq[i][e];
+                    tk += wk.x[e] * k.x[e] * dxk[i][e];
+                }
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                tq += __shfl_xor_sync(0xffffffffu, tq, off);
+                tk += __shfl_xor_sync(0xffffffffu, tk, off);
+            }
+            if (lane == 0) {
+                part[2 * kBWarps + 2 * w] = tq;
+                part[2 * kBWarps + 2 * w + 1] = tk;
+            }
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + tw) : "memory");
+            tq = tk = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                tq += part[2 * kBWarps + 2 * (4 * tw + r)];
+                tk += part[2 * kBWarps + 2 * (4 * tw + r) + 1];
+            }
+            // RMSNorm backward: dx = r w dxhat - (r^3 / C) x sum_c w_c x_c dxhat_c
+            const float cq3 = iq * iq * iq / C * tq, ck3 = ik * ik * ik / C * tk;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const int gi = lane + 32 * (4 * i + qw);
+                if (gi >= G8) continue;
+                const int c0 = gi * 8;
+                const F8 q = unpack_bf16x8(*reinterpret_cast<const uint4 *>(sq_ + c0));
+                const F8 k = unpack_bf16x8(*reinterpret_cast<const uint4 *>(sk_ + c0));
+                F8 wq, wk, oq, okk;
+                if (p.q_norm_w) wq = load8(p.q_norm_w + c0);
+                else for (int e = 0; e < 8; ++e) wq.x[e] = 1.f;
+                if (p.k_norm_w) wk = load8(p.k_norm_w + c0);
+                else for (int e = 0; e < 8; ++e) wk.x[e] = 1.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    oq.x[e] = iq * wq.x[e] * dxq[i][e] - cq3 * q.x[e];
+                    okk.x[e] = ik * wk.x[e] * dxk[i][e] - ck3 * k.x[e];
+                }
+                store8(static_cast<__nv_bfloat16 *>(p.dq_raw) + bn * C + c0, oq);
+                store8(static_cast<__nv_bfloat16 *>(p.dk_raw) + bn * C + c0, okk);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[buf]);  // this warp is done with the stage buffer
+    }
+}
+
+template <int NPL>
+int launch_bwd_stream(const CamBwdParams &p, cudaStream_t stream) {
+    auto kern = cam_prep_bwd_stream_kernel<NPL>;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const long nst = (long)p.B * ((p.N + kBTok - 1) / kBTok);
+    const unsigned grid = (unsigned)(nst < sms ? nst : sms);
+    kern<<<grid, 32 * (kBWarps + 1), kBSmem, stream>>>(p);
+    note_launch();
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 }  // namespace
 
 int launch_cam_prep_bwd(const CamBwdArgs &a, cudaStream_t stream) {
@@ -766,6 +1064,8 @@ int launch_cam_prep_bwd(const CamBwdArgs &a, cudaStream_t stream) {
                    log2((double)a.rope_base), a.dq_out, a.dk_out, a.dv_out, a.dpre, a.dpost, a.dq_raw, a.dk_raw,
                    a.dv_raw, a.B, a.N, a.H, a.D, a.k_scale, a.eps};
     const int C = a.H * a.D;
+    if (a.dtype == GDN_BF16 && a.rope_cos && C <= kMaxC && a.D / 2 <= kMaxDh)
+        return C <= 1024 ? launch_bwd_stream<1>(p, stream) : launch_bwd_stream<2>(p, stream);
     const int threads = ((C / 8 + 31) / 32) * 32;
     const long long tokens = (long long)a.B * a.N;
     if (a.dtype == GDN_BF16)
