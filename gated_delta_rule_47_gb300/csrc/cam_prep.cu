@@ -801,8 +801,9 @@ __device__ __forceinline__ F8 unpack_bf16x8(uint4 u) {
     return r;
 }
 
-// NPL = 8-element groups per lane (C <= 1024 * NPL).
-template <int NPL>
+// NPL = 8-element groups per lane (C <= 1024 * NPL); DT = the head size D when
+// it is fixed at compile time (its divisions become shifts), else 0.
+template <int NPL, int DT>
 __global__ void __launch_bounds__(32 * (kBWarps + 1), 1) cam_prep_bwd_stream_kernel(CamBwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((128u - (tc::smem_u32(smem_raw) & 127u)) & 127u);
@@ -810,7 +811,7 @@ __global__ void __launch_bounds__(32 * (kBWarps + 1), 1) cam_prep_bwd_stream_ker
     uint64_t *empty = full + kBBuf;                                       // [kBBuf]
     float *part = reinterpret_cast<float *>(empty + kBBuf);               // [2 sums][kBWarps][2] per-warp partials
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int H = p.H, D = p.D, N = p.N;
+    const int H = p.H, D = DT ? DT : p.D, N = p.N;
     const int C = H * D, Dh = D / 2, G8 = C / 8;
     const int spb = (N + kBTok - 1) / kBTok;  // stages per batch row
     const long nst = (long)p.B * spb;
@@ -1042,9 +1043,9 @@ __global__ void __launch_bounds__(32 * (kBWarps + 1), 1) cam_prep_bwd_stream_ker
     }
 }
 
-template <int NPL>
+template <int NPL, int DT>
 int launch_bwd_stream(const CamBwdParams &p, cudaStream_t stream) {
-    auto kern = cam_prep_bwd_stream_kernel<NPL>;
+    auto kern = cam_prep_bwd_stream_kernel<NPL, DT>;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -1065,7 +1066,8 @@ int launch_cam_prep_bwd(const CamBwdArgs &a, cudaStream_t stream) {
                    a.dv_raw, a.B, a.N, a.H, a.D, a.k_scale, a.eps};
     const int C = a.H * a.D;
     if (a.dtype == GDN_BF16 && a.rope_cos && C <= kMaxC && a.D / 2 <= kMaxDh)
-        return C <= 1024 ? launch_bwd_stream<1>(p, stream) : launch_bwd_stream<2>(p, stream);
+        return a.D == 128 ? (C <= 1024 ? launch_bwd_stream<1, 128>(p, stream) : launch_bwd_stream<2, 128>(p, stream))
+                          : (C <= 1024 ? launch_bwd_stream<1, 0>(p, stream) : launch_bwd_stream<2, 0>(p, stream));
     const int threads = ((C / 8 + 31) / 32) * 32;
     const long long tokens = (long long)a.B * a.N;
     if (a.dtype == GDN_BF16)
