@@ -64,3 +64,27 @@ def test_prep_backward_camera_workload_size():
                               up[2], None, None, inp["q_norm_w"], inp["k_norm_w"], inp["rope_cos"], inp["rope_sin"])
     for x, y in zip(got, ref):
         assert rel_err(x, y) <= TOL_BF16
+
+
+@pytest.mark.parametrize("B,N,H,D", [(1, 1, 16, 128), (2, 4, 8, 128), (1, 5, 4, 64)])
+@pytest.mark.parametrize("pre,post,weights", [(True, False, False), (False, True, True), (False, False, False)])
+def test_prep_backward_optional_inputs(B, N, H, D, pre, post, weights):
+    """bf16 with rotary tables (the streamed kernel): a single token, a full stage
+    and a partial one, with the norm weights and each ||k||^2 gradient left out or
+    given on its own, and D = 64 beside the D = 128 specialisation."""
+    inp = cam_inputs(B, N, H, D, seed=N + 7 * H, dtype="bf16", tables=True)
+    g = torch.Generator().manual_seed(13)
+    qw = torch.rand(H * D, generator=g) + 0.5 if weights else None
+    kw = torch.rand(H * D, generator=g) + 0.5 if weights else None
+    up, sq = grads(B, N, H, D, seed=5, dtype="bf16")
+    dpre, dpost = (sq[0] if pre else None), (sq[1] if post else None)
+    d = to_dev(inp)
+    got = binding.cam_prep_bwd(d["q_raw"], d["k_raw"], d["proj_q"], d["proj_kv"], up[0].cuda(), up[1].cuda(),
+                               up[2].cuda(), dpre.cuda() if pre else None, dpost.cuda() if post else None,
+                               qw.cuda() if weights else None, kw.cuda() if weights else None, d["rope_cos"],
+                               d["rope_sin"])
+    torch.cuda.synchronize()
+    ref = oracle.cam_prep_bwd(inp["q_raw"], inp["k_raw"], inp["v_raw"], inp["proj_q"], inp["proj_kv"], up[0], up[1],
+                              up[2], dpre, dpost, qw, kw, inp["rope_cos"], inp["rope_sin"])
+    for x, y in zip(got, ref):
+        assert rel_err(x, y) <= TOL_BF16
