@@ -321,15 +321,23 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         const float *t64 = reinterpret_cast<const float *>(sm + GR_T64);
         int j = 0;
         bool ok = true;
+        // beta of this thread's row, loaded a tile ahead of its use (raw bits)
+        auto beta_bits = [&](int it2, int i2) -> unsigned short {
+            if (it2 >= items) return 0;
+            const int t2 = 64 * i2 + r;
+            return t2 < p.S ? p.beta[(size_t)(it2 / p.F) * p.N + (size_t)(it2 % p.F) * p.S + t2] : (unsigned short)0;
+        };
+        unsigned short beta_nx = beta_bits(blockIdx.x, 0);
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
             const int bh = it / p.F, f = it % p.F;
-            const unsigned short *brow = p.beta + (size_t)bh * p.N + (size_t)f * p.S;
             const float *wk = (PREP && p.pp.wk) ? p.pp.wk + 128 * (bh % p.pp.H) : nullptr;
             for (int i = 0; i < nt; ++i, ++j) {
                 const int s = j % kGramStages, x = j & 1;
                 const int t = 64 * i + r;  // token within the frame
                 const bool valid = t < p.S;
-                const float beta = valid ? bf16_bits_to_float(brow[t]) : 0.f;
+                const unsigned short bcur = beta_nx;
+                beta_nx = i + 1 < nt ? beta_bits(it, i + 1) : beta_bits(it + (int)gridDim.x, 0);
+                const float beta = valid ? bf16_bits_to_float(bcur) : 0.f;
                 // the prep's per-token values, loaded before the wait
                 float P[16], rk = 0.f;
                 if (PREP && valid) {
