@@ -631,13 +631,25 @@ __global__ void __launch_bounds__(kTcThr, 1)
             }
             const float sk = p.l2 ? 1.f / fmaxf(nk, 1e-12f) : 1.f;
             float dbeta = 0.f, dec = 0.f;
+            // this row's v values for both halves, loaded before the products are waited for
+            uint4 vpre[2][2][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int ci = 0; ci < 2; ++ci)
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+                        vpre[h][ci][jj] = valid ? *reinterpret_cast<const uint4 *>(vrow + 64 * h + 16 * (2 * half + ci) + 8 * jj)
+                                                : make_uint4(0u, 0u, 0u, 0u);
             ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA1], j & 1, 4u));
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (h == 1) ok = ok && warp_all_ok(fb_wait(&bars[TBB_MMA2A], j & 1, 4u));
                 if (ok) {
                     tc_fence_after_sync();
-#pragma unroll 1
-                    for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {  // 16 columns at a time
+#pragma unroll
+                    for (int ci = 0; ci < 2; ++ci) {  // 16 columns at a time
+                        const int cc = 2 * half + ci;
                         uint32_t ke[16], dr[16];
                         tmem_ld16(tmem + lb + TM_KE + 64 * h + 16 * cc, ke);
                         tmem_ld16(tmem + lb + TM_DR + 64 * h + 16 * cc, dr);
@@ -645,8 +657,8 @@ __global__ void __launch_bounds__(kTcThr, 1)
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
                             const int c8 = 16 * cc + 8 * jj;  // column within the half
-                            float vv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            if (valid) unpack8(*reinterpret_cast<const uint4 *>(vrow + 64 * h + c8), vv);
+                            float vv[8];
+                            unpack8(vpre[h][ci][jj], vv);
                             float rr[8], ww[8], dv8[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
